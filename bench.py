@@ -1,0 +1,429 @@
+#!/usr/bin/env python3
+"""Benchmark of the SSD layer forward scan on B300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one full forward (every kernel of the chunked scan) over one batch of
+the workload.  ``value`` is tokens/s (batch*seqlen per step) with inputs already
+resident in HBM; ``e2e`` is the same metric through the host-buffer entry point
+(ssd_fwd_host) with the input copies in and the output copies out inside the
+timed region.  Inputs rotate over several device copies whose total exceeds the
+126 MB L2, so every step reads cold data.
+
+With N > 1 (torchrun) every rank runs its own copy of the workload on its own
+GPU (the batch dimension shards with no exchange: weak scaling); rank 0 prints
+the line with the max-over-ranks time.  ``--impl reference`` times the fp64
+CPU oracle instead (on the host cores, bounded samples of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from structured_state_space_03_b300 import workloads as wl  # noqa: E402
+
+METRIC = "SSD fwd tokens/s (batch·seqlen/s) at 1 B300; % of HBM/tensor roofline"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: enough for ~3 s)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.HEADLINE.name, choices=[w.name for w in wl.WORKLOADS])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# -- environment ------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "structured_state_space_03_b300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh)
+    ent = rec.get(kernel)
+    if not ent or ent.get("source_digest") != source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of the SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.rows = []
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            target = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={target}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, RuntimeError, AttributeError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def mark(self):
+        return len(self.rows)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, start, end):
+        rows = self.rows[start:end] or self.rows[-3:]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                smax.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, r[4:8]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# -- workload bookkeeping ---------------------------------------------------------------
+
+def unavoidable_bytes(w):
+    """x, y, dt, B, C, A, D and the states that cross HBM once per step."""
+    e = 2 if w.dtype == "bf16" else 4
+    tok = w.batch * w.seqlen
+    xy = 2 * tok * w.nheads * w.headdim * e
+    bc = 2 * tok * w.ngroups * w.dstate * e
+    dt = tok * w.nheads * 4
+    states = w.batch * w.nheads * w.headdim * w.dstate * 4 * (2 if w.with_init else 1)
+    return xy + bc + dt + states + 2 * w.nheads * 4
+
+
+def causal_flops(w):
+    """Algorithmic tensor-core FLOPs of the chunked scan (upper triangle excluded):
+    per (batch, chunk): G*N*Q(Q+1) + H*[P*Q(Q+1) + 4*Q*N*P]; the last chunk is partial."""
+    total = 0
+    for c in range(math.ceil(w.seqlen / w.chunk)):
+        q = min(w.chunk, w.seqlen - c * w.chunk)
+        total += w.ngroups * w.dstate * q * (q + 1) + w.nheads * (w.headdim * q * (q + 1)
+                                                                   + 4 * q * w.dstate * w.headdim)
+    return total * w.batch
+
+
+def kernel_algorithmic_bytes(w, name):
+    """Bytes a kernel must move to do its own share of the step, counting the
+    workspace states it exchanges with the other kernels (fp32)."""
+    e = 2 if w.dtype == "bf16" else 4
+    tok = w.batch * w.seqlen
+    x = tok * w.nheads * w.headdim * e
+    bc = tok * w.ngroups * w.dstate * e
+    dt = tok * w.nheads * 4
+    nc = math.ceil(w.seqlen / w.chunk)
+    st = w.batch * w.nheads * nc * w.headdim * w.dstate * 4
+    fin = w.batch * w.nheads * w.headdim * w.dstate * 4
+    if name.startswith("chunk_state"):
+        return x + bc + dt + st
+    if name.startswith("state_pass"):
+        return 2 * st + fin * (2 if w.with_init else 1)
+    if name.startswith("chunk_out"):
+        return x + 2 * bc + dt + st + x
+    if name.startswith("ssd_fused") or name.startswith("chunk_scan"):
+        return unavoidable_bytes(w)
+    return unavoidable_bytes(w)
+
+
+# -- the CPU oracle (baseline leg and reference arm) ------------------------------------
+
+def time_oracle(w, inp, seconds, cores):
+    """Run the oracle over growing row batches until `seconds` elapse or every
+    row is done; returns (tokens/s equivalent, rows done, elapsed)."""
+    import oracle
+    total_rows = w.batch * w.nheads * w.headdim
+    order = torch.randperm(total_rows, generator=torch.Generator().manual_seed(3)).tolist()
+    done, t0, step = 0, time.perf_counter(), max(cores, 8)
+    while done < total_rows and time.perf_counter() - t0 < seconds:
+        rows = order[done:done + step]
+        oracle.recurrence(**inp, rows=rows, nthreads=cores)
+        done += len(rows)
+        step = min(step * 2, 4096)
+    elapsed = time.perf_counter() - t0
+    tokens_equiv = w.batch * w.seqlen * done / total_rows
+    return tokens_equiv / elapsed, done, elapsed
+
+
+def cpu_baseline(w, inp, seconds):
+    cores = len(os.sched_getaffinity(0))
+    value, rows, elapsed = time_oracle(w, inp, seconds, cores)
+    total_rows = w.batch * w.nheads * w.headdim
+    return {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"sequential fp64 recurrence over {rows} of {total_rows} (batch, head, headdim) rows "
+                      f"for the full sequence ({elapsed:.1f} s); tokens/s scaled by the row fraction"}
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    inp = wl.workload_inputs(w)
+    cores = len(os.sched_getaffinity(0))
+    per_step = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    steps = args.steps or 5
+    for _ in range(args.warmup):
+        time_oracle(w, inp, per_step / 4, cores)
+    vals, rows_total, secs = [], 0, 0.0
+    for _ in range(steps):
+        v, rows, el = time_oracle(w, inp, per_step, cores)
+        vals.append(v)
+        rows_total += rows
+        secs += el
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: the fp64 recurrence over as many (batch, head, headdim) rows "
+                                   f"as fit in {per_step:.1f} s ({rows_total} rows over {steps} steps)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -- the GPU arm ------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    w = wl.by_name(args.workload)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import structured_state_space_03_b300 as ssd
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssd.lib()
+    dtype = wl.torch_dtype(w.dtype)
+    dims = (w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk)
+    kernels = ssd.ssd_fwd_kernels(*dims, dtype)
+    path = ssd.ssd_fwd_path(*dims, dtype)
+
+    inp = wl.workload_inputs(w)
+    per_set = unavoidable_bytes(w)
+    nsets = max(1, math.ceil(3 * L2_BYTES / per_set))
+    sets = []
+    for _ in range(nsets):
+        d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+        d["y"] = torch.empty_like(d["x"])
+        d["final"] = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, dtype=torch.float32, device=dev)
+        sets.append(d)
+    ws = torch.empty(ssd.ssd_fwd_workspace_size(*dims, dtype), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(k):
+        d = sets[k % nsets]
+        ssd.ssd_fwd_ws(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], chunk=w.chunk,
+                       workspace=ws, y=d["y"], final_state=d["final"], stream=stream)
+
+    for k in range(max(3, args.warmup)):
+        step(k)
+    torch.cuda.synchronize()
+    ssd.ssd_check_device_status(stream)
+
+    steps = args.steps
+    if steps <= 0:  # enough steps for a ~3 s timed region
+        t0 = time.perf_counter()
+        for k in range(20):
+            step(k)
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 20
+        steps = int(min(200000, max(50, 3.0 / max(per, 1e-6))))
+
+    # per-kernel timing on a subset of the timed steps (events bracket each kernel)
+    nk = len(kernels)
+    n_prof = min(steps, 2000)
+    prof_every = max(1, steps // n_prof)
+    prof_events = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(n_prof)]
+    for evs in prof_events:  # create the underlying CUDA events
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    mark0 = sampler.mark()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    pi = 0
+    for k in range(steps):
+        profiled = k % prof_every == 0 and pi < n_prof
+        if profiled:
+            ssd.ssd_profile_events(prof_events[pi])
+        step(k)
+        if profiled:
+            ssd.ssd_profile_events(None)
+            pi += 1
+    end.record(stream)
+    torch.cuda.synchronize()
+    mark1 = sampler.mark()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    time.sleep(0.25)
+    sampler.stop()
+    ssd.ssd_check_device_status(stream)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    per_kernel = [0.0] * nk
+    for evs in prof_events[:pi]:
+        for i in range(nk):
+            per_kernel[i] += evs[i].elapsed_time(evs[i + 1])
+    per_kernel = [v / max(pi, 1) for v in per_kernel]  # ms per launch
+    tot_k = sum(per_kernel) or 1.0
+    dom = max(range(nk), key=lambda i: per_kernel[i])
+    dom_name = kernels[dom]
+    peaks, peak_src = load_peaks()
+    dom_bytes = kernel_algorithmic_bytes(w, dom_name)
+    dom_gbs = dom_bytes / (per_kernel[dom] * 1e-3) / 1e9
+    traffic = recorded_traffic(dom_name)
+
+    ms_per_step = elapsed_ms / steps
+    tokens = w.tokens
+    value = tokens * steps * world / (elapsed_ms * 1e-3)
+    t_hbm = unavoidable_bytes(w) / (peaks["hbm_gbs"] * 1e9)
+    t_tc = causal_flops(w) / (peaks["bf16_tflops"] * 1e12)
+    t_roof = max(t_hbm, t_tc)
+
+    # end to end through the host-buffer entry point, pinned host memory
+    host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+    y_host = torch.empty_like(host["x"]).pin_memory()
+    f_host = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, dtype=torch.float32).pin_memory()
+    e2e_steps = max(5, min(steps, 100))
+
+    def host_step():
+        ssd.ssd_fwd_host(host["x"], host["dt"], host["A"], host["B"], host["C"], host["D"], host["init_state"],
+                         chunk=w.chunk, y=y_host, final_state=f_host, stream=stream)
+
+    for _ in range(3):
+        host_step()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        host_step()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = y_host.numel() * y_host.element_size() + f_host.numel() * 4
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk,
+                   "path": path, "l2": f"inputs rotate over {nsets} device copies "
+                                       f"({nsets * per_set / 2**20:.0f} MiB > 126 MB L2)"},
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": dom_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": dom_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dom_bytes, "launch_ms": per_kernel[dom],
+                     "peak_source": f"{peak_src} (copy bandwidth)"},
+        "step_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor", "unavoidable_bytes": unavoidable_bytes(w),
+                          "causal_flops": causal_flops(w), "roofline_ms": t_roof * 1e3,
+                          "frac": t_roof * 1e3 / ms_per_step, "peak_source": peak_src},
+        "kernels": {kernels[i]: {"ms_per_launch": per_kernel[i], "share": per_kernel[i] / tot_k}
+                    for i in range(nk)},
+        "e2e": {"value": tokens * e2e_steps * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "entry": "ssd_fwd_host"},
+        "gpu_launches": nk * steps,
+        "clocks": sampler.summary(mark0, mark1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

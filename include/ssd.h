@@ -1,0 +1,191 @@
+/*
+ * ssd.h -- C ABI of libssd, a single-GPU (B300, sm_103a) implementation of the
+ * Mamba-2 state-space-duality (SSD) layer's forward scan.
+ *
+ * The layer ("Mamba 模型" §4.1-4.2; "草稿:Mamba2", state space duality) maps
+ * per-token inputs x, step sizes dt and projections B, C to outputs y through
+ * the selective SSM recurrence, one independent recurrence per
+ * (batch, head, headdim row):
+ *
+ *     h_t = exp(dt_t * A_h) * h_{t-1} + dt_t * x_t (outer) B_t      h in R^{P x N}
+ *     y_t = C_t . h_t + D_h * x_t
+ *
+ * with a scalar A_h and D_h per head, B and C shared by the heads of one group
+ * (head h uses group h / (nheads/ngroups)), headdim P and state size N.  The
+ * library evaluates it the way the SSD papers describe: the causal
+ * semiseparable matrix is split into diagonal blocks of `chunk` tokens,
+ * computed as small masked matrix products inside each chunk, and off-diagonal
+ * blocks carried by the per-chunk hidden state ("Mamba 模型" §4.1, block
+ * decomposition; "Mamba-2架构深度解析" §2.2, the chunked hybrid mode).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are dense, row-major, with the layouts given below.
+ *   - x, B, C and y have element type `dtype` (fp32 or bf16).  dt, A, D and the
+ *     states are always fp32.  y is rounded to nearest-even in bf16 mode.
+ *   - Pointers passed to ssd_fwd / ssd_fwd_ws are DEVICE pointers on the
+ *     current CUDA device, owned by the caller; the library keeps none of them
+ *     after the enqueued work completes.  bf16 tensors must be 16-byte aligned,
+ *     fp32 tensors 4-byte aligned.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*, NULL = the
+ *     legacy default stream) and the call returns without synchronising.
+ *   - Invalid arguments are reported before anything is enqueued.
+ *   - y must not overlap any input.  init_state == final_state (an in-place
+ *     state carry) is allowed; any other overlap is undefined.
+ *   - The library holds no global mutable host state apart from a
+ *     thread-local error message, and may be called from several threads.
+ */
+#ifndef SSD_H
+#define SSD_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,  /* NULL required pointer, dimension <= 0, nheads % ngroups != 0,
+                                 misaligned pointer, workspace too small, unknown dtype */
+    SSD_ERR_UNSUPPORTED = 2,  /* valid but outside what this build handles (see ssd_fwd) */
+    SSD_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    SSD_ERR_NO_MEMORY = 4,    /* device or host allocation failed */
+    SSD_ERR_TIMEOUT = 5       /* a bounded device-side wait gave up (ssd_check_device_status) */
+} ssd_status_t;
+
+typedef enum {
+    SSD_DTYPE_F32 = 0,  /* x, B, C, y in fp32: computed with fp32 FMA (no tensor cores) */
+    SSD_DTYPE_BF16 = 1  /* x, B, C, y in bf16: tensor-core contractions, fp32 accumulation */
+} ssd_dtype_t;
+
+/* Which kernel family ssd_fwd runs for a problem (see ssd_fwd_path). */
+typedef enum {
+    SSD_PATH_NONE = -1,     /* the problem is rejected */
+    SSD_PATH_SIMT = 0,      /* fp32 FMA chunked kernels (any dtype) */
+    SSD_PATH_TCGEN05 = 1    /* bf16 chunked kernels on tcgen05 tensor cores, TMEM accumulators */
+} ssd_path_t;
+
+/*
+ * ssd_fwd -- the SSD layer forward scan over a whole batch of sequences.
+ *
+ *   x           [batch][seqlen][nheads][headdim]  dtype     input
+ *   dt          [batch][seqlen][nheads]           fp32      step sizes, taken as given
+ *                                                           (no softplus, bias or clamp)
+ *   A           [nheads]                          fp32      decay rate per head (normally < 0)
+ *   B, C        [batch][seqlen][ngroups][dstate]  dtype     input / output projections
+ *   D           [nheads]                          fp32      skip weight; NULL means 0
+ *   init_state  [batch][nheads][headdim][dstate]  fp32      state before token 0; NULL means 0
+ *   y           [batch][seqlen][nheads][headdim]  dtype     OUT
+ *   final_state [batch][nheads][headdim][dstate]  fp32      OUT state after the last token;
+ *                                                           NULL skips it
+ *   chunk       block length Q of the decomposition, 1..256 (the result does
+ *               not depend on it beyond rounding); seqlen need not be a
+ *               multiple of it.
+ *
+ * A device workspace of ssd_fwd_workspace_size() bytes is taken from the
+ * stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *
+ * Returns SSD_OK once the work is enqueued; SSD_ERR_INVALID_ARG as described
+ * above; SSD_ERR_UNSUPPORTED for chunk > 256, headdim > 256 or dstate > 256;
+ * SSD_ERR_NO_MEMORY if the workspace cannot be allocated; SSD_ERR_CUDA if a
+ * launch fails.  Errors raised while the kernels run are reported by
+ * ssd_check_device_status().
+ */
+SSD_API ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                     const float *D, const float *init_state, void *y, float *final_state,
+                     int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                     int chunk, ssd_dtype_t dtype, void *stream);
+
+/*
+ * ssd_fwd_workspace_size -- bytes of device workspace ssd_fwd_ws needs for
+ * this problem: the per-chunk hidden states of the block decomposition
+ * ("Mamba 模型" §4.1, off-diagonal blocks through the hidden state),
+ * [batch][nheads][nchunks][headdim][dstate] fp32, plus one fp32 chunk decay
+ * per (batch, head, chunk).  Writes the size to *bytes.  Same argument checks
+ * as ssd_fwd (no pointers involved).
+ */
+SSD_API ssd_status_t ssd_fwd_workspace_size(int batch, int seqlen, int nheads, int headdim, int ngroups,
+                                    int dstate, int chunk, ssd_dtype_t dtype, size_t *bytes);
+
+/*
+ * ssd_fwd_ws -- ssd_fwd with a caller-provided device workspace of at least
+ * ssd_fwd_workspace_size() bytes, 256-byte aligned.  Nothing is allocated.
+ * The workspace must not be used by anything else until the enqueued work has
+ * completed.  SSD_ERR_INVALID_ARG if it is NULL, misaligned or too small.
+ */
+SSD_API ssd_status_t ssd_fwd_ws(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                        const float *D, const float *init_state, void *y, float *final_state,
+                        int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                        int chunk, ssd_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/*
+ * ssd_fwd_host -- ssd_fwd on HOST buffers (same layouts and meanings).  The
+ * call copies the inputs to the current device, runs the scan on `stream`,
+ * copies y (and final_state when non-NULL) back and synchronises the stream
+ * before returning.  Device buffers come from the stream-ordered allocator and
+ * are released before return.  Pinned host memory gives the fastest copies;
+ * pageable memory works.  Same error codes as ssd_fwd; a device-side error is
+ * returned directly.
+ */
+SSD_API ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                          const float *D, const float *init_state, void *y, float *final_state,
+                          int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                          int chunk, ssd_dtype_t dtype, void *stream);
+
+/*
+ * ssd_fwd_path -- the kernel family ssd_fwd would run for these sizes
+ * (SSD_PATH_NONE when they are rejected).  Pure host function: no CUDA call.
+ */
+SSD_API ssd_path_t ssd_fwd_path(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                        int chunk, ssd_dtype_t dtype);
+
+/*
+ * ssd_fwd_kernels -- how many kernels one ssd_fwd launches for these sizes,
+ * with their names written comma-separated into `names` (when non-NULL,
+ * truncated to names_len bytes including the terminator).  Returns -1 when the
+ * sizes are rejected.  Pure host function: no CUDA call.
+ */
+SSD_API int ssd_fwd_kernels(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                            int chunk, ssd_dtype_t dtype, char *names, size_t names_len);
+
+/*
+ * ssd_profile_events -- per-kernel timing hook for benchmarks.  After a call
+ * with non-NULL `events` (cudaEvent_t handles passed as void*, owned by the
+ * caller, created on the device the forwards run on), every forward issued from
+ * this thread records events[0] on its stream before its first kernel and
+ * events[k] right after its k-th kernel, for k < count.  NULL or count <= 0
+ * switches the hook off.  The setting is thread-local; the library never
+ * creates, destroys or waits on these events.
+ */
+SSD_API ssd_status_t ssd_profile_events(void *const *events, int count);
+
+/*
+ * ssd_check_device_status -- synchronise `stream`, then read and clear the
+ * library's device error word on the current device.  Returns SSD_OK,
+ * SSD_ERR_TIMEOUT (a bounded wait inside a kernel gave up), SSD_ERR_INVALID_ARG
+ * (a kernel-side bounds check failed) or SSD_ERR_CUDA (the stream reported an
+ * error).
+ */
+SSD_API ssd_status_t ssd_check_device_status(void *stream);
+
+/* Static description of a status code. */
+SSD_API const char *ssd_status_string(ssd_status_t status);
+
+/* Thread-local detail of the last failing call on this thread ("" if none). */
+SSD_API const char *ssd_last_error_detail(void);
+
+/* Library version string. */
+SSD_API const char *ssd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_H */

@@ -1,0 +1,365 @@
+// ssd_api.cu -- the C ABI of libssd: argument checks, workspace, launch order.
+//
+// Launch sequence of one forward (all on the caller's stream, no host sync):
+//   1. chunk states S_c and chunk decays      (per batch, head, chunk)
+//   2. state passing h_{c+1} = a_c h_c + S_c  (sequential over chunks)
+//   3. outputs: diagonal block + off-diagonal term + D skip
+// following the block decomposition of "Mamba 模型" §4.1.
+#include <stdio.h>
+#include <stdarg.h>
+#include <string.h>
+#include <mutex>
+
+#include "ssd_internal.cuh"
+
+namespace ssd {
+
+static thread_local char g_detail[512];
+static thread_local cudaEvent_t g_profile_events[16];
+static thread_local int g_profile_count;
+
+static void profile_mark(int k, cudaStream_t s)
+{
+    if (k < g_profile_count) cudaEventRecord(g_profile_events[k], s);
+}
+
+static ssd_status_t fail(ssd_status_t st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_detail, sizeof g_detail, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+static ssd_status_t ok()
+{
+    g_detail[0] = 0;
+    return SSD_OK;
+}
+
+static __device__ unsigned int g_device_error;
+
+// Device address of the error word on the current device (looked up once per device).
+static unsigned int *device_error_word()
+{
+    static std::mutex mu;
+    static unsigned int *addr[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<unsigned int *>(p);
+    }
+    return addr[dev];
+}
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t workspace_bytes(const Problem &pr)
+{
+    const size_t units = (size_t)pr.batch * pr.nheads * pr.nchunks;
+    return align_up(units * pr.headdim * pr.dstate * sizeof(float), 256) +
+           align_up(units * sizeof(float), 256);
+}
+
+Workspace carve_workspace(const Problem &pr, void *base)
+{
+    const size_t units = (size_t)pr.batch * pr.nheads * pr.nchunks;
+    Workspace ws;
+    ws.states = static_cast<float *>(base);
+    ws.decay = reinterpret_cast<float *>(static_cast<char *>(base) +
+                                         align_up(units * pr.headdim * pr.dstate * sizeof(float), 256));
+    return ws;
+}
+
+// Checks that need no pointer; fills the dimension fields of `pr`.
+static ssd_status_t check_dims(Problem &pr, int batch, int seqlen, int nheads, int headdim, int ngroups,
+                               int dstate, int chunk, ssd_dtype_t dtype)
+{
+    if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0 || chunk <= 0)
+        return fail(SSD_ERR_INVALID_ARG,
+                    "every dimension must be positive (batch=%d seqlen=%d nheads=%d headdim=%d ngroups=%d "
+                    "dstate=%d chunk=%d)", batch, seqlen, nheads, headdim, ngroups, dstate, chunk);
+    if (nheads % ngroups != 0)
+        return fail(SSD_ERR_INVALID_ARG, "nheads (%d) must be a multiple of ngroups (%d)", nheads, ngroups);
+    if (dtype != SSD_DTYPE_F32 && dtype != SSD_DTYPE_BF16)
+        return fail(SSD_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (chunk > kMaxChunk)
+        return fail(SSD_ERR_UNSUPPORTED, "chunk %d exceeds %d", chunk, kMaxChunk);
+    if (headdim > kMaxHeaddim || dstate > kMaxDstate)
+        return fail(SSD_ERR_UNSUPPORTED, "headdim %d / dstate %d exceed %d / %d", headdim, dstate, kMaxHeaddim,
+                    kMaxDstate);
+    if (nheads > 65535 || batch > 65535)
+        return fail(SSD_ERR_UNSUPPORTED, "nheads and batch must each be <= 65535");
+    pr.batch = batch;
+    pr.seqlen = seqlen;
+    pr.nheads = nheads;
+    pr.headdim = headdim;
+    pr.ngroups = ngroups;
+    pr.dstate = dstate;
+    pr.chunk = chunk;
+    pr.nchunks = (seqlen + chunk - 1) / chunk;
+    pr.dtype = dtype;
+    return SSD_OK;
+}
+
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static ssd_status_t check_pointers(const Problem &pr)
+{
+    if (!pr.x || !pr.dt || !pr.A || !pr.B || !pr.C || !pr.y)
+        return fail(SSD_ERR_INVALID_ARG, "x, dt, A, B, C and y must be non-NULL");
+    const size_t el = pr.dtype == SSD_DTYPE_BF16 ? 16 : 4;
+    if (!aligned(pr.x, el) || !aligned(pr.B, el) || !aligned(pr.C, el) || !aligned(pr.y, el))
+        return fail(SSD_ERR_INVALID_ARG, "x, B, C and y must be %zu-byte aligned", el);
+    if (!aligned(pr.dt, 4) || !aligned(pr.A, 4) || (pr.D && !aligned(pr.D, 4)) ||
+        (pr.init_state && !aligned(pr.init_state, 4)) || (pr.final_state && !aligned(pr.final_state, 4)))
+        return fail(SSD_ERR_INVALID_ARG, "fp32 tensors must be 4-byte aligned");
+    return SSD_OK;
+}
+
+static ssd_path_t choose_path(const Problem &pr)
+{
+    (void)pr;
+    return SSD_PATH_SIMT;
+}
+
+static const char *kernel_names(ssd_path_t path)
+{
+    switch (path) {
+    case SSD_PATH_SIMT: return "chunk_state_simt,state_pass,chunk_out_simt";
+    default: return "";
+    }
+}
+
+static ssd_status_t run(const Problem &pr_in, void *workspace, cudaStream_t s)
+{
+    Problem pr = pr_in;
+    pr.err_word = device_error_word();
+    if (!pr.err_word) return fail(SSD_ERR_CUDA, "cannot resolve the device error word");
+    const Workspace ws = carve_workspace(pr, workspace);
+    profile_mark(0, s);
+    cudaError_t e = launch_chunk_state_simt(pr, ws, s);
+    profile_mark(1, s);
+    if (e == cudaSuccess) e = launch_state_pass(pr, ws, s);
+    profile_mark(2, s);
+    if (e == cudaSuccess) e = launch_chunk_out_simt(pr, ws, s);
+    profile_mark(3, s);
+    if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+static ssd_status_t make_problem(Problem &pr, const void *x, const float *dt, const float *A, const void *B,
+                                 const void *C, const float *D, const float *init_state, void *y,
+                                 float *final_state, int batch, int seqlen, int nheads, int headdim, int ngroups,
+                                 int dstate, int chunk, ssd_dtype_t dtype)
+{
+    memset(&pr, 0, sizeof pr);
+    ssd_status_t st = check_dims(pr, batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype);
+    if (st != SSD_OK) return st;
+    pr.x = x;
+    pr.dt = dt;
+    pr.A = A;
+    pr.B = B;
+    pr.C = C;
+    pr.D = D;
+    pr.init_state = init_state;
+    pr.y = y;
+    pr.final_state = final_state;
+    return check_pointers(pr);
+}
+
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+ssd_status_t ssd_fwd_workspace_size(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                                    int chunk, ssd_dtype_t dtype, size_t *bytes)
+{
+    if (!bytes) return fail(SSD_ERR_INVALID_ARG, "bytes must be non-NULL");
+    Problem pr;
+    memset(&pr, 0, sizeof pr);
+    ssd_status_t st = check_dims(pr, batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype);
+    if (st != SSD_OK) return st;
+    *bytes = workspace_bytes(pr);
+    return ok();
+}
+
+ssd_path_t ssd_fwd_path(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk,
+                        ssd_dtype_t dtype)
+{
+    Problem pr;
+    memset(&pr, 0, sizeof pr);
+    if (check_dims(pr, batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype) != SSD_OK)
+        return SSD_PATH_NONE;
+    return choose_path(pr);
+}
+
+int ssd_fwd_kernels(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk,
+                    ssd_dtype_t dtype, char *names, size_t names_len)
+{
+    Problem pr;
+    memset(&pr, 0, sizeof pr);
+    if (check_dims(pr, batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype) != SSD_OK) return -1;
+    const char *list = kernel_names(choose_path(pr));
+    if (names && names_len) snprintf(names, names_len, "%s", list);
+    int count = list[0] ? 1 : 0;
+    for (const char *c = list; *c; ++c) count += *c == ',';
+    return count;
+}
+
+ssd_status_t ssd_profile_events(void *const *events, int count)
+{
+    if (!events || count <= 0) {
+        g_profile_count = 0;
+        return ok();
+    }
+    if (count > 16) return fail(SSD_ERR_INVALID_ARG, "at most 16 profiling events");
+    for (int i = 0; i < count; ++i) {
+        if (!events[i]) return fail(SSD_ERR_INVALID_ARG, "profiling event %d is NULL", i);
+        g_profile_events[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    g_profile_count = count;
+    return ok();
+}
+
+ssd_status_t ssd_fwd_ws(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                        const float *D, const float *init_state, void *y, float *final_state, int batch,
+                        int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk,
+                        ssd_dtype_t dtype, void *workspace, size_t workspace_bytes_given, void *stream)
+{
+    Problem pr;
+    ssd_status_t st = make_problem(pr, x, dt, A, B, C, D, init_state, y, final_state, batch, seqlen, nheads,
+                                   headdim, ngroups, dstate, chunk, dtype);
+    if (st != SSD_OK) return st;
+    const size_t need = workspace_bytes(pr);
+    if (!workspace || !aligned(workspace, 256))
+        return fail(SSD_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+    if (workspace_bytes_given < need)
+        return fail(SSD_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes_given,
+                    need);
+    return run(pr, workspace, static_cast<cudaStream_t>(stream));
+}
+
+ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void *B, const void *C, const float *D,
+                     const float *init_state, void *y, float *final_state, int batch, int seqlen, int nheads,
+                     int headdim, int ngroups, int dstate, int chunk, ssd_dtype_t dtype, void *stream)
+{
+    Problem pr;
+    ssd_status_t st = make_problem(pr, x, dt, A, B, C, D, init_state, y, final_state, batch, seqlen, nheads,
+                                   headdim, ngroups, dstate, chunk, dtype);
+    if (st != SSD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t need = workspace_bytes(pr);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(e == cudaErrorMemoryAllocation ? SSD_ERR_NO_MEMORY : SSD_ERR_CUDA,
+                    "workspace allocation of %zu bytes failed: %s", need, cudaGetErrorString(e));
+    }
+    st = run(pr, ws, s);
+    e = cudaFreeAsync(ws, s);
+    if (st == SSD_OK && e != cudaSuccess)
+        return fail(SSD_ERR_CUDA, "workspace release failed: %s", cudaGetErrorString(e));
+    return st;
+}
+
+ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                          const float *D, const float *init_state, void *y, float *final_state, int batch,
+                          int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk,
+                          ssd_dtype_t dtype, void *stream)
+{
+    Problem pr;
+    memset(&pr, 0, sizeof pr);
+    ssd_status_t st = check_dims(pr, batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype);
+    if (st != SSD_OK) return st;
+    if (!x || !dt || !A || !B || !C || !y)
+        return fail(SSD_ERR_INVALID_ARG, "x, dt, A, B, C and y must be non-NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t el = dtype == SSD_DTYPE_BF16 ? 2 : 4;
+    const size_t tok = (size_t)batch * seqlen;
+    const size_t n_x = tok * nheads * headdim, n_dt = tok * nheads, n_bc = tok * ngroups * dstate;
+    const size_t n_state = (size_t)batch * nheads * headdim * dstate;
+    // one device block: x | B | C | y | dt | A | D | init | final | workspace, each 256-byte aligned
+    size_t off[11];
+    size_t sizes[10] = {n_x * el, n_bc * el, n_bc * el, n_x * el, n_dt * 4, (size_t)nheads * 4,
+                        D ? (size_t)nheads * 4 : 0, init_state ? n_state * 4 : 0,
+                        final_state ? n_state * 4 : 0, workspace_bytes(pr)};
+    off[0] = 0;
+    for (int i = 0; i < 10; ++i) off[i + 1] = align_up(off[i] + sizes[i], 256);
+    char *dev = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&dev), off[10], s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(e == cudaErrorMemoryAllocation ? SSD_ERR_NO_MEMORY : SSD_ERR_CUDA,
+                    "device allocation of %zu bytes failed: %s", off[10], cudaGetErrorString(e));
+    }
+    const void *src[9] = {x, B, C, nullptr, dt, A, D, init_state, nullptr};
+    for (int i = 0; i < 9 && e == cudaSuccess; ++i)
+        if (src[i] && sizes[i]) e = cudaMemcpyAsync(dev + off[i], src[i], sizes[i], cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) {
+        pr.x = dev + off[0];
+        pr.B = dev + off[1];
+        pr.C = dev + off[2];
+        pr.y = dev + off[3];
+        pr.dt = reinterpret_cast<const float *>(dev + off[4]);
+        pr.A = reinterpret_cast<const float *>(dev + off[5]);
+        pr.D = D ? reinterpret_cast<const float *>(dev + off[6]) : nullptr;
+        pr.init_state = init_state ? reinterpret_cast<const float *>(dev + off[7]) : nullptr;
+        pr.final_state = final_state ? reinterpret_cast<float *>(dev + off[8]) : nullptr;
+        st = run(pr, dev + off[9], s);
+        if (st == SSD_OK) {
+            e = cudaMemcpyAsync(y, dev + off[3], sizes[3], cudaMemcpyDeviceToHost, s);
+            if (e == cudaSuccess && final_state)
+                e = cudaMemcpyAsync(final_state, dev + off[8], sizes[8], cudaMemcpyDeviceToHost, s);
+        }
+    }
+    cudaError_t ef = cudaFreeAsync(dev, s);
+    cudaError_t es = cudaStreamSynchronize(s);
+    if (st != SSD_OK) return st;
+    if (e != cudaSuccess || ef != cudaSuccess || es != cudaSuccess)
+        return fail(SSD_ERR_CUDA, "host-buffer forward failed: %s",
+                    cudaGetErrorString(e != cudaSuccess ? e : (ef != cudaSuccess ? ef : es)));
+    return ssd_check_device_status(stream);
+}
+
+ssd_status_t ssd_check_device_status(void *stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "stream error: %s", cudaGetErrorString(e));
+    unsigned int word = 0;
+    const unsigned int zero = 0;
+    e = cudaMemcpyFromSymbol(&word, g_device_error, sizeof word);
+    if (e == cudaSuccess && word) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "reading the device error word failed: %s",
+                                      cudaGetErrorString(e));
+    if (word & kDevErrTimeout) return fail(SSD_ERR_TIMEOUT, "a bounded device-side wait gave up (word 0x%x)", word);
+    if (word & kDevErrBounds) return fail(SSD_ERR_INVALID_ARG, "a kernel-side check failed (word 0x%x)", word);
+    return ok();
+}
+
+const char *ssd_status_string(ssd_status_t status)
+{
+    switch (status) {
+    case SSD_OK: return "SSD_OK";
+    case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG: invalid argument";
+    case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: outside the sizes this build handles";
+    case SSD_ERR_CUDA: return "SSD_ERR_CUDA: CUDA runtime error";
+    case SSD_ERR_NO_MEMORY: return "SSD_ERR_NO_MEMORY: allocation failed";
+    case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: bounded device-side wait gave up";
+    }
+    return "unknown ssd_status_t";
+}
+
+const char *ssd_last_error_detail(void) { return g_detail; }
+
+const char *ssd_version(void) { return "libssd 0.1 (sm_103a)"; }
+
+}  // extern "C"

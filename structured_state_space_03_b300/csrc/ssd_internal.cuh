@@ -1,0 +1,104 @@
+// ssd_internal.cuh -- shared declarations of the CUDA side of libssd.
+//
+// Chunked evaluation of the SSD layer ("Mamba 模型" §4.1, block decomposition
+// of the semiseparable matrix; "Mamba-2架构深度解析" §2.2, chunked hybrid mode).
+// With Q = chunk, token t in chunk c = t / Q, and the in-chunk inclusive
+// prefix sum of the log-decays
+//
+//     cs_t = sum_{k = cQ .. t} dt_k * A_h                    (segment sum)
+//
+// the recurrence h_t = exp(dt_t A) h_{t-1} + dt_t x_t B_t^T unrolls into
+//
+//     S_c     = sum_{j in c} exp(cs_last - cs_j) dt_j x_j B_j^T     chunk state
+//     h_{c+1} = exp(cs_last) h_c + S_c,  h_0 = init_state           state passing
+//     y_i     = sum_{j in c, j <= i} (C_i . B_j) exp(cs_i - cs_j) dt_j x_j   diagonal block
+//             + exp(cs_i) C_i . h_c                                 off-diagonal blocks
+//             + D_h x_i                                             skip
+//
+// where h_c is the state entering chunk c.  All exponents are differences of
+// in-chunk prefix sums with the later index first, so they are <= 0 for A <= 0
+// and never overflow.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ssd.h"
+
+namespace ssd {
+
+// Device error word flags (OR-ed together; read and cleared by the host).
+enum : unsigned int {
+    kDevErrTimeout = 1u,  // a bounded wait gave up
+    kDevErrBounds = 2u,   // a kernel-side consistency check failed
+};
+
+struct Problem {
+    const void *x;
+    const float *dt;
+    const float *A;
+    const void *B;
+    const void *C;
+    const float *D;           // may be null
+    const float *init_state;  // may be null
+    void *y;
+    float *final_state;       // may be null
+    int batch, seqlen, nheads, headdim, ngroups, dstate, chunk;
+    int nchunks;
+    ssd_dtype_t dtype;
+    unsigned int *err_word;   // device address of the error word
+};
+
+// Workspace carved out of one device buffer.
+struct Workspace {
+    float *states;  // [batch][nheads][nchunks][headdim][dstate]: S_c, then h_c in place
+    float *decay;   // [batch][nheads][nchunks]: exp(cs_last) of each chunk
+};
+
+size_t workspace_bytes(const Problem &pr);
+Workspace carve_workspace(const Problem &pr, void *base);
+
+// SIMT (fp32 FMA) chunked kernels: any dtype, headdim/dstate/chunk <= 256.
+cudaError_t launch_chunk_state_simt(const Problem &pr, const Workspace &ws, cudaStream_t s);
+cudaError_t launch_chunk_out_simt(const Problem &pr, const Workspace &ws, cudaStream_t s);
+// Sequential inter-chunk state passing, shared by every path.
+cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream_t s);
+
+constexpr int kMaxChunk = 256;
+constexpr int kMaxHeaddim = 256;
+constexpr int kMaxDstate = 256;
+
+__device__ __forceinline__ float load_el(const float *p, size_t i) { return __ldg(p + i); }
+__device__ __forceinline__ float load_el(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ void store_el(float *p, size_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void store_el(__nv_bfloat16 *p, size_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+
+// Inclusive prefix sum over a 256-thread block (warp shuffles, then the warp
+// totals).  `warp_tot` is 8 floats of shared memory.  Every thread calls it.
+__device__ __forceinline__ float block_inclusive_scan_256(float v, float *warp_tot)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float w = lane < 8 ? warp_tot[lane] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        if (lane < 8) warp_tot[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) v += warp_tot[warp - 1];
+    __syncthreads();  // warp_tot may be reused by the caller
+    return v;
+}
+
+}  // namespace ssd

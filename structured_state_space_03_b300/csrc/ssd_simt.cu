@@ -1,0 +1,287 @@
+// ssd_simt.cu -- chunked SSD forward on fp32 FMA units (no tensor cores).
+//
+// This is the fp32 path (fp32 inputs need 1e-4 relative accuracy, which
+// neither TF32 nor bf16 tensor cores give) and the general path for sizes the
+// tensor-core kernels are not built for.  One CTA of 256 threads per
+// (chunk, head, batch); the chunk algebra is written out in ssd_internal.cuh.
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTile = 32;       // token tile (rows i and columns j of the diagonal block)
+constexpr int kStateOuts = 8;   // chunk-state outputs per thread per pass
+
+// Segment sum of one chunk: cs[t] (in-chunk inclusive prefix of dt*A) and
+// dt[t] into shared memory; returns cs of the chunk's last token.
+__device__ __forceinline__ float chunk_segsum(const Problem &pr, int b, int h, int t0, int len,
+                                              float *cs_s, float *dt_s, float *warp_tot)
+{
+    const int tid = threadIdx.x;
+    float dtv = 0.f;
+    if (tid < len) dtv = __ldg(pr.dt + ((size_t)b * pr.seqlen + t0 + tid) * pr.nheads + h);
+    const float cs = block_inclusive_scan_256(dtv * __ldg(pr.A + h), warp_tot);
+    if (tid < kMaxChunk) {
+        cs_s[tid] = cs;
+        dt_s[tid] = dtv;
+    }
+    __syncthreads();
+    return cs_s[len - 1];
+}
+
+// S_c[p][n] = sum_j exp(cs_last - cs_j) dt_j x_j[p] B_j[n]; also exp(cs_last).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) chunk_state_simt(Problem pr, Workspace ws)
+{
+    extern __shared__ float smem[];
+    __shared__ float warp_tot[8];
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int L = pr.seqlen, H = pr.nheads, P = pr.headdim, N = pr.dstate, G = pr.ngroups;
+    const int g = h / (H / G);
+    const int t0 = c * pr.chunk;
+    const int len = min(pr.chunk, L - t0);
+    float *cs_s = smem;             // [256]
+    float *dt_s = cs_s + kMaxChunk; // [256]
+    float *w_s = dt_s + kMaxChunk;  // [256]
+    float *x_s = w_s + kMaxChunk;   // [kTile][P], pre-scaled by w
+    float *b_s = x_s + kTile * P;   // [kTile][N]
+    const T *x = static_cast<const T *>(pr.x);
+    const T *Bm = static_cast<const T *>(pr.B);
+    const int tid = threadIdx.x;
+
+    const float cs_last = chunk_segsum(pr, b, h, t0, len, cs_s, dt_s, warp_tot);
+    if (tid < len) w_s[tid] = expf(cs_last - cs_s[tid]) * dt_s[tid];
+    const size_t bh = (size_t)b * H + h;
+    if (tid == 0) ws.decay[bh * pr.nchunks + c] = expf(cs_last);
+    __syncthreads();
+
+    const int PN = P * N;
+    float *out = ws.states + (bh * pr.nchunks + c) * (size_t)PN;
+    for (int o0 = 0; o0 < PN; o0 += kThreads * kStateOuts) {
+        float acc[kStateOuts];
+#pragma unroll
+        for (int k = 0; k < kStateOuts; ++k) acc[k] = 0.f;
+        for (int j0 = 0; j0 < len; j0 += kTile) {
+            const int tj = min(kTile, len - j0);
+            for (int e = tid; e < tj * P; e += kThreads) {
+                const int jj = e / P, p = e - jj * P;
+                x_s[e] = load_el(x, (((size_t)b * L + t0 + j0 + jj) * H + h) * P + p) * w_s[j0 + jj];
+            }
+            for (int e = tid; e < tj * N; e += kThreads) {
+                const int jj = e / N, n = e - jj * N;
+                b_s[e] = load_el(Bm, (((size_t)b * L + t0 + j0 + jj) * G + g) * N + n);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < kStateOuts; ++k) {
+                const int o = o0 + tid + k * kThreads;
+                if (o < PN) {
+                    const int p = o / N, n = o - p * N;
+                    float a = acc[k];
+                    for (int jj = 0; jj < tj; ++jj) a = fmaf(x_s[jj * P + p], b_s[jj * N + n], a);
+                    acc[k] = a;
+                }
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int k = 0; k < kStateOuts; ++k) {
+            const int o = o0 + tid + k * kThreads;
+            if (o < PN) out[o] = acc[k];
+        }
+    }
+}
+
+// y_i = sum_{j<=i} (C_i.B_j) exp(cs_i - cs_j) dt_j x_j + exp(cs_i) C_i.h_c + D x_i
+template <typename T>
+__global__ void __launch_bounds__(kThreads) chunk_out_simt(Problem pr, Workspace ws)
+{
+    extern __shared__ float smem[];
+    __shared__ float warp_tot[8];
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int L = pr.seqlen, H = pr.nheads, P = pr.headdim, N = pr.dstate, G = pr.ngroups;
+    const int g = h / (H / G);
+    const int t0 = c * pr.chunk;
+    const int len = min(pr.chunk, L - t0);
+    float *cs_s = smem;                 // [256]
+    float *dt_s = cs_s + kMaxChunk;     // [256]
+    float *c_s = dt_s + kMaxChunk;      // [kTile][N]   C rows of the current i tile
+    const int NB = N + 1;               // padded row stride of b_s (no bank conflicts)
+    float *b_s = c_s + kTile * N;       // [kTile][NB]  B rows of the current j tile
+    float *x_s = b_s + kTile * NB;      // [kTile][P]   x rows of the current j tile
+    float *s_s = x_s + kTile * P;       // [kTile][kTile+1] masked, decayed C.B
+    float *h_s = s_s + kTile * (kTile + 1);  // [P][kTile+1] slice of h_c over n
+    const T *x = static_cast<const T *>(pr.x);
+    const T *Bm = static_cast<const T *>(pr.B);
+    const T *Cm = static_cast<const T *>(pr.C);
+    T *y = static_cast<T *>(pr.y);
+    const int tid = threadIdx.x;
+    const size_t bh = (size_t)b * H + h;
+    const float *hc = ws.states + (bh * pr.nchunks + c) * (size_t)P * N;
+    const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
+
+    chunk_segsum(pr, b, h, t0, len, cs_s, dt_s, warp_tot);
+
+    constexpr int kOuts = kTile * kMaxHeaddim / kThreads;  // 32
+    for (int i0 = 0; i0 < len; i0 += kTile) {
+        const int ti = min(kTile, len - i0);
+        for (int e = tid; e < kTile * N; e += kThreads) {
+            const int ii = e / N, n = e - ii * N;
+            c_s[e] = ii < ti ? load_el(Cm, (((size_t)b * L + t0 + i0 + ii) * G + g) * N + n) : 0.f;
+        }
+        float acc[kOuts];
+#pragma unroll
+        for (int k = 0; k < kOuts; ++k) acc[k] = 0.f;
+
+        // off-diagonal blocks: C_i . h_c, over n in slices of kTile
+        for (int n0 = 0; n0 < N; n0 += kTile) {
+            const int tn = min(kTile, N - n0);
+            __syncthreads();
+            for (int e = tid; e < P * kTile; e += kThreads) {
+                const int p = e / kTile, nn = e - p * kTile;
+                h_s[p * (kTile + 1) + nn] = nn < tn ? hc[(size_t)p * N + n0 + nn] : 0.f;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < kOuts; ++k) {
+                const int o = tid + k * kThreads;
+                if (o < kTile * P) {
+                    const int ii = o / P, p = o - ii * P;
+                    float a = acc[k];
+                    for (int nn = 0; nn < tn; ++nn) a = fmaf(c_s[ii * N + n0 + nn], h_s[p * (kTile + 1) + nn], a);
+                    acc[k] = a;
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kOuts; ++k) {
+            const int o = tid + k * kThreads;
+            if (o < kTile * P) {
+                const int ii = o / P;
+                acc[k] *= ii < ti ? expf(cs_s[i0 + ii]) : 0.f;
+            }
+        }
+
+        // diagonal block: j tiles up to the end of this i tile
+        for (int j0 = 0; j0 < i0 + ti; j0 += kTile) {
+            const int tj = min(kTile, i0 + ti - j0);
+            __syncthreads();
+            for (int e = tid; e < kTile * N; e += kThreads) {
+                const int jj = e / N, n = e - jj * N;
+                b_s[jj * NB + n] = jj < tj ? load_el(Bm, (((size_t)b * L + t0 + j0 + jj) * G + g) * N + n) : 0.f;
+            }
+            for (int e = tid; e < kTile * P; e += kThreads) {
+                const int jj = e / P, p = e - jj * P;
+                x_s[e] = jj < tj ? load_el(x, (((size_t)b * L + t0 + j0 + jj) * H + h) * P + p) : 0.f;
+            }
+            __syncthreads();
+            for (int e = tid; e < kTile * kTile; e += kThreads) {
+                const int ii = e / kTile, jj = e - ii * kTile;
+                const int i = i0 + ii, j = j0 + jj;
+                float v = 0.f;
+                if (ii < ti && jj < tj && j <= i) {
+                    float d = 0.f;
+                    for (int n = 0; n < N; ++n) d = fmaf(c_s[ii * N + n], b_s[jj * NB + n], d);
+                    v = d * expf(cs_s[i] - cs_s[j]) * dt_s[j];
+                }
+                s_s[ii * (kTile + 1) + jj] = v;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < kOuts; ++k) {
+                const int o = tid + k * kThreads;
+                if (o < kTile * P) {
+                    const int ii = o / P, p = o - ii * P;
+                    float a = acc[k];
+                    for (int jj = 0; jj < tj; ++jj) a = fmaf(s_s[ii * (kTile + 1) + jj], x_s[jj * P + p], a);
+                    acc[k] = a;
+                }
+            }
+        }
+
+        // skip term and store
+#pragma unroll
+        for (int k = 0; k < kOuts; ++k) {
+            const int o = tid + k * kThreads;
+            if (o < kTile * P) {
+                const int ii = o / P, p = o - ii * P;
+                if (ii < ti) {
+                    const size_t idx = (((size_t)b * L + t0 + i0 + ii) * H + h) * P + p;
+                    store_el(y, idx, acc[k] + Dh * load_el(x, idx));
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// h_c (state entering chunk c) for every chunk, in place over S_c; final state.
+__global__ void __launch_bounds__(kThreads) state_pass(Problem pr, Workspace ws)
+{
+    const int PN = pr.headdim * pr.dstate;
+    const int e = blockIdx.x * kThreads + threadIdx.x;
+    const int h = blockIdx.y, b = blockIdx.z;
+    if (e >= PN) return;
+    const size_t bh = (size_t)b * pr.nheads + h;
+    float st = pr.init_state ? pr.init_state[bh * PN + e] : 0.f;
+    float *s = ws.states + bh * pr.nchunks * (size_t)PN + e;
+    const float *dec = ws.decay + bh * pr.nchunks;
+#pragma unroll 4
+    for (int c = 0; c < pr.nchunks; ++c) {
+        const float sc = s[(size_t)c * PN];
+        s[(size_t)c * PN] = st;
+        st = fmaf(__ldg(dec + c), st, sc);
+    }
+    if (pr.final_state) pr.final_state[bh * PN + e] = st;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes)
+{
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_state_simt(const Problem &pr, const Workspace &ws, cudaStream_t s)
+{
+    const size_t smem = sizeof(float) * (3 * kMaxChunk + kTile * (pr.headdim + pr.dstate));
+    const dim3 grid(pr.nchunks, pr.nheads, pr.batch);
+    cudaError_t e;
+    if (pr.dtype == SSD_DTYPE_F32) {
+        if ((e = set_smem(chunk_state_simt<float>, smem)) != cudaSuccess) return e;
+        chunk_state_simt<float><<<grid, kThreads, smem, s>>>(pr, ws);
+    } else {
+        if ((e = set_smem(chunk_state_simt<__nv_bfloat16>, smem)) != cudaSuccess) return e;
+        chunk_state_simt<__nv_bfloat16><<<grid, kThreads, smem, s>>>(pr, ws);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_out_simt(const Problem &pr, const Workspace &ws, cudaStream_t s)
+{
+    const size_t smem = sizeof(float) * (2 * kMaxChunk + kTile * (2 * pr.dstate + 1 + pr.headdim) +
+                                         kTile * (kTile + 1) + pr.headdim * (kTile + 1));
+    const dim3 grid(pr.nchunks, pr.nheads, pr.batch);
+    cudaError_t e;
+    if (pr.dtype == SSD_DTYPE_F32) {
+        if ((e = set_smem(chunk_out_simt<float>, smem)) != cudaSuccess) return e;
+        chunk_out_simt<float><<<grid, kThreads, smem, s>>>(pr, ws);
+    } else {
+        if ((e = set_smem(chunk_out_simt<__nv_bfloat16>, smem)) != cudaSuccess) return e;
+        chunk_out_simt<__nv_bfloat16><<<grid, kThreads, smem, s>>>(pr, ws);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream_t s)
+{
+    const int PN = pr.headdim * pr.dstate;
+    const dim3 grid((PN + kThreads - 1) / kThreads, pr.nheads, pr.batch);
+    state_pass<<<grid, kThreads, 0, s>>>(pr, ws);
+    return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -1,0 +1,73 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI,
+run the fp64 oracle on the same inputs, compare with the stated bounds.
+
+Bounds: max |y_gpu - y_ref| <= tol * RMS(y_ref) over the compared elements,
+tol = 1e-4 for fp32 inputs and 2e-2 for bf16 inputs; final states use the same
+bounds against RMS(final_ref).  The oracle sees exactly the values the GPU
+sees (bf16 inputs are widened exactly).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import structured_state_space_03_b300 as ssd
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+
+
+def to_cuda(inp):
+    return {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+
+
+def run_gpu(inp_cuda, chunk, return_final=True, **kw):
+    y, f = ssd.ssd_fwd(inp_cuda["x"], inp_cuda["dt"], inp_cuda["A"], inp_cuda["B"], inp_cuda["C"],
+                       inp_cuda["D"], inp_cuda["init_state"], chunk=chunk, return_final=return_final, **kw)
+    ssd.ssd_check_device_status()
+    return y, f
+
+
+def rel_err(got, want):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    if want.size == 0:
+        return 0.0
+    rms = float(np.sqrt(np.mean(want * want)))
+    diff = np.abs(got - want)
+    assert np.all(np.isfinite(got)), "non-finite values in the GPU result"
+    return float(diff.max()) / (rms if rms > 0 else 1.0)
+
+
+def assert_close(got, want, tol, what):
+    e = rel_err(got, want)
+    assert e <= tol, f"{what}: max-abs error {e:.3e} x RMS exceeds {tol:.1e}"
+    return e
+
+
+def check_full(inp, chunk, tol=None, **kw):
+    """Element-by-element comparison of y and final_state with the oracle."""
+    tol = tol or TOL[inp["x"].dtype]
+    yg, fg = run_gpu(to_cuda(inp), chunk, **kw)
+    yr, fr = oracle.recurrence(**inp)
+    ey = assert_close(yg.float().cpu().numpy(), yr, tol, "y")
+    ef = assert_close(fg.cpu().numpy(), fr, tol, "final_state") if fg is not None else 0.0
+    return ey, ef
+
+
+def check_rows(inp, rows, chunk, tol=None, inp_cuda=None):
+    """Comparison on sampled rows (b, h, p): the full time series of y for each
+    row and that row's final state; for sizes the oracle cannot do whole."""
+    tol = tol or TOL[inp["x"].dtype]
+    yg, fg = run_gpu(inp_cuda or to_cuda(inp), chunk)
+    b, L, H, P = inp["x"].shape
+    yr, fr = oracle.recurrence(**inp, rows=rows)
+    idx = torch.tensor(rows, dtype=torch.long)
+    bi, hi, pi = idx // (H * P), (idx // P) % H, idx % P
+    yg_rows = yg[bi.cuda(), :, hi.cuda(), pi.cuda()].float().cpu().numpy()  # [nrows, L]
+    ey = assert_close(yg_rows, yr, tol, "y (sampled rows)")
+    N = inp["B"].shape[3]
+    fg_rows = fg.reshape(b * H * P, N)[idx.cuda()].cpu().numpy()
+    ef = assert_close(fg_rows, fr, tol, "final_state (sampled rows)")
+    return ey, ef

@@ -1,0 +1,120 @@
+"""The C-ABI library loads, exports every declared symbol and rejects bad
+arguments before touching the GPU (runs without a GPU)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import structured_state_space_03_b300 as ssd
+from structured_state_space_03_b300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = set()
+    for hdr in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(hdr).read()
+        names |= set(re.findall(r"^SSD_API\s+[^;(]*?\b(\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ssd.lib()
+
+
+def test_header_declares_the_binding_surface():
+    names = declared_symbols()
+    assert "ssd_fwd" in names and "ssd_fwd_ws" in names
+    assert names == set(ssd.SIGNATURES), names ^ set(ssd.SIGNATURES)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    # nothing internal leaks out of the library
+    raw = ctypes.CDLL(ssd.LIB_PATH)
+    with pytest.raises(AttributeError):
+        raw.launch_state_pass  # noqa: B018
+
+
+def test_version_and_status_strings(lib):
+    assert "sm_103a" in ssd.ssd_version()
+    for st in range(6):
+        assert ssd.ssd_status_string(st).startswith("SSD_")
+    assert "unknown" in ssd.ssd_status_string(99)
+
+
+DIMS = dict(batch=2, seqlen=300, nheads=8, headdim=64, ngroups=2, dstate=64, chunk=128)
+
+
+def _fwd(lib, x=1, dt=1, A=1, B=1, C=1, y=1, **over):
+    d = dict(DIMS, dtype=ssd.SSD_DTYPE_BF16)
+    d.update(over)
+    p = lambda v: ctypes.c_void_p(v * 4096) if v else None
+    return lib.ssd_fwd(p(x), p(dt), p(A), p(B), p(C), None, None, p(y), None, d["batch"], d["seqlen"],
+                       d["nheads"], d["headdim"], d["ngroups"], d["dstate"], d["chunk"], d["dtype"], None)
+
+
+@pytest.mark.parametrize("missing", ["x", "dt", "A", "B", "C", "y"])
+def test_null_required_pointer_is_invalid(lib, missing):
+    assert _fwd(lib, **{missing: 0}) == ssd.SSD_ERR_INVALID_ARG
+    assert missing in ssd.ssd_last_error_detail()
+
+
+@pytest.mark.parametrize("field", ["batch", "seqlen", "nheads", "headdim", "ngroups", "dstate", "chunk"])
+@pytest.mark.parametrize("value", [0, -3])
+def test_nonpositive_dimension_is_invalid(lib, field, value):
+    assert _fwd(lib, **{field: value}) == ssd.SSD_ERR_INVALID_ARG
+
+
+def test_group_divisibility_and_dtype(lib):
+    assert _fwd(lib, ngroups=3) == ssd.SSD_ERR_INVALID_ARG
+    assert _fwd(lib, dtype=7) == ssd.SSD_ERR_INVALID_ARG
+
+
+def test_misaligned_bf16_pointer_is_invalid(lib):
+    d = dict(DIMS)
+    st = lib.ssd_fwd(ctypes.c_void_p(4096 + 2), ctypes.c_void_p(4096), ctypes.c_void_p(4096),
+                     ctypes.c_void_p(4096), ctypes.c_void_p(4096), None, None, ctypes.c_void_p(8192), None,
+                     *[d[k] for k in ("batch", "seqlen", "nheads", "headdim", "ngroups", "dstate", "chunk")],
+                     ssd.SSD_DTYPE_BF16, None)
+    assert st == ssd.SSD_ERR_INVALID_ARG and "aligned" in ssd.ssd_last_error_detail()
+
+
+@pytest.mark.parametrize("field,value", [("chunk", 512), ("headdim", 512), ("dstate", 300)])
+def test_outside_build_is_unsupported(lib, field, value):
+    assert _fwd(lib, **{field: value}) == ssd.SSD_ERR_UNSUPPORTED
+
+
+def test_workspace_size_and_checks(lib):
+    nc = -(-DIMS["seqlen"] // DIMS["chunk"])
+    units = DIMS["batch"] * DIMS["nheads"] * nc
+    want = units * DIMS["headdim"] * DIMS["dstate"] * 4
+    got = ssd.ssd_fwd_workspace_size(*DIMS.values(), ssd.SSD_DTYPE_BF16)
+    assert want <= got <= want + units * 4 + 512
+    out = ctypes.c_size_t(0)
+    assert lib.ssd_fwd_workspace_size(0, 1, 1, 1, 1, 1, 1, 1, ctypes.byref(out)) == ssd.SSD_ERR_INVALID_ARG
+    assert lib.ssd_fwd_workspace_size(1, 1, 1, 1, 1, 1, 1, 1, None) == ssd.SSD_ERR_INVALID_ARG
+
+
+def test_too_small_workspace_is_invalid(lib):
+    d = dict(DIMS)
+    need = ssd.ssd_fwd_workspace_size(*d.values(), ssd.SSD_DTYPE_BF16)
+    p = ctypes.c_void_p(1 << 20)
+    st = lib.ssd_fwd_ws(p, p, p, p, p, None, None, ctypes.c_void_p(2 << 20), None,
+                        *d.values(), ssd.SSD_DTYPE_BF16, ctypes.c_void_p(3 << 20), need - 1, None)
+    assert st == ssd.SSD_ERR_INVALID_ARG and "too small" in ssd.ssd_last_error_detail()
+    st = lib.ssd_fwd_ws(p, p, p, p, p, None, None, ctypes.c_void_p(2 << 20), None,
+                        *d.values(), ssd.SSD_DTYPE_BF16, ctypes.c_void_p((3 << 20) + 16), need, None)
+    assert st == ssd.SSD_ERR_INVALID_ARG and "aligned" in ssd.ssd_last_error_detail()
+
+
+def test_path_selection_is_a_pure_host_query(lib):
+    assert ssd.ssd_fwd_path(1, 256, 4, 16, 1, 16, 64, ssd.SSD_DTYPE_F32) == "simt"
+    assert ssd.ssd_fwd_path(1, 256, 4, 16, 1, 16, 999, ssd.SSD_DTYPE_F32) == "none"
+    assert ssd.ssd_fwd_path(1, 256, 4, 16, 3, 16, 64, ssd.SSD_DTYPE_F32) == "none"

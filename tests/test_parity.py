@@ -1,0 +1,203 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import structured_state_space_03_b300 as ssd
+from structured_state_space_03_b300.workloads import WORKLOADS, make_inputs, sample_rows, workload_inputs
+from parity import TOL, assert_close, check_full, check_rows, run_gpu, to_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    ssd.lib()
+
+
+# -- the five workloads ---------------------------------------------------------
+
+def test_tiny_f32_full():
+    w = WORKLOADS[0]
+    inp = workload_inputs(w)
+    check_full(inp, w.chunk)
+
+
+@pytest.mark.parametrize("w", WORKLOADS[1:], ids=[w.name for w in WORKLOADS[1:]])
+def test_workload_sampled_rows(w):
+    inp = workload_inputs(w)
+    rows = sample_rows(w, 48)
+    check_rows(inp, rows, w.chunk)
+
+
+# -- mid-size cases compared element by element (several chunks, ragged tail) ---
+
+MID = [
+    # b, L, H, P, N, G, Q, dtype
+    (2, 1000, 8, 64, 64, 2, 128, "bf16"),
+    (1, 777, 4, 64, 128, 1, 256, "bf16"),
+    (1, 600, 4, 64, 256, 1, 256, "bf16"),
+    (2, 513, 8, 128, 128, 2, 128, "bf16"),
+    (1, 300, 4, 64, 64, 4, 64, "bf16"),
+    (2, 333, 6, 32, 48, 3, 100, "f32"),
+    (1, 1000, 4, 16, 16, 1, 64, "f32"),
+]
+
+
+@pytest.mark.parametrize("case", MID, ids=[f"b{c[0]}L{c[1]}H{c[2]}P{c[3]}N{c[4]}G{c[5]}Q{c[6]}{c[7]}" for c in MID])
+@pytest.mark.parametrize("with_init", [False, True])
+def test_mid_full(case, with_init):
+    b, L, H, P, N, G, Q, dt = case
+    inp = make_inputs(b, L, H, P, N, G, dt, seed=L + P + N, with_init=with_init)
+    check_full(inp, Q)
+
+
+# -- edge cases ---------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [1, 5, 63, 64, 65, 127, 129])
+def test_short_and_ragged_sequences(dtype, L):
+    inp = make_inputs(2, L, 4, 64, 64, 1, dtype, seed=100 + L, with_init=True)
+    check_full(inp, 64)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_optional_tensors_absent(dtype):
+    inp = make_inputs(1, 200, 4, 64, 64, 1, dtype, seed=5, with_init=False, with_D=False)
+    check_full(inp, 64)
+    yg, fg = run_gpu(to_cuda(inp), 64, return_final=False)
+    assert fg is None
+    yr, _ = oracle.recurrence(**inp)
+    assert_close(yg.float().cpu().numpy(), yr, TOL[inp["x"].dtype], "y without final_state")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_A_zero_and_dt_zero(dtype):
+    inp = make_inputs(1, 300, 4, 64, 64, 1, dtype, seed=6, with_init=True)
+    inp["A"].zero_()
+    check_full(inp, 128)
+    inp = make_inputs(1, 300, 4, 64, 64, 1, dtype, seed=7, with_init=True)
+    inp["dt"].zero_()
+    check_full(inp, 128)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_in_place_state_carry(dtype):
+    """init_state and final_state may be the same buffer."""
+    inp = make_inputs(2, 300, 4, 64, 64, 1, dtype, seed=8, with_init=True)
+    c = to_cuda(inp)
+    state = c["init_state"].clone()
+    y, f = ssd.ssd_fwd(c["x"], c["dt"], c["A"], c["B"], c["C"], c["D"], state, chunk=128, final_state=state)
+    ssd.ssd_check_device_status()
+    yr, fr = oracle.recurrence(**inp)
+    tol = TOL[inp["x"].dtype]
+    assert_close(y.float().cpu().numpy(), yr, tol, "y")
+    assert_close(state.cpu().numpy(), fr, tol, "in-place final state")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_state_split_on_gpu(dtype):
+    """Two calls carrying the state match one call over the whole sequence."""
+    inp = make_inputs(1, 700, 4, 64, 64, 1, dtype, seed=9, with_init=True)
+    c = to_cuda(inp)
+    y, f = run_gpu(c, 128)
+    L1 = 300
+    first = {k: (v[:, :L1].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in c.items()}
+    second = {k: (v[:, L1:].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in c.items()}
+    y1, f1 = run_gpu(first, 128)
+    second["init_state"] = f1
+    y2, f2 = run_gpu(second, 128)
+    tol = TOL[inp["x"].dtype]
+    yr, fr = oracle.recurrence(**inp)
+    assert_close(torch.cat([y1, y2], 1).float().cpu().numpy(), yr, tol, "split y")
+    assert_close(f2.cpu().numpy(), fr, tol, "split final state")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_chunk_size_invariance(dtype):
+    inp = make_inputs(1, 1000, 4, 64, 64, 1, dtype, seed=10, with_init=True)
+    c = to_cuda(inp)
+    yr, fr = oracle.recurrence(**inp)
+    tol = TOL[inp["x"].dtype]
+    for Q in (64, 128, 256):
+        y, f = run_gpu(c, Q)
+        assert_close(y.float().cpu().numpy(), yr, tol, f"y chunk {Q}")
+        assert_close(f.cpu().numpy(), fr, tol, f"final chunk {Q}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_groups_match_replicated_heads(dtype):
+    inp = make_inputs(2, 400, 8, 64, 64, 2, dtype, seed=11, with_init=True)
+    c = to_cuda(inp)
+    y, f = run_gpu(c, 128)
+    rep = dict(c)
+    rep["B"] = c["B"].repeat_interleave(4, dim=2).contiguous()
+    rep["C"] = c["C"].repeat_interleave(4, dim=2).contiguous()
+    yr, fr = run_gpu(rep, 128)
+    tol = TOL[inp["x"].dtype]
+    assert_close(y.float().cpu().numpy(), yr.float().cpu().numpy(), tol, "grouped vs replicated")
+    assert_close(f.cpu().numpy(), fr.cpu().numpy(), tol, "grouped vs replicated final")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_causality_and_determinism(dtype):
+    inp = make_inputs(1, 500, 4, 64, 64, 1, dtype, seed=12)
+    c = to_cuda(inp)
+    y1, f1 = run_gpu(c, 128)
+    y2, f2 = run_gpu(c, 128)
+    assert torch.equal(y1, y2) and torch.equal(f1, f2), "two identical calls differ"
+    t = 301
+    c2 = dict(c)
+    c2["x"] = c["x"].clone()
+    c2["x"][:, t] += 1.0
+    y3, _ = run_gpu(c2, 128)
+    assert torch.equal(y3[:, :t], y1[:, :t]), "a later input changed an earlier output"
+    assert not torch.equal(y3[:, t:], y1[:, t:])
+
+
+def test_linearity_in_x_f32():
+    inp = make_inputs(1, 300, 4, 32, 32, 1, "f32", seed=13, with_D=True)
+    c = to_cuda(inp)
+    y1, _ = run_gpu(c, 64)
+    c2 = dict(c)
+    c2["x"] = c["x"] * 2.0
+    y2, _ = run_gpu(c2, 64)
+    assert_close(y2.cpu().numpy(), 2.0 * y1.cpu().numpy(), 1e-5, "y(2x) vs 2y(x)")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_host_buffer_entry_matches_device_entry(dtype):
+    inp = make_inputs(2, 300, 4, 64, 64, 1, dtype, seed=14, with_init=True)
+    yd, fd = run_gpu(to_cuda(inp), 128)
+    pinned = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+    yh, fh = ssd.ssd_fwd_host(pinned["x"], pinned["dt"], pinned["A"], pinned["B"], pinned["C"], pinned["D"],
+                              pinned["init_state"], chunk=128)
+    assert torch.equal(yh, yd.cpu()) and torch.equal(fh, fd.cpu())
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_caller_workspace_matches(dtype):
+    inp = make_inputs(2, 300, 4, 64, 64, 1, dtype, seed=15, with_init=True)
+    c = to_cuda(inp)
+    y, f = run_gpu(c, 128)
+    n = ssd.ssd_fwd_workspace_size(2, 300, 4, 64, 1, 64, 128, c["x"].dtype)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    yw, fw = ssd.ssd_fwd_ws(c["x"], c["dt"], c["A"], c["B"], c["C"], c["D"], c["init_state"], chunk=128,
+                            workspace=ws)
+    ssd.ssd_check_device_status()
+    assert torch.equal(y, yw) and torch.equal(f, fw)
+
+
+def test_runs_on_a_side_stream():
+    inp = make_inputs(1, 400, 4, 64, 64, 1, "bf16", seed=16, with_init=True)
+    c = to_cuda(inp)
+    y0, f0 = run_gpu(c, 128)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y1, f1 = ssd.ssd_fwd(c["x"], c["dt"], c["A"], c["B"], c["C"], c["D"], c["init_state"], chunk=128,
+                             stream=s)
+    ssd.ssd_check_device_status(s)
+    assert torch.equal(y0, y1) and torch.equal(f0, f1)
