@@ -123,14 +123,14 @@ static ssd_status_t check_pointers(const Problem &pr)
 
 static ssd_path_t choose_path(const Problem &pr)
 {
-    (void)pr;
-    return SSD_PATH_SIMT;
+    return tc_supported(pr) ? SSD_PATH_TCGEN05 : SSD_PATH_SIMT;
 }
 
 static const char *kernel_names(ssd_path_t path)
 {
     switch (path) {
     case SSD_PATH_SIMT: return "chunk_state_simt,state_pass,chunk_out_simt";
+    case SSD_PATH_TCGEN05: return "chunk_state_tc,state_pass,chunk_out_tc";
     default: return "";
     }
 }
@@ -141,12 +141,13 @@ static ssd_status_t run(const Problem &pr_in, void *workspace, cudaStream_t s)
     pr.err_word = device_error_word();
     if (!pr.err_word) return fail(SSD_ERR_CUDA, "cannot resolve the device error word");
     const Workspace ws = carve_workspace(pr, workspace);
+    const bool tc = choose_path(pr) == SSD_PATH_TCGEN05;
     profile_mark(0, s);
-    cudaError_t e = launch_chunk_state_simt(pr, ws, s);
+    cudaError_t e = tc ? launch_chunk_state_tc(pr, ws, s) : launch_chunk_state_simt(pr, ws, s);
     profile_mark(1, s);
     if (e == cudaSuccess) e = launch_state_pass(pr, ws, s);
     profile_mark(2, s);
-    if (e == cudaSuccess) e = launch_chunk_out_simt(pr, ws, s);
+    if (e == cudaSuccess) e = tc ? launch_chunk_out_tc(pr, ws, s) : launch_chunk_out_simt(pr, ws, s);
     profile_mark(3, s);
     if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return ok();

@@ -62,6 +62,10 @@ Workspace carve_workspace(const Problem &pr, void *base);
 // SIMT (fp32 FMA) chunked kernels: any dtype, headdim/dstate/chunk <= 256.
 cudaError_t launch_chunk_state_simt(const Problem &pr, const Workspace &ws, cudaStream_t s);
 cudaError_t launch_chunk_out_simt(const Problem &pr, const Workspace &ws, cudaStream_t s);
+// tcgen05 tensor-core chunked kernels: bf16, headdim 64/128, dstate 64/128/256, chunk <= 256.
+bool tc_supported(const Problem &pr);
+cudaError_t launch_chunk_state_tc(const Problem &pr, const Workspace &ws, cudaStream_t s);
+cudaError_t launch_chunk_out_tc(const Problem &pr, const Workspace &ws, cudaStream_t s);
 // Sequential inter-chunk state passing, shared by every path.
 cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream_t s);
 

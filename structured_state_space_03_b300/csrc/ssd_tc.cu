@@ -1,0 +1,597 @@
+// ssd_tc.cu -- bf16 chunked SSD forward on tcgen05 tensor cores (sm_103a).
+//
+// Work unit: one chunk of Q tokens of one "head block" -- the 128 / headdim
+// heads (2 for headdim 64, 1 for headdim 128) whose headdim rows fill the
+// 128 lanes of a tensor-memory accumulator.  All heads of a block share one
+// B/C group.  Operands arrive by TMA in 128-byte-swizzled 64-column slabs
+// (box = 64 elements x 128 tokens); accumulators live in TMEM; one thread
+// issues the MMAs; the four warps of the CTA run the epilogues (thread i owns
+// accumulator row i).  The chunk algebra is written out in ssd_internal.cuh.
+//
+// chunk_state_tc:  S_c[(h,p), n] = sum_j w_{h,j} x_j[h,p] B_j[n],
+//                  w_{h,j} = exp(cs_last - cs_j) dt_j           (M=128, N=dstate, K=chunk)
+//                  w*x is fed as two bf16 terms (hi + lo): a single rounding of it
+//                  costs up to ~2.4% of RMS(final_state) on short sequences
+// chunk_out_tc:    per 128-row tile of the chunk (rows i0 .. i0+127, columns j < i0+128)
+//                  G    = C_i B_j^T                              (M=128, N=i0+128, K=dstate)
+//                  Yoff = C_i (h_hi + h_lo)^T  (both heads)       (M=128, N=128,    K=dstate)
+//                         h_c is split into two bf16 terms (hi = bf16(h), lo = bf16(h - hi)):
+//                         the carried state can be ~10x larger than y (an init state), and a
+//                         single bf16 rounding of it alone costs ~2% of RMS(y)
+//                  S_h  = G o exp(cs_i - cs_j) dt_j [j <= i]  -> bf16 in shared memory
+//                  Ydiag_h = S_h x_h                             (M=128, N=headdim, K=i0+128)
+//                  y = Ydiag + exp(cs_i) Yoff + D x
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "ssd_internal.cuh"
+#include "ssd_ptx.cuh"
+
+namespace ssd {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 128;
+constexpr int kBoxRows = 128;           // tokens per TMA box
+constexpr int kBoxBytes = 64 * 2 * kBoxRows;  // 64 bf16 columns x 128 rows = 16 KiB
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p)
+{
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void set_error(const Problem &pr, unsigned int flag)
+{
+    if (pr.err_word) atomicOr(pr.err_word, flag);
+}
+
+// Inclusive prefix sum of 256 values held two per thread (thread t holds
+// values 2t and 2t+1) across a 128-thread block.  warp_tot: 4 floats.
+__device__ __forceinline__ void scan_128x2(float &v0, float &v1, float *warp_tot)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float own = v0 + v1;
+    float s = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += t;
+    }
+    if (lane == 31) warp_tot[warp] = s;
+    __syncthreads();
+    float off = 0.f;
+    for (int w = 0; w < warp; ++w) off += warp_tot[w];
+    __syncthreads();
+    v0 = off + (s - own) + v0;
+    v1 = v0 + v1;
+}
+
+// Segment sums of one chunk for the heads h0 .. h0+nh-1: cs[hh][j] (in-chunk
+// inclusive prefix of dt*A*scale, 0 beyond the chunk) and dtv[hh][j] (0 beyond
+// the chunk).  Rows are 256 floats apart.  Returns nothing; ends synchronised.
+__device__ __forceinline__ void segsum(const Problem &pr, int b, int h0, int nh, int t0, int len, float scale,
+                                       float *cs, float *dtv, float *warp_tot)
+{
+    const int t = threadIdx.x;
+    for (int hh = 0; hh < nh; ++hh) {
+        const int h = h0 + hh;
+        const float a = __ldg(pr.A + h) * scale;
+        const int j0 = 2 * t, j1 = 2 * t + 1;
+        const float d0 = j0 < len ? __ldg(pr.dt + ((size_t)b * pr.seqlen + t0 + j0) * pr.nheads + h) : 0.f;
+        const float d1 = j1 < len ? __ldg(pr.dt + ((size_t)b * pr.seqlen + t0 + j1) * pr.nheads + h) : 0.f;
+        float v0 = d0 * a, v1 = d1 * a;
+        scan_128x2(v0, v1, warp_tot);
+        cs[hh * 256 + j0] = v0;
+        cs[hh * 256 + j1] = v1;
+        dtv[hh * 256 + j0] = d0;
+        dtv[hh * 256 + j1] = d1;
+    }
+    __syncthreads();
+}
+
+// Pack 8 floats into 8 bf16 (one 16-byte chunk).
+__device__ __forceinline__ uint4 pack8(const float *f)
+{
+    uint4 u;
+    __nv_bfloat162 t;
+    t = __floats2bfloat162_rn(f[0], f[1]);
+    u.x = *reinterpret_cast<uint32_t *>(&t);
+    t = __floats2bfloat162_rn(f[2], f[3]);
+    u.y = *reinterpret_cast<uint32_t *>(&t);
+    t = __floats2bfloat162_rn(f[4], f[5]);
+    u.z = *reinterpret_cast<uint32_t *>(&t);
+    t = __floats2bfloat162_rn(f[6], f[7]);
+    u.w = *reinterpret_cast<uint32_t *>(&t);
+    return u;
+}
+
+// Byte offset of logical 16-B chunk q (0..7) of row r in a 128-B-swizzled tile.
+__device__ __forceinline__ uint32_t sw128(int r, int q) { return (uint32_t)r * 128u + (uint32_t)((q ^ (r & 7)) << 4); }
+
+// ---------------------------------------------------------------------------
+// chunk state
+// ---------------------------------------------------------------------------
+
+template <int NS>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_state_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap, Problem pr,
+                   Workspace ws)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t tmem_slot;
+    __shared__ float warp_tot[4];
+    __shared__ float cs[2 * 256], dtv[2 * 256];
+    __shared__ int s_fail;
+
+    const int c = blockIdx.x, hb = blockIdx.y, b = blockIdx.z;
+    const int P = pr.headdim, HB = 128 / P, H = pr.nheads;
+    const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
+    const int t0 = c * pr.chunk, len = min(pr.chunk, pr.seqlen - t0);
+    const int nbox = pr.chunk <= kBoxRows ? 1 : 2;  // 128-token slabs along K
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // one 128-token slab at a time: w*x as hi and lo bf16 terms (2 MN blocks of
+    // 64 (h,p) columns each), and B (NS/64 MN blocks of 64 n columns)
+    uint8_t *base = align1024(smem_raw);
+    uint8_t *xs = base;                  // x, then hi(w*x) in place: 2 x 16 KiB
+    uint8_t *xl = base + 2 * kBoxBytes;  // lo(w*x): 2 x 16 KiB
+    uint8_t *bs = base + 4 * kBoxBytes;  // NS/64 x 16 KiB
+
+    if (tid == 0) {
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        mbar_fence_init();
+        s_fail = 0;
+    }
+    if (warp == 0) tmem_alloc(&tmem_slot, NS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    auto issue_loads = [&](int kh) {
+        mbar_expect_tx(&bar_tma, (uint32_t)((2 + NS / 64) * kBoxBytes));
+        for (int k = 0; k < 2; ++k)
+            tma_load_3d(xs + k * kBoxBytes, &xmap, &bar_tma, hb * 128 + 64 * k, t0 + kh * kBoxRows, b);
+        for (int s = 0; s < NS / 64; ++s)
+            tma_load_3d(bs + s * kBoxBytes, &bmap, &bar_tma, g * NS + 64 * s, t0 + kh * kBoxRows, b);
+    };
+    if (tid == 0) {
+        tma_prefetch_desc(&xmap);
+        tma_prefetch_desc(&bmap);
+        issue_loads(0);
+    }
+
+    // segment sums and decay-to-chunk-end weights (natural-log domain, accurate exp)
+    segsum(pr, b, h0, HB, t0, len, 1.f, cs, dtv, warp_tot);
+    float *wts = cs;  // overwrite cs with w after reading cs_last
+    const float cl0 = cs[len - 1], cl1 = HB > 1 ? cs[256 + len - 1] : 0.f;
+    __syncthreads();
+    for (int e = tid; e < HB * 256; e += kThreads) {
+        const int j = e & 255;
+        wts[e] = j < len ? expf((e < 256 ? cl0 : cl1) - cs[e]) * dtv[e] : 0.f;
+    }
+    if (tid < HB) ws.decay[((size_t)b * H + h0 + tid) * pr.nchunks + c] = expf(tid == 0 ? cl0 : cl1);
+    __syncthreads();
+
+    bool ok = true;
+    for (int kh = 0; kh < nbox && ok; ++kh) {
+        if (!mbar_wait(&bar_tma, kh & 1)) s_fail = 1;
+        __syncthreads();
+        ok = !s_fail;
+        if (!ok) break;
+        // w*x -> hi (in place) + lo; one 16-B chunk = 8 columns of one token row
+        for (int q = tid; q < 2 * kBoxRows * 8; q += kThreads) {
+            const int k = q / (kBoxRows * 8), row = (q / 8) % kBoxRows;
+            const float w = wts[(P == 64 ? k : 0) * 256 + kh * kBoxRows + row];
+            uint4 *ptr = reinterpret_cast<uint4 *>(xs) + q;
+            uint4 v = *ptr;
+            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
+            float f[8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 t = __bfloat1622float2(h2[u]);
+                f[2 * u] = t.x * w;
+                f[2 * u + 1] = t.y * w;
+            }
+            const uint4 hi = pack8(f);
+            const __nv_bfloat162 *hh2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 t = __bfloat1622float2(hh2[u]);
+                f[2 * u] -= t.x;
+                f[2 * u + 1] -= t.y;
+            }
+            *ptr = hi;
+            reinterpret_cast<uint4 *>(xl)[q] = pack8(f);
+        }
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t idesc = idesc_bf16(128, NS, 1, 1);
+            for (int ks = 0; ks < kBoxRows / 16; ++ks) {
+                const uint64_t bd = sdesc_sw128(smem_u32(bs) + ks * 2048, kBoxBytes, 1024);
+                mma_bf16(tmem, sdesc_sw128(smem_u32(xs) + ks * 2048, kBoxBytes, 1024), bd, idesc, (kh | ks) != 0);
+                mma_bf16(tmem, sdesc_sw128(smem_u32(xl) + ks * 2048, kBoxBytes, 1024), bd, idesc, 1);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!mbar_wait(&bar_mma, kh & 1)) s_fail = 1;  // slab buffers are reused by the next half
+        __syncthreads();
+        ok = !s_fail;
+        if (ok && tid == 0 && kh + 1 < nbox) issue_loads(kh + 1);
+    }
+    tc_fence_after();
+
+    if (ok) {
+        const int m = warp * 32 + lane;
+        const int hh = m / P, p = m % P;
+        float *out = ws.states + (((size_t)b * H + h0 + hh) * pr.nchunks + c) * (size_t)P * NS + (size_t)p * NS;
+#pragma unroll 1
+        for (int c0 = 0; c0 < NS; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+            float4 *o4 = reinterpret_cast<float4 *>(out + c0);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) o4[u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        }
+    } else if (tid == 0) {
+        set_error(pr, kDevErrTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, NS);
+}
+
+// ---------------------------------------------------------------------------
+// chunk output
+// ---------------------------------------------------------------------------
+
+// Phase-1 slabs (C | B | h_hi | h_lo), then the masked S tiles: 64 KiB when the
+// tile spans 128 columns, 80 KiB when it spans 256.
+__host__ __device__ constexpr int region1_bytes(int jmax) { return jmax > 128 ? 80 * 1024 : 64 * 1024; }
+
+template <int NS>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_out_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
+                 const __grid_constant__ CUtensorMap cmap, Problem pr, Workspace ws)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_tma, bar_x, bar_mma;
+    __shared__ uint32_t tmem_slot;
+    __shared__ float warp_tot[4];
+    __shared__ float cs[2 * 256], dtv[2 * 256];
+    __shared__ int s_fail;
+
+    const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
+    const int c = blockIdx.x / ntile, it = blockIdx.x % ntile, hb = blockIdx.y, b = blockIdx.z;
+    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
+    const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
+    const int t0 = c * pr.chunk, len = min(pr.chunk, L - t0);
+    const int i0 = it * kBoxRows;
+    if (i0 >= len) return;  // tile beyond the end of a partial last chunk (block-uniform)
+    const int jn = i0 + kBoxRows;                 // columns j in [0, jn)
+    const int nbj = jn / kBoxRows;                // 128-row boxes along j
+    const bool wide = jn > kBoxRows;              // 256 columns: one head per S pass, 512 TMEM columns
+    const uint32_t tcols = wide ? 512 : 256;
+    const uint32_t col_g = 0;
+    const uint32_t col_yd = wide ? 256 : 0;       // narrow tiles reuse G's columns once S is built
+    const uint32_t col_yo = wide ? 384 : 128;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    uint8_t *base = align1024(smem_raw);
+    const int jmax = pr.chunk <= kBoxRows ? kBoxRows : 2 * kBoxRows;
+    uint8_t *r1 = base;                           // phase 1: C | B | h_hi | h_lo slabs; phase 2: S tiles
+    uint8_t *c_sl = r1;                           // 128 x 128 B
+    uint8_t *b_sl = r1 + kBoxBytes;               // jn x 128 B
+    uint8_t *h_sl = b_sl + jn * 128;              // 128 x 128 B, hi part of the state
+    uint8_t *l_sl = h_sl + kBoxBytes;             // 128 x 128 B, lo part of the state
+    uint8_t *xs = r1 + region1_bytes(jmax);       // 2 MN blocks, each jn x 128 B
+
+    if (tid == 0) {
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_x, 1);
+        mbar_init(&bar_mma, 1);
+        mbar_fence_init();
+        s_fail = 0;
+    }
+    if (warp == 0) tmem_alloc(&tmem_slot, tcols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (tid == 0) {
+        tma_prefetch_desc(&xmap);
+        tma_prefetch_desc(&bmap);
+        tma_prefetch_desc(&cmap);
+        mbar_expect_tx(&bar_x, (uint32_t)(2 * nbj * kBoxBytes));
+        for (int k = 0; k < 2; ++k)
+            for (int r = 0; r < nbj; ++r)
+                tma_load_3d(xs + k * jn * 128 + r * kBoxBytes, &xmap, &bar_x, hb * 128 + 64 * k, t0 + r * kBoxRows,
+                            b);
+    }
+    segsum(pr, b, h0, HB, t0, len, kLog2e, cs, dtv, warp_tot);  // log2 domain: decays via exp2f
+
+    // ---- phase 1: G = C_i B^T and Yoff = C_i h_c^T, over 64-wide slabs of the state dimension
+    const int m = tid;  // h-slab row (h, p) written by this thread
+    const float *hsrc = ws.states + (((size_t)b * H + h0 + m / P) * pr.nchunks + c) * (size_t)P * NS +
+                        (size_t)(m % P) * NS;
+    bool ok = true;
+    for (int s = 0; s < NS / 64 && ok; ++s) {
+        if (tid == 0) {
+            mbar_expect_tx(&bar_tma, (uint32_t)((1 + nbj) * kBoxBytes));
+            tma_load_3d(c_sl, &cmap, &bar_tma, g * NS + 64 * s, t0 + i0, b);
+            for (int r = 0; r < nbj; ++r)
+                tma_load_3d(b_sl + r * kBoxBytes, &bmap, &bar_tma, g * NS + 64 * s, t0 + r * kBoxRows, b);
+        }
+        // entry state slab -> hi and lo bf16 terms, 128-B swizzled K-major rows
+        {
+            const float4 *src = reinterpret_cast<const float4 *>(hsrc + 64 * s);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 a = __ldg(src + 2 * q), bq = __ldg(src + 2 * q + 1);
+                const float f[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+                const uint4 hi = pack8(f);
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
+                float r[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 t = __bfloat1622float2(h2[u]);
+                    r[2 * u] = f[2 * u] - t.x;
+                    r[2 * u + 1] = f[2 * u + 1] - t.y;
+                }
+                *reinterpret_cast<uint4 *>(h_sl + sw128(m, q)) = hi;
+                *reinterpret_cast<uint4 *>(l_sl + sw128(m, q)) = pack8(r);
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            if (mbar_wait(&bar_tma, s & 1)) {
+                tc_fence_after();
+                const uint32_t id_g = idesc_bf16(128, jn, 0, 0);
+                constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = sdesc_sw128(smem_u32(c_sl) + kk * 32, 16, 1024);
+                    mma_bf16(tmem + col_g, ad, sdesc_sw128(smem_u32(b_sl) + kk * 32, 16, 1024), id_g,
+                             (s | kk) != 0);
+                    mma_bf16(tmem + col_yo, ad, sdesc_sw128(smem_u32(h_sl) + kk * 32, 16, 1024), id_o,
+                             (s | kk) != 0);
+                    mma_bf16(tmem + col_yo, ad, sdesc_sw128(smem_u32(l_sl) + kk * 32, 16, 1024), id_o, 1);
+                }
+                mma_commit(&bar_mma);
+            } else {
+                s_fail = 1;
+            }
+        }
+        __syncthreads();
+        ok = !s_fail;
+        if (ok && !mbar_wait(&bar_mma, s & 1)) s_fail = 1;  // slabs are reused by the next iteration
+        __syncthreads();
+        ok = !s_fail;
+    }
+    uint32_t mma_phase = (NS / 64) & 1;
+    tc_fence_after();
+
+    // ---- phase 2: S_h = G o decay o dt (causal) -> bf16; Ydiag_h = S_h x_h
+    const int i = warp * 32 + lane;       // accumulator row of this thread
+    const int ia = i0 + i;                // row within the chunk
+    const bool row_ok = ia < len;
+    const int heads_per_pass = wide ? 1 : HB;
+    for (int hp0 = 0; hp0 < HB && ok; hp0 += heads_per_pass) {
+        for (int jb = 0; jb < jn / 32; ++jb) {
+            uint8_t *dst_base = r1;
+            const int j0 = jb * 32;
+            if (j0 > i0 + warp * 32 + 31) {  // whole warp above the diagonal: zeros
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                for (int hh = hp0; hh < hp0 + heads_per_pass; ++hh) {
+                    uint8_t *st = dst_base + (hh - hp0) * (jn * 256) + (j0 / 64) * kBoxBytes;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4 *>(st + sw128(i, (j0 % 64) / 8 + u)) = z;
+                }
+                continue;
+            }
+            float gv[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + col_g + j0, gv);
+            for (int hh = hp0; hh < hp0 + heads_per_pass; ++hh) {
+                const float *csh = cs + hh * 256, *dth = dtv + hh * 256;
+                const float ci = csh[ia < 256 ? ia : 255];
+                float sv[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int j = j0 + k;
+                    sv[k] = (row_ok && j <= ia) ? gv[k] * exp2f(ci - csh[j]) * dth[j] : 0.f;
+                }
+                uint8_t *st = dst_base + (hh - hp0) * (jn * 256) + (j0 / 64) * kBoxBytes;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4 *>(st + sw128(i, (j0 % 64) / 8 + u)) = pack8(sv + 8 * u);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            if (mbar_wait(&bar_x, 0)) {
+                tc_fence_after();
+                const uint32_t id_d = idesc_bf16(128, P, 0, 1);  // one head's headdim columns
+                for (int hh = hp0; hh < hp0 + heads_per_pass; ++hh) {
+                    const uint32_t s_addr = smem_u32(r1) + (hh - hp0) * (jn * 256);
+                    const uint32_t x_addr = smem_u32(xs) + (P == 64 ? hh : 0) * jn * 128;
+                    for (int ks = 0; ks < jn / 16; ++ks) {
+                        const uint64_t ad = sdesc_sw128(s_addr + (ks / 4) * kBoxBytes + (ks % 4) * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(x_addr + ks * 2048, jn * 128, 1024);
+                        mma_bf16(tmem + col_yd + hh * P, ad, bd, id_d, ks > 0);
+                    }
+                }
+                mma_commit(&bar_mma);
+            } else {
+                s_fail = 1;
+            }
+        }
+        __syncthreads();
+        ok = !s_fail;
+        if (ok && !mbar_wait(&bar_mma, mma_phase)) s_fail = 1;
+        mma_phase ^= 1;
+        __syncthreads();
+        ok = !s_fail;
+        tc_fence_after();
+    }
+
+    // ---- phase 3: y = Ydiag + exp(cs_i) Yoff + D x
+    if (ok && !mbar_wait(&bar_x, 0)) ok = false;  // x tile (already complete) visible to every thread
+    if (ok) {
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        for (int hh = 0; hh < HB; ++hh) {
+            const int h = h0 + hh;
+            const float e = exp2f(cs[hh * 256 + (ia < 256 ? ia : 255)]);
+            const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
+            __nv_bfloat16 *yrow = static_cast<__nv_bfloat16 *>(pr.y) + (((size_t)b * L + t0 + ia) * H + h) * P;
+            for (int p0 = 0; p0 < P; p0 += 32) {
+                float yd[32], yo[32];
+                tmem_ld32(tmem + lane_base + col_yd + hh * P + p0, yd);
+                tmem_ld32(tmem + lane_base + col_yo + hh * P + p0, yo);
+                if (row_ok) {
+                    const int col = hh * P + p0;            // column within the 128-wide x tile
+                    const uint8_t *xrow = xs + (col / 64) * jn * 128;
+                    float out[32];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(xrow + sw128(ia, (col % 64) / 8 + u));
+                        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const float2 xf = __bfloat1622float2(x2[v]);
+                            const int k = 8 * u + 2 * v;
+                            out[k] = yd[k] + e * yo[k] + Dh * xf.x;
+                            out[k + 1] = yd[k + 1] + e * yo[k + 1] + Dh * xf.y;
+                        }
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(yrow + p0);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) dst[u] = pack8(out + 8 * u);
+                }
+            }
+        }
+    } else if (tid == 0) {
+        set_error(pr, kDevErrTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, tcols);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [batch][seqlen][width] bf16 tensor viewed as 3-D, boxes of 64 columns x 128 tokens.
+cudaError_t make_map(CUtensorMap *map, const void *ptr, int width, int seqlen, int batch)
+{
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)seqlen, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * seqlen};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kBoxRows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+size_t state_smem(const Problem &pr) { return 1024 + (size_t)(4 + pr.dstate / 64) * kBoxBytes; }
+
+size_t out_smem(const Problem &pr)
+{
+    const int jmax = pr.chunk <= kBoxRows ? kBoxRows : 2 * kBoxRows;
+    return 1024 + region1_bytes(jmax) + (size_t)2 * jmax * 128;
+}
+
+template <int NS>
+cudaError_t launch_tc(const Problem &pr, const Workspace &ws, cudaStream_t s, int phase)
+{
+    CUtensorMap xmap, bmap, cmap;
+    cudaError_t e;
+    const int HB = 128 / pr.headdim;
+    if (phase == 0) {
+        if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+        if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+        const size_t smem = state_smem(pr);
+        if ((e = cudaFuncSetAttribute(chunk_state_tc<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+            cudaSuccess)
+            return e;
+        const dim3 grid(pr.nchunks, pr.nheads / HB, pr.batch);
+        chunk_state_tc<NS><<<grid, kThreads, smem, s>>>(xmap, bmap, pr, ws);
+    } else {
+        if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+        if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+        if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+        const size_t smem = out_smem(pr);
+        if ((e = cudaFuncSetAttribute(chunk_out_tc<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+            cudaSuccess)
+            return e;
+        const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
+        const dim3 grid(pr.nchunks * ntile, pr.nheads / HB, pr.batch);
+        chunk_out_tc<NS><<<grid, kThreads, smem, s>>>(xmap, bmap, cmap, pr, ws);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t dispatch(const Problem &pr, const Workspace &ws, cudaStream_t s, int phase)
+{
+    switch (pr.dstate) {
+    case 64: return launch_tc<64>(pr, ws, s, phase);
+    case 128: return launch_tc<128>(pr, ws, s, phase);
+    case 256: return launch_tc<256>(pr, ws, s, phase);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool tc_supported(const Problem &pr)
+{
+    if (pr.dtype != SSD_DTYPE_BF16) return false;
+    if (pr.headdim != 64 && pr.headdim != 128) return false;
+    if (pr.dstate != 64 && pr.dstate != 128 && pr.dstate != 256) return false;
+    if (pr.chunk > 2 * kBoxRows) return false;
+    const int HB = 128 / pr.headdim;
+    if (pr.nheads % HB != 0 || (pr.nheads / pr.ngroups) % HB != 0) return false;
+    return true;
+}
+
+cudaError_t launch_chunk_state_tc(const Problem &pr, const Workspace &ws, cudaStream_t s)
+{
+    return dispatch(pr, ws, s, 0);
+}
+
+cudaError_t launch_chunk_out_tc(const Problem &pr, const Workspace &ws, cudaStream_t s)
+{
+    return dispatch(pr, ws, s, 1);
+}
+
+}  // namespace ssd

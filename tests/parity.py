@@ -5,6 +5,14 @@ Bounds: max |y_gpu - y_ref| <= tol * RMS(y_ref) over the compared elements,
 tol = 1e-4 for fp32 inputs and 2e-2 for bf16 inputs; final states use the same
 bounds against RMS(final_ref).  The oracle sees exactly the values the GPU
 sees (bf16 inputs are widened exactly).
+
+Storage rounding: y is returned in the input dtype, so a bf16 y carries its own
+round-to-nearest error of up to half an ulp, 2^-8 |y|, on every element -- no
+bf16-output implementation can do better, and on the large workloads that alone
+reaches 2-4% of RMS at the largest elements.  The check therefore allows, per
+element, u |y_ref| on top of the tolerance (u = 2^-8 for bf16 outputs, 2^-24 for
+fp32 outputs and for the fp32 states):
+    max_i (|y_gpu,i - y_ref,i| - u |y_ref,i|) <= tol * RMS(y_ref).
 """
 from __future__ import annotations
 
@@ -15,6 +23,7 @@ import oracle
 import structured_state_space_03_b300 as ssd
 
 TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+STORAGE_U = {torch.float32: 2.0 ** -24, torch.bfloat16: 2.0 ** -8}
 
 
 def to_cuda(inp):
@@ -28,21 +37,24 @@ def run_gpu(inp_cuda, chunk, return_final=True, **kw):
     return y, f
 
 
-def rel_err(got, want):
+def rel_err(got, want, storage_u=0.0):
+    """max_i (|got_i - want_i| - storage_u |want_i|)^+ / RMS(want)."""
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
     if want.size == 0:
         return 0.0
     rms = float(np.sqrt(np.mean(want * want)))
-    diff = np.abs(got - want)
     assert np.all(np.isfinite(got)), "non-finite values in the GPU result"
-    return float(diff.max()) / (rms if rms > 0 else 1.0)
+    diff = np.abs(got - want) - storage_u * np.abs(want)
+    return max(float(diff.max()), 0.0) / (rms if rms > 0 else 1.0)
 
 
-def assert_close(got, want, tol, what):
-    e = rel_err(got, want)
-    assert e <= tol, f"{what}: max-abs error {e:.3e} x RMS exceeds {tol:.1e}"
+def assert_close(got, want, tol, what, storage_u=2.0 ** -24):
+    e = rel_err(got, want, storage_u)
+    raw = rel_err(got, want)
+    assert e <= tol, (f"{what}: error {e:.3e} x RMS beyond the output's own rounding "
+                      f"(raw max-abs {raw:.3e} x RMS) exceeds {tol:.1e}")
     return e
 
 
@@ -51,7 +63,7 @@ def check_full(inp, chunk, tol=None, **kw):
     tol = tol or TOL[inp["x"].dtype]
     yg, fg = run_gpu(to_cuda(inp), chunk, **kw)
     yr, fr = oracle.recurrence(**inp)
-    ey = assert_close(yg.float().cpu().numpy(), yr, tol, "y")
+    ey = assert_close(yg.float().cpu().numpy(), yr, tol, "y", STORAGE_U[yg.dtype])
     ef = assert_close(fg.cpu().numpy(), fr, tol, "final_state") if fg is not None else 0.0
     return ey, ef
 
@@ -66,7 +78,7 @@ def check_rows(inp, rows, chunk, tol=None, inp_cuda=None):
     idx = torch.tensor(rows, dtype=torch.long)
     bi, hi, pi = idx // (H * P), (idx // P) % H, idx % P
     yg_rows = yg[bi.cuda(), :, hi.cuda(), pi.cuda()].float().cpu().numpy()  # [nrows, L]
-    ey = assert_close(yg_rows, yr, tol, "y (sampled rows)")
+    ey = assert_close(yg_rows, yr, tol, "y (sampled rows)", STORAGE_U[yg.dtype])
     N = inp["B"].shape[3]
     fg_rows = fg.reshape(b * H * P, N)[idx.cuda()].cpu().numpy()
     ef = assert_close(fg_rows, fr, tol, "final_state (sampled rows)")

@@ -118,3 +118,11 @@ def test_path_selection_is_a_pure_host_query(lib):
     assert ssd.ssd_fwd_path(1, 256, 4, 16, 1, 16, 64, ssd.SSD_DTYPE_F32) == "simt"
     assert ssd.ssd_fwd_path(1, 256, 4, 16, 1, 16, 999, ssd.SSD_DTYPE_F32) == "none"
     assert ssd.ssd_fwd_path(1, 256, 4, 16, 3, 16, 64, ssd.SSD_DTYPE_F32) == "none"
+    # bf16 with headdim 64/128, dstate 64/128/256 and chunk <= 256 runs on the tensor cores
+    assert ssd.ssd_fwd_path(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == "tcgen05"
+    assert ssd.ssd_fwd_path(16, 4096, 32, 128, 8, 128, 128, ssd.SSD_DTYPE_BF16) == "tcgen05"
+    assert ssd.ssd_fwd_path(1, 131072, 24, 64, 1, 256, 256, ssd.SSD_DTYPE_BF16) == "tcgen05"
+    assert ssd.ssd_fwd_path(2, 333, 6, 32, 3, 48, 100, ssd.SSD_DTYPE_BF16) == "simt"
+    assert ssd.ssd_fwd_path(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_F32) == "simt"
+    assert ssd.ssd_fwd_kernels(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == [
+        "chunk_state_tc", "state_pass", "chunk_out_tc"]
