@@ -67,8 +67,11 @@ typedef enum {
 /* Which kernel family ssd_fwd runs for a problem (see ssd_fwd_path). */
 typedef enum {
     SSD_PATH_NONE = -1,     /* the problem is rejected */
-    SSD_PATH_SIMT = 0,      /* fp32 FMA chunked kernels (any dtype) */
-    SSD_PATH_TCGEN05 = 1    /* bf16 chunked kernels on tcgen05 tensor cores, TMEM accumulators */
+    SSD_PATH_SIMT = 0,           /* fp32 FMA chunked kernels (any dtype) */
+    SSD_PATH_TCGEN05 = 1,        /* bf16 chunked kernels on tcgen05 tensor cores, TMEM accumulators:
+                                    chunk states, state passing, outputs */
+    SSD_PATH_TCGEN05_FUSED = 2   /* one bf16 tcgen05 kernel; chunk-to-chunk states resolved by a
+                                    decoupled look-back (headdim 64/128, dstate 64/128, chunk <= 128) */
 } ssd_path_t;
 
 /*

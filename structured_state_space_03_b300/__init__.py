@@ -28,8 +28,9 @@ LIB_PATH = os.path.join(_PKG, "libssd.so")
 
 SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_NO_MEMORY, SSD_ERR_TIMEOUT = range(6)
 SSD_DTYPE_F32, SSD_DTYPE_BF16 = 0, 1
-SSD_PATH_NONE, SSD_PATH_SIMT, SSD_PATH_TCGEN05 = -1, 0, 1
-PATH_NAMES = {SSD_PATH_NONE: "none", SSD_PATH_SIMT: "simt", SSD_PATH_TCGEN05: "tcgen05"}
+SSD_PATH_NONE, SSD_PATH_SIMT, SSD_PATH_TCGEN05, SSD_PATH_TCGEN05_FUSED = -1, 0, 1, 2
+PATH_NAMES = {SSD_PATH_NONE: "none", SSD_PATH_SIMT: "simt", SSD_PATH_TCGEN05: "tcgen05",
+              SSD_PATH_TCGEN05_FUSED: "tcgen05_fused"}
 
 # Every function declared in include/ssd.h, with its ctypes signature.
 _P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t

@@ -58,8 +58,11 @@ static unsigned int *device_error_word()
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+static ssd_path_t choose_path(const Problem &pr);
+
 size_t workspace_bytes(const Problem &pr)
 {
+    if (choose_path(pr) == SSD_PATH_TCGEN05_FUSED) return fused_workspace_bytes(pr);
     const size_t units = (size_t)pr.batch * pr.nheads * pr.nchunks;
     return align_up(units * pr.headdim * pr.dstate * sizeof(float), 256) +
            align_up(units * sizeof(float), 256);
@@ -123,6 +126,7 @@ static ssd_status_t check_pointers(const Problem &pr)
 
 static ssd_path_t choose_path(const Problem &pr)
 {
+    if (fused_supported(pr)) return SSD_PATH_TCGEN05_FUSED;
     return tc_supported(pr) ? SSD_PATH_TCGEN05 : SSD_PATH_SIMT;
 }
 
@@ -131,6 +135,7 @@ static const char *kernel_names(ssd_path_t path)
     switch (path) {
     case SSD_PATH_SIMT: return "chunk_state_simt,state_pass,chunk_out_simt";
     case SSD_PATH_TCGEN05: return "chunk_state_tc,state_pass,chunk_out_tc";
+    case SSD_PATH_TCGEN05_FUSED: return "ssd_fused_tc";
     default: return "";
     }
 }
@@ -140,8 +145,16 @@ static ssd_status_t run(const Problem &pr_in, void *workspace, cudaStream_t s)
     Problem pr = pr_in;
     pr.err_word = device_error_word();
     if (!pr.err_word) return fail(SSD_ERR_CUDA, "cannot resolve the device error word");
+    const ssd_path_t path = choose_path(pr);
+    if (path == SSD_PATH_TCGEN05_FUSED) {
+        profile_mark(0, s);
+        cudaError_t e = launch_fused_tc(pr, workspace, s);
+        profile_mark(1, s);
+        if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+        return ok();
+    }
     const Workspace ws = carve_workspace(pr, workspace);
-    const bool tc = choose_path(pr) == SSD_PATH_TCGEN05;
+    const bool tc = path == SSD_PATH_TCGEN05;
     profile_mark(0, s);
     cudaError_t e = tc ? launch_chunk_state_tc(pr, ws, s) : launch_chunk_state_simt(pr, ws, s);
     profile_mark(1, s);

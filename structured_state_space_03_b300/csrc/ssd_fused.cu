@@ -1,0 +1,727 @@
+// ssd_fused.cu -- single-kernel bf16 SSD forward on tcgen05 (sm_103a) for
+// chunk <= 128, headdim 64/128, dstate 64/128.
+//
+// One CTA (256 threads) per (chunk c, batch b, head block hb), a head block
+// being the 128/headdim heads whose (head, headdim) rows fill the 128 TMEM
+// lanes.  x, B and C of the chunk are read from HBM once and y is written once;
+// the chunk-to-chunk recurrence h_{c+1} = a_c h_c + S_c is resolved between
+// CTAs by a decoupled look-back over states published in the workspace.
+//
+// Inside the chunk the decay exp(cs_i - cs_j) is rank one per head:
+//   exp(cs_i - cs_j) = r_i v_j,  r_i = exp(cs_i - ref),  v_j = exp(ref - cs_j)
+// with ref the midpoint of the chunk's cs range, so both factors stay within
+// e^(+-60) whenever the range ("span") is at most 120.  Then (ssd_internal.cuh)
+//   S_c          = e^(cs_last - ref) (v o dt o x)^T B
+//   y_i          = r_i [ sum_{j<=i} (C_i . B_j) wx_j  +  e^ref C_i . h_c ]  +  D x_i,
+//   wx_j         = v_j dt_j x_j
+// and the masked matrix tril(C B^T) no longer depends on the head: one bf16
+// copy of it serves every head of the block, and a single accumulator holds
+// both matrix products.  wx (as hi + lo bf16 terms) is the operand of both the
+// chunk-state and the diagonal-block GEMM.  Steps:
+//
+//   1. TMA x, B, C; segment sums, span, ref, r, v, a_c = exp(cs_last).
+//   2. G = C B^T (tcgen05) -> masked bf16 tril(G) in shared memory.
+//   3. Eight 16-token steps, double-buffered: build wx (hi, lo), then
+//      S_c += wx^T B and Y += tril(G)[:, step] wx on the tensor cores.
+//   4. Look-back: if the predecessor chunk's inclusive state h_c is published,
+//      read it; else publish (S_c, a_c) as this chunk's aggregate first, then
+//      walk back combining aggregates until an inclusive state (or chunk 0 and
+//      the init state).  Publish h_{c+1} = a_c h_c + S_c; the last chunk writes
+//      final_state.
+//   5. Y += C (e^ref h_c)^T (h as hi + lo), then y = r_i Y + D x, staged in
+//      shared memory and written by TMA.
+//
+// A chunk whose span exceeds 120 (an extreme decay inside one chunk) keeps
+// steps 1-4 with the decay referenced to the chunk end, skips 5, and is queued;
+// the last CTA to finish computes the queued chunks' outputs directly in fp32.
+//
+// Forward progress: CTAs take their unit from an atomic ticket in chunk-major
+// order (after allocating tensor memory), so every unit a CTA waits on belongs
+// to a CTA that started earlier, and no CTA waits before it has published its
+// aggregate or its inclusive state.  Every wait is bounded (%globaltimer); a
+// wait that gives up sets the device error word and the CTA leaves, which
+// makes its successors give up too instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "ssd_internal.cuh"
+#include "ssd_ptx.cuh"
+
+namespace ssd {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();  // ssd_tc.cu
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 256;
+constexpr int kRows = 128;                 // tokens per tile, TMEM lanes
+constexpr int kSlab = 64 * 2 * kRows;      // 64 bf16 columns x 128 rows = 16 KiB
+constexpr float kSpanMax = 120.f;          // widest in-chunk cs range of the factored path
+
+enum : uint32_t { kFlagNone = 0, kFlagAggregate = 1, kFlagInclusive = 2 };
+enum { kCtrTicket = 0, kCtrDone = 1, kCtrFallback = 2, kCtrCount = 4 };
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p)
+{
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t sw128(int r, int q) { return (uint32_t)r * 128u + (uint32_t)((q ^ (r & 7)) << 4); }
+
+__device__ __forceinline__ uint4 pack8(const float *f)
+{
+    uint4 u;
+    __nv_bfloat162 t;
+    t = __floats2bfloat162_rn(f[0], f[1]);
+    u.x = *reinterpret_cast<uint32_t *>(&t);
+    t = __floats2bfloat162_rn(f[2], f[3]);
+    u.y = *reinterpret_cast<uint32_t *>(&t);
+    t = __floats2bfloat162_rn(f[4], f[5]);
+    u.z = *reinterpret_cast<uint32_t *>(&t);
+    t = __floats2bfloat162_rn(f[6], f[7]);
+    u.w = *reinterpret_cast<uint32_t *>(&t);
+    return u;
+}
+
+// hi = bf16(f), lo = bf16(f - hi), 8 values
+__device__ __forceinline__ void split8(const float *f, uint4 &hi, uint4 &lo)
+{
+    hi = pack8(f);
+    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
+    float r[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float2 t = __bfloat1622float2(h2[u]);
+        r[2 * u] = f[2 * u] - t.x;
+        r[2 * u + 1] = f[2 * u + 1] - t.y;
+    }
+    lo = pack8(r);
+}
+
+// acc += s * src[0..32) (src read through L2)
+__device__ __forceinline__ void fma_row32(float (&acc)[32], float s, const float *src)
+{
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 v = __ldcg(s4 + q);
+        acc[4 * q] = fmaf(s, v.x, acc[4 * q]);
+        acc[4 * q + 1] = fmaf(s, v.y, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(s, v.z, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(s, v.w, acc[4 * q + 3]);
+    }
+}
+
+struct FusedArgs {
+    float *agg;          // [units][128][NS] aggregate chunk states S_c
+    float *incl;         // [units][128][NS] inclusive states h_{c+1}
+    float *alpha;        // [units][2] chunk decays a_c per head of the block
+    uint32_t *flags;     // [units] publication state (counters follow)
+    uint32_t *counters;  // ticket, finished CTAs, queued chunks
+    uint32_t *queue;     // [units] chunks left to the last CTA
+};
+
+// Direct fp32 evaluation of one unit's outputs (queued chunks only).  The
+// entry state h_c is the predecessor's published inclusive state (or the init
+// state).  `gsm` holds C_i . B_j (64 KiB of shared memory).
+__device__ void finish_queued_unit(const Problem &pr, const FusedArgs &fa, int NS, size_t unit, float *gsm,
+                                   float *cs, float *dtv, float *warp_tot)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
+    const int nhb = H / HB, nc = pr.nchunks;
+    const int c = (int)(unit % nc), hb = (int)((unit / nc) % nhb), b = (int)(unit / ((size_t)nc * nhb));
+    const int h0 = hb * HB, G = pr.ngroups, g = h0 / (H / G);
+    const int t0 = c * pr.chunk, len = min(pr.chunk, L - t0);
+    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(pr.x);
+    const __nv_bfloat16 *Bm = static_cast<const __nv_bfloat16 *>(pr.B);
+    const __nv_bfloat16 *Cm = static_cast<const __nv_bfloat16 *>(pr.C);
+
+    // segment sums: warps 0-3 head 0, warps 4-7 head 1
+    {
+        const int hh = warp >> 2, t = tid & 127;
+        const bool active = hh < HB;
+        const float d = (active && t < len) ? pr.dt[((size_t)b * L + t0 + t) * H + h0 + hh] : 0.f;
+        float v = d * (active ? pr.A[h0 + hh] : 0.f);
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+        }
+        __syncthreads();
+        if (lane == 31) warp_tot[warp] = v;
+        __syncthreads();
+        for (int w = hh * 4; w < warp; ++w) v += warp_tot[w];
+        cs[hh * kRows + t] = v;
+        dtv[hh * kRows + t] = d;
+    }
+    // G_ij = C_i . B_j (causal part only)
+    for (int e = tid; e < kRows * kRows; e += kThreads) {
+        const int i = e >> 7, j = e & 127;
+        float s = 0.f;
+        if (i < len && j <= i) {
+            const __nv_bfloat16 *ci = Cm + (((size_t)b * L + t0 + i) * G + g) * NS;
+            const __nv_bfloat16 *bj = Bm + (((size_t)b * L + t0 + j) * G + g) * NS;
+            for (int n = 0; n < NS; ++n) s = fmaf(__bfloat162float(ci[n]), __bfloat162float(bj[n]), s);
+        }
+        gsm[e] = s;
+    }
+    __syncthreads();
+    const float *hprev = c > 0 ? fa.incl + (unit - 1) * (size_t)kRows * NS : nullptr;
+    for (int o = tid; o < kRows * kRows; o += kThreads) {
+        const int i = o >> 7, col = o & 127;  // col = (head, headdim) within the block
+        if (i >= len) continue;
+        const int hh = col / P, p = col % P, h = h0 + hh;
+        const float *csh = cs + hh * kRows, *dth = dtv + hh * kRows;
+        float acc = 0.f;
+        for (int j = 0; j <= i; ++j)
+            acc = fmaf(gsm[i * kRows + j] * expf(csh[i] - csh[j]) * dth[j],
+                       __bfloat162float(x[(((size_t)b * L + t0 + j) * H + h) * P + p]), acc);
+        float off = 0.f;
+        const __nv_bfloat16 *ci = Cm + (((size_t)b * L + t0 + i) * G + g) * NS;
+        for (int n = 0; n < NS; ++n) {
+            float hv = 0.f;
+            if (hprev) hv = __ldcg(hprev + (size_t)col * NS + n);
+            else if (pr.init_state) hv = pr.init_state[(((size_t)b * H + h) * P + p) * NS + n];
+            off = fmaf(__bfloat162float(ci[n]), hv, off);
+        }
+        const size_t yi = (((size_t)b * L + t0 + i) * H + h) * P + p;
+        const float Dh = pr.D ? pr.D[h] : 0.f;
+        static_cast<__nv_bfloat16 *>(pr.y)[yi] =
+            __float2bfloat16_rn(acc + expf(csh[i]) * off + Dh * __bfloat162float(x[yi]));
+    }
+    __syncthreads();
+}
+
+template <int NS>
+__global__ void __launch_bounds__(kThreads, 2)
+    ssd_fused_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
+                 const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap, Problem pr,
+                 FusedArgs fa)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_ld, bar_c, bar_g, bar_mma[2];
+    __shared__ uint32_t tmem_slot, s_ticket;
+    __shared__ float warp_tot[8], warp_mn[8], warp_mx[8];
+    __shared__ float cs[2 * kRows], dtv[2 * kRows];
+    __shared__ float vw[2 * kRows];    // v_j dt_j (0 past the chunk end)
+    __shared__ float rs[2 * kRows];    // r_i
+    __shared__ float s_alpha[2], s_sfac[2], s_yscale[2];
+    __shared__ int s_fail, s_mode, s_stop, s_stop_incl, s_last;
+
+    constexpr int NSL = NS / 64;        // 64-wide slabs of the state dimension
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3;       // TMEM lane quarter this warp may access
+    const int half = warp >> 2;         // which head / half of the columns this warp handles
+    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
+    const int nhb = H / HB, nc = pr.nchunks;
+    const unsigned total_units = gridDim.x;
+
+    // TMEM first, ticket second: a CTA never holds a ticket (that others may wait
+    // on) while it is itself still waiting for resources
+    if (warp == 0) tmem_alloc(&tmem_slot, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        s_ticket = atomicAdd(fa.counters + kCtrTicket, 1u);
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_c, 1);
+        mbar_init(&bar_g, 1);
+        mbar_init(&bar_mma[0], 1);
+        mbar_init(&bar_mma[1], 1);
+        mbar_fence_init();
+        s_fail = 0;
+        s_last = 0;
+    }
+    __syncthreads();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t col_y = 0, col_st = 128;   // Y (G first), chunk state
+
+    // chunk-major unit order: every predecessor chunk has a smaller ticket
+    const int ticket = (int)s_ticket;
+    const int c = ticket / (pr.batch * nhb);
+    const int rest = ticket - c * (pr.batch * nhb);
+    const int b = rest / nhb, hb = rest - (rest / nhb) * nhb;
+    const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
+    const int t0 = c * pr.chunk, len = min(pr.chunk, L - t0);
+    const size_t unit = ((size_t)b * nhb + hb) * nc + c;   // (b, hb, c) in the workspace
+
+    uint8_t *base = align1024(smem_raw);
+    uint8_t *xs = base;                              // x: 2 MN blocks x 16 KiB
+    uint8_t *bs = xs + 2 * kSlab;                    // B, later C again: NSL slabs
+    uint8_t *cm = bs + NSL * kSlab;                  // C, then tril(G) (2 slabs), later y staging
+    uint8_t *rr = cm + 2 * kSlab;                    // wx ping-pong: 2 x (hi 4 KiB | lo 4 KiB)
+    uint8_t *hh_s = NS == 64 ? cm : rr + kSlab;      // h hi | lo (NSL slabs each)
+
+    if (tid == 0) {
+        tma_prefetch_desc(&xmap);
+        tma_prefetch_desc(&bmap);
+        tma_prefetch_desc(&cmap);
+        mbar_expect_tx(&bar_ld, (uint32_t)((2 + 2 * NSL) * kSlab));
+        for (int k = 0; k < 2; ++k) tma_load_3d(xs + k * kSlab, &xmap, &bar_ld, hb * 128 + 64 * k, t0, b);
+        for (int s = 0; s < NSL; ++s) {
+            tma_load_3d(bs + s * kSlab, &bmap, &bar_ld, g * NS + 64 * s, t0, b);
+            tma_load_3d(cm + s * kSlab, &cmap, &bar_ld, g * NS + 64 * s, t0, b);
+        }
+    }
+
+    // ---- segment sums, span, reference, factors: warps 0-3 head 0, warps 4-7 head 1
+    bool fast;
+    {
+        const int hh = half, t = tid & 127;
+        const bool active = hh < HB;
+        const float a = active ? __ldg(pr.A + h0 + hh) : 0.f;
+        const float d = (active && t < len) ? __ldg(pr.dt + ((size_t)b * L + t0 + t) * H + h0 + hh) : 0.f;
+        float v = d * a;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+        }
+        if (lane == 31) warp_tot[warp] = v;
+        __syncthreads();
+        for (int w = half * 4; w < warp; ++w) v += warp_tot[w];
+        // range of cs over the chunk's tokens
+        float mn = t < len ? v : 3.0e38f, mx = t < len ? v : -3.0e38f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        if (lane == 0) {
+            warp_mn[warp] = mn;
+            warp_mx[warp] = mx;
+        }
+        cs[hh * kRows + t] = v;
+        dtv[hh * kRows + t] = d;
+        __syncthreads();
+        float lo_[2], hi_[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            lo_[k] = fminf(fminf(warp_mn[4 * k], warp_mn[4 * k + 1]), fminf(warp_mn[4 * k + 2], warp_mn[4 * k + 3]));
+            hi_[k] = fmaxf(fmaxf(warp_mx[4 * k], warp_mx[4 * k + 1]), fmaxf(warp_mx[4 * k + 2], warp_mx[4 * k + 3]));
+        }
+        fast = (hi_[0] - lo_[0] <= kSpanMax) && (HB == 1 || hi_[1] - lo_[1] <= kSpanMax);
+        const float cl = cs[hh * kRows + len - 1];
+        const float ref = 0.5f * ((hh == 0 ? lo_[0] : lo_[1]) + (hh == 0 ? hi_[0] : hi_[1]));
+        const float refw = fast ? ref : cl, refy = fast ? ref : 0.f;
+        if (active) {
+            vw[hh * kRows + t] = t < len ? expf(refw - v) * d : 0.f;
+            rs[hh * kRows + t] = expf(v - refy);
+            if (t == 0) {
+                s_alpha[hh] = expf(cl);
+                s_sfac[hh] = expf(cl - refw);
+                s_yscale[hh] = expf(refy);
+            }
+        }
+    }
+
+    bool ok = mbar_wait(&bar_ld, 0);
+    if (!ok) s_fail = 1;
+    __syncthreads();
+    ok = !s_fail;
+
+    // ---- G = C B^T, then the masked bf16 tril(G) over C
+    if (ok && tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t id_g = idesc_bf16(128, 128, 0, 0);
+        for (int ks = 0; ks < NS / 16; ++ks) {
+            const uint32_t off = (ks / 4) * kSlab + (ks % 4) * 32;
+            mma_bf16(tmem + col_y, sdesc_sw128(smem_u32(cm) + off, 16, 1024), sdesc_sw128(smem_u32(bs) + off, 16, 1024),
+                     id_g, ks > 0);
+        }
+        mma_commit(&bar_g);
+    }
+    if (ok && !mbar_wait(&bar_g, 0)) s_fail = 1;
+    __syncthreads();
+    ok = !s_fail;
+    tc_fence_after();
+    const int m = quarter * 32 + lane;   // TMEM row of this thread: token i, or (head, headdim)
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    if (ok && fast) {
+        for (int jb = 2 * half; jb < 2 * half + 2; ++jb) {
+            uint8_t *dst = cm + (jb >> 1) * kSlab;
+            const int q0 = (jb & 1) * 4;
+            if (jb > quarter) {  // every row of this warp is above the diagonal
+                const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4 *>(dst + sw128(m, q0 + u)) = z;
+                continue;
+            }
+            float gv[32];
+            tmem_ld32(tmem + lane_base + col_y + jb * 32, gv);
+            if (jb == quarter) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if (jb * 32 + k > m) gv[k] = 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4 *>(dst + sw128(m, q0 + u)) = pack8(gv + 8 * u);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- eight 16-token steps: wx (hi, lo) -> S_c += wx^T B ; Y += tril(G)[:, step] wx
+    if (ok) {
+        const int mb = tid >> 7, row = (tid >> 3) & 15, qq = tid & 7;
+        const float *vh = vw + (P == 64 ? mb : 0) * kRows;
+        for (int k = 0; k < 8; ++k) {
+            const int bb = k & 1;
+            uint8_t *buf = rr + bb * 8192;
+            if (k >= 2 && !mbar_wait(&bar_mma[bb], ((k - 2) >> 1) & 1)) s_fail = 1;
+            const int j = 16 * k + row;
+            const float w = vh[j];
+            const uint4 xv = *reinterpret_cast<const uint4 *>(xs + mb * kSlab + sw128(j, qq));
+            const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+            float f[8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 t = __bfloat1622float2(x2[u]);
+                f[2 * u] = t.x * w;
+                f[2 * u + 1] = t.y * w;
+            }
+            uint4 hi, lo;
+            split8(f, hi, lo);
+            *reinterpret_cast<uint4 *>(buf + mb * 2048 + sw128(row, qq)) = hi;
+            *reinterpret_cast<uint4 *>(buf + 4096 + mb * 2048 + sw128(row, qq)) = lo;
+            fence_async_smem();
+            __syncthreads();
+            if (s_fail) break;
+            if (tid == 0) {
+                tc_fence_after();
+                constexpr uint32_t id_s = idesc_bf16(128, NS, 1, 1);
+                const uint64_t bd = sdesc_sw128(smem_u32(bs) + k * 2048, kSlab, 1024);
+                mma_bf16(tmem + col_st, sdesc_sw128(smem_u32(buf), 2048, 1024), bd, id_s, k > 0);
+                mma_bf16(tmem + col_st, sdesc_sw128(smem_u32(buf) + 4096, 2048, 1024), bd, id_s, 1);
+                if (fast) {
+                    constexpr uint32_t id_d = idesc_bf16(128, 128, 0, 1);
+                    const uint64_t ad = sdesc_sw128(smem_u32(cm) + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
+                    mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(buf), 2048, 1024), id_d, k > 0);
+                    mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(buf) + 4096, 2048, 1024), id_d, 1);
+                }
+                mma_commit(&bar_mma[bb]);
+            }
+        }
+        if (!s_fail && (!mbar_wait(&bar_mma[0], 1) || !mbar_wait(&bar_mma[1], 1))) s_fail = 1;
+    }
+    __syncthreads();
+    ok = !s_fail;
+    tc_fence_after();
+    if (ok && fast && tid == 0) {  // B is consumed: bring C back for the off-diagonal product
+        mbar_expect_tx(&bar_c, (uint32_t)(NSL * kSlab));
+        for (int s = 0; s < NSL; ++s) tma_load_3d(bs + s * kSlab, &cmap, &bar_c, g * NS + 64 * s, t0, b);
+    }
+
+    // ---- state passing by decoupled look-back; this thread: row m = (head, headdim),
+    // state columns [n0, n0 + NS/2)
+    const int hh_m = m / P, p_m = m % P;
+    const size_t ustride = (size_t)kRows * NS;
+    const int n0 = half * (NS / 2);
+    const size_t row_off = (size_t)m * NS + n0;
+    const float sfac = s_sfac[hh_m];
+    if (ok && tid == 0) {
+        int mode = 0;  // 0: chunk 0, 1: predecessor inclusive ready, 2: look back
+        if (c > 0) mode = ld_acquire(fa.flags + unit - 1) == kFlagInclusive ? 1 : 2;
+        s_mode = mode;
+    }
+    __syncthreads();
+    const int mode = s_mode;
+    if (ok && mode == 2) {
+        // publish the aggregate (S_c, a_c) before waiting on anyone
+        float *dst = fa.agg + unit * ustride + row_off;
+        for (int cc = 0; cc < NS / 2; cc += 32) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + col_st + n0 + cc, v);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                __stcg(reinterpret_cast<float4 *>(dst + cc) + u, make_float4(sfac * v[4 * u], sfac * v[4 * u + 1],
+                                                                             sfac * v[4 * u + 2], sfac * v[4 * u + 3]));
+        }
+        if (tid < HB) fa.alpha[unit * 2 + tid] = s_alpha[tid];
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            st_release(fa.flags + unit, kFlagAggregate);
+            int k = c - 1, incl = 0;
+            const uint64_t tstart = globaltimer();
+            for (;;) {
+                const uint32_t f = ld_acquire(fa.flags + unit - (c - k));
+                if (f == kFlagNone) {
+                    if (globaltimer() - tstart > kWaitLimitNs) {
+                        s_fail = 1;
+                        break;
+                    }
+                    __nanosleep(64);
+                    continue;
+                }
+                if (f == kFlagInclusive) {
+                    incl = 1;
+                    break;
+                }
+                if (k == 0) break;
+                --k;
+            }
+            s_stop = k;
+            s_stop_incl = incl;
+        }
+        __syncthreads();
+        ok = !s_fail;
+    }
+
+    if (ok) {
+        const int stop = mode == 2 ? s_stop : (mode == 1 ? c - 1 : 0);
+        const int stop_incl = mode == 2 ? s_stop_incl : (mode == 1 ? 1 : 0);
+        if (mode == 1) (void)ld_acquire(fa.flags + unit - 1);
+        const float a_own = s_alpha[hh_m], ysc = s_yscale[hh_m];
+        const int hg = h0 + hh_m;
+        const float *init = pr.init_state ? pr.init_state + (((size_t)b * H + hg) * P + p_m) * NS + n0 : nullptr;
+        for (int cc = 0; cc < NS / 2; cc += 32) {
+            float acc[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+            if (mode == 0) {
+                if (init) fma_row32(acc, 1.f, init + cc);
+            } else {
+                float dec = 1.f;
+                for (int k = c - 1; k > stop; --k) {  // aggregates of chunks stop+1 .. c-1
+                    const size_t u = unit - (c - k);
+                    fma_row32(acc, dec, fa.agg + u * ustride + row_off + cc);
+                    dec *= __ldcg(fa.alpha + u * 2 + hh_m);
+                }
+                const size_t u = unit - (c - stop);
+                fma_row32(acc, dec, (stop_incl ? fa.incl : fa.agg) + u * ustride + row_off + cc);
+                if (!stop_incl && init) {  // reached chunk 0 through aggregates: decayed init state
+                    dec *= __ldcg(fa.alpha + u * 2 + hh_m);
+                    fma_row32(acc, dec, init + cc);
+                }
+            }
+            if (fast) {  // e^ref h_c -> bf16 hi / lo operand slabs (row m)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float f[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) f[u] = ysc * acc[8 * q + u];
+                    uint4 hi, lo;
+                    split8(f, hi, lo);
+                    const int n = n0 + cc + 8 * q;
+                    const uint32_t o = (n / 64) * kSlab + sw128(m, (n % 64) / 8);
+                    *reinterpret_cast<uint4 *>(hh_s + o) = hi;
+                    *reinterpret_cast<uint4 *>(hh_s + NSL * kSlab + o) = lo;
+                }
+            }
+            // h_{c+1} = a_c h_c + S_c
+            float sc[32];
+            tmem_ld32(tmem + lane_base + col_st + n0 + cc, sc);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) sc[k] = fmaf(a_own, acc[k], sfac * sc[k]);
+            float4 *dst = reinterpret_cast<float4 *>(fa.incl + unit * ustride + row_off + cc);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                __stcg(dst + q, make_float4(sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3]));
+            if (c == nc - 1 && pr.final_state) {
+                float4 *fo = reinterpret_cast<float4 *>(pr.final_state + (((size_t)b * H + hg) * P + p_m) * NS + n0 + cc);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) fo[q] = make_float4(sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3]);
+            }
+        }
+        __threadfence();
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (ok && tid == 0) {
+        st_release(fa.flags + unit, kFlagInclusive);
+        if (fast) {
+            // Y += C (e^ref h_c)^T
+            if (!mbar_wait(&bar_c, 0)) {
+                s_fail = 1;
+            } else {
+                tc_fence_after();
+                constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 0);
+                for (int ks = 0; ks < NS / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * kSlab + (ks % 4) * 32;
+                    const uint64_t ad = sdesc_sw128(smem_u32(bs) + off, 16, 1024);
+                    mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(hh_s) + off, 16, 1024), id_o, 1);
+                    mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(hh_s) + NSL * kSlab + off, 16, 1024), id_o, 1);
+                }
+                mma_commit(&bar_g);
+            }
+        } else {
+            fa.queue[atomicAdd(fa.counters + kCtrFallback, 1u)] = (uint32_t)unit;
+        }
+    }
+    __syncthreads();
+    ok = ok && !s_fail;
+    if (ok && fast && !mbar_wait(&bar_g, 1)) s_fail = 1;
+    __syncthreads();
+    ok = ok && !s_fail;
+    tc_fence_after();
+
+    // ---- y = r_i Y + D x; this thread: row i, 64 of the 128 (head, headdim) columns
+    const bool tma_out = pr.chunk == kRows;  // full 128-row tiles: staged in shared memory, TMA store
+    uint8_t *ystage = cm;
+    if (ok && fast) {
+        const int i = m, col0 = half * 64;
+        const int hh = col0 / P, h = h0 + hh;
+        const float r = rs[hh * kRows + i];
+        const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
+        for (int pc = 0; pc < 64; pc += 32) {
+            const int col = col0 + pc;
+            float yv[32];
+            tmem_ld32(tmem + lane_base + col_y + col, yv);
+            uint4 outv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xs + half * kSlab + sw128(i, pc / 8 + u));
+                const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                float o[8];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const float2 xf = __bfloat1622float2(x2[v]);
+                    o[2 * v] = fmaf(Dh, xf.x, r * yv[8 * u + 2 * v]);
+                    o[2 * v + 1] = fmaf(Dh, xf.y, r * yv[8 * u + 2 * v + 1]);
+                }
+                outv[u] = pack8(o);
+            }
+            if (tma_out) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4 *>(ystage + half * kSlab + sw128(i, pc / 8 + u)) = outv[u];
+            } else if (i < len) {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
+                                                       (((size_t)b * L + t0 + i) * H + h0) * P + col);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) dst[u] = outv[u];
+            }
+        }
+    }
+    if (tma_out) {
+        fence_async_smem();
+        __syncthreads();
+        if (ok && fast && tid == 0) {
+            for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, hb * 128 + 64 * k, t0, b);
+            bulk_commit();
+            bulk_wait_read_all();
+        }
+    }
+    if (!ok && tid == 0) atomicOr(pr.err_word, kDevErrTimeout);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+
+    // ---- the last CTA to finish computes the queued chunks' outputs
+    if (tid == 0) {
+        __threadfence();
+        s_last = atomicAdd(fa.counters + kCtrDone, 1u) == total_units - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        const uint32_t nq = *reinterpret_cast<volatile uint32_t *>(fa.counters + kCtrFallback);
+        for (uint32_t q = 0; q < nq; ++q)
+            finish_queued_unit(pr, fa, NS, fa.queue[q], reinterpret_cast<float *>(base), cs, dtv, warp_tot);
+    }
+}
+
+cudaError_t make_map(CUtensorMap *map, const void *ptr, int width, int seqlen, int batch)
+{
+    auto fn = tensor_map_encoder();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)seqlen, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * seqlen};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kRows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// x | B (then C) | C (then tril(G), then y) | wx ping-pong | h hi/lo (dstate 128 only)
+size_t fused_smem(int NS)
+{
+    const size_t body = (size_t)(2 + NS / 64 + 2) * kSlab + kSlab;  // ..., wx ping-pong 16 KiB
+    const size_t hreg = NS == 64 ? 0 : (size_t)2 * (NS / 64) * kSlab;
+    return 1024 + body + hreg;
+}
+
+size_t units_of(const Problem &pr) { return (size_t)pr.batch * (pr.nheads / (128 / pr.headdim)) * pr.nchunks; }
+
+template <int NS>
+cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
+{
+    CUtensorMap xmap, bmap, cmap, ymap;
+    cudaError_t e;
+    if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+    if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+    if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+    if ((e = make_map(&ymap, pr.y, pr.nheads * pr.headdim, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+    const size_t smem = fused_smem(NS);
+    if ((e = cudaFuncSetAttribute(ssd_fused_tc<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        cudaSuccess)
+        return e;
+    const size_t units = units_of(pr);
+    if ((e = cudaMemsetAsync(fa.flags, 0, (units + kCtrCount) * sizeof(uint32_t), s)) != cudaSuccess) return e;
+    ssd_fused_tc<NS><<<(unsigned)units, kThreads, smem, s>>>(xmap, bmap, cmap, ymap, pr, fa);
+    return cudaGetLastError();
+}
+
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+
+bool fused_supported(const Problem &pr)
+{
+    if (pr.dtype != SSD_DTYPE_BF16) return false;
+    if (pr.headdim != 64 && pr.headdim != 128) return false;
+    if (pr.dstate != 64 && pr.dstate != 128) return false;
+    if (pr.chunk > kRows) return false;
+    const int HB = 128 / pr.headdim;
+    if (pr.nheads % HB != 0 || (pr.nheads / pr.ngroups) % HB != 0) return false;
+    return units_of(pr) < (1u << 31);
+}
+
+size_t fused_workspace_bytes(const Problem &pr)
+{
+    const size_t units = units_of(pr);
+    const size_t states = units * kRows * pr.dstate * sizeof(float);
+    return 2 * up256(states) + up256(units * 2 * sizeof(float)) + up256((units + kCtrCount) * sizeof(uint32_t)) +
+           up256(units * sizeof(uint32_t));
+}
+
+cudaError_t launch_fused_tc(const Problem &pr, void *workspace, cudaStream_t s)
+{
+    const size_t units = units_of(pr);
+    const size_t states = units * kRows * pr.dstate * sizeof(float);
+    char *p = static_cast<char *>(workspace);
+    FusedArgs fa;
+    fa.agg = reinterpret_cast<float *>(p);
+    p += up256(states);
+    fa.incl = reinterpret_cast<float *>(p);
+    p += up256(states);
+    fa.alpha = reinterpret_cast<float *>(p);
+    p += up256(units * 2 * sizeof(float));
+    fa.flags = reinterpret_cast<uint32_t *>(p);
+    fa.counters = fa.flags + units;
+    p += up256((units + kCtrCount) * sizeof(uint32_t));
+    fa.queue = reinterpret_cast<uint32_t *>(p);
+    return pr.dstate == 64 ? launch<64>(pr, fa, s) : launch<128>(pr, fa, s);
+}
+
+}  // namespace ssd

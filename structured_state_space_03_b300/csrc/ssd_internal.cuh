@@ -66,7 +66,12 @@ cudaError_t launch_chunk_out_simt(const Problem &pr, const Workspace &ws, cudaSt
 bool tc_supported(const Problem &pr);
 cudaError_t launch_chunk_state_tc(const Problem &pr, const Workspace &ws, cudaStream_t s);
 cudaError_t launch_chunk_out_tc(const Problem &pr, const Workspace &ws, cudaStream_t s);
-// Sequential inter-chunk state passing, shared by every path.
+// Single fused tcgen05 kernel with a decoupled look-back over published chunk
+// states: bf16, headdim 64/128, dstate 64/128, chunk <= 128.
+bool fused_supported(const Problem &pr);
+size_t fused_workspace_bytes(const Problem &pr);
+cudaError_t launch_fused_tc(const Problem &pr, void *workspace, cudaStream_t s);
+// Sequential inter-chunk state passing, shared by the multi-kernel paths.
 cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream_t s);
 
 constexpr int kMaxChunk = 256;

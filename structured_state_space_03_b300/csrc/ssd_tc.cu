@@ -573,6 +573,8 @@ cudaError_t dispatch(const Problem &pr, const Workspace &ws, cudaStream_t s, int
 
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return encode_fn(); }
+
 bool tc_supported(const Problem &pr)
 {
     if (pr.dtype != SSD_DTYPE_BF16) return false;

@@ -94,9 +94,14 @@ def test_outside_build_is_unsupported(lib, field, value):
 def test_workspace_size_and_checks(lib):
     nc = -(-DIMS["seqlen"] // DIMS["chunk"])
     units = DIMS["batch"] * DIMS["nheads"] * nc
-    want = units * DIMS["headdim"] * DIMS["dstate"] * 4
+    states = units * DIMS["headdim"] * DIMS["dstate"] * 4
+    # multi-kernel paths: one fp32 state per (batch, head, chunk) plus the chunk decays
+    got = ssd.ssd_fwd_workspace_size(*DIMS.values(), ssd.SSD_DTYPE_F32)
+    assert states <= got <= states + units * 4 + 512
+    # fused path: published aggregate and inclusive states, decays and flags
+    assert ssd.ssd_fwd_path(*DIMS.values(), ssd.SSD_DTYPE_BF16) == "tcgen05_fused"
     got = ssd.ssd_fwd_workspace_size(*DIMS.values(), ssd.SSD_DTYPE_BF16)
-    assert want <= got <= want + units * 4 + 512
+    assert 2 * states <= got <= 2 * states + units * 8 + 1024
     out = ctypes.c_size_t(0)
     assert lib.ssd_fwd_workspace_size(0, 1, 1, 1, 1, 1, 1, 1, ctypes.byref(out)) == ssd.SSD_ERR_INVALID_ARG
     assert lib.ssd_fwd_workspace_size(1, 1, 1, 1, 1, 1, 1, 1, None) == ssd.SSD_ERR_INVALID_ARG
@@ -118,11 +123,15 @@ def test_path_selection_is_a_pure_host_query(lib):
     assert ssd.ssd_fwd_path(1, 256, 4, 16, 1, 16, 64, ssd.SSD_DTYPE_F32) == "simt"
     assert ssd.ssd_fwd_path(1, 256, 4, 16, 1, 16, 999, ssd.SSD_DTYPE_F32) == "none"
     assert ssd.ssd_fwd_path(1, 256, 4, 16, 3, 16, 64, ssd.SSD_DTYPE_F32) == "none"
-    # bf16 with headdim 64/128, dstate 64/128/256 and chunk <= 256 runs on the tensor cores
-    assert ssd.ssd_fwd_path(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == "tcgen05"
-    assert ssd.ssd_fwd_path(16, 4096, 32, 128, 8, 128, 128, ssd.SSD_DTYPE_BF16) == "tcgen05"
+    # bf16 with headdim 64/128, dstate 64/128 and chunk <= 128: one fused tcgen05 kernel;
+    # dstate 256 or chunk up to 256: the three-kernel tcgen05 path
+    assert ssd.ssd_fwd_path(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == "tcgen05_fused"
+    assert ssd.ssd_fwd_path(16, 4096, 32, 128, 8, 128, 128, ssd.SSD_DTYPE_BF16) == "tcgen05_fused"
+    assert ssd.ssd_fwd_path(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == "tcgen05"
     assert ssd.ssd_fwd_path(1, 131072, 24, 64, 1, 256, 256, ssd.SSD_DTYPE_BF16) == "tcgen05"
+    assert ssd.ssd_fwd_path(1, 1000, 4, 64, 1, 256, 128, ssd.SSD_DTYPE_BF16) == "tcgen05"
     assert ssd.ssd_fwd_path(2, 333, 6, 32, 3, 48, 100, ssd.SSD_DTYPE_BF16) == "simt"
     assert ssd.ssd_fwd_path(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_F32) == "simt"
-    assert ssd.ssd_fwd_kernels(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == [
+    assert ssd.ssd_fwd_kernels(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == ["ssd_fused_tc"]
+    assert ssd.ssd_fwd_kernels(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == [
         "chunk_state_tc", "state_pass", "chunk_out_tc"]

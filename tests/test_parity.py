@@ -29,7 +29,7 @@ def test_tiny_f32_full():
 @pytest.mark.parametrize("w", WORKLOADS[1:], ids=[w.name for w in WORKLOADS[1:]])
 def test_workload_sampled_rows(w):
     assert ssd.ssd_fwd_path(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk,
-                            ssd.SSD_DTYPE_BF16) == "tcgen05"
+                            ssd.SSD_DTYPE_BF16) in ("tcgen05", "tcgen05_fused")
     inp = workload_inputs(w)
     rows = sample_rows(w, 48)
     check_rows(inp, rows, w.chunk)
@@ -40,6 +40,9 @@ def test_workload_sampled_rows(w):
 MID = [
     # b, L, H, P, N, G, Q, dtype
     (2, 1000, 8, 64, 64, 2, 128, "bf16"),
+    (1, 8000, 2, 64, 64, 1, 64, "bf16"),      # 125 chained chunks of one head pair: deep look-back
+    (3, 700, 4, 128, 128, 2, 100, "bf16"),
+    (1, 1000, 4, 64, 256, 1, 128, "bf16"),
     (1, 777, 4, 64, 128, 1, 256, "bf16"),
     (1, 600, 4, 64, 256, 1, 256, "bf16"),
     (2, 513, 8, 128, 128, 2, 128, "bf16"),
@@ -205,3 +208,20 @@ def test_runs_on_a_side_stream():
                              stream=s)
     ssd.ssd_check_device_status(s)
     assert torch.equal(y0, y1) and torch.equal(f0, f1)
+
+
+@pytest.mark.parametrize("case", [(1, 300, 4, 64, 64, 1, 128), (2, 256, 2, 128, 64, 1, 128), (1, 200, 2, 64, 128, 1, 64)],
+                         ids=["P64N64", "P128N64", "P64N128Q64"])
+def test_extreme_in_chunk_decay(case):
+    """dt up to 2 with |A| up to 16: the decay inside one chunk spans far more
+    than the factored (rank-one) path allows; those chunks are finished by the
+    direct fp32 evaluation."""
+    b, L, H, P, N, G, Q = case
+    inp = make_inputs(b, L, H, P, N, G, "bf16", seed=77, dt_range=(0.5, 2.0), with_init=True)
+    check_full(inp, Q)
+
+
+def test_mixed_fast_and_queued_chunks():
+    inp = make_inputs(1, 512, 8, 64, 64, 1, "bf16", seed=78, with_init=True)
+    inp["dt"][:, :, 4:] *= 20.0  # head blocks 2 and 3: spans beyond the factored path in every chunk
+    check_full(inp, 128)
