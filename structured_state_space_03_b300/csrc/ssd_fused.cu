@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ float vw[2 * kRows];    // v_j dt_j (0 past the chunk end)
     __shared__ float rs[2 * kRows];    // r_i
     __shared__ float s_alpha[2], s_sfac[2], s_yscale[2];
-    __shared__ int s_fail, s_mode, s_stop, s_stop_incl, s_last;
+    __shared__ int s_fail, s_mode, s_stop, s_last;
 
     constexpr int NSL = NS / 64;        // 64-wide slabs of the state dimension
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -456,37 +456,48 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (tid < HB) fa.alpha[unit * 2 + tid] = s_alpha[tid];
         __threadfence();
         __syncthreads();
-        if (tid == 0) {
-            st_release(fa.flags + unit, kFlagAggregate);
-            int k = c - 1, incl = 0;
+        if (warp == 0) {
+            if (lane == 0) st_release(fa.flags + unit, kFlagAggregate);
+            // Walk back, 32 predecessors per poll: stop at the nearest chunk whose
+            // inclusive state is published (or before chunk 0: the init state);
+            // every chunk in between must have published its aggregate.
+            int top = c - 1, stop = -1;
             const uint64_t tstart = globaltimer();
+            bool timed_out = false;
             for (;;) {
-                const uint32_t f = ld_acquire(fa.flags + unit - (c - k));
-                if (f == kFlagNone) {
-                    if (globaltimer() - tstart > kWaitLimitNs) {
-                        s_fail = 1;
+                const int k = top - lane;
+                const uint32_t f = k >= 0 ? ld_acquire(fa.flags + unit - (c - k)) : kFlagInclusive;
+                const uint32_t end_mask = __ballot_sync(0xffffffffu, f == kFlagInclusive);
+                const uint32_t none_mask = __ballot_sync(0xffffffffu, f == kFlagNone);
+                const uint32_t before = end_mask ? (end_mask & (0u - end_mask)) - 1u : 0xffffffffu;
+                if ((none_mask & (end_mask ? before : 0xffffffffu)) == 0u) {
+                    if (end_mask) {
+                        stop = top - (__ffs(end_mask) - 1);  // -1: the init state
                         break;
                     }
-                    __nanosleep(64);
+                    top -= 32;  // 32 aggregates, keep walking
                     continue;
                 }
-                if (f == kFlagInclusive) {
-                    incl = 1;
+                if (globaltimer() - tstart > kWaitLimitNs) {
+                    timed_out = true;
                     break;
                 }
-                if (k == 0) break;
-                --k;
+                __nanosleep(64);
             }
-            s_stop = k;
-            s_stop_incl = incl;
+            if (lane == 0) {
+                s_stop = stop;
+                if (timed_out) s_fail = 1;
+            }
         }
         __syncthreads();
         ok = !s_fail;
     }
 
     if (ok) {
-        const int stop = mode == 2 ? s_stop : (mode == 1 ? c - 1 : 0);
-        const int stop_incl = mode == 2 ? s_stop_incl : (mode == 1 ? 1 : 0);
+        // h_c in the recurrence's own order: start from the stop chunk's inclusive
+        // state (or the init state) and apply h <- a_k h + S_k for each later chunk,
+        // so the result does not depend on how far the walk went
+        const int stop = mode == 2 ? s_stop : c - 1;   // mode 0: c - 1 = -1, the init state
         if (mode == 1) (void)ld_acquire(fa.flags + unit - 1);
         const float a_own = s_alpha[hh_m], ysc = s_yscale[hh_m];
         const int hg = h0 + hh_m;
@@ -495,20 +506,19 @@ __global__ void __launch_bounds__(kThreads, 2)
             float acc[32];
 #pragma unroll
             for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-            if (mode == 0) {
-                if (init) fma_row32(acc, 1.f, init + cc);
-            } else {
-                float dec = 1.f;
-                for (int k = c - 1; k > stop; --k) {  // aggregates of chunks stop+1 .. c-1
-                    const size_t u = unit - (c - k);
-                    fma_row32(acc, dec, fa.agg + u * ustride + row_off + cc);
-                    dec *= __ldcg(fa.alpha + u * 2 + hh_m);
-                }
-                const size_t u = unit - (c - stop);
-                fma_row32(acc, dec, (stop_incl ? fa.incl : fa.agg) + u * ustride + row_off + cc);
-                if (!stop_incl && init) {  // reached chunk 0 through aggregates: decayed init state
-                    dec *= __ldcg(fa.alpha + u * 2 + hh_m);
-                    fma_row32(acc, dec, init + cc);
+            if (stop >= 0) fma_row32(acc, 1.f, fa.incl + (unit - (c - stop)) * ustride + row_off + cc);
+            else if (init) fma_row32(acc, 1.f, init + cc);
+            for (int k = stop + 1; k < c; ++k) {
+                const size_t u = unit - (c - k);
+                const float a = __ldcg(fa.alpha + u * 2 + hh_m);
+                const float4 *src = reinterpret_cast<const float4 *>(fa.agg + u * ustride + row_off + cc);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 v = __ldcg(src + q);
+                    acc[4 * q] = fmaf(a, acc[4 * q], v.x);
+                    acc[4 * q + 1] = fmaf(a, acc[4 * q + 1], v.y);
+                    acc[4 * q + 2] = fmaf(a, acc[4 * q + 2], v.z);
+                    acc[4 * q + 3] = fmaf(a, acc[4 * q + 3], v.w);
                 }
             }
             if (fast) {  // e^ref h_c -> bf16 hi / lo operand slabs (row m)
