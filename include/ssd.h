@@ -143,6 +143,35 @@ SSD_API ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A
                           int chunk, ssd_dtype_t dtype, void *stream);
 
 /*
+ * ssd_fwd_noalloc -- ssd_fwd for callers that may not allocate device memory.
+ * This entry point has no counterpart in the SSD papers; it exists for
+ * deployment: processes that hand all device memory to a framework-owned pool,
+ * plugins hosted by such runtimes, and latency-critical loops that cannot
+ * afford an allocator call, which can synchronise the device or fail under
+ * memory pressure.
+ *
+ * Same arguments, layouts and asynchronous behaviour as ssd_fwd.  Instead of a
+ * workspace it uses a fixed 32 MiB scratch array compiled into the library,
+ * which every device that loads the library holds until the process exits; it
+ * calls no allocator at all.  It runs the fused bf16 kernel only (bf16,
+ * headdim 64 or 128, dstate 64 or 128, chunk <= 128) and returns
+ * SSD_ERR_UNSUPPORTED, with the needed and available sizes in
+ * ssd_last_error_detail(), for anything else or for a problem whose scratch
+ * (ssd_fwd_workspace_size) exceeds 32 MiB.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ * capture.  All calls on a device share the one array, and each call clears
+ * the parts that must start at zero: calls whose work overlaps on the GPU
+ * (different streams, or another thread) race and corrupt each other's
+ * results.  Serialise them.
+ */
+SSD_API ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                                     const float *D, const float *init_state, void *y, float *final_state,
+                                     int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                                     int chunk, ssd_dtype_t dtype, void *stream);
+
+/*
  * ssd_fwd_path -- the kernel family ssd_fwd would run for these sizes
  * (SSD_PATH_NONE when they are rejected).  Pure host function: no CUDA call.
  */

@@ -40,6 +40,7 @@ SIGNATURES = {
     "ssd_fwd": (_I, _FWD + [_P]),
     "ssd_fwd_ws": (_I, _FWD + [_P, _S, _P]),
     "ssd_fwd_host": (_I, _FWD + [_P]),
+    "ssd_fwd_noalloc": (_I, _FWD + [_P]),
     "ssd_fwd_workspace_size": (_I, _DIMS + [ctypes.POINTER(ctypes.c_size_t)]),
     "ssd_fwd_path": (_I, _DIMS),
     "ssd_fwd_kernels": (_I, _DIMS + [ctypes.c_char_p, _S]),
@@ -170,6 +171,20 @@ def ssd_fwd(x, dt, A, B, C, D=None, init_state=None, *, chunk: int, y=None, fina
     _check(lib().ssd_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state), _ptr(y),
                          _ptr(final_state), b, L, H, P, G, N, chunk, _dtype_code(x.dtype),
                          _stream_handle(stream)))
+    return y, final_state
+
+
+def ssd_fwd_noalloc(x, dt, A, B, C, D=None, init_state=None, *, chunk: int, y=None, final_state=None,
+                    return_final: bool = True, stream=None):
+    """SSD forward that allocates nothing on the device side of the call: the
+    library's fixed 32 MiB scratch replaces the workspace (see include/ssd.h for
+    who needs this and its limits).  ``y``/``final_state`` may be passed in to
+    avoid allocating outputs here as well."""
+    b, L, H, P, G, N = _validate(x, dt, A, B, C, D, init_state, "cuda")
+    y, final_state = _outputs(x, b, H, P, N, y, final_state, return_final)
+    _check(lib().ssd_fwd_noalloc(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
+                                 _ptr(y), _ptr(final_state), b, L, H, P, G, N, chunk, _dtype_code(x.dtype),
+                                 _stream_handle(stream)))
     return y, final_state
 
 

@@ -284,6 +284,63 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
     return st;
 }
 
+// ---------------------------------------------------------------------------
+// Forward without any allocation, for callers that may not allocate device
+// memory: processes whose device memory is handed in full to a framework-owned
+// pool, plugins hosted by such runtimes, and latency-critical loops that cannot
+// afford an allocator call (it can synchronise the device or fail under memory
+// pressure).  Its scratch is the fixed array below, which every device that
+// loads this library keeps until the process exits.
+// ---------------------------------------------------------------------------
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array on the current device.  The first call
+// on a device looks it up (cudaGetSymbolAddress); later calls reuse it.
+static ssd_status_t noalloc_scratch(void **out)
+{
+    static std::mutex mu;
+    static void *addr[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(SSD_ERR_UNSUPPORTED, "device ordinal %d beyond 63", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return fail(SSD_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return SSD_OK;
+}
+
+ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                             const float *D, const float *init_state, void *y, float *final_state, int batch,
+                             int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk,
+                             ssd_dtype_t dtype, void *stream)
+{
+    Problem pr;
+    ssd_status_t st = make_problem(pr, x, dt, A, B, C, D, init_state, y, final_state, batch, seqlen, nheads,
+                                   headdim, ngroups, dstate, chunk, dtype);
+    if (st != SSD_OK) return st;
+    if (choose_path(pr) != SSD_PATH_TCGEN05_FUSED)
+        return fail(SSD_ERR_UNSUPPORTED,
+                    "ssd_fwd_noalloc runs the fused bf16 kernel only (bf16, headdim 64 or 128, dstate 64 or "
+                    "128, chunk <= 128)");
+    const size_t need = workspace_bytes(pr);
+    if (need > kNoAllocScratchBytes)
+        return fail(SSD_ERR_UNSUPPORTED,
+                    "problem needs %zu bytes of scratch; the fixed scratch of ssd_fwd_noalloc holds %zu bytes",
+                    need, kNoAllocScratchBytes);
+    void *scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)) != SSD_OK) return st;
+    return run(pr, scratch, static_cast<cudaStream_t>(stream));
+}
+
 ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const void *B, const void *C,
                           const float *D, const float *init_state, void *y, float *final_state, int batch,
                           int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk,
