@@ -21,19 +21,25 @@
 //
 //   1. TMA x, B, C; segment sums, span, ref, r, v, a_c = exp(cs_last).
 //   2. G = C B^T (tcgen05) -> masked bf16 tril(G) in shared memory.
-//   3. Eight 16-token steps, double-buffered: build wx (hi, lo), then
-//      S_c += wx^T B and Y += tril(G)[:, step] wx on the tensor cores.
-//   4. Look-back: if the predecessor chunk's inclusive state h_c is published,
+//   3. Eight 16-token steps through a 3-buffer ring (full/empty mbarriers):
+//      all threads build wx (hi, lo) for step k while thread 0 issues step
+//      k-1's S_c += wx^T B and Y += tril(G)[:, step] wx on the tensor cores.
+//   4. Look-back: if the predecessor chunk's inclusive state is published,
 //      read it; else publish (S_c, a_c) as this chunk's aggregate first, then
-//      walk back combining aggregates until an inclusive state (or chunk 0 and
-//      the init state).  Publish h_{c+1} = a_c h_c + S_c; the last chunk writes
-//      final_state.
+//      walk back (32 predecessors per poll) to the nearest published inclusive
+//      state (or the init state) and apply h <- a_k h + S_k forward, the
+//      recurrence's own order, so the result is independent of the walk.
+//      Publish h_{c+1} = a_c h_c + S_c; the last chunk writes final_state.
+//      Publication: each thread writes its part, then adds 1 to the unit's
+//      counter with release semantics (no fence, no barrier); a reader that
+//      acquires the full count sees every part.
 //   5. Y += C (e^ref h_c)^T (h as hi + lo), then y = r_i Y + D x, staged in
 //      shared memory and written by TMA.
 //
 // A chunk whose span exceeds 120 (an extreme decay inside one chunk) keeps
-// steps 1-4 with the decay referenced to the chunk end, skips 5, and is queued;
-// the last CTA to finish computes the queued chunks' outputs directly in fp32.
+// steps 1-4 with the decay referenced to the chunk end and replaces 5 by a
+// direct evaluation with per-element decays (slow; never taken by the
+// workloads here, exercised by the tests).
 //
 // Forward progress: CTAs take their unit from an atomic ticket in chunk-major
 // order (after allocating tensor memory), so every unit a CTA waits on belongs
@@ -61,7 +67,7 @@ constexpr int kSlab = 64 * 2 * kRows;      // 64 bf16 columns x 128 rows = 16 Ki
 constexpr float kSpanMax = 120.f;          // widest in-chunk cs range of the factored path
 
 enum : uint32_t { kFlagNone = 0, kFlagAggregate = 1, kFlagInclusive = 2 };
-enum { kCtrTicket = 0, kCtrDone = 1, kCtrFallback = 2, kCtrCount = 4 };
+enum { kCtrTicket = 0, kCtrCount = 4 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
@@ -75,9 +81,10 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
     return v;
 }
 
-__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v)
+// Fire-and-forget increment that orders this thread's earlier writes before it.
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
 {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t sw128(int r, int q) { return (uint32_t)r * 128u + (uint32_t)((q ^ (r & 7)) << 4); }
@@ -126,84 +133,64 @@ __device__ __forceinline__ void fma_row32(float (&acc)[32], float s, const float
     }
 }
 
+// A unit's aggregate (inclusive) state is published once its aggcnt (inclcnt)
+// reaches the CTA's thread count: every thread adds 1 with release semantics
+// after writing its own part, so an acquiring reader that sees the full count
+// sees every part.
 struct FusedArgs {
     float *agg;          // [units][128][NS] aggregate chunk states S_c
     float *incl;         // [units][128][NS] inclusive states h_{c+1}
     float *alpha;        // [units][2] chunk decays a_c per head of the block
-    uint32_t *flags;     // [units] publication state (counters follow)
-    uint32_t *counters;  // ticket, finished CTAs, queued chunks
-    uint32_t *queue;     // [units] chunks left to the last CTA
+    uint32_t *aggcnt;    // [units] aggregate publication count
+    uint32_t *inclcnt;   // [units] inclusive publication count (counters follow)
+    uint32_t *counters;  // ticket
 };
 
-// Direct fp32 evaluation of one unit's outputs (queued chunks only).  The
-// entry state h_c is the predecessor's published inclusive state (or the init
-// state).  `gsm` holds C_i . B_j (64 KiB of shared memory).
-__device__ void finish_queued_unit(const Problem &pr, const FusedArgs &fa, int NS, size_t unit, float *gsm,
-                                   float *cs, float *dtv, float *warp_tot)
+// Direct fp32 evaluation of this unit's outputs with per-element decays, for a
+// chunk whose decay range is too wide for the factored form.  `hcs` holds h_c
+// ([128][NS] fp32, rows (head, headdim)); `gsm` (32 KiB) receives C_i . B_j for
+// 64 output rows at a time.  Slow, and used only for such chunks.
+__device__ void direct_unit_outputs(const Problem &pr, int NS, int b, int hb, int c, const float *hcs, float *gsm,
+                                    const float *cs, const float *dtv)
 {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
-    const int nhb = H / HB, nc = pr.nchunks;
-    const int c = (int)(unit % nc), hb = (int)((unit / nc) % nhb), b = (int)(unit / ((size_t)nc * nhb));
     const int h0 = hb * HB, G = pr.ngroups, g = h0 / (H / G);
     const int t0 = c * pr.chunk, len = min(pr.chunk, L - t0);
     const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(pr.x);
     const __nv_bfloat16 *Bm = static_cast<const __nv_bfloat16 *>(pr.B);
     const __nv_bfloat16 *Cm = static_cast<const __nv_bfloat16 *>(pr.C);
-
-    // segment sums: warps 0-3 head 0, warps 4-7 head 1
-    {
-        const int hh = warp >> 2, t = tid & 127;
-        const bool active = hh < HB;
-        const float d = (active && t < len) ? pr.dt[((size_t)b * L + t0 + t) * H + h0 + hh] : 0.f;
-        float v = d * (active ? pr.A[h0 + hh] : 0.f);
-        for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += u;
+    for (int i0 = 0; i0 < kRows; i0 += 64) {
+        __syncthreads();
+        for (int e = tid; e < 64 * kRows; e += kThreads) {  // causal part of C_i . B_j, rows i0 .. i0+63
+            const int i = i0 + (e >> 7), j = e & 127;
+            float s = 0.f;
+            if (i < len && j <= i) {
+                const __nv_bfloat16 *ci = Cm + (((size_t)b * L + t0 + i) * G + g) * NS;
+                const __nv_bfloat16 *bj = Bm + (((size_t)b * L + t0 + j) * G + g) * NS;
+                for (int n = 0; n < NS; ++n) s = fmaf(__bfloat162float(ci[n]), __bfloat162float(bj[n]), s);
+            }
+            gsm[e] = s;
         }
         __syncthreads();
-        if (lane == 31) warp_tot[warp] = v;
-        __syncthreads();
-        for (int w = hh * 4; w < warp; ++w) v += warp_tot[w];
-        cs[hh * kRows + t] = v;
-        dtv[hh * kRows + t] = d;
-    }
-    // G_ij = C_i . B_j (causal part only)
-    for (int e = tid; e < kRows * kRows; e += kThreads) {
-        const int i = e >> 7, j = e & 127;
-        float s = 0.f;
-        if (i < len && j <= i) {
+        for (int o = tid; o < 64 * kRows; o += kThreads) {
+            const int i = i0 + (o >> 7), col = o & 127;  // col = (head, headdim) within the block
+            if (i >= len) continue;
+            const int hh = col / P, p = col % P, h = h0 + hh;
+            const float *csh = cs + hh * kRows, *dth = dtv + hh * kRows;
+            float acc = 0.f;
+            for (int j = 0; j <= i; ++j)
+                acc = fmaf(gsm[(i - i0) * kRows + j] * expf(csh[i] - csh[j]) * dth[j],
+                           __bfloat162float(x[(((size_t)b * L + t0 + j) * H + h) * P + p]), acc);
+            float off = 0.f;
             const __nv_bfloat16 *ci = Cm + (((size_t)b * L + t0 + i) * G + g) * NS;
-            const __nv_bfloat16 *bj = Bm + (((size_t)b * L + t0 + j) * G + g) * NS;
-            for (int n = 0; n < NS; ++n) s = fmaf(__bfloat162float(ci[n]), __bfloat162float(bj[n]), s);
+            for (int n = 0; n < NS; ++n) off = fmaf(__bfloat162float(ci[n]), hcs[col * NS + n], off);
+            const size_t yi = (((size_t)b * L + t0 + i) * H + h) * P + p;
+            const float Dh = pr.D ? pr.D[h] : 0.f;
+            static_cast<__nv_bfloat16 *>(pr.y)[yi] =
+                __float2bfloat16_rn(acc + expf(csh[i]) * off + Dh * __bfloat162float(x[yi]));
         }
-        gsm[e] = s;
     }
-    __syncthreads();
-    const float *hprev = c > 0 ? fa.incl + (unit - 1) * (size_t)kRows * NS : nullptr;
-    for (int o = tid; o < kRows * kRows; o += kThreads) {
-        const int i = o >> 7, col = o & 127;  // col = (head, headdim) within the block
-        if (i >= len) continue;
-        const int hh = col / P, p = col % P, h = h0 + hh;
-        const float *csh = cs + hh * kRows, *dth = dtv + hh * kRows;
-        float acc = 0.f;
-        for (int j = 0; j <= i; ++j)
-            acc = fmaf(gsm[i * kRows + j] * expf(csh[i] - csh[j]) * dth[j],
-                       __bfloat162float(x[(((size_t)b * L + t0 + j) * H + h) * P + p]), acc);
-        float off = 0.f;
-        const __nv_bfloat16 *ci = Cm + (((size_t)b * L + t0 + i) * G + g) * NS;
-        for (int n = 0; n < NS; ++n) {
-            float hv = 0.f;
-            if (hprev) hv = __ldcg(hprev + (size_t)col * NS + n);
-            else if (pr.init_state) hv = pr.init_state[(((size_t)b * H + h) * P + p) * NS + n];
-            off = fmaf(__bfloat162float(ci[n]), hv, off);
-        }
-        const size_t yi = (((size_t)b * L + t0 + i) * H + h) * P + p;
-        const float Dh = pr.D ? pr.D[h] : 0.f;
-        static_cast<__nv_bfloat16 *>(pr.y)[yi] =
-            __float2bfloat16_rn(acc + expf(csh[i]) * off + Dh * __bfloat162float(x[yi]));
-    }
-    __syncthreads();
 }
 
 template <int NS>
@@ -213,14 +200,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                  FusedArgs fa)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_ld, bar_c, bar_g, bar_mma[2];
+    __shared__ __align__(8) uint64_t bar_ld, bar_c, bar_g, bar_full[3], bar_empty[3];
     __shared__ uint32_t tmem_slot, s_ticket;
     __shared__ float warp_tot[8], warp_mn[8], warp_mx[8];
     __shared__ float cs[2 * kRows], dtv[2 * kRows];
     __shared__ float vw[2 * kRows];    // v_j dt_j (0 past the chunk end)
     __shared__ float rs[2 * kRows];    // r_i
     __shared__ float s_alpha[2], s_sfac[2], s_yscale[2];
-    __shared__ int s_fail, s_mode, s_stop, s_last;
+    __shared__ int s_fail, s_mode, s_stop;
 
     constexpr int NSL = NS / 64;        // 64-wide slabs of the state dimension
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -228,7 +215,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int half = warp >> 2;         // which head / half of the columns this warp handles
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
     const int nhb = H / HB, nc = pr.nchunks;
-    const unsigned total_units = gridDim.x;
 
     // TMEM first, ticket second: a CTA never holds a ticket (that others may wait
     // on) while it is itself still waiting for resources
@@ -241,11 +227,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_init(&bar_ld, 1);
         mbar_init(&bar_c, 1);
         mbar_init(&bar_g, 1);
-        mbar_init(&bar_mma[0], 1);
-        mbar_init(&bar_mma[1], 1);
+        for (int k = 0; k < 3; ++k) {
+            mbar_init(&bar_full[k], kThreads / 32);  // one arrival per warp
+            mbar_init(&bar_empty[k], 1);
+        }
         mbar_fence_init();
         s_fail = 0;
-        s_last = 0;
     }
     __syncthreads();
     const uint32_t tmem = tmem_slot;
@@ -264,8 +251,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *xs = base;                              // x: 2 MN blocks x 16 KiB
     uint8_t *bs = xs + 2 * kSlab;                    // B, later C again: NSL slabs
     uint8_t *cm = bs + NSL * kSlab;                  // C, then tril(G) (2 slabs), later y staging
-    uint8_t *rr = cm + 2 * kSlab;                    // wx ping-pong: 2 x (hi 4 KiB | lo 4 KiB)
-    uint8_t *hh_s = NS == 64 ? cm : rr + kSlab;      // h hi | lo (NSL slabs each)
+    uint8_t *rr = cm + 2 * kSlab;                    // wx ring: 3 x (hi 4 KiB | lo 4 KiB)
+    uint8_t *hh_s = NS == 64 ? cm : rr + 3 * 8192;   // h hi | lo (NSL slabs each)
 
     if (tid == 0) {
         tma_prefetch_desc(&xmap);
@@ -377,14 +364,38 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_before();
     __syncthreads();
 
-    // ---- eight 16-token steps: wx (hi, lo) -> S_c += wx^T B ; Y += tril(G)[:, step] wx
+    // ---- eight 16-token steps through a 3-buffer ring: every thread builds its
+    // 16-byte chunk of wx (hi, lo) for step k, each warp then arrives once on
+    // full[k % 3]; after its own chunk thread 0 issues step k-1 (S_c += wx^T B ;
+    // Y += tril(G)[:, step] wx) and commits it to empty[(k-1) % 3], which the
+    // buffer's next writers wait on.
     if (ok) {
         const int mb = tid >> 7, row = (tid >> 3) & 15, qq = tid & 7;
         const float *vh = vw + (P == 64 ? mb : 0) * kRows;
-        for (int k = 0; k < 8; ++k) {
-            const int bb = k & 1;
+        auto issue = [&](int k) {
+            const int bb = k % 3;
+            if (!mbar_wait(&bar_full[bb], (k / 3) & 1)) return false;
+            tc_fence_after();
+            const uint32_t buf = smem_u32(rr) + bb * 8192;
+            constexpr uint32_t id_s = idesc_bf16(128, NS, 1, 1);
+            const uint64_t bd = sdesc_sw128(smem_u32(bs) + k * 2048, kSlab, 1024);
+            mma_bf16(tmem + col_st, sdesc_sw128(buf, 2048, 1024), bd, id_s, k > 0);
+            mma_bf16(tmem + col_st, sdesc_sw128(buf + 4096, 2048, 1024), bd, id_s, 1);
+            if (fast) {
+                constexpr uint32_t id_d = idesc_bf16(128, 128, 0, 1);
+                const uint64_t ad = sdesc_sw128(smem_u32(cm) + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
+                mma_bf16(tmem + col_y, ad, sdesc_sw128(buf, 2048, 1024), id_d, k > 0);
+                mma_bf16(tmem + col_y, ad, sdesc_sw128(buf + 4096, 2048, 1024), id_d, 1);
+            }
+            mma_commit(&bar_empty[bb]);
+            return true;
+        };
+        bool good = true;
+        for (int k = 0; k < 8 && good; ++k) {
+            const int bb = k % 3;
+            if (k >= 3 && !mbar_wait(&bar_empty[bb], ((k - 3) / 3) & 1)) good = false;
+            if (!good) break;
             uint8_t *buf = rr + bb * 8192;
-            if (k >= 2 && !mbar_wait(&bar_mma[bb], ((k - 2) >> 1) & 1)) s_fail = 1;
             const int j = 16 * k + row;
             const float w = vh[j];
             const uint4 xv = *reinterpret_cast<const uint4 *>(xs + mb * kSlab + sw128(j, qq));
@@ -401,24 +412,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             *reinterpret_cast<uint4 *>(buf + mb * 2048 + sw128(row, qq)) = hi;
             *reinterpret_cast<uint4 *>(buf + 4096 + mb * 2048 + sw128(row, qq)) = lo;
             fence_async_smem();
-            __syncthreads();
-            if (s_fail) break;
-            if (tid == 0) {
-                tc_fence_after();
-                constexpr uint32_t id_s = idesc_bf16(128, NS, 1, 1);
-                const uint64_t bd = sdesc_sw128(smem_u32(bs) + k * 2048, kSlab, 1024);
-                mma_bf16(tmem + col_st, sdesc_sw128(smem_u32(buf), 2048, 1024), bd, id_s, k > 0);
-                mma_bf16(tmem + col_st, sdesc_sw128(smem_u32(buf) + 4096, 2048, 1024), bd, id_s, 1);
-                if (fast) {
-                    constexpr uint32_t id_d = idesc_bf16(128, 128, 0, 1);
-                    const uint64_t ad = sdesc_sw128(smem_u32(cm) + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
-                    mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(buf), 2048, 1024), id_d, k > 0);
-                    mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(buf) + 4096, 2048, 1024), id_d, 1);
-                }
-                mma_commit(&bar_mma[bb]);
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_full[bb]);
+            // thread 0 issues the previous step once its own chunk of this step is in
+            if (tid == 0 && k >= 1) good = issue(k - 1);
         }
-        if (!s_fail && (!mbar_wait(&bar_mma[0], 1) || !mbar_wait(&bar_mma[1], 1))) s_fail = 1;
+        if (good && tid == 0) good = issue(7);
+        // the last commit (step 7, buffer 1, its third phase) covers every earlier MMA
+        if (good && !mbar_wait(&bar_empty[1], 0)) good = false;
+        if (!good) s_fail = 1;
     }
     __syncthreads();
     ok = !s_fail;
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float sfac = s_sfac[hh_m];
     if (ok && tid == 0) {
         int mode = 0;  // 0: chunk 0, 1: predecessor inclusive ready, 2: look back
-        if (c > 0) mode = ld_acquire(fa.flags + unit - 1) == kFlagInclusive ? 1 : 2;
+        if (c > 0) mode = ld_acquire(fa.inclcnt + unit - 1) == kThreads ? 1 : 2;
         s_mode = mode;
     }
     __syncthreads();
@@ -454,10 +456,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                                                                              sfac * v[4 * u + 2], sfac * v[4 * u + 3]));
         }
         if (tid < HB) fa.alpha[unit * 2 + tid] = s_alpha[tid];
-        __threadfence();
-        __syncthreads();
+        red_release_add(fa.aggcnt + unit, 1u);
         if (warp == 0) {
-            if (lane == 0) st_release(fa.flags + unit, kFlagAggregate);
             // Walk back, 32 predecessors per poll: stop at the nearest chunk whose
             // inclusive state is published (or before chunk 0: the init state);
             // every chunk in between must have published its aggregate.
@@ -466,7 +466,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             bool timed_out = false;
             for (;;) {
                 const int k = top - lane;
-                const uint32_t f = k >= 0 ? ld_acquire(fa.flags + unit - (c - k)) : kFlagInclusive;
+                uint32_t f = kFlagInclusive;  // before chunk 0: the init state
+                if (k >= 0) {
+                    const size_t uk = unit - (c - k);
+                    f = ld_acquire(fa.inclcnt + uk) == kThreads ? kFlagInclusive
+                        : (ld_acquire(fa.aggcnt + uk) == kThreads ? kFlagAggregate : kFlagNone);
+                }
                 const uint32_t end_mask = __ballot_sync(0xffffffffu, f == kFlagInclusive);
                 const uint32_t none_mask = __ballot_sync(0xffffffffu, f == kFlagNone);
                 const uint32_t before = end_mask ? (end_mask & (0u - end_mask)) - 1u : 0xffffffffu;
@@ -498,7 +503,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         // state (or the init state) and apply h <- a_k h + S_k for each later chunk,
         // so the result does not depend on how far the walk went
         const int stop = mode == 2 ? s_stop : c - 1;   // mode 0: c - 1 = -1, the init state
-        if (mode == 1) (void)ld_acquire(fa.flags + unit - 1);
         const float a_own = s_alpha[hh_m], ysc = s_yscale[hh_m];
         const int hg = h0 + hh_m;
         const float *init = pr.init_state ? pr.init_state + (((size_t)b * H + hg) * P + p_m) * NS + n0 : nullptr;
@@ -508,7 +512,27 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int k = 0; k < 32; ++k) acc[k] = 0.f;
             if (stop >= 0) fma_row32(acc, 1.f, fa.incl + (unit - (c - stop)) * ustride + row_off + cc);
             else if (init) fma_row32(acc, 1.f, init + cc);
-            for (int k = stop + 1; k < c; ++k) {
+            int k = stop + 1;
+            for (; k + 1 < c; k += 2) {  // two aggregates per round trip
+                const size_t u = unit - (c - k);
+                const float a0 = __ldcg(fa.alpha + u * 2 + hh_m), a1 = __ldcg(fa.alpha + (u + 1) * 2 + hh_m);
+                const float4 *s0 = reinterpret_cast<const float4 *>(fa.agg + u * ustride + row_off + cc);
+                const float4 *s1 = reinterpret_cast<const float4 *>(fa.agg + (u + 1) * ustride + row_off + cc);
+                float4 v0[8], v1[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    v0[q] = __ldcg(s0 + q);
+                    v1[q] = __ldcg(s1 + q);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    acc[4 * q] = fmaf(a1, fmaf(a0, acc[4 * q], v0[q].x), v1[q].x);
+                    acc[4 * q + 1] = fmaf(a1, fmaf(a0, acc[4 * q + 1], v0[q].y), v1[q].y);
+                    acc[4 * q + 2] = fmaf(a1, fmaf(a0, acc[4 * q + 2], v0[q].z), v1[q].z);
+                    acc[4 * q + 3] = fmaf(a1, fmaf(a0, acc[4 * q + 3], v0[q].w), v1[q].w);
+                }
+            }
+            if (k < c) {
                 const size_t u = unit - (c - k);
                 const float a = __ldcg(fa.alpha + u * 2 + hh_m);
                 const float4 *src = reinterpret_cast<const float4 *>(fa.agg + u * ustride + row_off + cc);
@@ -520,6 +544,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                     acc[4 * q + 2] = fmaf(a, acc[4 * q + 2], v.z);
                     acc[4 * q + 3] = fmaf(a, acc[4 * q + 3], v.w);
                 }
+            }
+            if (!fast) {  // the direct path reads h_c from shared memory (the unused h hi/lo region)
+                float *hcs = reinterpret_cast<float *>(hh_s) + (size_t)m * NS + n0 + cc;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) hcs[k] = acc[k];
             }
             if (fast) {  // e^ref h_c -> bf16 hi / lo operand slabs (row m)
 #pragma unroll
@@ -550,13 +579,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int q = 0; q < 8; ++q) fo[q] = make_float4(sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3]);
             }
         }
-        __threadfence();
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     if (ok && tid == 0) {
-        st_release(fa.flags + unit, kFlagInclusive);
         if (fast) {
             // Y += C (e^ref h_c)^T
             if (!mbar_wait(&bar_c, 0)) {
@@ -572,10 +599,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 mma_commit(&bar_g);
             }
-        } else {
-            fa.queue[atomicAdd(fa.counters + kCtrFallback, 1u)] = (uint32_t)unit;
         }
     }
+    // publish h_{c+1} (written above) now that the off-diagonal MMA is running:
+    // the release waits for this thread's stores, off the critical path
+    if (ok) red_release_add(fa.inclcnt + unit, 1u);
     __syncthreads();
     ok = ok && !s_fail;
     if (ok && fast && !mbar_wait(&bar_g, 1)) s_fail = 1;
@@ -634,19 +662,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
-
-    // ---- the last CTA to finish computes the queued chunks' outputs
-    if (tid == 0) {
-        __threadfence();
-        s_last = atomicAdd(fa.counters + kCtrDone, 1u) == total_units - 1;
-    }
-    __syncthreads();
-    if (s_last) {
-        __threadfence();
-        const uint32_t nq = *reinterpret_cast<volatile uint32_t *>(fa.counters + kCtrFallback);
-        for (uint32_t q = 0; q < nq; ++q)
-            finish_queued_unit(pr, fa, NS, fa.queue[q], reinterpret_cast<float *>(base), cs, dtv, warp_tot);
-    }
+    if (ok && !fast)  // decay range too wide for the factored form: direct outputs (C_i . B_j over x)
+        direct_unit_outputs(pr, NS, b, hb, c, reinterpret_cast<const float *>(hh_s), reinterpret_cast<float *>(xs),
+                            cs, dtv);
 }
 
 cudaError_t make_map(CUtensorMap *map, const void *ptr, int width, int seqlen, int batch)
@@ -663,10 +681,10 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int width, int seqlen, i
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// x | B (then C) | C (then tril(G), then y) | wx ping-pong | h hi/lo (dstate 128 only)
+// x | B (then C) | C (then tril(G), then y) | wx ring | h hi/lo (dstate 128 only)
 size_t fused_smem(int NS)
 {
-    const size_t body = (size_t)(2 + NS / 64 + 2) * kSlab + kSlab;  // ..., wx ping-pong 16 KiB
+    const size_t body = (size_t)(2 + NS / 64 + 2) * kSlab + 3 * 8192;  // ..., wx ring 24 KiB
     const size_t hreg = NS == 64 ? 0 : (size_t)2 * (NS / 64) * kSlab;
     return 1024 + body + hreg;
 }
@@ -687,7 +705,7 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
         cudaSuccess)
         return e;
     const size_t units = units_of(pr);
-    if ((e = cudaMemsetAsync(fa.flags, 0, (units + kCtrCount) * sizeof(uint32_t), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(fa.aggcnt, 0, (2 * units + kCtrCount) * sizeof(uint32_t), s)) != cudaSuccess) return e;
     ssd_fused_tc<NS><<<(unsigned)units, kThreads, smem, s>>>(xmap, bmap, cmap, ymap, pr, fa);
     return cudaGetLastError();
 }
@@ -711,8 +729,7 @@ size_t fused_workspace_bytes(const Problem &pr)
 {
     const size_t units = units_of(pr);
     const size_t states = units * kRows * pr.dstate * sizeof(float);
-    return 2 * up256(states) + up256(units * 2 * sizeof(float)) + up256((units + kCtrCount) * sizeof(uint32_t)) +
-           up256(units * sizeof(uint32_t));
+    return 2 * up256(states) + up256(units * 2 * sizeof(float)) + up256((2 * units + kCtrCount) * sizeof(uint32_t));
 }
 
 cudaError_t launch_fused_tc(const Problem &pr, void *workspace, cudaStream_t s)
@@ -727,10 +744,9 @@ cudaError_t launch_fused_tc(const Problem &pr, void *workspace, cudaStream_t s)
     p += up256(states);
     fa.alpha = reinterpret_cast<float *>(p);
     p += up256(units * 2 * sizeof(float));
-    fa.flags = reinterpret_cast<uint32_t *>(p);
-    fa.counters = fa.flags + units;
-    p += up256((units + kCtrCount) * sizeof(uint32_t));
-    fa.queue = reinterpret_cast<uint32_t *>(p);
+    fa.aggcnt = reinterpret_cast<uint32_t *>(p);
+    fa.inclcnt = fa.aggcnt + units;
+    fa.counters = fa.inclcnt + units;
     return pr.dstate == 64 ? launch<64>(pr, fa, s) : launch<128>(pr, fa, s);
 }
 
