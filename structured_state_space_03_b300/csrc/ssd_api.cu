@@ -130,12 +130,12 @@ static ssd_path_t choose_path(const Problem &pr)
     return tc_supported(pr) ? SSD_PATH_TCGEN05 : SSD_PATH_SIMT;
 }
 
-static const char *kernel_names(ssd_path_t path)
+static const char *kernel_names(const Problem &pr)
 {
-    switch (path) {
+    switch (choose_path(pr)) {
     case SSD_PATH_SIMT: return "chunk_state_simt,state_pass,chunk_out_simt";
     case SSD_PATH_TCGEN05: return "chunk_state_tc,state_pass,chunk_out_tc";
-    case SSD_PATH_TCGEN05_FUSED: return "ssd_fused_tc";
+    case SSD_PATH_TCGEN05_FUSED: return pr.dstate == 64 ? "ssd_fused_ov_tc" : "ssd_fused_tc";
     default: return "";
     }
 }
@@ -220,7 +220,7 @@ int ssd_fwd_kernels(int batch, int seqlen, int nheads, int headdim, int ngroups,
     Problem pr;
     memset(&pr, 0, sizeof pr);
     if (check_dims(pr, batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype) != SSD_OK) return -1;
-    const char *list = kernel_names(choose_path(pr));
+    const char *list = kernel_names(pr);
     if (names && names_len) snprintf(names, names_len, "%s", list);
     int count = list[0] ? 1 : 0;
     for (const char *c = list; *c; ++c) count += *c == ',';
