@@ -50,6 +50,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "ssd_internal.cuh"
 #include "ssd_ptx.cuh"
 
@@ -79,6 +81,12 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// Publication flag (after a fence by the same thread).
+__device__ __forceinline__ void st_relaxed_flag(uint32_t *p)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(1u) : "memory");
 }
 
 // Fire-and-forget increment that orders this thread's earlier writes before it.
@@ -150,10 +158,17 @@ struct FusedArgs {
 // chunk whose decay range is too wide for the factored form.  `hcs` holds h_c
 // ([128][NS] fp32, rows (head, headdim)); `gsm` (32 KiB) receives C_i . B_j for
 // 64 output rows at a time.  Slow, and used only for such chunks.
-__device__ void direct_unit_outputs(const Problem &pr, int NS, int b, int hb, int c, const float *hcs, float *gsm,
-                                    const float *cs, const float *dtv)
+// Named barrier `id` over `n` threads (id 0 with the whole CTA is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int n)
 {
-    const int tid = threadIdx.x;
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Evaluation is shared by the `gn` threads numbered `gt` of barrier `bar_id`.
+__device__ void direct_unit_outputs(const Problem &pr, int NS, int b, int hb, int c, const float *hcs, float *gsm,
+                                    const float *cs, const float *dtv, int gt, int gn, int bar_id)
+{
+    const int tid = gt;
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
     const int h0 = hb * HB, G = pr.ngroups, g = h0 / (H / G);
     const int t0 = c * pr.chunk, len = min(pr.chunk, L - t0);
@@ -161,8 +176,8 @@ __device__ void direct_unit_outputs(const Problem &pr, int NS, int b, int hb, in
     const __nv_bfloat16 *Bm = static_cast<const __nv_bfloat16 *>(pr.B);
     const __nv_bfloat16 *Cm = static_cast<const __nv_bfloat16 *>(pr.C);
     for (int i0 = 0; i0 < kRows; i0 += 64) {
-        __syncthreads();
-        for (int e = tid; e < 64 * kRows; e += kThreads) {  // causal part of C_i . B_j, rows i0 .. i0+63
+        named_sync(bar_id, gn);
+        for (int e = tid; e < 64 * kRows; e += gn) {  // causal part of C_i . B_j, rows i0 .. i0+63
             const int i = i0 + (e >> 7), j = e & 127;
             float s = 0.f;
             if (i < len && j <= i) {
@@ -172,8 +187,8 @@ __device__ void direct_unit_outputs(const Problem &pr, int NS, int b, int hb, in
             }
             gsm[e] = s;
         }
-        __syncthreads();
-        for (int o = tid; o < 64 * kRows; o += kThreads) {
+        named_sync(bar_id, gn);
+        for (int o = tid; o < 64 * kRows; o += gn) {
             const int i = i0 + (o >> 7), col = o & 127;  // col = (head, headdim) within the block
             if (i >= len) continue;
             const int hh = col / P, p = col % P, h = h0 + hh;
@@ -664,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 0) tmem_dealloc(tmem, 256);
     if (ok && !fast)  // decay range too wide for the factored form: direct outputs (C_i . B_j over x)
         direct_unit_outputs(pr, NS, b, hb, c, reinterpret_cast<const float *>(hh_s), reinterpret_cast<float *>(xs),
-                            cs, dtv);
+                            cs, dtv, tid, kThreads, 0);
 }
 
 // Named barrier over one half of the CTA (warps 0-3: id 1, warps 4-7: id 2).
@@ -1138,7 +1153,594 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 0) tmem_dealloc(tmem, 256);
     if (ok && !fast)
         direct_unit_outputs(pr, NS, b, hb, c, reinterpret_cast<const float *>(hh_s),
-                            reinterpret_cast<float *>(base + 2 * kSlab), cs, dtv);
+                            reinterpret_cast<float *>(base + 2 * kSlab), cs, dtv, tid, kThreads, 0);
+}
+
+// ---------------------------------------------------------------------------
+// dstate 64, persistent.  One CTA per SM takes units (chunk-major tickets, as
+// above) one after another and keeps two of them in flight: two shared-memory
+// stages of 96 KiB and two 256-column TMEM slots.  Warp roles:
+//   warp 0      tickets and TMA loads (x, B, C) into a free stage;
+//   warp 1      G = C B^T, then the chunk-state and diagonal-block MMAs;
+//   warps 2-5   segment sums and factors, wx (hi, lo), tril(G) into TMEM;
+//   warps 6-9   look-back for h_c (publishing the aggregate S_c if the walk is
+//               still waiting when S_c is ready), inclusive state, h operand,
+//               and the off-diagonal MMA Y += C (e^ref h_c)^T;
+//   warps 10-13 y = r Y + D x, staged and stored by TMA, then free the stage.
+// Each role walks the units of the CTA in ticket order, so the forward-progress
+// argument of the one-unit kernels holds: the smallest unfinished ticket only
+// waits on finished units.  Stage s, 96 KiB: [0, 32K) x -> wx hi -> h hi | lo;
+// [32K, 64K) wx lo -> y staging; [64K, 80K) B; [80K, 96K) C.  TMEM slot s at
+// column 256 s: Y [0,128), S_c [128,192), tril(G) [192,256).
+// ---------------------------------------------------------------------------
+constexpr int kPipeThreads = 14 * 32;
+constexpr int kStageBytes = 6 * kSlab;
+enum { kWarpLoad = 0, kWarpMma = 1, kWarpFront = 2, kWarpState = 6, kWarpEpi = 10 };
+enum { kBarFront = 1, kBarState = 2, kBarEpi = 3 };
+
+// Named barrier over `n` threads that also returns whether any of them passed `pred`.
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+struct PipeUnit {
+    int b, hb, c, h0, g, t0, len;
+    size_t unit;
+};
+
+__device__ __forceinline__ PipeUnit decode_unit(const Problem &pr, int ticket, int nhb)
+{
+    PipeUnit u;
+    u.c = ticket / (pr.batch * nhb);
+    const int rest = ticket - u.c * (pr.batch * nhb);
+    u.b = rest / nhb;
+    u.hb = rest - u.b * nhb;
+    const int HB = 128 / pr.headdim;
+    u.h0 = u.hb * HB;
+    u.g = u.h0 / (pr.nheads / pr.ngroups);
+    u.t0 = u.c * pr.chunk;
+    u.len = min(pr.chunk, pr.seqlen - u.t0);
+    u.unit = ((size_t)u.b * nhb + u.hb) * pr.nchunks + u.c;
+    return u;
+}
+
+__global__ void __launch_bounds__(kPipeThreads, 1)
+    ssd_fused_pipe_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
+                      const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap, Problem pr,
+                      FusedArgs fa, int units)
+{
+    constexpr int NS = 64;
+    extern __shared__ uint8_t smem_raw[];
+    // per stage (it & 1): full, free, slot, g, fr, mma, yo; per unit in flight (it & 3): info,
+    // seg and the unit's scalars, which the epilogue may still read after the stage is free
+    __shared__ __align__(8) uint64_t bar_info[4], bar_seg[4], bar_full[2], bar_free[2], bar_slot[2], bar_lo[2],
+        bar_g[2], bar_fr[2], bar_mma[2], bar_yo[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int s_tk[4], s_fast[4];
+    __shared__ float cs[4][2 * kRows], dtv[4][2 * kRows], vw[4][2 * kRows], rs[4][2 * kRows];
+    __shared__ float s_alpha[4][2], s_sfac[4][2], s_ysc[4][2];
+    __shared__ float wtot[4][2], wmn[4][2], wmx[4][2];
+    __shared__ int s_walk[2];
+    __shared__ int s_fail;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;  // TMEM lane of this thread (warps 2-13)
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
+    const int nhb = H / HB, nc = pr.nchunks;
+    const uint32_t col_y = 0, col_st = 128, col_m = 192;
+
+    if (warp == kWarpMma) tmem_alloc(&tmem_slot, 512);
+    if (tid == 0) {
+        for (int k = 0; k < 4; ++k) {
+            mbar_init(&bar_info[k], 1);
+            mbar_init(&bar_seg[k], 128);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&bar_full[k], 1);
+            mbar_init(&bar_free[k], 1);
+            mbar_init(&bar_slot[k], 1);
+            mbar_init(&bar_lo[k], 1);
+            mbar_init(&bar_g[k], 1);
+            mbar_init(&bar_fr[k], 128);
+            mbar_init(&bar_mma[k], 1);
+            mbar_init(&bar_yo[k], 1);
+        }
+        mbar_fence_init();
+        s_fail = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    uint8_t *base = align1024(smem_raw);
+
+    if (warp == kWarpLoad) {
+        // ================= tickets and loads
+        if (lane == 0) {
+            tma_prefetch_desc(&xmap);
+            tma_prefetch_desc(&bmap);
+            tma_prefetch_desc(&cmap);
+            tma_prefetch_desc(&ymap);
+            for (int it = 0;; ++it) {
+                const int s = it & 1, ss = it & 3;
+                const uint32_t ph = (it >> 1) & 1;
+                bool ok = it < 2 || mbar_wait(&bar_free[s], ph ^ 1);
+                const uint32_t t = ok ? atomicAdd(fa.counters + kCtrTicket, 1u) : 0xffffffffu;
+                const int tk = t < (uint32_t)units ? (int)t : -1;
+                if (!ok) s_fail = 1;
+                s_tk[ss] = tk;
+                mbar_arrive(&bar_info[ss]);
+                if (tk < 0) break;
+                const PipeUnit u = decode_unit(pr, tk, nhb);
+                uint8_t *st = base + s * kStageBytes;
+                mbar_expect_tx(&bar_full[s], (uint32_t)(4 * kSlab));
+                for (int k = 0; k < 2; ++k) tma_load_3d(st + k * kSlab, &xmap, &bar_full[s], u.hb * 128 + 64 * k, u.t0, u.b);
+                tma_load_3d(st + 4 * kSlab, &bmap, &bar_full[s], u.g * NS, u.t0, u.b);
+                tma_load_3d(st + 5 * kSlab, &cmap, &bar_full[s], u.g * NS, u.t0, u.b);
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // ================= G, chunk-state and diagonal-block MMAs
+        if (lane == 0) {
+            constexpr uint32_t id_g = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t id_s = idesc_bf16(128, NS, 1, 1);
+            constexpr uint32_t id_d = idesc_bf16(128, 128, 0, 1);
+            for (int it = 0;; ++it) {
+                const int s = it & 1, ss = it & 3;
+                const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
+                if (!mbar_wait(&bar_info[ss], pq)) {
+                    s_fail = 1;
+                    break;
+                }
+                if (s_tk[ss] < 0) break;
+                const uint32_t slot = tmem + s * 256;
+                const uint32_t st = smem_u32(base + s * kStageBytes);
+                if (it >= 2 && !mbar_wait(&bar_slot[s], ph ^ 1)) {
+                    s_fail = 1;
+                    break;
+                }
+                if (!mbar_wait(&bar_full[s], ph)) {
+                    s_fail = 1;
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < NS / 16; ++ks)
+                    mma_bf16(slot + col_y, sdesc_sw128(st + 5 * kSlab + ks * 32, 16, 1024),
+                             sdesc_sw128(st + 4 * kSlab + ks * 32, 16, 1024), id_g, ks > 0);
+                mma_commit(&bar_g[s]);
+                if (!mbar_wait(&bar_fr[s], ph)) {
+                    s_fail = 1;
+                    break;
+                }
+                tc_fence_after();
+                const bool fast = s_fast[ss] != 0;
+                for (int ks = 0; ks < kRows / 16; ++ks) {
+                    const uint64_t bd = sdesc_sw128(st + 4 * kSlab + ks * 2048, kSlab, 1024);
+                    const uint64_t whi = sdesc_sw128(st + ks * 2048, kSlab, 1024);
+                    const uint64_t wlo = sdesc_sw128(st + 2 * kSlab + ks * 2048, kSlab, 1024);
+                    mma_bf16(slot + col_st, whi, bd, id_s, ks > 0);
+                    mma_bf16(slot + col_st, wlo, bd, id_s, 1);
+                    if (fast) {
+                        mma_bf16_tA(slot + col_y, slot + col_m + ks * 8, whi, id_d, ks > 0);
+                        mma_bf16_tA(slot + col_y, slot + col_m + ks * 8, wlo, id_d, 1);
+                    }
+                }
+                mma_commit(&bar_mma[s]);
+            }
+        }
+    } else if (warp < kWarpState) {
+        // ================= segment sums, wx, tril(G)
+        const int ft = tid - 32 * kWarpFront, fw = warp - kWarpFront;  // token ft, in warp order
+        for (int it = 0;; ++it) {
+            const int s = it & 1, ss = it & 3;
+            const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
+            bool ok = mbar_wait(&bar_info[ss], pq);
+            const int tk = s_tk[ss];
+            if (named_sync_or(kBarFront, 128, !ok || tk < 0)) break;
+            const PipeUnit u = decode_unit(pr, tk, nhb);
+            uint8_t *st = base + s * kStageBytes;
+            float v[2], d[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const bool act = hh < HB;
+                const float a = act ? __ldg(pr.A + u.h0 + hh) : 0.f;
+                d[hh] = (act && ft < u.len) ? __ldg(pr.dt + ((size_t)u.b * L + u.t0 + ft) * H + u.h0 + hh) : 0.f;
+                v[hh] = d[hh] * a;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float t = __shfl_up_sync(0xffffffffu, v[hh], o);
+                    if (lane >= o) v[hh] += t;
+                }
+                if (lane == 31) wtot[fw][hh] = v[hh];
+            }
+            named_sync(kBarFront, 128);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                for (int w = 0; w < fw; ++w) v[hh] += wtot[w][hh];
+                float mn = ft < u.len ? v[hh] : 3.0e38f, mx = ft < u.len ? v[hh] : -3.0e38f;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                }
+                if (lane == 0) {
+                    wmn[fw][hh] = mn;
+                    wmx[fw][hh] = mx;
+                }
+                cs[ss][hh * kRows + ft] = v[hh];
+                dtv[ss][hh * kRows + ft] = d[hh];
+            }
+            named_sync(kBarFront, 128);
+            float lo_[2], hi_[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                lo_[hh] = fminf(fminf(wmn[0][hh], wmn[1][hh]), fminf(wmn[2][hh], wmn[3][hh]));
+                hi_[hh] = fmaxf(fmaxf(wmx[0][hh], wmx[1][hh]), fmaxf(wmx[2][hh], wmx[3][hh]));
+            }
+            const bool fast = (hi_[0] - lo_[0] <= kSpanMax) && (HB == 1 || hi_[1] - lo_[1] <= kSpanMax);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                if (hh >= HB) break;
+                const float cl = cs[ss][hh * kRows + u.len - 1];
+                const float ref = 0.5f * (lo_[hh] + hi_[hh]);
+                const float refw = fast ? ref : cl, refy = fast ? ref : 0.f;
+                vw[ss][hh * kRows + ft] = ft < u.len ? expf(refw - v[hh]) * d[hh] : 0.f;
+                rs[ss][hh * kRows + ft] = expf(v[hh] - refy);
+                if (ft == 0) {
+                    s_alpha[ss][hh] = expf(cl);
+                    s_sfac[ss][hh] = expf(cl - refw);
+                    s_ysc[ss][hh] = expf(refy);
+                }
+            }
+            if (ft == 0) s_fast[ss] = fast ? 1 : 0;
+            mbar_arrive(&bar_seg[ss]);
+            named_sync(kBarFront, 128);  // every v_j dt_j is in shared memory
+            // wx = v dt x, hi in place over x, lo at +32K
+            ok = mbar_wait(&bar_full[s], ph) && (it < 2 || mbar_wait(&bar_lo[s], ph ^ 1));
+            if (ok) {
+#pragma unroll 4
+                for (int q = ft; q < 2 * kRows * 8; q += 128) {
+                    const int mb = q >> 10, j = (q >> 3) & 127, qq = q & 7;
+                    const float w = vw[ss][(P == 64 ? mb : 0) * kRows + j];
+                    uint4 *ptr = reinterpret_cast<uint4 *>(st + mb * kSlab + sw128(j, qq));
+                    const uint4 xv = *ptr;
+                    const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                    float f[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 t = __bfloat1622float2(x2[k]);
+                        f[2 * k] = t.x * w;
+                        f[2 * k + 1] = t.y * w;
+                    }
+                    uint4 hi, lo;
+                    split8(f, hi, lo);
+                    *ptr = hi;
+                    *reinterpret_cast<uint4 *>(st + 2 * kSlab + mb * kSlab + sw128(j, qq)) = lo;
+                }
+            }
+            fence_async_smem();
+            ok = ok && mbar_wait(&bar_g[s], ph);
+            tc_fence_after();
+            if (ok && fast) {  // tril(G) -> bf16 pairs in TMEM (row m, columns jb*32 .. jb*32+31)
+                const uint32_t slot = tmem + s * 256 + lane_base;
+                for (int jb = 0; jb < 4; ++jb) {
+                    uint32_t pk[16];
+                    if (jb > quarter) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) pk[k] = 0u;
+                    } else {
+                        float gv[32];
+                        tmem_ld32(slot + col_y + jb * 32, gv);
+                        if (jb == quarter) {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                if (jb * 32 + k > m) gv[k] = 0.f;
+                        }
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            __nv_bfloat162 t2 = __floats2bfloat162_rn(gv[2 * k], gv[2 * k + 1]);
+                            pk[k] = *reinterpret_cast<uint32_t *>(&t2);
+                        }
+                    }
+                    tmem_st16(slot + col_m + jb * 16, pk);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bar_fr[s]);
+            if (named_sync_or(kBarFront, 128, !ok)) {
+                s_fail = 1;
+                break;
+            }
+        }
+    } else if (warp < kWarpEpi) {
+        // ================= look-back, h operand, off-diagonal MMA, inclusive state
+        const int stt = tid - 32 * kWarpState;
+        const int hh_m = m / P, p_m = m % P;
+        const size_t ustride = (size_t)kRows * NS;
+        for (int it = 0;; ++it) {
+            const int s = it & 1, ss = it & 3;
+            const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
+            bool ok = mbar_wait(&bar_info[ss], pq);
+            const int tk = s_tk[ss];
+            if (named_sync_or(kBarState, 128, !ok || tk < 0)) break;
+            const PipeUnit u = decode_unit(pr, tk, nhb);
+            const int c = u.c;
+            const uint32_t slot = tmem + s * 256 + lane_base;
+            // walk back to the nearest inclusive state; -2: S_c became ready first
+            // (publish it as the aggregate, then walk on); -3: gave up
+            int stop = c - 1;
+            if (c > 0) {
+                for (int round = 0; round < 2; ++round) {
+                    if (warp == kWarpState) {
+                        int res = -3, top = c - 1;
+                        const uint64_t tstart = globaltimer();
+                        for (;;) {
+                            const int k = top - lane;
+                            uint32_t f = kFlagInclusive;
+                            if (k >= 0) {
+                                const size_t uk = u.unit - (c - k);
+                                f = ld_acquire(fa.inclcnt + uk) != 0u ? kFlagInclusive
+                                    : (ld_acquire(fa.aggcnt + uk) != 0u ? kFlagAggregate : kFlagNone);
+                            }
+                            const uint32_t end_mask = __ballot_sync(0xffffffffu, f == kFlagInclusive);
+                            const uint32_t none_mask = __ballot_sync(0xffffffffu, f == kFlagNone);
+                            const uint32_t before = end_mask ? (end_mask & (0u - end_mask)) - 1u : 0xffffffffu;
+                            if ((none_mask & (end_mask ? before : 0xffffffffu)) == 0u) {
+                                if (end_mask) {
+                                    res = top - (__ffs(end_mask) - 1);
+                                    break;
+                                }
+                                top -= 32;
+                                continue;
+                            }
+                            if (round == 0 && mbar_test_wait(&bar_mma[s], ph)) {
+                                res = -2;
+                                break;
+                            }
+                            if (globaltimer() - tstart > kWaitLimitNs) break;
+                            __nanosleep(200);
+                        }
+                        if (lane == 0) s_walk[round] = res;
+                    }
+                    named_sync(kBarState, 128);
+                    const int res = s_walk[round];
+                    if (res >= -1) {
+                        stop = res;
+                        break;
+                    }
+                    if (res == -3) {
+                        ok = false;
+                        break;
+                    }
+                    // publish S_c (scaled to the chunk end) as this unit's aggregate
+                    ok = mbar_wait(&bar_mma[s], ph) && mbar_wait(&bar_seg[ss], pq);
+                    tc_fence_after();
+                    if (ok) {
+                        const float sfac = s_sfac[ss][hh_m];
+                        float4 *dst = reinterpret_cast<float4 *>(fa.agg + u.unit * ustride) + m;
+                        for (int cc = 0; cc < NS; cc += 32) {
+                            float sv[32];
+                            tmem_ld32(slot + col_st + cc, sv);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                __stcg(dst + (cc / 4 + q) * kRows,
+                                       make_float4(sfac * sv[4 * q], sfac * sv[4 * q + 1], sfac * sv[4 * q + 2],
+                                                   sfac * sv[4 * q + 3]));
+                        }
+                        if (stt < HB) fa.alpha[u.unit * 2 + stt] = s_alpha[ss][stt];
+                    }
+                    // one release for the whole unit: the barrier orders every
+                    // thread's stores before the leader's fence and flag
+                    if (!named_sync_or(kBarState, 128, !ok) && stt == 0) {
+                        __threadfence();
+                        st_relaxed_flag(fa.aggcnt + u.unit);
+                    }
+                }
+            }
+            // h_c for row m, in the recurrence's own order
+            float acc[NS];
+#pragma unroll
+            for (int k = 0; k < NS; ++k) acc[k] = 0.f;
+            const int hg = u.h0 + hh_m;
+            if (ok) {
+                const float *init = pr.init_state ? pr.init_state + (((size_t)u.b * H + hg) * P + p_m) * NS : nullptr;
+                // published states: [NS/4][128 rows][4] per unit, so a warp moves 512 contiguous bytes
+                const float4 *src0 = stop >= 0 ? reinterpret_cast<const float4 *>(fa.incl + (u.unit - (c - stop)) * ustride) + m
+                                               : reinterpret_cast<const float4 *>(init);
+                const int sq = stop >= 0 ? kRows : 1;
+                if (src0) {
+#pragma unroll
+                    for (int q = 0; q < NS / 4; ++q) {
+                        const float4 vv = __ldcg(src0 + q * sq);
+                        acc[4 * q] = vv.x;
+                        acc[4 * q + 1] = vv.y;
+                        acc[4 * q + 2] = vv.z;
+                        acc[4 * q + 3] = vv.w;
+                    }
+                }
+                for (int k = stop + 1; k < c; ++k) {
+                    const size_t uk = u.unit - (c - k);
+                    const float a = __ldcg(fa.alpha + uk * 2 + hh_m);
+                    const float4 *src = reinterpret_cast<const float4 *>(fa.agg + uk * ustride) + m;
+#pragma unroll
+                    for (int q = 0; q < NS / 4; ++q) {
+                        const float4 vv = __ldcg(src + q * kRows);
+                        acc[4 * q] = fmaf(a, acc[4 * q], vv.x);
+                        acc[4 * q + 1] = fmaf(a, acc[4 * q + 1], vv.y);
+                        acc[4 * q + 2] = fmaf(a, acc[4 * q + 2], vv.z);
+                        acc[4 * q + 3] = fmaf(a, acc[4 * q + 3], vv.w);
+                    }
+                }
+            }
+            ok = ok && mbar_wait(&bar_mma[s], ph) && mbar_wait(&bar_seg[ss], pq);
+            tc_fence_after();
+            const bool fast = s_fast[ss] != 0;
+            uint8_t *hh_s = base + s * kStageBytes;  // wx hi is dead once the MMAs are done
+            if (ok) {
+                if (fast) {  // e^ref h_c -> bf16 hi / lo K-major slabs
+                    const float ysc = s_ysc[ss][hh_m];
+#pragma unroll
+                    for (int q = 0; q < NS / 8; ++q) {
+                        float f[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) f[k] = ysc * acc[8 * q + k];
+                        uint4 hi, lo;
+                        split8(f, hi, lo);
+                        *reinterpret_cast<uint4 *>(hh_s + sw128(m, q)) = hi;
+                        *reinterpret_cast<uint4 *>(hh_s + kSlab + sw128(m, q)) = lo;
+                    }
+                } else {  // the direct path reads h_c in fp32
+                    float *hcs = reinterpret_cast<float *>(hh_s) + (size_t)m * NS;
+#pragma unroll
+                    for (int k = 0; k < NS; ++k) hcs[k] = acc[k];
+                }
+                // h_{c+1} = a_c h_c + S_c (S_c referenced to the chunk end), in place
+                const float sfac = s_sfac[ss][hh_m], a_own = s_alpha[ss][hh_m];
+#pragma unroll
+                for (int cc = 0; cc < NS; cc += 32) {
+                    float sc[32];
+                    tmem_ld32(slot + col_st + cc, sc);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) acc[cc + k] = fmaf(a_own, acc[cc + k], sfac * sc[k]);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            const bool any_fail = named_sync_or(kBarState, 128, !ok);
+            if (stt == 0) {
+                if (!any_fail && fast) {  // Y += C (e^ref h_c)^T; the stage is free once it completes
+                    tc_fence_after();
+                    constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 0);
+                    const uint32_t sa = smem_u32(base + s * kStageBytes);
+                    for (int ks = 0; ks < NS / 16; ++ks) {
+                        const uint64_t ad = sdesc_sw128(sa + 5 * kSlab + ks * 32, 16, 1024);
+                        mma_bf16(tmem + s * 256 + col_y, ad, sdesc_sw128(sa + ks * 32, 16, 1024), id_o, 1);
+                        mma_bf16(tmem + s * 256 + col_y, ad, sdesc_sw128(sa + kSlab + ks * 32, 16, 1024), id_o, 1);
+                    }
+                    mma_commit(&bar_yo[s]);
+                    mma_commit(&bar_free[s]);
+                } else {
+                    mbar_arrive(&bar_yo[s]);  // the direct path frees the stage itself
+                }
+            }
+            if (any_fail) {
+                s_fail = 1;
+                break;
+            }
+            // publish h_{c+1}
+            float4 *dst = reinterpret_cast<float4 *>(fa.incl + u.unit * ustride) + m;
+            float *fo = (c == nc - 1 && pr.final_state) ? pr.final_state + (((size_t)u.b * H + hg) * P + p_m) * NS
+                                                        : nullptr;
+#pragma unroll
+            for (int q = 0; q < NS / 4; ++q) {
+                const float4 vv = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                __stcg(dst + q * kRows, vv);
+                if (fo) reinterpret_cast<float4 *>(fo)[q] = vv;
+            }
+            named_sync(kBarState, 128);
+            if (stt == 0) {
+                __threadfence();
+                st_relaxed_flag(fa.inclcnt + u.unit);
+            }
+        }
+    } else {
+        // ================= y = r Y + D x, staged over the dead wx lo and stored by TMA
+        const int et = tid - 32 * kWarpEpi;
+        const bool tma_out = pr.chunk == kRows;
+        for (int it = 0;; ++it) {
+            const int s = it & 1, ss = it & 3;
+            const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
+            bool ok = mbar_wait(&bar_info[ss], pq);
+            const int tk = s_tk[ss];
+            if (named_sync_or(kBarEpi, 128, !ok || tk < 0)) break;
+            const PipeUnit u = decode_unit(pr, tk, nhb);
+            uint8_t *st = base + s * kStageBytes;
+            uint8_t *ystage = st + 2 * kSlab;
+            const bool row_in = m < u.len;
+            // x of this thread's output row (re-read through L2), fetched before the wait
+            uint4 xpre[16];
+            {
+                const uint4 *xrow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(pr.x) +
+                                                                    (((size_t)u.b * L + u.t0 + m) * H + u.h0) * P);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) xpre[k] = row_in ? __ldg(xrow + k) : make_uint4(0, 0, 0, 0);
+            }
+            ok = mbar_wait(&bar_seg[ss], pq) && mbar_wait(&bar_yo[s], ph);
+            tc_fence_after();
+            const bool fast = s_fast[ss] != 0;
+            if (ok && fast) {
+                const uint32_t slot = tmem + s * 256 + lane_base;
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
+                                                       (((size_t)u.b * L + u.t0 + m) * H + u.h0) * P);
+#pragma unroll
+                for (int col = 0; col < 128; col += 32) {
+                    const int hh = col / P, h = u.h0 + hh;
+                    const float r = rs[ss][hh * kRows + m];
+                    const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
+                    float yv[32];
+                    tmem_ld32(slot + col_y + col, yv);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xpre[col / 8 + k]);
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 xf = __bfloat1622float2(x2[e]);
+                            o[2 * e] = fmaf(Dh, xf.x, r * yv[8 * k + 2 * e]);
+                            o[2 * e + 1] = fmaf(Dh, xf.y, r * yv[8 * k + 2 * e + 1]);
+                        }
+                        const uint4 ov = pack8(o);
+                        if (tma_out)
+                            *reinterpret_cast<uint4 *>(ystage + (col / 64) * kSlab + sw128(m, (col % 64) / 8 + k)) = ov;
+                        else if (row_in)
+                            dst[col / 8 + k] = ov;
+                    }
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            const bool all_ok = !named_sync_or(kBarEpi, 128, !ok);
+            if (et == 0) {
+                mbar_arrive(&bar_slot[s]);  // Y has been read
+                if (all_ok && fast && tma_out) {
+                    for (int k = 0; k < 2; ++k)
+                        tma_store_3d(&ymap, ystage + k * kSlab, u.hb * 128 + 64 * k, u.t0, u.b);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
+                if (!(all_ok && !fast)) mbar_arrive(&bar_lo[s]);  // the staging region is free again
+            }
+            if (all_ok && !fast) {
+                direct_unit_outputs(pr, NS, u.b, u.hb, u.c, reinterpret_cast<const float *>(st),
+                                    reinterpret_cast<float *>(st + 2 * kSlab), cs[ss], dtv[ss], et, 128, kBarEpi);
+                named_sync(kBarEpi, 128);  // every thread is done with the stage
+                if (et == 0) {
+                    mbar_arrive(&bar_lo[s]);
+                    mbar_arrive(&bar_free[s]);
+                }
+            }
+            if (!all_ok) {
+                s_fail = 1;
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    if (s_fail && tid == 0) atomicOr(pr.err_word, kDevErrTimeout);
+    tc_fence_after();
+    if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
 cudaError_t make_map(CUtensorMap *map, const void *ptr, int width, int seqlen, int batch)
@@ -1179,10 +1781,15 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
     const size_t units = units_of(pr);
     if ((e = cudaMemsetAsync(fa.aggcnt, 0, (2 * units + kCtrCount) * sizeof(uint32_t), s)) != cudaSuccess) return e;
     if (NS == 64) {
-        if ((e = cudaFuncSetAttribute(ssd_fused_ov_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        const size_t psmem = 1024 + (size_t)2 * kStageBytes;
+        if ((e = cudaFuncSetAttribute(ssd_fused_pipe_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem)) !=
             cudaSuccess)
             return e;
-        ssd_fused_ov_tc<<<(unsigned)units, kThreads, smem, s>>>(xmap, bmap, cmap, ymap, pr, fa);
+        int dev = 0, nsm = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        const unsigned grid = (unsigned)std::min<size_t>(units, (size_t)nsm);
+        ssd_fused_pipe_tc<<<grid, kPipeThreads, psmem, s>>>(xmap, bmap, cmap, ymap, pr, fa, (int)units);
     } else {
         if ((e = cudaFuncSetAttribute(ssd_fused_tc<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
             cudaSuccess)
