@@ -51,6 +51,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "ssd_internal.cuh"
 #include "ssd_ptx.cuh"
@@ -83,10 +84,11 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
     return v;
 }
 
-// Publication flag (after a fence by the same thread).
-__device__ __forceinline__ void st_relaxed_flag(uint32_t *p)
+// Publication flag: a release store by one thread after a barrier, which
+// orders every participating thread's earlier writes before the flag.
+__device__ __forceinline__ void st_release_flag(uint32_t *p)
 {
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(1u) : "memory");
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(1u) : "memory");
 }
 
 // Fire-and-forget increment that orders this thread's earlier writes before it.
@@ -1175,8 +1177,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 // ---------------------------------------------------------------------------
 constexpr int kPipeThreads = 14 * 32;
 constexpr int kStageBytes = 6 * kSlab;
-enum { kWarpLoad = 0, kWarpMma = 1, kWarpFront = 2, kWarpState = 6, kWarpEpi = 10 };
-enum { kBarFront = 1, kBarState = 2, kBarEpi = 3 };
+constexpr int kDtBytes = kRows * 4 * sizeof(float);  // dt box: 128 tokens x 4 heads
+enum { kWarpLoad = 0, kWarpMma = 1, kWarpFront = 2, kWarpState = 6 };
+enum { kBarFront = 1, kBarTeam0 = 2 };  // team 1 uses barrier 3
 
 // Named barrier over `n` threads that also returns whether any of them passed `pred`.
 __device__ __forceinline__ bool named_sync_or(int id, int n, bool pred)
@@ -1216,21 +1219,21 @@ __device__ __forceinline__ PipeUnit decode_unit(const Problem &pr, int ticket, i
 
 __global__ void __launch_bounds__(kPipeThreads, 1)
     ssd_fused_pipe_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
-                      const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap, Problem pr,
-                      FusedArgs fa, int units)
+                      const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap,
+                      const __grid_constant__ CUtensorMap dtmap, Problem pr, FusedArgs fa, int units, int dt_tma)
 {
     constexpr int NS = 64;
     extern __shared__ uint8_t smem_raw[];
     // per stage (it & 1): full, free, slot, g, fr, mma, yo; per unit in flight (it & 3): info,
     // seg and the unit's scalars, which the epilogue may still read after the stage is free
-    __shared__ __align__(8) uint64_t bar_info[4], bar_seg[4], bar_full[2], bar_free[2], bar_slot[2], bar_lo[2],
-        bar_g[2], bar_fr[2], bar_mma[2], bar_yo[2];
+    __shared__ __align__(8) uint64_t bar_info[4], bar_seg[4], bar_full[2], bar_dt[2], bar_free[2], bar_slot[2],
+        bar_lo[2], bar_g[2], bar_fr[2], bar_mma[2], bar_yo[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int s_tk[4], s_fast[4];
     __shared__ float cs[4][2 * kRows], dtv[4][2 * kRows], vw[4][2 * kRows], rs[4][2 * kRows];
     __shared__ float s_alpha[4][2], s_sfac[4][2], s_ysc[4][2];
     __shared__ float wtot[4][2], wmn[4][2], wmx[4][2];
-    __shared__ int s_walk[2];
+    __shared__ int s_walk[2][2];
     __shared__ int s_fail;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1249,6 +1252,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(&bar_full[k], 1);
+            mbar_init(&bar_dt[k], 1);
             mbar_init(&bar_free[k], 1);
             mbar_init(&bar_slot[k], 1);
             mbar_init(&bar_lo[k], 1);
@@ -1273,6 +1277,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             tma_prefetch_desc(&bmap);
             tma_prefetch_desc(&cmap);
             tma_prefetch_desc(&ymap);
+            int ends = 0;
+            if (dt_tma) tma_prefetch_desc(&dtmap);
             for (int it = 0;; ++it) {
                 const int s = it & 1, ss = it & 3;
                 const uint32_t ph = (it >> 1) & 1;
@@ -1282,9 +1288,19 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 if (!ok) s_fail = 1;
                 s_tk[ss] = tk;
                 mbar_arrive(&bar_info[ss]);
-                if (tk < 0) break;
+                if (tk < 0) {
+                    // the two teams take alternate units: each needs its own end marker
+                    if (++ends == 2 || !ok) break;
+                    continue;
+                }
                 const PipeUnit u = decode_unit(pr, tk, nhb);
                 uint8_t *st = base + s * kStageBytes;
+                if (dt_tma) {  // dt[t0 .. t0+127][4 heads from h0 rounded down to 4]
+                    mbar_expect_tx(&bar_dt[s], (uint32_t)(kRows * 4 * sizeof(float)));
+                    tma_load_3d(base + 2 * kStageBytes + s * kDtBytes, &dtmap, &bar_dt[s], u.h0 & ~3, u.t0, u.b);
+                } else {
+                    mbar_arrive(&bar_dt[s]);
+                }
                 mbar_expect_tx(&bar_full[s], (uint32_t)(4 * kSlab));
                 for (int k = 0; k < 2; ++k) tma_load_3d(st + k * kSlab, &xmap, &bar_full[s], u.hb * 128 + 64 * k, u.t0, u.b);
                 tma_load_3d(st + 4 * kSlab, &bmap, &bar_full[s], u.g * NS, u.t0, u.b);
@@ -1348,15 +1364,23 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
             bool ok = mbar_wait(&bar_info[ss], pq);
             const int tk = s_tk[ss];
-            if (named_sync_or(kBarFront, 128, !ok || tk < 0)) break;
+            if (named_sync_or(kBarFront, 128, !ok)) {
+                s_fail = 1;
+                break;
+            }
+            if (tk < 0) break;  // the same ticket for every thread
             const PipeUnit u = decode_unit(pr, tk, nhb);
             uint8_t *st = base + s * kStageBytes;
+            const float *dts = reinterpret_cast<const float *>(base + 2 * kStageBytes + s * kDtBytes) + ft * 4 + (u.h0 & 3);
+            if (dt_tma) ok = ok && mbar_wait(&bar_dt[s], ph);
             float v[2], d[2];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const bool act = hh < HB;
                 const float a = act ? __ldg(pr.A + u.h0 + hh) : 0.f;
-                d[hh] = (act && ft < u.len) ? __ldg(pr.dt + ((size_t)u.b * L + u.t0 + ft) * H + u.h0 + hh) : 0.f;
+                d[hh] = (act && ft < u.len)
+                            ? (dt_tma ? dts[hh] : __ldg(pr.dt + ((size_t)u.b * L + u.t0 + ft) * H + u.h0 + hh))
+                            : 0.f;
                 v[hh] = d[hh] * a;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -1417,12 +1441,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     uint4 *ptr = reinterpret_cast<uint4 *>(st + mb * kSlab + sw128(j, qq));
                     const uint4 xv = *ptr;
                     const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                    const float2 w2 = make_float2(w, w);
                     float f[8];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float2 t = __bfloat1622float2(x2[k]);
-                        f[2 * k] = t.x * w;
-                        f[2 * k + 1] = t.y * w;
+                        const float2 t = __fmul2_rn(__bfloat1622float2(x2[k]), w2);
+                        f[2 * k] = t.x;
+                        f[2 * k + 1] = t.y;
                     }
                     uint4 hi, lo;
                     split8(f, hi, lo);
@@ -1464,26 +1489,39 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 break;
             }
         }
-    } else if (warp < kWarpEpi) {
-        // ================= look-back, h operand, off-diagonal MMA, inclusive state
-        const int stt = tid - 32 * kWarpState;
+    } else {
+        // ================= two teams, warps 6-9 for the even units (stage 0) and
+        // 10-13 for the odd ones (stage 1): look-back for h_c (publishing S_c as the
+        // aggregate if the walk is still waiting when S_c is ready), h operand,
+        // off-diagonal MMA, inclusive state, then y = r Y + D x staged over the dead
+        // wx lo and stored by TMA
+        const int team = (warp - kWarpState) >> 2;
+        const int tt = tid - 32 * (kWarpState + 4 * team);
+        const int bar_team = kBarTeam0 + team;
         const int hh_m = m / P, p_m = m % P;
         const size_t ustride = (size_t)kRows * NS;
-        for (int it = 0;; ++it) {
-            const int s = it & 1, ss = it & 3;
+        const bool tma_out = pr.chunk == kRows;
+        const int s = team;
+        uint8_t *st = base + s * kStageBytes;
+        const uint32_t slot = tmem + s * 256 + lane_base;
+        for (int it = team;; it += 2) {
+            const int ss = it & 3;
             const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
             bool ok = mbar_wait(&bar_info[ss], pq);
             const int tk = s_tk[ss];
-            if (named_sync_or(kBarState, 128, !ok || tk < 0)) break;
+            if (named_sync_or(bar_team, 128, !ok)) {
+                s_fail = 1;
+                break;
+            }
+            if (tk < 0) break;  // the same ticket for every thread
             const PipeUnit u = decode_unit(pr, tk, nhb);
             const int c = u.c;
-            const uint32_t slot = tmem + s * 256 + lane_base;
             // walk back to the nearest inclusive state; -2: S_c became ready first
             // (publish it as the aggregate, then walk on); -3: gave up
             int stop = c - 1;
             if (c > 0) {
                 for (int round = 0; round < 2; ++round) {
-                    if (warp == kWarpState) {
+                    if (tt < 32) {
                         int res = -3, top = c - 1;
                         const uint64_t tstart = globaltimer();
                         for (;;) {
@@ -1505,17 +1543,17 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                                 top -= 32;
                                 continue;
                             }
-                            if (round == 0 && mbar_test_wait(&bar_mma[s], ph)) {
+                            if (round == 0 && c < nc - 1 && mbar_test_wait(&bar_mma[s], ph)) {
                                 res = -2;
                                 break;
                             }
                             if (globaltimer() - tstart > kWaitLimitNs) break;
-                            __nanosleep(200);
+                            __nanosleep(128);
                         }
-                        if (lane == 0) s_walk[round] = res;
+                        if (lane == 0) s_walk[team][round] = res;
                     }
-                    named_sync(kBarState, 128);
-                    const int res = s_walk[round];
+                    named_sync(bar_team, 128);
+                    const int res = s_walk[team][round];
                     if (res >= -1) {
                         stop = res;
                         break;
@@ -1539,14 +1577,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                                        make_float4(sfac * sv[4 * q], sfac * sv[4 * q + 1], sfac * sv[4 * q + 2],
                                                    sfac * sv[4 * q + 3]));
                         }
-                        if (stt < HB) fa.alpha[u.unit * 2 + stt] = s_alpha[ss][stt];
+                        if (tt < HB) fa.alpha[u.unit * 2 + tt] = s_alpha[ss][tt];
                     }
                     // one release for the whole unit: the barrier orders every
-                    // thread's stores before the leader's fence and flag
-                    if (!named_sync_or(kBarState, 128, !ok) && stt == 0) {
-                        __threadfence();
-                        st_relaxed_flag(fa.aggcnt + u.unit);
-                    }
+                    // thread's stores before the leader's release store
+                    if (!named_sync_or(bar_team, 128, !ok) && tt == 0) st_release_flag(fa.aggcnt + u.unit);
                 }
             }
             // h_c for row m, in the recurrence's own order
@@ -1587,9 +1622,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             ok = ok && mbar_wait(&bar_mma[s], ph) && mbar_wait(&bar_seg[ss], pq);
             tc_fence_after();
             const bool fast = s_fast[ss] != 0;
-            uint8_t *hh_s = base + s * kStageBytes;  // wx hi is dead once the MMAs are done
             if (ok) {
-                if (fast) {  // e^ref h_c -> bf16 hi / lo K-major slabs
+                if (fast) {  // e^ref h_c -> bf16 hi / lo K-major slabs over the dead wx hi
                     const float ysc = s_ysc[ss][hh_m];
 #pragma unroll
                     for (int q = 0; q < NS / 8; ++q) {
@@ -1598,11 +1632,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                         for (int k = 0; k < 8; ++k) f[k] = ysc * acc[8 * q + k];
                         uint4 hi, lo;
                         split8(f, hi, lo);
-                        *reinterpret_cast<uint4 *>(hh_s + sw128(m, q)) = hi;
-                        *reinterpret_cast<uint4 *>(hh_s + kSlab + sw128(m, q)) = lo;
+                        *reinterpret_cast<uint4 *>(st + sw128(m, q)) = hi;
+                        *reinterpret_cast<uint4 *>(st + kSlab + sw128(m, q)) = lo;
                     }
                 } else {  // the direct path reads h_c in fp32
-                    float *hcs = reinterpret_cast<float *>(hh_s) + (size_t)m * NS;
+                    float *hcs = reinterpret_cast<float *>(st) + (size_t)m * NS;
 #pragma unroll
                     for (int k = 0; k < NS; ++k) hcs[k] = acc[k];
                 }
@@ -1618,12 +1652,12 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             }
             fence_async_smem();
             tc_fence_before();
-            const bool any_fail = named_sync_or(kBarState, 128, !ok);
-            if (stt == 0) {
-                if (!any_fail && fast) {  // Y += C (e^ref h_c)^T; the stage is free once it completes
+            bool any_fail = named_sync_or(bar_team, 128, !ok);
+            if (tt == 0) {
+                if (!any_fail && fast) {  // Y += C (e^ref h_c)^T; the stage's x, B, C are free once it completes
                     tc_fence_after();
                     constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 0);
-                    const uint32_t sa = smem_u32(base + s * kStageBytes);
+                    const uint32_t sa = smem_u32(st);
                     for (int ks = 0; ks < NS / 16; ++ks) {
                         const uint64_t ad = sdesc_sw128(sa + 5 * kSlab + ks * 32, 16, 1024);
                         mma_bf16(tmem + s * 256 + col_y, ad, sdesc_sw128(sa + ks * 32, 16, 1024), id_o, 1);
@@ -1635,53 +1669,34 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     mbar_arrive(&bar_yo[s]);  // the direct path frees the stage itself
                 }
             }
-            if (any_fail) {
-                s_fail = 1;
-                break;
-            }
             // publish h_{c+1}
-            float4 *dst = reinterpret_cast<float4 *>(fa.incl + u.unit * ustride) + m;
-            float *fo = (c == nc - 1 && pr.final_state) ? pr.final_state + (((size_t)u.b * H + hg) * P + p_m) * NS
-                                                        : nullptr;
+            if (!any_fail) {
+                float4 *dst = reinterpret_cast<float4 *>(fa.incl + u.unit * ustride) + m;
+                float *fo = (c == nc - 1 && pr.final_state)
+                                ? pr.final_state + (((size_t)u.b * H + hg) * P + p_m) * NS
+                                : nullptr;
 #pragma unroll
-            for (int q = 0; q < NS / 4; ++q) {
-                const float4 vv = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-                __stcg(dst + q * kRows, vv);
-                if (fo) reinterpret_cast<float4 *>(fo)[q] = vv;
+                for (int q = 0; q < NS / 4; ++q) {
+                    const float4 vv = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                    __stcg(dst + q * kRows, vv);
+                    if (fo) reinterpret_cast<float4 *>(fo)[q] = vv;
+                }
             }
-            named_sync(kBarState, 128);
-            if (stt == 0) {
-                __threadfence();
-                st_relaxed_flag(fa.inclcnt + u.unit);
-            }
-        }
-    } else {
-        // ================= y = r Y + D x, staged over the dead wx lo and stored by TMA
-        const int et = tid - 32 * kWarpEpi;
-        const bool tma_out = pr.chunk == kRows;
-        for (int it = 0;; ++it) {
-            const int s = it & 1, ss = it & 3;
-            const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
-            bool ok = mbar_wait(&bar_info[ss], pq);
-            const int tk = s_tk[ss];
-            if (named_sync_or(kBarEpi, 128, !ok || tk < 0)) break;
-            const PipeUnit u = decode_unit(pr, tk, nhb);
-            uint8_t *st = base + s * kStageBytes;
-            uint8_t *ystage = st + 2 * kSlab;
+            named_sync(bar_team, 128);
+            if (tt == 0 && !any_fail) st_release_flag(fa.inclcnt + u.unit);
+            // ---- epilogue: x of this thread's output row through L2, then Y
             const bool row_in = m < u.len;
-            // x of this thread's output row (re-read through L2), fetched before the wait
             uint4 xpre[16];
             {
                 const uint4 *xrow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(pr.x) +
                                                                     (((size_t)u.b * L + u.t0 + m) * H + u.h0) * P);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) xpre[k] = row_in ? __ldg(xrow + k) : make_uint4(0, 0, 0, 0);
+                for (int k = 0; k < 16; ++k) xpre[k] = (row_in && fast) ? __ldg(xrow + k) : make_uint4(0, 0, 0, 0);
             }
-            ok = mbar_wait(&bar_seg[ss], pq) && mbar_wait(&bar_yo[s], ph);
+            ok = !any_fail && mbar_wait(&bar_yo[s], ph);
             tc_fence_after();
-            const bool fast = s_fast[ss] != 0;
+            uint8_t *ystage = st + 2 * kSlab;
             if (ok && fast) {
-                const uint32_t slot = tmem + s * 256 + lane_base;
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
                                                        (((size_t)u.b * L + u.t0 + m) * H + u.h0) * P);
 #pragma unroll
@@ -1691,15 +1706,17 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
                     float yv[32];
                     tmem_ld32(slot + col_y + col, yv);
+                    const float2 r2 = make_float2(r, r), D2 = make_float2(Dh, Dh);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xpre[col / 8 + k]);
                         float o[8];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float2 xf = __bfloat1622float2(x2[e]);
-                            o[2 * e] = fmaf(Dh, xf.x, r * yv[8 * k + 2 * e]);
-                            o[2 * e + 1] = fmaf(Dh, xf.y, r * yv[8 * k + 2 * e + 1]);
+                            const float2 ry = __fmul2_rn(r2, make_float2(yv[8 * k + 2 * e], yv[8 * k + 2 * e + 1]));
+                            const float2 ov2 = __ffma2_rn(D2, __bfloat1622float2(x2[e]), ry);
+                            o[2 * e] = ov2.x;
+                            o[2 * e + 1] = ov2.y;
                         }
                         const uint4 ov = pack8(o);
                         if (tma_out)
@@ -1711,12 +1728,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             }
             fence_async_smem();
             tc_fence_before();
-            const bool all_ok = !named_sync_or(kBarEpi, 128, !ok);
-            if (et == 0) {
+            const bool all_ok = !named_sync_or(bar_team, 128, !ok);
+            if (tt == 0) {
                 mbar_arrive(&bar_slot[s]);  // Y has been read
                 if (all_ok && fast && tma_out) {
-                    for (int k = 0; k < 2; ++k)
-                        tma_store_3d(&ymap, ystage + k * kSlab, u.hb * 128 + 64 * k, u.t0, u.b);
+                    for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, u.hb * 128 + 64 * k, u.t0, u.b);
                     bulk_commit();
                     bulk_wait_read_all();
                 }
@@ -1724,9 +1740,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             }
             if (all_ok && !fast) {
                 direct_unit_outputs(pr, NS, u.b, u.hb, u.c, reinterpret_cast<const float *>(st),
-                                    reinterpret_cast<float *>(st + 2 * kSlab), cs[ss], dtv[ss], et, 128, kBarEpi);
-                named_sync(kBarEpi, 128);  // every thread is done with the stage
-                if (et == 0) {
+                                    reinterpret_cast<float *>(st + 2 * kSlab), cs[ss], dtv[ss], tt, 128, bar_team);
+                named_sync(bar_team, 128);  // every thread is done with the stage
+                if (tt == 0) {
                     mbar_arrive(&bar_lo[s]);
                     mbar_arrive(&bar_free[s]);
                 }
@@ -1757,6 +1773,21 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int width, int seqlen, i
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// fp32 [batch][seqlen][width] with a 4 x 128 box (no swizzle), for dt.
+cudaError_t make_map_f32(CUtensorMap *map, const void *ptr, int width, int seqlen, int batch)
+{
+    auto fn = tensor_map_encoder();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)seqlen, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)width * 4, (cuuint64_t)width * 4 * seqlen};
+    const cuuint32_t box[3] = {4, (cuuint32_t)kRows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // x | B (then C) | C (then tril(G), then y) | wx ring | h hi/lo (dstate 128 only)
 size_t fused_smem(int NS)
 {
@@ -1781,7 +1812,12 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
     const size_t units = units_of(pr);
     if ((e = cudaMemsetAsync(fa.aggcnt, 0, (2 * units + kCtrCount) * sizeof(uint32_t), s)) != cudaSuccess) return e;
     if (NS == 64) {
-        const size_t psmem = 1024 + (size_t)2 * kStageBytes;
+        const size_t psmem = 1024 + (size_t)2 * kStageBytes + 2 * kDtBytes;
+        // dt through TMA when its rows are 16-byte multiples and the base is aligned
+        CUtensorMap dtmap;
+        memset(&dtmap, 0, sizeof dtmap);
+        int dt_tma = (pr.nheads % 4 == 0 && (reinterpret_cast<uintptr_t>(pr.dt) & 15) == 0) ? 1 : 0;
+        if (dt_tma && make_map_f32(&dtmap, pr.dt, pr.nheads, pr.seqlen, pr.batch) != cudaSuccess) dt_tma = 0;
         if ((e = cudaFuncSetAttribute(ssd_fused_pipe_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem)) !=
             cudaSuccess)
             return e;
@@ -1789,7 +1825,7 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
         const unsigned grid = (unsigned)std::min<size_t>(units, (size_t)nsm);
-        ssd_fused_pipe_tc<<<grid, kPipeThreads, psmem, s>>>(xmap, bmap, cmap, ymap, pr, fa, (int)units);
+        ssd_fused_pipe_tc<<<grid, kPipeThreads, psmem, s>>>(xmap, bmap, cmap, ymap, dtmap, pr, fa, (int)units, dt_tma);
     } else {
         if ((e = cudaFuncSetAttribute(ssd_fused_tc<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
             cudaSuccess)
