@@ -1227,7 +1227,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     // per stage (it & 1): full, free, slot, g, fr, mma, yo; per unit in flight (it & 3): info,
     // seg and the unit's scalars, which the epilogue may still read after the stage is free
     __shared__ __align__(8) uint64_t bar_info[4], bar_seg[4], bar_full[2], bar_dt[2], bar_free[2], bar_slot[2],
-        bar_lo[2], bar_g[2], bar_fr[2], bar_mma[2], bar_yo[2];
+        bar_lo[2], bar_g[2], bar_fr[2], bar_mma[2], bar_yo[2], bar_xe[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int s_tk[4], s_fast[4];
     __shared__ float cs[4][2 * kRows], dtv[4][2 * kRows], vw[4][2 * kRows], rs[4][2 * kRows];
@@ -1260,6 +1260,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             mbar_init(&bar_fr[k], 128);
             mbar_init(&bar_mma[k], 1);
             mbar_init(&bar_yo[k], 1);
+            mbar_init(&bar_xe[k], 1);
         }
         mbar_fence_init();
         s_fail = 0;
@@ -1622,6 +1623,15 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             ok = ok && mbar_wait(&bar_mma[s], ph) && mbar_wait(&bar_seg[ss], pq);
             tc_fence_after();
             const bool fast = s_fast[ss] != 0;
+            if (tt == 0) {  // x of the unit for the D x term, into the staging region (wx lo is dead)
+                if (ok && fast) {
+                    mbar_expect_tx(&bar_xe[s], (uint32_t)(2 * kSlab));
+                    for (int k = 0; k < 2; ++k)
+                        tma_load_3d(st + 2 * kSlab + k * kSlab, &xmap, &bar_xe[s], u.hb * 128 + 64 * k, u.t0, u.b);
+                } else {
+                    mbar_arrive(&bar_xe[s]);
+                }
+            }
             if (ok) {
                 if (fast) {  // e^ref h_c -> bf16 hi / lo K-major slabs over the dead wx hi
                     const float ysc = s_ysc[ss][hh_m];
@@ -1684,32 +1694,28 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             }
             named_sync(bar_team, 128);
             if (tt == 0 && !any_fail) st_release_flag(fa.inclcnt + u.unit);
-            // ---- epilogue: x of this thread's output row through L2, then Y
+            // ---- epilogue: y = r Y + D x, x read from the staging region and y
+            // written over it (the same swizzled position), then stored by TMA
             const bool row_in = m < u.len;
-            uint4 xpre[16];
-            {
-                const uint4 *xrow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(pr.x) +
-                                                                    (((size_t)u.b * L + u.t0 + m) * H + u.h0) * P);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) xpre[k] = (row_in && fast) ? __ldg(xrow + k) : make_uint4(0, 0, 0, 0);
-            }
-            ok = !any_fail && mbar_wait(&bar_yo[s], ph);
+            ok = !any_fail && mbar_wait(&bar_yo[s], ph) && mbar_wait(&bar_xe[s], ph);
             tc_fence_after();
             uint8_t *ystage = st + 2 * kSlab;
             if (ok && fast) {
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
                                                        (((size_t)u.b * L + u.t0 + m) * H + u.h0) * P);
 #pragma unroll
-                for (int col = 0; col < 128; col += 32) {
+                for (int col = 0; col < 128; col += 64) {
                     const int hh = col / P, h = u.h0 + hh;
                     const float r = rs[ss][hh * kRows + m];
                     const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
-                    float yv[32];
-                    tmem_ld32(slot + col_y + col, yv);
+                    float yv[64];
+                    tmem_ld64(slot + col_y + col, yv);
                     const float2 r2 = make_float2(r, r), D2 = make_float2(Dh, Dh);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xpre[col / 8 + k]);
+                    for (int k = 0; k < 8; ++k) {
+                        uint4 *sp = reinterpret_cast<uint4 *>(ystage + (col / 64) * kSlab + sw128(m, k));
+                        const uint4 xv = *sp;
+                        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
                         float o[8];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -1720,7 +1726,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                         }
                         const uint4 ov = pack8(o);
                         if (tma_out)
-                            *reinterpret_cast<uint4 *>(ystage + (col / 64) * kSlab + sw128(m, (col % 64) / 8 + k)) = ov;
+                            *sp = ov;
                         else if (row_in)
                             dst[col / 8 + k] = ov;
                     }
