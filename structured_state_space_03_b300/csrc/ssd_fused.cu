@@ -1178,6 +1178,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 constexpr int kPipeThreads = 14 * 32;
 constexpr int kStageBytes = 6 * kSlab;
 constexpr int kDtBytes = kRows * 4 * sizeof(float);  // dt box: 128 tokens x 4 heads
+constexpr uint32_t kParts = 4;  // an inclusive state is published when each of a team's four warps released its quarter
 enum { kWarpLoad = 0, kWarpMma = 1, kWarpFront = 2, kWarpState = 6 };
 enum { kBarFront = 1, kBarTeam0 = 2 };  // team 1 uses barrier 3
 
@@ -1530,7 +1531,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                             uint32_t f = kFlagInclusive;
                             if (k >= 0) {
                                 const size_t uk = u.unit - (c - k);
-                                f = ld_acquire(fa.inclcnt + uk) != 0u ? kFlagInclusive
+                                f = ld_acquire(fa.inclcnt + uk) == kParts ? kFlagInclusive
                                     : (ld_acquire(fa.aggcnt + uk) != 0u ? kFlagAggregate : kFlagNone);
                             }
                             const uint32_t end_mask = __ballot_sync(0xffffffffu, f == kFlagInclusive);
@@ -1660,6 +1661,22 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     for (int k = 0; k < 32; ++k) acc[cc + k] = fmaf(a_own, acc[cc + k], sfac * sc[k]);
                 }
             }
+            // publish h_{c+1} first (it is what the successors wait for): each warp
+            // releases its quarter, and the state counts as published at kParts
+            if (ok) {
+                float4 *dst = reinterpret_cast<float4 *>(fa.incl + u.unit * ustride) + m;
+                float *fo = (c == nc - 1 && pr.final_state)
+                                ? pr.final_state + (((size_t)u.b * H + hg) * P + p_m) * NS
+                                : nullptr;
+#pragma unroll
+                for (int q = 0; q < NS / 4; ++q) {
+                    const float4 vv = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                    __stcg(dst + q * kRows, vv);
+                    if (fo) reinterpret_cast<float4 *>(fo)[q] = vv;
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && ok) red_release_add(fa.inclcnt + u.unit, 1u);
             fence_async_smem();
             tc_fence_before();
             bool any_fail = named_sync_or(bar_team, 128, !ok);
@@ -1679,21 +1696,6 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     mbar_arrive(&bar_yo[s]);  // the direct path frees the stage itself
                 }
             }
-            // publish h_{c+1}
-            if (!any_fail) {
-                float4 *dst = reinterpret_cast<float4 *>(fa.incl + u.unit * ustride) + m;
-                float *fo = (c == nc - 1 && pr.final_state)
-                                ? pr.final_state + (((size_t)u.b * H + hg) * P + p_m) * NS
-                                : nullptr;
-#pragma unroll
-                for (int q = 0; q < NS / 4; ++q) {
-                    const float4 vv = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-                    __stcg(dst + q * kRows, vv);
-                    if (fo) reinterpret_cast<float4 *>(fo)[q] = vv;
-                }
-            }
-            named_sync(bar_team, 128);
-            if (tt == 0 && !any_fail) st_release_flag(fa.inclcnt + u.unit);
             // ---- epilogue: y = r Y + D x, x read from the staging region and y
             // written over it (the same swizzled position), then stored by TMA
             const bool row_in = m < u.len;
