@@ -1,11 +1,14 @@
 // ssd_fused.cu -- single-kernel bf16 SSD forward on tcgen05 (sm_103a) for
 // chunk <= 128, headdim 64/128, dstate 64/128.
 //
-// One CTA (256 threads) per (chunk c, batch b, head block hb), a head block
-// being the 128/headdim heads whose (head, headdim) rows fill the 128 TMEM
-// lanes.  x, B and C of the chunk are read from HBM once and y is written once;
-// the chunk-to-chunk recurrence h_{c+1} = a_c h_c + S_c is resolved between
-// CTAs by a decoupled look-back over states published in the workspace.
+// A unit is (chunk c, batch b, head block hb), a head block being the
+// 128/headdim heads whose (head, headdim) rows fill the 128 TMEM lanes.  x, B
+// and C of the chunk are read from HBM once and y is written once; the
+// chunk-to-chunk recurrence h_{c+1} = a_c h_c + S_c is resolved between units
+// by a decoupled look-back over states published in the workspace.  dstate 128
+// runs one CTA (256 threads) per unit (ssd_fused_tc, described here); dstate
+// 64 runs the persistent ssd_fused_pipe_tc further down, one CTA per SM with two
+// units in flight, on the same arithmetic.
 //
 // Inside the chunk the decay exp(cs_i - cs_j) is rank one per head:
 //   exp(cs_i - cs_j) = r_i v_j,  r_i = exp(cs_i - ref),  v_j = exp(ref - cs_j)
@@ -684,496 +687,29 @@ __global__ void __launch_bounds__(kThreads, 2)
                             cs, dtv, tid, kThreads, 0);
 }
 
-// Named barrier over one half of the CTA (warps 0-3: id 1, warps 4-7: id 2).
-__device__ __forceinline__ void half_sync(int half)
-{
-    asm volatile("bar.sync %0, 128;" ::"r"(1 + half) : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// dstate 64.  Same algorithm, two changes of structure:
-//   * the masked tril(C B^T) is the A operand of the diagonal-block MMAs held in
-//     tensor memory (64 columns), which frees the shared memory to build all of
-//     wx (hi and lo, 128 tokens) at once -- hi in place over the x tile -- and
-//     to issue the 32 chunk-state and diagonal-block MMAs back to back; x for
-//     the D x term is re-read through L2 in the epilogue;
-//   * warps 4-7 resolve the entry state h_c by look-back from the start of the
-//     CTA, while warps 0-3 run G, the mask, wx and the MMAs.  Warps 0-3 publish
-//     the aggregate S_c only if h_c is not yet known when the MMAs finish, so a
-//     chunk's aggregate never waits on its own look-back (forward progress as in
-//     ssd_fused_tc).  Counters are complete at 128: one half of the CTA
-//     publishes each state.
-// Shared memory (96 KiB): [0, 64K) x -> wx hi | wx lo, later h hi | lo and the
-// y staging; [64K, 80K) B; [80K, 96K) C.  TMEM: Y [0,128), S_c [128,192),
-// tril(G) as bf16 pairs [192,256).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 2)
-    ssd_fused_ov_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
-                    const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap, Problem pr,
-                    FusedArgs fa)
-{
-    constexpr int NS = 64;
-    constexpr uint32_t kHalfCount = kThreads / 2;
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_ld, bar_g, bar_mma, bar_yo, bar_wx;
-    __shared__ uint32_t tmem_slot, s_ticket;
-    __shared__ float warp_tot[8], warp_mn[8], warp_mx[8];
-    __shared__ float cs[2 * kRows], dtv[2 * kRows];
-    __shared__ float vw[2 * kRows];
-    __shared__ float rs[2 * kRows];
-    __shared__ float s_alpha[2], s_sfac[2], s_yscale[2];
-    __shared__ int s_fail, s_mode, s_stop, s_agg;
-    __shared__ volatile int s_hc_known;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
-    const int nhb = H / HB, nc = pr.nchunks;
-
-    if (warp == 0) tmem_alloc(&tmem_slot, 256);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-        s_ticket = atomicAdd(fa.counters + kCtrTicket, 1u);
-        mbar_init(&bar_ld, 1);
-        mbar_init(&bar_g, 1);
-        mbar_init(&bar_mma, 1);
-        mbar_init(&bar_yo, 1);
-        mbar_init(&bar_wx, 7);  // warps 0-3 and 5-7 build wx
-        mbar_fence_init();
-        s_fail = 0;
-        s_hc_known = 0;
-    }
-    __syncthreads();
-    const uint32_t tmem = tmem_slot;
-    const uint32_t col_y = 0, col_st = 128, col_m = 192;
-
-    const int ticket = (int)s_ticket;
-    const int c = ticket / (pr.batch * nhb);
-    const int rest = ticket - c * (pr.batch * nhb);
-    const int b = rest / nhb, hb = rest - (rest / nhb) * nhb;
-    const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
-    const int t0 = c * pr.chunk, len = min(pr.chunk, L - t0);
-    const size_t unit = ((size_t)b * nhb + hb) * nc + c;
-    const size_t ustride = (size_t)kRows * NS;
-
-    uint8_t *base = align1024(smem_raw);
-    uint8_t *wx = base;                 // x tile -> wx hi (in place) | wx lo at +32K
-    uint8_t *bs = base + 4 * kSlab;     // B
-    uint8_t *csm = bs + kSlab;          // C
-    uint8_t *hh_s = base;               // after the MMAs: h hi | lo
-    uint8_t *ystage = base + 2 * kSlab; // after the MMAs: y tiles
-
-    if (tid == 0) {
-        tma_prefetch_desc(&xmap);
-        tma_prefetch_desc(&bmap);
-        tma_prefetch_desc(&cmap);
-        mbar_expect_tx(&bar_ld, (uint32_t)(4 * kSlab));
-        for (int k = 0; k < 2; ++k) tma_load_3d(wx + k * kSlab, &xmap, &bar_ld, hb * 128 + 64 * k, t0, b);
-        tma_load_3d(bs, &bmap, &bar_ld, g * NS, t0, b);
-        tma_load_3d(csm, &cmap, &bar_ld, g * NS, t0, b);
-    }
-
-    // ---- segment sums, span, reference, factors (warps 0-3 head 0, warps 4-7 head 1)
-    bool fast;
-    {
-        const int hh = half, t = tid & 127;
-        const bool active = hh < HB;
-        const float a = active ? __ldg(pr.A + h0 + hh) : 0.f;
-        const float d = (active && t < len) ? __ldg(pr.dt + ((size_t)b * L + t0 + t) * H + h0 + hh) : 0.f;
-        float v = d * a;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += u;
-        }
-        if (lane == 31) warp_tot[warp] = v;
-        __syncthreads();
-        for (int w = half * 4; w < warp; ++w) v += warp_tot[w];
-        float mn = t < len ? v : 3.0e38f, mx = t < len ? v : -3.0e38f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        }
-        if (lane == 0) {
-            warp_mn[warp] = mn;
-            warp_mx[warp] = mx;
-        }
-        cs[hh * kRows + t] = v;
-        dtv[hh * kRows + t] = d;
-        __syncthreads();
-        float lo_[2], hi_[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            lo_[k] = fminf(fminf(warp_mn[4 * k], warp_mn[4 * k + 1]), fminf(warp_mn[4 * k + 2], warp_mn[4 * k + 3]));
-            hi_[k] = fmaxf(fmaxf(warp_mx[4 * k], warp_mx[4 * k + 1]), fmaxf(warp_mx[4 * k + 2], warp_mx[4 * k + 3]));
-        }
-        fast = (hi_[0] - lo_[0] <= kSpanMax) && (HB == 1 || hi_[1] - lo_[1] <= kSpanMax);
-        const float cl = cs[hh * kRows + len - 1];
-        const float ref = 0.5f * ((hh == 0 ? lo_[0] : lo_[1]) + (hh == 0 ? hi_[0] : hi_[1]));
-        const float refw = fast ? ref : cl, refy = fast ? ref : 0.f;
-        if (active) {
-            vw[hh * kRows + t] = t < len ? expf(refw - v) * d : 0.f;
-            rs[hh * kRows + t] = expf(v - refy);
-            if (t == 0) {
-                s_alpha[hh] = expf(cl);
-                s_sfac[hh] = expf(cl - refw);
-                s_yscale[hh] = expf(refy);
-            }
-        }
-        __syncthreads();
-    }
-    const int m = quarter * 32 + lane;   // TMEM row of this thread
-    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-
-    // ---- wx = v dt x for all 128 tokens, hi in place over x, lo at +32K; built by
-    // every warp except warp 4 (which walks back) -- 224 threads, up to 10 chunks each
-    if (warp != 4) {
-        const bool got = mbar_wait(&bar_ld, 0);
-        const int bt = tid < 128 ? tid : tid - 32;
-        if (got && tid == 0) {  // G = C B^T first, so it runs under the wx build
-            tc_fence_after();
-            constexpr uint32_t id_g = idesc_bf16(128, 128, 0, 0);
-            for (int ks = 0; ks < NS / 16; ++ks) {
-                const uint32_t off = ks * 32;
-                mma_bf16(tmem + col_y, sdesc_sw128(smem_u32(csm) + off, 16, 1024),
-                         sdesc_sw128(smem_u32(bs) + off, 16, 1024), id_g, ks > 0);
-            }
-            mma_commit(&bar_g);
-        }
-        if (got) {
-#pragma unroll 2
-            for (int q = bt; q < 2 * kRows * 8; q += 224) {
-                const int mb = q >> 10, j = (q >> 3) & 127, qq = q & 7;
-                const float w = vw[(P == 64 ? mb : 0) * kRows + j];
-                uint4 *ptr = reinterpret_cast<uint4 *>(wx + mb * kSlab + sw128(j, qq));
-                const uint4 xv = *ptr;
-                const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-                float f[8];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 t = __bfloat1622float2(x2[u]);
-                    f[2 * u] = t.x * w;
-                    f[2 * u + 1] = t.y * w;
-                }
-                uint4 hi, lo;
-                split8(f, hi, lo);
-                *ptr = hi;
-                *reinterpret_cast<uint4 *>(wx + 2 * kSlab + mb * kSlab + sw128(j, qq)) = lo;
-            }
-        } else {
-            s_fail = 1;
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_wx);
-    }
-
-    if (half == 0) {
-        // ================= warps 0-3: G -> tril(G) in TMEM, wx, all MMAs, aggregate
-        bool ok = !s_fail;
-        if (ok && !mbar_wait(&bar_g, 0)) ok = false;
-        tc_fence_after();
-        if (ok && fast) {  // tril(G) -> bf16 pairs in TMEM (row m, columns jb*32 .. jb*32+31)
-            for (int jb = 0; jb < 4; ++jb) {
-                uint32_t pk[16];
-                if (jb > quarter) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) pk[k] = 0u;
-                } else {
-                    float gv[32];
-                    tmem_ld32(tmem + lane_base + col_y + jb * 32, gv);
-                    if (jb == quarter) {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            if (jb * 32 + k > m) gv[k] = 0.f;
-                    }
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        __nv_bfloat162 t2 = __floats2bfloat162_rn(gv[2 * k], gv[2 * k + 1]);
-                        pk[k] = *reinterpret_cast<uint32_t *>(&t2);
-                    }
-                }
-                tmem_st16(tmem + lane_base + col_m + jb * 16, pk);
-            }
-        }
-        tc_fence_before();
-        if (!ok) s_fail = 1;
-        half_sync(0);
-        ok = !s_fail;
-        if (ok && tid == 0 && !mbar_wait(&bar_wx, 0)) ok = false;
-        if (ok && tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id_s = idesc_bf16(128, NS, 1, 1);
-            constexpr uint32_t id_d = idesc_bf16(128, 128, 0, 1);
-            const uint32_t wxa = smem_u32(wx), ba = smem_u32(bs);
-            for (int ks = 0; ks < kRows / 16; ++ks) {
-                const uint64_t bd = sdesc_sw128(ba + ks * 2048, kSlab, 1024);
-                const uint64_t whi = sdesc_sw128(wxa + ks * 2048, kSlab, 1024);
-                const uint64_t wlo = sdesc_sw128(wxa + 2 * kSlab + ks * 2048, kSlab, 1024);
-                mma_bf16(tmem + col_st, whi, bd, id_s, ks > 0);
-                mma_bf16(tmem + col_st, wlo, bd, id_s, 1);
-                if (fast) {
-                    mma_bf16_tA(tmem + col_y, tmem + col_m + ks * 8, whi, id_d, ks > 0);
-                    mma_bf16_tA(tmem + col_y, tmem + col_m + ks * 8, wlo, id_d, 1);
-                }
-            }
-            mma_commit(&bar_mma);
-        }
-        if (!ok) s_fail = 1;
-        if (ok && !mbar_wait(&bar_mma, 0)) s_fail = 1;
-        tc_fence_after();
-        // aggregate, unless warps 4-7 already know h_c
-        if (tid == 0) s_agg = (c > 0 && !s_hc_known) ? 1 : 0;
-        half_sync(0);
-        ok = !s_fail;
-        if (ok && s_agg) {
-            const float sfac = s_sfac[m / P];
-            float *dst = fa.agg + unit * ustride + (size_t)m * NS;
-            for (int cc = 0; cc < NS; cc += 32) {
-                float v[32];
-                tmem_ld32(tmem + lane_base + col_st + cc, v);
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    __stcg(reinterpret_cast<float4 *>(dst + cc) + u, make_float4(sfac * v[4 * u], sfac * v[4 * u + 1],
-                                                                                 sfac * v[4 * u + 2], sfac * v[4 * u + 3]));
-            }
-            if (tid < HB) fa.alpha[unit * 2 + tid] = s_alpha[tid];
-            red_release_add(fa.aggcnt + unit, 1u);
-        }
-    } else {
-        // ================= warps 4-7: entry state h_c by look-back, inclusive state, h operand
-        const int ht = tid - 128;
-        bool ok = true;
-        if (warp == 4) {  // warps 5-7 are still building wx
-            int mode = 0;
-            if (c > 0) mode = ld_acquire(fa.inclcnt + unit - 1) == kHalfCount ? 1 : 2;
-            if (lane == 0) {
-                s_mode = mode;
-                if (mode != 2) s_hc_known = 1;
-            }
-            __syncwarp();
-            if (mode == 2) {
-                int top = c - 1, stop = -1;
-                const uint64_t tstart = globaltimer();
-                bool timed_out = false;
-                for (;;) {
-                    const int k = top - lane;
-                    uint32_t f = kFlagInclusive;
-                    if (k >= 0) {
-                        const size_t uk = unit - (c - k);
-                        f = ld_acquire(fa.inclcnt + uk) == kHalfCount ? kFlagInclusive
-                            : (ld_acquire(fa.aggcnt + uk) == kHalfCount ? kFlagAggregate : kFlagNone);
-                    }
-                    const uint32_t end_mask = __ballot_sync(0xffffffffu, f == kFlagInclusive);
-                    const uint32_t none_mask = __ballot_sync(0xffffffffu, f == kFlagNone);
-                    const uint32_t before = end_mask ? (end_mask & (0u - end_mask)) - 1u : 0xffffffffu;
-                    if ((none_mask & (end_mask ? before : 0xffffffffu)) == 0u) {
-                        if (end_mask) {
-                            stop = top - (__ffs(end_mask) - 1);
-                            break;
-                        }
-                        top -= 32;
-                        continue;
-                    }
-                    if (globaltimer() - tstart > kWaitLimitNs) {
-                        timed_out = true;
-                        break;
-                    }
-                    __nanosleep(64);
-                }
-                if (lane == 0) {
-                    s_stop = stop;
-                    if (timed_out) s_fail = 1;
-                    else s_hc_known = 1;
-                }
-            }
-        }
-        half_sync(1);
-        const int mode = s_mode;
-        ok = !s_fail;
-        // h_c for row m, all 64 state columns, in the recurrence's own order
-        const int hh_m = m / P, p_m = m % P, hg = h0 + hh_m;
-        float acc[NS];
-#pragma unroll
-        for (int k = 0; k < NS; ++k) acc[k] = 0.f;
-        if (ok) {
-            const int stop = mode == 2 ? s_stop : c - 1;
-            const float *init = pr.init_state ? pr.init_state + (((size_t)b * H + hg) * P + p_m) * NS : nullptr;
-            const size_t row_off = (size_t)m * NS;
-            const float4 *src0 = stop >= 0 ? reinterpret_cast<const float4 *>(fa.incl + (unit - (c - stop)) * ustride + row_off)
-                                           : reinterpret_cast<const float4 *>(init);
-            if (src0) {
-#pragma unroll
-                for (int q = 0; q < NS / 4; ++q) {
-                    const float4 v = __ldcg(src0 + q);
-                    acc[4 * q] = v.x;
-                    acc[4 * q + 1] = v.y;
-                    acc[4 * q + 2] = v.z;
-                    acc[4 * q + 3] = v.w;
-                }
-            }
-            for (int k = stop + 1; k < c; ++k) {
-                const size_t u = unit - (c - k);
-                const float a = __ldcg(fa.alpha + u * 2 + hh_m);
-                const float4 *src = reinterpret_cast<const float4 *>(fa.agg + u * ustride + row_off);
-#pragma unroll
-                for (int q = 0; q < NS / 4; ++q) {
-                    const float4 v = __ldcg(src + q);
-                    acc[4 * q] = fmaf(a, acc[4 * q], v.x);
-                    acc[4 * q + 1] = fmaf(a, acc[4 * q + 1], v.y);
-                    acc[4 * q + 2] = fmaf(a, acc[4 * q + 2], v.z);
-                    acc[4 * q + 3] = fmaf(a, acc[4 * q + 3], v.w);
-                }
-            }
-        }
-        // wait for the MMAs: S_c is in TMEM, and wx (the h operand's slot) is dead
-        if (ok && !mbar_wait(&bar_mma, 0)) s_fail = 1;
-        tc_fence_after();
-        ok = ok && !s_fail;
-        if (ok) {
-            const float sfac = s_sfac[hh_m], a_own = s_alpha[hh_m], ysc = s_yscale[hh_m];
-            float *dst = fa.incl + unit * ustride + (size_t)m * NS;
-            float *fo = (c == nc - 1 && pr.final_state) ? pr.final_state + (((size_t)b * H + hg) * P + p_m) * NS
-                                                         : nullptr;
-#pragma unroll
-            for (int cc = 0; cc < NS; cc += 32) {
-                float sc[32];
-                tmem_ld32(tmem + lane_base + col_st + cc, sc);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) sc[k] = fmaf(a_own, acc[cc + k], sfac * sc[k]);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 v = make_float4(sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3]);
-                    __stcg(reinterpret_cast<float4 *>(dst + cc) + q, v);
-                    if (fo) reinterpret_cast<float4 *>(fo + cc)[q] = v;
-                }
-            }
-            if (fast) {  // e^ref h_c -> bf16 hi / lo K-major slabs over the dead wx
-#pragma unroll
-                for (int q = 0; q < NS / 8; ++q) {
-                    float f[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) f[u] = ysc * acc[8 * q + u];
-                    uint4 hi, lo;
-                    split8(f, hi, lo);
-                    *reinterpret_cast<uint4 *>(hh_s + sw128(m, q)) = hi;
-                    *reinterpret_cast<uint4 *>(hh_s + kSlab + sw128(m, q)) = lo;
-                }
-            } else {  // the direct path reads h_c from shared memory
-                float *hcs = reinterpret_cast<float *>(hh_s) + (size_t)m * NS;
-#pragma unroll
-                for (int k = 0; k < NS; ++k) hcs[k] = acc[k];
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        if (!ok) s_fail = 1;
-        half_sync(1);
-        if (ok && fast && ht == 0) {  // Y += C (e^ref h_c)^T
-            tc_fence_after();
-            constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 0);
-            for (int ks = 0; ks < NS / 16; ++ks) {
-                const uint32_t off = ks * 32;
-                const uint64_t ad = sdesc_sw128(smem_u32(csm) + off, 16, 1024);
-                mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(hh_s) + off, 16, 1024), id_o, 1);
-                mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(hh_s) + kSlab + off, 16, 1024), id_o, 1);
-            }
-            mma_commit(&bar_yo);
-        }
-        // publish h_{c+1} while the off-diagonal MMA runs
-        if (ok) red_release_add(fa.inclcnt + unit, 1u);
-    }
-    // x of this thread's output row segment (re-read through L2), fetched before the wait
-    const int col0 = half * 64;
-    uint4 xpre[8];
-    {
-        const bool row_in = t0 + m < L;
-        const uint4 *xrow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(pr.x) +
-                                                            (((size_t)b * L + t0 + m) * H + h0) * P + col0);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) xpre[u] = (row_in && fast) ? __ldg(xrow + u) : make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
-    bool ok = !s_fail;
-    if (ok && fast && !mbar_wait(&bar_yo, 0)) s_fail = 1;
-    __syncthreads();
-    ok = !s_fail;
-    tc_fence_after();
-
-    // ---- y = r_i Y + D x; row i = m, columns [64 half, 64 half + 64)
-    const bool tma_out = pr.chunk == kRows;
-    if (ok && fast) {
-        const int i = m;
-        const int hh = col0 / P, h = h0 + hh;
-        const float r = rs[hh * kRows + i];
-        const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
-        for (int pc = 0; pc < 64; pc += 32) {
-            const int col = col0 + pc;
-            float yv[32];
-            tmem_ld32(tmem + lane_base + col_y + col, yv);
-            uint4 outv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint4 xv = xpre[pc / 8 + u];
-                const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-                float o[8];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const float2 xf = __bfloat1622float2(x2[v]);
-                    o[2 * v] = fmaf(Dh, xf.x, r * yv[8 * u + 2 * v]);
-                    o[2 * v + 1] = fmaf(Dh, xf.y, r * yv[8 * u + 2 * v + 1]);
-                }
-                outv[u] = pack8(o);
-            }
-            if (tma_out) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    *reinterpret_cast<uint4 *>(ystage + half * kSlab + sw128(i, pc / 8 + u)) = outv[u];
-            } else if (i < len) {
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
-                                                       (((size_t)b * L + t0 + i) * H + h0) * P + col);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) dst[u] = outv[u];
-            }
-        }
-    }
-    if (tma_out) {
-        fence_async_smem();
-        __syncthreads();
-        if (ok && fast && tid == 0) {
-            for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, hb * 128 + 64 * k, t0, b);
-            bulk_commit();
-            bulk_wait_read_all();
-        }
-    }
-    if (!ok && tid == 0) atomicOr(pr.err_word, kDevErrTimeout);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
-    if (ok && !fast)
-        direct_unit_outputs(pr, NS, b, hb, c, reinterpret_cast<const float *>(hh_s),
-                            reinterpret_cast<float *>(base + 2 * kSlab), cs, dtv, tid, kThreads, 0);
-}
-
 // ---------------------------------------------------------------------------
 // dstate 64, persistent.  One CTA per SM takes units (chunk-major tickets, as
 // above) one after another and keeps two of them in flight: two shared-memory
-// stages of 96 KiB and two 256-column TMEM slots.  Warp roles:
-//   warp 0      tickets and TMA loads (x, B, C) into a free stage;
+// stages of 96 KiB and two 256-column TMEM slots, unit it using stage and slot
+// it & 1.  Warp roles:
+//   warp 0      tickets; TMA loads of dt, x, B and C into a free stage;
 //   warp 1      G = C B^T, then the chunk-state and diagonal-block MMAs;
 //   warps 2-5   segment sums and factors, wx (hi, lo), tril(G) into TMEM;
-//   warps 6-9   look-back for h_c (publishing the aggregate S_c if the walk is
-//               still waiting when S_c is ready), inclusive state, h operand,
-//               and the off-diagonal MMA Y += C (e^ref h_c)^T;
-//   warps 10-13 y = r Y + D x, staged and stored by TMA, then free the stage.
-// Each role walks the units of the CTA in ticket order, so the forward-progress
-// argument of the one-unit kernels holds: the smallest unfinished ticket only
-// waits on finished units.  Stage s, 96 KiB: [0, 32K) x -> wx hi -> h hi | lo;
-// [32K, 64K) wx lo -> y staging; [64K, 80K) B; [80K, 96K) C.  TMEM slot s at
-// column 256 s: Y [0,128), S_c [128,192), tril(G) [192,256).
+//   warps 6-9   team 0 (the units of stage 0), warps 10-13 team 1 (stage 1):
+//               look-back for h_c (publishing S_c as the aggregate if the walk
+//               is still waiting when S_c is ready), h_{c+1} published, the h
+//               operand and the off-diagonal MMA Y += C (e^ref h_c)^T, then
+//               y = r Y + D x with x brought into the staging region by TMA,
+//               and the TMA store of y.
+// Each role walks its units in ticket order, so the forward-progress argument
+// of the one-unit kernel holds: the smallest unfinished ticket only waits on
+// finished units.  Stage s, 96 KiB: [0, 32K) x -> wx hi -> h hi | lo;
+// [32K, 64K) wx lo -> x -> y (staging); [64K, 80K) B; [80K, 96K) C; after the
+// two stages, 2 KiB of dt per stage.  TMEM slot s at column 256 s: Y [0,128),
+// S_c [128,192), tril(G) [192,256).  The stage's x, B and C are reloaded as soon
+// as the off-diagonal MMA completes; the wx-lo region waits for the y store.
+// Per-unit scalars and the info and seg barriers have four sets (it & 3): a
+// team may still read them after its stage has been handed to the next unit.
 // ---------------------------------------------------------------------------
 constexpr int kPipeThreads = 14 * 32;
 constexpr int kStageBytes = 6 * kSlab;
@@ -1796,10 +1332,9 @@ cudaError_t make_map_f32(CUtensorMap *map, const void *ptr, int width, int seqle
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// x | B (then C) | C (then tril(G), then y) | wx ring | h hi/lo (dstate 128 only)
+// ssd_fused_tc: x | B (then C) | C (then tril(G), then y) | wx ring | h hi/lo
 size_t fused_smem(int NS)
 {
-    if (NS == 64) return 1024 + (size_t)6 * kSlab;  // ssd_fused_ov_tc: wx hi|lo (64K), B, C
     const size_t body = (size_t)(2 + NS / 64 + 2) * kSlab + 3 * 8192;  // ..., wx ring 24 KiB
     const size_t hreg = NS == 64 ? 0 : (size_t)2 * (NS / 64) * kSlab;
     return 1024 + body + hreg;
@@ -1816,10 +1351,9 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
     if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
     if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
     if ((e = make_map(&ymap, pr.y, pr.nheads * pr.headdim, pr.seqlen, pr.batch)) != cudaSuccess) return e;
-    const size_t smem = fused_smem(NS);
     const size_t units = units_of(pr);
     if ((e = cudaMemsetAsync(fa.aggcnt, 0, (2 * units + kCtrCount) * sizeof(uint32_t), s)) != cudaSuccess) return e;
-    if (NS == 64) {
+    if constexpr (NS == 64) {
         const size_t psmem = 1024 + (size_t)2 * kStageBytes + 2 * kDtBytes;
         // dt through TMA when its rows are 16-byte multiples and the base is aligned
         CUtensorMap dtmap;
@@ -1835,6 +1369,7 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
         const unsigned grid = (unsigned)std::min<size_t>(units, (size_t)nsm);
         ssd_fused_pipe_tc<<<grid, kPipeThreads, psmem, s>>>(xmap, bmap, cmap, ymap, dtmap, pr, fa, (int)units, dt_tma);
     } else {
+        const size_t smem = fused_smem(NS);
         if ((e = cudaFuncSetAttribute(ssd_fused_tc<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
             cudaSuccess)
             return e;
