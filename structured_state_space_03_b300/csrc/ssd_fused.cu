@@ -711,11 +711,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 // Per-unit scalars and the info and seg barriers have four sets (it & 3): a
 // team may still read them after its stage has been handed to the next unit.
 // ---------------------------------------------------------------------------
-constexpr int kPipeThreads = 14 * 32;
+constexpr int kPipeThreads = 16 * 32;
 constexpr int kStageBytes = 6 * kSlab;
 constexpr int kDtBytes = kRows * 4 * sizeof(float);  // dt box: 128 tokens x 4 heads
-constexpr uint32_t kParts = 4;  // an inclusive state is published when each of a team's four warps released its quarter
-enum { kWarpLoad = 0, kWarpMma = 1, kWarpFront = 2, kWarpState = 6 };
+constexpr int kSlices = kRows / 16;  // wx is built, and consumed by the MMAs, 16 tokens at a time
+enum { kWarpLoad = 0, kWarpMma = 1, kWarpFront = 2, kWarpState = 6, kWarpPub = 14 };
 enum { kBarFront = 1, kBarTeam0 = 2 };  // team 1 uses barrier 3
 
 // Named barrier over `n` threads that also returns whether any of them passed `pred`.
@@ -764,7 +764,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     // per stage (it & 1): full, free, slot, g, fr, mma, yo; per unit in flight (it & 3): info,
     // seg and the unit's scalars, which the epilogue may still read after the stage is free
     __shared__ __align__(8) uint64_t bar_info[4], bar_seg[4], bar_full[2], bar_dt[2], bar_free[2], bar_slot[2],
-        bar_lo[2], bar_g[2], bar_fr[2], bar_mma[2], bar_yo[2], bar_xe[2];
+        bar_lo[2], bar_g[2], bar_mask[2], bar_slice[2][kSlices], bar_mma[2], bar_yo[2], bar_xe[2], bar_pincl[2],
+        bar_pdone[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int s_tk[4], s_fast[4];
     __shared__ float cs[4][2 * kRows], dtv[4][2 * kRows], vw[4][2 * kRows], rs[4][2 * kRows];
@@ -794,10 +795,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             mbar_init(&bar_slot[k], 1);
             mbar_init(&bar_lo[k], 1);
             mbar_init(&bar_g[k], 1);
-            mbar_init(&bar_fr[k], 128);
+            mbar_init(&bar_mask[k], 128);
+            for (int q = 0; q < kSlices; ++q) mbar_init(&bar_slice[k][q], 128);
             mbar_init(&bar_mma[k], 1);
             mbar_init(&bar_yo[k], 1);
             mbar_init(&bar_xe[k], 1);
+            mbar_init(&bar_pincl[k], 4);
+            mbar_init(&bar_pdone[k], 1);
         }
         mbar_fence_init();
         s_fail = 0;
@@ -874,13 +878,20 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     mma_bf16(slot + col_y, sdesc_sw128(st + 5 * kSlab + ks * 32, 16, 1024),
                              sdesc_sw128(st + 4 * kSlab + ks * 32, 16, 1024), id_g, ks > 0);
                 mma_commit(&bar_g[s]);
-                if (!mbar_wait(&bar_fr[s], ph)) {
+                // tril(G) in TMEM first, then each 16-token slice of wx as the front
+                // warps finish it, so the build and the MMAs overlap
+                if (!mbar_wait(&bar_mask[s], ph)) {
                     s_fail = 1;
                     break;
                 }
-                tc_fence_after();
                 const bool fast = s_fast[ss] != 0;
+                bool okm = true;
                 for (int ks = 0; ks < kRows / 16; ++ks) {
+                    if (!mbar_wait(&bar_slice[s][ks], ph)) {
+                        okm = false;
+                        break;
+                    }
+                    tc_fence_after();
                     const uint64_t bd = sdesc_sw128(st + 4 * kSlab + ks * 2048, kSlab, 1024);
                     const uint64_t whi = sdesc_sw128(st + ks * 2048, kSlab, 1024);
                     const uint64_t wlo = sdesc_sw128(st + 2 * kSlab + ks * 2048, kSlab, 1024);
@@ -890,6 +901,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                         mma_bf16_tA(slot + col_y, slot + col_m + ks * 8, whi, id_d, ks > 0);
                         mma_bf16_tA(slot + col_y, slot + col_m + ks * 8, wlo, id_d, 1);
                     }
+                }
+                if (!okm) {
+                    s_fail = 1;
+                    break;
                 }
                 mma_commit(&bar_mma[s]);
             }
@@ -969,31 +984,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             if (ft == 0) s_fast[ss] = fast ? 1 : 0;
             mbar_arrive(&bar_seg[ss]);
             named_sync(kBarFront, 128);  // every v_j dt_j is in shared memory
-            // wx = v dt x, hi in place over x, lo at +32K
             ok = mbar_wait(&bar_full[s], ph) && (it < 2 || mbar_wait(&bar_lo[s], ph ^ 1));
-            if (ok) {
-#pragma unroll 4
-                for (int q = ft; q < 2 * kRows * 8; q += 128) {
-                    const int mb = q >> 10, j = (q >> 3) & 127, qq = q & 7;
-                    const float w = vw[ss][(P == 64 ? mb : 0) * kRows + j];
-                    uint4 *ptr = reinterpret_cast<uint4 *>(st + mb * kSlab + sw128(j, qq));
-                    const uint4 xv = *ptr;
-                    const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-                    const float2 w2 = make_float2(w, w);
-                    float f[8];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float2 t = __fmul2_rn(__bfloat1622float2(x2[k]), w2);
-                        f[2 * k] = t.x;
-                        f[2 * k + 1] = t.y;
-                    }
-                    uint4 hi, lo;
-                    split8(f, hi, lo);
-                    *ptr = hi;
-                    *reinterpret_cast<uint4 *>(st + 2 * kSlab + mb * kSlab + sw128(j, qq)) = lo;
-                }
-            }
-            fence_async_smem();
             ok = ok && mbar_wait(&bar_g[s], ph);
             tc_fence_after();
             if (ok && fast) {  // tril(G) -> bf16 pairs in TMEM (row m, columns jb*32 .. jb*32+31)
@@ -1021,10 +1012,62 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bar_fr[s]);
+            mbar_arrive(&bar_mask[s]);
+            // wx = v dt x, hi in place over x, lo at +32K, in 16-token slices: slice
+            // ks is rows 16 ks .. 16 ks + 15 of both 64-column slabs (256 chunks)
+#pragma unroll 1
+            for (int ks = 0; ks < kSlices; ++ks) {
+                if (ok) {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int idx = ft + 128 * r;
+                        const int mb = idx >> 7, j = 16 * ks + ((idx >> 3) & 15), qq = idx & 7;
+                        const float w = vw[ss][(P == 64 ? mb : 0) * kRows + j];
+                        uint4 *ptr = reinterpret_cast<uint4 *>(st + mb * kSlab + sw128(j, qq));
+                        const uint4 xv = *ptr;
+                        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                        const float2 w2 = make_float2(w, w);
+                        float f[8];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 t = __fmul2_rn(__bfloat1622float2(x2[k]), w2);
+                            f[2 * k] = t.x;
+                            f[2 * k + 1] = t.y;
+                        }
+                        uint4 hi, lo;
+                        split8(f, hi, lo);
+                        *ptr = hi;
+                        *reinterpret_cast<uint4 *>(st + 2 * kSlab + mb * kSlab + sw128(j, qq)) = lo;
+                    }
+                }
+                fence_async_smem();
+                mbar_arrive(&bar_slice[s][ks]);
+            }
             if (named_sync_or(kBarFront, 128, !ok)) {
                 s_fail = 1;
                 break;
+            }
+        }
+    } else if (warp >= kWarpPub) {
+        // ================= publishers, one per team: release a unit's inclusive state
+        // once the team's four warps have stored it, so no team warp stalls on it
+        const int team = warp - kWarpPub, s = team;
+        if (lane == 0) {
+            for (int it = team;; it += 2) {
+                const int ss = it & 3;
+                const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
+                if (!mbar_wait(&bar_info[ss], pq)) {
+                    s_fail = 1;
+                    break;
+                }
+                const int tk = s_tk[ss];
+                if (tk < 0) break;
+                if (!mbar_wait(&bar_pincl[s], ph)) {
+                    s_fail = 1;
+                    break;
+                }
+                if (!s_fail) red_release_add(fa.inclcnt + decode_unit(pr, tk, nhb).unit, 1u);
+                mbar_arrive(&bar_pdone[s]);
             }
         }
     } else {
@@ -1054,6 +1097,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             if (tk < 0) break;  // the same ticket for every thread
             const PipeUnit u = decode_unit(pr, tk, nhb);
             const int c = u.c;
+            if (it >= 2 && !mbar_wait(&bar_pdone[s], ph ^ 1)) ok = false;
             // walk back to the nearest inclusive state; -2: S_c became ready first
             // (publish it as the aggregate, then walk on); -3: gave up
             int stop = c - 1;
@@ -1067,7 +1111,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                             uint32_t f = kFlagInclusive;
                             if (k >= 0) {
                                 const size_t uk = u.unit - (c - k);
-                                f = ld_acquire(fa.inclcnt + uk) == kParts ? kFlagInclusive
+                                f = ld_acquire(fa.inclcnt + uk) != 0u ? kFlagInclusive
                                     : (ld_acquire(fa.aggcnt + uk) != 0u ? kFlagAggregate : kFlagNone);
                             }
                             const uint32_t end_mask = __ballot_sync(0xffffffffu, f == kFlagInclusive);
@@ -1119,7 +1163,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     }
                     // one release for the whole unit: the barrier orders every
                     // thread's stores before the leader's release store
-                    if (!named_sync_or(bar_team, 128, !ok) && tt == 0) st_release_flag(fa.aggcnt + u.unit);
+                    if (!named_sync_or(bar_team, 128, !ok) && tt == 32) st_release_flag(fa.aggcnt + u.unit);
                 }
             }
             // h_c for row m, in the recurrence's own order
@@ -1212,7 +1256,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 }
             }
             __syncwarp();
-            if (lane == 0 && ok) red_release_add(fa.inclcnt + u.unit, 1u);
+            if (lane == 0) mbar_arrive(&bar_pincl[s]);  // the team's publisher releases h_{c+1}
             fence_async_smem();
             tc_fence_before();
             bool any_fail = named_sync_or(bar_team, 128, !ok);
