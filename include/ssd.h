@@ -172,6 +172,36 @@ SSD_API ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float
                                      int chunk, ssd_dtype_t dtype, void *stream);
 
 /*
+ * ssd_step -- one recurrent step of the layer, the constant-size-state
+ * inference form ("深挖-Mamba", Mamba-vs-Transformer comparison table: no KV
+ * cache, only the fixed-size hidden state h_t; section "Mamba-2 (2024)":
+ * matrix form for training, recurrent form for inference).  For one new token
+ * per sequence, for every (b, h, p) with g = h / (nheads / ngroups):
+ *
+ *     a        = exp(dt[b][h] * A[h])
+ *     s[n]     = a * s[n] + dt[b][h] * x[b][h][p] * B[b][g][n]   (state, in place)
+ *     y[b][h][p] = sum_n C[b][g][n] * s[n] + D[h] * x[b][h][p]
+ *
+ * i.e. exactly ssd_fwd for seqlen 1 with init_state = final_state = state, so
+ * a chain of steps continues a prefix run by ssd_fwd (its final_state) token by
+ * token.  Device pointers:
+ *   x      [batch][nheads][headdim]            dtype
+ *   dt     [batch][nheads] fp32;  A, D [nheads] fp32 (D may be NULL: no skip)
+ *   B, C   [batch][ngroups][dstate]            dtype
+ *   state  [batch][nheads][headdim][dstate] fp32, read and overwritten
+ *   y      out [batch][nheads][headdim]        dtype (bf16: round to nearest even)
+ * y must not overlap state or any input.  The caller owns every buffer; the
+ * library keeps no pointer after the enqueued work completes.  Nothing is
+ * allocated.  Returns SSD_OK once the kernel is enqueued on `stream`;
+ * SSD_ERR_INVALID_ARG for a NULL required pointer, a dimension <= 0,
+ * nheads % ngroups != 0, an unknown dtype or a misaligned pointer;
+ * SSD_ERR_CUDA if the launch fails.
+ */
+SSD_API ssd_status_t ssd_step(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                              const float *D, float *state, void *y, int batch, int nheads, int headdim,
+                              int ngroups, int dstate, ssd_dtype_t dtype, void *stream);
+
+/*
  * ssd_fwd_path -- the kernel family ssd_fwd would run for these sizes
  * (SSD_PATH_NONE when they are rejected).  Pure host function: no CUDA call.
  */

@@ -4,7 +4,7 @@ Thin ctypes marshalling over the C ABI declared in ``include/ssd.h``; every
 step of the computation runs in the library's CUDA kernels.  PyTorch is used
 for device memory and streams only.  The functions carry the C names:
 
-    ssd_fwd, ssd_fwd_ws, ssd_fwd_host, ssd_fwd_workspace_size, ssd_fwd_path,
+    ssd_fwd, ssd_fwd_ws, ssd_fwd_host, ssd_fwd_workspace_size, ssd_fwd_path, ssd_step,
     ssd_check_device_status, ssd_status_string, ssd_last_error_detail, ssd_version
 
 Layouts: x, y [batch, seqlen, nheads, headdim]; dt [batch, seqlen, nheads];
@@ -41,6 +41,7 @@ SIGNATURES = {
     "ssd_fwd_ws": (_I, _FWD + [_P, _S, _P]),
     "ssd_fwd_host": (_I, _FWD + [_P]),
     "ssd_fwd_noalloc": (_I, _FWD + [_P]),
+    "ssd_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ssd_fwd_workspace_size": (_I, _DIMS + [ctypes.POINTER(ctypes.c_size_t)]),
     "ssd_fwd_path": (_I, _DIMS),
     "ssd_fwd_kernels": (_I, _DIMS + [ctypes.c_char_p, _S]),
@@ -186,6 +187,36 @@ def ssd_fwd_noalloc(x, dt, A, B, C, D=None, init_state=None, *, chunk: int, y=No
                                  _ptr(y), _ptr(final_state), b, L, H, P, G, N, chunk, _dtype_code(x.dtype),
                                  _stream_handle(stream)))
     return y, final_state
+
+
+def ssd_step(x, dt, A, B, C, D=None, *, state, y=None, stream=None):
+    """One recurrent step for one new token per sequence on CUDA tensors.
+
+    x [batch, nheads, headdim]; dt [batch, nheads] float32; A, D [nheads]
+    float32; B, C [batch, ngroups, dstate]; ``state`` [batch, nheads, headdim,
+    dstate] float32 is updated in place.  x, B, C, y share one dtype.  Returns y.
+    """
+    if x.dim() != 3 or B.dim() != 3:
+        raise ValueError("x must be [batch, nheads, headdim] and B, C [batch, ngroups, dstate]")
+    b, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    el = x.dtype
+    for name, t, shape, dtype in (("dt", dt, (b, H), torch.float32), ("A", A, (H,), torch.float32),
+                                  ("B", B, (b, G, N), el), ("C", C, (b, G, N), el), ("D", D, (H,), torch.float32),
+                                  ("state", state, (b, H, P, N), torch.float32)):
+        if t is None:
+            continue
+        if tuple(t.shape) != shape or t.dtype != dtype or not t.is_contiguous() or t.device.type != "cuda":
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor of shape {shape}")
+    if not x.is_contiguous() or x.device.type != "cuda":
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if y is None:
+        y = torch.empty_like(x)
+    elif y.shape != x.shape or y.dtype != el or not y.is_contiguous():
+        raise ValueError("y must be a contiguous tensor like x")
+    _check(lib().ssd_step(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state), _ptr(y), b, H, P, G, N,
+                          _dtype_code(el), _stream_handle(stream)))
+    return y
 
 
 def ssd_fwd_workspace_size(batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype) -> int:

@@ -400,6 +400,28 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
     return ssd_check_device_status(stream);
 }
 
+ssd_status_t ssd_step(const void *x, const float *dt, const float *A, const void *B, const void *C, const float *D,
+                      float *state, void *y, int batch, int nheads, int headdim, int ngroups, int dstate,
+                      ssd_dtype_t dtype, void *stream)
+{
+    if (batch <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0)
+        return fail(SSD_ERR_INVALID_ARG, "every dimension must be positive (batch=%d nheads=%d headdim=%d ngroups=%d "
+                    "dstate=%d)", batch, nheads, headdim, ngroups, dstate);
+    if (nheads % ngroups != 0)
+        return fail(SSD_ERR_INVALID_ARG, "nheads (%d) must be a multiple of ngroups (%d)", nheads, ngroups);
+    if (dtype != SSD_DTYPE_F32 && dtype != SSD_DTYPE_BF16) return fail(SSD_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (!x || !dt || !A || !B || !C || !state || !y)
+        return fail(SSD_ERR_INVALID_ARG, "x, dt, A, B, C, state and y must be non-NULL");
+    const size_t el = dtype == SSD_DTYPE_BF16 ? 2 : 4;
+    if (!aligned(x, el) || !aligned(B, el) || !aligned(C, el) || !aligned(y, el) || !aligned(dt, 4) ||
+        !aligned(A, 4) || (D && !aligned(D, 4)) || !aligned(state, 4))
+        return fail(SSD_ERR_INVALID_ARG, "pointers must be aligned to their element size");
+    const cudaError_t e = launch_step(x, dt, A, B, C, D, state, y, batch, nheads, headdim, ngroups, dstate, dtype,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "ssd_step launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 ssd_status_t ssd_check_device_status(void *stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -110,4 +110,9 @@ __device__ __forceinline__ float block_inclusive_scan_256(float v, float *warp_t
     return v;
 }
 
+// One recurrent step (ssd_step.cu): state [batch][nheads][headdim][dstate] fp32 in place.
+cudaError_t launch_step(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                        const float *D, float *state, void *y, int batch, int nheads, int headdim, int ngroups,
+                        int dstate, ssd_dtype_t dtype, cudaStream_t s);
+
 }  // namespace ssd

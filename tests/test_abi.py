@@ -136,3 +136,31 @@ def test_path_selection_is_a_pure_host_query(lib):
     assert ssd.ssd_fwd_kernels(16, 4096, 32, 128, 8, 128, 128, ssd.SSD_DTYPE_BF16) == ["ssd_fused_tc"]
     assert ssd.ssd_fwd_kernels(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == [
         "chunk_state_tc", "state_pass", "chunk_out_tc"]
+
+
+def _step(lib, x=1, dt=1, A=1, B=1, C=1, state=1, y=1, **over):
+    d = dict(batch=2, nheads=8, headdim=64, ngroups=2, dstate=64, dtype=ssd.SSD_DTYPE_BF16)
+    d.update(over)
+    p = lambda v: ctypes.c_void_p(v * 4096) if v else None
+    return lib.ssd_step(p(x), p(dt), p(A), p(B), p(C), None, p(state), p(y), d["batch"], d["nheads"], d["headdim"],
+                        d["ngroups"], d["dstate"], d["dtype"], None)
+
+
+@pytest.mark.parametrize("missing", ["x", "dt", "A", "B", "C", "state", "y"])
+def test_step_null_pointer_is_invalid(lib, missing):
+    assert _step(lib, **{missing: 0}) == ssd.SSD_ERR_INVALID_ARG
+    assert "non-NULL" in ssd.ssd_last_error_detail()
+
+
+@pytest.mark.parametrize("field", ["batch", "nheads", "headdim", "ngroups", "dstate"])
+def test_step_nonpositive_dimension_is_invalid(lib, field):
+    assert _step(lib, **{field: 0}) == ssd.SSD_ERR_INVALID_ARG
+
+
+def test_step_groups_dtype_and_alignment(lib):
+    assert _step(lib, ngroups=3) == ssd.SSD_ERR_INVALID_ARG
+    assert _step(lib, dtype=9) == ssd.SSD_ERR_INVALID_ARG
+    st = lib.ssd_step(ctypes.c_void_p(4097), ctypes.c_void_p(4096), ctypes.c_void_p(4096), ctypes.c_void_p(4096),
+                      ctypes.c_void_p(4096), None, ctypes.c_void_p(4096), ctypes.c_void_p(8192), 1, 2, 4, 1, 8,
+                      ssd.SSD_DTYPE_BF16, None)
+    assert st == ssd.SSD_ERR_INVALID_ARG and "aligned" in ssd.ssd_last_error_detail()
