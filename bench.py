@@ -208,7 +208,7 @@ def decode_step_measurement(dev, peaks, stream, batch=64, steps=400):
     dt = (torch.rand(batch, H, generator=gen) * 0.099 + 0.001).to(dev)
     A = -torch.exp(torch.rand(H, generator=gen) * math.log(16.0)).to(dev)
     D = torch.randn(H, generator=gen).to(dev)
-    states = [torch.randn(batch, H, P, N, generator=gen).to(dev) * 0.1 for _ in range(2)]
+    states = [(torch.randn(batch, H, P, N, generator=gen) * 0.1).to(dev) for _ in range(2)]
     y = torch.empty_like(x)
     for k in range(10):
         ssd.ssd_step(x, dt, A, B, C, D, state=states[k % 2], y=y, stream=stream)
