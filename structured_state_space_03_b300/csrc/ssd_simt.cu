@@ -227,11 +227,26 @@ __global__ void __launch_bounds__(kThreads) state_pass(Problem pr, Workspace ws)
     float st = pr.init_state ? pr.init_state[bh * PN + e] : 0.f;
     float *s = ws.states + bh * pr.nchunks * (size_t)PN + e;
     const float *dec = ws.decay + bh * pr.nchunks;
-#pragma unroll 4
-    for (int c = 0; c < pr.nchunks; ++c) {
-        const float sc = s[(size_t)c * PN];
-        s[(size_t)c * PN] = st;
-        st = fmaf(__ldg(dec + c), st, sc);
+    // kAhead chunk states are loaded before any is overwritten, so each thread
+    // keeps kAhead independent loads in flight instead of one per chunk
+    constexpr int kAhead = 16;
+    const int nc = pr.nchunks;
+    for (int c0 = 0; c0 < nc; c0 += kAhead) {
+        float sc[kAhead], dk[kAhead];
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k) {
+            if (c0 + k < nc) {
+                sc[k] = s[(size_t)(c0 + k) * PN];
+                dk[k] = __ldg(dec + c0 + k);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k) {
+            if (c0 + k < nc) {
+                s[(size_t)(c0 + k) * PN] = st;
+                st = fmaf(dk[k], st, sc[k]);
+            }
+        }
     }
     if (pr.final_state) pr.final_state[bh * PN + e] = st;
 }
