@@ -47,6 +47,8 @@ MID = [
     (1, 600, 4, 64, 256, 1, 256, "bf16"),
     (2, 513, 8, 128, 128, 2, 128, "bf16"),
     (1, 300, 4, 64, 64, 4, 64, "bf16"),
+    (2, 600, 4, 128, 64, 2, 128, "bf16"),     # persistent kernel, one head per unit, ragged tail
+    (1, 700, 6, 64, 64, 3, 96, "bf16"),       # persistent kernel, nheads % 4 != 0 (dt without TMA), chunk 96
     (2, 333, 6, 32, 48, 3, 100, "f32"),
     (1, 1000, 4, 16, 16, 1, 64, "f32"),
 ]
