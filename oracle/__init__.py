@@ -52,6 +52,9 @@ def _bind(lib):
     common = [p, p, p, p, p, p, p, ctypes.c_int, L, L, L, L, L, L]
     lib.oracle_ssd_recurrence.argtypes = common + [p, L, p, p, ctypes.c_int]
     lib.oracle_ssd_recurrence.restype = ctypes.c_int
+    if hasattr(lib, "oracle_ssd_recurrence_pre"):
+        lib.oracle_ssd_recurrence_pre.argtypes = [p, p, p, ctypes.c_int] + common[2:] + [p, L, p, p, ctypes.c_int]
+        lib.oracle_ssd_recurrence_pre.restype = ctypes.c_int
     for name in ("oracle_ssd_quadratic", "oracle_ssd_assoc_scan"):
         fn = getattr(lib, name)
         fn.argtypes = common + [p, p]
@@ -187,4 +190,37 @@ def recurrence_with(lib, x, dt, A, B, C, D=None, init_state=None):
                                    None, nrows, _ptr(y), _ptr(fin), 1)
     if rc != 0:
         raise RuntimeError(f"oracle_ssd_recurrence failed with {rc}")
+    return (y.reshape(b, H, P, L).transpose(0, 3, 1, 2).copy(), fin.reshape(b, H, P, N))
+
+
+PRE_SOFTPLUS, PRE_ZOH = 1, 2
+
+
+def recurrence_pre(x, dt, A, B, C, D=None, init_state=None, dt_bias=None, softplus=False, zoh=False, rows=None,
+                   nthreads=None, lib=None):
+    """O1 with the pre-step of dt: d = dt + dt_bias, through a softplus when
+    ``softplus``, decay exp(d A), and the input scale (exp(d A) - 1) / A when
+    ``zoh`` (d otherwise).  Same returns as ``recurrence``."""
+    arrs, xd, (b, L, H, P, G, N) = _prepare(x, dt, A, B, C, D, init_state)
+    xa, dta, Aa, Ba, Ca, Da, ia = arrs
+    ba = None if dt_bias is None else _as_input(dt_bias, "dt_bias", False)[0]
+    if ba is not None and ba.shape != (H,):
+        raise ValueError("dt_bias must be [H]")
+    lib = lib or load_library()
+    if rows is None:
+        nrows = b * H * P
+        ra = None
+    else:
+        ra = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = ra.shape[0]
+    y = np.empty((nrows, L), np.float64)
+    fin = np.empty((nrows, N), np.float64)
+    flags = (PRE_SOFTPLUS if softplus else 0) | (PRE_ZOH if zoh else 0)
+    rc = lib.oracle_ssd_recurrence_pre(_ptr(xa), _ptr(dta), _ptr(ba), flags, _ptr(Aa), _ptr(Ba), _ptr(Ca),
+                                       _ptr(Da), _ptr(ia), xd, b, L, H, P, G, N, _ptr(ra), nrows, _ptr(y),
+                                       _ptr(fin), int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_ssd_recurrence_pre failed with {rc}")
+    if rows is not None:
+        return y, fin
     return (y.reshape(b, H, P, L).transpose(0, 3, 1, 2).copy(), fin.reshape(b, H, P, N))

@@ -29,6 +29,15 @@
  *   - "Mamba 模型" §3.4 (parallel associative scan, used by
  *     oracle_ssd_assoc_scan as an independent evaluation order).
  *
+ * oracle_ssd_recurrence_pre adds the per-(token, head) pre-step of the scalar
+ * inputs, from the same discretisation ("Mamba模型：线性复杂度序列建模的革命性突破"
+ * §2.2 and "Mamba 模型" §2.3.1: zero-order hold Bbar = (dt A)^-1 (exp(dt A) - 1)
+ * dt B; §3.2 of the first page: dt through a softplus):
+ *     d_t   = dt_t + dt_bias[h]        (dt_bias may be NULL => 0)
+ *     d_t   = log(1 + exp(d_t))        if ORACLE_PRE_SOFTPLUS
+ *     s_t   = exp(d_t A) s_{t-1} + u_t x_t B_t
+ *     u_t   = (exp(d_t A) - 1) / A     if ORACLE_PRE_ZOH (d_t when A = 0), else d_t
+ *
  * Layouts (row-major, the same as the CUDA library's public ABI):
  *   x, y   [batch][seqlen][nheads][headdim]
  *   dt     [batch][seqlen][nheads]           fp32
@@ -50,6 +59,8 @@
 
 #define ORACLE_IN_F32 0
 #define ORACLE_IN_BF16 1
+#define ORACLE_PRE_SOFTPLUS 1
+#define ORACLE_PRE_ZOH 2
 
 typedef struct {
     const void *x;
@@ -58,6 +69,8 @@ typedef struct {
     const float *D, *init;
     int in_dtype;
     long batch, seqlen, nheads, headdim, ngroups, dstate;
+    const float *dt_bias;  /* pre-step (oracle_ssd_recurrence_pre only) */
+    int pre_flags;
 } oracle_problem;
 
 /* Widen one stored input element to fp64 (exact for both fp32 and bf16). */
@@ -127,6 +140,40 @@ static void recurrence_row(const oracle_problem *pr, long r, double *s, double *
             final_row[n] = s[n];
 }
 
+/* The same recurrence with the pre-step of the scalar inputs (see the header). */
+static void recurrence_row_pre(const oracle_problem *pr, long r, double *s, double *y_row, double *final_row)
+{
+    long b, h, p, g;
+    row_coords(pr, r, &b, &h, &p, &g);
+    const long L = pr->seqlen, H = pr->nheads, P = pr->headdim, G = pr->ngroups, N = pr->dstate;
+    const double A_h = (double)pr->A[h];
+    const double D_h = pr->D ? (double)pr->D[h] : 0.0;
+    const double bias = pr->dt_bias ? (double)pr->dt_bias[h] : 0.0;
+
+    for (long n = 0; n < N; ++n)
+        s[n] = pr->init ? (double)pr->init[((b * H + h) * P + p) * N + n] : 0.0;
+
+    for (long t = 0; t < L; ++t) {
+        double d = (double)pr->dt[(b * L + t) * H + h] + bias;
+        if (pr->pre_flags & ORACLE_PRE_SOFTPLUS)
+            d = log(1.0 + exp(d));
+        const double decay = exp(d * A_h);
+        const double u = (pr->pre_flags & ORACLE_PRE_ZOH) ? (A_h != 0.0 ? (decay - 1.0) / A_h : d) : d;
+        const double x_t = widen(pr->x, ((b * L + t) * H + h) * P + p, pr->in_dtype);
+        const long bc = ((b * L + t) * G + g) * N;
+        double acc = 0.0;
+        for (long n = 0; n < N; ++n) {
+            s[n] = decay * s[n] + u * x_t * widen(pr->B, bc + n, pr->in_dtype);
+            acc += widen(pr->C, bc + n, pr->in_dtype) * s[n];
+        }
+        if (y_row)
+            y_row[t] = acc + D_h * x_t;
+    }
+    if (final_row)
+        for (long n = 0; n < N; ++n)
+            final_row[n] = s[n];
+}
+
 typedef struct {
     const oracle_problem *pr;
     const long *rows;
@@ -149,7 +196,7 @@ static void *recurrence_worker(void *arg)
         if (i >= job->nrows)
             break;
         long r = job->rows ? job->rows[i] : i;
-        recurrence_row(job->pr, r, s,
+        (job->pr->dt_bias || job->pr->pre_flags ? recurrence_row_pre : recurrence_row)(job->pr, r, s,
                        job->y_rows ? job->y_rows + i * job->pr->seqlen : NULL,
                        job->final_rows ? job->final_rows + i * job->pr->dstate : NULL);
     }
@@ -161,12 +208,37 @@ static void *recurrence_worker(void *arg)
  * Sequential fp64 recurrence for the rows listed in `rows` (all rows, in
  * order, when rows == NULL), threaded over rows with `nthreads` workers.
  */
+static int run_recurrence(const oracle_problem *prp, const long *rows, long nrows, double *y_rows,
+                          double *final_rows, int nthreads);
+
 int oracle_ssd_recurrence(const void *x, const float *dt, const float *A, const void *B, const void *C,
                           const float *D, const float *init_state, int in_dtype, long batch, long seqlen,
                           long nheads, long headdim, long ngroups, long dstate, const long *rows, long nrows,
                           double *y_rows, double *final_rows, int nthreads)
 {
-    oracle_problem pr = {x, dt, A, B, C, D, init_state, in_dtype, batch, seqlen, nheads, headdim, ngroups, dstate};
+    oracle_problem pr = {x, dt, A, B, C, D, init_state, in_dtype, batch, seqlen, nheads, headdim, ngroups, dstate,
+                         NULL, 0};
+    return run_recurrence(&pr, rows, nrows, y_rows, final_rows, nthreads);
+}
+
+/* The recurrence with the pre-step of dt (flags ORACLE_PRE_SOFTPLUS, ORACLE_PRE_ZOH). */
+int oracle_ssd_recurrence_pre(const void *x, const float *dt, const float *dt_bias, int pre_flags, const float *A,
+                              const void *B, const void *C, const float *D, const float *init_state, int in_dtype,
+                              long batch, long seqlen, long nheads, long headdim, long ngroups, long dstate,
+                              const long *rows, long nrows, double *y_rows, double *final_rows, int nthreads)
+{
+    if (pre_flags & ~(ORACLE_PRE_SOFTPLUS | ORACLE_PRE_ZOH))
+        return -1;
+    oracle_problem pr = {x, dt, A, B, C, D, init_state, in_dtype, batch, seqlen, nheads, headdim, ngroups, dstate,
+                         dt_bias, pre_flags};
+    return run_recurrence(&pr, rows, nrows, y_rows, final_rows, nthreads);
+}
+
+static int run_recurrence(const oracle_problem *prp, const long *rows, long nrows, double *y_rows,
+                          double *final_rows, int nthreads)
+{
+    const oracle_problem pr = *prp;
+    const long batch = pr.batch, nheads = pr.nheads, headdim = pr.headdim;
     if (check_problem(&pr))
         return -1;
     const long total = batch * nheads * headdim;
@@ -222,7 +294,8 @@ int oracle_ssd_quadratic(const void *x, const float *dt, const float *A, const v
                          long nheads, long headdim, long ngroups, long dstate, double *y_rows,
                          double *final_rows)
 {
-    oracle_problem pr = {x, dt, A, B, C, D, init_state, in_dtype, batch, seqlen, nheads, headdim, ngroups, dstate};
+    oracle_problem pr = {x, dt, A, B, C, D, init_state, in_dtype, batch, seqlen, nheads, headdim, ngroups, dstate,
+                         NULL, 0};
     if (check_problem(&pr))
         return -1;
     const long L = seqlen, H = nheads, P = headdim, G = ngroups, N = dstate;
@@ -303,7 +376,8 @@ int oracle_ssd_assoc_scan(const void *x, const float *dt, const float *A, const 
                           long nheads, long headdim, long ngroups, long dstate, double *y_rows,
                           double *final_rows)
 {
-    oracle_problem pr = {x, dt, A, B, C, D, init_state, in_dtype, batch, seqlen, nheads, headdim, ngroups, dstate};
+    oracle_problem pr = {x, dt, A, B, C, D, init_state, in_dtype, batch, seqlen, nheads, headdim, ngroups, dstate,
+                         NULL, 0};
     if (check_problem(&pr))
         return -1;
     const long L = seqlen, H = nheads, P = headdim, G = ngroups, N = dstate;
