@@ -151,7 +151,7 @@ static void recurrence_row_pre(const oracle_problem *pr, long r, double *s, doub
     const double bias = pr->dt_bias ? (double)pr->dt_bias[h] : 0.0;
 
     for (long n = 0; n < N; ++n)
-        s[n] = pr->init ? (double)pr->init[((b * H + h) * P + p) * N + n] : 0.0;
+        s[n] = pr->init ? (double)pr->init[(((b * H + h) * P + p) * N) + n] : 0.0;
 
     for (long t = 0; t < L; ++t) {
         double d = (double)pr->dt[(b * L + t) * H + h] + bias;
@@ -159,7 +159,7 @@ static void recurrence_row_pre(const oracle_problem *pr, long r, double *s, doub
             d = log(1.0 + exp(d));
         const double decay = exp(d * A_h);
         const double u = (pr->pre_flags & ORACLE_PRE_ZOH) ? (A_h != 0.0 ? (decay - 1.0) / A_h : d) : d;
-        const double x_t = widen(pr->x, ((b * L + t) * H + h) * P + p, pr->in_dtype);
+        const double x_t = widen(pr->x, (b * L + t) * H * P + h * P + p, pr->in_dtype);
         const long bc = ((b * L + t) * G + g) * N;
         double acc = 0.0;
         for (long n = 0; n < N; ++n) {
@@ -167,11 +167,11 @@ static void recurrence_row_pre(const oracle_problem *pr, long r, double *s, doub
             acc += widen(pr->C, bc + n, pr->in_dtype) * s[n];
         }
         if (y_row)
-            y_row[t] = acc + D_h * x_t;
+            y_row[t] = D_h * x_t + acc;
     }
     if (final_row)
         for (long n = 0; n < N; ++n)
-            final_row[n] = s[n];
+            final_row[n] = s[n];  /* the state after the last token */
 }
 
 typedef struct {
