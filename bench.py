@@ -229,6 +229,43 @@ def decode_step_measurement(dev, peaks, stream, batch=64, steps=400):
             "l2": "two state sets of 84 MB alternate (> 126 MB L2)"}
 
 
+def pre_step_measurement(sets, w, stream, steps=100):
+    """The headline forward through ssd_fwd_pre (softplus of dt + bias and the
+    zero-order-hold input scale, applied on the device) against ssd_fwd on the
+    same inputs; both allocate their workspace per call the same way."""
+    import structured_state_space_03_b300 as ssd
+    dev = sets[0]["x"].device
+    bias = torch.full((w.nheads,), -1.0, device=dev)
+
+    def timed(fn):
+        for k in range(5):
+            fn(k)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for k in range(steps):
+            fn(k)
+        e.record(stream)
+        torch.cuda.synchronize()
+        ssd.ssd_check_device_status(stream)
+        return s.elapsed_time(e) / steps * 1e3
+
+    def plain(k):
+        d = sets[k % len(sets)]
+        ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], chunk=w.chunk, y=d["y"],
+                    final_state=d["final"], stream=stream)
+
+    def pre(k):
+        d = sets[k % len(sets)]
+        ssd.ssd_fwd_pre(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], chunk=w.chunk,
+                        dt_bias=bias, softplus=True, zoh=True, y=d["y"], final_state=d["final"], stream=stream)
+
+    t_plain, t_pre = timed(plain), timed(pre)
+    return {"workload": w.name, "modes": "softplus(dt + bias), zero-order hold", "us_per_step_ssd_fwd": t_plain,
+            "us_per_step_ssd_fwd_pre": t_pre, "overhead_us": t_pre - t_plain,
+            "tokens_per_s": w.tokens / (t_pre * 1e-6), "kernels": ["pre_kernel", "ssd_fused_pipe_tc"]}
+
+
 def time_oracle(w, inp, seconds, cores):
     """Run the oracle over growing row batches until `seconds` elapse or every
     row is done; returns (tokens/s equivalent, rows done, elapsed)."""
@@ -452,6 +489,8 @@ def main():
     }
     if rank == 0 and world == 1:
         line["decode_step"] = decode_step_measurement(dev, peaks, stream)
+        if w is wl.HEADLINE:
+            line["pre_step"] = pre_step_measurement(sets, w, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
     if rank == 0:

@@ -171,6 +171,35 @@ SSD_API ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float
                                      int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
                                      int chunk, ssd_dtype_t dtype, void *stream);
 
+/* Pre-step flags of ssd_fwd_pre. */
+enum { SSD_PRE_SOFTPLUS = 1, SSD_PRE_ZOH = 2 };
+
+/*
+ * ssd_fwd_pre -- ssd_fwd with the per-(token, head) pre-step of its scalar
+ * inputs applied on the device first.  The discretisation of the pages
+ * ("Mamba模型：线性复杂度序列建模的革命性突破" §2.2, "Mamba 模型" §2.3.1: zero-order
+ * hold, Abar = exp(dt A), Bbar = (dt A)^-1 (exp(dt A) - 1) dt B; §3.2 of the
+ * first page: dt comes out of a softplus) gives, for a scalar A per head:
+ *
+ *     dt_eff[b][t][h] = softplus(dt + dt_bias[h])   if pre_flags & SSD_PRE_SOFTPLUS
+ *                       dt + dt_bias[h]              otherwise (dt_bias NULL => 0)
+ *     decay           = exp(dt_eff A[h])
+ *     input scale     = expm1(dt_eff A[h]) / A[h]    if pre_flags & SSD_PRE_ZOH (dt_eff when A[h] = 0)
+ *                       dt_eff                       otherwise (the SSD layer's dt B)
+ *
+ *     h_t = decay_t h_{t-1} + scale_t x_t B_t,   y_t = C_t . h_t + D x_t
+ *
+ * With dt_bias NULL and pre_flags 0 it is ssd_fwd.  dt_bias is [nheads] fp32
+ * device memory or NULL; every other argument, layout, ownership rule and error
+ * is that of ssd_fwd (the workspace, which also holds dt_eff and the scale,
+ * comes from the stream-ordered allocator).  SSD_ERR_INVALID_ARG also for
+ * unknown pre_flags bits or a misaligned dt_bias.
+ */
+SSD_API ssd_status_t ssd_fwd_pre(const void *x, const float *dt, const float *dt_bias, int pre_flags, const float *A,
+                                 const void *B, const void *C, const float *D, const float *init_state, void *y,
+                                 float *final_state, int batch, int seqlen, int nheads, int headdim, int ngroups,
+                                 int dstate, int chunk, ssd_dtype_t dtype, void *stream);
+
 /*
  * ssd_step -- one recurrent step of the layer, the constant-size-state
  * inference form ("深挖-Mamba", Mamba-vs-Transformer comparison table: no KV

@@ -4,7 +4,7 @@ Thin ctypes marshalling over the C ABI declared in ``include/ssd.h``; every
 step of the computation runs in the library's CUDA kernels.  PyTorch is used
 for device memory and streams only.  The functions carry the C names:
 
-    ssd_fwd, ssd_fwd_ws, ssd_fwd_host, ssd_fwd_workspace_size, ssd_fwd_path, ssd_step,
+    ssd_fwd, ssd_fwd_ws, ssd_fwd_host, ssd_fwd_pre, ssd_fwd_workspace_size, ssd_fwd_path, ssd_step,
     ssd_check_device_status, ssd_status_string, ssd_last_error_detail, ssd_version
 
 Layouts: x, y [batch, seqlen, nheads, headdim]; dt [batch, seqlen, nheads];
@@ -28,6 +28,7 @@ LIB_PATH = os.path.join(_PKG, "libssd.so")
 
 SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_NO_MEMORY, SSD_ERR_TIMEOUT = range(6)
 SSD_DTYPE_F32, SSD_DTYPE_BF16 = 0, 1
+SSD_PRE_SOFTPLUS, SSD_PRE_ZOH = 1, 2
 SSD_PATH_NONE, SSD_PATH_SIMT, SSD_PATH_TCGEN05, SSD_PATH_TCGEN05_FUSED = -1, 0, 1, 2
 PATH_NAMES = {SSD_PATH_NONE: "none", SSD_PATH_SIMT: "simt", SSD_PATH_TCGEN05: "tcgen05",
               SSD_PATH_TCGEN05_FUSED: "tcgen05_fused"}
@@ -42,6 +43,7 @@ SIGNATURES = {
     "ssd_fwd_host": (_I, _FWD + [_P]),
     "ssd_fwd_noalloc": (_I, _FWD + [_P]),
     "ssd_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "ssd_fwd_pre": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "ssd_fwd_workspace_size": (_I, _DIMS + [ctypes.POINTER(ctypes.c_size_t)]),
     "ssd_fwd_path": (_I, _DIMS),
     "ssd_fwd_kernels": (_I, _DIMS + [ctypes.c_char_p, _S]),
@@ -186,6 +188,23 @@ def ssd_fwd_noalloc(x, dt, A, B, C, D=None, init_state=None, *, chunk: int, y=No
     _check(lib().ssd_fwd_noalloc(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state),
                                  _ptr(y), _ptr(final_state), b, L, H, P, G, N, chunk, _dtype_code(x.dtype),
                                  _stream_handle(stream)))
+    return y, final_state
+
+
+def ssd_fwd_pre(x, dt, A, B, C, D=None, init_state=None, *, chunk: int, dt_bias=None, softplus: bool = False,
+                zoh: bool = False, y=None, final_state=None, return_final: bool = True, stream=None):
+    """ssd_fwd with the device-side pre-step of dt: dt_eff = softplus(dt + dt_bias)
+    (``softplus``) or dt + dt_bias, and the zero-order-hold input scale
+    expm1(dt_eff A) / A in place of dt_eff (``zoh``)."""
+    b, L, H, P, G, N = _validate(x, dt, A, B, C, D, init_state, "cuda")
+    if dt_bias is not None and (tuple(dt_bias.shape) != (H,) or dt_bias.dtype != torch.float32
+                                or not dt_bias.is_contiguous() or dt_bias.device.type != "cuda"):
+        raise ValueError(f"dt_bias must be a contiguous CUDA float32 tensor of shape ({H},)")
+    y, final_state = _outputs(x, b, H, P, N, y, final_state, return_final)
+    flags = (SSD_PRE_SOFTPLUS if softplus else 0) | (SSD_PRE_ZOH if zoh else 0)
+    _check(lib().ssd_fwd_pre(_ptr(x), _ptr(dt), _ptr(dt_bias), flags, _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                             _ptr(init_state), _ptr(y), _ptr(final_state), b, L, H, P, G, N, chunk,
+                             _dtype_code(x.dtype), _stream_handle(stream)))
     return y, final_state
 
 

@@ -284,6 +284,46 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
     return st;
 }
 
+ssd_status_t ssd_fwd_pre(const void *x, const float *dt, const float *dt_bias, int pre_flags, const float *A,
+                         const void *B, const void *C, const float *D, const float *init_state, void *y,
+                         float *final_state, int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                         int chunk, ssd_dtype_t dtype, void *stream)
+{
+    if (pre_flags & ~(SSD_PRE_SOFTPLUS | SSD_PRE_ZOH)) return fail(SSD_ERR_INVALID_ARG, "unknown pre_flags 0x%x", pre_flags);
+    if (dt_bias && !aligned(dt_bias, 4)) return fail(SSD_ERR_INVALID_ARG, "dt_bias must be 4-byte aligned");
+    Problem pr;
+    ssd_status_t st = make_problem(pr, x, dt, A, B, C, D, init_state, y, final_state, batch, seqlen, nheads,
+                                   headdim, ngroups, dstate, chunk, dtype);
+    if (st != SSD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t main_bytes = (workspace_bytes(pr) + 255) / 256 * 256;
+    const size_t n = (size_t)batch * seqlen * nheads;
+    const size_t col = (n * sizeof(float) + 255) / 256 * 256;
+    const bool zoh = (pre_flags & SSD_PRE_ZOH) != 0;
+    const size_t need = main_bytes + col * (zoh ? 2 : 1);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(e == cudaErrorMemoryAllocation ? SSD_ERR_NO_MEMORY : SSD_ERR_CUDA,
+                    "workspace allocation of %zu bytes failed: %s", need, cudaGetErrorString(e));
+    }
+    float *dt_eff = reinterpret_cast<float *>(static_cast<char *>(ws) + main_bytes);
+    float *scale = zoh ? reinterpret_cast<float *>(static_cast<char *>(ws) + main_bytes + col) : nullptr;
+    e = launch_pre(dt, dt_bias, A, pre_flags, dt_eff, scale, batch, seqlen, nheads, s);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(ws, s);
+        return fail(SSD_ERR_CUDA, "pre-step launch failed: %s", cudaGetErrorString(e));
+    }
+    pr.dt = dt_eff;
+    pr.dtin = scale;
+    st = run(pr, ws, s);
+    e = cudaFreeAsync(ws, s);
+    if (st == SSD_OK && e != cudaSuccess)
+        return fail(SSD_ERR_CUDA, "workspace release failed: %s", cudaGetErrorString(e));
+    return st;
+}
+
 // ---------------------------------------------------------------------------
 // Forward without any allocation, for callers that may not allocate device
 // memory: processes whose device memory is handed in full to a framework-owned

@@ -293,6 +293,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool active = hh < HB;
         const float a = active ? __ldg(pr.A + h0 + hh) : 0.f;
         const float d = (active && t < len) ? __ldg(pr.dt + ((size_t)b * L + t0 + t) * H + h0 + hh) : 0.f;
+        const float din =  // input scale
+            pr.dtin ? ((active && t < len) ? __ldg(pr.dtin + ((size_t)b * L + t0 + t) * H + h0 + hh) : 0.f) : d;
         float v = d * a;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             warp_mx[warp] = mx;
         }
         cs[hh * kRows + t] = v;
-        dtv[hh * kRows + t] = d;
+        dtv[hh * kRows + t] = din;
         __syncthreads();
         float lo_[2], hi_[2];
 #pragma unroll
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float ref = 0.5f * ((hh == 0 ? lo_[0] : lo_[1]) + (hh == 0 ? hi_[0] : hi_[1]));
         const float refw = fast ? ref : cl, refy = fast ? ref : 0.f;
         if (active) {
-            vw[hh * kRows + t] = t < len ? expf(refw - v) * d : 0.f;
+            vw[hh * kRows + t] = t < len ? expf(refw - v) * din : 0.f;
             rs[hh * kRows + t] = expf(v - refy);
             if (t == 0) {
                 s_alpha[hh] = expf(cl);
@@ -926,7 +928,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             uint8_t *st = base + s * kStageBytes;
             const float *dts = reinterpret_cast<const float *>(base + 2 * kStageBytes + s * kDtBytes) + ft * 4 + (u.h0 & 3);
             if (dt_tma) ok = ok && mbar_wait(&bar_dt[s], ph);
-            float v[2], d[2];
+            float v[2], d[2], din[2];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const bool act = hh < HB;
@@ -934,6 +936,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 d[hh] = (act && ft < u.len)
                             ? (dt_tma ? dts[hh] : __ldg(pr.dt + ((size_t)u.b * L + u.t0 + ft) * H + u.h0 + hh))
                             : 0.f;
+                din[hh] = pr.dtin ? ((act && ft < u.len) ? __ldg(pr.dtin + ((size_t)u.b * L + u.t0 + ft) * H + u.h0 + hh) : 0.f)
+                                  : d[hh];  // input scale
                 v[hh] = d[hh] * a;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -957,7 +961,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     wmx[fw][hh] = mx;
                 }
                 cs[ss][hh * kRows + ft] = v[hh];
-                dtv[ss][hh * kRows + ft] = d[hh];
+                dtv[ss][hh * kRows + ft] = din[hh];
             }
             named_sync(kBarFront, 128);
             float lo_[2], hi_[2];
@@ -973,7 +977,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 const float cl = cs[ss][hh * kRows + u.len - 1];
                 const float ref = 0.5f * (lo_[hh] + hi_[hh]);
                 const float refw = fast ? ref : cl, refy = fast ? ref : 0.f;
-                vw[ss][hh * kRows + ft] = ft < u.len ? expf(refw - v[hh]) * d[hh] : 0.f;
+                vw[ss][hh * kRows + ft] = ft < u.len ? expf(refw - v[hh]) * din[hh] : 0.f;
                 rs[ss][hh * kRows + ft] = expf(v[hh] - refy);
                 if (ft == 0) {
                     s_alpha[ss][hh] = expf(cl);

@@ -36,7 +36,8 @@ enum : unsigned int {
 
 struct Problem {
     const void *x;
-    const float *dt;
+    const float *dt;          // step of each token: the decay is exp(dt A)
+    const float *dtin;        // input scale of each token (same layout as dt); null: dt itself
     const float *A;
     const void *B;
     const void *C;
@@ -109,6 +110,12 @@ __device__ __forceinline__ float block_inclusive_scan_256(float v, float *warp_t
     __syncthreads();  // warp_tot may be reused by the caller
     return v;
 }
+
+// Pre-step (ssd_pre.cu): dt_eff = softplus(dt + bias) (or dt + bias) and, for
+// the zero-order-hold input, the scale expm1(dt_eff A) / A, per (b, t, h).
+enum : int { kPreSoftplus = 1, kPreZoh = 2 };
+cudaError_t launch_pre(const float *dt, const float *dt_bias, const float *A, int flags, float *dt_eff,
+                       float *scale, int batch, int seqlen, int nheads, cudaStream_t s);
 
 // One recurrent step (ssd_step.cu): state [batch][nheads][headdim][dstate] fp32 in place.
 cudaError_t launch_step(const void *x, const float *dt, const float *A, const void *B, const void *C,

@@ -24,7 +24,8 @@ __device__ __forceinline__ float chunk_segsum(const Problem &pr, int b, int h, i
     const float cs = block_inclusive_scan_256(dtv * __ldg(pr.A + h), warp_tot);
     if (tid < kMaxChunk) {
         cs_s[tid] = cs;
-        dt_s[tid] = dtv;
+        dt_s[tid] = pr.dtin ? (tid < len ? __ldg(pr.dtin + ((size_t)b * pr.seqlen + t0 + tid) * pr.nheads + h) : 0.f)
+                            : dtv;  // input scale
     }
     __syncthreads();
     return cs_s[len - 1];

@@ -87,8 +87,13 @@ __device__ __forceinline__ void segsum(const Problem &pr, int b, int h0, int nh,
         scan_128x2(v0, v1, warp_tot);
         cs[hh * 256 + j0] = v0;
         cs[hh * 256 + j1] = v1;
-        dtv[hh * 256 + j0] = d0;
-        dtv[hh * 256 + j1] = d1;
+        if (pr.dtin) {  // input scale
+            dtv[hh * 256 + j0] = j0 < len ? __ldg(pr.dtin + ((size_t)b * pr.seqlen + t0 + j0) * pr.nheads + h) : 0.f;
+            dtv[hh * 256 + j1] = j1 < len ? __ldg(pr.dtin + ((size_t)b * pr.seqlen + t0 + j1) * pr.nheads + h) : 0.f;
+        } else {
+            dtv[hh * 256 + j0] = d0;
+            dtv[hh * 256 + j1] = d1;
+        }
     }
     __syncthreads();
 }

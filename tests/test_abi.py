@@ -164,3 +164,18 @@ def test_step_groups_dtype_and_alignment(lib):
                       ctypes.c_void_p(4096), None, ctypes.c_void_p(4096), ctypes.c_void_p(8192), 1, 2, 4, 1, 8,
                       ssd.SSD_DTYPE_BF16, None)
     assert st == ssd.SSD_ERR_INVALID_ARG and "aligned" in ssd.ssd_last_error_detail()
+
+
+def test_pre_flags_and_bias_alignment(lib):
+    d = dict(DIMS)
+    p = ctypes.c_void_p(4096)
+    args = lambda flags, bias: (p, p, bias, flags, p, p, p, None, None, ctypes.c_void_p(8192), None,
+                                *[d[k] for k in ("batch", "seqlen", "nheads", "headdim", "ngroups", "dstate", "chunk")],
+                                ssd.SSD_DTYPE_BF16, None)
+    assert lib.ssd_fwd_pre(*args(4, None)) == ssd.SSD_ERR_INVALID_ARG
+    assert "pre_flags" in ssd.ssd_last_error_detail()
+    assert lib.ssd_fwd_pre(*args(ssd.SSD_PRE_ZOH, ctypes.c_void_p(4098))) == ssd.SSD_ERR_INVALID_ARG
+    assert "dt_bias" in ssd.ssd_last_error_detail()
+    # the shared checks of ssd_fwd still apply
+    d["ngroups"] = 3
+    assert lib.ssd_fwd_pre(*args(0, None)) == ssd.SSD_ERR_INVALID_ARG
