@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--workload", default=wl.HEADLINE.name, choices=[w.name for w in wl.WORKLOADS])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=0.0,
+                    help="oracle seconds per step of --impl reference (0: spread ~150 s over the steps)")
     return ap.parse_args()
 
 
@@ -60,6 +62,17 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's `value` (a no-op with one rank): the job's
+    time is its slowest rank's."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def load_peaks():
@@ -300,7 +313,7 @@ def run_reference(args, w, rank, world):
         return
     inp = wl.workload_inputs(w)
     cores = len(os.sched_getaffinity(0))
-    per_step = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step = args.ref_seconds or max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     steps = args.steps or 5
     for _ in range(args.warmup):
         time_oracle(w, inp, per_step / 4, cores)
@@ -418,10 +431,7 @@ def main():
     time.sleep(0.25)
     sampler.stop()
     ssd.ssd_check_device_status(stream)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     per_kernel = [0.0] * nk
     for evs in prof_events[:pi]:
@@ -461,10 +471,7 @@ def main():
     for _ in range(e2e_steps):
         host_step()
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, dev)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = y_host.numel() * y_host.element_size() + f_host.numel() * 4
 
