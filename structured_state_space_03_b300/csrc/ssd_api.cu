@@ -8,6 +8,7 @@
 #include <stdio.h>
 #include <stdarg.h>
 #include <string.h>
+#include <algorithm>
 #include <mutex>
 
 #include "ssd_internal.cuh"
@@ -381,6 +382,28 @@ ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float *A, con
     return run(pr, scratch, static_cast<cudaStream_t>(stream));
 }
 
+// Copy streams of the host-buffer entry, one pair per device, created on first use.
+static ssd_status_t copy_streams(cudaStream_t *in, cudaStream_t *out)
+{
+    static std::mutex mu;
+    static cudaStream_t streams[64][2];
+    static bool made[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(SSD_ERR_UNSUPPORTED, "device ordinal %d beyond 64", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!made[dev]) {
+        for (int k = 0; k < 2; ++k)
+            if ((e = cudaStreamCreateWithFlags(&streams[dev][k], cudaStreamNonBlocking)) != cudaSuccess)
+                return fail(SSD_ERR_CUDA, "copy stream creation failed: %s", cudaGetErrorString(e));
+        made[dev] = true;
+    }
+    *in = streams[dev][0];
+    *out = streams[dev][1];
+    return SSD_OK;
+}
+
 ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const void *B, const void *C,
                           const float *D, const float *init_state, void *y, float *final_state, int batch,
                           int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk,
@@ -392,16 +415,54 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
     if (st != SSD_OK) return st;
     if (!x || !dt || !A || !B || !C || !y)
         return fail(SSD_ERR_INVALID_ARG, "x, dt, A, B, C and y must be non-NULL");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStream_t s = static_cast<cudaStream_t>(stream), sin = nullptr, sout = nullptr;
+    if ((st = copy_streams(&sin, &sout)) != SSD_OK) return st;
     const size_t el = dtype == SSD_DTYPE_BF16 ? 2 : 4;
+    const size_t H = nheads, P = headdim, G = ngroups, N = dstate;
     const size_t tok = (size_t)batch * seqlen;
-    const size_t n_x = tok * nheads * headdim, n_dt = tok * nheads, n_bc = tok * ngroups * dstate;
-    const size_t n_state = (size_t)batch * nheads * headdim * dstate;
-    // one device block: x | B | C | y | dt | A | D | init | final | workspace, each 256-byte aligned
+    const size_t n_x = tok * H * P, n_dt = tok * H, n_bc = tok * G * N;
+    const size_t n_state = (size_t)batch * H * P * N;
+
+    // The problem is cut into parts whose copies and compute overlap: uploads on
+    // one stream, the scan on `stream`, downloads on another (the two copy
+    // directions run at once).  Four or more batch elements: groups of them.
+    // Fewer: each batch element in whole-chunk token ranges, the state of one
+    // range carried into the next in place (init_state == final_state).
+    struct Part { int b0, nb, t0, nt; };
+    Part parts[4];
+    int np = 0;
+    const int nc = pr.nchunks;
+    // parts start at token boundaries: keep their device addresses 16-byte aligned
+    const bool splittable = (H * P * el) % 16 == 0 && (G * N * el) % 16 == 0;
+    if (!splittable) {
+        parts[np++] = {0, batch, 0, seqlen};
+    } else if (batch >= 4) {
+        for (int k = 0; k < 4; ++k) {
+            const int b0 = (int)((long long)batch * k / 4), b1 = (int)((long long)batch * (k + 1) / 4);
+            parts[np++] = {b0, b1 - b0, 0, seqlen};
+        }
+    } else {
+        const int per = std::max(1, std::min(nc, 4 / batch));  // token ranges per batch element
+        for (int b = 0; b < batch; ++b)
+            for (int k = 0; k < per; ++k) {
+                const int c0 = nc * k / per, c1 = nc * (k + 1) / per;
+                parts[np++] = {b, 1, c0 * chunk, std::min(seqlen, c1 * chunk) - c0 * chunk};
+            }
+    }
+    const bool chained = np > 1 && parts[0].nb == 1 && np > batch;  // token ranges carry the state
+    size_t ws_need = 0;
+    for (int k = 0; k < np; ++k) {
+        Problem q = pr;
+        q.batch = parts[k].nb;
+        q.seqlen = parts[k].nt;
+        q.nchunks = (parts[k].nt + chunk - 1) / chunk;
+        ws_need = std::max(ws_need, workspace_bytes(q));
+    }
+    // one device block: x | B | C | y | dt | A | D | state in | state out | workspace
+    const bool need_state = final_state || chained;
     size_t off[11];
-    size_t sizes[10] = {n_x * el, n_bc * el, n_bc * el, n_x * el, n_dt * 4, (size_t)nheads * 4,
-                        D ? (size_t)nheads * 4 : 0, init_state ? n_state * 4 : 0,
-                        final_state ? n_state * 4 : 0, workspace_bytes(pr)};
+    size_t sizes[10] = {n_x * el, n_bc * el, n_bc * el, n_x * el, n_dt * 4, H * 4, D ? H * 4 : 0,
+                        init_state ? n_state * 4 : 0, need_state ? n_state * 4 : 0, ws_need};
     off[0] = 0;
     for (int i = 0; i < 10; ++i) off[i + 1] = align_up(off[i] + sizes[i], 256);
     char *dev = nullptr;
@@ -411,29 +472,70 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
         return fail(e == cudaErrorMemoryAllocation ? SSD_ERR_NO_MEMORY : SSD_ERR_CUDA,
                     "device allocation of %zu bytes failed: %s", off[10], cudaGetErrorString(e));
     }
-    const void *src[9] = {x, B, C, nullptr, dt, A, D, init_state, nullptr};
-    for (int i = 0; i < 9 && e == cudaSuccess; ++i)
-        if (src[i] && sizes[i]) e = cudaMemcpyAsync(dev + off[i], src[i], sizes[i], cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) {
-        pr.x = dev + off[0];
-        pr.B = dev + off[1];
-        pr.C = dev + off[2];
-        pr.y = dev + off[3];
-        pr.dt = reinterpret_cast<const float *>(dev + off[4]);
-        pr.A = reinterpret_cast<const float *>(dev + off[5]);
-        pr.D = D ? reinterpret_cast<const float *>(dev + off[6]) : nullptr;
-        pr.init_state = init_state ? reinterpret_cast<const float *>(dev + off[7]) : nullptr;
-        pr.final_state = final_state ? reinterpret_cast<float *>(dev + off[8]) : nullptr;
-        st = run(pr, dev + off[9], s);
-        if (st == SSD_OK) {
-            e = cudaMemcpyAsync(y, dev + off[3], sizes[3], cudaMemcpyDeviceToHost, s);
-            if (e == cudaSuccess && final_state)
-                e = cudaMemcpyAsync(final_state, dev + off[8], sizes[8], cudaMemcpyDeviceToHost, s);
-        }
+    cudaEvent_t ev[2 * 4 + 2];
+    int nev = 0;
+    for (; nev < 2 * np + 2 && e == cudaSuccess; ++nev) e = cudaEventCreateWithFlags(&ev[nev], cudaEventDisableTiming);
+    if (e != cudaSuccess) --nev;
+    cudaEvent_t ev_alloc = ev[2 * np], ev_out = ev[2 * np + 1];
+    char *const hx = (char *)x, *const hy = (char *)y, *const hB = (char *)B, *const hC = (char *)C;
+    const char *hdt = reinterpret_cast<const char *>(dt);
+    auto up = [&](size_t doff, const void *src, size_t bytes) {
+        if (e == cudaSuccess && bytes) e = cudaMemcpyAsync(dev + doff, src, bytes, cudaMemcpyHostToDevice, sin);
+    };
+    // the allocation is ordered on `stream`; the copy streams wait for it
+    if (e == cudaSuccess) e = cudaEventRecord(ev_alloc, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(sin, ev_alloc, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(sout, ev_alloc, 0);
+    up(off[5], A, sizes[5]);
+    up(off[6], D, sizes[6]);
+    up(off[7], init_state, sizes[7]);
+    for (int k = 0; k < np && e == cudaSuccess && st == SSD_OK; ++k) {
+        const Part &pt = parts[k];
+        const size_t t_first = (size_t)pt.b0 * seqlen + pt.t0;       // first token of the part
+        const size_t t_count = (size_t)pt.nb * pt.nt;
+        const size_t ox = t_first * H * P * el, obc = t_first * G * N * el, odt = t_first * H * 4;
+        up(off[0] + ox, hx + ox, t_count * H * P * el);
+        up(off[1] + obc, hB + obc, t_count * G * N * el);
+        up(off[2] + obc, hC + obc, t_count * G * N * el);
+        up(off[4] + odt, hdt + odt, t_count * H * 4);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[2 * k], sin);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev[2 * k], 0);
+        if (e != cudaSuccess) break;
+        Problem q = pr;
+        q.batch = pt.nb;
+        q.seqlen = pt.nt;
+        q.nchunks = (pt.nt + chunk - 1) / chunk;
+        q.x = dev + off[0] + ox;
+        q.B = dev + off[1] + obc;
+        q.C = dev + off[2] + obc;
+        q.y = dev + off[3] + ox;
+        q.dt = reinterpret_cast<const float *>(dev + off[4] + odt);
+        q.A = reinterpret_cast<const float *>(dev + off[5]);
+        q.D = D ? reinterpret_cast<const float *>(dev + off[6]) : nullptr;
+        const size_t ost = (size_t)pt.b0 * H * P * N * 4;
+        float *state_out = need_state ? reinterpret_cast<float *>(dev + off[8] + ost) : nullptr;
+        if (chained && pt.t0 > 0)
+            q.init_state = state_out;  // carried in place from the previous token range
+        else
+            q.init_state = init_state ? reinterpret_cast<const float *>(dev + off[7] + ost) : nullptr;
+        q.final_state = state_out;
+        st = run(q, dev + off[9], s);
+        if (st != SSD_OK) break;
+        if ((e = cudaEventRecord(ev[2 * k + 1], s)) == cudaSuccess) e = cudaStreamWaitEvent(sout, ev[2 * k + 1], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(hy + ox, dev + off[3] + ox, t_count * H * P * el, cudaMemcpyDeviceToHost, sout);
     }
+    if (e == cudaSuccess && st == SSD_OK && final_state)
+        e = cudaMemcpyAsync(final_state, dev + off[8], sizes[8], cudaMemcpyDeviceToHost, sout);
+    // the block is released on `stream` after both copy streams are done with it
+    cudaError_t e2 = cudaEventRecord(ev_out, sout);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(s, ev_out, 0);
+    cudaError_t e3 = cudaEventRecord(ev_alloc, sin);
+    if (e3 == cudaSuccess) e3 = cudaStreamWaitEvent(s, ev_alloc, 0);
     cudaError_t ef = cudaFreeAsync(dev, s);
     cudaError_t es = cudaStreamSynchronize(s);
+    for (int k = 0; k < nev; ++k) cudaEventDestroy(ev[k]);
     if (st != SSD_OK) return st;
+    if (e == cudaSuccess) e = e2 != cudaSuccess ? e2 : e3;
     if (e != cudaSuccess || ef != cudaSuccess || es != cudaSuccess)
         return fail(SSD_ERR_CUDA, "host-buffer forward failed: %s",
                     cudaGetErrorString(e != cudaSuccess ? e : (ef != cudaSuccess ? ef : es)));

@@ -187,6 +187,30 @@ def test_host_buffer_entry_matches_device_entry(dtype):
     assert torch.equal(yh, yd.cpu()) and torch.equal(fh, fd.cpu())
 
 
+# The host entry overlaps copies and compute over parts: batch groups (batch >= 4)
+# or whole-chunk token ranges with the state carried between them (batch < 4);
+# shapes whose token rows are not 16-byte multiples run as one part.
+HOST_CASES = [(1, 700, 4, 64, 64, 1, 128, "bf16"), (5, 300, 4, 64, 64, 2, 128, "bf16"),
+              (3, 450, 2, 128, 128, 1, 64, "bf16"), (1, 500, 4, 16, 6, 1, 64, "f32"),
+              (2, 900, 4, 64, 256, 1, 256, "bf16")]
+
+
+@pytest.mark.parametrize("case", HOST_CASES, ids=[f"b{c[0]}L{c[1]}N{c[4]}Q{c[6]}{c[7]}" for c in HOST_CASES])
+def test_host_entry_parts_match_device_entry(case):
+    b, L, H, P, N, G, Q, dtype = case
+    inp = make_inputs(b, L, H, P, N, G, dtype, seed=15 + b, with_init=True)
+    yd, fd = run_gpu(to_cuda(inp), Q)
+    pinned = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+    yh, fh = ssd.ssd_fwd_host(pinned["x"], pinned["dt"], pinned["A"], pinned["B"], pinned["C"], pinned["D"],
+                              pinned["init_state"], chunk=Q)
+    el = inp["x"].dtype
+    assert_close(yh.float().numpy(), yd.float().cpu().numpy(), TOL[el] / 4, "y, host vs device entry", STORAGE_U[el])
+    assert_close(fh.numpy(), fd.cpu().numpy(), TOL[el] / 4, "final state, host vs device entry")
+    yr, fr = oracle.recurrence(**inp)
+    assert_close(yh.float().numpy(), yr, TOL[el], "y, host entry vs oracle", STORAGE_U[el])
+    assert_close(fh.numpy(), fr, TOL[el], "final state, host entry vs oracle")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_caller_workspace_matches(dtype):
     inp = make_inputs(2, 300, 4, 64, 64, 1, dtype, seed=15, with_init=True)
