@@ -132,14 +132,15 @@ SSD_API ssd_status_t ssd_fwd_ws(const void *x, const float *dt, const float *A, 
  * ssd_fwd_host -- ssd_fwd on HOST buffers (same layouts and meanings).  The
  * call copies the inputs to the current device, runs the scan on `stream`,
  * copies y (and final_state when non-NULL) back and synchronises the stream
- * before returning.  The work is cut into up to four parts -- groups of batch
+ * before returning.  The work is cut into up to eight parts -- groups of batch
  * elements, or whole-chunk token ranges of each sequence with the state carried
  * from one range to the next -- so that uploads (on a library-owned stream),
  * the scan (on `stream`) and downloads (on a second library-owned stream)
  * overlap.  Device buffers come from the stream-ordered allocator and are
  * released before return.  Pinned host memory gives the fastest copies and the
- * overlap; pageable memory works.  Same error codes as ssd_fwd; a device-side
- * error is returned directly.
+ * overlap; pageable memory works.  Calls on one device are serialised (they
+ * share the copy streams).  Same error codes as ssd_fwd; a device-side error is
+ * returned directly.
  */
 SSD_API ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const void *B, const void *C,
                           const float *D, const float *init_state, void *y, float *final_state,

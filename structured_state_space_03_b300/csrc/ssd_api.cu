@@ -382,25 +382,37 @@ ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float *A, con
     return run(pr, scratch, static_cast<cudaStream_t>(stream));
 }
 
-// Copy streams of the host-buffer entry, one pair per device, created on first use.
-static ssd_status_t copy_streams(cudaStream_t *in, cudaStream_t *out)
+// Host-buffer entry: the problem is cut into at most kHostParts parts.
+constexpr int kHostParts = 8;
+
+// Copy streams and events of the host-buffer entry, one set per device, made on
+// first use; calls on one device take its lock for their whole duration.
+struct HostCopyRes {
+    std::mutex mu;
+    bool made = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t ev[2 * kHostParts + 2];
+};
+
+static ssd_status_t host_copy_res(HostCopyRes **res)
 {
     static std::mutex mu;
-    static cudaStream_t streams[64][2];
-    static bool made[64];
+    static HostCopyRes all[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return fail(SSD_ERR_UNSUPPORTED, "device ordinal %d beyond 64", dev);
     std::lock_guard<std::mutex> lock(mu);
-    if (!made[dev]) {
-        for (int k = 0; k < 2; ++k)
-            if ((e = cudaStreamCreateWithFlags(&streams[dev][k], cudaStreamNonBlocking)) != cudaSuccess)
-                return fail(SSD_ERR_CUDA, "copy stream creation failed: %s", cudaGetErrorString(e));
-        made[dev] = true;
+    HostCopyRes &r = all[dev];
+    if (!r.made) {
+        if ((e = cudaStreamCreateWithFlags(&r.in, cudaStreamNonBlocking)) == cudaSuccess)
+            e = cudaStreamCreateWithFlags(&r.out, cudaStreamNonBlocking);
+        for (int k = 0; k < 2 * kHostParts + 2 && e == cudaSuccess; ++k)
+            e = cudaEventCreateWithFlags(&r.ev[k], cudaEventDisableTiming);
+        if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "copy stream or event creation failed: %s", cudaGetErrorString(e));
+        r.made = true;
     }
-    *in = streams[dev][0];
-    *out = streams[dev][1];
+    *res = &r;
     return SSD_OK;
 }
 
@@ -415,8 +427,10 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
     if (st != SSD_OK) return st;
     if (!x || !dt || !A || !B || !C || !y)
         return fail(SSD_ERR_INVALID_ARG, "x, dt, A, B, C and y must be non-NULL");
-    cudaStream_t s = static_cast<cudaStream_t>(stream), sin = nullptr, sout = nullptr;
-    if ((st = copy_streams(&sin, &sout)) != SSD_OK) return st;
+    HostCopyRes *res = nullptr;
+    if ((st = host_copy_res(&res)) != SSD_OK) return st;
+    std::lock_guard<std::mutex> lock(res->mu);
+    cudaStream_t s = static_cast<cudaStream_t>(stream), sin = res->in, sout = res->out;
     const size_t el = dtype == SSD_DTYPE_BF16 ? 2 : 4;
     const size_t H = nheads, P = headdim, G = ngroups, N = dstate;
     const size_t tok = (size_t)batch * seqlen;
@@ -425,24 +439,24 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
 
     // The problem is cut into parts whose copies and compute overlap: uploads on
     // one stream, the scan on `stream`, downloads on another (the two copy
-    // directions run at once).  Four or more batch elements: groups of them.
-    // Fewer: each batch element in whole-chunk token ranges, the state of one
-    // range carried into the next in place (init_state == final_state).
+    // directions run at once).  kHostParts or more batch elements: groups of
+    // them.  Fewer: each batch element in whole-chunk token ranges, the state of
+    // one range carried into the next in place (init_state == final_state).
     struct Part { int b0, nb, t0, nt; };
-    Part parts[4];
+    Part parts[kHostParts];
     int np = 0;
     const int nc = pr.nchunks;
     // parts start at token boundaries: keep their device addresses 16-byte aligned
     const bool splittable = (H * P * el) % 16 == 0 && (G * N * el) % 16 == 0;
     if (!splittable) {
         parts[np++] = {0, batch, 0, seqlen};
-    } else if (batch >= 4) {
-        for (int k = 0; k < 4; ++k) {
-            const int b0 = (int)((long long)batch * k / 4), b1 = (int)((long long)batch * (k + 1) / 4);
+    } else if (batch >= kHostParts) {
+        for (int k = 0; k < kHostParts; ++k) {
+            const int b0 = (int)((long long)batch * k / kHostParts), b1 = (int)((long long)batch * (k + 1) / kHostParts);
             parts[np++] = {b0, b1 - b0, 0, seqlen};
         }
     } else {
-        const int per = std::max(1, std::min(nc, 4 / batch));  // token ranges per batch element
+        const int per = std::max(1, std::min(nc, kHostParts / batch));  // token ranges per batch element
         for (int b = 0; b < batch; ++b)
             for (int k = 0; k < per; ++k) {
                 const int c0 = nc * k / per, c1 = nc * (k + 1) / per;
@@ -472,10 +486,7 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
         return fail(e == cudaErrorMemoryAllocation ? SSD_ERR_NO_MEMORY : SSD_ERR_CUDA,
                     "device allocation of %zu bytes failed: %s", off[10], cudaGetErrorString(e));
     }
-    cudaEvent_t ev[2 * 4 + 2];
-    int nev = 0;
-    for (; nev < 2 * np + 2 && e == cudaSuccess; ++nev) e = cudaEventCreateWithFlags(&ev[nev], cudaEventDisableTiming);
-    if (e != cudaSuccess) --nev;
+    cudaEvent_t *ev = res->ev;
     cudaEvent_t ev_alloc = ev[2 * np], ev_out = ev[2 * np + 1];
     char *const hx = (char *)x, *const hy = (char *)y, *const hB = (char *)B, *const hC = (char *)C;
     const char *hdt = reinterpret_cast<const char *>(dt);
@@ -533,7 +544,6 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
     if (e3 == cudaSuccess) e3 = cudaStreamWaitEvent(s, ev_alloc, 0);
     cudaError_t ef = cudaFreeAsync(dev, s);
     cudaError_t es = cudaStreamSynchronize(s);
-    for (int k = 0; k < nev; ++k) cudaEventDestroy(ev[k]);
     if (st != SSD_OK) return st;
     if (e == cudaSuccess) e = e2 != cudaSuccess ? e2 : e3;
     if (e != cudaSuccess || ef != cudaSuccess || es != cudaSuccess)
