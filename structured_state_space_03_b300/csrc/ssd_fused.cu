@@ -133,12 +133,12 @@ __device__ __forceinline__ void split8(const float *f, uint4 &hi, uint4 &lo)
 }
 
 // acc += s * src[0..32) (src read through L2)
-__device__ __forceinline__ void fma_row32(float (&acc)[32], float s, const float *src)
+__device__ __forceinline__ void fma_row32(float (&acc)[32], float s, const float *src, int qstride = 1)
 {
     const float4 *s4 = reinterpret_cast<const float4 *>(src);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-        const float4 v = __ldcg(s4 + q);
+        const float4 v = __ldcg(s4 + q * qstride);
         acc[4 * q] = fmaf(s, v.x, acc[4 * q]);
         acc[4 * q + 1] = fmaf(s, v.y, acc[4 * q + 1]);
         acc[4 * q + 2] = fmaf(s, v.z, acc[4 * q + 2]);
@@ -457,7 +457,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int hh_m = m / P, p_m = m % P;
     const size_t ustride = (size_t)kRows * NS;
     const int n0 = half * (NS / 2);
-    const size_t row_off = (size_t)m * NS + n0;
+    // published states: [NS/4][128 rows][4] per unit (a warp moves 512 contiguous
+    // bytes); the float4 holding columns [n, n + 4) of row m sits at (n / 4) * kRows + m
+    const size_t row_off = (size_t)(n0 / 4) * kRows * 4 + (size_t)m * 4;
     const float sfac = s_sfac[hh_m];
     if (ok && tid == 0) {
         int mode = 0;  // 0: chunk 0, 1: predecessor inclusive ready, 2: look back
@@ -468,13 +470,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int mode = s_mode;
     if (ok && mode == 2) {
         // publish the aggregate (S_c, a_c) before waiting on anyone
-        float *dst = fa.agg + unit * ustride + row_off;
+        float4 *dst = reinterpret_cast<float4 *>(fa.agg + unit * ustride + row_off);
         for (int cc = 0; cc < NS / 2; cc += 32) {
             float v[32];
             tmem_ld32(tmem + lane_base + col_st + n0 + cc, v);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                __stcg(reinterpret_cast<float4 *>(dst + cc) + u, make_float4(sfac * v[4 * u], sfac * v[4 * u + 1],
+                __stcg(dst + (cc / 4 + u) * kRows, make_float4(sfac * v[4 * u], sfac * v[4 * u + 1],
                                                                              sfac * v[4 * u + 2], sfac * v[4 * u + 3]));
         }
         if (tid < HB) fa.alpha[unit * 2 + tid] = s_alpha[tid];
@@ -532,19 +534,19 @@ __global__ void __launch_bounds__(kThreads, 2)
             float acc[32];
 #pragma unroll
             for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-            if (stop >= 0) fma_row32(acc, 1.f, fa.incl + (unit - (c - stop)) * ustride + row_off + cc);
+            if (stop >= 0) fma_row32(acc, 1.f, fa.incl + (unit - (c - stop)) * ustride + row_off + cc * kRows, kRows);
             else if (init) fma_row32(acc, 1.f, init + cc);
             int k = stop + 1;
             for (; k + 1 < c; k += 2) {  // two aggregates per round trip
                 const size_t u = unit - (c - k);
                 const float a0 = __ldcg(fa.alpha + u * 2 + hh_m), a1 = __ldcg(fa.alpha + (u + 1) * 2 + hh_m);
-                const float4 *s0 = reinterpret_cast<const float4 *>(fa.agg + u * ustride + row_off + cc);
-                const float4 *s1 = reinterpret_cast<const float4 *>(fa.agg + (u + 1) * ustride + row_off + cc);
+                const float4 *s0 = reinterpret_cast<const float4 *>(fa.agg + u * ustride + row_off + cc * kRows);
+                const float4 *s1 = reinterpret_cast<const float4 *>(fa.agg + (u + 1) * ustride + row_off + cc * kRows);
                 float4 v0[8], v1[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    v0[q] = __ldcg(s0 + q);
-                    v1[q] = __ldcg(s1 + q);
+                    v0[q] = __ldcg(s0 + q * kRows);
+                    v1[q] = __ldcg(s1 + q * kRows);
                 }
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
@@ -557,10 +559,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (k < c) {
                 const size_t u = unit - (c - k);
                 const float a = __ldcg(fa.alpha + u * 2 + hh_m);
-                const float4 *src = reinterpret_cast<const float4 *>(fa.agg + u * ustride + row_off + cc);
+                const float4 *src = reinterpret_cast<const float4 *>(fa.agg + u * ustride + row_off + cc * kRows);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const float4 v = __ldcg(src + q);
+                    const float4 v = __ldcg(src + q * kRows);
                     acc[4 * q] = fmaf(a, acc[4 * q], v.x);
                     acc[4 * q + 1] = fmaf(a, acc[4 * q + 1], v.y);
                     acc[4 * q + 2] = fmaf(a, acc[4 * q + 2], v.z);
@@ -591,10 +593,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             tmem_ld32(tmem + lane_base + col_st + n0 + cc, sc);
 #pragma unroll
             for (int k = 0; k < 32; ++k) sc[k] = fmaf(a_own, acc[k], sfac * sc[k]);
-            float4 *dst = reinterpret_cast<float4 *>(fa.incl + unit * ustride + row_off + cc);
+            float4 *dst = reinterpret_cast<float4 *>(fa.incl + unit * ustride + row_off + cc * kRows);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-                __stcg(dst + q, make_float4(sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3]));
+                __stcg(dst + q * kRows, make_float4(sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3]));
             if (c == nc - 1 && pr.final_state) {
                 float4 *fo = reinterpret_cast<float4 *>(pr.final_state + (((size_t)b * H + hg) * P + p_m) * NS + n0 + cc);
 #pragma unroll

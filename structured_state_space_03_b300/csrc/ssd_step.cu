@@ -45,7 +45,6 @@ __global__ void __launch_bounds__(256) ssd_step_kernel(const T *__restrict__ x, 
     const long long row = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);  // (b, h, p)
     const long long rows = (long long)batch * H * P;
     if (row >= rows) return;
-    const int p = (int)(row % P);
     const int h = (int)((row / P) % H);
     const int b = (int)(row / ((long long)P * H));
     const int g = h / (H / G);
