@@ -40,6 +40,8 @@ def test_workload_sampled_rows(w):
 MID = [
     # b, L, H, P, N, G, Q, dtype
     (2, 1000, 8, 64, 64, 2, 128, "bf16"),
+    (3, 777, 4, 64, 64, 1, 128, "bf16"),      # one group of four heads, ragged tail
+    (2, 1000, 8, 64, 64, 2, 64, "bf16"),      # chunk 64
     (1, 8000, 2, 64, 64, 1, 64, "bf16"),      # 125 chained chunks of one head pair: deep look-back
     (3, 700, 4, 128, 128, 2, 100, "bf16"),
     (1, 1000, 4, 64, 256, 1, 128, "bf16"),
