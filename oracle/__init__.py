@@ -224,3 +224,38 @@ def recurrence_pre(x, dt, A, B, C, D=None, init_state=None, dt_bias=None, softpl
     if rows is not None:
         return y, fin
     return (y.reshape(b, H, P, L).transpose(0, 3, 1, 2).copy(), fin.reshape(b, H, P, N))
+
+
+def recurrence_varlen(x, dt, A, B, C, D=None, init_state=None, cu_seqlens=None, nthreads=None):
+    """O1 over packed variable-length sequences ("Mamba-2架构深度解析" §5, dynamic
+    sequence packing; reading: every packed sequence is its own recurrence, so
+    the state restarts from that sequence's initial state at its first token).
+
+    x [T, H, P], dt [T, H], B and C [T, G, N] hold the sequences back to back;
+    sequence s owns tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 (cu_seqlens[0] = 0,
+    nondecreasing, last = T; empty sequences allowed).  init_state is
+    [nseq, H, P, N] or None (zero).  Returns (y [T, H, P], final_state
+    [nseq, H, P, N]) in fp64; an empty sequence's final state is its initial
+    state.
+    """
+    cu = [int(v) for v in cu_seqlens]
+    if not cu or cu[0] != 0 or any(b < a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must start at 0 and be nondecreasing")
+    T, H, P = (int(v) for v in x.shape)
+    if cu[-1] != T:
+        raise ValueError("cu_seqlens must end at the packed token count")
+    N = int(B.shape[2])
+    nseq = len(cu) - 1
+    y = np.zeros((T, H, P), np.float64)
+    fin = np.zeros((nseq, H, P, N), np.float64)
+    for s in range(nseq):
+        a, e = cu[s], cu[s + 1]
+        h0 = None if init_state is None else init_state[s:s + 1]
+        if e == a:
+            if h0 is not None:
+                fin[s] = np.asarray(_as_input(h0, "init_state", False)[0], np.float64)[0]
+            continue
+        ys, fs = recurrence(x[None, a:e], dt[None, a:e], A, B[None, a:e], C[None, a:e], D, h0, nthreads=nthreads)
+        y[a:e] = ys[0]
+        fin[s] = fs[0]
+    return y, fin
