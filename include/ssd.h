@@ -176,6 +176,36 @@ SSD_API ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float
                                      int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
                                      int chunk, ssd_dtype_t dtype, void *stream);
 
+/*
+ * ssd_fwd_varlen -- ssd_fwd over packed variable-length sequences ("dynamic
+ * sequence packing", "Mamba-2架构深度解析" §5): nseq sequences stored back to
+ * back along one token dimension, each its own recurrence.  Sequence s owns the
+ * packed tokens cu_seqlens[s] .. cu_seqlens[s+1]-1; its state starts from
+ * init_state[s] (or zero) at its first token and ends in final_state[s]:
+ *
+ *     x, y        [total][nheads][headdim]   dtype, total = cu_seqlens[nseq]
+ *     dt          [total][nheads]            fp32
+ *     B, C        [total][ngroups][dstate]   dtype
+ *     init_state, final_state  [nseq][nheads][headdim][dstate] fp32, each may be NULL
+ *     cu_seqlens  HOST int32 [nseq + 1]: cu_seqlens[0] = 0, nondecreasing;
+ *                 read during the call only (the library builds its chunk table from it)
+ *
+ * A, D, chunk, dtype, stream, the alignment rules and the asynchrony are those
+ * of ssd_fwd; the workspace (the per-chunk states plus the chunk table) comes
+ * from the stream-ordered allocator.  Empty sequences are allowed: their
+ * final state is their initial state (or zero).  Chunks never straddle two
+ * sequences: each sequence is cut into chunks from its own first token, the
+ * last one partial.  Runs on the persistent fused kernel: bf16, headdim 64 or
+ * 128, dstate 64, chunk <= 128, nheads / ngroups a multiple of 128 / headdim;
+ * SSD_ERR_UNSUPPORTED otherwise, or for more than INT32_MAX packed tokens.
+ * SSD_ERR_INVALID_ARG for a NULL cu_seqlens, nseq <= 0, offsets that do not
+ * start at 0 or decrease, and the checks of ssd_fwd.
+ */
+SSD_API ssd_status_t ssd_fwd_varlen(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                                    const float *D, const int *cu_seqlens, int nseq, const float *init_state,
+                                    void *y, float *final_state, int nheads, int headdim, int ngroups, int dstate,
+                                    int chunk, ssd_dtype_t dtype, void *stream);
+
 /* Pre-step flags of ssd_fwd_pre. */
 enum { SSD_PRE_SOFTPLUS = 1, SSD_PRE_ZOH = 2 };
 

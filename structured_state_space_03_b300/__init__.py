@@ -4,7 +4,8 @@ Thin ctypes marshalling over the C ABI declared in ``include/ssd.h``; every
 step of the computation runs in the library's CUDA kernels.  PyTorch is used
 for device memory and streams only.  The functions carry the C names:
 
-    ssd_fwd, ssd_fwd_ws, ssd_fwd_host, ssd_fwd_pre, ssd_fwd_workspace_size, ssd_fwd_path, ssd_step,
+    ssd_fwd, ssd_fwd_ws, ssd_fwd_host, ssd_fwd_pre, ssd_fwd_varlen, ssd_fwd_noalloc, ssd_fwd_workspace_size,
+    ssd_fwd_path, ssd_step,
     ssd_check_device_status, ssd_status_string, ssd_last_error_detail, ssd_version
 
 Layouts: x, y [batch, seqlen, nheads, headdim]; dt [batch, seqlen, nheads];
@@ -44,6 +45,8 @@ SIGNATURES = {
     "ssd_fwd_noalloc": (_I, _FWD + [_P]),
     "ssd_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "ssd_fwd_pre": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "ssd_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_int), _I, _P, _P, _P, _I, _I, _I, _I, _I,
+                            _I, _P]),
     "ssd_fwd_workspace_size": (_I, _DIMS + [ctypes.POINTER(ctypes.c_size_t)]),
     "ssd_fwd_path": (_I, _DIMS),
     "ssd_fwd_kernels": (_I, _DIMS + [ctypes.c_char_p, _S]),
@@ -205,6 +208,49 @@ def ssd_fwd_pre(x, dt, A, B, C, D=None, init_state=None, *, chunk: int, dt_bias=
     _check(lib().ssd_fwd_pre(_ptr(x), _ptr(dt), _ptr(dt_bias), flags, _ptr(A), _ptr(B), _ptr(C), _ptr(D),
                              _ptr(init_state), _ptr(y), _ptr(final_state), b, L, H, P, G, N, chunk,
                              _dtype_code(x.dtype), _stream_handle(stream)))
+    return y, final_state
+
+
+def ssd_fwd_varlen(x, dt, A, B, C, D=None, init_state=None, *, cu_seqlens, chunk: int, y=None, final_state=None,
+                   return_final: bool = True, stream=None):
+    """ssd_fwd over packed variable-length sequences on CUDA tensors.
+
+    x [total, nheads, headdim]; dt [total, nheads] float32; B, C [total, ngroups,
+    dstate]; ``cu_seqlens`` (host: a sequence of ints or a CPU tensor) holds the
+    nseq + 1 offsets of the sequences in the packed token dimension; init_state
+    and final_state are [nseq, nheads, headdim, dstate] float32.  Each sequence
+    is its own recurrence.  Returns (y, final_state).
+    """
+    cu = [int(v) for v in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+    nseq = len(cu) - 1
+    if nseq < 1:
+        raise ValueError("cu_seqlens needs at least two offsets")
+    if x.dim() != 3 or B.dim() != 3:
+        raise ValueError("x must be [total, nheads, headdim] and B, C [total, ngroups, dstate]")
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    el = x.dtype
+    for name, t, shape, dtype in (("dt", dt, (T, H), torch.float32), ("A", A, (H,), torch.float32),
+                                  ("B", B, (T, G, N), el), ("C", C, (T, G, N), el), ("D", D, (H,), torch.float32),
+                                  ("init_state", init_state, (nseq, H, P, N), torch.float32)):
+        if t is None:
+            continue
+        if tuple(t.shape) != shape or t.dtype != dtype or not t.is_contiguous() or t.device.type != "cuda":
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor of shape {shape}")
+    if not x.is_contiguous() or x.device.type != "cuda":
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if cu[-1] != T:
+        raise ValueError(f"cu_seqlens must end at the packed token count {T}")
+    if y is None:
+        y = torch.empty_like(x)
+    elif y.shape != x.shape or y.dtype != el or not y.is_contiguous():
+        raise ValueError("y must be a contiguous tensor like x")
+    if final_state is None and return_final:
+        final_state = torch.empty(nseq, H, P, N, dtype=torch.float32, device=x.device)
+    offs = (ctypes.c_int * (nseq + 1))(*cu)
+    _check(lib().ssd_fwd_varlen(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), offs, nseq, _ptr(init_state),
+                                _ptr(y), _ptr(final_state), H, P, G, N, chunk, _dtype_code(el),
+                                _stream_handle(stream)))
     return y, final_state
 
 

@@ -10,6 +10,7 @@
 #include <string.h>
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "ssd_internal.cuh"
 
@@ -279,6 +280,103 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
                     "workspace allocation of %zu bytes failed: %s", need, cudaGetErrorString(e));
     }
     st = run(pr, ws, s);
+    e = cudaFreeAsync(ws, s);
+    if (st == SSD_OK && e != cudaSuccess)
+        return fail(SSD_ERR_CUDA, "workspace release failed: %s", cudaGetErrorString(e));
+    return st;
+}
+
+ssd_status_t ssd_fwd_varlen(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                            const float *D, const int *cu_seqlens, int nseq, const float *init_state, void *y,
+                            float *final_state, int nheads, int headdim, int ngroups, int dstate, int chunk,
+                            ssd_dtype_t dtype, void *stream)
+{
+    if (!cu_seqlens || nseq <= 0) return fail(SSD_ERR_INVALID_ARG, "cu_seqlens must be non-NULL and nseq positive");
+    if (cu_seqlens[0] != 0) return fail(SSD_ERR_INVALID_ARG, "cu_seqlens[0] must be 0 (got %d)", cu_seqlens[0]);
+    for (int q = 0; q < nseq; ++q)
+        if (cu_seqlens[q + 1] < cu_seqlens[q])
+            return fail(SSD_ERR_INVALID_ARG, "cu_seqlens decreases at %d (%d -> %d)", q, cu_seqlens[q],
+                        cu_seqlens[q + 1]);
+    const int total = cu_seqlens[nseq];
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t state_el = (size_t)nheads * headdim * dstate;
+    if (total == 0) {  // only empty sequences: the final states are the initial states
+        Problem chk;
+        memset(&chk, 0, sizeof chk);
+        ssd_status_t st = check_dims(chk, nseq, 1, nheads, headdim, ngroups, dstate, chunk, dtype);
+        if (st != SSD_OK) return st;
+        cudaError_t e = cudaSuccess;
+        if (final_state && final_state != init_state)
+            e = init_state ? cudaMemcpyAsync(final_state, init_state, nseq * state_el * sizeof(float),
+                                             cudaMemcpyDeviceToDevice, s)
+                           : cudaMemsetAsync(final_state, 0, nseq * state_el * sizeof(float), s);
+        return e == cudaSuccess ? ok() : fail(SSD_ERR_CUDA, "final state copy failed: %s", cudaGetErrorString(e));
+    }
+    Problem pr;
+    ssd_status_t st = make_problem(pr, x, dt, A, B, C, D, init_state, y, final_state, nseq, total, nheads, headdim,
+                                   ngroups, dstate, chunk, dtype);
+    if (st != SSD_OK) return st;
+    if (choose_path(pr) != SSD_PATH_TCGEN05_FUSED || dstate != 64)
+        return fail(SSD_ERR_UNSUPPORTED,
+                    "packed sequences run on the persistent fused kernel: bf16, headdim 64 or 128, dstate 64, "
+                    "chunk <= 128, nheads / ngroups a multiple of 128 / headdim");
+    // chunk table in chunk-major order (a counting sort over the chunk index)
+    std::vector<int> nchunk(nseq);
+    int max_nc = 0;
+    size_t total_chunks = 0;
+    for (int q = 0; q < nseq; ++q) {
+        const int len = cu_seqlens[q + 1] - cu_seqlens[q];
+        nchunk[q] = (len + chunk - 1) / chunk;
+        max_nc = std::max(max_nc, nchunk[q]);
+        total_chunks += nchunk[q];
+    }
+    std::vector<size_t> cursor(max_nc + 1, 0);
+    for (int q = 0; q < nseq; ++q)
+        for (int c = 0; c < nchunk[q]; ++c) ++cursor[c + 1];
+    for (int c = 0; c < max_nc; ++c) cursor[c + 1] += cursor[c];
+    std::vector<ChunkDesc> table(total_chunks);
+    size_t gbase = 0;
+    for (int q = 0; q < nseq; ++q) {
+        const int len = cu_seqlens[q + 1] - cu_seqlens[q];
+        for (int c = 0; c < nchunk[q]; ++c) {
+            ChunkDesc &d = table[cursor[c]++];
+            d.b = q;
+            d.c = c;
+            d.gchunk = (int)(gbase + c);
+            d.tok0 = cu_seqlens[q] + c * chunk;
+            d.len = std::min(chunk, len - c * chunk);
+            d.last = c == nchunk[q] - 1;
+            d.pad0 = d.pad1 = 0;
+        }
+        gbase += nchunk[q];
+    }
+    pr.total_chunks = (int)total_chunks;
+    pr.chunks = reinterpret_cast<const ChunkDesc *>(1);  // marks the packed layout for the size query below
+    if (!fused_supported(pr)) return fail(SSD_ERR_UNSUPPORTED, "too many chunks for the packed layout");
+    const size_t main_bytes = align_up(workspace_bytes(pr), 256);
+    const size_t need = main_bytes + total_chunks * sizeof(ChunkDesc);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(e == cudaErrorMemoryAllocation ? SSD_ERR_NO_MEMORY : SSD_ERR_CUDA,
+                    "workspace allocation of %zu bytes failed: %s", need, cudaGetErrorString(e));
+    }
+    ChunkDesc *dtab = reinterpret_cast<ChunkDesc *>(static_cast<char *>(ws) + main_bytes);
+    e = cudaMemcpyAsync(dtab, table.data(), total_chunks * sizeof(ChunkDesc), cudaMemcpyHostToDevice, s);
+    // empty sequences get no unit: their final state is their initial state
+    for (int q = 0; q < nseq && e == cudaSuccess; ++q) {
+        if (nchunk[q] != 0 || !final_state || final_state == init_state) continue;
+        e = init_state ? cudaMemcpyAsync(final_state + q * state_el, init_state + q * state_el,
+                                         state_el * sizeof(float), cudaMemcpyDeviceToDevice, s)
+                       : cudaMemsetAsync(final_state + q * state_el, 0, state_el * sizeof(float), s);
+    }
+    if (e == cudaSuccess) {
+        pr.chunks = dtab;
+        st = run(pr, ws, s);
+    } else {
+        st = fail(SSD_ERR_CUDA, "chunk table upload failed: %s", cudaGetErrorString(e));
+    }
     e = cudaFreeAsync(ws, s);
     if (st == SSD_OK && e != cudaSuccess)
         return fail(SSD_ERR_CUDA, "workspace release failed: %s", cudaGetErrorString(e));

@@ -170,13 +170,12 @@ __device__ __forceinline__ void named_sync(int id, int n)
 }
 
 // Evaluation is shared by the `gn` threads numbered `gt` of barrier `bar_id`.
-__device__ void direct_unit_outputs(const Problem &pr, int NS, int b, int hb, int c, const float *hcs, float *gsm,
-                                    const float *cs, const float *dtv, int gt, int gn, int bar_id)
+__device__ void direct_unit_outputs(const Problem &pr, int NS, size_t tok0, int len, int hb, const float *hcs,
+                                    float *gsm, const float *cs, const float *dtv, int gt, int gn, int bar_id)
 {
     const int tid = gt;
-    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
+    const int P = pr.headdim, HB = 128 / P, H = pr.nheads;
     const int h0 = hb * HB, G = pr.ngroups, g = h0 / (H / G);
-    const int t0 = c * pr.chunk, len = min(pr.chunk, L - t0);
     const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(pr.x);
     const __nv_bfloat16 *Bm = static_cast<const __nv_bfloat16 *>(pr.B);
     const __nv_bfloat16 *Cm = static_cast<const __nv_bfloat16 *>(pr.C);
@@ -186,8 +185,8 @@ __device__ void direct_unit_outputs(const Problem &pr, int NS, int b, int hb, in
             const int i = i0 + (e >> 7), j = e & 127;
             float s = 0.f;
             if (i < len && j <= i) {
-                const __nv_bfloat16 *ci = Cm + (((size_t)b * L + t0 + i) * G + g) * NS;
-                const __nv_bfloat16 *bj = Bm + (((size_t)b * L + t0 + j) * G + g) * NS;
+                const __nv_bfloat16 *ci = Cm + ((tok0 + i) * G + g) * NS;
+                const __nv_bfloat16 *bj = Bm + ((tok0 + j) * G + g) * NS;
                 for (int n = 0; n < NS; ++n) s = fmaf(__bfloat162float(ci[n]), __bfloat162float(bj[n]), s);
             }
             gsm[e] = s;
@@ -201,11 +200,11 @@ __device__ void direct_unit_outputs(const Problem &pr, int NS, int b, int hb, in
             float acc = 0.f;
             for (int j = 0; j <= i; ++j)
                 acc = fmaf(gsm[(i - i0) * kRows + j] * expf(csh[i] - csh[j]) * dth[j],
-                           __bfloat162float(x[(((size_t)b * L + t0 + j) * H + h) * P + p]), acc);
+                           __bfloat162float(x[((tok0 + j) * H + h) * P + p]), acc);
             float off = 0.f;
-            const __nv_bfloat16 *ci = Cm + (((size_t)b * L + t0 + i) * G + g) * NS;
+            const __nv_bfloat16 *ci = Cm + ((tok0 + i) * G + g) * NS;
             for (int n = 0; n < NS; ++n) off = fmaf(__bfloat162float(ci[n]), hcs[col * NS + n], off);
-            const size_t yi = (((size_t)b * L + t0 + i) * H + h) * P + p;
+            const size_t yi = ((tok0 + i) * H + h) * P + p;
             const float Dh = pr.D ? pr.D[h] : 0.f;
             static_cast<__nv_bfloat16 *>(pr.y)[yi] =
                 __float2bfloat16_rn(acc + expf(csh[i]) * off + Dh * __bfloat162float(x[yi]));
@@ -687,7 +686,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
     if (ok && !fast)  // decay range too wide for the factored form: direct outputs (C_i . B_j over x)
-        direct_unit_outputs(pr, NS, b, hb, c, reinterpret_cast<const float *>(hh_s), reinterpret_cast<float *>(xs),
+        direct_unit_outputs(pr, NS, (size_t)b * L + t0, len, hb, reinterpret_cast<const float *>(hh_s),
+                            reinterpret_cast<float *>(xs),
                             cs, dtv, tid, kThreads, 0);
 }
 
@@ -737,24 +737,49 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool pred)
     return r != 0;
 }
 
+// A unit: sequence b (a batch element or a packed sequence), chunk c of it, head
+// block hb.  tok is the global index of its first token (row of the token
+// dimension flattened over the batch), (tt, tb) its TMA coordinates, last
+// whether c is the sequence's last chunk.  Units of one (b, hb) have
+// consecutive indices in chunk order, so chunk k of the same sequence is
+// unit - (c - k).
 struct PipeUnit {
-    int b, hb, c, h0, g, t0, len;
-    size_t unit;
+    int b, hb, c, h0, g, tt, tb, len;
+    bool last;
+    size_t tok, unit;
 };
 
 __device__ __forceinline__ PipeUnit decode_unit(const Problem &pr, int ticket, int nhb)
 {
     PipeUnit u;
-    u.c = ticket / (pr.batch * nhb);
-    const int rest = ticket - u.c * (pr.batch * nhb);
-    u.b = rest / nhb;
-    u.hb = rest - u.b * nhb;
+    if (pr.chunks) {  // packed sequences: the chunk table is already chunk-major
+        const int k = ticket / nhb;
+        u.hb = ticket - k * nhb;
+        const int4 d0 = __ldg(reinterpret_cast<const int4 *>(pr.chunks + k));
+        const int4 d1 = __ldg(reinterpret_cast<const int4 *>(pr.chunks + k) + 1);
+        u.b = d0.x;
+        u.c = d0.y;
+        u.tok = (size_t)d0.w;
+        u.tt = d0.w;
+        u.tb = 0;
+        u.len = d1.x;
+        u.last = d1.y != 0;
+        u.unit = (size_t)u.hb * pr.total_chunks + d0.z;
+    } else {
+        u.c = ticket / (pr.batch * nhb);
+        const int rest = ticket - u.c * (pr.batch * nhb);
+        u.b = rest / nhb;
+        u.hb = rest - u.b * nhb;
+        u.tt = u.c * pr.chunk;
+        u.tb = u.b;
+        u.tok = (size_t)u.b * pr.seqlen + u.tt;
+        u.len = min(pr.chunk, pr.seqlen - u.tt);
+        u.last = u.c == pr.nchunks - 1;
+        u.unit = ((size_t)u.b * nhb + u.hb) * pr.nchunks + u.c;
+    }
     const int HB = 128 / pr.headdim;
     u.h0 = u.hb * HB;
     u.g = u.h0 / (pr.nheads / pr.ngroups);
-    u.t0 = u.c * pr.chunk;
-    u.len = min(pr.chunk, pr.seqlen - u.t0);
-    u.unit = ((size_t)u.b * nhb + u.hb) * pr.nchunks + u.c;
     return u;
 }
 
@@ -782,8 +807,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;  // TMEM lane of this thread (warps 2-13)
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
-    const int nhb = H / HB, nc = pr.nchunks;
+    const int P = pr.headdim, HB = 128 / P, H = pr.nheads;
+    const int nhb = H / HB;
     const uint32_t col_y = 0, col_st = 128, col_m = 192;
 
     if (warp == kWarpMma) tmem_alloc(&tmem_slot, 512);
@@ -843,14 +868,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 uint8_t *st = base + s * kStageBytes;
                 if (dt_tma) {  // dt[t0 .. t0+127][4 heads from h0 rounded down to 4]
                     mbar_expect_tx(&bar_dt[s], (uint32_t)(kRows * 4 * sizeof(float)));
-                    tma_load_3d(base + 2 * kStageBytes + s * kDtBytes, &dtmap, &bar_dt[s], u.h0 & ~3, u.t0, u.b);
+                    tma_load_3d(base + 2 * kStageBytes + s * kDtBytes, &dtmap, &bar_dt[s], u.h0 & ~3, u.tt, u.tb);
                 } else {
                     mbar_arrive(&bar_dt[s]);
                 }
                 mbar_expect_tx(&bar_full[s], (uint32_t)(4 * kSlab));
-                for (int k = 0; k < 2; ++k) tma_load_3d(st + k * kSlab, &xmap, &bar_full[s], u.hb * 128 + 64 * k, u.t0, u.b);
-                tma_load_3d(st + 4 * kSlab, &bmap, &bar_full[s], u.g * NS, u.t0, u.b);
-                tma_load_3d(st + 5 * kSlab, &cmap, &bar_full[s], u.g * NS, u.t0, u.b);
+                for (int k = 0; k < 2; ++k) tma_load_3d(st + k * kSlab, &xmap, &bar_full[s], u.hb * 128 + 64 * k, u.tt, u.tb);
+                tma_load_3d(st + 4 * kSlab, &bmap, &bar_full[s], u.g * NS, u.tt, u.tb);
+                tma_load_3d(st + 5 * kSlab, &cmap, &bar_full[s], u.g * NS, u.tt, u.tb);
             }
         }
     } else if (warp == kWarpMma) {
@@ -936,9 +961,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 const bool act = hh < HB;
                 const float a = act ? __ldg(pr.A + u.h0 + hh) : 0.f;
                 d[hh] = (act && ft < u.len)
-                            ? (dt_tma ? dts[hh] : __ldg(pr.dt + ((size_t)u.b * L + u.t0 + ft) * H + u.h0 + hh))
+                            ? (dt_tma ? dts[hh] : __ldg(pr.dt + (u.tok + ft) * H + u.h0 + hh))
                             : 0.f;
-                din[hh] = pr.dtin ? ((act && ft < u.len) ? __ldg(pr.dtin + ((size_t)u.b * L + u.t0 + ft) * H + u.h0 + hh) : 0.f)
+                din[hh] = pr.dtin ? ((act && ft < u.len) ? __ldg(pr.dtin + (u.tok + ft) * H + u.h0 + hh) : 0.f)
                                   : d[hh];  // input scale
                 v[hh] = d[hh] * a;
 #pragma unroll
@@ -1087,7 +1112,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         const int bar_team = kBarTeam0 + team;
         const int hh_m = m / P, p_m = m % P;
         const size_t ustride = (size_t)kRows * NS;
-        const bool tma_out = pr.chunk == kRows;
+        // full 128-row tiles go out by TMA; a packed sequence's partial last chunk is
+        // stored row by row, since the rows after it belong to the next sequence
+        const bool tma_tiles = pr.chunk == kRows;
         const int s = team;
         uint8_t *st = base + s * kStageBytes;
         const uint32_t slot = tmem + s * 256 + lane_base;
@@ -1103,6 +1130,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             if (tk < 0) break;  // the same ticket for every thread
             const PipeUnit u = decode_unit(pr, tk, nhb);
             const int c = u.c;
+            const bool tma_out = tma_tiles && (!pr.chunks || u.len == kRows);
             if (it >= 2 && !mbar_wait(&bar_pdone[s], ph ^ 1)) ok = false;
             // walk back to the nearest inclusive state; -2: S_c became ready first
             // (publish it as the aggregate, then walk on); -3: gave up
@@ -1131,7 +1159,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                                 top -= 32;
                                 continue;
                             }
-                            if (round == 0 && c < nc - 1 && mbar_test_wait(&bar_mma[s], ph)) {
+                            if (round == 0 && !u.last && mbar_test_wait(&bar_mma[s], ph)) {
                                 res = -2;
                                 break;
                             }
@@ -1214,7 +1242,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 if (ok && fast) {
                     mbar_expect_tx(&bar_xe[s], (uint32_t)(2 * kSlab));
                     for (int k = 0; k < 2; ++k)
-                        tma_load_3d(st + 2 * kSlab + k * kSlab, &xmap, &bar_xe[s], u.hb * 128 + 64 * k, u.t0, u.b);
+                        tma_load_3d(st + 2 * kSlab + k * kSlab, &xmap, &bar_xe[s], u.hb * 128 + 64 * k, u.tt, u.tb);
                 } else {
                     mbar_arrive(&bar_xe[s]);
                 }
@@ -1251,7 +1279,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             // releases its quarter, and the state counts as published at kParts
             if (ok) {
                 float4 *dst = reinterpret_cast<float4 *>(fa.incl + u.unit * ustride) + m;
-                float *fo = (c == nc - 1 && pr.final_state)
+                float *fo = (u.last && pr.final_state)
                                 ? pr.final_state + (((size_t)u.b * H + hg) * P + p_m) * NS
                                 : nullptr;
 #pragma unroll
@@ -1290,7 +1318,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             uint8_t *ystage = st + 2 * kSlab;
             if (ok && fast) {
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
-                                                       (((size_t)u.b * L + u.t0 + m) * H + u.h0) * P);
+                                                       ((u.tok + m) * H + u.h0) * P);
 #pragma unroll
                 for (int col = 0; col < 128; col += 64) {
                     const int hh = col / P, h = u.h0 + hh;
@@ -1326,14 +1354,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             if (tt == 0) {
                 mbar_arrive(&bar_slot[s]);  // Y has been read
                 if (all_ok && fast && tma_out) {
-                    for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, u.hb * 128 + 64 * k, u.t0, u.b);
+                    for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, u.hb * 128 + 64 * k, u.tt, u.tb);
                     bulk_commit();
                     bulk_wait_read_all();
                 }
                 if (!(all_ok && !fast)) mbar_arrive(&bar_lo[s]);  // the staging region is free again
             }
             if (all_ok && !fast) {
-                direct_unit_outputs(pr, NS, u.b, u.hb, u.c, reinterpret_cast<const float *>(st),
+                direct_unit_outputs(pr, NS, u.tok, u.len, u.hb, reinterpret_cast<const float *>(st),
                                     reinterpret_cast<float *>(st + 2 * kSlab), cs[ss], dtv[ss], tt, 128, bar_team);
                 named_sync(bar_team, 128);  // every thread is done with the stage
                 if (tt == 0) {
@@ -1390,17 +1418,22 @@ size_t fused_smem(int NS)
     return 1024 + body + hreg;
 }
 
-size_t units_of(const Problem &pr) { return (size_t)pr.batch * (pr.nheads / (128 / pr.headdim)) * pr.nchunks; }
+size_t units_of(const Problem &pr)
+{
+    const size_t nhb = pr.nheads / (128 / pr.headdim);
+    return nhb * (pr.chunks ? (size_t)pr.total_chunks : (size_t)pr.batch * pr.nchunks);
+}
 
 template <int NS>
 cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
 {
     CUtensorMap xmap, bmap, cmap, ymap;
     cudaError_t e;
-    if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, pr.batch)) != cudaSuccess) return e;
-    if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
-    if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
-    if ((e = make_map(&ymap, pr.y, pr.nheads * pr.headdim, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+    const int mb = pr.chunks ? 1 : pr.batch;  // packed sequences: one batch row of seqlen tokens
+    if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
+    if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
+    if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
+    if ((e = make_map(&ymap, pr.y, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
     const size_t units = units_of(pr);
     if ((e = cudaMemsetAsync(fa.aggcnt, 0, (2 * units + kCtrCount) * sizeof(uint32_t), s)) != cudaSuccess) return e;
     if constexpr (NS == 64) {
@@ -1409,7 +1442,7 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
         CUtensorMap dtmap;
         memset(&dtmap, 0, sizeof dtmap);
         int dt_tma = (pr.nheads % 4 == 0 && (reinterpret_cast<uintptr_t>(pr.dt) & 15) == 0) ? 1 : 0;
-        if (dt_tma && make_map_f32(&dtmap, pr.dt, pr.nheads, pr.seqlen, pr.batch) != cudaSuccess) dt_tma = 0;
+        if (dt_tma && make_map_f32(&dtmap, pr.dt, pr.nheads, pr.seqlen, mb) != cudaSuccess) dt_tma = 0;
         if ((e = cudaFuncSetAttribute(ssd_fused_pipe_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem)) !=
             cudaSuccess)
             return e;

@@ -34,6 +34,13 @@ enum : unsigned int {
     kDevErrBounds = 2u,   // a kernel-side consistency check failed
 };
 
+// One chunk of a packed variable-length sequence: sequence b, chunk c of it,
+// its index in the sequence-major numbering of all chunks, its first token in
+// the packed token dimension, its length, and whether it is the sequence's last.
+struct ChunkDesc {
+    int b, c, gchunk, tok0, len, last, pad0, pad1;
+};
+
 struct Problem {
     const void *x;
     const float *dt;          // step of each token: the decay is exp(dt A)
@@ -48,6 +55,13 @@ struct Problem {
     int batch, seqlen, nheads, headdim, ngroups, dstate, chunk;
     int nchunks;
     ssd_dtype_t dtype;
+    // Packed variable-length sequences (null: the batch layout).  Then batch is
+    // the number of sequences, seqlen the packed token count, every tensor's
+    // token dimension is the packed one (batch dimension 1), and chunks[k],
+    // k < total_chunks, lists the chunks in chunk-major order (every sequence's
+    // chunk 0, then every chunk 1, ...).
+    const ChunkDesc *chunks;
+    int total_chunks;
     unsigned int *err_word;   // device address of the error word
 };
 

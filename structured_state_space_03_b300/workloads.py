@@ -97,6 +97,41 @@ def make_inputs(batch, seqlen, nheads, headdim, dstate, ngroups, dtype="bf16", s
             "init_state": init}
 
 
+def make_varlen_inputs(lengths, nheads, headdim, dstate, ngroups, dtype="bf16", seed=0,
+                       dt_range=(1e-3, 1e-1), with_init=False, with_D=True):
+    """Draw one seeded packed input set on the CPU: the sequences of ``lengths``
+    back to back along one token dimension.
+
+    Returns the dict of ``make_inputs`` with the batch dimension dropped (x
+    [T,H,P], dt [T,H], B, C [T,G,N]; init_state [nseq,H,P,N] or None) plus
+    ``cu_seqlens`` (a list of nseq + 1 offsets).
+    """
+    lengths = [int(v) for v in lengths]
+    T = sum(lengths)
+    d = make_inputs(1, T, nheads, headdim, dstate, ngroups, dtype, seed, dt_range, False, with_D)
+    out = {k: (v[0] if k in ("x", "dt", "B", "C") else v) for k, v in d.items()}
+    if with_init:
+        g = torch.Generator(device="cpu")
+        g.manual_seed(int(seed) + 1)
+        out["init_state"] = torch.randn(len(lengths), nheads, headdim, dstate, generator=g, dtype=torch.float32)
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    out["cu_seqlens"] = cu
+    return out
+
+
+def varlen_lengths(total, nseq, seed, min_len=1):
+    """Seeded mix of nseq sequence lengths summing to total: lengths drawn
+    log-uniformly (short and long sequences together), then rescaled."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    w = torch.exp(torch.empty(nseq, dtype=torch.float64).uniform_(0.0, math.log(64.0), generator=g))
+    raw = (w / w.sum() * (total - nseq * min_len)).floor().long() + min_len
+    raw[-1] += total - int(raw.sum())
+    return [int(v) for v in raw]
+
+
 def workload_inputs(w: Workload):
     return make_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.dtype,
                        w.seed, w.dt_range, w.with_init)

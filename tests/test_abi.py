@@ -179,3 +179,27 @@ def test_pre_flags_and_bias_alignment(lib):
     # the shared checks of ssd_fwd still apply
     d["ngroups"] = 3
     assert lib.ssd_fwd_pre(*args(0, None)) == ssd.SSD_ERR_INVALID_ARG
+
+
+def _varlen(lib, cu, nseq=None, dstate=64, dtype=ssd.SSD_DTYPE_BF16, headdim=64):
+    p = ctypes.c_void_p(1 << 20)
+    offs = None if cu is None else (ctypes.c_int * len(cu))(*cu)
+    n = (len(cu) - 1) if nseq is None else nseq
+    return lib.ssd_fwd_varlen(p, p, p, p, p, None, offs, n, None, ctypes.c_void_p(2 << 20), None,
+                              8, headdim, 2, dstate, 128, dtype, None)
+
+
+def test_varlen_offsets_are_checked_before_any_launch(lib):
+    assert _varlen(lib, None, nseq=2) == ssd.SSD_ERR_INVALID_ARG
+    assert _varlen(lib, [0, 5], nseq=0) == ssd.SSD_ERR_INVALID_ARG
+    assert _varlen(lib, [1, 5]) == ssd.SSD_ERR_INVALID_ARG
+    assert "cu_seqlens[0]" in ssd.ssd_last_error_detail()
+    assert _varlen(lib, [0, 5, 4]) == ssd.SSD_ERR_INVALID_ARG
+    assert "decreases" in ssd.ssd_last_error_detail()
+
+
+def test_varlen_runs_only_where_the_persistent_kernel_does(lib):
+    assert _varlen(lib, [0, 5, 9], dstate=128) == ssd.SSD_ERR_UNSUPPORTED
+    assert _varlen(lib, [0, 5, 9], dtype=ssd.SSD_DTYPE_F32) == ssd.SSD_ERR_UNSUPPORTED
+    assert _varlen(lib, [0, 5, 9], headdim=32) == ssd.SSD_ERR_UNSUPPORTED
+    assert "persistent fused kernel" in ssd.ssd_last_error_detail()
