@@ -282,6 +282,53 @@ def pre_step_measurement(sets, w, stream, steps=100):
             "tokens_per_s": w.tokens / (t_pre * 1e-6), "kernels": ["pre_kernel", "ssd_fused_pipe_tc"]}
 
 
+def varlen_step_measurement(sets, w, stream, peaks, steps=100, nseq=12, seed=5):
+    """Packed variable-length sequences (ssd_fwd_varlen): the headline's
+    batch x seqlen tokens repacked as nseq sequences of seeded mixed lengths
+    (log-uniform over a 64x range), on the same heads, against ssd_fwd on the
+    batch layout of the same tokens.  Both allocate their workspace per call;
+    the packed call also builds and uploads its chunk table."""
+    import structured_state_space_03_b300 as ssd
+    total = w.batch * w.seqlen
+    lengths = wl.varlen_lengths(total, nseq, seed)
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    packed = [{k: d[k].reshape(total, *d[k].shape[2:]) for k in ("x", "dt", "B", "C", "y")} for d in sets]
+
+    def timed(fn):
+        for k in range(5):
+            fn(k)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for k in range(steps):
+            fn(k)
+        e.record(stream)
+        torch.cuda.synchronize()
+        ssd.ssd_check_device_status(stream)
+        return s.elapsed_time(e) / steps * 1e3
+
+    def batch(k):
+        d = sets[k % len(sets)]
+        ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], None, chunk=w.chunk, y=d["y"],
+                    return_final=False, stream=stream)
+
+    def varlen(k):
+        d, q = sets[k % len(sets)], packed[k % len(sets)]
+        ssd.ssd_fwd_varlen(q["x"], q["dt"], d["A"], q["B"], q["C"], d["D"], None, cu_seqlens=cu, chunk=w.chunk,
+                           y=q["y"], return_final=False, stream=stream)
+
+    t_batch, t_var = timed(batch), timed(varlen)
+    nbytes = unavoidable_bytes(w) - w.batch * w.nheads * w.headdim * w.dstate * 4  # no states in or out
+    return {"tokens": total, "sequences": nseq, "lengths": lengths, "chunk": w.chunk,
+            "heads": f"{w.nheads} x {w.headdim}, dstate {w.dstate}, {w.ngroups} group(s), {w.dtype}",
+            "us_per_step_ssd_fwd_varlen": t_var, "us_per_step_ssd_fwd_batch": t_batch,
+            "tokens_per_s": total / (t_var * 1e-6), "algorithmic_bytes": nbytes,
+            "frac_of_hbm": nbytes / (t_var * 1e-6) / (peaks["hbm_gbs"] * 1e9),
+            "kernels": ["ssd_fused_pipe_tc"]}
+
+
 def time_oracle(w, inp, seconds, cores):
     """Run the oracle over growing row batches until `seconds` elapse or every
     row is done; returns (tokens/s equivalent, rows done, elapsed)."""
@@ -501,6 +548,7 @@ def main():
         line["decode_step"] = decode_step_measurement(dev, peaks, stream)
         if w is wl.HEADLINE:
             line["pre_step"] = pre_step_measurement(sets, w, stream)
+            line["varlen_step"] = varlen_step_measurement(sets, w, stream, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
     if rank == 0:

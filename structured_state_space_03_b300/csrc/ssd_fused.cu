@@ -738,32 +738,30 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool pred)
 }
 
 // A unit: sequence b (a batch element or a packed sequence), chunk c of it, head
-// block hb.  tok is the global index of its first token (row of the token
-// dimension flattened over the batch), (tt, tb) its TMA coordinates, last
-// whether c is the sequence's last chunk.  Units of one (b, hb) have
-// consecutive indices in chunk order, so chunk k of the same sequence is
-// unit - (c - k).
+// block hb.  (tt, tb) are its TMA coordinates (first token, batch row); the
+// global index of its first token is tb * seqlen + tt in both layouts (packed
+// sequences sit in one batch row).  Units of one (b, hb) have consecutive
+// indices in chunk order, so chunk k of the same sequence is unit - (c - k).
 struct PipeUnit {
-    int b, hb, c, h0, g, tt, tb, len;
-    bool last;
-    size_t tok, unit;
+    int b, hb, c, h0, g, tt, tb, len, last;
+    size_t unit;
 };
 
+template <bool kPacked>
 __device__ __forceinline__ PipeUnit decode_unit(const Problem &pr, int ticket, int nhb)
 {
     PipeUnit u;
-    if (pr.chunks) {  // packed sequences: the chunk table is already chunk-major
+    if constexpr (kPacked) {  // packed sequences: the chunk table is already chunk-major
         const int k = ticket / nhb;
         u.hb = ticket - k * nhb;
         const int4 d0 = __ldg(reinterpret_cast<const int4 *>(pr.chunks + k));
         const int4 d1 = __ldg(reinterpret_cast<const int4 *>(pr.chunks + k) + 1);
         u.b = d0.x;
         u.c = d0.y;
-        u.tok = (size_t)d0.w;
         u.tt = d0.w;
         u.tb = 0;
         u.len = d1.x;
-        u.last = d1.y != 0;
+        u.last = d1.y;
         u.unit = (size_t)u.hb * pr.total_chunks + d0.z;
     } else {
         u.c = ticket / (pr.batch * nhb);
@@ -772,9 +770,8 @@ __device__ __forceinline__ PipeUnit decode_unit(const Problem &pr, int ticket, i
         u.hb = rest - u.b * nhb;
         u.tt = u.c * pr.chunk;
         u.tb = u.b;
-        u.tok = (size_t)u.b * pr.seqlen + u.tt;
         u.len = min(pr.chunk, pr.seqlen - u.tt);
-        u.last = u.c == pr.nchunks - 1;
+        u.last = 0;  // unit_is_last() derives it from c
         u.unit = ((size_t)u.b * nhb + u.hb) * pr.nchunks + u.c;
     }
     const int HB = 128 / pr.headdim;
@@ -783,6 +780,14 @@ __device__ __forceinline__ PipeUnit decode_unit(const Problem &pr, int ticket, i
     return u;
 }
 
+template <bool kPacked>
+__device__ __forceinline__ bool unit_is_last(const Problem &pr, const PipeUnit &u)
+{
+    if constexpr (kPacked) return u.last != 0;
+    return u.c == pr.nchunks - 1;
+}
+
+template <bool kPacked>
 __global__ void __launch_bounds__(kPipeThreads, 1)
     ssd_fused_pipe_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
                       const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap,
@@ -864,7 +869,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     if (++ends == 2 || !ok) break;
                     continue;
                 }
-                const PipeUnit u = decode_unit(pr, tk, nhb);
+                const PipeUnit u = decode_unit<kPacked>(pr, tk, nhb);
                 uint8_t *st = base + s * kStageBytes;
                 if (dt_tma) {  // dt[t0 .. t0+127][4 heads from h0 rounded down to 4]
                     mbar_expect_tx(&bar_dt[s], (uint32_t)(kRows * 4 * sizeof(float)));
@@ -951,7 +956,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 break;
             }
             if (tk < 0) break;  // the same ticket for every thread
-            const PipeUnit u = decode_unit(pr, tk, nhb);
+            const PipeUnit u = decode_unit<kPacked>(pr, tk, nhb);
             uint8_t *st = base + s * kStageBytes;
             const float *dts = reinterpret_cast<const float *>(base + 2 * kStageBytes + s * kDtBytes) + ft * 4 + (u.h0 & 3);
             if (dt_tma) ok = ok && mbar_wait(&bar_dt[s], ph);
@@ -961,9 +966,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 const bool act = hh < HB;
                 const float a = act ? __ldg(pr.A + u.h0 + hh) : 0.f;
                 d[hh] = (act && ft < u.len)
-                            ? (dt_tma ? dts[hh] : __ldg(pr.dt + (u.tok + ft) * H + u.h0 + hh))
+                            ? (dt_tma ? dts[hh] : __ldg(pr.dt + ((size_t)u.tb * pr.seqlen + u.tt + ft) * H + u.h0 + hh))
                             : 0.f;
-                din[hh] = pr.dtin ? ((act && ft < u.len) ? __ldg(pr.dtin + (u.tok + ft) * H + u.h0 + hh) : 0.f)
+                din[hh] = pr.dtin ? ((act && ft < u.len) ? __ldg(pr.dtin + ((size_t)u.tb * pr.seqlen + u.tt + ft) * H + u.h0 + hh) : 0.f)
                                   : d[hh];  // input scale
                 v[hh] = d[hh] * a;
 #pragma unroll
@@ -1097,7 +1102,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     s_fail = 1;
                     break;
                 }
-                if (!s_fail) red_release_add(fa.inclcnt + decode_unit(pr, tk, nhb).unit, 1u);
+                if (!s_fail) red_release_add(fa.inclcnt + decode_unit<kPacked>(pr, tk, nhb).unit, 1u);
                 mbar_arrive(&bar_pdone[s]);
             }
         }
@@ -1128,9 +1133,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 break;
             }
             if (tk < 0) break;  // the same ticket for every thread
-            const PipeUnit u = decode_unit(pr, tk, nhb);
+            const PipeUnit u = decode_unit<kPacked>(pr, tk, nhb);
             const int c = u.c;
-            const bool tma_out = tma_tiles && (!pr.chunks || u.len == kRows);
+            const bool tma_out = tma_tiles && (!kPacked || u.len == kRows);
             if (it >= 2 && !mbar_wait(&bar_pdone[s], ph ^ 1)) ok = false;
             // walk back to the nearest inclusive state; -2: S_c became ready first
             // (publish it as the aggregate, then walk on); -3: gave up
@@ -1159,7 +1164,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                                 top -= 32;
                                 continue;
                             }
-                            if (round == 0 && !u.last && mbar_test_wait(&bar_mma[s], ph)) {
+                            if (round == 0 && !unit_is_last<kPacked>(pr, u) && mbar_test_wait(&bar_mma[s], ph)) {
                                 res = -2;
                                 break;
                             }
@@ -1279,7 +1284,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             // releases its quarter, and the state counts as published at kParts
             if (ok) {
                 float4 *dst = reinterpret_cast<float4 *>(fa.incl + u.unit * ustride) + m;
-                float *fo = (u.last && pr.final_state)
+                float *fo = (unit_is_last<kPacked>(pr, u) && pr.final_state)
                                 ? pr.final_state + (((size_t)u.b * H + hg) * P + p_m) * NS
                                 : nullptr;
 #pragma unroll
@@ -1318,7 +1323,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             uint8_t *ystage = st + 2 * kSlab;
             if (ok && fast) {
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
-                                                       ((u.tok + m) * H + u.h0) * P);
+                                                       (((size_t)u.tb * pr.seqlen + u.tt + m) * H + u.h0) * P);
 #pragma unroll
                 for (int col = 0; col < 128; col += 64) {
                     const int hh = col / P, h = u.h0 + hh;
@@ -1361,7 +1366,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 if (!(all_ok && !fast)) mbar_arrive(&bar_lo[s]);  // the staging region is free again
             }
             if (all_ok && !fast) {
-                direct_unit_outputs(pr, NS, u.tok, u.len, u.hb, reinterpret_cast<const float *>(st),
+                direct_unit_outputs(pr, NS, (size_t)u.tb * pr.seqlen + u.tt, u.len, u.hb, reinterpret_cast<const float *>(st),
                                     reinterpret_cast<float *>(st + 2 * kSlab), cs[ss], dtv[ss], tt, 128, bar_team);
                 named_sync(bar_team, 128);  // every thread is done with the stage
                 if (tt == 0) {
@@ -1443,14 +1448,14 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
         memset(&dtmap, 0, sizeof dtmap);
         int dt_tma = (pr.nheads % 4 == 0 && (reinterpret_cast<uintptr_t>(pr.dt) & 15) == 0) ? 1 : 0;
         if (dt_tma && make_map_f32(&dtmap, pr.dt, pr.nheads, pr.seqlen, mb) != cudaSuccess) dt_tma = 0;
-        if ((e = cudaFuncSetAttribute(ssd_fused_pipe_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem)) !=
-            cudaSuccess)
+        auto kern = pr.chunks ? ssd_fused_pipe_tc<true> : ssd_fused_pipe_tc<false>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem)) != cudaSuccess)
             return e;
         int dev = 0, nsm = 0;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
         const unsigned grid = (unsigned)std::min<size_t>(units, (size_t)nsm);
-        ssd_fused_pipe_tc<<<grid, kPipeThreads, psmem, s>>>(xmap, bmap, cmap, ymap, dtmap, pr, fa, (int)units, dt_tma);
+        kern<<<grid, kPipeThreads, psmem, s>>>(xmap, bmap, cmap, ymap, dtmap, pr, fa, (int)units, dt_tma);
     } else {
         const size_t smem = fused_smem(NS);
         if ((e = cudaFuncSetAttribute(ssd_fused_tc<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
