@@ -316,9 +316,9 @@ ssd_status_t ssd_fwd_varlen(const void *x, const float *dt, const float *A, cons
     ssd_status_t st = make_problem(pr, x, dt, A, B, C, D, init_state, y, final_state, nseq, total, nheads, headdim,
                                    ngroups, dstate, chunk, dtype);
     if (st != SSD_OK) return st;
-    if (choose_path(pr) != SSD_PATH_TCGEN05_FUSED || dstate != 64)
+    if (choose_path(pr) != SSD_PATH_TCGEN05_FUSED)
         return fail(SSD_ERR_UNSUPPORTED,
-                    "packed sequences run on the persistent fused kernel: bf16, headdim 64 or 128, dstate 64, "
+                    "packed sequences run on the fused kernels: bf16, headdim 64 or 128, dstate 64 or 128, "
                     "chunk <= 128, nheads / ngroups a multiple of 128 / headdim");
     // chunk table in chunk-major order (a counting sort over the chunk index)
     std::vector<int> nchunk(nseq);

@@ -212,7 +212,7 @@ __device__ void direct_unit_outputs(const Problem &pr, int NS, size_t tok0, int 
     }
 }
 
-template <int NS>
+template <int NS, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 2)
     ssd_fused_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
                  const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap, Problem pr,
@@ -257,14 +257,36 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t tmem = tmem_slot;
     const uint32_t col_y = 0, col_st = 128;   // Y (G first), chunk state
 
-    // chunk-major unit order: every predecessor chunk has a smaller ticket
+    // chunk-major unit order: every predecessor chunk has a smaller ticket.  (tt, tb):
+    // TMA coordinates of the first token, whose global index is tb * seqlen + tt
+    // (packed sequences sit in one batch row); units of one (b, hb) are consecutive
+    // in chunk order
     const int ticket = (int)s_ticket;
-    const int c = ticket / (pr.batch * nhb);
-    const int rest = ticket - c * (pr.batch * nhb);
-    const int b = rest / nhb, hb = rest - (rest / nhb) * nhb;
+    int c, b, hb, tt, tb, len, lastflag = 0;
+    size_t unit;
+    if constexpr (kPacked) {
+        const int k = ticket / nhb;
+        hb = ticket - k * nhb;
+        const int4 d0 = __ldg(reinterpret_cast<const int4 *>(pr.chunks + k));
+        const int4 d1 = __ldg(reinterpret_cast<const int4 *>(pr.chunks + k) + 1);
+        b = d0.x;
+        c = d0.y;
+        tt = d0.w;
+        tb = 0;
+        len = d1.x;
+        lastflag = d1.y;
+        unit = (size_t)hb * pr.total_chunks + d0.z;
+    } else {
+        c = ticket / (pr.batch * nhb);
+        const int rest = ticket - c * (pr.batch * nhb);
+        b = rest / nhb;
+        hb = rest - b * nhb;
+        tt = c * pr.chunk;
+        tb = b;
+        len = min(pr.chunk, L - tt);
+        unit = ((size_t)b * nhb + hb) * nc + c;
+    }
     const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
-    const int t0 = c * pr.chunk, len = min(pr.chunk, L - t0);
-    const size_t unit = ((size_t)b * nhb + hb) * nc + c;   // (b, hb, c) in the workspace
 
     uint8_t *base = align1024(smem_raw);
     uint8_t *xs = base;                              // x: 2 MN blocks x 16 KiB
@@ -278,10 +300,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_prefetch_desc(&bmap);
         tma_prefetch_desc(&cmap);
         mbar_expect_tx(&bar_ld, (uint32_t)((2 + 2 * NSL) * kSlab));
-        for (int k = 0; k < 2; ++k) tma_load_3d(xs + k * kSlab, &xmap, &bar_ld, hb * 128 + 64 * k, t0, b);
+        for (int k = 0; k < 2; ++k) tma_load_3d(xs + k * kSlab, &xmap, &bar_ld, hb * 128 + 64 * k, tt, tb);
         for (int s = 0; s < NSL; ++s) {
-            tma_load_3d(bs + s * kSlab, &bmap, &bar_ld, g * NS + 64 * s, t0, b);
-            tma_load_3d(cm + s * kSlab, &cmap, &bar_ld, g * NS + 64 * s, t0, b);
+            tma_load_3d(bs + s * kSlab, &bmap, &bar_ld, g * NS + 64 * s, tt, tb);
+            tma_load_3d(cm + s * kSlab, &cmap, &bar_ld, g * NS + 64 * s, tt, tb);
         }
     }
 
@@ -291,9 +313,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int hh = half, t = tid & 127;
         const bool active = hh < HB;
         const float a = active ? __ldg(pr.A + h0 + hh) : 0.f;
-        const float d = (active && t < len) ? __ldg(pr.dt + ((size_t)b * L + t0 + t) * H + h0 + hh) : 0.f;
+        const float d = (active && t < len) ? __ldg(pr.dt + ((size_t)tb * L + tt + t) * H + h0 + hh) : 0.f;
         const float din =  // input scale
-            pr.dtin ? ((active && t < len) ? __ldg(pr.dtin + ((size_t)b * L + t0 + t) * H + h0 + hh) : 0.f) : d;
+            pr.dtin ? ((active && t < len) ? __ldg(pr.dtin + ((size_t)tb * L + tt + t) * H + h0 + hh) : 0.f) : d;
         float v = d * a;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -448,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
     if (ok && fast && tid == 0) {  // B is consumed: bring C back for the off-diagonal product
         mbar_expect_tx(&bar_c, (uint32_t)(NSL * kSlab));
-        for (int s = 0; s < NSL; ++s) tma_load_3d(bs + s * kSlab, &cmap, &bar_c, g * NS + 64 * s, t0, b);
+        for (int s = 0; s < NSL; ++s) tma_load_3d(bs + s * kSlab, &cmap, &bar_c, g * NS + 64 * s, tt, tb);
     }
 
     // ---- state passing by decoupled look-back; this thread: row m = (head, headdim),
@@ -596,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 __stcg(dst + q * kRows, make_float4(sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3]));
-            if (c == nc - 1 && pr.final_state) {
+            if ((kPacked ? lastflag != 0 : c == nc - 1) && pr.final_state) {
                 float4 *fo = reinterpret_cast<float4 *>(pr.final_state + (((size_t)b * H + hg) * P + p_m) * NS + n0 + cc);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) fo[q] = make_float4(sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3]);
@@ -635,7 +657,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
 
     // ---- y = r_i Y + D x; this thread: row i, 64 of the 128 (head, headdim) columns
-    const bool tma_out = pr.chunk == kRows;  // full 128-row tiles: staged in shared memory, TMA store
+    // full 128-row tiles: staged in shared memory, TMA store (a packed sequence's partial
+    // chunk is stored row by row: the rows after it belong to the next sequence)
+    const bool tma_out = pr.chunk == kRows && (!kPacked || len == kRows);
     uint8_t *ystage = cm;
     if (ok && fast) {
         const int i = m, col0 = half * 64;
@@ -666,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     *reinterpret_cast<uint4 *>(ystage + half * kSlab + sw128(i, pc / 8 + u)) = outv[u];
             } else if (i < len) {
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
-                                                       (((size_t)b * L + t0 + i) * H + h0) * P + col);
+                                                       (((size_t)tb * L + tt + i) * H + h0) * P + col);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) dst[u] = outv[u];
             }
@@ -676,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         fence_async_smem();
         __syncthreads();
         if (ok && fast && tid == 0) {
-            for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, hb * 128 + 64 * k, t0, b);
+            for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, hb * 128 + 64 * k, tt, tb);
             bulk_commit();
             bulk_wait_read_all();
         }
@@ -686,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
     if (ok && !fast)  // decay range too wide for the factored form: direct outputs (C_i . B_j over x)
-        direct_unit_outputs(pr, NS, (size_t)b * L + t0, len, hb, reinterpret_cast<const float *>(hh_s),
+        direct_unit_outputs(pr, NS, (size_t)tb * L + tt, len, hb, reinterpret_cast<const float *>(hh_s),
                             reinterpret_cast<float *>(xs),
                             cs, dtv, tid, kThreads, 0);
 }
@@ -871,7 +895,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 }
                 const PipeUnit u = decode_unit<kPacked>(pr, tk, nhb);
                 uint8_t *st = base + s * kStageBytes;
-                if (dt_tma) {  // dt[t0 .. t0+127][4 heads from h0 rounded down to 4]
+                if (dt_tma) {  // dt of the unit's 128 tokens x 4 heads from h0 rounded down to 4
                     mbar_expect_tx(&bar_dt[s], (uint32_t)(kRows * 4 * sizeof(float)));
                     tma_load_3d(base + 2 * kStageBytes + s * kDtBytes, &dtmap, &bar_dt[s], u.h0 & ~3, u.tt, u.tb);
                 } else {
@@ -1458,10 +1482,10 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
         kern<<<grid, kPipeThreads, psmem, s>>>(xmap, bmap, cmap, ymap, dtmap, pr, fa, (int)units, dt_tma);
     } else {
         const size_t smem = fused_smem(NS);
-        if ((e = cudaFuncSetAttribute(ssd_fused_tc<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-            cudaSuccess)
+        auto kern = pr.chunks ? ssd_fused_tc<NS, true> : ssd_fused_tc<NS, false>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
             return e;
-        ssd_fused_tc<NS><<<(unsigned)units, kThreads, smem, s>>>(xmap, bmap, cmap, ymap, pr, fa);
+        kern<<<(unsigned)units, kThreads, smem, s>>>(xmap, bmap, cmap, ymap, pr, fa);
     }
     return cudaGetLastError();
 }

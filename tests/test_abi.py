@@ -198,8 +198,8 @@ def test_varlen_offsets_are_checked_before_any_launch(lib):
     assert "decreases" in ssd.ssd_last_error_detail()
 
 
-def test_varlen_runs_only_where_the_persistent_kernel_does(lib):
-    assert _varlen(lib, [0, 5, 9], dstate=128) == ssd.SSD_ERR_UNSUPPORTED
+def test_varlen_runs_only_where_the_fused_kernels_do(lib):
+    assert _varlen(lib, [0, 5, 9], dstate=256) == ssd.SSD_ERR_UNSUPPORTED
     assert _varlen(lib, [0, 5, 9], dtype=ssd.SSD_DTYPE_F32) == ssd.SSD_ERR_UNSUPPORTED
     assert _varlen(lib, [0, 5, 9], headdim=32) == ssd.SSD_ERR_UNSUPPORTED
-    assert "persistent fused kernel" in ssd.ssd_last_error_detail()
+    assert "fused kernels" in ssd.ssd_last_error_detail()

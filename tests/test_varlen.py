@@ -52,6 +52,8 @@ CASES = [
     ([700, 1, 128, 0, 255, 129, 64, 3], 8, 64, 64, 2, 128),
     ([300, 77, 0, 128, 1, 500], 4, 128, 64, 2, 100),
     ([17, 200, 33, 64, 65, 0, 0, 190], 6, 64, 64, 3, 64),
+    ([400, 0, 1, 127, 129, 60], 4, 64, 128, 1, 128),    # dstate 128: the one-unit fused kernel
+    ([250, 3, 128, 0, 77], 4, 128, 128, 2, 96),
 ]
 
 
@@ -122,7 +124,7 @@ def test_state_carried_in_place_and_empty_sequences():
 
 
 def test_unsupported_sizes_are_rejected():
-    d = _cuda_inputs(make_varlen_inputs([10, 20], 4, 64, 128, 1, "bf16", seed=41))
+    d = _cuda_inputs(make_varlen_inputs([10, 20], 4, 64, 256, 1, "bf16", seed=41))
     with pytest.raises(ssd.SsdError) as err:
         ssd.ssd_fwd_varlen(d["x"], d["dt"], d["A"], d["B"], d["C"], cu_seqlens=[0, 10, 30], chunk=128)
     assert err.value.status == ssd.SSD_ERR_UNSUPPORTED
