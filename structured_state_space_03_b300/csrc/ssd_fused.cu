@@ -1276,6 +1276,31 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     mbar_arrive(&bar_xe[s]);
                 }
             }
+            // h_{c+1} = a_c h_c + S_c (S_c referenced to the chunk end), 32 columns at a
+            // time, stored as it is formed: it is what the successors wait for, so it
+            // goes out before the h_c operand of this unit's own off-diagonal product
+            if (ok) {
+                const float sfac = s_sfac[ss][hh_m], a_own = s_alpha[ss][hh_m];
+                float4 *dst = reinterpret_cast<float4 *>(fa.incl + u.unit * ustride) + m;
+                const bool wf = unit_is_last<kPacked>(pr, u) && pr.final_state;
+#pragma unroll
+                for (int cc = 0; cc < NS; cc += 32) {
+                    float sc[32];
+                    tmem_ld32(slot + col_st + cc, sc);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) sc[k] = fmaf(a_own, acc[cc + k], sfac * sc[k]);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 vv = make_float4(sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3]);
+                        __stcg(dst + (cc / 4 + q) * kRows, vv);
+                        if (wf)
+                            reinterpret_cast<float4 *>(pr.final_state + (((size_t)u.b * H + hg) * P + p_m) * NS)[cc / 4 + q] =
+                                vv;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_pincl[s]);  // the team's publisher releases h_{c+1}
             if (ok) {
                 if (fast) {  // e^ref h_c -> bf16 hi / lo K-major slabs over the dead wx hi
                     const float ysc = s_ysc[ss][hh_m];
@@ -1294,32 +1319,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
 #pragma unroll
                     for (int k = 0; k < NS; ++k) hcs[k] = acc[k];
                 }
-                // h_{c+1} = a_c h_c + S_c (S_c referenced to the chunk end), in place
-                const float sfac = s_sfac[ss][hh_m], a_own = s_alpha[ss][hh_m];
-#pragma unroll
-                for (int cc = 0; cc < NS; cc += 32) {
-                    float sc[32];
-                    tmem_ld32(slot + col_st + cc, sc);
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) acc[cc + k] = fmaf(a_own, acc[cc + k], sfac * sc[k]);
-                }
             }
-            // publish h_{c+1} first (it is what the successors wait for): each warp
-            // releases its quarter, and the state counts as published at kParts
-            if (ok) {
-                float4 *dst = reinterpret_cast<float4 *>(fa.incl + u.unit * ustride) + m;
-                float *fo = (unit_is_last<kPacked>(pr, u) && pr.final_state)
-                                ? pr.final_state + (((size_t)u.b * H + hg) * P + p_m) * NS
-                                : nullptr;
-#pragma unroll
-                for (int q = 0; q < NS / 4; ++q) {
-                    const float4 vv = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-                    __stcg(dst + q * kRows, vv);
-                    if (fo) reinterpret_cast<float4 *>(fo)[q] = vv;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_pincl[s]);  // the team's publisher releases h_{c+1}
             fence_async_smem();
             tc_fence_before();
             bool any_fail = named_sync_or(bar_team, 128, !ok);
