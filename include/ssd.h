@@ -136,8 +136,11 @@ SSD_API ssd_status_t ssd_fwd_ws(const void *x, const float *dt, const float *A, 
  * elements, or whole-chunk token ranges of each sequence with the state carried
  * from one range to the next -- so that uploads (on a library-owned stream),
  * the scan (on `stream`) and downloads (on a second library-owned stream)
- * overlap.  Device buffers come from the stream-ordered allocator and are
- * released before return.  Pinned host memory gives the fastest copies and the
+ * overlap.  Device buffers come from a library-owned stream-ordered memory
+ * pool (one per device) and go back to it before return; the pool keeps that
+ * memory for later calls (about twice the call's input size, the largest call
+ * so far) until the process exits, so a loop of calls does not map device
+ * memory again each time.  Pinned host memory gives the fastest copies and the
  * overlap; pageable memory works.  Calls on one device are serialised (they
  * share the copy streams).  Same error codes as ssd_fwd; a device-side error is
  * returned directly.

@@ -483,13 +483,17 @@ ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float *A, con
 // Host-buffer entry: the problem is cut into at most kHostParts parts.
 constexpr int kHostParts = 8;
 
-// Copy streams and events of the host-buffer entry, one set per device, made on
-// first use; calls on one device take its lock for their whole duration.
+// Copy streams, events and device memory pool of the host-buffer entry, one set
+// per device, made on first use; calls on one device take its lock for their
+// whole duration.  The pool keeps the memory of earlier calls (its release
+// threshold is unlimited), so a call in a loop does not map its ~2x input size
+// of device memory again each time; the process's default pool is left as it is.
 struct HostCopyRes {
     std::mutex mu;
     bool made = false;
     cudaStream_t in = nullptr, out = nullptr;
     cudaEvent_t ev[2 * kHostParts + 2];
+    cudaMemPool_t pool = nullptr;
 };
 
 static ssd_status_t host_copy_res(HostCopyRes **res)
@@ -507,7 +511,18 @@ static ssd_status_t host_copy_res(HostCopyRes **res)
             e = cudaStreamCreateWithFlags(&r.out, cudaStreamNonBlocking);
         for (int k = 0; k < 2 * kHostParts + 2 && e == cudaSuccess; ++k)
             e = cudaEventCreateWithFlags(&r.ev[k], cudaEventDisableTiming);
-        if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "copy stream or event creation failed: %s", cudaGetErrorString(e));
+        if (e == cudaSuccess) {
+            cudaMemPoolProps props;
+            memset(&props, 0, sizeof props);
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            e = cudaMemPoolCreate(&r.pool, &props);
+            uint64_t keep = ~uint64_t(0);
+            if (e == cudaSuccess) e = cudaMemPoolSetAttribute(r.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        }
+        if (e != cudaSuccess)
+            return fail(SSD_ERR_CUDA, "copy stream, event or memory pool creation failed: %s", cudaGetErrorString(e));
         r.made = true;
     }
     *res = &r;
@@ -578,7 +593,7 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
     off[0] = 0;
     for (int i = 0; i < 10; ++i) off[i + 1] = align_up(off[i] + sizes[i], 256);
     char *dev = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&dev), off[10], s);
+    cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&dev), off[10], res->pool, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(e == cudaErrorMemoryAllocation ? SSD_ERR_NO_MEMORY : SSD_ERR_CUDA,
