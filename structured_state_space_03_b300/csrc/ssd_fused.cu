@@ -804,6 +804,96 @@ __device__ __forceinline__ PipeUnit decode_unit(const Problem &pr, int ticket, i
     return u;
 }
 
+// Direct fp32 evaluation of a wide unit's outputs in the persistent kernel.
+// Thread m of the team is token m of the chunk.  G = C B^T (fp32 sums of the
+// bf16 products) is still in the unit's TMEM accumulator, row m at g_taddr:
+// such a unit skips the diagonal and off-diagonal products.  Per head and
+// 64-column block, y_m = exp(cs_m) C_m . h_c + sum_{j<=m} G_mj exp(cs_m - cs_j)
+// dt_j x_j + D x_m, each weight formed once per (m, j, head).  The sums live in
+// `accs` ([64 columns][128 tokens] fp32, 32 KiB of shared memory, so a warp's
+// accesses fall in distinct banks), which keeps this rarely taken path light
+// on registers.  `hcs` is h_c, [128 rows (head, headdim)][64] fp32 in shared
+// memory; cs and dtv are the unit's per-token cs and input scale, [2][128].
+__device__ void direct_unit_tmem(const Problem &pr, size_t tok0, int len, int h0, uint32_t g_taddr,
+                                 const float *hcs, float *accs, const float *cs, const float *dtv, int m)
+{
+    constexpr int NS = 64;
+    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, G = pr.ngroups, g = h0 / (H / G);
+    const bool row = m < len;
+    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(pr.x);
+    const uint4 *crow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(pr.C) +
+                                                        ((tok0 + (row ? m : 0)) * G + g) * NS);
+    for (int hh = 0; hh < HB; ++hh) {
+        const int h = h0 + hh;
+        const float *csh = cs + hh * kRows, *dth = dtv + hh * kRows;
+        const float csm = csh[m], ecs = expf(csm);
+        const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
+        for (int pc = 0; pc < P; pc += 64) {
+            // exp(cs_m) C_m . h_c
+            for (int p = 0; p < 64; ++p) {
+                const float *hr = hcs + (size_t)(hh * P + pc + p) * NS;
+                float off = 0.f;
+                if (row) {
+#pragma unroll
+                    for (int q = 0; q < NS / 8; ++q) {
+                        const uint4 cv = __ldg(crow + q);
+                        const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&cv);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 t = __bfloat1622float2(c2[e]);
+                            off = fmaf(t.x, hr[8 * q + 2 * e], off);
+                            off = fmaf(t.y, hr[8 * q + 2 * e + 1], off);
+                        }
+                    }
+                }
+                accs[p * kRows + m] = ecs * off;
+            }
+            // + sum_{j <= m} G_mj exp(cs_m - cs_j) dt_j x_j
+            for (int jb = 0; jb < 8; ++jb) {
+                float gv[16];
+                tmem_ld16(g_taddr + jb * 16, gv);  // warp-collective: every lane, every row
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int j = jb * 16 + k;
+                    if (!row || j > m) continue;
+                    const float w = gv[k] * expf(csm - csh[j]) * dth[j];
+                    const uint4 *xr = reinterpret_cast<const uint4 *>(x + ((tok0 + j) * H + h) * P + pc);
+#pragma unroll 1
+                    for (int q = 0; q < 8; ++q) {
+                        const uint4 xv = __ldg(xr + q);
+                        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 t = __bfloat1622float2(x2[e]);
+                            float *a0 = accs + (8 * q + 2 * e) * kRows + m;
+                            a0[0] = fmaf(w, t.x, a0[0]);
+                            a0[kRows] = fmaf(w, t.y, a0[kRows]);
+                        }
+                    }
+                }
+            }
+            if (row) {  // + D x_m, rounded to bf16 and stored
+                const size_t base = ((tok0 + m) * H + h) * P + pc;
+                const uint4 *xm = reinterpret_cast<const uint4 *>(x + base);
+                uint4 *ym = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) + base);
+#pragma unroll 1
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 xv = __ldg(xm + q);
+                    const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                    float o[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 t = __bfloat1622float2(x2[e]);
+                        o[2 * e] = fmaf(Dh, t.x, accs[(8 * q + 2 * e) * kRows + m]);
+                        o[2 * e + 1] = fmaf(Dh, t.y, accs[(8 * q + 2 * e + 1) * kRows + m]);
+                    }
+                    ym[q] = pack8(o);
+                }
+            }
+        }
+    }
+}
+
 template <bool kPacked>
 __device__ __forceinline__ bool unit_is_last(const Problem &pr, const PipeUnit &u)
 {
@@ -1381,7 +1471,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             tc_fence_before();
             const bool all_ok = !named_sync_or(bar_team, 128, !ok);
             if (tt == 0) {
-                mbar_arrive(&bar_slot[s]);  // Y has been read
+                if (!(all_ok && !fast)) mbar_arrive(&bar_slot[s]);  // Y has been read (a wide unit reads G below)
                 if (all_ok && fast && tma_out) {
                     for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, u.hb * 128 + 64 * k, u.tt, u.tb);
                     bulk_commit();
@@ -1390,10 +1480,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 if (!(all_ok && !fast)) mbar_arrive(&bar_lo[s]);  // the staging region is free again
             }
             if (all_ok && !fast) {
-                direct_unit_outputs(pr, NS, (size_t)u.tb * pr.seqlen + u.tt, u.len, u.hb, reinterpret_cast<const float *>(st),
-                                    reinterpret_cast<float *>(st + 2 * kSlab), cs[ss], dtv[ss], tt, 128, bar_team);
-                named_sync(bar_team, 128);  // every thread is done with the stage
+                tc_fence_after();
+                direct_unit_tmem(pr, (size_t)u.tb * pr.seqlen + u.tt, u.len, u.h0, slot + col_y,
+                                 reinterpret_cast<const float *>(st), reinterpret_cast<float *>(st + 2 * kSlab),
+                                 cs[ss], dtv[ss], m);
+                tc_fence_before();
+                named_sync(bar_team, 128);  // every thread is done with the stage and the TMEM slot
                 if (tt == 0) {
+                    mbar_arrive(&bar_slot[s]);
                     mbar_arrive(&bar_lo[s]);
                     mbar_arrive(&bar_free[s]);
                 }
