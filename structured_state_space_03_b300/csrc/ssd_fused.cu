@@ -809,7 +809,7 @@ __device__ __forceinline__ PipeUnit decode_unit(const Problem &pr, int ticket, i
 // bf16 products) is still in the unit's TMEM accumulator, row m at g_taddr:
 // such a unit skips the diagonal and off-diagonal products.  Per head and
 // 64-column block, y_m = exp(cs_m) C_m . h_c + sum_{j<=m} G_mj exp(cs_m - cs_j)
-// dt_j x_j + D x_m, each weight formed once per (m, j, head).  The sums live in
+// dt_j x_j + D x_m, each weight formed once per (m, j, head, block).  The sums live in
 // `accs` ([64 columns][128 tokens] fp32, 32 KiB of shared memory, so a warp's
 // accesses fall in distinct banks), which keeps this rarely taken path light
 // on registers.  `hcs` is h_c, [128 rows (head, headdim)][64] fp32 in shared
