@@ -159,55 +159,103 @@ struct FusedArgs {
     uint32_t *counters;  // ticket
 };
 
-// Direct fp32 evaluation of this unit's outputs with per-element decays, for a
-// chunk whose decay range is too wide for the factored form.  `hcs` holds h_c
-// ([128][NS] fp32, rows (head, headdim)); `gsm` (32 KiB) receives C_i . B_j for
-// 64 output rows at a time.  Slow, and used only for such chunks.
 // Named barrier `id` over `n` threads (id 0 with the whole CTA is __syncthreads).
 __device__ __forceinline__ void named_sync(int id, int n)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Evaluation is shared by the `gn` threads numbered `gt` of barrier `bar_id`.
-__device__ void direct_unit_outputs(const Problem &pr, int NS, size_t tok0, int len, int hb, const float *hcs,
-                                    float *gsm, const float *cs, const float *dtv, int gt, int gn, int bar_id)
+// Direct fp32 evaluation of a wide unit's outputs (decay range beyond the
+// factored form).  Token m of the chunk is handled by kThr threads (`part` =
+// 0 .. kThr-1), each taking 64 / kThr columns of every 64-column block.  G = C B^T
+// (fp32 sums of the bf16 products) is still in the unit's TMEM accumulator,
+// row m at g_taddr: such a unit skips the diagonal and off-diagonal products.
+// Per head and block, y_m = exp(cs_m) C_m . h_c + sum_{j<=m} G_mj
+// exp(cs_m - cs_j) dt_j x_j + D x_m, each weight formed once per (m, j, head,
+// block, part).  The sums live in `accs` ([64 columns][128 tokens] fp32, 32 KiB
+// of shared memory, so a warp's accesses fall in distinct banks), which keeps
+// this rarely taken path light on registers.  `hcs` is h_c, [128 rows (head,
+// headdim)][NS] fp32 in shared memory; cs and dtv are the unit's per-token cs
+// and input scale, [2][128].
+template <int NS, int kThr>
+__device__ void direct_unit_tmem(const Problem &pr, size_t tok0, int len, int h0, uint32_t g_taddr,
+                                 const float *hcs, float *accs, const float *cs, const float *dtv, int m, int part)
 {
-    const int tid = gt;
-    const int P = pr.headdim, HB = 128 / P, H = pr.nheads;
-    const int h0 = hb * HB, G = pr.ngroups, g = h0 / (H / G);
+    constexpr int kW = 64 / kThr;  // columns of a block per thread
+    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, G = pr.ngroups, g = h0 / (H / G);
+    const bool row = m < len;
     const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(pr.x);
-    const __nv_bfloat16 *Bm = static_cast<const __nv_bfloat16 *>(pr.B);
-    const __nv_bfloat16 *Cm = static_cast<const __nv_bfloat16 *>(pr.C);
-    for (int i0 = 0; i0 < kRows; i0 += 64) {
-        named_sync(bar_id, gn);
-        for (int e = tid; e < 64 * kRows; e += gn) {  // causal part of C_i . B_j, rows i0 .. i0+63
-            const int i = i0 + (e >> 7), j = e & 127;
-            float s = 0.f;
-            if (i < len && j <= i) {
-                const __nv_bfloat16 *ci = Cm + ((tok0 + i) * G + g) * NS;
-                const __nv_bfloat16 *bj = Bm + ((tok0 + j) * G + g) * NS;
-                for (int n = 0; n < NS; ++n) s = fmaf(__bfloat162float(ci[n]), __bfloat162float(bj[n]), s);
+    const uint4 *crow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(pr.C) +
+                                                        ((tok0 + (row ? m : 0)) * G + g) * NS);
+    for (int hh = 0; hh < HB; ++hh) {
+        const int h = h0 + hh;
+        const float *csh = cs + hh * kRows, *dth = dtv + hh * kRows;
+        const float csm = csh[m], ecs = expf(csm);
+        const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
+        for (int pb = 0; pb < P; pb += 64) {
+            const int pc = pb + part * kW;  // this thread's first column
+            float *acp = accs + part * kW * kRows;
+            // exp(cs_m) C_m . h_c
+            for (int p = 0; p < kW; ++p) {
+                const float *hr = hcs + (size_t)(hh * P + pc + p) * NS;
+                float off = 0.f;
+                if (row) {
+#pragma unroll
+                    for (int q = 0; q < NS / 8; ++q) {
+                        const uint4 cv = __ldg(crow + q);
+                        const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&cv);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 t = __bfloat1622float2(c2[e]);
+                            off = fmaf(t.x, hr[8 * q + 2 * e], off);
+                            off = fmaf(t.y, hr[8 * q + 2 * e + 1], off);
+                        }
+                    }
+                }
+                acp[p * kRows + m] = ecs * off;
             }
-            gsm[e] = s;
-        }
-        named_sync(bar_id, gn);
-        for (int o = tid; o < 64 * kRows; o += gn) {
-            const int i = i0 + (o >> 7), col = o & 127;  // col = (head, headdim) within the block
-            if (i >= len) continue;
-            const int hh = col / P, p = col % P, h = h0 + hh;
-            const float *csh = cs + hh * kRows, *dth = dtv + hh * kRows;
-            float acc = 0.f;
-            for (int j = 0; j <= i; ++j)
-                acc = fmaf(gsm[(i - i0) * kRows + j] * expf(csh[i] - csh[j]) * dth[j],
-                           __bfloat162float(x[((tok0 + j) * H + h) * P + p]), acc);
-            float off = 0.f;
-            const __nv_bfloat16 *ci = Cm + ((tok0 + i) * G + g) * NS;
-            for (int n = 0; n < NS; ++n) off = fmaf(__bfloat162float(ci[n]), hcs[col * NS + n], off);
-            const size_t yi = ((tok0 + i) * H + h) * P + p;
-            const float Dh = pr.D ? pr.D[h] : 0.f;
-            static_cast<__nv_bfloat16 *>(pr.y)[yi] =
-                __float2bfloat16_rn(acc + expf(csh[i]) * off + Dh * __bfloat162float(x[yi]));
+            // + sum_{j <= m} G_mj exp(cs_m - cs_j) dt_j x_j
+            for (int jb = 0; jb < 8; ++jb) {
+                float gv[16];
+                tmem_ld16(g_taddr + jb * 16, gv);  // warp-collective: every lane, every row
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int j = jb * 16 + k;
+                    if (!row || j > m) continue;
+                    const float w = gv[k] * expf(csm - csh[j]) * dth[j];
+                    const uint4 *xr = reinterpret_cast<const uint4 *>(x + ((tok0 + j) * H + h) * P + pc);
+#pragma unroll 1
+                    for (int q = 0; q < kW / 8; ++q) {
+                        const uint4 xv = __ldg(xr + q);
+                        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 t = __bfloat1622float2(x2[e]);
+                            float *a0 = acp + (8 * q + 2 * e) * kRows + m;
+                            a0[0] = fmaf(w, t.x, a0[0]);
+                            a0[kRows] = fmaf(w, t.y, a0[kRows]);
+                        }
+                    }
+                }
+            }
+            if (row) {  // + D x_m, rounded to bf16 and stored
+                const size_t base = ((tok0 + m) * H + h) * P + pc;
+                const uint4 *xm = reinterpret_cast<const uint4 *>(x + base);
+                uint4 *ym = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) + base);
+#pragma unroll 1
+                for (int q = 0; q < kW / 8; ++q) {
+                    const uint4 xv = __ldg(xm + q);
+                    const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                    float o[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 t = __bfloat1622float2(x2[e]);
+                        o[2 * e] = fmaf(Dh, t.x, acp[(8 * q + 2 * e) * kRows + m]);
+                        o[2 * e + 1] = fmaf(Dh, t.y, acp[(8 * q + 2 * e + 1) * kRows + m]);
+                    }
+                    ym[q] = pack8(o);
+                }
+            }
         }
     }
 }
@@ -707,12 +755,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (!ok && tid == 0) atomicOr(pr.err_word, kDevErrTimeout);
     tc_fence_before();
-    __syncthreads();
+    // decay range too wide for the factored form: direct outputs from G in TMEM,
+    // two threads per token (the warp halves), sums over the dead x tile
+    if (__syncthreads_and(ok && !fast)) {
+        tc_fence_after();
+        direct_unit_tmem<NS, 2>(pr, (size_t)tb * L + tt, len, hb * HB, tmem + lane_base + col_y,
+                                reinterpret_cast<const float *>(hh_s), reinterpret_cast<float *>(xs), cs, dtv, m,
+                                half);
+        tc_fence_before();
+        __syncthreads();
+    }
     if (warp == 0) tmem_dealloc(tmem, 256);
-    if (ok && !fast)  // decay range too wide for the factored form: direct outputs (C_i . B_j over x)
-        direct_unit_outputs(pr, NS, (size_t)tb * L + tt, len, hb, reinterpret_cast<const float *>(hh_s),
-                            reinterpret_cast<float *>(xs),
-                            cs, dtv, tid, kThreads, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -802,96 +855,6 @@ __device__ __forceinline__ PipeUnit decode_unit(const Problem &pr, int ticket, i
     u.h0 = u.hb * HB;
     u.g = u.h0 / (pr.nheads / pr.ngroups);
     return u;
-}
-
-// Direct fp32 evaluation of a wide unit's outputs in the persistent kernel.
-// Thread m of the team is token m of the chunk.  G = C B^T (fp32 sums of the
-// bf16 products) is still in the unit's TMEM accumulator, row m at g_taddr:
-// such a unit skips the diagonal and off-diagonal products.  Per head and
-// 64-column block, y_m = exp(cs_m) C_m . h_c + sum_{j<=m} G_mj exp(cs_m - cs_j)
-// dt_j x_j + D x_m, each weight formed once per (m, j, head, block).  The sums live in
-// `accs` ([64 columns][128 tokens] fp32, 32 KiB of shared memory, so a warp's
-// accesses fall in distinct banks), which keeps this rarely taken path light
-// on registers.  `hcs` is h_c, [128 rows (head, headdim)][64] fp32 in shared
-// memory; cs and dtv are the unit's per-token cs and input scale, [2][128].
-__device__ void direct_unit_tmem(const Problem &pr, size_t tok0, int len, int h0, uint32_t g_taddr,
-                                 const float *hcs, float *accs, const float *cs, const float *dtv, int m)
-{
-    constexpr int NS = 64;
-    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, G = pr.ngroups, g = h0 / (H / G);
-    const bool row = m < len;
-    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(pr.x);
-    const uint4 *crow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(pr.C) +
-                                                        ((tok0 + (row ? m : 0)) * G + g) * NS);
-    for (int hh = 0; hh < HB; ++hh) {
-        const int h = h0 + hh;
-        const float *csh = cs + hh * kRows, *dth = dtv + hh * kRows;
-        const float csm = csh[m], ecs = expf(csm);
-        const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
-        for (int pc = 0; pc < P; pc += 64) {
-            // exp(cs_m) C_m . h_c
-            for (int p = 0; p < 64; ++p) {
-                const float *hr = hcs + (size_t)(hh * P + pc + p) * NS;
-                float off = 0.f;
-                if (row) {
-#pragma unroll
-                    for (int q = 0; q < NS / 8; ++q) {
-                        const uint4 cv = __ldg(crow + q);
-                        const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&cv);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 t = __bfloat1622float2(c2[e]);
-                            off = fmaf(t.x, hr[8 * q + 2 * e], off);
-                            off = fmaf(t.y, hr[8 * q + 2 * e + 1], off);
-                        }
-                    }
-                }
-                accs[p * kRows + m] = ecs * off;
-            }
-            // + sum_{j <= m} G_mj exp(cs_m - cs_j) dt_j x_j
-            for (int jb = 0; jb < 8; ++jb) {
-                float gv[16];
-                tmem_ld16(g_taddr + jb * 16, gv);  // warp-collective: every lane, every row
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int j = jb * 16 + k;
-                    if (!row || j > m) continue;
-                    const float w = gv[k] * expf(csm - csh[j]) * dth[j];
-                    const uint4 *xr = reinterpret_cast<const uint4 *>(x + ((tok0 + j) * H + h) * P + pc);
-#pragma unroll 1
-                    for (int q = 0; q < 8; ++q) {
-                        const uint4 xv = __ldg(xr + q);
-                        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 t = __bfloat1622float2(x2[e]);
-                            float *a0 = accs + (8 * q + 2 * e) * kRows + m;
-                            a0[0] = fmaf(w, t.x, a0[0]);
-                            a0[kRows] = fmaf(w, t.y, a0[kRows]);
-                        }
-                    }
-                }
-            }
-            if (row) {  // + D x_m, rounded to bf16 and stored
-                const size_t base = ((tok0 + m) * H + h) * P + pc;
-                const uint4 *xm = reinterpret_cast<const uint4 *>(x + base);
-                uint4 *ym = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) + base);
-#pragma unroll 1
-                for (int q = 0; q < 8; ++q) {
-                    const uint4 xv = __ldg(xm + q);
-                    const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-                    float o[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 t = __bfloat1622float2(x2[e]);
-                        o[2 * e] = fmaf(Dh, t.x, accs[(8 * q + 2 * e) * kRows + m]);
-                        o[2 * e + 1] = fmaf(Dh, t.y, accs[(8 * q + 2 * e + 1) * kRows + m]);
-                    }
-                    ym[q] = pack8(o);
-                }
-            }
-        }
-    }
 }
 
 template <bool kPacked>
@@ -1481,9 +1444,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             }
             if (all_ok && !fast) {
                 tc_fence_after();
-                direct_unit_tmem(pr, (size_t)u.tb * pr.seqlen + u.tt, u.len, u.h0, slot + col_y,
-                                 reinterpret_cast<const float *>(st), reinterpret_cast<float *>(st + 2 * kSlab),
-                                 cs[ss], dtv[ss], m);
+                direct_unit_tmem<NS, 1>(pr, (size_t)u.tb * pr.seqlen + u.tt, u.len, u.h0, slot + col_y,
+                                        reinterpret_cast<const float *>(st), reinterpret_cast<float *>(st + 2 * kSlab),
+                                        cs[ss], dtv[ss], m, 0);
                 tc_fence_before();
                 named_sync(bar_team, 128);  // every thread is done with the stage and the TMEM slot
                 if (tt == 0) {
