@@ -48,8 +48,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=wl.HEADLINE.name, choices=[w.name for w in wl.WORKLOADS])
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the sub-record of the other large workloads (headline run only)")
     ap.add_argument("--ref-seconds", type=float, default=0.0,
                     help="oracle seconds per step of --impl reference (0: spread ~150 s over the steps)")
     return ap.parse_args()
@@ -329,30 +331,52 @@ def varlen_step_measurement(sets, w, stream, peaks, steps=100, nseq=12, seed=5):
             "kernels": ["ssd_fused_pipe_tc"]}
 
 
-def time_oracle(w, inp, seconds, cores):
-    """Run the oracle over growing row batches until `seconds` elapse or every
-    row is done; returns (tokens/s equivalent, rows done, elapsed)."""
+def plan_oracle_rows(w, inp, cores, seconds_per_call):
+    """The (batch, head, headdim) rows one timed oracle call covers: every row
+    when they fit in ``seconds_per_call`` on ``cores`` threads, else a seeded
+    subset sized from a short calibration call (a multiple of ``cores``)."""
     import oracle
-    total_rows = w.batch * w.nheads * w.headdim
-    order = torch.randperm(total_rows, generator=torch.Generator().manual_seed(3)).tolist()
-    done, t0, step = 0, time.perf_counter(), max(cores, 8)
-    while done < total_rows and time.perf_counter() - t0 < seconds:
-        rows = order[done:done + step]
-        oracle.recurrence(**inp, rows=rows, nthreads=cores)
-        done += len(rows)
-        step = min(step * 2, 4096)
-    elapsed = time.perf_counter() - t0
-    tokens_equiv = w.batch * w.seqlen * done / total_rows
-    return tokens_equiv / elapsed, done, elapsed
+    total = w.batch * w.nheads * w.headdim
+    order = torch.randperm(total, generator=torch.Generator().manual_seed(3)).tolist()
+    probe = order[:min(total, 2 * cores)]
+    t0 = time.perf_counter()
+    oracle.recurrence(**inp, rows=probe, nthreads=cores)
+    per_row = (time.perf_counter() - t0) / len(probe) * cores  # thread-seconds per row
+    fit = int(seconds_per_call * cores / max(per_row, 1e-9))
+    n = total if fit >= total else max(cores, fit // cores * cores)
+    return sorted(order[:n])
+
+
+def oracle_rate(w, inp, rows, cores):
+    """One timed oracle call over ``rows``: tokens/s, scaled by the row fraction."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.recurrence(**inp, rows=rows, nthreads=cores)
+    el = time.perf_counter() - t0
+    return w.batch * w.seqlen * len(rows) / (w.batch * w.nheads * w.headdim) / el, el
+
+
+def oracle_sample_text(w, rows, calls, per_call_s):
+    total = w.batch * w.nheads * w.headdim
+    what = "every" if len(rows) == total else f"a seeded subset of {len(rows)} of the {total}"
+    return (f"the sequential fp64 recurrence over {what} (batch, head, headdim) rows for the full sequence, "
+            f"one threaded call per sample, median of {calls} calls (~{per_call_s:.2f} s each); "
+            f"tokens/s scaled by the row fraction")
 
 
 def cpu_baseline(w, inp, seconds):
+    """The oracle timed on the host cores: the same rows and method as the
+    reference arm, repeated for ``seconds``; the median call."""
     cores = len(os.sched_getaffinity(0))
-    value, rows, elapsed = time_oracle(w, inp, seconds, cores)
-    total_rows = w.batch * w.nheads * w.headdim
+    rows = plan_oracle_rows(w, inp, cores, min(seconds, 3.0))
+    vals, secs = [], 0.0
+    while secs < seconds or len(vals) < 3:
+        v, el = oracle_rate(w, inp, rows, cores)
+        vals.append(v)
+        secs += el
+    value = statistics.median(vals)
     return {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"sequential fp64 recurrence over {rows} of {total_rows} (batch, head, headdim) rows "
-                      f"for the full sequence ({elapsed:.1f} s); tokens/s scaled by the row fraction"}
+            "sample": oracle_sample_text(w, rows, len(vals), secs / len(vals))}
 
 
 def run_reference(args, w, rank, world):
@@ -360,32 +384,164 @@ def run_reference(args, w, rank, world):
         return
     inp = wl.workload_inputs(w)
     cores = len(os.sched_getaffinity(0))
-    per_step = args.ref_seconds or max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     steps = args.steps or 5
+    per_step = args.ref_seconds or max(0.5, min(3.0, 150.0 / max(1, steps + args.warmup)))
+    rows = plan_oracle_rows(w, inp, cores, per_step)
     for _ in range(args.warmup):
-        time_oracle(w, inp, per_step / 4, cores)
-    vals, rows_total, secs = [], 0, 0.0
+        oracle_rate(w, inp, rows, cores)
+    vals, secs = [], 0.0
     for _ in range(steps):
-        v, rows, el = time_oracle(w, inp, per_step, cores)
+        v, el = oracle_rate(w, inp, rows, cores)
         vals.append(v)
-        rows_total += rows
         secs += el
-    value = statistics.mean(vals)
+    value = statistics.median(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
-                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk},
+        "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"each step: the fp64 recurrence over as many (batch, head, headdim) rows "
-                                   f"as fit in {per_step:.1f} s ({rows_total} rows over {steps} steps)"},
+                         "sample": oracle_sample_text(w, rows, steps, secs / steps)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+def workload_config(w):
+    """The workload as both arms name it."""
+    return {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads, "headdim": w.headdim,
+            "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk}
+
+
 # -- the GPU arm ------------------------------------------------------------------------
+
+def device_sets(w, inp, dev):
+    """Device copies of one input set, enough that the steps rotating over them
+    read more than three times the L2 between two uses of one copy."""
+    per_set = unavoidable_bytes(w)
+    nsets = max(2, math.ceil(3 * L2_BYTES / per_set))
+    sets = []
+    for _ in range(nsets):
+        d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+        d["y"] = torch.empty_like(d["x"])
+        d["final"] = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, dtype=torch.float32, device=dev)
+        sets.append(d)
+    return sets, per_set
+
+
+def make_step(w, sets, ws):
+    import structured_state_space_03_b300 as ssd
+
+    def step(k, stream):
+        d = sets[k % len(sets)]
+        ssd.ssd_fwd_ws(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], chunk=w.chunk,
+                       workspace=ws, y=d["y"], final_state=d["final"], stream=stream)
+    return step
+
+
+def capture(step, first, count):
+    """A CUDA graph of ``count`` consecutive steps (rotation index from ``first``)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        for k in range(first, first + count):
+            step(k, cs)
+    return g
+
+
+def graph_plan(steps, max_nodes=200):
+    """Graphs replayed in the timed region: (steps per graph, replays) pairs
+    covering exactly ``steps`` steps."""
+    per = min(steps, max_nodes)
+    plan = [(per, steps // per)]
+    if steps % per:
+        plan.append((steps % per, 1))
+    return plan
+
+
+def per_kernel_times(step, nk, stream, count):
+    """Device time of each kernel of a step, from events the library records
+    right around each launch: ``count`` profiled steps captured in a CUDA graph
+    and replayed (untimed otherwise), so host-side launch work does not sit
+    between an event and its kernel.  Returns (ms per launch per kernel, how)."""
+    import structured_state_space_03_b300 as ssd
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in range(count)]
+    for row in evs:  # create the underlying CUDA events
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    how = "event pairs around each launch, in a CUDA graph of the profiled steps"
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream()
+            for k in range(count):
+                ssd.ssd_profile_events(evs[k])
+                step(k, cs)
+                ssd.ssd_profile_events(None)
+        g.replay()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        out = [0.0] * nk
+        for row in evs:
+            for i in range(nk):
+                out[i] += row[2 * i].elapsed_time(row[2 * i + 1])
+        del g
+    except RuntimeError:
+        ssd.ssd_profile_events(None)
+        torch.cuda.synchronize()
+        how = "event pairs around each launch, steps issued one by one"
+        for k in range(count):
+            ssd.ssd_profile_events(evs[k])
+            step(k, stream)
+            ssd.ssd_profile_events(None)
+        torch.cuda.synchronize()
+        out = [0.0] * nk
+        for row in evs:
+            for i in range(nk):
+                out[i] += row[2 * i].elapsed_time(row[2 * i + 1])
+    ssd.ssd_check_device_status(stream)
+    return [v / count for v in out], how
+
+
+def workload_record(w, dev, stream, peaks, steps=20):
+    """One workload measured the way the headline is: ms per step over a graph
+    of ``steps`` steps, the roofline of the step and each kernel's share."""
+    import structured_state_space_03_b300 as ssd
+    dtype = wl.torch_dtype(w.dtype)
+    dims = (w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk)
+    kernels = ssd.ssd_fwd_kernels(*dims, dtype)
+    inp = wl.workload_inputs(w)
+    sets, per_set = device_sets(w, inp, dev)
+    ws = torch.empty(ssd.ssd_fwd_workspace_size(*dims, dtype), dtype=torch.uint8, device=dev)
+    step = make_step(w, sets, ws)
+    for k in range(3):
+        step(k, stream)
+    torch.cuda.synchronize()
+    ssd.ssd_check_device_status(stream)
+    g = capture(step, 0, steps)
+    g.replay()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    g.replay()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    ssd.ssd_check_device_status(stream)
+    ms = s0.elapsed_time(s1) / steps
+    pk, _ = per_kernel_times(step, len(kernels), stream, 5)
+    t_hbm = unavoidable_bytes(w) / (peaks["hbm_gbs"] * 1e9)
+    t_tc = causal_flops(w) / (peaks["bf16_tflops"] * 1e12)
+    rec = {"ms_per_step": ms, "tokens_per_s": w.tokens / (ms * 1e-3), "path": ssd.ssd_fwd_path(*dims, dtype),
+           "unavoidable_bytes": unavoidable_bytes(w), "causal_flops": causal_flops(w),
+           "roofline_ms": max(t_hbm, t_tc) * 1e3, "bound": "hbm" if t_hbm >= t_tc else "tensor",
+           "frac": max(t_hbm, t_tc) * 1e3 / ms, "steps": steps,
+           "kernels": {kernels[i]: pk[i] for i in range(len(kernels))}}
+    del sets, ws, g
+    torch.cuda.empty_cache()
+    return rec
+
 
 def main():
     args = parse_args()
@@ -409,26 +565,18 @@ def main():
     dims = (w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk)
     kernels = ssd.ssd_fwd_kernels(*dims, dtype)
     path = ssd.ssd_fwd_path(*dims, dtype)
+    nk = len(kernels)
 
     inp = wl.workload_inputs(w)
-    per_set = unavoidable_bytes(w)
-    nsets = max(1, math.ceil(3 * L2_BYTES / per_set))
-    sets = []
-    for _ in range(nsets):
-        d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
-        d["y"] = torch.empty_like(d["x"])
-        d["final"] = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, dtype=torch.float32, device=dev)
-        sets.append(d)
+    sets, per_set = device_sets(w, inp, dev)
+    nsets = len(sets)
     ws = torch.empty(ssd.ssd_fwd_workspace_size(*dims, dtype), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    step = make_step(w, sets, ws)
 
-    def step(k):
-        d = sets[k % nsets]
-        ssd.ssd_fwd_ws(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], chunk=w.chunk,
-                       workspace=ws, y=d["y"], final_state=d["final"], stream=stream)
-
-    for k in range(max(3, args.warmup)):
-        step(k)
+    warmup = max(3, args.warmup)
+    for k in range(warmup):
+        step(k, stream)
     torch.cuda.synchronize()
     ssd.ssd_check_device_status(stream)
 
@@ -436,20 +584,23 @@ def main():
     if steps <= 0:  # enough steps for a ~3 s timed region
         t0 = time.perf_counter()
         for k in range(20):
-            step(k)
+            step(k, stream)
         torch.cuda.synchronize()
         per = (time.perf_counter() - t0) / 20
         steps = int(min(200000, max(50, 3.0 / max(per, 1e-6))))
 
-    # per-kernel timing on a subset of the timed steps (events bracket each kernel)
-    nk = len(kernels)
-    n_prof = min(steps, 2000)
-    prof_every = max(1, steps // n_prof)
-    prof_events = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(n_prof)]
-    for evs in prof_events:  # create the underlying CUDA events
-        for e in evs:
-            e.record(stream)
+    # The timed region replays CUDA graphs of the steps, so host-side launch
+    # work (Python, argument checks) does not leave the GPU idle between steps.
+    plan = graph_plan(steps)
+    graphs = []
+    first = 0
+    for per, reps in plan:
+        graphs.append((capture(step, first, per), reps))
+        first += per
+    for g, _ in graphs:  # upload and warm each graph once
+        g.replay()
     torch.cuda.synchronize()
+    ssd.ssd_check_device_status(stream)
 
     sampler = ClockSampler(local)
     time.sleep(0.3)
@@ -460,15 +611,9 @@ def main():
     mark0 = sampler.mark()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    pi = 0
-    for k in range(steps):
-        profiled = k % prof_every == 0 and pi < n_prof
-        if profiled:
-            ssd.ssd_profile_events(prof_events[pi])
-        step(k)
-        if profiled:
-            ssd.ssd_profile_events(None)
-            pi += 1
+    for g, reps in graphs:
+        for _ in range(reps):
+            g.replay()
     end.record(stream)
     torch.cuda.synchronize()
     mark1 = sampler.mark()
@@ -480,11 +625,21 @@ def main():
     ssd.ssd_check_device_status(stream)
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
-    per_kernel = [0.0] * nk
-    for evs in prof_events[:pi]:
-        for i in range(nk):
-            per_kernel[i] += evs[i].elapsed_time(evs[i + 1])
-    per_kernel = [v / max(pi, 1) for v in per_kernel]  # ms per launch
+    # the same steps issued one call at a time from Python, the stream kept
+    # busy by `warmup` queued steps (for reference; not the headline)
+    for k in range(warmup):
+        step(k, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(steps):
+        step(k, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ssd.ssd_check_device_status(stream)
+    eager_ms = e0.elapsed_time(e1) / steps
+
+    # each kernel's own device time, in a separate untimed pass
+    per_kernel, kernel_timing = per_kernel_times(step, nk, stream, max(5, min(steps, 100)))
     tot_k = sum(per_kernel) or 1.0
     dom = max(range(nk), key=lambda i: per_kernel[i])
     dom_name = kernels[dom]
@@ -524,31 +679,40 @@ def main():
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
-        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
-                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk,
-                   "path": path, "l2": f"inputs rotate over {nsets} device copies "
-                                       f"({nsets * per_set / 2**20:.0f} MiB > 126 MB L2)"},
+        "config": workload_config(w),
+        "run": {"path": path, "kernels": kernels,
+                "timing": f"CUDA events around graph replays of the {steps} steps ({len(graphs)} graph(s))",
+                "l2": f"inputs rotate over {nsets} device copies ({nsets * per_set / 2**20:.0f} MiB > 126 MB L2)"},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": dom_gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": dom_gbs / peaks["hbm_gbs"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": dom_bytes, "launch_ms": per_kernel[dom],
+                     "launch_timing": kernel_timing,
                      "peak_source": f"{peak_src} (copy bandwidth)"},
         "step_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor", "unavoidable_bytes": unavoidable_bytes(w),
                           "causal_flops": causal_flops(w), "roofline_ms": t_roof * 1e3,
                           "frac": t_roof * 1e3 / ms_per_step, "peak_source": peak_src},
         "kernels": {kernels[i]: {"ms_per_launch": per_kernel[i], "share": per_kernel[i] / tot_k}
                     for i in range(nk)},
+        "eager": {"ms_per_step": eager_ms, "tokens_per_s": tokens * world / (eager_ms * 1e-3),
+                  "how": "ssd_fwd_ws called once per step from Python, stream pre-filled"},
         "e2e": {"value": tokens * e2e_steps * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "entry": "ssd_fwd_host"},
         "gpu_launches": nk * steps,
         "clocks": sampler.summary(mark0, mark1),
     }
+    del graphs
     if rank == 0 and world == 1:
         line["decode_step"] = decode_step_measurement(dev, peaks, stream)
         if w is wl.HEADLINE:
             line["pre_step"] = pre_step_measurement(sets, w, stream)
             line["varlen_step"] = varlen_step_measurement(sets, w, stream, peaks)
+            if not args.no_workloads:
+                del sets
+                torch.cuda.empty_cache()
+                line["workloads"] = {o.name: workload_record(o, dev, stream, peaks)
+                                     for o in wl.WORKLOADS[2:]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
     if rank == 0:

@@ -288,12 +288,35 @@ SSD_API int ssd_fwd_kernels(int batch, int seqlen, int nheads, int headdim, int 
  * ssd_profile_events -- per-kernel timing hook for benchmarks.  After a call
  * with non-NULL `events` (cudaEvent_t handles passed as void*, owned by the
  * caller, created on the device the forwards run on), every forward issued from
- * this thread records events[0] on its stream before its first kernel and
- * events[k] right after its k-th kernel, for k < count.  NULL or count <= 0
- * switches the hook off.  The setting is thread-local; the library never
- * creates, destroys or waits on these events.
+ * this thread records, for its k-th kernel (k = 0, 1, ...), events[2k] on its
+ * stream right before the launch -- after the library's host-side set-up for
+ * that kernel and any memset it needs -- and events[2k+1] right after it,
+ * while 2k+1 < count.  The time between the two is the kernel's own device
+ * time.  NULL or count <= 0 switches the hook off; count is at most 16.  The
+ * setting is thread-local; the library never creates, destroys or waits on
+ * these events.
  */
 SSD_API ssd_status_t ssd_profile_events(void *const *events, int count);
+
+/*
+ * ssd_test_set_fault -- failure-detection test hook; not for production use.
+ * The fused kernels resolve the chunk-to-chunk recurrence by waiting, inside
+ * the kernel, for other units' published chunk states ("Mamba 模型" §4.1: the
+ * off-diagonal blocks pass through the hidden state).  Every such wait, and
+ * every wait on the kernels' own barriers, is bounded; a wait that runs out
+ * sets the device error word, the kernel gives up instead of hanging, and
+ * ssd_check_device_status() returns SSD_ERR_TIMEOUT.  This hook makes that
+ * path testable without any fault: for forwards issued later from the calling
+ * thread, every bounded wait of the fused kernels gives up after
+ * `wait_limit_ns` nanoseconds (0 restores the default, 2 s), and the unit
+ * `withhold_unit` (its index among the fused kernels' units, -1 for none;
+ * unit 0 is chunk 0 of the first head block of batch element 0) never
+ * publishes its chunk state, so the units after it in its sequence wait for a
+ * flag that nothing sets.  The outputs of such a forward are undefined; the
+ * kernel still ends and the context stays usable.  Thread-local setting;
+ * SSD_ERR_INVALID_ARG for withhold_unit < -1.
+ */
+SSD_API ssd_status_t ssd_test_set_fault(unsigned long long wait_limit_ns, long long withhold_unit);
 
 /*
  * ssd_check_device_status -- synchronise `stream`, then read and clear the

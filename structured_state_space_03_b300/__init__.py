@@ -5,7 +5,7 @@ step of the computation runs in the library's CUDA kernels.  PyTorch is used
 for device memory and streams only.  The functions carry the C names:
 
     ssd_fwd, ssd_fwd_ws, ssd_fwd_host, ssd_fwd_pre, ssd_fwd_varlen, ssd_fwd_noalloc, ssd_fwd_workspace_size,
-    ssd_fwd_path, ssd_step,
+    ssd_fwd_path, ssd_step, ssd_fwd_kernels, ssd_profile_events, ssd_test_set_fault,
     ssd_check_device_status, ssd_status_string, ssd_last_error_detail, ssd_version
 
 Layouts: x, y [batch, seqlen, nheads, headdim]; dt [batch, seqlen, nheads];
@@ -52,6 +52,7 @@ SIGNATURES = {
     "ssd_fwd_kernels": (_I, _DIMS + [ctypes.c_char_p, _S]),
     "ssd_profile_events": (_I, [ctypes.POINTER(_P), _I]),
     "ssd_check_device_status": (_I, [_P]),
+    "ssd_test_set_fault": (_I, [ctypes.c_ulonglong, ctypes.c_longlong]),
     "ssd_status_string": (ctypes.c_char_p, [_I]),
     "ssd_last_error_detail": (ctypes.c_char_p, []),
     "ssd_version": (ctypes.c_char_p, []),
@@ -340,6 +341,13 @@ def ssd_profile_events(events):
         return
     arr = (_P * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(lib().ssd_profile_events(arr, len(events)))
+
+
+def ssd_test_set_fault(wait_limit_ns: int = 0, withhold_unit: int = -1):
+    """Failure-detection test hook (this thread's later forwards): bounded waits
+    of the fused kernels give up after ``wait_limit_ns`` (0: the 2 s default)
+    and unit ``withhold_unit`` (-1: none) never publishes its chunk state."""
+    _check(lib().ssd_test_set_fault(int(wait_limit_ns), int(withhold_unit)))
 
 
 def ssd_check_device_status(stream=None):

@@ -17,13 +17,9 @@
 namespace ssd {
 
 static thread_local char g_detail[512];
-static thread_local cudaEvent_t g_profile_events[16];
-static thread_local int g_profile_count;
-
-static void profile_mark(int k, cudaStream_t s)
-{
-    if (k < g_profile_count) cudaEventRecord(g_profile_events[k], s);
-}
+// Failure-detection test settings of this thread (ssd_test_set_fault).
+static thread_local unsigned long long t_wait_ns;
+static thread_local long long t_withhold = -1;
 
 static ssd_status_t fail(ssd_status_t st, const char *fmt, ...)
 {
@@ -145,25 +141,22 @@ static const char *kernel_names(const Problem &pr)
 static ssd_status_t run(const Problem &pr_in, void *workspace, cudaStream_t s)
 {
     Problem pr = pr_in;
+    pr.wait_ns = t_wait_ns ? t_wait_ns : 2000000000ull;
+    pr.withhold = t_withhold;
     pr.err_word = device_error_word();
     if (!pr.err_word) return fail(SSD_ERR_CUDA, "cannot resolve the device error word");
     const ssd_path_t path = choose_path(pr);
+    profile_forward_begin();
     if (path == SSD_PATH_TCGEN05_FUSED) {
-        profile_mark(0, s);
         cudaError_t e = launch_fused_tc(pr, workspace, s);
-        profile_mark(1, s);
         if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
         return ok();
     }
     const Workspace ws = carve_workspace(pr, workspace);
     const bool tc = path == SSD_PATH_TCGEN05;
-    profile_mark(0, s);
     cudaError_t e = tc ? launch_chunk_state_tc(pr, ws, s) : launch_chunk_state_simt(pr, ws, s);
-    profile_mark(1, s);
     if (e == cudaSuccess) e = launch_state_pass(pr, ws, s);
-    profile_mark(2, s);
     if (e == cudaSuccess) e = tc ? launch_chunk_out_tc(pr, ws, s) : launch_chunk_out_simt(pr, ws, s);
-    profile_mark(3, s);
     if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -232,15 +225,13 @@ int ssd_fwd_kernels(int batch, int seqlen, int nheads, int headdim, int ngroups,
 ssd_status_t ssd_profile_events(void *const *events, int count)
 {
     if (!events || count <= 0) {
-        g_profile_count = 0;
+        profile_set(nullptr, 0);
         return ok();
     }
-    if (count > 16) return fail(SSD_ERR_INVALID_ARG, "at most 16 profiling events");
-    for (int i = 0; i < count; ++i) {
+    if (count > kMaxProfileEvents) return fail(SSD_ERR_INVALID_ARG, "at most %d profiling events", kMaxProfileEvents);
+    for (int i = 0; i < count; ++i)
         if (!events[i]) return fail(SSD_ERR_INVALID_ARG, "profiling event %d is NULL", i);
-        g_profile_events[i] = static_cast<cudaEvent_t>(events[i]);
-    }
-    g_profile_count = count;
+    profile_set(events, count);
     return ok();
 }
 
@@ -684,6 +675,14 @@ ssd_status_t ssd_step(const void *x, const float *dt, const float *A, const void
     const cudaError_t e = launch_step(x, dt, A, B, C, D, state, y, batch, nheads, headdim, ngroups, dstate, dtype,
                                       static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "ssd_step launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+ssd_status_t ssd_test_set_fault(unsigned long long wait_limit_ns, long long withhold_unit)
+{
+    if (withhold_unit < -1) return fail(SSD_ERR_INVALID_ARG, "withhold_unit must be -1 or a unit index");
+    t_wait_ns = wait_limit_ns;
+    t_withhold = withhold_unit;
     return ok();
 }
 

@@ -61,8 +61,6 @@
 
 namespace ssd {
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();  // ssd_tc.cu
-
 namespace {
 
 using namespace ptx;
@@ -277,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ int s_fail, s_mode, s_stop;
 
     constexpr int NSL = NS / 64;        // 64-wide slabs of the state dimension
+    const uint64_t lim = pr.wait_ns;    // limit of every bounded wait
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;       // TMEM lane quarter this warp may access
     const int half = warp >> 2;         // which head / half of the columns this warp handles
@@ -342,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *cm = bs + NSL * kSlab;                  // C, then tril(G) (2 slabs), later y staging
     uint8_t *rr = cm + 2 * kSlab;                    // wx ring: 3 x (hi 4 KiB | lo 4 KiB)
     uint8_t *hh_s = NS == 64 ? cm : rr + 3 * 8192;   // h hi | lo (NSL slabs each)
+    uint8_t *gl = hh_s + 2 * NSL * kSlab;            // tril(G) lo (2 slabs)
 
     if (tid == 0) {
         tma_prefetch_desc(&xmap);
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
 
-    bool ok = mbar_wait(&bar_ld, 0);
+    bool ok = mbar_wait(&bar_ld, 0, lim);
     if (!ok) s_fail = 1;
     __syncthreads();
     ok = !s_fail;
@@ -424,20 +424,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         mma_commit(&bar_g);
     }
-    if (ok && !mbar_wait(&bar_g, 0)) s_fail = 1;
+    if (ok && !mbar_wait(&bar_g, 0, lim)) s_fail = 1;
     __syncthreads();
     ok = !s_fail;
     tc_fence_after();
     const int m = quarter * 32 + lane;   // TMEM row of this thread: token i, or (head, headdim)
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     if (ok && fast) {
+        // tril(G) as two bf16 terms (hi = bf16(G), lo = bf16(G - hi)): at dstate 128 a
+        // single rounding of G alone costs up to ~2% of RMS(y) where dt is large
         for (int jb = 2 * half; jb < 2 * half + 2; ++jb) {
-            uint8_t *dst = cm + (jb >> 1) * kSlab;
+            uint8_t *dst = cm + (jb >> 1) * kSlab, *dstl = gl + (jb >> 1) * kSlab;
             const int q0 = (jb & 1) * 4;
             if (jb > quarter) {  // every row of this warp is above the diagonal
                 const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4 *>(dst + sw128(m, q0 + u)) = z;
+                for (int u = 0; u < 4; ++u) {
+                    *reinterpret_cast<uint4 *>(dst + sw128(m, q0 + u)) = z;
+                    *reinterpret_cast<uint4 *>(dstl + sw128(m, q0 + u)) = z;
+                }
                 continue;
             }
             float gv[32];
@@ -448,7 +453,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (jb * 32 + k > m) gv[k] = 0.f;
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4 *>(dst + sw128(m, q0 + u)) = pack8(gv + 8 * u);
+            for (int u = 0; u < 4; ++u) {
+                uint4 hi, lo;
+                split8(gv + 8 * u, hi, lo);
+                *reinterpret_cast<uint4 *>(dst + sw128(m, q0 + u)) = hi;
+                *reinterpret_cast<uint4 *>(dstl + sw128(m, q0 + u)) = lo;
+            }
         }
     }
     fence_async_smem();
@@ -465,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float *vh = vw + (P == 64 ? mb : 0) * kRows;
         auto issue = [&](int k) {
             const int bb = k % 3;
-            if (!mbar_wait(&bar_full[bb], (k / 3) & 1)) return false;
+            if (!mbar_wait(&bar_full[bb], (k / 3) & 1, lim)) return false;
             tc_fence_after();
             const uint32_t buf = smem_u32(rr) + bb * 8192;
             constexpr uint32_t id_s = idesc_bf16(128, NS, 1, 1);
@@ -474,9 +484,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             mma_bf16(tmem + col_st, sdesc_sw128(buf + 4096, 2048, 1024), bd, id_s, 1);
             if (fast) {
                 constexpr uint32_t id_d = idesc_bf16(128, 128, 0, 1);
-                const uint64_t ad = sdesc_sw128(smem_u32(cm) + (k >> 2) * kSlab + (k & 3) * 32, 16, 1024);
+                const uint32_t goff = (k >> 2) * kSlab + (k & 3) * 32;
+                const uint64_t ad = sdesc_sw128(smem_u32(cm) + goff, 16, 1024);
+                const uint64_t adl = sdesc_sw128(smem_u32(gl) + goff, 16, 1024);
                 mma_bf16(tmem + col_y, ad, sdesc_sw128(buf, 2048, 1024), id_d, k > 0);
                 mma_bf16(tmem + col_y, ad, sdesc_sw128(buf + 4096, 2048, 1024), id_d, 1);
+                mma_bf16(tmem + col_y, adl, sdesc_sw128(buf, 2048, 1024), id_d, 1);
             }
             mma_commit(&bar_empty[bb]);
             return true;
@@ -484,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         bool good = true;
         for (int k = 0; k < 8 && good; ++k) {
             const int bb = k % 3;
-            if (k >= 3 && !mbar_wait(&bar_empty[bb], ((k - 3) / 3) & 1)) good = false;
+            if (k >= 3 && !mbar_wait(&bar_empty[bb], ((k - 3) / 3) & 1, lim)) good = false;
             if (!good) break;
             uint8_t *buf = rr + bb * 8192;
             const int j = 16 * k + row;
@@ -510,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (good && tid == 0) good = issue(7);
         // the last commit (step 7, buffer 1, its third phase) covers every earlier MMA
-        if (good && !mbar_wait(&bar_empty[1], 0)) good = false;
+        if (good && !mbar_wait(&bar_empty[1], 0, lim)) good = false;
         if (!good) s_fail = 1;
     }
     __syncthreads();
@@ -549,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                                                              sfac * v[4 * u + 2], sfac * v[4 * u + 3]));
         }
         if (tid < HB) fa.alpha[unit * 2 + tid] = s_alpha[tid];
-        red_release_add(fa.aggcnt + unit, 1u);
+        if ((long long)unit != pr.withhold) red_release_add(fa.aggcnt + unit, 1u);
         if (warp == 0) {
             // Walk back, 32 predecessors per poll: stop at the nearest chunk whose
             // inclusive state is published (or before chunk 0: the init state);
@@ -576,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     top -= 32;  // 32 aggregates, keep walking
                     continue;
                 }
-                if (globaltimer() - tstart > kWaitLimitNs) {
+                if (globaltimer() - tstart > lim) {
                     timed_out = true;
                     break;
                 }
@@ -679,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (ok && tid == 0) {
         if (fast) {
             // Y += C (e^ref h_c)^T
-            if (!mbar_wait(&bar_c, 0)) {
+            if (!mbar_wait(&bar_c, 0, lim)) {
                 s_fail = 1;
             } else {
                 tc_fence_after();
@@ -696,10 +709,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     // publish h_{c+1} (written above) now that the off-diagonal MMA is running:
     // the release waits for this thread's stores, off the critical path
-    if (ok) red_release_add(fa.inclcnt + unit, 1u);
+    if (ok && (long long)unit != pr.withhold) red_release_add(fa.inclcnt + unit, 1u);
     __syncthreads();
     ok = ok && !s_fail;
-    if (ok && fast && !mbar_wait(&bar_g, 1)) s_fail = 1;
+    if (ok && fast && !mbar_wait(&bar_g, 1, lim)) s_fail = 1;
     __syncthreads();
     ok = ok && !s_fail;
     tc_fence_after();
@@ -871,6 +884,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                       const __grid_constant__ CUtensorMap dtmap, Problem pr, FusedArgs fa, int units, int dt_tma)
 {
     constexpr int NS = 64;
+    const uint64_t lim = pr.wait_ns;  // limit of every bounded wait
     extern __shared__ uint8_t smem_raw[];
     // per stage (it & 1): full, free, slot, g, fr, mma, yo; per unit in flight (it & 3): info,
     // seg and the unit's scalars, which the epilogue may still read after the stage is free
@@ -935,7 +949,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             for (int it = 0;; ++it) {
                 const int s = it & 1, ss = it & 3;
                 const uint32_t ph = (it >> 1) & 1;
-                bool ok = it < 2 || mbar_wait(&bar_free[s], ph ^ 1);
+                bool ok = it < 2 || mbar_wait(&bar_free[s], ph ^ 1, lim);
                 const uint32_t t = ok ? atomicAdd(fa.counters + kCtrTicket, 1u) : 0xffffffffu;
                 const int tk = t < (uint32_t)units ? (int)t : -1;
                 if (!ok) s_fail = 1;
@@ -969,18 +983,18 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             for (int it = 0;; ++it) {
                 const int s = it & 1, ss = it & 3;
                 const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
-                if (!mbar_wait(&bar_info[ss], pq)) {
+                if (!mbar_wait(&bar_info[ss], pq, lim)) {
                     s_fail = 1;
                     break;
                 }
                 if (s_tk[ss] < 0) break;
                 const uint32_t slot = tmem + s * 256;
                 const uint32_t st = smem_u32(base + s * kStageBytes);
-                if (it >= 2 && !mbar_wait(&bar_slot[s], ph ^ 1)) {
+                if (it >= 2 && !mbar_wait(&bar_slot[s], ph ^ 1, lim)) {
                     s_fail = 1;
                     break;
                 }
-                if (!mbar_wait(&bar_full[s], ph)) {
+                if (!mbar_wait(&bar_full[s], ph, lim)) {
                     s_fail = 1;
                     break;
                 }
@@ -991,14 +1005,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 mma_commit(&bar_g[s]);
                 // tril(G) in TMEM first, then each 16-token slice of wx as the front
                 // warps finish it, so the build and the MMAs overlap
-                if (!mbar_wait(&bar_mask[s], ph)) {
+                if (!mbar_wait(&bar_mask[s], ph, lim)) {
                     s_fail = 1;
                     break;
                 }
                 const bool fast = s_fast[ss] != 0;
                 bool okm = true;
                 for (int ks = 0; ks < kRows / 16; ++ks) {
-                    if (!mbar_wait(&bar_slice[s][ks], ph)) {
+                    if (!mbar_wait(&bar_slice[s][ks], ph, lim)) {
                         okm = false;
                         break;
                     }
@@ -1026,7 +1040,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         for (int it = 0;; ++it) {
             const int s = it & 1, ss = it & 3;
             const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
-            bool ok = mbar_wait(&bar_info[ss], pq);
+            bool ok = mbar_wait(&bar_info[ss], pq, lim);
             const int tk = s_tk[ss];
             if (named_sync_or(kBarFront, 128, !ok)) {
                 s_fail = 1;
@@ -1036,7 +1050,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             const PipeUnit u = decode_unit<kPacked>(pr, tk, nhb);
             uint8_t *st = base + s * kStageBytes;
             const float *dts = reinterpret_cast<const float *>(base + 2 * kStageBytes + s * kDtBytes) + ft * 4 + (u.h0 & 3);
-            if (dt_tma) ok = ok && mbar_wait(&bar_dt[s], ph);
+            if (dt_tma) ok = ok && mbar_wait(&bar_dt[s], ph, lim);
             float v[2], d[2], din[2];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -1097,8 +1111,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             if (ft == 0) s_fast[ss] = fast ? 1 : 0;
             mbar_arrive(&bar_seg[ss]);
             named_sync(kBarFront, 128);  // every v_j dt_j is in shared memory
-            ok = mbar_wait(&bar_full[s], ph) && (it < 2 || mbar_wait(&bar_lo[s], ph ^ 1));
-            ok = ok && mbar_wait(&bar_g[s], ph);
+            ok = mbar_wait(&bar_full[s], ph, lim) && (it < 2 || mbar_wait(&bar_lo[s], ph ^ 1, lim));
+            ok = ok && mbar_wait(&bar_g[s], ph, lim);
             tc_fence_after();
             if (ok && fast) {  // tril(G) -> bf16 pairs in TMEM (row m, columns jb*32 .. jb*32+31)
                 const uint32_t slot = tmem + s * 256 + lane_base;
@@ -1169,17 +1183,18 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             for (int it = team;; it += 2) {
                 const int ss = it & 3;
                 const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
-                if (!mbar_wait(&bar_info[ss], pq)) {
+                if (!mbar_wait(&bar_info[ss], pq, lim)) {
                     s_fail = 1;
                     break;
                 }
                 const int tk = s_tk[ss];
                 if (tk < 0) break;
-                if (!mbar_wait(&bar_pincl[s], ph)) {
+                if (!mbar_wait(&bar_pincl[s], ph, lim)) {
                     s_fail = 1;
                     break;
                 }
-                if (!s_fail) red_release_add(fa.inclcnt + decode_unit<kPacked>(pr, tk, nhb).unit, 1u);
+                const size_t pu = decode_unit<kPacked>(pr, tk, nhb).unit;
+                if (!s_fail && (long long)pu != pr.withhold) red_release_add(fa.inclcnt + pu, 1u);
                 mbar_arrive(&bar_pdone[s]);
             }
         }
@@ -1203,7 +1218,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         for (int it = team;; it += 2) {
             const int ss = it & 3;
             const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
-            bool ok = mbar_wait(&bar_info[ss], pq);
+            bool ok = mbar_wait(&bar_info[ss], pq, lim);
             const int tk = s_tk[ss];
             if (named_sync_or(bar_team, 128, !ok)) {
                 s_fail = 1;
@@ -1213,7 +1228,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             const PipeUnit u = decode_unit<kPacked>(pr, tk, nhb);
             const int c = u.c;
             const bool tma_out = tma_tiles && (!kPacked || u.len == kRows);
-            if (it >= 2 && !mbar_wait(&bar_pdone[s], ph ^ 1)) ok = false;
+            if (it >= 2 && !mbar_wait(&bar_pdone[s], ph ^ 1, lim)) ok = false;
             // walk back to the nearest inclusive state; -2: S_c became ready first
             // (publish it as the aggregate, then walk on); -3: gave up
             int stop = c - 1;
@@ -1245,7 +1260,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                                 res = -2;
                                 break;
                             }
-                            if (globaltimer() - tstart > kWaitLimitNs) break;
+                            if (globaltimer() - tstart > lim) break;
                             __nanosleep(128);
                         }
                         if (lane == 0) s_walk[team][round] = res;
@@ -1261,7 +1276,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                         break;
                     }
                     // publish S_c (scaled to the chunk end) as this unit's aggregate
-                    ok = mbar_wait(&bar_mma[s], ph) && mbar_wait(&bar_seg[ss], pq);
+                    ok = mbar_wait(&bar_mma[s], ph, lim) && mbar_wait(&bar_seg[ss], pq, lim);
                     tc_fence_after();
                     if (ok) {
                         const float sfac = s_sfac[ss][hh_m];
@@ -1279,7 +1294,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     }
                     // one release for the whole unit: the barrier orders every
                     // thread's stores before the leader's release store
-                    if (!named_sync_or(bar_team, 128, !ok) && tt == 32) st_release_flag(fa.aggcnt + u.unit);
+                    if (!named_sync_or(bar_team, 128, !ok) && tt == 32 && (long long)u.unit != pr.withhold)
+                        st_release_flag(fa.aggcnt + u.unit);
                 }
             }
             // h_c for row m, in the recurrence's own order
@@ -1317,7 +1333,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     }
                 }
             }
-            ok = ok && mbar_wait(&bar_mma[s], ph) && mbar_wait(&bar_seg[ss], pq);
+            ok = ok && mbar_wait(&bar_mma[s], ph, lim) && mbar_wait(&bar_seg[ss], pq, lim);
             tc_fence_after();
             const bool fast = s_fast[ss] != 0;
             if (tt == 0) {  // x of the unit for the D x term, into the staging region (wx lo is dead)
@@ -1395,7 +1411,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             // ---- epilogue: y = r Y + D x, x read from the staging region and y
             // written over it (the same swizzled position), then stored by TMA
             const bool row_in = m < u.len;
-            ok = !any_fail && mbar_wait(&bar_yo[s], ph) && mbar_wait(&bar_xe[s], ph);
+            ok = !any_fail && mbar_wait(&bar_yo[s], ph, lim) && mbar_wait(&bar_xe[s], ph, lim);
             tc_fence_after();
             uint8_t *ystage = st + 2 * kSlab;
             if (ok && fast) {
@@ -1467,41 +1483,24 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
+// [batch][seqlen][width] bf16, 64 x 128 boxes with the 128-byte swizzle
 cudaError_t make_map(CUtensorMap *map, const void *ptr, int width, int seqlen, int batch)
 {
-    auto fn = tensor_map_encoder();
-    if (!fn) return cudaErrorNotSupported;
-    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)seqlen, (cuuint64_t)batch};
-    const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * seqlen};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kRows, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return cached_tensor_map(map, ptr, true, width, seqlen, batch, 64, kRows, true);
 }
 
 // fp32 [batch][seqlen][width] with a 4 x 128 box (no swizzle), for dt.
 cudaError_t make_map_f32(CUtensorMap *map, const void *ptr, int width, int seqlen, int batch)
 {
-    auto fn = tensor_map_encoder();
-    if (!fn) return cudaErrorNotSupported;
-    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)seqlen, (cuuint64_t)batch};
-    const cuuint64_t strides[2] = {(cuuint64_t)width * 4, (cuuint64_t)width * 4 * seqlen};
-    const cuuint32_t box[3] = {4, (cuuint32_t)kRows, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return cached_tensor_map(map, ptr, false, width, seqlen, batch, 4, kRows, false);
 }
 
-// ssd_fused_tc: x | B (then C) | C (then tril(G), then y) | wx ring | h hi/lo
+// ssd_fused_tc: x | B (then C) | C (then tril(G) hi, then y) | wx ring | h hi/lo | tril(G) lo
 size_t fused_smem(int NS)
 {
     const size_t body = (size_t)(2 + NS / 64 + 2) * kSlab + 3 * 8192;  // ..., wx ring 24 KiB
     const size_t hreg = NS == 64 ? 0 : (size_t)2 * (NS / 64) * kSlab;
-    return 1024 + body + hreg;
+    return 1024 + body + hreg + 2 * kSlab;
 }
 
 size_t units_of(const Problem &pr)
@@ -1521,7 +1520,6 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
     if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
     if ((e = make_map(&ymap, pr.y, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
     const size_t units = units_of(pr);
-    if ((e = cudaMemsetAsync(fa.aggcnt, 0, (2 * units + kCtrCount) * sizeof(uint32_t), s)) != cudaSuccess) return e;
     if constexpr (NS == 64) {
         const size_t psmem = 1024 + (size_t)2 * kStageBytes + 2 * kDtBytes;
         // dt through TMA when its rows are 16-byte multiples and the base is aligned
@@ -1530,19 +1528,24 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
         int dt_tma = (pr.nheads % 4 == 0 && (reinterpret_cast<uintptr_t>(pr.dt) & 15) == 0) ? 1 : 0;
         if (dt_tma && make_map_f32(&dtmap, pr.dt, pr.nheads, pr.seqlen, mb) != cudaSuccess) dt_tma = 0;
         auto kern = pr.chunks ? ssd_fused_pipe_tc<true> : ssd_fused_pipe_tc<false>;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem)) != cudaSuccess)
-            return e;
-        int dev = 0, nsm = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = ensure_smem_limit(reinterpret_cast<const void *>(kern), psmem)) != cudaSuccess) return e;
+        int nsm = 0;
+        if ((e = sm_count(&nsm)) != cudaSuccess) return e;
         const unsigned grid = (unsigned)std::min<size_t>(units, (size_t)nsm);
+        if ((e = cudaMemsetAsync(fa.aggcnt, 0, (2 * units + kCtrCount) * sizeof(uint32_t), s)) != cudaSuccess)
+            return e;
+        profile_kernel_begin(s);
         kern<<<grid, kPipeThreads, psmem, s>>>(xmap, bmap, cmap, ymap, dtmap, pr, fa, (int)units, dt_tma);
+        profile_kernel_end(s);
     } else {
         const size_t smem = fused_smem(NS);
         auto kern = pr.chunks ? ssd_fused_tc<NS, true> : ssd_fused_tc<NS, false>;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        if ((e = ensure_smem_limit(reinterpret_cast<const void *>(kern), smem)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(fa.aggcnt, 0, (2 * units + kCtrCount) * sizeof(uint32_t), s)) != cudaSuccess)
             return e;
+        profile_kernel_begin(s);
         kern<<<(unsigned)units, kThreads, smem, s>>>(xmap, bmap, cmap, ymap, pr, fa);
+        profile_kernel_end(s);
     }
     return cudaGetLastError();
 }

@@ -1,0 +1,165 @@
+// ssd_host.cu -- host-side state the launchers share: cached TMA tensor maps,
+// per-device kernel attributes and SM counts, and the per-kernel timing hook.
+//
+// A forward on the headline sizes runs one kernel of ~tens of microseconds, so
+// per-call host work (encoding tensor maps, raising a kernel's shared-memory
+// limit, querying the SM count) is a visible share of a step when calls are
+// issued back to back.  Everything here is computed once and reused:
+//   * tensor maps: a small per-thread cache keyed by every encode parameter
+//     (base pointer, sizes, strides, box, swizzle), so an identical request
+//     returns the identical 128-byte map without calling the driver;
+//   * cudaFuncSetAttribute(MaxDynamicSharedMemorySize): once per (device,
+//     kernel, size) -- a process-wide table under a mutex;
+//   * the SM count: once per device.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "ssd_internal.cuh"
+
+namespace ssd {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();  // ssd_tc.cu
+
+namespace {
+
+struct MapKey {
+    const void *ptr;
+    int dtype;  // CUtensorMapDataType
+    uint64_t dims[3];
+    uint64_t strides[2];
+    uint32_t box[3];
+    int swizzle;
+    int promo;
+};
+
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    bool used;
+};
+
+constexpr int kMapCache = 32;
+thread_local MapEntry t_maps[kMapCache];
+thread_local int t_map_next;
+
+struct AttrEntry {
+    int dev;
+    const void *func;
+    int bytes;
+};
+
+std::mutex g_attr_mu;
+AttrEntry g_attr[256];
+int g_attr_n;
+
+std::mutex g_sm_mu;
+int g_sm_count[64];
+
+thread_local cudaEvent_t t_prof[kMaxProfileEvents];
+thread_local int t_prof_count;
+thread_local int t_prof_next;
+
+}  // namespace
+
+cudaError_t cached_tensor_map(CUtensorMap *out, const void *ptr, bool bf16, int width, int rows, int batch,
+                              int box_cols, int box_rows, bool swizzle128)
+{
+    MapKey k;
+    memset(&k, 0, sizeof k);
+    const uint64_t el = bf16 ? 2 : 4;
+    k.ptr = ptr;
+    k.dtype = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    k.dims[0] = (uint64_t)width;
+    k.dims[1] = (uint64_t)rows;
+    k.dims[2] = (uint64_t)batch;
+    k.strides[0] = (uint64_t)width * el;
+    k.strides[1] = (uint64_t)width * el * rows;
+    k.box[0] = (uint32_t)box_cols;
+    k.box[1] = (uint32_t)box_rows;
+    k.box[2] = 1;
+    k.swizzle = swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    k.promo = swizzle128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_NONE;
+    for (int i = 0; i < kMapCache; ++i) {
+        if (t_maps[i].used && memcmp(&t_maps[i].key, &k, sizeof k) == 0) {
+            *out = t_maps[i].map;
+            return cudaSuccess;
+        }
+    }
+    auto fn = tensor_map_encoder();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(out, (CUtensorMapDataType)k.dtype, 3, const_cast<void *>(ptr), k.dims, k.strides, k.box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, (CUtensorMapSwizzle)k.swizzle,
+                    (CUtensorMapL2promotion)k.promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    MapEntry &e = t_maps[t_map_next];
+    t_map_next = (t_map_next + 1) % kMapCache;
+    e.key = k;
+    e.map = *out;
+    e.used = true;
+    return cudaSuccess;
+}
+
+cudaError_t ensure_smem_limit(const void *func, size_t bytes)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    for (int i = 0; i < g_attr_n; ++i)
+        if (g_attr[i].dev == dev && g_attr[i].func == func && g_attr[i].bytes >= (int)bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < g_attr_n; ++i)
+        if (g_attr[i].dev == dev && g_attr[i].func == func) {
+            g_attr[i].bytes = (int)bytes;
+            return cudaSuccess;
+        }
+    if (g_attr_n < 256) g_attr[g_attr_n++] = {dev, func, (int)bytes};
+    return cudaSuccess;
+}
+
+cudaError_t sm_count(int *n)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_sm_mu);
+    if (!g_sm_count[dev]) {
+        int v = 0;
+        if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        g_sm_count[dev] = v;
+    }
+    *n = g_sm_count[dev];
+    return cudaSuccess;
+}
+
+void profile_set(void *const *events, int count)
+{
+    t_prof_count = 0;
+    for (int i = 0; i < count && i < kMaxProfileEvents; ++i) t_prof[i] = static_cast<cudaEvent_t>(events[i]);
+    t_prof_count = count < kMaxProfileEvents ? count : kMaxProfileEvents;
+    t_prof_next = 0;
+}
+
+void profile_forward_begin() { t_prof_next = 0; }
+
+// External records: under stream capture they become event-record nodes of the
+// graph (timed on replay) instead of capture-internal dependencies.
+void profile_kernel_begin(cudaStream_t s)
+{
+    if (2 * t_prof_next < t_prof_count) cudaEventRecordWithFlags(t_prof[2 * t_prof_next], s, cudaEventRecordExternal);
+}
+
+void profile_kernel_end(cudaStream_t s)
+{
+    if (2 * t_prof_next + 1 < t_prof_count)
+        cudaEventRecordWithFlags(t_prof[2 * t_prof_next + 1], s, cudaEventRecordExternal);
+    ++t_prof_next;
+}
+
+}  // namespace ssd

@@ -20,6 +20,7 @@
 // and never overflow.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -63,6 +64,11 @@ struct Problem {
     const ChunkDesc *chunks;
     int total_chunks;
     unsigned int *err_word;   // device address of the error word
+    // Failure-detection test settings (ssd_test_set_fault): the limit of every
+    // bounded wait of the fused kernels, and the unit (index in the fused
+    // workspace) whose look-back publications are withheld (-1: none).
+    unsigned long long wait_ns;
+    long long withhold;
 };
 
 // Workspace carved out of one device buffer.
@@ -88,6 +94,21 @@ size_t fused_workspace_bytes(const Problem &pr);
 cudaError_t launch_fused_tc(const Problem &pr, void *workspace, cudaStream_t s);
 // Sequential inter-chunk state passing, shared by the multi-kernel paths.
 cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream_t s);
+
+// Host-side caches and the per-kernel timing hook (ssd_host.cu).
+// A 3-D [batch][rows][width] tensor map (bf16 or fp32), box box_cols x box_rows x 1,
+// 128-byte swizzle or none; identical requests reuse one encoded map.
+cudaError_t cached_tensor_map(CUtensorMap *out, const void *ptr, bool bf16, int width, int rows, int batch,
+                              int box_cols, int box_rows, bool swizzle128);
+// Raise a kernel's dynamic shared-memory limit once per (device, kernel, size).
+cudaError_t ensure_smem_limit(const void *func, size_t bytes);
+// SM count of the current device (queried once).
+cudaError_t sm_count(int *n);
+constexpr int kMaxProfileEvents = 16;
+void profile_set(void *const *events, int count);
+void profile_forward_begin();               // at the start of every forward
+void profile_kernel_begin(cudaStream_t s);  // right before a kernel launch, after its host setup
+void profile_kernel_end(cudaStream_t s);    // right after it
 
 constexpr int kMaxChunk = 256;
 constexpr int kMaxHeaddim = 256;

@@ -256,7 +256,7 @@ template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes)
 {
     if (bytes <= 48 * 1024) return cudaSuccess;
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    return ensure_smem_limit(reinterpret_cast<const void *>(kernel), bytes);
 }
 
 }  // namespace
@@ -268,10 +268,14 @@ cudaError_t launch_chunk_state_simt(const Problem &pr, const Workspace &ws, cuda
     cudaError_t e;
     if (pr.dtype == SSD_DTYPE_F32) {
         if ((e = set_smem(chunk_state_simt<float>, smem)) != cudaSuccess) return e;
+        profile_kernel_begin(s);
         chunk_state_simt<float><<<grid, kThreads, smem, s>>>(pr, ws);
+        profile_kernel_end(s);
     } else {
         if ((e = set_smem(chunk_state_simt<__nv_bfloat16>, smem)) != cudaSuccess) return e;
+        profile_kernel_begin(s);
         chunk_state_simt<__nv_bfloat16><<<grid, kThreads, smem, s>>>(pr, ws);
+        profile_kernel_end(s);
     }
     return cudaGetLastError();
 }
@@ -284,10 +288,14 @@ cudaError_t launch_chunk_out_simt(const Problem &pr, const Workspace &ws, cudaSt
     cudaError_t e;
     if (pr.dtype == SSD_DTYPE_F32) {
         if ((e = set_smem(chunk_out_simt<float>, smem)) != cudaSuccess) return e;
+        profile_kernel_begin(s);
         chunk_out_simt<float><<<grid, kThreads, smem, s>>>(pr, ws);
+        profile_kernel_end(s);
     } else {
         if ((e = set_smem(chunk_out_simt<__nv_bfloat16>, smem)) != cudaSuccess) return e;
+        profile_kernel_begin(s);
         chunk_out_simt<__nv_bfloat16><<<grid, kThreads, smem, s>>>(pr, ws);
+        profile_kernel_end(s);
     }
     return cudaGetLastError();
 }
@@ -296,7 +304,9 @@ cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream
 {
     const int PN = pr.headdim * pr.dstate;
     const dim3 grid((PN + kThreads - 1) / kThreads, pr.nheads, pr.batch);
+    profile_kernel_begin(s);
     state_pass<<<grid, kThreads, 0, s>>>(pr, ws);
+    profile_kernel_end(s);
     return cudaGetLastError();
 }
 

@@ -516,16 +516,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 // [batch][seqlen][width] bf16 tensor viewed as 3-D, boxes of 64 columns x 128 tokens.
 cudaError_t make_map(CUtensorMap *map, const void *ptr, int width, int seqlen, int batch)
 {
-    auto fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)seqlen, (cuuint64_t)batch};
-    const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * seqlen};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kBoxRows, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return cached_tensor_map(map, ptr, true, width, seqlen, batch, 64, kBoxRows, true);
 }
 
 size_t state_smem(const Problem &pr) { return 1024 + (size_t)(4 + pr.dstate / 64) * kBoxBytes; }
@@ -546,22 +537,22 @@ cudaError_t launch_tc(const Problem &pr, const Workspace &ws, cudaStream_t s, in
         if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, pr.batch)) != cudaSuccess) return e;
         if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
         const size_t smem = state_smem(pr);
-        if ((e = cudaFuncSetAttribute(chunk_state_tc<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-            cudaSuccess)
-            return e;
+        if ((e = ensure_smem_limit(reinterpret_cast<const void *>(chunk_state_tc<NS>), smem)) != cudaSuccess) return e;
         const dim3 grid(pr.nchunks, pr.nheads / HB, pr.batch);
+        profile_kernel_begin(s);
         chunk_state_tc<NS><<<grid, kThreads, smem, s>>>(xmap, bmap, pr, ws);
+        profile_kernel_end(s);
     } else {
         if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, pr.batch)) != cudaSuccess) return e;
         if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
         if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
         const size_t smem = out_smem(pr);
-        if ((e = cudaFuncSetAttribute(chunk_out_tc<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-            cudaSuccess)
-            return e;
+        if ((e = ensure_smem_limit(reinterpret_cast<const void *>(chunk_out_tc<NS>), smem)) != cudaSuccess) return e;
         const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
         const dim3 grid(pr.nchunks * ntile, pr.nheads / HB, pr.batch);
+        profile_kernel_begin(s);
         chunk_out_tc<NS><<<grid, kThreads, smem, s>>>(xmap, bmap, cmap, pr, ws);
+        profile_kernel_end(s);
     }
     return cudaGetLastError();
 }

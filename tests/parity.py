@@ -83,3 +83,49 @@ def check_rows(inp, rows, chunk, tol=None, inp_cuda=None):
     fg_rows = fg.reshape(b * H * P, N)[idx.cuda()].cpu().numpy()
     ef = assert_close(fg_rows, fr, tol, "final_state (sampled rows)")
     return ey, ef
+
+
+def check_all_rows(inp, chunk, tol=None, rows_per_call=None, record=None):
+    """Every (b, h, p) row of a large workload against the oracle: one GPU run,
+    then the oracle over row batches (bounded host memory), the comparison
+    accumulated over the whole tensor -- max_i (|d_i| - u |ref_i|)^+ over every
+    element against the RMS of the whole reference, for y and for the final
+    state.  Returns the storage-adjusted and the raw errors (x RMS); with
+    ``record`` (a dict) they are also stored there."""
+    tol = tol or TOL[inp["x"].dtype]
+    b, L, H, P = inp["x"].shape
+    N = inp["B"].shape[3]
+    yg, fg = run_gpu(to_cuda(inp), chunk)
+    total = b * H * P
+    per = rows_per_call or max(64, min(4096, int(2 ** 27 // max(L, 1))))
+    u = STORAGE_U[yg.dtype]
+    yg_rows = yg.permute(0, 2, 3, 1).reshape(total, L)  # [rows, L] on the device
+    fg_rows = fg.reshape(total, N)
+    stats = {"y": [0.0, 0.0, 0.0, 0], "final_state": [0.0, 0.0, 0.0, 0]}  # adj max, raw max, sum sq, count
+
+    def acc(key, got, want, uu):
+        d = np.abs(got - want)
+        st = stats[key]
+        st[0] = max(st[0], float((d - uu * np.abs(want)).max()))
+        st[1] = max(st[1], float(d.max()))
+        st[2] += float(np.sum(want * want))
+        st[3] += want.size
+
+    for r0 in range(0, total, per):
+        rows = list(range(r0, min(total, r0 + per)))
+        yr, fr = oracle.recurrence(**inp, rows=rows)
+        got_y = yg_rows[r0:r0 + len(rows)].float().cpu().numpy().astype(np.float64)
+        got_f = fg_rows[r0:r0 + len(rows)].cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(got_y)) and np.all(np.isfinite(got_f)), "non-finite values in the GPU result"
+        acc("y", got_y, yr, u)
+        acc("final_state", got_f, fr, 2.0 ** -24)
+    out = {}
+    for key, (adj, raw, ss, n) in stats.items():
+        rms = float(np.sqrt(ss / n)) or 1.0
+        out[key] = {"err": max(adj, 0.0) / rms, "raw": raw / rms, "rms": rms}
+    if record is not None:
+        record.update(out)
+    for key in ("y", "final_state"):
+        assert out[key]["err"] <= tol, (f"{key} (all rows): error {out[key]['err']:.3e} x RMS beyond the output's "
+                                        f"own rounding (raw max-abs {out[key]['raw']:.3e} x RMS) exceeds {tol:.1e}")
+    return out

@@ -203,3 +203,9 @@ def test_varlen_runs_only_where_the_fused_kernels_do(lib):
     assert _varlen(lib, [0, 5, 9], dtype=ssd.SSD_DTYPE_F32) == ssd.SSD_ERR_UNSUPPORTED
     assert _varlen(lib, [0, 5, 9], headdim=32) == ssd.SSD_ERR_UNSUPPORTED
     assert "fused kernels" in ssd.ssd_last_error_detail()
+
+
+def test_fault_hook_argument_checks(lib):
+    assert lib.ssd_test_set_fault(0, -2) == ssd.SSD_ERR_INVALID_ARG
+    assert lib.ssd_test_set_fault(1000, 3) == ssd.SSD_OK
+    assert lib.ssd_test_set_fault(0, -1) == ssd.SSD_OK
