@@ -281,7 +281,9 @@ def pre_step_measurement(sets, w, stream, steps=100):
     return {"workload": w.name, "modes": "softplus(dt + bias), bias = log(expm1(0.01)); zero-order hold",
             "us_per_step_ssd_fwd": t_plain,
             "us_per_step_ssd_fwd_pre": t_pre, "overhead_us": t_pre - t_plain,
-            "tokens_per_s": w.tokens / (t_pre * 1e-6), "kernels": ["pre_kernel", "ssd_fused_pipe_tc"]}
+            "tokens_per_s": w.tokens / (t_pre * 1e-6),
+            "kernels": ["pre_kernel"] + ssd.ssd_fwd_kernels(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate,
+                                                            w.chunk, wl.torch_dtype(w.dtype))}
 
 
 def varlen_step_measurement(sets, w, stream, peaks, steps=100, nseq=12, seed=5):

@@ -165,7 +165,11 @@ SSD_API ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A
  * headdim 64 or 128, dstate 64 or 128, chunk <= 128) and returns
  * SSD_ERR_UNSUPPORTED, with the needed and available sizes in
  * ssd_last_error_detail(), for anything else or for a problem whose scratch
- * (ssd_fwd_workspace_size) exceeds 32 MiB.
+ * (ssd_fwd_workspace_size) exceeds 32 MiB.  At dstate 64 the scratch is one
+ * state slot per CTA, at most 16 MiB, so every size fits (the 2.7B-shaped
+ * layer, batch 2 x 2048 tokens, uses 16 MiB); at dstate 128 it is 128 KiB per
+ * (chunk, head block) unit, so at most 255 units fit (the grouped layer of
+ * 16 x 4096 tokens, 32 heads x 128, needs 2 GiB and is rejected).
  *
  * The first call on a device looks up the scratch array's device address
  * (cudaGetSymbolAddress) and caches it; make that first call before any stream

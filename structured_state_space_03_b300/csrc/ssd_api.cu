@@ -133,7 +133,8 @@ static const char *kernel_names(const Problem &pr)
     switch (choose_path(pr)) {
     case SSD_PATH_SIMT: return "chunk_state_simt,state_pass,chunk_out_simt";
     case SSD_PATH_TCGEN05: return "chunk_state_tc,state_pass,chunk_out_tc";
-    case SSD_PATH_TCGEN05_FUSED: return pr.dstate == 64 ? "ssd_fused_pipe_tc" : "ssd_fused_tc";
+    case SSD_PATH_TCGEN05_FUSED:
+        return seq_supported(pr) ? "ssd_seq_pipe_tc" : (pr.dstate == 64 ? "ssd_fused_pipe_tc" : "ssd_fused_tc");
     default: return "";
     }
 }

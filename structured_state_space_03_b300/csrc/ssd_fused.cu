@@ -589,7 +589,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     top -= 32;  // 32 aggregates, keep walking
                     continue;
                 }
-                if (globaltimer() - tstart > lim) {
+                // every lane must take the same exit: the next pass's ballots need all 32
+                if (__any_sync(0xffffffffu, globaltimer() - tstart > lim)) {
                     timed_out = true;
                     break;
                 }
@@ -1113,6 +1114,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             named_sync(kBarFront, 128);  // every v_j dt_j is in shared memory
             ok = mbar_wait(&bar_full[s], ph, lim) && (it < 2 || mbar_wait(&bar_lo[s], ph ^ 1, lim));
             ok = ok && mbar_wait(&bar_g[s], ph, lim);
+            ok = __all_sync(0xffffffffu, ok);  // the TMEM accesses below are warp-collective
             tc_fence_after();
             if (ok && fast) {  // tril(G) -> bf16 pairs in TMEM (row m, columns jb*32 .. jb*32+31)
                 const uint32_t slot = tmem + s * 256 + lane_base;
@@ -1256,11 +1258,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                                 top -= 32;
                                 continue;
                             }
-                            if (round == 0 && !unit_is_last<kPacked>(pr, u) && mbar_test_wait(&bar_mma[s], ph)) {
+                            // every lane must take the same exit: the next pass's ballots need all 32
+                            if (round == 0 && !unit_is_last<kPacked>(pr, u) &&
+                                __any_sync(0xffffffffu, mbar_test_wait(&bar_mma[s], ph))) {
                                 res = -2;
                                 break;
                             }
-                            if (globaltimer() - tstart > lim) break;
+                            if (__any_sync(0xffffffffu, globaltimer() - tstart > lim)) break;
                             __nanosleep(128);
                         }
                         if (lane == 0) s_walk[team][round] = res;
@@ -1277,6 +1281,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     }
                     // publish S_c (scaled to the chunk end) as this unit's aggregate
                     ok = mbar_wait(&bar_mma[s], ph, lim) && mbar_wait(&bar_seg[ss], pq, lim);
+                    ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
                     tc_fence_after();
                     if (ok) {
                         const float sfac = s_sfac[ss][hh_m];
@@ -1334,6 +1339,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 }
             }
             ok = ok && mbar_wait(&bar_mma[s], ph, lim) && mbar_wait(&bar_seg[ss], pq, lim);
+            ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
             tc_fence_after();
             const bool fast = s_fast[ss] != 0;
             if (tt == 0) {  // x of the unit for the D x term, into the staging region (wx lo is dead)
@@ -1412,6 +1418,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             // written over it (the same swizzled position), then stored by TMA
             const bool row_in = m < u.len;
             ok = !any_fail && mbar_wait(&bar_yo[s], ph, lim) && mbar_wait(&bar_xe[s], ph, lim);
+            ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
             tc_fence_after();
             uint8_t *ystage = st + 2 * kSlab;
             if (ok && fast) {
@@ -1567,6 +1574,7 @@ bool fused_supported(const Problem &pr)
 
 size_t fused_workspace_bytes(const Problem &pr)
 {
+    if (seq_supported(pr)) return seq_workspace_bytes(pr);
     const size_t units = units_of(pr);
     const size_t states = units * kRows * pr.dstate * sizeof(float);
     return 2 * up256(states) + up256(units * 2 * sizeof(float)) + up256((2 * units + kCtrCount) * sizeof(uint32_t));
@@ -1574,6 +1582,7 @@ size_t fused_workspace_bytes(const Problem &pr)
 
 cudaError_t launch_fused_tc(const Problem &pr, void *workspace, cudaStream_t s)
 {
+    if (seq_supported(pr)) return launch_seq_tc(pr, workspace, s);
     const size_t units = units_of(pr);
     const size_t states = units * kRows * pr.dstate * sizeof(float);
     char *p = static_cast<char *>(workspace);

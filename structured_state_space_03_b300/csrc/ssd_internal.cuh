@@ -92,6 +92,12 @@ cudaError_t launch_chunk_out_tc(const Problem &pr, const Workspace &ws, cudaStre
 bool fused_supported(const Problem &pr);
 size_t fused_workspace_bytes(const Problem &pr);
 cudaError_t launch_fused_tc(const Problem &pr, void *workspace, cudaStream_t s);
+// Sequence-pipelined fused kernel (ssd_seq.cu): dstate 64, the batch layout of
+// the fused kernels; every CTA carries the recurrence of its own run of chunks
+// on chip and exchanges states only where a sequence continues on the next CTA.
+bool seq_supported(const Problem &pr);
+size_t seq_workspace_bytes(const Problem &pr);
+cudaError_t launch_seq_tc(const Problem &pr, void *workspace, cudaStream_t s);
 // Sequential inter-chunk state passing, shared by the multi-kernel paths.
 cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream_t s);
 

@@ -133,6 +133,7 @@ def test_path_selection_is_a_pure_host_query(lib):
     assert ssd.ssd_fwd_path(2, 333, 6, 32, 3, 48, 100, ssd.SSD_DTYPE_BF16) == "simt"
     assert ssd.ssd_fwd_path(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_F32) == "simt"
     assert ssd.ssd_fwd_kernels(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == ["ssd_fused_pipe_tc"]
+    assert ssd.ssd_fwd_kernels(1, 65536, 8, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == ["ssd_seq_pipe_tc"]
     assert ssd.ssd_fwd_kernels(16, 4096, 32, 128, 8, 128, 128, ssd.SSD_DTYPE_BF16) == ["ssd_fused_tc"]
     assert ssd.ssd_fwd_kernels(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == [
         "chunk_state_tc", "state_pass", "chunk_out_tc"]

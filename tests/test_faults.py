@@ -21,8 +21,10 @@ from parity import check_full, to_cuda
 
 pytestmark = pytest.mark.gpu
 
-# (b, L, H, P, N, G, Q): the persistent dstate-64 kernel, the one-unit dstate-128 kernel
-FUSED = [(2, 1000, 8, 64, 64, 2, 128), (1, 700, 4, 128, 128, 1, 100)]
+# (b, L, H, P, N, G, Q): the sequence-pipelined dstate-64 kernel (few sequences), the
+# persistent look-back dstate-64 kernel (40 sequences), the one-unit dstate-128 kernel
+FUSED = [(2, 1000, 8, 64, 64, 2, 128), (1, 700, 80, 64, 64, 1, 128), (1, 700, 4, 128, 128, 1, 100)]
+KERNELS = ["ssd_seq_pipe_tc", "ssd_fused_pipe_tc", "ssd_fused_tc"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -40,10 +42,10 @@ def _reset_hook():
     ssd.ssd_test_set_fault(0, -1)
 
 
-@pytest.mark.parametrize("case", FUSED, ids=[f"N{c[4]}" for c in FUSED])
-def test_withheld_state_times_out_then_recovers(case):
+@pytest.mark.parametrize("case,kernel", list(zip(FUSED, KERNELS)), ids=KERNELS)
+def test_withheld_state_times_out_then_recovers(case, kernel):
     b, L, H, P, N, G, Q = case
-    assert ssd.ssd_fwd_path(b, L, H, P, G, N, Q, torch.bfloat16) == "tcgen05_fused"
+    assert ssd.ssd_fwd_kernels(b, L, H, P, G, N, Q, torch.bfloat16) == [kernel]
     inp = make_inputs(b, L, H, P, N, G, "bf16", seed=71 + N, with_init=True)
     c = to_cuda(inp)
     ssd.ssd_check_device_status()  # start from a clear error word

@@ -95,7 +95,12 @@ def test_equal_lengths_equal_the_batch_layout():
     yb, fb = ssd.ssd_fwd(c["x"].reshape(b, L, H, P), c["dt"].reshape(b, L, H), c["A"], c["B"].reshape(b, L, G, N),
                          c["C"].reshape(b, L, G, N), c["D"], c["init_state"], chunk=Q)
     ssd.ssd_check_device_status()
-    assert torch.equal(y.reshape(b, L, H, P), yb) and torch.equal(f, fb)
+    # the packed layout runs its own kernel instance (and, at dstate 64, another
+    # kernel than the batch layout): the same values up to rounding, y within one
+    # unit of its own bf16 rounding
+    assert_close(y.reshape(b, L, H, P).float().cpu().numpy(), yb.float().cpu().numpy(), TOL[torch.bfloat16] / 100,
+                 "y, packed vs batch layout", 2 * STORAGE_U[torch.bfloat16])
+    assert_close(f.cpu().numpy(), fb.cpu().numpy(), TOL[torch.bfloat16] / 100, "final state, packed vs batch layout")
 
 
 def test_state_carried_in_place_and_empty_sequences():
