@@ -18,6 +18,12 @@ scalar-per-head A and input scaling dt*B):
 semiseparable matrix form of "Mamba 模型" §4.1 by brute force (O2) and
 ``assoc_scan`` evaluates the same map by a Blelloch scan over (decay, input)
 pairs ("Mamba 模型" §3.4) (O3); both exist to pin O1, not to replace it.
+
+``backward`` (O4) returns the gradients of sum(dy * y) + sum(dfinal * final)
+with respect to every input, by the reverse-time adjoint of the recurrence with
+each row's states recomputed ("Mamba 模型" §3.4 on recomputation in the
+backward pass); tests/test_oracle_backward.py pins it by central differences of
+O1, torch autodiff of the written-out recurrence and closed forms.
 """
 from __future__ import annotations
 
@@ -55,6 +61,9 @@ def _bind(lib):
     if hasattr(lib, "oracle_ssd_recurrence_pre"):
         lib.oracle_ssd_recurrence_pre.argtypes = [p, p, p, ctypes.c_int] + common[2:] + [p, L, p, p, ctypes.c_int]
         lib.oracle_ssd_recurrence_pre.restype = ctypes.c_int
+    if hasattr(lib, "oracle_ssd_backward"):
+        lib.oracle_ssd_backward.argtypes = common + [p, p, p, p, p, p, p, p, p, ctypes.c_int]
+        lib.oracle_ssd_backward.restype = ctypes.c_int
     for name in ("oracle_ssd_quadratic", "oracle_ssd_assoc_scan"):
         fn = getattr(lib, name)
         fn.argtypes = common + [p, p]
@@ -191,6 +200,30 @@ def recurrence_with(lib, x, dt, A, B, C, D=None, init_state=None):
     if rc != 0:
         raise RuntimeError(f"oracle_ssd_recurrence failed with {rc}")
     return (y.reshape(b, H, P, L).transpose(0, 3, 1, 2).copy(), fin.reshape(b, H, P, N))
+
+
+def backward(x, dt, A, B, C, D=None, init_state=None, dy=None, dfinal=None, nthreads=None, lib=None):
+    """Gradients of  sum(dy * y) + sum(dfinal * final_state)  through the
+    recurrence (fp64, reverse-time adjoint with each row's states recomputed).
+    ``dy`` [b,L,H,P] and ``dfinal`` [b,H,P,N] (or None) are taken as fp64.
+    Returns a dict of fp64 arrays: dx [b,L,H,P], ddt [b,L,H], dA [H], dB and
+    dC [b,L,G,N], dD [H], dinit [b,H,P,N]."""
+    arrs, xd, (b, L, H, P, G, N) = _prepare(x, dt, A, B, C, D, init_state)
+    lib = lib or load_library()
+    dya = np.ascontiguousarray(np.asarray(dy, dtype=np.float64))
+    if dya.shape != (b, L, H, P):
+        raise ValueError("dy must be [b,L,H,P]")
+    dfa = None if dfinal is None else np.ascontiguousarray(np.asarray(dfinal, dtype=np.float64))
+    if dfa is not None and dfa.shape != (b, H, P, N):
+        raise ValueError("dfinal must be [b,H,P,N]")
+    out = {"dx": np.empty((b, L, H, P)), "ddt": np.empty((b, L, H)), "dA": np.empty(H), "dB": np.empty((b, L, G, N)),
+           "dC": np.empty((b, L, G, N)), "dD": np.empty(H), "dinit": np.empty((b, H, P, N))}
+    rc = lib.oracle_ssd_backward(*[_ptr(a) for a in arrs], xd, b, L, H, P, G, N, _ptr(dya), _ptr(dfa),
+                                 _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]),
+                                 _ptr(out["dD"]), _ptr(out["dinit"]), int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_ssd_backward failed with {rc}")
+    return out
 
 
 PRE_SOFTPLUS, PRE_ZOH = 1, 2

@@ -1,5 +1,6 @@
 /*
- * ssd_oracle.c -- plain, slow, fp64 CPU oracle for the Mamba-2 SSD layer forward.
+ * ssd_oracle.c -- plain, slow, fp64 CPU oracle for the Mamba-2 SSD layer forward
+ * and, at the end of the file, its backward (gradients of a scalar loss).
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the yardstick the CUDA library is
  * checked against; it is used by the tests, by the smoke check and by the
@@ -467,4 +468,177 @@ int oracle_ssd_assoc_scan(const void *x, const float *dt, const float *A, const 
     free(u);
     free(tmp);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward: gradients of a scalar loss through the recurrence.             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The loss is  sum_{b,t,h,p} dy[b,t,h,p] y[b,t,h,p] + sum dfinal * final_state
+ * (dy and dfinal are the incoming gradients; dfinal may be NULL => 0), and the
+ * gradients follow the recurrence above by the chain rule, in reverse time
+ * ("Mamba 模型" §3.4: the backward pass recomputes the intermediate states
+ * instead of reading stored ones; here each row's states are recomputed by a
+ * forward sweep and kept for its reverse sweep).  Per row (b, h, p), with
+ * a_t = exp(dt_t A_h) and lam_t = dLoss/ds_t (the whole vector over n):
+ *     lam_{L-1} = dy_{L-1}[p] C_{L-1} + dfinal[b,h,p,:]
+ *     lam_t     = dy_t[p] C_t + a_{t+1} lam_{t+1}
+ *     dC_t[n]  += dy_t[p] s_t[n]
+ *     dB_t[n]  += dt_t x_t[p] lam_t[n]
+ *     dx_t[p]   = D_h dy_t[p] + dt_t (B_t . lam_t)
+ *     ddt_t    += x_t[p] (B_t . lam_t) + A_h a_t (lam_t . s_{t-1})
+ *     dA_h     += dt_t a_t (lam_t . s_{t-1})
+ *     dD_h     += dy_t[p] x_t[p]
+ *     dinit[b,h,p,:] = a_0 lam_0
+ * (dB, dC sum over the heads of the group and over p; ddt over p; dA, dD over
+ * b, t and p.)  dy is given in fp64 (the exact values the caller's dtype
+ * holds).  Outputs are fp64, all with the layouts of the forward inputs:
+ * dx [b][L][H][P], ddt [b][L][H], dA [H], dB, dC [b][L][G][N], dD [H],
+ * dinit [b][H][P][N].  Work is threaded over (batch, group) pairs, each worker
+ * owning every output element it writes.
+ */
+typedef struct {
+    const oracle_problem *pr;
+    const double *dy, *dfinal;
+    double *dx, *ddt, *dB, *dC, *dinit;
+    double *dA_part, *dD_part;  /* [batch * ngroups][nheads] partial sums */
+    long next, npairs;
+    int failed;
+} backward_job;
+
+static void backward_pair(backward_job *job, long bg, double *s_all, double *lam)
+{
+    const oracle_problem *pr = job->pr;
+    const long L = pr->seqlen, H = pr->nheads, P = pr->headdim, G = pr->ngroups, N = pr->dstate;
+    const long b = bg / G, g = bg % G, hpg = H / G;
+    for (long h = g * hpg; h < (g + 1) * hpg; ++h) {
+        const double A_h = (double)pr->A[h];
+        const double D_h = pr->D ? (double)pr->D[h] : 0.0;
+        for (long p = 0; p < P; ++p) {
+            /* forward sweep: s_all[(t+1)*N + n] = s_t[n], s_all[n] = s_{-1}[n] */
+            for (long n = 0; n < N; ++n)
+                s_all[n] = pr->init ? (double)pr->init[((b * H + h) * P + p) * N + n] : 0.0;
+            for (long t = 0; t < L; ++t) {
+                const long ti = (b * L + t) * H + h; /* (b, t, h) */
+                const double dt_t = (double)pr->dt[ti];
+                const double a_t = exp(dt_t * A_h);
+                const double x_t = widen(pr->x, ti * P + p, pr->in_dtype);
+                const long bc = ((b * L + t) * G + g) * N;
+                for (long n = 0; n < N; ++n)
+                    s_all[(t + 1) * N + n] = a_t * s_all[t * N + n] + dt_t * x_t * widen(pr->B, bc + n, pr->in_dtype);
+            }
+            /* reverse sweep */
+            for (long n = 0; n < N; ++n)
+                lam[n] = job->dfinal ? job->dfinal[((b * H + h) * P + p) * N + n] : 0.0;
+            for (long t = L - 1; t >= 0; --t) {
+                const long ti = (b * L + t) * H + h;
+                const double dt_t = (double)pr->dt[ti];
+                const double a_t = exp(dt_t * A_h);
+                const long xi = ti * P + p;
+                const double x_t = widen(pr->x, xi, pr->in_dtype);
+                const double dy_t = job->dy[xi];
+                const long bc = ((b * L + t) * G + g) * N;
+                double b_lam = 0.0, lam_sprev = 0.0;
+                for (long n = 0; n < N; ++n) {
+                    lam[n] += dy_t * widen(pr->C, bc + n, pr->in_dtype);  /* lam_t */
+                    const double B_n = widen(pr->B, bc + n, pr->in_dtype);
+                    job->dC[bc + n] += dy_t * s_all[(t + 1) * N + n];
+                    job->dB[bc + n] += dt_t * x_t * lam[n];
+                    b_lam += B_n * lam[n];
+                    lam_sprev += lam[n] * s_all[t * N + n];
+                }
+                job->dx[xi] = D_h * dy_t + dt_t * b_lam;
+                job->ddt[ti] += x_t * b_lam + A_h * a_t * lam_sprev;
+                job->dA_part[bg * H + h] += dt_t * a_t * lam_sprev;
+                job->dD_part[bg * H + h] += dy_t * x_t;
+                for (long n = 0; n < N; ++n)
+                    lam[n] *= a_t;  /* a_t lam_t: the part of lam_{t-1} carried back */
+            }
+            if (job->dinit)
+                for (long n = 0; n < N; ++n)
+                    job->dinit[((b * H + h) * P + p) * N + n] = lam[n];
+        }
+    }
+}
+
+static void *backward_worker(void *arg)
+{
+    backward_job *job = (backward_job *)arg;
+    const long L = job->pr->seqlen, N = job->pr->dstate;
+    double *s_all = (double *)malloc(sizeof(double) * (size_t)((L + 1) * N));
+    double *lam = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!s_all || !lam) {
+        __atomic_store_n(&job->failed, 1, __ATOMIC_RELAXED);
+        free(s_all);
+        free(lam);
+        return NULL;
+    }
+    for (;;) {
+        long i = __atomic_fetch_add(&job->next, 1, __ATOMIC_RELAXED);
+        if (i >= job->npairs)
+            break;
+        backward_pair(job, i, s_all, lam);
+    }
+    free(s_all);
+    free(lam);
+    return NULL;
+}
+
+int oracle_ssd_backward(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                        const float *D, const float *init_state, int in_dtype, long batch, long seqlen,
+                        long nheads, long headdim, long ngroups, long dstate, const double *dy,
+                        const double *dfinal, double *dx, double *ddt, double *dA, double *dB, double *dC,
+                        double *dD, double *dinit, int nthreads)
+{
+    oracle_problem pr = {x, dt, A, B, C, D, init_state, in_dtype, batch, seqlen, nheads, headdim, ngroups, dstate,
+                         NULL, 0};
+    if (check_problem(&pr) || !dy || !dx || !ddt || !dA || !dB || !dC || !dD)
+        return -1;
+    const long npairs = batch * ngroups;
+    memset(ddt, 0, sizeof(double) * (size_t)(batch * seqlen * nheads));
+    memset(dB, 0, sizeof(double) * (size_t)(batch * seqlen * ngroups * dstate));
+    memset(dC, 0, sizeof(double) * (size_t)(batch * seqlen * ngroups * dstate));
+    double *dA_part = (double *)calloc((size_t)(npairs * nheads), sizeof(double));
+    double *dD_part = (double *)calloc((size_t)(npairs * nheads), sizeof(double));
+    if (!dA_part || !dD_part) {
+        free(dA_part);
+        free(dD_part);
+        return -2;
+    }
+    backward_job job = {&pr, dy, dfinal, dx, ddt, dB, dC, dinit, dA_part, dD_part, 0, npairs, 0};
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > npairs)
+        nthreads = (int)npairs;
+    if (nthreads == 1) {
+        backward_worker(&job);
+    } else {
+        pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+        int started = 0;
+        if (tid)
+            for (int i = 0; i < nthreads; ++i) {
+                if (pthread_create(&tid[i], NULL, backward_worker, &job) != 0)
+                    break;
+                ++started;
+            }
+        if (started == 0)
+            backward_worker(&job);
+        for (int i = 0; i < started; ++i)
+            pthread_join(tid[i], NULL);
+        free(tid);
+    }
+    /* the per-pair partial sums, added in a fixed order */
+    for (long h = 0; h < nheads; ++h) {
+        double a = 0.0, d = 0.0;
+        for (long i = 0; i < npairs; ++i) {
+            a += dA_part[i * nheads + h];
+            d += dD_part[i * nheads + h];
+        }
+        dA[h] = a;
+        dD[h] = d;
+    }
+    free(dA_part);
+    free(dD_part);
+    return job.failed ? -2 : 0;
 }
