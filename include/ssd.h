@@ -1,6 +1,6 @@
 /*
  * ssd.h -- C ABI of libssd, a single-GPU (B300, sm_103a) implementation of the
- * Mamba-2 state-space-duality (SSD) layer's forward scan.
+ * Mamba-2 state-space-duality (SSD) layer's forward scan, and its backward.
  *
  * The layer ("Mamba 模型" §4.1-4.2; "草稿:Mamba2", state space duality) maps
  * per-token inputs x, step sizes dt and projections B, C to outputs y through
@@ -271,6 +271,75 @@ SSD_API ssd_status_t ssd_fwd_pre(const void *x, const float *dt, const float *dt
 SSD_API ssd_status_t ssd_step(const void *x, const float *dt, const float *A, const void *B, const void *C,
                               const float *D, float *state, void *y, int batch, int nheads, int headdim,
                               int ngroups, int dstate, ssd_dtype_t dtype, void *stream);
+
+/*
+ * ssd_bwd -- backward of ssd_fwd: the gradients of a scalar loss L with
+ * respect to every input, given the loss's gradients dy = dL/dy and
+ * dfinal_state = dL/d final_state.  By the chain rule through the recurrence
+ * above, with lam_t = dL/dh_t (per (batch, head, headdim row), a vector over
+ * dstate), lam_{L-1} = dy_{L-1} C_{L-1} + dfinal, lam_t = dy_t C_t + a_{t+1} lam_{t+1},
+ * a_t = exp(dt_t A_h):
+ *
+ *     dx_t    = D_h dy_t + dt_t (B_t . lam_t)
+ *     dB_t    = sum over the group's heads and rows of dt_t x_t lam_t
+ *     dC_t    = sum over the group's heads and rows of dy_t h_t
+ *     ddt_t   = sum over rows of x_t (B_t . lam_t) + A_h a_t (lam_t . h_{t-1})
+ *     dA_h    = sum over batch, tokens and rows of dt_t a_t (lam_t . h_{t-1})
+ *     dD_h    = sum of dy_t x_t;     dinit = a_0 lam_0
+ *
+ * The pages ask the backward to recompute the intermediate states rather than
+ * store them ("Mamba 模型" §3.4, recomputation); this call keeps nothing from
+ * the forward: it recomputes the per-chunk states from the inputs with the
+ * same block decomposition ("Mamba 模型" §4.1; its own chunk length, 64
+ * tokens) and runs the adjoint state recurrence backwards over the chunks.
+ *
+ *   x, dt, A, B, C, D, init_state   the forward's inputs, as in ssd_fwd (D and
+ *                                   init_state may be NULL, meaning 0)
+ *   dy           [batch][seqlen][nheads][headdim]  dtype (the type of x)
+ *   dfinal_state [batch][nheads][headdim][dstate]  fp32, NULL means 0
+ *   dx           OUT [batch][seqlen][nheads][headdim]  fp32
+ *   ddt          OUT [batch][seqlen][nheads]           fp32
+ *   dA           OUT [nheads]                          fp32
+ *   dB, dC       OUT [batch][seqlen][ngroups][dstate]  fp32
+ *   dD           OUT [nheads] fp32, NULL skips it (written also when D is NULL)
+ *   dinit_state  OUT [batch][nheads][headdim][dstate]  fp32, NULL skips it
+ *
+ * Every gradient is fp32 whatever dtype is: all arithmetic is fp32 FMA, and
+ * the sums over heads, chunks and batch run in a fixed order, so two calls on
+ * the same inputs give identical bits.  A_h <= 0 is assumed (every exponent is
+ * then <= 0).  Device pointers, alignment, ownership and asynchrony as for
+ * ssd_fwd; outputs must not overlap inputs or each other.  A device workspace
+ * of ssd_bwd_workspace_size() bytes is taken from the stream-ordered allocator.
+ * Returns SSD_OK once the work is enqueued; SSD_ERR_INVALID_ARG for a NULL
+ * required pointer, a dimension <= 0, nheads % ngroups != 0, an unknown dtype or
+ * a misaligned pointer; SSD_ERR_UNSUPPORTED for headdim > 128 or dstate > 256;
+ * SSD_ERR_NO_MEMORY / SSD_ERR_CUDA as for ssd_fwd.
+ */
+SSD_API ssd_status_t ssd_bwd(const void *x, const float *dt, const float *A, const void *B, const void *C,
+                             const float *D, const float *init_state, const void *dy, const float *dfinal_state,
+                             float *dx, float *ddt, float *dA, float *dB, float *dC, float *dD, float *dinit_state,
+                             int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                             ssd_dtype_t dtype, void *stream);
+
+/*
+ * ssd_bwd_workspace_size -- bytes of device workspace one ssd_bwd takes for
+ * these sizes: the recomputed chunk states and the adjoint chunk states
+ * (2 x [batch][nheads][nchunks][headdim][dstate] fp32, 64-token chunks), chunk
+ * decays, per-chunk parts of dA and dD, and, when a group has more than one
+ * head, per-head parts of dB and dC (2 x [batch][seqlen][nheads][dstate] fp32).
+ * Same argument checks as ssd_bwd (no pointers involved).
+ */
+SSD_API ssd_status_t ssd_bwd_workspace_size(int batch, int seqlen, int nheads, int headdim, int ngroups,
+                                            int dstate, ssd_dtype_t dtype, size_t *bytes);
+
+/*
+ * ssd_bwd_kernels -- how many kernels one ssd_bwd launches for these sizes,
+ * with their names written comma-separated into `names` as ssd_fwd_kernels
+ * does; -1 when the sizes are rejected.  Pure host function.  ssd_profile_events
+ * times ssd_bwd's kernels the same way as a forward's.
+ */
+SSD_API int ssd_bwd_kernels(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                            ssd_dtype_t dtype, char *names, size_t names_len);
 
 /*
  * ssd_fwd_path -- the kernel family ssd_fwd would run for these sizes

@@ -1,11 +1,13 @@
-"""Python binding of libssd: the Mamba-2 SSD layer forward scan on one B300.
+"""Python binding of libssd: the Mamba-2 SSD layer forward scan (and its
+backward) on one B300.
 
 Thin ctypes marshalling over the C ABI declared in ``include/ssd.h``; every
 step of the computation runs in the library's CUDA kernels.  PyTorch is used
 for device memory and streams only.  The functions carry the C names:
 
     ssd_fwd, ssd_fwd_ws, ssd_fwd_host, ssd_fwd_pre, ssd_fwd_varlen, ssd_fwd_noalloc, ssd_fwd_workspace_size,
-    ssd_fwd_path, ssd_step, ssd_fwd_kernels, ssd_profile_events, ssd_test_set_fault,
+    ssd_fwd_path, ssd_step, ssd_fwd_kernels, ssd_bwd, ssd_bwd_workspace_size, ssd_bwd_kernels,
+    ssd_profile_events, ssd_test_set_fault,
     ssd_check_device_status, ssd_status_string, ssd_last_error_detail, ssd_version
 
 Layouts: x, y [batch, seqlen, nheads, headdim]; dt [batch, seqlen, nheads];
@@ -47,6 +49,9 @@ SIGNATURES = {
     "ssd_fwd_pre": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "ssd_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_int), _I, _P, _P, _P, _I, _I, _I, _I, _I,
                             _I, _P]),
+    "ssd_bwd": (_I, [_P] * 16 + [_I] * 7 + [_P]),
+    "ssd_bwd_workspace_size": (_I, [_I] * 7 + [ctypes.POINTER(ctypes.c_size_t)]),
+    "ssd_bwd_kernels": (_I, [_I] * 7 + [ctypes.c_char_p, _S]),
     "ssd_fwd_workspace_size": (_I, _DIMS + [ctypes.POINTER(ctypes.c_size_t)]),
     "ssd_fwd_path": (_I, _DIMS),
     "ssd_fwd_kernels": (_I, _DIMS + [ctypes.c_char_p, _S]),
@@ -283,6 +288,49 @@ def ssd_step(x, dt, A, B, C, D=None, *, state, y=None, stream=None):
     _check(lib().ssd_step(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state), _ptr(y), b, H, P, G, N,
                           _dtype_code(el), _stream_handle(stream)))
     return y
+
+
+def ssd_bwd(x, dt, A, B, C, D=None, init_state=None, *, dy, dfinal_state=None, want_dD: bool = True,
+            want_dinit: bool = True, stream=None):
+    """Backward of ssd_fwd on CUDA tensors: gradients of a loss given ``dy``
+    (like x) and ``dfinal_state`` (float32 [batch, nheads, headdim, dstate] or
+    None).  Returns a dict of float32 tensors dx, ddt, dA, dB, dC, dD and
+    dinit_state (the last two None when not wanted)."""
+    b, L, H, P, G, N = _validate(x, dt, A, B, C, D, init_state, "cuda")
+    if tuple(dy.shape) != tuple(x.shape) or dy.dtype != x.dtype or not dy.is_contiguous() or dy.device != x.device:
+        raise ValueError("dy must be a contiguous tensor like x")
+    if dfinal_state is not None and (tuple(dfinal_state.shape) != (b, H, P, N) or dfinal_state.dtype != torch.float32
+                                     or not dfinal_state.is_contiguous() or dfinal_state.device != x.device):
+        raise ValueError("dfinal_state must be contiguous float32 [batch, nheads, headdim, dstate] on x's device")
+    f32 = dict(dtype=torch.float32, device=x.device)
+    out = {"dx": torch.empty(b, L, H, P, **f32), "ddt": torch.empty(b, L, H, **f32), "dA": torch.empty(H, **f32),
+           "dB": torch.empty(b, L, G, N, **f32), "dC": torch.empty(b, L, G, N, **f32),
+           "dD": torch.empty(H, **f32) if want_dD else None,
+           "dinit_state": torch.empty(b, H, P, N, **f32) if want_dinit else None}
+    _check(lib().ssd_bwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init_state), _ptr(dy),
+                         _ptr(dfinal_state), _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]),
+                         _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dinit_state"]), b, L, H, P, G, N,
+                         _dtype_code(x.dtype), _stream_handle(stream)))
+    return out
+
+
+def ssd_bwd_workspace_size(batch, seqlen, nheads, headdim, ngroups, dstate, dtype) -> int:
+    code = _dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype)
+    out = ctypes.c_size_t(0)
+    _check(lib().ssd_bwd_workspace_size(batch, seqlen, nheads, headdim, ngroups, dstate, code, ctypes.byref(out)))
+    return out.value
+
+
+def ssd_bwd_kernels(batch, seqlen, nheads, headdim, ngroups, dstate, dtype) -> list:
+    """Names of the kernels one ssd_bwd launches for these sizes, in order."""
+    code = _dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype)
+    buf = ctypes.create_string_buffer(512)
+    n = lib().ssd_bwd_kernels(batch, seqlen, nheads, headdim, ngroups, dstate, code, buf, 512)
+    if n < 0:
+        raise SsdError(SSD_ERR_INVALID_ARG, "sizes rejected")
+    names = buf.value.decode().split(",") if n else []
+    assert len(names) == n
+    return names
 
 
 def ssd_fwd_workspace_size(batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype) -> int:

@@ -679,6 +679,101 @@ ssd_status_t ssd_step(const void *x, const float *dt, const float *A, const void
     return ok();
 }
 
+static ssd_status_t make_bwd_problem(BwdProblem &p, int batch, int seqlen, int nheads, int headdim, int ngroups,
+                                     int dstate, ssd_dtype_t dtype)
+{
+    memset(&p, 0, sizeof p);
+    if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim <= 0 || ngroups <= 0 || dstate <= 0)
+        return fail(SSD_ERR_INVALID_ARG,
+                    "every dimension must be positive (batch=%d seqlen=%d nheads=%d headdim=%d ngroups=%d dstate=%d)",
+                    batch, seqlen, nheads, headdim, ngroups, dstate);
+    if (nheads % ngroups != 0)
+        return fail(SSD_ERR_INVALID_ARG, "nheads (%d) must be a multiple of ngroups (%d)", nheads, ngroups);
+    if (dtype != SSD_DTYPE_F32 && dtype != SSD_DTYPE_BF16) return fail(SSD_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (headdim > kBwdMaxHeaddim || dstate > kMaxDstate)
+        return fail(SSD_ERR_UNSUPPORTED, "the backward handles headdim <= %d and dstate <= %d (got %d, %d)",
+                    kBwdMaxHeaddim, kMaxDstate, headdim, dstate);
+    if (nheads > 65535 || batch > 65535)
+        return fail(SSD_ERR_UNSUPPORTED, "nheads and batch must each be <= 65535");
+    p.batch = batch;
+    p.seqlen = seqlen;
+    p.nheads = nheads;
+    p.headdim = headdim;
+    p.ngroups = ngroups;
+    p.dstate = dstate;
+    p.dtype = dtype;
+    return SSD_OK;
+}
+
+ssd_status_t ssd_bwd(const void *x, const float *dt, const float *A, const void *B, const void *C, const float *D,
+                     const float *init_state, const void *dy, const float *dfinal_state, float *dx, float *ddt,
+                     float *dA, float *dB, float *dC, float *dD, float *dinit_state, int batch, int seqlen,
+                     int nheads, int headdim, int ngroups, int dstate, ssd_dtype_t dtype, void *stream)
+{
+    BwdProblem p;
+    ssd_status_t st = make_bwd_problem(p, batch, seqlen, nheads, headdim, ngroups, dstate, dtype);
+    if (st != SSD_OK) return st;
+    if (!x || !dt || !A || !B || !C || !dy || !dx || !ddt || !dA || !dB || !dC)
+        return fail(SSD_ERR_INVALID_ARG, "x, dt, A, B, C, dy, dx, ddt, dA, dB and dC must be non-NULL");
+    const size_t el = dtype == SSD_DTYPE_BF16 ? 2 : 4;
+    if (!aligned(x, el) || !aligned(B, el) || !aligned(C, el) || !aligned(dy, el))
+        return fail(SSD_ERR_INVALID_ARG, "x, B, C and dy must be aligned to their element size");
+    const void *f32[] = {dt, A, D, init_state, dfinal_state, dx, ddt, dA, dB, dC, dD, dinit_state};
+    for (const void *q : f32)
+        if (q && !aligned(q, 4)) return fail(SSD_ERR_INVALID_ARG, "fp32 tensors must be 4-byte aligned");
+    p.x = x;
+    p.dt = dt;
+    p.A = A;
+    p.B = B;
+    p.C = C;
+    p.D = D;
+    p.init_state = init_state;
+    p.dy = dy;
+    p.dfinal = dfinal_state;
+    p.dx = dx;
+    p.ddt = ddt;
+    p.dA = dA;
+    p.dB = dB;
+    p.dC = dC;
+    p.dD = dD;
+    p.dinit = dinit_state;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t need = bwd_workspace_bytes(p);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(e == cudaErrorMemoryAllocation ? SSD_ERR_NO_MEMORY : SSD_ERR_CUDA,
+                    "workspace allocation of %zu bytes failed: %s", need, cudaGetErrorString(e));
+    }
+    profile_forward_begin();
+    e = launch_bwd(p, ws, s);
+    const cudaError_t ef = cudaFreeAsync(ws, s);
+    if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "backward launch failed: %s", cudaGetErrorString(e));
+    if (ef != cudaSuccess) return fail(SSD_ERR_CUDA, "workspace release failed: %s", cudaGetErrorString(ef));
+    return ok();
+}
+
+int ssd_bwd_kernels(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate, ssd_dtype_t dtype,
+                    char *names, size_t names_len)
+{
+    BwdProblem p;
+    if (make_bwd_problem(p, batch, seqlen, nheads, headdim, ngroups, dstate, dtype) != SSD_OK) return -1;
+    if (names && names_len) snprintf(names, names_len, "%s", bwd_kernel_names(p));
+    return bwd_kernel_count(p);
+}
+
+ssd_status_t ssd_bwd_workspace_size(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
+                                    ssd_dtype_t dtype, size_t *bytes)
+{
+    if (!bytes) return fail(SSD_ERR_INVALID_ARG, "bytes must be non-NULL");
+    BwdProblem p;
+    ssd_status_t st = make_bwd_problem(p, batch, seqlen, nheads, headdim, ngroups, dstate, dtype);
+    if (st != SSD_OK) return st;
+    *bytes = bwd_workspace_bytes(p);
+    return ok();
+}
+
 ssd_status_t ssd_test_set_fault(unsigned long long wait_limit_ns, long long withhold_unit)
 {
     if (withhold_unit < -1) return fail(SSD_ERR_INVALID_ARG, "withhold_unit must be -1 or a unit index");

@@ -148,17 +148,26 @@ void profile_set(void *const *events, int count)
 
 void profile_forward_begin() { t_prof_next = 0; }
 
-// External records: under stream capture they become event-record nodes of the
-// graph (timed on replay) instead of capture-internal dependencies.
+// Under stream capture an external record becomes an event-record node of the
+// graph (timed on replay) instead of a capture-internal dependency; outside a
+// capture that flag is refused, and a plain record is what is wanted.
+static void profile_record(cudaEvent_t e, cudaStream_t s)
+{
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, s);
+}
+
 void profile_kernel_begin(cudaStream_t s)
 {
-    if (2 * t_prof_next < t_prof_count) cudaEventRecordWithFlags(t_prof[2 * t_prof_next], s, cudaEventRecordExternal);
+    if (2 * t_prof_next < t_prof_count) profile_record(t_prof[2 * t_prof_next], s);
 }
 
 void profile_kernel_end(cudaStream_t s)
 {
-    if (2 * t_prof_next + 1 < t_prof_count)
-        cudaEventRecordWithFlags(t_prof[2 * t_prof_next + 1], s, cudaEventRecordExternal);
+    if (2 * t_prof_next + 1 < t_prof_count) profile_record(t_prof[2 * t_prof_next + 1], s);
     ++t_prof_next;
 }
 

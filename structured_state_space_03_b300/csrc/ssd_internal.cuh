@@ -101,6 +101,30 @@ cudaError_t launch_seq_tc(const Problem &pr, void *workspace, cudaStream_t s);
 // Sequential inter-chunk state passing, shared by the multi-kernel paths.
 cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream_t s);
 
+// Backward (ssd_bwd.cu): gradients of a scalar loss given dL/dy and dL/d(final
+// state); fp32 FMA kernels, headdim <= kBwdMaxHeaddim, dstate <= kMaxDstate.
+struct BwdProblem {
+    const void *x;
+    const float *dt;
+    const float *A;
+    const void *B;
+    const void *C;
+    const float *D;           // may be null
+    const float *init_state;  // may be null
+    const void *dy;           // [batch][seqlen][nheads][headdim], element type dtype
+    const float *dfinal;      // may be null
+    float *dx, *ddt, *dA, *dB, *dC;
+    float *dD;                // may be null
+    float *dinit;             // may be null
+    int batch, seqlen, nheads, headdim, ngroups, dstate;
+    ssd_dtype_t dtype;
+};
+constexpr int kBwdMaxHeaddim = 128;
+size_t bwd_workspace_bytes(const BwdProblem &p);
+int bwd_kernel_count(const BwdProblem &p);
+const char *bwd_kernel_names(const BwdProblem &p);
+cudaError_t launch_bwd(const BwdProblem &p, void *workspace, cudaStream_t s);
+
 // Host-side caches and the per-kernel timing hook (ssd_host.cu).
 // A 3-D [batch][rows][width] tensor map (bf16 or fp32), box box_cols x box_rows x 1,
 // 128-byte swizzle or none; identical requests reuse one encoded map.

@@ -157,3 +157,15 @@ def sample_rows(w_or_dims, count: int, seed: int = 7):
     while len(rows) < min(count, total):
         rows.add(int(torch.randint(0, total, (1,), generator=g)))
     return sorted(rows)
+
+
+def make_cotangents(batch, seqlen, nheads, headdim, dstate, dtype="bf16", seed=0, with_dfinal=True):
+    """Draw the incoming gradients of a backward: dy [b,L,H,P] ~ N(0, 1) in the
+    element type of x (rounded to bf16 for bf16 workloads) and dfinal
+    [b,H,P,N] ~ N(0, 1) fp32 (or None).  One CPU generator, draw order dy, dfinal."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 7919)
+    dy = torch.randn(batch, seqlen, nheads, headdim, generator=g, dtype=torch.float32).to(torch_dtype(dtype))
+    dfinal = (torch.randn(batch, nheads, headdim, dstate, generator=g, dtype=torch.float32)
+              if with_dfinal else None)
+    return dy, dfinal

@@ -210,3 +210,43 @@ def test_fault_hook_argument_checks(lib):
     assert lib.ssd_test_set_fault(0, -2) == ssd.SSD_ERR_INVALID_ARG
     assert lib.ssd_test_set_fault(1000, 3) == ssd.SSD_OK
     assert lib.ssd_test_set_fault(0, -1) == ssd.SSD_OK
+
+
+def _bwd(lib, headdim=64, dstate=64, ngroups=2, dtype=None, **ptrs):
+    names = ("x", "dt", "A", "B", "C", "D", "init", "dy", "dfinal", "dx", "ddt", "dA", "dB", "dC", "dD", "dinit")
+    required = {"x", "dt", "A", "B", "C", "dy", "dx", "ddt", "dA", "dB", "dC"}
+    vals = {n: (ptrs.get(n, 1 if n in required else 0)) for n in names}
+    p = lambda v: ctypes.c_void_p(v * 4096) if v else None
+    return lib.ssd_bwd(*[p(vals[n]) for n in names], 2, 300, 8, headdim, ngroups, dstate,
+                       ssd.SSD_DTYPE_BF16 if dtype is None else dtype, None)
+
+
+@pytest.mark.parametrize("missing", ["x", "dt", "A", "B", "C", "dy", "dx", "ddt", "dA", "dB", "dC"])
+def test_backward_null_required_pointer_is_invalid(lib, missing):
+    assert _bwd(lib, **{missing: 0}) == ssd.SSD_ERR_INVALID_ARG
+    assert missing in ssd.ssd_last_error_detail()
+
+
+def test_backward_size_and_type_checks(lib):
+    assert _bwd(lib, headdim=256) == ssd.SSD_ERR_UNSUPPORTED
+    assert _bwd(lib, dstate=300) == ssd.SSD_ERR_UNSUPPORTED
+    assert _bwd(lib, ngroups=3) == ssd.SSD_ERR_INVALID_ARG
+    assert _bwd(lib, dtype=5) == ssd.SSD_ERR_INVALID_ARG
+    st = lib.ssd_bwd(*[ctypes.c_void_p(4096 + 1)] + [ctypes.c_void_p(4096)] * 15, 2, 300, 8, 64, 2, 64,
+                     ssd.SSD_DTYPE_BF16, None)
+    assert st == ssd.SSD_ERR_INVALID_ARG and "aligned" in ssd.ssd_last_error_detail()
+
+
+def test_backward_kernel_list_and_workspace(lib):
+    assert ssd.ssd_bwd_kernels(2, 300, 8, 64, 2, 128, ssd.SSD_DTYPE_BF16) == [
+        "bwd_chunk_states", "bwd_state_pass", "bwd_chunk", "bwd_reduce_groups", "bwd_reduce_heads"]
+    # one head per group: dB and dC are written directly, no reduction over heads
+    assert ssd.ssd_bwd_kernels(2, 300, 8, 64, 8, 128, ssd.SSD_DTYPE_BF16) == [
+        "bwd_chunk_states", "bwd_state_pass", "bwd_chunk", "bwd_reduce_heads"]
+    nc = -(-300 // 64)
+    states = 2 * (2 * 8 * nc * 64 * 128 * 4)
+    parts = 2 * (2 * 300 * 8 * 128 * 4)
+    grouped = ssd.ssd_bwd_workspace_size(2, 300, 8, 64, 2, 128, ssd.SSD_DTYPE_BF16)
+    per_head = ssd.ssd_bwd_workspace_size(2, 300, 8, 64, 8, 128, ssd.SSD_DTYPE_BF16)
+    assert states <= per_head <= states + 4096
+    assert grouped - per_head >= parts
