@@ -14,6 +14,11 @@ With N > 1 (torchrun) every rank runs its own copy of the workload on its own
 GPU (the batch dimension shards with no exchange: weak scaling); rank 0 prints
 the line with the max-over-ranks time.  ``--impl reference`` times the fp64
 CPU oracle instead (on the host cores, bounded samples of the same workload).
+
+The headline line also carries sub-records measured after the timed region:
+the single-token decode step, the forward with the dt pre-step, packed
+variable-length sequences, the backward (ssd_bwd) on the same workload, and
+the other large workloads.
 """
 from __future__ import annotations
 
@@ -52,6 +57,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the sub-record of the other large workloads (headline run only)")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward sub-record (headline run only)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip every sub-record (decode, pre-step, packed, backward, other workloads)")
     ap.add_argument("--ref-seconds", type=float, default=0.0,
                     help="oracle seconds per step of --impl reference (0: spread ~150 s over the steps)")
     return ap.parse_args()
@@ -545,6 +553,104 @@ def workload_record(w, dev, stream, peaks, steps=20):
     return rec
 
 
+FP32_LANES_PER_SM = 128  # fp32 FMA lanes per SM (4 sub-partitions x 32)
+
+
+def fp32_fma_peak_tflops(peaks):
+    """Peak fp32 FMA throughput of the plain ALU path: SMs x lanes x 2 flops x
+    the maximum SM clock (148 x 128 x 2 x 2.032 GHz = 77.0 TFLOP/s on B300)."""
+    return 148 * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2032.0) * 1e6 / 1e12
+
+
+def bwd_flops(w, q=64):
+    """Algorithmic FLOPs of the chunked backward (64-token chunks), masked
+    (lower-triangular) products counted on their triangle: per (batch, chunk of
+    q tokens) G * q(q+1)N for C B^T, and per head 2q(q+1)P (dy x^T, M^T dy) +
+    2q(q+1)N (K^T C, K dt B) + 10qPN (B g^T, dy h, x g, the two chunk states)."""
+    total = 0
+    for c in range(math.ceil(w.seqlen / q)):
+        n = min(q, w.seqlen - c * q)
+        total += w.ngroups * n * (n + 1) * w.dstate + w.nheads * (
+            2 * n * (n + 1) * w.headdim + 2 * n * (n + 1) * w.dstate + 10 * n * w.headdim * w.dstate)
+    return total * w.batch
+
+
+def bwd_unavoidable_bytes(w):
+    """x, dy, B, C, dt read and dx, ddt, dB, dC (fp32) written once, plus the
+    states (init, dfinal in; dinit out) and A, D, dA, dD."""
+    e = 2 if w.dtype == "bf16" else 4
+    tok = w.batch * w.seqlen
+    ins = 2 * tok * w.nheads * w.headdim * e + 2 * tok * w.ngroups * w.dstate * e + tok * w.nheads * 4
+    outs = tok * w.nheads * w.headdim * 4 + tok * w.nheads * 4 + 2 * tok * w.ngroups * w.dstate * 4
+    states = 3 * w.batch * w.nheads * w.headdim * w.dstate * 4
+    return ins + outs + states + 4 * w.nheads * 4
+
+
+def backward_measurement(w, dev, stream, peaks, steps=20):
+    """The backward (ssd_bwd) on the workload: ms per step over a CUDA graph of
+    ``steps`` backward calls rotating over input sets larger than L2, each
+    kernel's device time, the step against its roofline and the dominant
+    kernel against the fp32 FMA peak it runs on."""
+    import structured_state_space_03_b300 as ssd
+    dtype = wl.torch_dtype(w.dtype)
+    names = ssd.ssd_bwd_kernels(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, dtype)
+    inp = wl.workload_inputs(w)
+    dy, dfinal = wl.make_cotangents(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.dtype, seed=w.seed)
+    per_set = bwd_unavoidable_bytes(w)
+    nsets = max(2, math.ceil(3 * L2_BYTES / per_set))
+    sets = []
+    for _ in range(nsets):
+        d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+        d["dy"], d["dfinal"] = dy.to(dev), dfinal.to(dev)
+        sets.append(d)
+
+    def step(k, st):
+        d = sets[k % nsets]
+        ssd.ssd_bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"], dy=d["dy"],
+                    dfinal_state=d["dfinal"], stream=st)
+
+    for k in range(3):
+        step(k, stream)
+    torch.cuda.synchronize()
+    ssd.ssd_check_device_status(stream)
+    g = capture(step, 0, steps)
+    g.replay()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    g.replay()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    ssd.ssd_check_device_status(stream)
+    ms = s0.elapsed_time(s1) / steps
+    pk, how = per_kernel_times(step, len(names), stream, 5)
+    dom = max(range(len(names)), key=lambda i: pk[i])
+    flops = bwd_flops(w)
+    # the in-chunk kernel's share of the FLOPs: everything but the two chunk states
+    states_flops = 4 * w.batch * w.seqlen * w.nheads * w.headdim * w.dstate
+    kflops = {"bwd_chunk": flops - states_flops, "bwd_chunk_states": states_flops}
+    alu_peak = fp32_fma_peak_tflops(peaks)
+    t_hbm = per_set / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    rec = {"workload": w.name, "ms_per_step": ms, "tokens_per_s": w.tokens / (ms * 1e-3), "steps": steps,
+           "kernels": {names[i]: {"ms_per_launch": pk[i], "share": pk[i] / (sum(pk) or 1.0)}
+                       for i in range(len(names))},
+           "kernel_timing": how,
+           "step_roofline": {"unavoidable_bytes": per_set, "algorithmic_flops": flops,
+                             "roofline_ms": max(t_hbm, t_tc) * 1e3, "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                             "frac": max(t_hbm, t_tc) * 1e3 / ms},
+           "l2": f"inputs rotate over {nsets} device copies ({nsets * per_set / 2**20:.0f} MiB > 126 MB L2)"}
+    if names[dom] in kflops:
+        ach = kflops[names[dom]] / (pk[dom] * 1e-3) / 1e12
+        rec["roofline"] = {"bound": "alu", "kernel": names[dom], "achieved": ach, "peak": alu_peak,
+                           "unit": "TFLOP/s", "frac": ach / alu_peak, "traffic": recorded_traffic(names[dom]),
+                           "algorithmic_flops_per_launch": kflops[names[dom]], "launch_ms": pk[dom],
+                           "peak_source": "148 SMs x 128 fp32 lanes x 2 flops x max SM clock"}
+    del sets, g
+    torch.cuda.empty_cache()
+    return rec
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
@@ -705,11 +811,13 @@ def main():
         "clocks": sampler.summary(mark0, mark1),
     }
     del graphs
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not args.no_extras:
         line["decode_step"] = decode_step_measurement(dev, peaks, stream)
         if w is wl.HEADLINE:
             line["pre_step"] = pre_step_measurement(sets, w, stream)
             line["varlen_step"] = varlen_step_measurement(sets, w, stream, peaks)
+            if not args.no_backward:
+                line["backward"] = backward_measurement(w, dev, stream, peaks)
             if not args.no_workloads:
                 del sets
                 torch.cuda.empty_cache()
