@@ -202,9 +202,11 @@ SSD_API ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float
  * from the stream-ordered allocator.  Empty sequences are allowed: their
  * final state is their initial state (or zero).  Chunks never straddle two
  * sequences: each sequence is cut into chunks from its own first token, the
- * last one partial.  Runs on the fused kernels: bf16, headdim 64 or 128,
- * dstate 64 or 128, chunk <= 128, nheads / ngroups a multiple of 128 / headdim;
- * SSD_ERR_UNSUPPORTED otherwise, or for more than INT32_MAX packed tokens.
+ * last one partial.  Every kernel family takes packed sequences: the fused
+ * kernels where ssd_fwd would run them (their units walk a chunk table), the
+ * multi-kernel tcgen05 and fp32 paths otherwise (one CTA per chunk-table entry,
+ * the state passing restarted at each sequence).  SSD_ERR_UNSUPPORTED for the
+ * sizes ssd_fwd rejects, or for more than INT32_MAX packed tokens or chunks.
  * SSD_ERR_INVALID_ARG for a NULL cu_seqlens, nseq <= 0, offsets that do not
  * start at 0 or decrease, and the checks of ssd_fwd.
  */

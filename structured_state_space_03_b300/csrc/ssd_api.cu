@@ -58,17 +58,24 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 static ssd_path_t choose_path(const Problem &pr);
 
+// chunk states of the multi-kernel paths: [batch][nheads][nchunks], or
+// [1][nheads][total_chunks] for packed sequences
+static size_t state_units(const Problem &pr)
+{
+    return pr.chunks ? (size_t)pr.nheads * pr.total_chunks : (size_t)pr.batch * pr.nheads * pr.nchunks;
+}
+
 size_t workspace_bytes(const Problem &pr)
 {
     if (choose_path(pr) == SSD_PATH_TCGEN05_FUSED) return fused_workspace_bytes(pr);
-    const size_t units = (size_t)pr.batch * pr.nheads * pr.nchunks;
+    const size_t units = state_units(pr);
     return align_up(units * pr.headdim * pr.dstate * sizeof(float), 256) +
            align_up(units * sizeof(float), 256);
 }
 
 Workspace carve_workspace(const Problem &pr, void *base)
 {
-    const size_t units = (size_t)pr.batch * pr.nheads * pr.nchunks;
+    const size_t units = state_units(pr);
     Workspace ws;
     ws.states = static_cast<float *>(base);
     ws.decay = reinterpret_cast<float *>(static_cast<char *>(base) +
@@ -308,10 +315,6 @@ ssd_status_t ssd_fwd_varlen(const void *x, const float *dt, const float *A, cons
     ssd_status_t st = make_problem(pr, x, dt, A, B, C, D, init_state, y, final_state, nseq, total, nheads, headdim,
                                    ngroups, dstate, chunk, dtype);
     if (st != SSD_OK) return st;
-    if (choose_path(pr) != SSD_PATH_TCGEN05_FUSED)
-        return fail(SSD_ERR_UNSUPPORTED,
-                    "packed sequences run on the fused kernels: bf16, headdim 64 or 128, dstate 64 or 128, "
-                    "chunk <= 128, nheads / ngroups a multiple of 128 / headdim");
     // chunk table in chunk-major order (a counting sort over the chunk index)
     std::vector<int> nchunk(nseq);
     int max_nc = 0;
@@ -342,11 +345,19 @@ ssd_status_t ssd_fwd_varlen(const void *x, const float *dt, const float *A, cons
         }
         gbase += nchunk[q];
     }
+    if (total_chunks > (size_t)INT32_MAX) return fail(SSD_ERR_UNSUPPORTED, "too many chunks for the packed layout");
     pr.total_chunks = (int)total_chunks;
     pr.chunks = reinterpret_cast<const ChunkDesc *>(1);  // marks the packed layout for the size query below
-    if (!fused_supported(pr)) return fail(SSD_ERR_UNSUPPORTED, "too many chunks for the packed layout");
+    // the multi-kernel paths also need each sequence's first chunk (sequence-major numbering)
+    const bool fused = choose_path(pr) == SSD_PATH_TCGEN05_FUSED;
+    std::vector<int> seq_first(fused ? 0 : nseq + 1);
+    if (!fused) {
+        seq_first[0] = 0;
+        for (int q = 0; q < nseq; ++q) seq_first[q + 1] = seq_first[q] + nchunk[q];
+    }
     const size_t main_bytes = align_up(workspace_bytes(pr), 256);
-    const size_t need = main_bytes + total_chunks * sizeof(ChunkDesc);
+    const size_t table_bytes = align_up(total_chunks * sizeof(ChunkDesc), 256);
+    const size_t need = main_bytes + table_bytes + seq_first.size() * sizeof(int);
     void *ws = nullptr;
     cudaError_t e = cudaMallocAsync(&ws, need, s);
     if (e != cudaSuccess) {
@@ -355,7 +366,10 @@ ssd_status_t ssd_fwd_varlen(const void *x, const float *dt, const float *A, cons
                     "workspace allocation of %zu bytes failed: %s", need, cudaGetErrorString(e));
     }
     ChunkDesc *dtab = reinterpret_cast<ChunkDesc *>(static_cast<char *>(ws) + main_bytes);
+    int *dfirst = reinterpret_cast<int *>(static_cast<char *>(ws) + main_bytes + table_bytes);
     e = cudaMemcpyAsync(dtab, table.data(), total_chunks * sizeof(ChunkDesc), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && !fused)
+        e = cudaMemcpyAsync(dfirst, seq_first.data(), seq_first.size() * sizeof(int), cudaMemcpyHostToDevice, s);
     // empty sequences get no unit: their final state is their initial state
     for (int q = 0; q < nseq && e == cudaSuccess; ++q) {
         if (nchunk[q] != 0 || !final_state || final_state == init_state) continue;
@@ -365,6 +379,7 @@ ssd_status_t ssd_fwd_varlen(const void *x, const float *dt, const float *A, cons
     }
     if (e == cudaSuccess) {
         pr.chunks = dtab;
+        pr.seq_first = fused ? nullptr : dfirst;
         st = run(pr, ws, s);
     } else {
         st = fail(SSD_ERR_CUDA, "chunk table upload failed: %s", cudaGetErrorString(e));

@@ -63,6 +63,10 @@ struct Problem {
     // chunk 0, then every chunk 1, ...).
     const ChunkDesc *chunks;
     int total_chunks;
+    // Packed layout on the multi-kernel paths: seq_first[q] is the index, in the
+    // sequence-major numbering of all chunks (ChunkDesc::gchunk), of sequence q's
+    // first chunk; seq_first[batch] = total_chunks (device memory).
+    const int *seq_first;
     unsigned int *err_word;   // device address of the error word
     // Failure-detection test settings (ssd_test_set_fault): the limit of every
     // bounded wait of the fused kernels, and the unit (index in the fused
@@ -76,6 +80,51 @@ struct Workspace {
     float *states;  // [batch][nheads][nchunks][headdim][dstate]: S_c, then h_c in place
     float *decay;   // [batch][nheads][nchunks]: exp(cs_last) of each chunk
 };
+// (The packed layout uses [1][nheads][total_chunks] in the sequence-major chunk
+// numbering instead of [batch][nheads][nchunks].)
+
+// The chunk a CTA of the multi-kernel paths works on.  Batch layout: chunk cx
+// of batch element bz.  Packed layout: entry cx of the chunk table (bz is 0).
+struct ChunkRef {
+    int seq;  // batch element or packed sequence
+    int tb;   // batch coordinate of the token tensors (0 when packed)
+    int t0;   // first token of the chunk within its batch row
+    int len;  // tokens in the chunk
+    int sb;   // batch coordinate of the chunk's state and decay (0 when packed)
+    int sc;   // chunk coordinate of the chunk's state and decay
+    int nct;  // chunk extent of the state layout
+};
+
+__device__ __forceinline__ ChunkRef chunk_ref(const Problem &pr, int cx, int bz)
+{
+    ChunkRef r;
+    if (pr.chunks) {
+        const ChunkDesc d = pr.chunks[cx];
+        r.seq = d.b;
+        r.tb = 0;
+        r.t0 = d.tok0;
+        r.len = d.len;
+        r.sb = 0;
+        r.sc = d.gchunk;
+        r.nct = pr.total_chunks;
+    } else {
+        r.seq = bz;
+        r.tb = bz;
+        r.t0 = cx * pr.chunk;
+        r.len = min(pr.chunk, pr.seqlen - r.t0);
+        r.sb = bz;
+        r.sc = cx;
+        r.nct = pr.nchunks;
+    }
+    return r;
+}
+
+// Index of head h's state / decay of the chunk in the workspace (in states of
+// headdim x dstate, or in floats of the decay array).
+__device__ __forceinline__ size_t state_slot(const Problem &pr, const ChunkRef &r, int h)
+{
+    return ((size_t)r.sb * pr.nheads + h) * r.nct + r.sc;
+}
 
 size_t workspace_bytes(const Problem &pr);
 Workspace carve_workspace(const Problem &pr, void *base);

@@ -15,16 +15,16 @@ constexpr int kStateOuts = 8;   // chunk-state outputs per thread per pass
 
 // Segment sum of one chunk: cs[t] (in-chunk inclusive prefix of dt*A) and
 // dt[t] into shared memory; returns cs of the chunk's last token.
-__device__ __forceinline__ float chunk_segsum(const Problem &pr, int b, int h, int t0, int len,
+__device__ __forceinline__ float chunk_segsum(const Problem &pr, int tb, int h, int t0, int len,
                                               float *cs_s, float *dt_s, float *warp_tot)
 {
     const int tid = threadIdx.x;
     float dtv = 0.f;
-    if (tid < len) dtv = __ldg(pr.dt + ((size_t)b * pr.seqlen + t0 + tid) * pr.nheads + h);
+    if (tid < len) dtv = __ldg(pr.dt + ((size_t)tb * pr.seqlen + t0 + tid) * pr.nheads + h);
     const float cs = block_inclusive_scan_256(dtv * __ldg(pr.A + h), warp_tot);
     if (tid < kMaxChunk) {
         cs_s[tid] = cs;
-        dt_s[tid] = pr.dtin ? (tid < len ? __ldg(pr.dtin + ((size_t)b * pr.seqlen + t0 + tid) * pr.nheads + h) : 0.f)
+        dt_s[tid] = pr.dtin ? (tid < len ? __ldg(pr.dtin + ((size_t)tb * pr.seqlen + t0 + tid) * pr.nheads + h) : 0.f)
                             : dtv;  // input scale
     }
     __syncthreads();
@@ -37,11 +37,11 @@ __global__ void __launch_bounds__(kThreads) chunk_state_simt(Problem pr, Workspa
 {
     extern __shared__ float smem[];
     __shared__ float warp_tot[8];
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int h = blockIdx.y;
+    const ChunkRef ref = chunk_ref(pr, blockIdx.x, blockIdx.z);
     const int L = pr.seqlen, H = pr.nheads, P = pr.headdim, N = pr.dstate, G = pr.ngroups;
     const int g = h / (H / G);
-    const int t0 = c * pr.chunk;
-    const int len = min(pr.chunk, L - t0);
+    const int b = ref.tb, t0 = ref.t0, len = ref.len;
     float *cs_s = smem;             // [256]
     float *dt_s = cs_s + kMaxChunk; // [256]
     float *w_s = dt_s + kMaxChunk;  // [256]
@@ -53,12 +53,12 @@ __global__ void __launch_bounds__(kThreads) chunk_state_simt(Problem pr, Workspa
 
     const float cs_last = chunk_segsum(pr, b, h, t0, len, cs_s, dt_s, warp_tot);
     if (tid < len) w_s[tid] = expf(cs_last - cs_s[tid]) * dt_s[tid];
-    const size_t bh = (size_t)b * H + h;
-    if (tid == 0) ws.decay[bh * pr.nchunks + c] = expf(cs_last);
+    const size_t slot = state_slot(pr, ref, h);
+    if (tid == 0) ws.decay[slot] = expf(cs_last);
     __syncthreads();
 
     const int PN = P * N;
-    float *out = ws.states + (bh * pr.nchunks + c) * (size_t)PN;
+    float *out = ws.states + slot * (size_t)PN;
     for (int o0 = 0; o0 < PN; o0 += kThreads * kStateOuts) {
         float acc[kStateOuts];
 #pragma unroll
@@ -100,11 +100,11 @@ __global__ void __launch_bounds__(kThreads) chunk_out_simt(Problem pr, Workspace
 {
     extern __shared__ float smem[];
     __shared__ float warp_tot[8];
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int h = blockIdx.y;
+    const ChunkRef ref = chunk_ref(pr, blockIdx.x, blockIdx.z);
     const int L = pr.seqlen, H = pr.nheads, P = pr.headdim, N = pr.dstate, G = pr.ngroups;
     const int g = h / (H / G);
-    const int t0 = c * pr.chunk;
-    const int len = min(pr.chunk, L - t0);
+    const int b = ref.tb, t0 = ref.t0, len = ref.len;
     float *cs_s = smem;                 // [256]
     float *dt_s = cs_s + kMaxChunk;     // [256]
     float *c_s = dt_s + kMaxChunk;      // [kTile][N]   C rows of the current i tile
@@ -118,8 +118,7 @@ __global__ void __launch_bounds__(kThreads) chunk_out_simt(Problem pr, Workspace
     const T *Cm = static_cast<const T *>(pr.C);
     T *y = static_cast<T *>(pr.y);
     const int tid = threadIdx.x;
-    const size_t bh = (size_t)b * H + h;
-    const float *hc = ws.states + (bh * pr.nchunks + c) * (size_t)P * N;
+    const float *hc = ws.states + state_slot(pr, ref, h) * (size_t)P * N;
     const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
 
     chunk_segsum(pr, b, h, t0, len, cs_s, dt_s, warp_tot);
@@ -226,12 +225,15 @@ __global__ void __launch_bounds__(kThreads) state_pass(Problem pr, Workspace ws)
     if (e >= PN) return;
     const size_t bh = (size_t)b * pr.nheads + h;
     float st = pr.init_state ? pr.init_state[bh * PN + e] : 0.f;
-    float *s = ws.states + bh * pr.nchunks * (size_t)PN + e;
-    const float *dec = ws.decay + bh * pr.nchunks;
+    // batch layout: the nchunks chunks of (b, h); packed: sequence b's chunks, a
+    // contiguous range of the sequence-major numbering in the layout [1][H][total]
+    const size_t first = pr.chunks ? (size_t)h * pr.total_chunks + pr.seq_first[b] : bh * pr.nchunks;
+    float *s = ws.states + first * (size_t)PN + e;
+    const float *dec = ws.decay + first;
     // kAhead chunk states are loaded before any is overwritten, so each thread
     // keeps kAhead independent loads in flight instead of one per chunk
     constexpr int kAhead = 16;
-    const int nc = pr.nchunks;
+    const int nc = pr.chunks ? pr.seq_first[b + 1] - pr.seq_first[b] : pr.nchunks;
     for (int c0 = 0; c0 < nc; c0 += kAhead) {
         float sc[kAhead], dk[kAhead];
 #pragma unroll
@@ -264,7 +266,7 @@ cudaError_t set_smem(K kernel, size_t bytes)
 cudaError_t launch_chunk_state_simt(const Problem &pr, const Workspace &ws, cudaStream_t s)
 {
     const size_t smem = sizeof(float) * (3 * kMaxChunk + kTile * (pr.headdim + pr.dstate));
-    const dim3 grid(pr.nchunks, pr.nheads, pr.batch);
+    const dim3 grid(pr.chunks ? pr.total_chunks : pr.nchunks, pr.nheads, pr.chunks ? 1 : pr.batch);
     cudaError_t e;
     if (pr.dtype == SSD_DTYPE_F32) {
         if ((e = set_smem(chunk_state_simt<float>, smem)) != cudaSuccess) return e;
@@ -284,7 +286,7 @@ cudaError_t launch_chunk_out_simt(const Problem &pr, const Workspace &ws, cudaSt
 {
     const size_t smem = sizeof(float) * (2 * kMaxChunk + kTile * (2 * pr.dstate + 1 + pr.headdim) +
                                          kTile * (kTile + 1) + pr.headdim * (kTile + 1));
-    const dim3 grid(pr.nchunks, pr.nheads, pr.batch);
+    const dim3 grid(pr.chunks ? pr.total_chunks : pr.nchunks, pr.nheads, pr.chunks ? 1 : pr.batch);
     cudaError_t e;
     if (pr.dtype == SSD_DTYPE_F32) {
         if ((e = set_smem(chunk_out_simt<float>, smem)) != cudaSuccess) return e;

@@ -133,10 +133,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float cs[2 * 256], dtv[2 * 256];
     __shared__ int s_fail;
 
-    const int c = blockIdx.x, hb = blockIdx.y, b = blockIdx.z;
+    const int hb = blockIdx.y;
+    const ChunkRef ref = chunk_ref(pr, blockIdx.x, blockIdx.z);
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads;
     const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
-    const int t0 = c * pr.chunk, len = min(pr.chunk, pr.seqlen - t0);
+    const int b = ref.tb, t0 = ref.t0, len = ref.len;  // b: batch row of the token tensors
     const int nbox = pr.chunk <= kBoxRows ? 1 : 2;  // 128-token slabs along K
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = e & 255;
         wts[e] = j < len ? expf((e < 256 ? cl0 : cl1) - cs[e]) * dtv[e] : 0.f;
     }
-    if (tid < HB) ws.decay[((size_t)b * H + h0 + tid) * pr.nchunks + c] = expf(tid == 0 ? cl0 : cl1);
+    if (tid < HB) ws.decay[state_slot(pr, ref, h0 + tid)] = expf(tid == 0 ? cl0 : cl1);
     __syncthreads();
 
     bool ok = true;
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
         const int m = warp * 32 + lane;
         const int hh = m / P, p = m % P;
-        float *out = ws.states + (((size_t)b * H + h0 + hh) * pr.nchunks + c) * (size_t)P * NS + (size_t)p * NS;
+        float *out = ws.states + state_slot(pr, ref, h0 + hh) * (size_t)P * NS + (size_t)p * NS;
 #pragma unroll 1
         for (int c0 = 0; c0 < NS; c0 += 32) {
             float v[32];
@@ -275,10 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int s_fail;
 
     const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
-    const int c = blockIdx.x / ntile, it = blockIdx.x % ntile, hb = blockIdx.y, b = blockIdx.z;
+    const int it = blockIdx.x % ntile, hb = blockIdx.y;
+    const ChunkRef ref = chunk_ref(pr, blockIdx.x / ntile, blockIdx.z);
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
     const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
-    const int t0 = c * pr.chunk, len = min(pr.chunk, L - t0);
+    const int b = ref.tb, t0 = ref.t0, len = ref.len;  // b: batch row of the token tensors
     const int i0 = it * kBoxRows;
     if (i0 >= len) return;  // tile beyond the end of a partial last chunk (block-uniform)
     const int jn = i0 + kBoxRows;                 // columns j in [0, jn)
@@ -326,8 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- phase 1: G = C_i B^T and Yoff = C_i h_c^T, over 64-wide slabs of the state dimension
     const int m = tid;  // h-slab row (h, p) written by this thread
-    const float *hsrc = ws.states + (((size_t)b * H + h0 + m / P) * pr.nchunks + c) * (size_t)P * NS +
-                        (size_t)(m % P) * NS;
+    const float *hsrc = ws.states + state_slot(pr, ref, h0 + m / P) * (size_t)P * NS + (size_t)(m % P) * NS;
     bool ok = true;
     for (int s = 0; s < NS / 64 && ok; ++s) {
         if (tid == 0) {
@@ -533,23 +534,26 @@ cudaError_t launch_tc(const Problem &pr, const Workspace &ws, cudaStream_t s, in
     CUtensorMap xmap, bmap, cmap;
     cudaError_t e;
     const int HB = 128 / pr.headdim;
+    // packed sequences: one batch row of seqlen tokens, one CTA (row) per chunk-table entry
+    const int mb = pr.chunks ? 1 : pr.batch;
+    const int ncx = pr.chunks ? pr.total_chunks : pr.nchunks;
     if (phase == 0) {
-        if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, pr.batch)) != cudaSuccess) return e;
-        if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+        if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
+        if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
         const size_t smem = state_smem(pr);
         if ((e = ensure_smem_limit(reinterpret_cast<const void *>(chunk_state_tc<NS>), smem)) != cudaSuccess) return e;
-        const dim3 grid(pr.nchunks, pr.nheads / HB, pr.batch);
+        const dim3 grid(ncx, pr.nheads / HB, mb);
         profile_kernel_begin(s);
         chunk_state_tc<NS><<<grid, kThreads, smem, s>>>(xmap, bmap, pr, ws);
         profile_kernel_end(s);
     } else {
-        if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, pr.batch)) != cudaSuccess) return e;
-        if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
-        if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, pr.batch)) != cudaSuccess) return e;
+        if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
+        if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
+        if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
         const size_t smem = out_smem(pr);
         if ((e = ensure_smem_limit(reinterpret_cast<const void *>(chunk_out_tc<NS>), smem)) != cudaSuccess) return e;
         const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
-        const dim3 grid(pr.nchunks * ntile, pr.nheads / HB, pr.batch);
+        const dim3 grid(ncx * ntile, pr.nheads / HB, mb);
         profile_kernel_begin(s);
         chunk_out_tc<NS><<<grid, kThreads, smem, s>>>(xmap, bmap, cmap, pr, ws);
         profile_kernel_end(s);

@@ -199,11 +199,11 @@ def test_varlen_offsets_are_checked_before_any_launch(lib):
     assert "decreases" in ssd.ssd_last_error_detail()
 
 
-def test_varlen_runs_only_where_the_fused_kernels_do(lib):
-    assert _varlen(lib, [0, 5, 9], dstate=256) == ssd.SSD_ERR_UNSUPPORTED
-    assert _varlen(lib, [0, 5, 9], dtype=ssd.SSD_DTYPE_F32) == ssd.SSD_ERR_UNSUPPORTED
-    assert _varlen(lib, [0, 5, 9], headdim=32) == ssd.SSD_ERR_UNSUPPORTED
-    assert "fused kernels" in ssd.ssd_last_error_detail()
+def test_varlen_rejects_what_the_forward_rejects(lib):
+    # every kernel family takes packed sequences; sizes outside the build are refused up front
+    assert _varlen(lib, [0, 5, 9], dstate=300) == ssd.SSD_ERR_UNSUPPORTED
+    assert _varlen(lib, [0, 5, 9], headdim=512) == ssd.SSD_ERR_UNSUPPORTED
+    assert _varlen(lib, [0, 5, 9], dtype=9) == ssd.SSD_ERR_INVALID_ARG
 
 
 def test_fault_hook_argument_checks(lib):

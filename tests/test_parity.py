@@ -261,6 +261,34 @@ def test_caller_workspace_matches(dtype):
     assert torch.equal(y, yw) and torch.equal(f, fw)
 
 
+def test_raw_c_abi_call_with_status_checks():
+    # ssd_fwd through plain ctypes pointers (no binding wrapper): the status of every
+    # call is checked on the host, then the result against the oracle
+    import ctypes
+    lib = ctypes.CDLL(ssd.LIB_PATH)
+    b, L, H, P, N, G, Q = 2, 300, 4, 64, 64, 2, 128
+    inp = make_inputs(b, L, H, P, N, G, "bf16", seed=18, with_init=True)
+    c = to_cuda(inp)
+    y = torch.empty_like(c["x"])
+    fin = torch.empty(b, H, P, N, dtype=torch.float32, device="cuda")
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())
+    lib.ssd_fwd.restype = ctypes.c_int
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    args = [vp(c["x"]), vp(c["dt"]), vp(c["A"]), vp(c["B"]), vp(c["C"]), vp(c["D"]), vp(c["init_state"]), vp(y),
+            vp(fin)]
+    st = lib.ssd_fwd(*args, b, L, H, P, G, N, Q, ssd.SSD_DTYPE_BF16, stream)
+    assert st == ssd.SSD_OK, ssd.ssd_last_error_detail()
+    lib.ssd_check_device_status.restype = ctypes.c_int
+    assert lib.ssd_check_device_status(stream) == ssd.SSD_OK
+    # a rejected call enqueues nothing and leaves the outputs alone
+    y2 = y.clone()
+    assert lib.ssd_fwd(*args, b, L, H, P, 3, N, Q, ssd.SSD_DTYPE_BF16, stream) == ssd.SSD_ERR_INVALID_ARG
+    assert lib.ssd_check_device_status(stream) == ssd.SSD_OK and torch.equal(y, y2)
+    yr, fr = oracle.recurrence(**inp)
+    assert_close(y.float().cpu().numpy(), yr, TOL[torch.bfloat16], "y", STORAGE_U[torch.bfloat16])
+    assert_close(fin.cpu().numpy(), fr, TOL[torch.bfloat16], "final state")
+
+
 def test_runs_on_a_side_stream():
     inp = make_inputs(1, 400, 4, 64, 64, 1, "bf16", seed=16, with_init=True)
     c = to_cuda(inp)

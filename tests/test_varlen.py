@@ -65,6 +65,42 @@ def test_packed_sequences_match_oracle(case, with_init):
     _check(d, Q)
 
 
+# the multi-kernel paths: (lengths, H, P, N, G, chunk, dtype, path)
+MULTI = [
+    ([700, 1, 256, 0, 255, 257, 64, 3], 4, 64, 256, 1, 128, "bf16", "tcgen05"),   # dstate 256
+    ([600, 0, 1, 256, 255, 300], 4, 64, 128, 2, 256, "bf16", "tcgen05"),          # chunk 256: two tiles per chunk
+    ([300, 77, 0, 128, 1, 200], 4, 128, 64, 2, 256, "bf16", "tcgen05"),           # headdim 128, chunk 256
+    ([333, 17, 0, 64, 65, 1, 190], 6, 32, 48, 3, 100, "f32", "simt"),
+    ([250, 3, 128, 0, 77], 4, 32, 64, 2, 64, "bf16", "simt"),                     # headdim 32: fp32 FMA path
+]
+
+
+@pytest.mark.parametrize("case", MULTI, ids=[f"{c[7]}_n{len(c[0])}P{c[2]}N{c[3]}Q{c[5]}{c[6]}" for c in MULTI])
+@pytest.mark.parametrize("with_init", [False, True])
+def test_packed_sequences_on_the_multi_kernel_paths(case, with_init):
+    lengths, H, P, N, G, Q, dt, path = case
+    el = torch.float32 if dt == "f32" else torch.bfloat16
+    assert ssd.ssd_fwd_path(1, sum(lengths), H, P, G, N, Q, el) == path
+    d = make_varlen_inputs(lengths, H, P, N, G, dt, seed=sum(lengths) + Q + 1, with_init=with_init)
+    _check(d, Q)
+
+
+def test_packed_multi_kernel_in_place_state_carry():
+    # init_state == final_state on the three-kernel path: each sequence reads its own state before overwriting it
+    lengths = [300, 0, 129, 5]
+    d = make_varlen_inputs(lengths, 4, 64, 256, 1, "bf16", seed=41, with_init=True)
+    yr, fr = oracle.recurrence_varlen(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["init_state"],
+                                      d["cu_seqlens"])
+    c = _cuda_inputs(d)
+    st = c["init_state"].clone()
+    y, f = ssd.ssd_fwd_varlen(c["x"], c["dt"], c["A"], c["B"], c["C"], c["D"], st, cu_seqlens=d["cu_seqlens"],
+                              chunk=128, final_state=st)
+    ssd.ssd_check_device_status()
+    assert f.data_ptr() == st.data_ptr()
+    assert_close(y.float().cpu().numpy(), yr, TOL[torch.bfloat16], "y (packed, in place)", STORAGE_U[torch.bfloat16])
+    assert_close(st.cpu().numpy(), fr, TOL[torch.bfloat16], "final_state (packed, in place)")
+
+
 def test_many_short_sequences():
     g = torch.Generator().manual_seed(11)
     lengths = [int(v) for v in torch.randint(0, 41, (300,), generator=g)]
@@ -128,12 +164,13 @@ def test_state_carried_in_place_and_empty_sequences():
     assert torch.count_nonzero(f3) == 0
 
 
-def test_unsupported_sizes_are_rejected():
-    d = _cuda_inputs(make_varlen_inputs([10, 20], 4, 64, 256, 1, "bf16", seed=41))
+def test_sizes_outside_the_build_are_rejected():
+    # every kernel family takes packed sequences; what ssd_fwd refuses, the packed entry refuses too
+    d = _cuda_inputs(make_varlen_inputs([10, 20], 4, 64, 64, 1, "bf16", seed=41))
     with pytest.raises(ssd.SsdError) as err:
-        ssd.ssd_fwd_varlen(d["x"], d["dt"], d["A"], d["B"], d["C"], cu_seqlens=[0, 10, 30], chunk=128)
+        ssd.ssd_fwd_varlen(d["x"], d["dt"], d["A"], d["B"], d["C"], cu_seqlens=[0, 10, 30], chunk=512)
     assert err.value.status == ssd.SSD_ERR_UNSUPPORTED
-    d = _cuda_inputs(make_varlen_inputs([10, 20], 4, 64, 64, 1, "f32", seed=42))
+    d = _cuda_inputs(make_varlen_inputs([10, 20], 4, 64, 300, 1, "bf16", seed=42))
     with pytest.raises(ssd.SsdError) as err:
         ssd.ssd_fwd_varlen(d["x"], d["dt"], d["A"], d["B"], d["C"], cu_seqlens=[0, 10, 30], chunk=64)
     assert err.value.status == ssd.SSD_ERR_UNSUPPORTED
