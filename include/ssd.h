@@ -292,8 +292,8 @@ SSD_API ssd_status_t ssd_step(const void *x, const float *dt, const float *A, co
  * The pages ask the backward to recompute the intermediate states rather than
  * store them ("Mamba 模型" §3.4, recomputation); this call keeps nothing from
  * the forward: it recomputes the per-chunk states from the inputs with the
- * same block decomposition ("Mamba 模型" §4.1; its own chunk length, 64
- * tokens) and runs the adjoint state recurrence backwards over the chunks.
+ * same block decomposition ("Mamba 模型" §4.1; its own chunk length, 64 or
+ * 128 tokens) and runs the adjoint state recurrence backwards over the chunks.
  *
  *   x, dt, A, B, C, D, init_state   the forward's inputs, as in ssd_fwd (D and
  *                                   init_state may be NULL, meaning 0)
@@ -306,9 +306,12 @@ SSD_API ssd_status_t ssd_step(const void *x, const float *dt, const float *A, co
  *   dD           OUT [nheads] fp32, NULL skips it (written also when D is NULL)
  *   dinit_state  OUT [batch][nheads][headdim][dstate]  fp32, NULL skips it
  *
- * Every gradient is fp32 whatever dtype is: all arithmetic is fp32 FMA, and
- * the sums over heads, chunks and batch run in a fixed order, so two calls on
- * the same inputs give identical bits.  A_h <= 0 is assumed (every exponent is
+ * Every gradient is fp32 whatever dtype is.  For bf16 inputs with headdim 64
+ * and dstate 64 (x, dy, B, C 16-byte aligned) the in-chunk products run on
+ * tcgen05 tensor cores over 128-token chunks, every fp32 operand split into two
+ * bf16 terms so that the products keep fp32-level accuracy; every other size
+ * runs on fp32 FMA over 64-token chunks.  The sums over heads, chunks and batch
+ * run in a fixed order, so two calls on the same inputs give identical bits.  A_h <= 0 is assumed (every exponent is
  * then <= 0).  Device pointers, alignment, ownership and asynchrony as for
  * ssd_fwd; outputs must not overlap inputs or each other.  A device workspace
  * of ssd_bwd_workspace_size() bytes is taken from the stream-ordered allocator.

@@ -752,6 +752,8 @@ ssd_status_t ssd_bwd(const void *x, const float *dt, const float *A, const void 
     p.dC = dC;
     p.dD = dD;
     p.dinit = dinit_state;
+    p.err_word = device_error_word();
+    if (!p.err_word) return fail(SSD_ERR_CUDA, "cannot resolve the device error word");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t need = bwd_workspace_bytes(p);
     void *ws = nullptr;

@@ -40,6 +40,8 @@
 #include <algorithm>
 
 #include "ssd_internal.cuh"
+#include "ssd_ptx.cuh"
+#include "ssd_tile.cuh"
 
 namespace ssd {
 namespace {
@@ -68,9 +70,11 @@ struct BwdArgs {
     float *decay;             // [b][H][nc]
     float *dBp, *dCp;         // [b][L][H][N] per-head parts (null when one head per group)
     float *dAp, *dDp;         // [b][nc][H] per-chunk parts
+    unsigned int *err_word;   // device error word
 };
 
-// In-chunk prefix sums of dt*A (cs) and dt (cum) for the kBQ tokens from t0.
+// In-chunk prefix sums of dt*A (cs) and dt (cum) for the Q tokens from t0.
+template <int Q>
 __device__ __forceinline__ void chunk_scalars(const BwdArgs &a, int b, int h, int t0, int len, float *cs_s,
                                               float *dt_s, float *cum_s, float *warp_tot)
 {
@@ -79,7 +83,7 @@ __device__ __forceinline__ void chunk_scalars(const BwdArgs &a, int b, int h, in
     if (tid < len) dtv = __ldg(a.dt + ((size_t)b * a.seqlen + t0 + tid) * a.nheads + h);
     const float cs = block_inclusive_scan_256(dtv * __ldg(a.A + h), warp_tot);
     const float cum = block_inclusive_scan_256(dtv, warp_tot);
-    if (tid < kBQ) {
+    if (tid < Q) {
         cs_s[tid] = cs;
         dt_s[tid] = dtv;
         cum_s[tid] = cum;
@@ -91,82 +95,89 @@ __device__ __forceinline__ void chunk_scalars(const BwdArgs &a, int b, int h, in
 // 1. S_c[p][n] = sum_j e^{cs_end - cs_j} dt_j x_j[p] B_j[n] and
 //    G_c[p][n] = sum_i e^{cs_i} dy_i[p] C_i[n], kNT state columns per pass.
 //    Thread (ty, tx) owns rows p = ty + 16 a and columns n = tx + 16 q.
-template <typename T, int MP>
+template <typename T, int MP, int Q>
 __global__ void __launch_bounds__(kThreads) bwd_chunk_states(BwdArgs a)
 {
     extern __shared__ float sm[];
     __shared__ float warp_tot[8];
-    __shared__ float cs_s[kBQ], dt_s[kBQ], cum_s[kBQ];
+    __shared__ float cs_s[Q], dt_s[Q], cum_s[Q];
     constexpr int PP = MP * 16;
+    constexpr int KS = 64;        // tokens staged in shared memory at a time
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int L = a.seqlen, H = a.nheads, P = a.headdim, N = a.dstate, G = a.ngroups;
     const int g = h / (H / G);
-    const int t0 = c * kBQ, len = min(kBQ, L - t0);
+    const int t0 = c * Q, len = min(Q, L - t0);
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    float *xs = sm;               // [kBQ][PP]  x_j e^{cs_end - cs_j} dt_j
-    float *ys = xs + kBQ * PP;    // [kBQ][PP]  dy_i e^{cs_i}
-    float *bs = ys + kBQ * PP;    // [kBQ][kNT]
-    float *cm = bs + kBQ * kNT;   // [kBQ][kNT]
+    float *xs = sm;               // [KS][PP]  x_j e^{cs_end - cs_j} dt_j
+    float *ys = xs + KS * PP;     // [KS][PP]  dy_i e^{cs_i}
+    float *bs = ys + KS * PP;     // [KS][kNT]
+    float *cm = bs + KS * kNT;    // [KS][kNT]
     const T *x = static_cast<const T *>(a.x);
     const T *dy = static_cast<const T *>(a.dy);
     const T *Bm = static_cast<const T *>(a.B);
     const T *Cm = static_cast<const T *>(a.C);
 
-    chunk_scalars(a, b, h, t0, len, cs_s, dt_s, cum_s, warp_tot);
+    chunk_scalars<Q>(a, b, h, t0, len, cs_s, dt_s, cum_s, warp_tot);
     const float cs_end = cs_s[len - 1];
     const size_t bh = (size_t)b * H + h;
     if (tid == 0) a.decay[bh * a.nchunks + c] = expf(cs_end);
-    for (int e = tid; e < kBQ * PP; e += kThreads) {
-        const int t = e / PP, p = e - t * PP;
-        float xv = 0.f, yv = 0.f;
-        if (t < len && p < P) {
-            const size_t i = (((size_t)b * L + t0 + t) * H + h) * P + p;
-            xv = load_el(x, i) * (expf(cs_end - cs_s[t]) * dt_s[t]);
-            yv = load_el(dy, i) * expf(cs_s[t]);
-        }
-        xs[e] = xv;
-        ys[e] = yv;
-    }
     float *S = a.hs + (bh * a.nchunks + c) * (size_t)P * N;
     float *Gc = a.gs + (bh * a.nchunks + c) * (size_t)P * N;
     for (int n0 = 0; n0 < N; n0 += kNT) {
-        __syncthreads();  // xs / ys written; the previous pass's readers of bs / cm done
-        for (int e = tid; e < kBQ * kNT; e += kThreads) {
-            const int t = e / kNT, n = n0 + (e - t * kNT);
-            float bv = 0.f, cv = 0.f;
-            if (t < len && n < N) {
-                const size_t i = (((size_t)b * L + t0 + t) * G + g) * N + n;
-                bv = load_el(Bm, i);
-                cv = load_el(Cm, i);
-            }
-            bs[e] = bv;
-            cm[e] = cv;
-        }
-        __syncthreads();
         float accS[MP][4], accG[MP][4];
 #pragma unroll
         for (int i = 0; i < MP; ++i)
 #pragma unroll
             for (int q = 0; q < 4; ++q) accS[i][q] = accG[i][q] = 0.f;
-        for (int t = 0; t < len; ++t) {
-            float xv[MP], yv[MP], bv[4], cv[4];
-#pragma unroll
-            for (int i = 0; i < MP; ++i) {
-                xv[i] = xs[t * PP + ty + 16 * i];
-                yv[i] = ys[t * PP + ty + 16 * i];
+        for (int k0 = 0; k0 < len; k0 += KS) {
+            const int kn = min(KS, len - k0);
+            __syncthreads();  // the previous block's readers are done
+            // with one block per chunk, x and dy are staged once for every state-column pass
+            if (Q > KS || n0 == 0)
+            for (int e = tid; e < KS * PP; e += kThreads) {
+                const int t = e / PP, p = e - t * PP;
+                float xv = 0.f, yv = 0.f;
+                if (t < kn && p < P) {
+                    const int tc = k0 + t;
+                    const size_t i = (((size_t)b * L + t0 + tc) * H + h) * P + p;
+                    xv = load_el(x, i) * (expf(cs_end - cs_s[tc]) * dt_s[tc]);
+                    yv = load_el(dy, i) * expf(cs_s[tc]);
+                }
+                xs[e] = xv;
+                ys[e] = yv;
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                bv[q] = bs[t * kNT + tx + 16 * q];
-                cv[q] = cm[t * kNT + tx + 16 * q];
+            for (int e = tid; e < KS * kNT; e += kThreads) {
+                const int t = e / kNT, n = n0 + (e - t * kNT);
+                float bv = 0.f, cv = 0.f;
+                if (t < kn && n < N) {
+                    const size_t i = (((size_t)b * L + t0 + k0 + t) * G + g) * N + n;
+                    bv = load_el(Bm, i);
+                    cv = load_el(Cm, i);
+                }
+                bs[e] = bv;
+                cm[e] = cv;
             }
+            __syncthreads();
+            for (int t = 0; t < kn; ++t) {
+                float xv[MP], yv[MP], bv[4], cv[4];
 #pragma unroll
-            for (int i = 0; i < MP; ++i)
+                for (int i = 0; i < MP; ++i) {
+                    xv[i] = xs[t * PP + ty + 16 * i];
+                    yv[i] = ys[t * PP + ty + 16 * i];
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    accS[i][q] = fmaf(xv[i], bv[q], accS[i][q]);
-                    accG[i][q] = fmaf(yv[i], cv[q], accG[i][q]);
+                    bv[q] = bs[t * kNT + tx + 16 * q];
+                    cv[q] = cm[t * kNT + tx + 16 * q];
                 }
+#pragma unroll
+                for (int i = 0; i < MP; ++i)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        accS[i][q] = fmaf(xv[i], bv[q], accS[i][q]);
+                        accG[i][q] = fmaf(yv[i], cv[q], accG[i][q]);
+                    }
+            }
         }
 #pragma unroll
         for (int i = 0; i < MP; ++i) {
@@ -254,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk(BwdArgs a)
     const float *hc = a.hs + (bh * a.nchunks + c) * PN;
     const float *gc = a.gs + (bh * a.nchunks + c) * PN;
 
-    chunk_scalars(a, b, h, t0, len, cs_s, dt_s, cum_s, warp_tot);
+    chunk_scalars<kBQ>(a, b, h, t0, len, cs_s, dt_s, cum_s, warp_tot);
     const float cs_end = cs_s[len - 1];
     if (tid < kBQ) {
         eS[tid] = tid < len ? expf(cs_end - cs_s[tid]) : 0.f;
@@ -603,34 +614,435 @@ __global__ void __launch_bounds__(kThreads) bwd_reduce_heads(BwdArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// 3'. The in-chunk terms on tcgen05 tensor cores (bf16 inputs, headdim 64,
+//     dstate 64, 128-token chunks): one CTA of 128 threads per (chunk, head,
+//     batch); thread t owns token row t of every accumulator (TMEM lane t).
+//     x, dy, B, C arrive by TMA as 128-byte-swizzled [128 tokens][64] bf16
+//     tiles.  Exact bf16 products (dy x^T, C B^T) take the inputs as they are;
+//     every fp32 operand (h_c, g_c, dt B, K, M) goes in as hi + lo bf16 terms,
+//     so each product carries fp32-level accuracy into its fp32 accumulator.
+//     TMEM columns: dy x^T [0,128) then K^T C [0,64) and K (dt B) [64,128);
+//     C B^T [128,256) then M^T dy [128,192); C h^T [256,320); B g^T [320,384);
+//     dy h [384,448); x g [448,512).
+namespace tcb {
+
+using namespace ptx;
+using tile::sw128;
+using tile::split8;
+
+constexpr int kQ = 128, kD = 64;
+constexpr int kTc = 128;          // threads
+constexpr int kTile = kQ * kD * 2;  // one [128][64] bf16 tile: 16 KiB
+// shared-memory layout (bytes from the 1024-aligned base)
+constexpr int oX = 0, oDY = kTile, oB = 2 * kTile, oC = 3 * kTile;
+constexpr int oBh = 4 * kTile, oBl = 5 * kTile;                  // dt B, hi / lo
+constexpr int oHh = 6 * kTile, oHl = oHh + kTile / 2;            // h_c [64 p][64 n], hi / lo
+constexpr int oGh = 7 * kTile, oGl = oGh + kTile / 2;            // g_c, hi / lo
+constexpr int oKh = 8 * kTile, oKl = 10 * kTile;                 // K then M [128 i][2 x 64 j], hi / lo
+constexpr int kSmemTc = 12 * kTile + 1024;
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t a) { return sdesc_sw128(a, 16, 1024); }
+__device__ __forceinline__ uint64_t mdesc(uint32_t a) { return sdesc_sw128(a, kTile, 1024); }
+
+// Sum of v[k] over the 32 lanes of the warp for every k, scattered: lane l
+// returns the sum for k = l (a halving exchange, 31 shuffles).
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int k = 0; k < off; ++k) {
+            const float send = upper ? v[k] : v[k + off];
+            const float keep = upper ? v[k + off] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return v[0];
+}
+
+// Inclusive prefix sum over the 128 threads (warp_tot: 4 floats); every thread calls it.
+__device__ __forceinline__ float scan128(float v, float *warp_tot)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) v += warp_tot[w];
+    __syncthreads();
+    return v;
+}
+
+// Sum over the 128 threads in a fixed order; every thread gets it.
+__device__ __forceinline__ float sum128(float v, float *warp_tot)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) warp_tot[threadIdx.x >> 5] = v;
+    __syncthreads();
+    const float s = (warp_tot[0] + warp_tot[1]) + (warp_tot[2] + warp_tot[3]);
+    __syncthreads();
+    return s;
+}
+
+// Row t (64 bf16) of a [128][64] swizzled tile, as floats.
+__device__ __forceinline__ void load_row(const uint8_t *tilep, int t, float (&f)[64])
+{
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(tilep + sw128(t, q));
+        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 v = __bfloat1622float2(b2[e]);
+            f[8 * q + 2 * e] = v.x;
+            f[8 * q + 2 * e + 1] = v.y;
+        }
+    }
+}
+
+// e_ij = exp(cs_i - cs_j) on the causal triangle of the chunk (0 elsewhere), for
+// the 32 columns j = 32 jb ...; cs in shared memory.
+__device__ __forceinline__ void decay_row(const float *cs, int i, int jb, bool row_in, float (&e)[32])
+{
+    const float ci = cs[i];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        const int j = 32 * jb + k;
+        e[k] = (row_in && j <= i) ? expf(ci - cs[j]) : 0.f;
+    }
+}
+
+// 32 values of row i as hi / lo bf16 into a [128][2 x 64] operand (columns 32 jb ...).
+__device__ __forceinline__ void store_split32(uint8_t *hi_base, uint8_t *lo_base, int i, int jb, const float (&v)[32])
+{
+    const int slab = jb >> 1, q0 = (jb & 1) * 4;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        uint4 hi, lo;
+        split8(&v[8 * u], hi, lo);
+        *reinterpret_cast<uint4 *>(hi_base + slab * kTile + sw128(i, q0 + u)) = hi;
+        *reinterpret_cast<uint4 *>(lo_base + slab * kTile + sw128(i, q0 + u)) = lo;
+    }
+}
+
+__global__ void __launch_bounds__(kTc, 1)
+    bwd_chunk_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap dymap,
+                 const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap cmap, BwdArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_ld, bar_mma;
+    __shared__ uint32_t tmem_slot;
+    __shared__ float warp_tot[4];
+    __shared__ float cs_s[kQ], dt_s[kQ], cum_s[kQ], row_s[kQ], zv_s[kQ], ddt_s[kQ];
+    __shared__ float colp[4][kQ];
+    __shared__ int s_fail;
+
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int L = a.seqlen, H = a.nheads, G = a.ngroups, g = h / (H / G);
+    const int t0 = c * kQ, len = min(kQ, L - t0);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint8_t *base = tile::align1024(smem_raw);
+    const uint32_t sb = smem_u32(base);
+    const size_t bh = (size_t)b * H + h;
+    const float *hc = a.hs + (bh * a.nchunks + c) * (size_t)(kD * kD);
+    const float *gc = a.gs + (bh * a.nchunks + c) * (size_t)(kD * kD);
+    const float Ah = __ldg(a.A + h);
+
+    if (tid == 0) {
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_mma, 1);
+        mbar_fence_init();
+        s_fail = 0;
+    }
+    if (warp == 0) tmem_alloc(&tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t lrow = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
+
+    if (tid == 0) {
+        tma_prefetch_desc(&xmap);
+        tma_prefetch_desc(&dymap);
+        tma_prefetch_desc(&bmap);
+        tma_prefetch_desc(&cmap);
+        mbar_expect_tx(&bar_ld, (uint32_t)(4 * kTile));
+        tma_load_3d(base + oX, &xmap, &bar_ld, h * kD, t0, b);
+        tma_load_3d(base + oDY, &dymap, &bar_ld, h * kD, t0, b);
+        tma_load_3d(base + oB, &bmap, &bar_ld, g * kD, t0, b);
+        tma_load_3d(base + oC, &cmap, &bar_ld, g * kD, t0, b);
+    }
+
+    // scalars of the chunk: cs (prefix of dt A), dt, cum (prefix of dt); 0 / constant past len
+    const float dtv = tid < len ? __ldg(a.dt + ((size_t)b * L + t0 + tid) * H + h) : 0.f;
+    const float cs_t = scan128(dtv * Ah, warp_tot);
+    const float cum_t = scan128(dtv, warp_tot);
+    cs_s[tid] = cs_t;
+    dt_s[tid] = dtv;
+    cum_s[tid] = cum_t;
+
+    // h_c, g_c -> [64 p][64 n] hi / lo tiles (thread: row p = tid / 2, columns 32 (tid & 1) ...); <g_c, h_c>
+    float u = 0.f;
+    {
+        const int p = tid >> 1, q0 = (tid & 1) * 4;
+#pragma unroll
+        for (int q = q0; q < q0 + 4; ++q) {
+            float hv[8], gv[8];
+            const float4 *hp = reinterpret_cast<const float4 *>(hc + p * kD + 8 * q);
+            const float4 *gp = reinterpret_cast<const float4 *>(gc + p * kD + 8 * q);
+            const float4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1), g0 = __ldcg(gp), g1 = __ldcg(gp + 1);
+            hv[0] = h0.x; hv[1] = h0.y; hv[2] = h0.z; hv[3] = h0.w; hv[4] = h1.x; hv[5] = h1.y; hv[6] = h1.z; hv[7] = h1.w;
+            gv[0] = g0.x; gv[1] = g0.y; gv[2] = g0.z; gv[3] = g0.w; gv[4] = g1.x; gv[5] = g1.y; gv[6] = g1.z; gv[7] = g1.w;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) u = fmaf(hv[k], gv[k], u);
+            uint4 hi, lo;
+            split8(hv, hi, lo);
+            *reinterpret_cast<uint4 *>(base + oHh + sw128(p, q)) = hi;
+            *reinterpret_cast<uint4 *>(base + oHl + sw128(p, q)) = lo;
+            split8(gv, hi, lo);
+            *reinterpret_cast<uint4 *>(base + oGh + sw128(p, q)) = hi;
+            *reinterpret_cast<uint4 *>(base + oGl + sw128(p, q)) = lo;
+        }
+    }
+    bool ok = mbar_wait(&bar_ld, 0);
+    // dt_j B_j -> hi / lo (row j = tid)
+    if (ok) {
+        float f[64];
+        load_row(base + oB, tid, f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = dtv * f[8 * q + k];
+            uint4 hi, lo;
+            split8(v, hi, lo);
+            *reinterpret_cast<uint4 *>(base + oBh + sw128(tid, q)) = hi;
+            *reinterpret_cast<uint4 *>(base + oBl + sw128(tid, q)) = lo;
+        }
+    } else {
+        s_fail = 1;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    ok = !s_fail;
+
+    // dy x^T, C B^T, C h^T, B g^T, dy h, x g
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        constexpr uint32_t id_sq = idesc_bf16(128, 128, 0, 0);
+        constexpr uint32_t id_kk = idesc_bf16(128, 64, 0, 0);
+        constexpr uint32_t id_km = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint32_t kk = ks * 32, km = ks * 2048;  // K step: 16 elements of a row / 16 rows
+            mma_bf16(tmem + 0, kdesc(sb + oDY + kk), kdesc(sb + oX + kk), id_sq, ks > 0);
+            mma_bf16(tmem + 128, kdesc(sb + oC + kk), kdesc(sb + oB + kk), id_sq, ks > 0);
+            mma_bf16(tmem + 256, kdesc(sb + oC + kk), kdesc(sb + oHh + kk), id_kk, ks > 0);
+            mma_bf16(tmem + 256, kdesc(sb + oC + kk), kdesc(sb + oHl + kk), id_kk, 1);
+            mma_bf16(tmem + 320, kdesc(sb + oB + kk), kdesc(sb + oGh + kk), id_kk, ks > 0);
+            mma_bf16(tmem + 320, kdesc(sb + oB + kk), kdesc(sb + oGl + kk), id_kk, 1);
+            mma_bf16(tmem + 384, kdesc(sb + oDY + kk), mdesc(sb + oHh + km), id_km, ks > 0);
+            mma_bf16(tmem + 384, kdesc(sb + oDY + kk), mdesc(sb + oHl + km), id_km, 1);
+            mma_bf16(tmem + 448, kdesc(sb + oX + kk), mdesc(sb + oGh + km), id_km, ks > 0);
+            mma_bf16(tmem + 448, kdesc(sb + oX + kk), mdesc(sb + oGl + km), id_km, 1);
+        }
+        mma_commit(&bar_mma);
+    }
+    ok = ok && mbar_wait(&bar_mma, 0);
+    ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
+    tc_fence_after();
+
+    // K = e o (dy x^T) -> hi / lo operand; W = e o (C B^T) o (dy x^T) dt_j below the diagonal:
+    // row sums here, column sums by a per-warp exchange; the diagonal of dy x^T gives dD's part
+    const int i = tid;
+    const bool row_in = i < len;
+    float rs = 0.f, diag = 0.f;
+    if (ok) {
+#pragma unroll 1
+        for (int jb = 0; jb < 4; ++jb) {
+            float dx[32], cb[32], e[32], w[32];
+            tmem_ld32(lrow + 32 * jb, dx);
+            tmem_ld32(lrow + 128 + 32 * jb, cb);
+            decay_row(cs_s, i, jb, row_in, e);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int j = 32 * jb + k;
+                if (j == i) diag = dx[k];
+                const float kv = e[k] * dx[k];
+                w[k] = j < i ? kv * cb[k] * dt_s[j] : 0.f;
+                rs += w[k];
+                dx[k] = kv;
+            }
+            store_split32(base + oKh, base + oKl, i, jb, dx);
+            colp[warp][32 * jb + lane] = reduce_scatter32(w, lane);
+        }
+    }
+    row_s[i] = rs;
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // K^T C and K (dt B)
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        constexpr uint32_t id_mm = idesc_bf16(128, 64, 1, 1);
+        constexpr uint32_t id_km = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+        for (int ks = 0; ks < kQ / 16; ++ks) {
+            const uint32_t km = ks * 2048;                                    // 16 rows of a [128][..] operand
+            const uint32_t kk = (ks >> 2) * kTile + (ks & 3) * 32;            // 16 columns of the K operand
+            mma_bf16(tmem + 0, mdesc(sb + oKh + km), mdesc(sb + oC + km), id_mm, ks > 0);
+            mma_bf16(tmem + 0, mdesc(sb + oKl + km), mdesc(sb + oC + km), id_mm, 1);
+            mma_bf16(tmem + 64, kdesc(sb + oKh + kk), mdesc(sb + oBh + km), id_km, ks > 0);
+            mma_bf16(tmem + 64, kdesc(sb + oKh + kk), mdesc(sb + oBl + km), id_km, 1);
+            mma_bf16(tmem + 64, kdesc(sb + oKl + kk), mdesc(sb + oBh + km), id_km, 1);
+        }
+        mma_commit(&bar_mma);
+    }
+    // meanwhile: Z_i = dy_i . (C_i h^T) and V_j = dt_j x_j . (B_j g^T) from columns the MMAs above do not touch
+    float zi = 0.f, vj = 0.f;
+    if (ok) {
+        float r[64], f[64];
+        tmem_ld64(lrow + 256, r);
+        load_row(base + oDY, i, f);
+#pragma unroll
+        for (int k = 0; k < 64; ++k) zi = fmaf(f[k], r[k], zi);
+        tmem_ld64(lrow + 320, r);
+        load_row(base + oX, i, f);
+#pragma unroll
+        for (int k = 0; k < 64; ++k) vj = fmaf(f[k], r[k], vj);
+        vj *= dtv;
+    }
+    ok = ok && mbar_wait(&bar_mma, 1);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+
+    // M = e o (C B^T) -> hi / lo over the K operand, then M^T dy
+    if (ok) {
+#pragma unroll 1
+        for (int jb = 0; jb < 4; ++jb) {
+            float cb[32], e[32];
+            tmem_ld32(lrow + 128 + 32 * jb, cb);
+            decay_row(cs_s, i, jb, row_in, e);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) cb[k] *= e[k];
+            store_split32(base + oKh, base + oKl, i, jb, cb);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        constexpr uint32_t id_mm = idesc_bf16(128, 64, 1, 1);
+#pragma unroll
+        for (int ks = 0; ks < kQ / 16; ++ks) {
+            const uint32_t km = ks * 2048;
+            mma_bf16(tmem + 128, mdesc(sb + oKh + km), mdesc(sb + oDY + km), id_mm, ks > 0);
+            mma_bf16(tmem + 128, mdesc(sb + oKl + km), mdesc(sb + oDY + km), id_mm, 1);
+        }
+        mma_commit(&bar_mma);
+    }
+    ok = ok && mbar_wait(&bar_mma, 0);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+
+    // outputs of row j = tid: dB, dC (per head, or the group's when it has one head), dx, x . inner
+    const float cs_end = cs_s[len - 1];
+    const float eSj = row_in ? expf(cs_end - cs_t) : 0.f, eCj = row_in ? expf(cs_t) : 0.f;
+    const bool direct = a.dBp == nullptr;
+    float xin = 0.f;
+    if (ok) {
+        float acc[64], add[64];
+        const size_t orow = (((size_t)b * L + t0 + i) * (direct ? G : H) + (direct ? g : h)) * kD;
+        tmem_ld64(lrow + 0, acc);
+        tmem_ld64(lrow + 448, add);
+        if (row_in) {
+            float4 *o = reinterpret_cast<float4 *>((direct ? a.dB : a.dBp) + orow);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                o[q] = make_float4(dtv * fmaf(eSj, add[4 * q], acc[4 * q]), dtv * fmaf(eSj, add[4 * q + 1], acc[4 * q + 1]),
+                                   dtv * fmaf(eSj, add[4 * q + 2], acc[4 * q + 2]),
+                                   dtv * fmaf(eSj, add[4 * q + 3], acc[4 * q + 3]));
+        }
+        tmem_ld64(lrow + 64, acc);
+        tmem_ld64(lrow + 384, add);
+        if (row_in) {
+            float4 *o = reinterpret_cast<float4 *>((direct ? a.dC : a.dCp) + orow);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                o[q] = make_float4(fmaf(eCj, add[4 * q], acc[4 * q]), fmaf(eCj, add[4 * q + 1], acc[4 * q + 1]),
+                                   fmaf(eCj, add[4 * q + 2], acc[4 * q + 2]), fmaf(eCj, add[4 * q + 3], acc[4 * q + 3]));
+        }
+        tmem_ld64(lrow + 128, acc);
+        tmem_ld64(lrow + 320, add);
+        float f[64];
+        const float Dh = a.D ? __ldg(a.D + h) : 0.f;
+#pragma unroll
+        for (int k = 0; k < 64; ++k) acc[k] = fmaf(eSj, add[k], acc[k]);  // inner_j
+        load_row(base + oX, i, f);
+#pragma unroll
+        for (int k = 0; k < 64; ++k) xin = fmaf(f[k], acc[k], xin);
+        load_row(base + oDY, i, f);
+        if (row_in) {
+            float4 *o = reinterpret_cast<float4 *>(a.dx + (((size_t)b * L + t0 + i) * H + h) * kD);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                o[q] = make_float4(fmaf(Dh, f[4 * q], dtv * acc[4 * q]), fmaf(Dh, f[4 * q + 1], dtv * acc[4 * q + 1]),
+                                   fmaf(Dh, f[4 * q + 2], dtv * acc[4 * q + 2]),
+                                   fmaf(Dh, f[4 * q + 3], dtv * acc[4 * q + 3]));
+        }
+    }
+    tc_fence_before();
+    ddt_s[i] = xin;
+    zv_s[i] = eSj * vj;  // e^{cs_end - cs_j} V_j
+    __syncthreads();
+
+    // dL/dcs_t, then ddt = x . inner + A sum_{t' >= t} dcs_t', and the dA / dD parts
+    const float colsum = (colp[0][i] + colp[1][i]) + (colp[2][i] + colp[3][i]);
+    const float ssum = sum128(row_in ? zv_s[i] : 0.f, warp_tot);  // sum_j e^{cs_end - cs_j} V_j
+    const float usum = sum128(u, warp_tot);
+    const float dsum = sum128(diag, warp_tot);
+    float d = 0.f;
+    if (row_in) {
+        d = row_s[i] - colsum + eCj * zi - zv_s[i];
+        if (i == len - 1) d += ssum + expf(cs_end) * usum;
+    }
+    // suffix sum: total - (inclusive prefix) + own
+    const float pre = scan128(d, warp_tot);
+    const float tot = sum128(d, warp_tot);
+    if (row_in && ok) a.ddt[((size_t)b * L + t0 + i) * H + h] = fmaf(Ah, tot - pre + d, ddt_s[i]);
+    const float da = sum128(d * cum_s[i], warp_tot);
+    if (tid == 0 && ok) {
+        const size_t o = ((size_t)b * a.nchunks + c) * H + h;
+        a.dAp[o] = da;
+        a.dDp[o] = dsum;
+    }
+    if (tid == 0 && !ok && a.err_word) atomicOr(a.err_word, kDevErrTimeout);
+    tc_fence_after();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace tcb
+
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
-template <int MP>
-size_t chunk_states_smem() { return sizeof(float) * (2 * kBQ * MP * 16 + 2 * kBQ * kNT); }
+template <int MP, int Q>
+size_t chunk_states_smem() { return sizeof(float) * (2 * 64 * MP * 16 + 2 * 64 * kNT); }
 template <int MP>
 size_t chunk_smem() { return sizeof(float) * (2 * kBQ * (MP * 16 + 1) + 2 * kBQ * (kBQ + 1) + 2 * kBQ * (kNS + 1) + 2 * MP * 16 * (kNS + 1)); }
 
-template <typename T, int MP>
-cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t s)
+cudaError_t launch_reductions(const BwdArgs &a, cudaStream_t s)
 {
-    const dim3 grid(a.nchunks, a.nheads, a.batch);
     cudaError_t e;
-    const size_t s1 = chunk_states_smem<MP>(), s3 = chunk_smem<MP>();
-    if ((e = ensure_smem_limit((const void *)bwd_chunk_states<T, MP>, s1)) != cudaSuccess) return e;
-    if ((e = ensure_smem_limit((const void *)bwd_chunk<T, MP>, s3)) != cudaSuccess) return e;
-    profile_kernel_begin(s);
-    bwd_chunk_states<T, MP><<<grid, kThreads, s1, s>>>(a);
-    profile_kernel_end(s);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t PN = (size_t)a.headdim * a.dstate;
-    profile_kernel_begin(s);
-    bwd_state_pass<<<dim3((unsigned)((PN + kThreads - 1) / kThreads), a.nheads, a.batch), kThreads, 0, s>>>(a);
-    profile_kernel_end(s);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    profile_kernel_begin(s);
-    bwd_chunk<T, MP><<<grid, kThreads, s3, s>>>(a);
-    profile_kernel_end(s);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.dBp) {
         int sms = 148;
         if ((e = sm_count(&sms)) != cudaSuccess) return e;
@@ -648,6 +1060,62 @@ cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t s)
     return cudaGetLastError();
 }
 
+template <typename T, int MP>
+cudaError_t launch_bwd_typed(const BwdArgs &a, cudaStream_t s)
+{
+    const dim3 grid(a.nchunks, a.nheads, a.batch);
+    cudaError_t e;
+    const size_t s1 = chunk_states_smem<MP, kBQ>(), s3 = chunk_smem<MP>();
+    if ((e = ensure_smem_limit((const void *)bwd_chunk_states<T, MP, kBQ>, s1)) != cudaSuccess) return e;
+    if ((e = ensure_smem_limit((const void *)bwd_chunk<T, MP>, s3)) != cudaSuccess) return e;
+    profile_kernel_begin(s);
+    bwd_chunk_states<T, MP, kBQ><<<grid, kThreads, s1, s>>>(a);
+    profile_kernel_end(s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t PN = (size_t)a.headdim * a.dstate;
+    profile_kernel_begin(s);
+    bwd_state_pass<<<dim3((unsigned)((PN + kThreads - 1) / kThreads), a.nheads, a.batch), kThreads, 0, s>>>(a);
+    profile_kernel_end(s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    profile_kernel_begin(s);
+    bwd_chunk<T, MP><<<grid, kThreads, s3, s>>>(a);
+    profile_kernel_end(s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_reductions(a, s);
+}
+
+// bf16, headdim 64, dstate 64: chunk states and state passes as on the fp32 path
+// (128-token chunks), the in-chunk terms on tcgen05
+cudaError_t launch_bwd_tc(const BwdArgs &a, cudaStream_t s)
+{
+    CUtensorMap xm, dym, bm, cm;
+    cudaError_t e;
+    const int H = a.nheads, G = a.ngroups;
+    if ((e = cached_tensor_map(&xm, a.x, true, H * 64, a.seqlen, a.batch, 64, 128, true)) != cudaSuccess) return e;
+    if ((e = cached_tensor_map(&dym, a.dy, true, H * 64, a.seqlen, a.batch, 64, 128, true)) != cudaSuccess) return e;
+    if ((e = cached_tensor_map(&bm, a.B, true, G * 64, a.seqlen, a.batch, 64, 128, true)) != cudaSuccess) return e;
+    if ((e = cached_tensor_map(&cm, a.C, true, G * 64, a.seqlen, a.batch, 64, 128, true)) != cudaSuccess) return e;
+    const dim3 grid(a.nchunks, H, a.batch);
+    const size_t s1 = chunk_states_smem<4, tcb::kQ>();
+    if ((e = ensure_smem_limit((const void *)bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ>, s1)) != cudaSuccess)
+        return e;
+    if ((e = ensure_smem_limit((const void *)tcb::bwd_chunk_tc, tcb::kSmemTc)) != cudaSuccess) return e;
+    profile_kernel_begin(s);
+    bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ><<<grid, kThreads, s1, s>>>(a);
+    profile_kernel_end(s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t PN = (size_t)a.headdim * a.dstate;
+    profile_kernel_begin(s);
+    bwd_state_pass<<<dim3((unsigned)((PN + kThreads - 1) / kThreads), H, a.batch), kThreads, 0, s>>>(a);
+    profile_kernel_end(s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    profile_kernel_begin(s);
+    tcb::bwd_chunk_tc<<<grid, tcb::kTc, tcb::kSmemTc, s>>>(xm, dym, bm, cm, a);
+    profile_kernel_end(s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_reductions(a, s);
+}
+
 template <typename T>
 cudaError_t launch_bwd_dtype(const BwdArgs &a, cudaStream_t s)
 {
@@ -657,11 +1125,23 @@ cudaError_t launch_bwd_dtype(const BwdArgs &a, cudaStream_t s)
     return launch_bwd_typed<T, 8>(a, s);
 }
 
+bool aligned16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+
+// The tensor-core path: bf16, headdim 64, dstate 64, TMA-aligned inputs.
+bool use_tc(const BwdProblem &p)
+{
+    return p.dtype == SSD_DTYPE_BF16 && p.headdim == 64 && p.dstate == 64 && aligned16(p.x) && aligned16(p.dy) &&
+           aligned16(p.B) && aligned16(p.C);
+}
+
+int chunk_len(const BwdProblem &p) { return use_tc(p) ? tcb::kQ : kBQ; }
+
 }  // namespace
 
 size_t bwd_workspace_bytes(const BwdProblem &p)
 {
-    const size_t nc = (size_t)(p.seqlen + kBQ - 1) / kBQ;
+    const int q = chunk_len(p);
+    const size_t nc = (size_t)(p.seqlen + q - 1) / q;
     const size_t units = (size_t)p.batch * p.nheads * nc;
     size_t v = 2 * align256(units * p.headdim * p.dstate * sizeof(float)) + align256(units * sizeof(float)) +
                2 * align256((size_t)p.batch * nc * p.nheads * sizeof(float));
@@ -674,6 +1154,10 @@ int bwd_kernel_count(const BwdProblem &p) { return p.nheads != p.ngroups ? 5 : 4
 
 const char *bwd_kernel_names(const BwdProblem &p)
 {
+    if (use_tc(p))
+        return p.nheads != p.ngroups
+                   ? "bwd_chunk_states,bwd_state_pass,bwd_chunk_tc,bwd_reduce_groups,bwd_reduce_heads"
+                   : "bwd_chunk_states,bwd_state_pass,bwd_chunk_tc,bwd_reduce_heads";
     return p.nheads != p.ngroups ? "bwd_chunk_states,bwd_state_pass,bwd_chunk,bwd_reduce_groups,bwd_reduce_heads"
                                  : "bwd_chunk_states,bwd_state_pass,bwd_chunk,bwd_reduce_heads";
 }
@@ -703,7 +1187,9 @@ cudaError_t launch_bwd(const BwdProblem &p, void *workspace, cudaStream_t s)
     a.headdim = p.headdim;
     a.ngroups = p.ngroups;
     a.dstate = p.dstate;
-    a.nchunks = (p.seqlen + kBQ - 1) / kBQ;
+    const int q = chunk_len(p);
+    a.nchunks = (p.seqlen + q - 1) / q;
+    a.err_word = p.err_word;
     const size_t units = (size_t)p.batch * p.nheads * a.nchunks;
     const size_t st = align256(units * p.headdim * p.dstate * sizeof(float));
     const size_t part = align256((size_t)p.batch * a.nchunks * p.nheads * sizeof(float));
@@ -720,6 +1206,7 @@ cudaError_t launch_bwd(const BwdProblem &p, void *workspace, cudaStream_t s)
     } else {
         a.dBp = a.dCp = nullptr;
     }
+    if (use_tc(p)) return launch_bwd_tc(a, s);
     return p.dtype == SSD_DTYPE_BF16 ? launch_bwd_dtype<__nv_bfloat16>(a, s) : launch_bwd_dtype<float>(a, s);
 }
 

@@ -918,7 +918,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             mbar_init(&bar_full[k], 1);
             mbar_init(&bar_dt[k], 1);
             mbar_init(&bar_free[k], 1);
-            mbar_init(&bar_slot[k], 1);
+            mbar_init(&bar_slot[k], 4);
             mbar_init(&bar_lo[k], 1);
             mbar_init(&bar_g[k], 1);
             mbar_init(&bar_mask[k], 128);
@@ -1112,8 +1112,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             if (ft == 0) s_fast[ss] = fast ? 1 : 0;
             mbar_arrive(&bar_seg[ss]);
             named_sync(kBarFront, 128);  // every v_j dt_j is in shared memory
-            ok = mbar_wait(&bar_full[s], ph, lim) && (it < 2 || mbar_wait(&bar_lo[s], ph ^ 1, lim));
-            ok = ok && mbar_wait(&bar_g[s], ph, lim);
+            ok = mbar_wait(&bar_full[s], ph, lim) && mbar_wait(&bar_g[s], ph, lim);
             ok = __all_sync(0xffffffffu, ok);  // the TMEM accesses below are warp-collective
             tc_fence_after();
             if (ok && fast) {  // tril(G) -> bf16 pairs in TMEM (row m, columns jb*32 .. jb*32+31)
@@ -1142,6 +1141,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&bar_mask[s]);
+            // the lo region is the staging region of the unit two back: wait for its y store
+            // only now, so the tril(G) build above overlaps that store
+            ok = ok && (it < 2 || mbar_wait(&bar_lo[s], ph ^ 1, lim));
             // wx = v dt x, hi in place over x, lo at +32K, in 16-token slices: slice
             // ks is rows 16 ks .. 16 ks + 15 of both 64-column slabs (256 chunks)
 #pragma unroll 1
@@ -1431,6 +1433,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
                     float yv[64];
                     tmem_ld64(slot + col_y + col, yv);
+                    if (col == 64) {  // this warp's last read of Y: its quarter of the slot is free
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar_slot[s]);
+                    }
                     const float2 r2 = make_float2(r, r), D2 = make_float2(Dh, Dh);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -1456,8 +1463,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             fence_async_smem();
             tc_fence_before();
             const bool all_ok = !named_sync_or(bar_team, 128, !ok);
+            // every warp frees the slot once per unit: above after its last read of Y, here
+            // when it read nothing (a failed unit); a wide unit reads G below and frees it after
+            if (!(ok && fast) && !(all_ok && !fast) && lane == 0) mbar_arrive(&bar_slot[s]);
             if (tt == 0) {
-                if (!(all_ok && !fast)) mbar_arrive(&bar_slot[s]);  // Y has been read (a wide unit reads G below)
                 if (all_ok && fast && tma_out) {
                     for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, u.hb * 128 + 64 * k, u.tt, u.tb);
                     bulk_commit();
@@ -1472,8 +1481,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                                         cs[ss], dtv[ss], m, 0);
                 tc_fence_before();
                 named_sync(bar_team, 128);  // every thread is done with the stage and the TMEM slot
+                if (lane == 0) mbar_arrive(&bar_slot[s]);
                 if (tt == 0) {
-                    mbar_arrive(&bar_slot[s]);
                     mbar_arrive(&bar_lo[s]);
                     mbar_arrive(&bar_free[s]);
                 }

@@ -167,6 +167,7 @@ struct BwdProblem {
     float *dinit;             // may be null
     int batch, seqlen, nheads, headdim, ngroups, dstate;
     ssd_dtype_t dtype;
+    unsigned int *err_word;   // device error word (a failed bounded wait sets kDevErrTimeout)
 };
 constexpr int kBwdMaxHeaddim = 128;
 size_t bwd_workspace_bytes(const BwdProblem &p);

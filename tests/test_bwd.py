@@ -66,6 +66,11 @@ CASES = [
     (1, 100, 2, 64, 256, 1, "bf16", False, True, True),    # dstate 256
     (3, 64, 2, 16, 16, 1, "f32", True, True, True),        # exactly one chunk
     (2, 1, 2, 16, 16, 2, "f32", True, True, True),         # one token
+    # the tensor-core in-chunk kernel (bf16, headdim 64, dstate 64, 128-token chunks)
+    (2, 300, 8, 64, 64, 2, "bf16", True, True, True),      # ragged tail, 4 heads per group
+    (1, 128, 4, 64, 64, 4, "bf16", True, True, False),     # exactly one chunk, one head per group, no D
+    (2, 1, 2, 64, 64, 1, "bf16", True, True, True),        # one token
+    (1, 1000, 2, 64, 64, 1, "bf16", False, False, True),   # eight chunks, no initial state, no dfinal
 ]
 
 
@@ -120,3 +125,10 @@ def test_per_kernel_timing_hook_outside_capture():
     ssd.ssd_check_device_status()
     times = [evs[2 * k].elapsed_time(evs[2 * k + 1]) for k in range(len(names))]
     assert all(t > 0 for t in times), dict(zip(names, times))
+
+
+def test_tensor_core_kernel_is_the_one_that_runs():
+    assert "bwd_chunk_tc" in ssd.ssd_bwd_kernels(2, 300, 8, 64, 2, 64, torch.bfloat16)
+    assert "bwd_chunk_tc" in ssd.ssd_bwd_kernels(2, 2048, 80, 64, 1, 64, torch.bfloat16)
+    assert "bwd_chunk" in ssd.ssd_bwd_kernels(2, 300, 8, 64, 2, 128, torch.bfloat16)
+    assert "bwd_chunk" in ssd.ssd_bwd_kernels(2, 300, 8, 64, 2, 64, torch.float32)
