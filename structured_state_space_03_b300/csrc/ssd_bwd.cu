@@ -38,6 +38,7 @@
 //                        more than one head), dA / dD over batch and chunks
 // Every reduction runs in a fixed order, so results are bitwise reproducible.
 #include <algorithm>
+#include <cstring>
 
 #include "ssd_internal.cuh"
 #include "ssd_ptx.cuh"
@@ -95,7 +96,9 @@ __device__ __forceinline__ void chunk_scalars(const BwdArgs &a, int b, int h, in
 // 1. S_c[p][n] = sum_j e^{cs_end - cs_j} dt_j x_j[p] B_j[n] and
 //    G_c[p][n] = sum_i e^{cs_i} dy_i[p] C_i[n], kNT state columns per pass.
 //    Thread (ty, tx) owns rows p = ty + 16 a and columns n = tx + 16 q.
-template <typename T, int MP, int Q>
+// kWithS false: G_c only (S_c and the decays come from the forward's tcgen05
+// chunk-state kernel).
+template <typename T, int MP, int Q, bool kWithS = true>
 __global__ void __launch_bounds__(kThreads) bwd_chunk_states(BwdArgs a)
 {
     extern __shared__ float sm[];
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_states(BwdArgs a)
     chunk_scalars<Q>(a, b, h, t0, len, cs_s, dt_s, cum_s, warp_tot);
     const float cs_end = cs_s[len - 1];
     const size_t bh = (size_t)b * H + h;
-    if (tid == 0) a.decay[bh * a.nchunks + c] = expf(cs_end);
+    if (kWithS && tid == 0) a.decay[bh * a.nchunks + c] = expf(cs_end);
     float *S = a.hs + (bh * a.nchunks + c) * (size_t)P * N;
     float *Gc = a.gs + (bh * a.nchunks + c) * (size_t)P * N;
     for (int n0 = 0; n0 < N; n0 += kNT) {
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_states(BwdArgs a)
                 if (t < kn && p < P) {
                     const int tc = k0 + t;
                     const size_t i = (((size_t)b * L + t0 + tc) * H + h) * P + p;
-                    xv = load_el(x, i) * (expf(cs_end - cs_s[tc]) * dt_s[tc]);
+                    if (kWithS) xv = load_el(x, i) * (expf(cs_end - cs_s[tc]) * dt_s[tc]);
                     yv = load_el(dy, i) * expf(cs_s[tc]);
                 }
                 xs[e] = xv;
@@ -174,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_states(BwdArgs a)
                 for (int i = 0; i < MP; ++i)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        accS[i][q] = fmaf(xv[i], bv[q], accS[i][q]);
+                        if (kWithS) accS[i][q] = fmaf(xv[i], bv[q], accS[i][q]);
                         accG[i][q] = fmaf(yv[i], cv[q], accG[i][q]);
                     }
             }
@@ -187,7 +190,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_states(BwdArgs a)
             for (int q = 0; q < 4; ++q) {
                 const int n = n0 + tx + 16 * q;
                 if (n < N) {
-                    S[(size_t)p * N + n] = accS[i][q];
+                    if (kWithS) S[(size_t)p * N + n] = accS[i][q];
                     Gc[(size_t)p * N + n] = accG[i][q];
                 }
             }
@@ -1097,13 +1100,46 @@ cudaError_t launch_bwd_tc(const BwdArgs &a, cudaStream_t s)
     if ((e = cached_tensor_map(&cm, a.C, true, G * 64, a.seqlen, a.batch, 64, 128, true)) != cudaSuccess) return e;
     const dim3 grid(a.nchunks, H, a.batch);
     const size_t s1 = chunk_states_smem<4, tcb::kQ>();
-    if ((e = ensure_smem_limit((const void *)bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ>, s1)) != cudaSuccess)
-        return e;
-    if ((e = ensure_smem_limit((const void *)tcb::bwd_chunk_tc, tcb::kSmemTc)) != cudaSuccess) return e;
-    profile_kernel_begin(s);
-    bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ><<<grid, kThreads, s1, s>>>(a);
-    profile_kernel_end(s);
+    if (H % 2 == 0 && (H / G) % 2 == 0) {
+        // S_c and the chunk decays are exactly the forward's chunk-state product: on
+        // tcgen05 (its head pairs lie inside one group); G_c on the fp32 kernel
+        Problem fp;
+        memset(&fp, 0, sizeof fp);
+        fp.x = a.x;
+        fp.dt = a.dt;
+        fp.A = a.A;
+        fp.B = a.B;
+        fp.C = a.C;
+        fp.batch = a.batch;
+        fp.seqlen = a.seqlen;
+        fp.nheads = H;
+        fp.headdim = 64;
+        fp.ngroups = G;
+        fp.dstate = 64;
+        fp.chunk = tcb::kQ;
+        fp.nchunks = a.nchunks;
+        fp.dtype = SSD_DTYPE_BF16;
+        fp.err_word = a.err_word;
+        Workspace fws;
+        fws.states = a.hs;
+        fws.decay = a.decay;
+        if ((e = launch_chunk_state_tc(fp, fws, s)) != cudaSuccess) return e;
+        if ((e = ensure_smem_limit((const void *)bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ, false>, s1)) !=
+            cudaSuccess)
+            return e;
+        profile_kernel_begin(s);
+        bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ, false><<<grid, kThreads, s1, s>>>(a);
+        profile_kernel_end(s);
+    } else {  // both state sums on the fp32 kernel
+        if ((e = ensure_smem_limit((const void *)bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ, true>, s1)) !=
+            cudaSuccess)
+            return e;
+        profile_kernel_begin(s);
+        bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ, true><<<grid, kThreads, s1, s>>>(a);
+        profile_kernel_end(s);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = ensure_smem_limit((const void *)tcb::bwd_chunk_tc, tcb::kSmemTc)) != cudaSuccess) return e;
     const size_t PN = (size_t)a.headdim * a.dstate;
     profile_kernel_begin(s);
     bwd_state_pass<<<dim3((unsigned)((PN + kThreads - 1) / kThreads), H, a.batch), kThreads, 0, s>>>(a);
@@ -1136,6 +1172,10 @@ bool use_tc(const BwdProblem &p)
 
 int chunk_len(const BwdProblem &p) { return use_tc(p) ? tcb::kQ : kBQ; }
 
+// On the tensor-core path, S_c comes from the forward's chunk-state kernel when
+// its head pairs (128 TMEM lanes = 2 heads of 64) fall inside one group.
+bool fwd_states(const BwdProblem &p) { return use_tc(p) && p.nheads % 2 == 0 && (p.nheads / p.ngroups) % 2 == 0; }
+
 }  // namespace
 
 size_t bwd_workspace_bytes(const BwdProblem &p)
@@ -1150,10 +1190,14 @@ size_t bwd_workspace_bytes(const BwdProblem &p)
     return v;
 }
 
-int bwd_kernel_count(const BwdProblem &p) { return p.nheads != p.ngroups ? 5 : 4; }
+int bwd_kernel_count(const BwdProblem &p) { return (p.nheads != p.ngroups ? 5 : 4) + (fwd_states(p) ? 1 : 0); }
 
 const char *bwd_kernel_names(const BwdProblem &p)
 {
+    if (fwd_states(p))
+        return p.nheads != p.ngroups
+                   ? "chunk_state_tc,bwd_chunk_states,bwd_state_pass,bwd_chunk_tc,bwd_reduce_groups,bwd_reduce_heads"
+                   : "chunk_state_tc,bwd_chunk_states,bwd_state_pass,bwd_chunk_tc,bwd_reduce_heads";
     if (use_tc(p))
         return p.nheads != p.ngroups
                    ? "bwd_chunk_states,bwd_state_pass,bwd_chunk_tc,bwd_reduce_groups,bwd_reduce_heads"
