@@ -619,8 +619,9 @@ __global__ void __launch_bounds__(kThreads) bwd_reduce_heads(BwdArgs a)
 
 // ---------------------------------------------------------------------------
 // 3'. The in-chunk terms on tcgen05 tensor cores (bf16 inputs, headdim 64,
-//     dstate 64, 128-token chunks): one CTA of 128 threads per (chunk, head,
-//     batch); thread t owns token row t of every accumulator (TMEM lane t).
+//     dstate 64, 128-token chunks): one CTA of 256 threads per (chunk, head,
+//     batch); warps w and w + 4 own token rows 32 (w & 3) .. 32 (w & 3) + 31 of
+//     every accumulator (their TMEM lanes) and split its columns.
 //     x, dy, B, C arrive by TMA as 128-byte-swizzled [128 tokens][64] bf16
 //     tiles.  Exact bf16 products (dy x^T, C B^T) take the inputs as they are;
 //     every fp32 operand (h_c, g_c, dt B, K, M) goes in as hi + lo bf16 terms,
@@ -635,7 +636,7 @@ using tile::sw128;
 using tile::split8;
 
 constexpr int kQ = 128, kD = 64;
-constexpr int kTc = 128;          // threads
+constexpr int kTc = 256;          // threads: two warps per TMEM lane quarter
 constexpr int kTile = kQ * kD * 2;  // one [128][64] bf16 tile: 16 KiB
 // shared-memory layout (bytes from the 1024-aligned base)
 constexpr int oX = 0, oDY = kTile, oB = 2 * kTile, oC = 3 * kTile;
@@ -665,30 +666,15 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
     return v[0];
 }
 
-// Inclusive prefix sum over the 128 threads (warp_tot: 4 floats); every thread calls it.
-__device__ __forceinline__ float scan128(float v, float *warp_tot)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float t = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += t;
-    }
-    if (lane == 31) warp_tot[warp] = v;
-    __syncthreads();
-    for (int w = 0; w < warp; ++w) v += warp_tot[w];
-    __syncthreads();
-    return v;
-}
-
-// Sum over the 128 threads in a fixed order; every thread gets it.
-__device__ __forceinline__ float sum128(float v, float *warp_tot)
+// Sum over the 256 threads in a fixed order (warp_tot: 8 floats); every thread gets it.
+__device__ __forceinline__ float sum256(float v, float *warp_tot)
 {
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if ((threadIdx.x & 31) == 0) warp_tot[threadIdx.x >> 5] = v;
     __syncthreads();
-    const float s = (warp_tot[0] + warp_tot[1]) + (warp_tot[2] + warp_tot[3]);
+    const float s = ((warp_tot[0] + warp_tot[1]) + (warp_tot[2] + warp_tot[3])) +
+                    ((warp_tot[4] + warp_tot[5]) + (warp_tot[6] + warp_tot[7]));
     __syncthreads();
     return s;
 }
@@ -741,8 +727,9 @@ __global__ void __launch_bounds__(kTc, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_ld, bar_mma;
     __shared__ uint32_t tmem_slot;
-    __shared__ float warp_tot[4];
-    __shared__ float cs_s[kQ], dt_s[kQ], cum_s[kQ], row_s[kQ], zv_s[kQ], ddt_s[kQ];
+    __shared__ float warp_tot[8];
+    __shared__ float cs_s[kQ], dt_s[kQ], cum_s[kQ], z_s[kQ], zv_s[kQ], ddt_s[kQ];
+    __shared__ float row_s[2][kQ], diag_s[2][kQ];
     __shared__ float colp[4][kQ];
     __shared__ int s_fail;
 
@@ -750,6 +737,9 @@ __global__ void __launch_bounds__(kTc, 1)
     const int L = a.seqlen, H = a.nheads, G = a.ngroups, g = h / (H / G);
     const int t0 = c * kQ, len = min(kQ, L - t0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // warps w and w + 4 share TMEM lanes 32 (w & 3) .. (token rows i) and split the columns
+    const int quarter = warp & 3, half = warp >> 2;
+    const int i = quarter * 32 + lane;
     uint8_t *base = tile::align1024(smem_raw);
     const uint32_t sb = smem_u32(base);
     const size_t bh = (size_t)b * H + h;
@@ -768,7 +758,7 @@ __global__ void __launch_bounds__(kTc, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    const uint32_t lrow = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
+    const uint32_t lrow = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lanes
 
     if (tid == 0) {
         tma_prefetch_desc(&xmap);
@@ -782,20 +772,24 @@ __global__ void __launch_bounds__(kTc, 1)
         tma_load_3d(base + oC, &cmap, &bar_ld, g * kD, t0, b);
     }
 
-    // scalars of the chunk: cs (prefix of dt A), dt, cum (prefix of dt); 0 / constant past len
-    const float dtv = tid < len ? __ldg(a.dt + ((size_t)b * L + t0 + tid) * H + h) : 0.f;
-    const float cs_t = scan128(dtv * Ah, warp_tot);
-    const float cum_t = scan128(dtv, warp_tot);
-    cs_s[tid] = cs_t;
-    dt_s[tid] = dtv;
-    cum_s[tid] = cum_t;
+    // scalars of the chunk (threads 0..127 = tokens): cs (prefix of dt A), dt, cum (prefix of dt)
+    {
+        const float d = tid < len ? __ldg(a.dt + ((size_t)b * L + t0 + tid) * H + h) : 0.f;
+        const float cs_t = block_inclusive_scan_256(d * Ah, warp_tot);
+        const float cum_t = block_inclusive_scan_256(d, warp_tot);
+        if (tid < kQ) {
+            cs_s[tid] = cs_t;
+            dt_s[tid] = d;
+            cum_s[tid] = cum_t;
+        }
+    }
 
-    // h_c, g_c -> [64 p][64 n] hi / lo tiles (thread: row p = tid / 2, columns 32 (tid & 1) ...); <g_c, h_c>
+    // h_c, g_c -> [64 p][64 n] hi / lo tiles (row p = tid / 4, two 8-column chunks); <g_c, h_c>
     float u = 0.f;
     {
-        const int p = tid >> 1, q0 = (tid & 1) * 4;
+        const int p = tid >> 2, q0 = (tid & 3) * 2;
 #pragma unroll
-        for (int q = q0; q < q0 + 4; ++q) {
+        for (int q = q0; q < q0 + 2; ++q) {
             float hv[8], gv[8];
             const float4 *hp = reinterpret_cast<const float4 *>(hc + p * kD + 8 * q);
             const float4 *gp = reinterpret_cast<const float4 *>(gc + p * kD + 8 * q);
@@ -813,20 +807,26 @@ __global__ void __launch_bounds__(kTc, 1)
             *reinterpret_cast<uint4 *>(base + oGl + sw128(p, q)) = lo;
         }
     }
+    __syncthreads();  // the scalars are in shared memory
+    const float dti = dt_s[i];
     bool ok = mbar_wait(&bar_ld, 0);
-    // dt_j B_j -> hi / lo (row j = tid)
+    // dt_j B_j -> hi / lo (row i, the four 8-column chunks of this half)
     if (ok) {
-        float f[64];
-        load_row(base + oB, tid, f);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 4 * half; q < 4 * half + 4; ++q) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(base + oB + sw128(i, q));
+            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
             float v[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = dtv * f[8 * q + k];
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(b2[e]);
+                v[2 * e] = dti * f.x;
+                v[2 * e + 1] = dti * f.y;
+            }
             uint4 hi, lo;
             split8(v, hi, lo);
-            *reinterpret_cast<uint4 *>(base + oBh + sw128(tid, q)) = hi;
-            *reinterpret_cast<uint4 *>(base + oBl + sw128(tid, q)) = lo;
+            *reinterpret_cast<uint4 *>(base + oBh + sw128(i, q)) = hi;
+            *reinterpret_cast<uint4 *>(base + oBl + sw128(i, q)) = lo;
         }
     } else {
         s_fail = 1;
@@ -863,31 +863,34 @@ __global__ void __launch_bounds__(kTc, 1)
     tc_fence_after();
 
     // K = e o (dy x^T) -> hi / lo operand; W = e o (C B^T) o (dy x^T) dt_j below the diagonal:
-    // row sums here, column sums by a per-warp exchange; the diagonal of dy x^T gives dD's part
-    const int i = tid;
+    // row sums here, column sums by a per-warp exchange; the diagonal of dy x^T gives dD's part.
+    // This half: column blocks 2 half, 2 half + 1.
     const bool row_in = i < len;
-    float rs = 0.f, diag = 0.f;
-    if (ok) {
+    {
+        float rs = 0.f, diag = 0.f;
+        if (ok) {
 #pragma unroll 1
-        for (int jb = 0; jb < 4; ++jb) {
-            float dx[32], cb[32], e[32], w[32];
-            tmem_ld32(lrow + 32 * jb, dx);
-            tmem_ld32(lrow + 128 + 32 * jb, cb);
-            decay_row(cs_s, i, jb, row_in, e);
+            for (int jb = 2 * half; jb < 2 * half + 2; ++jb) {
+                float dx[32], cb[32], e[32], w[32];
+                tmem_ld32(lrow + 32 * jb, dx);
+                tmem_ld32(lrow + 128 + 32 * jb, cb);
+                decay_row(cs_s, i, jb, row_in, e);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const int j = 32 * jb + k;
-                if (j == i) diag = dx[k];
-                const float kv = e[k] * dx[k];
-                w[k] = j < i ? kv * cb[k] * dt_s[j] : 0.f;
-                rs += w[k];
-                dx[k] = kv;
+                for (int k = 0; k < 32; ++k) {
+                    const int j = 32 * jb + k;
+                    if (j == i) diag = dx[k];
+                    const float kv = e[k] * dx[k];
+                    w[k] = j < i ? kv * cb[k] * dt_s[j] : 0.f;
+                    rs += w[k];
+                    dx[k] = kv;
+                }
+                store_split32(base + oKh, base + oKl, i, jb, dx);
+                colp[quarter][32 * jb + lane] = reduce_scatter32(w, lane);
             }
-            store_split32(base + oKh, base + oKl, i, jb, dx);
-            colp[warp][32 * jb + lane] = reduce_scatter32(w, lane);
         }
+        row_s[half][i] = rs;
+        diag_s[half][i] = diag;
     }
-    row_s[i] = rs;
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -909,19 +912,19 @@ __global__ void __launch_bounds__(kTc, 1)
         }
         mma_commit(&bar_mma);
     }
-    // meanwhile: Z_i = dy_i . (C_i h^T) and V_j = dt_j x_j . (B_j g^T) from columns the MMAs above do not touch
-    float zi = 0.f, vj = 0.f;
+    // meanwhile, from columns the MMAs above do not touch: Z_i = dy_i . (C_i h^T) (first half),
+    // V_i = dt_i x_i . (B_i g^T) (second half)
     if (ok) {
         float r[64], f[64];
-        tmem_ld64(lrow + 256, r);
-        load_row(base + oDY, i, f);
+        tmem_ld64(lrow + (half == 0 ? 256 : 320), r);
+        load_row(base + (half == 0 ? oDY : oX), i, f);
+        float acc = 0.f;
 #pragma unroll
-        for (int k = 0; k < 64; ++k) zi = fmaf(f[k], r[k], zi);
-        tmem_ld64(lrow + 320, r);
-        load_row(base + oX, i, f);
-#pragma unroll
-        for (int k = 0; k < 64; ++k) vj = fmaf(f[k], r[k], vj);
-        vj *= dtv;
+        for (int k = 0; k < 64; ++k) acc = fmaf(f[k], r[k], acc);
+        if (half == 0)
+            z_s[i] = acc;
+        else
+            zv_s[i] = row_in ? expf(cs_s[len - 1] - cs_s[i]) * dti * acc : 0.f;  // e^{cs_end - cs_i} V_i
     }
     ok = ok && mbar_wait(&bar_mma, 1);
     ok = __all_sync(0xffffffffu, ok);
@@ -930,7 +933,7 @@ __global__ void __launch_bounds__(kTc, 1)
     // M = e o (C B^T) -> hi / lo over the K operand, then M^T dy
     if (ok) {
 #pragma unroll 1
-        for (int jb = 0; jb < 4; ++jb) {
+        for (int jb = 2 * half; jb < 2 * half + 2; ++jb) {
             float cb[32], e[32];
             tmem_ld32(lrow + 128 + 32 * jb, cb);
             decay_row(cs_s, i, jb, row_in, e);
@@ -957,23 +960,23 @@ __global__ void __launch_bounds__(kTc, 1)
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
 
-    // outputs of row j = tid: dB, dC (per head, or the group's when it has one head), dx, x . inner
-    const float cs_end = cs_s[len - 1];
-    const float eSj = row_in ? expf(cs_end - cs_t) : 0.f, eCj = row_in ? expf(cs_t) : 0.f;
-    const bool direct = a.dBp == nullptr;
-    float xin = 0.f;
-    if (ok) {
-        float acc[64], add[64];
+    // outputs of row i: dB and dC (first half; per head, or the group's when it has one
+    // head), dx and x . inner (second half)
+    const float cs_end = cs_s[len - 1], cs_i = cs_s[i];
+    const float eS = row_in ? expf(cs_end - cs_i) : 0.f, eC = row_in ? expf(cs_i) : 0.f;
+    if (ok && half == 0) {
+        const bool direct = a.dBp == nullptr;
         const size_t orow = (((size_t)b * L + t0 + i) * (direct ? G : H) + (direct ? g : h)) * kD;
+        float acc[64], add[64];
         tmem_ld64(lrow + 0, acc);
         tmem_ld64(lrow + 448, add);
         if (row_in) {
             float4 *o = reinterpret_cast<float4 *>((direct ? a.dB : a.dBp) + orow);
 #pragma unroll
             for (int q = 0; q < 16; ++q)
-                o[q] = make_float4(dtv * fmaf(eSj, add[4 * q], acc[4 * q]), dtv * fmaf(eSj, add[4 * q + 1], acc[4 * q + 1]),
-                                   dtv * fmaf(eSj, add[4 * q + 2], acc[4 * q + 2]),
-                                   dtv * fmaf(eSj, add[4 * q + 3], acc[4 * q + 3]));
+                o[q] = make_float4(dti * fmaf(eS, add[4 * q], acc[4 * q]), dti * fmaf(eS, add[4 * q + 1], acc[4 * q + 1]),
+                                   dti * fmaf(eS, add[4 * q + 2], acc[4 * q + 2]),
+                                   dti * fmaf(eS, add[4 * q + 3], acc[4 * q + 3]));
         }
         tmem_ld64(lrow + 64, acc);
         tmem_ld64(lrow + 384, add);
@@ -981,48 +984,51 @@ __global__ void __launch_bounds__(kTc, 1)
             float4 *o = reinterpret_cast<float4 *>((direct ? a.dC : a.dCp) + orow);
 #pragma unroll
             for (int q = 0; q < 16; ++q)
-                o[q] = make_float4(fmaf(eCj, add[4 * q], acc[4 * q]), fmaf(eCj, add[4 * q + 1], acc[4 * q + 1]),
-                                   fmaf(eCj, add[4 * q + 2], acc[4 * q + 2]), fmaf(eCj, add[4 * q + 3], acc[4 * q + 3]));
+                o[q] = make_float4(fmaf(eC, add[4 * q], acc[4 * q]), fmaf(eC, add[4 * q + 1], acc[4 * q + 1]),
+                                   fmaf(eC, add[4 * q + 2], acc[4 * q + 2]), fmaf(eC, add[4 * q + 3], acc[4 * q + 3]));
         }
+    } else if (ok) {
+        float acc[64], add[64], f[64];
         tmem_ld64(lrow + 128, acc);
         tmem_ld64(lrow + 320, add);
-        float f[64];
         const float Dh = a.D ? __ldg(a.D + h) : 0.f;
 #pragma unroll
-        for (int k = 0; k < 64; ++k) acc[k] = fmaf(eSj, add[k], acc[k]);  // inner_j
+        for (int k = 0; k < 64; ++k) acc[k] = fmaf(eS, add[k], acc[k]);  // inner_i
         load_row(base + oX, i, f);
+        float xin = 0.f;
 #pragma unroll
         for (int k = 0; k < 64; ++k) xin = fmaf(f[k], acc[k], xin);
+        ddt_s[i] = xin;
         load_row(base + oDY, i, f);
         if (row_in) {
             float4 *o = reinterpret_cast<float4 *>(a.dx + (((size_t)b * L + t0 + i) * H + h) * kD);
 #pragma unroll
             for (int q = 0; q < 16; ++q)
-                o[q] = make_float4(fmaf(Dh, f[4 * q], dtv * acc[4 * q]), fmaf(Dh, f[4 * q + 1], dtv * acc[4 * q + 1]),
-                                   fmaf(Dh, f[4 * q + 2], dtv * acc[4 * q + 2]),
-                                   fmaf(Dh, f[4 * q + 3], dtv * acc[4 * q + 3]));
+                o[q] = make_float4(fmaf(Dh, f[4 * q], dti * acc[4 * q]), fmaf(Dh, f[4 * q + 1], dti * acc[4 * q + 1]),
+                                   fmaf(Dh, f[4 * q + 2], dti * acc[4 * q + 2]),
+                                   fmaf(Dh, f[4 * q + 3], dti * acc[4 * q + 3]));
         }
     }
     tc_fence_before();
-    ddt_s[i] = xin;
-    zv_s[i] = eSj * vj;  // e^{cs_end - cs_j} V_j
     __syncthreads();
 
-    // dL/dcs_t, then ddt = x . inner + A sum_{t' >= t} dcs_t', and the dA / dD parts
-    const float colsum = (colp[0][i] + colp[1][i]) + (colp[2][i] + colp[3][i]);
-    const float ssum = sum128(row_in ? zv_s[i] : 0.f, warp_tot);  // sum_j e^{cs_end - cs_j} V_j
-    const float usum = sum128(u, warp_tot);
-    const float dsum = sum128(diag, warp_tot);
+    // dL/dcs_t (threads 0..127 = tokens t), then ddt = x . inner + A sum_{t' >= t} dcs_t' and the
+    // dA / dD parts; sums over all 256 threads in a fixed order (the second half adds zeros)
+    const bool tok = tid < kQ && tid < len;
+    const float zv = tok ? zv_s[tid] : 0.f;
+    const float ssum = sum256(zv, warp_tot);  // sum_j e^{cs_end - cs_j} V_j
+    const float usum = sum256(u, warp_tot);
+    const float dsum = sum256(tid < kQ ? diag_s[0][tid] + diag_s[1][tid] : 0.f, warp_tot);
     float d = 0.f;
-    if (row_in) {
-        d = row_s[i] - colsum + eCj * zi - zv_s[i];
-        if (i == len - 1) d += ssum + expf(cs_end) * usum;
+    if (tok) {
+        const float colsum = (colp[0][tid] + colp[1][tid]) + (colp[2][tid] + colp[3][tid]);
+        d = (row_s[0][tid] + row_s[1][tid]) - colsum + expf(cs_s[tid]) * z_s[tid] - zv;
+        if (tid == len - 1) d += ssum + expf(cs_end) * usum;
     }
-    // suffix sum: total - (inclusive prefix) + own
-    const float pre = scan128(d, warp_tot);
-    const float tot = sum128(d, warp_tot);
-    if (row_in && ok) a.ddt[((size_t)b * L + t0 + i) * H + h] = fmaf(Ah, tot - pre + d, ddt_s[i]);
-    const float da = sum128(d * cum_s[i], warp_tot);
+    const float pre = block_inclusive_scan_256(d, warp_tot);
+    const float tot = sum256(d, warp_tot);
+    if (tok && ok) a.ddt[((size_t)b * L + t0 + tid) * H + h] = fmaf(Ah, tot - pre + d, ddt_s[tid]);
+    const float da = sum256(tid < kQ ? d * cum_s[tid] : 0.f, warp_tot);
     if (tid == 0 && ok) {
         const size_t o = ((size_t)b * a.nchunks + c) * H + h;
         a.dAp[o] = da;
