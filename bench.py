@@ -586,6 +586,19 @@ def bwd_unavoidable_bytes(w):
     return ins + outs + states + 4 * w.nheads * 4
 
 
+def bwd_chunk_bytes(w, q):
+    """Bytes the in-chunk backward kernel must move per launch: x, dy, B, C and dt
+    in, one recomputed and one adjoint fp32 state per (batch, head, q-token chunk)
+    in, dx, ddt, dB and dC (fp32) out."""
+    e = 2 if w.dtype == "bf16" else 4
+    tok = w.batch * w.seqlen
+    nc = math.ceil(w.seqlen / q)
+    ins = 2 * tok * w.nheads * w.headdim * e + 2 * tok * w.ngroups * w.dstate * e + tok * w.nheads * 4
+    states = 2 * w.batch * w.nheads * nc * w.headdim * w.dstate * 4
+    outs = tok * w.nheads * w.headdim * 4 + tok * w.nheads * 4 + 2 * tok * w.ngroups * w.dstate * 4
+    return ins + states + outs
+
+
 def backward_measurement(w, dev, stream, peaks, steps=20):
     """The backward (ssd_bwd) on the workload: ms per step over a CUDA graph of
     ``steps`` backward calls rotating over input sets larger than L2, each
@@ -628,19 +641,30 @@ def backward_measurement(w, dev, stream, peaks, steps=20):
     flops = bwd_flops(w)
     # the in-chunk kernel's share of the FLOPs: everything but the two chunk states
     states_flops = 4 * w.batch * w.seqlen * w.nheads * w.headdim * w.dstate
-    kflops = {"bwd_chunk": flops - states_flops, "bwd_chunk_states": states_flops}
+    kflops = {"bwd_chunk": flops - states_flops, "bwd_chunk_tc": flops - states_flops,
+              "bwd_chunk_states": states_flops}
     alu_peak = fp32_fma_peak_tflops(peaks)
     t_hbm = per_set / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    # a kernel that runs twice in a step (the chunk-state kernel: S_c, then G_c) is listed as name#2
+    keys = [n if names[:k].count(n) == 0 else f"{n}#{names[:k].count(n) + 1}" for k, n in enumerate(names)]
     rec = {"workload": w.name, "ms_per_step": ms, "tokens_per_s": w.tokens / (ms * 1e-3), "steps": steps,
-           "kernels": {names[i]: {"ms_per_launch": pk[i], "share": pk[i] / (sum(pk) or 1.0)}
+           "kernels": {keys[i]: {"ms_per_launch": pk[i], "share": pk[i] / (sum(pk) or 1.0)}
                        for i in range(len(names))},
            "kernel_timing": how,
            "step_roofline": {"unavoidable_bytes": per_set, "algorithmic_flops": flops,
                              "roofline_ms": max(t_hbm, t_tc) * 1e3, "bound": "hbm" if t_hbm >= t_tc else "tensor",
                              "frac": max(t_hbm, t_tc) * 1e3 / ms},
            "l2": f"inputs rotate over {nsets} device copies ({nsets * per_set / 2**20:.0f} MiB > 126 MB L2)"}
-    if names[dom] in kflops:
+    if names[dom] == "bwd_chunk_tc":
+        # tensor cores: its FLOPs take ~8 us at the bf16 peak, so the bound is its bytes
+        nbytes = bwd_chunk_bytes(w, 128)
+        ach = nbytes / (pk[dom] * 1e-3) / 1e9
+        rec["roofline"] = {"bound": "hbm", "kernel": names[dom], "achieved": ach, "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": recorded_traffic(names[dom]),
+                           "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": kflops[names[dom]],
+                           "launch_ms": pk[dom], "peak_source": "measured (copy bandwidth)"}
+    elif names[dom] in kflops:
         ach = kflops[names[dom]] / (pk[dom] * 1e-3) / 1e12
         rec["roofline"] = {"bound": "alu", "kernel": names[dom], "achieved": ach, "peak": alu_peak,
                            "unit": "TFLOP/s", "frac": ach / alu_peak, "traffic": recorded_traffic(names[dom]),

@@ -96,9 +96,7 @@ __device__ __forceinline__ void chunk_scalars(const BwdArgs &a, int b, int h, in
 // 1. S_c[p][n] = sum_j e^{cs_end - cs_j} dt_j x_j[p] B_j[n] and
 //    G_c[p][n] = sum_i e^{cs_i} dy_i[p] C_i[n], kNT state columns per pass.
 //    Thread (ty, tx) owns rows p = ty + 16 a and columns n = tx + 16 q.
-// kWithS false: G_c only (S_c and the decays come from the forward's tcgen05
-// chunk-state kernel).
-template <typename T, int MP, int Q, bool kWithS = true>
+template <typename T, int MP, int Q>
 __global__ void __launch_bounds__(kThreads) bwd_chunk_states(BwdArgs a)
 {
     extern __shared__ float sm[];
@@ -123,7 +121,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_states(BwdArgs a)
     chunk_scalars<Q>(a, b, h, t0, len, cs_s, dt_s, cum_s, warp_tot);
     const float cs_end = cs_s[len - 1];
     const size_t bh = (size_t)b * H + h;
-    if (kWithS && tid == 0) a.decay[bh * a.nchunks + c] = expf(cs_end);
+    if (tid == 0) a.decay[bh * a.nchunks + c] = expf(cs_end);
     float *S = a.hs + (bh * a.nchunks + c) * (size_t)P * N;
     float *Gc = a.gs + (bh * a.nchunks + c) * (size_t)P * N;
     for (int n0 = 0; n0 < N; n0 += kNT) {
@@ -143,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_states(BwdArgs a)
                 if (t < kn && p < P) {
                     const int tc = k0 + t;
                     const size_t i = (((size_t)b * L + t0 + tc) * H + h) * P + p;
-                    if (kWithS) xv = load_el(x, i) * (expf(cs_end - cs_s[tc]) * dt_s[tc]);
+                    xv = load_el(x, i) * (expf(cs_end - cs_s[tc]) * dt_s[tc]);
                     yv = load_el(dy, i) * expf(cs_s[tc]);
                 }
                 xs[e] = xv;
@@ -177,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_states(BwdArgs a)
                 for (int i = 0; i < MP; ++i)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        if (kWithS) accS[i][q] = fmaf(xv[i], bv[q], accS[i][q]);
+                        accS[i][q] = fmaf(xv[i], bv[q], accS[i][q]);
                         accG[i][q] = fmaf(yv[i], cv[q], accG[i][q]);
                     }
             }
@@ -190,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_states(BwdArgs a)
             for (int q = 0; q < 4; ++q) {
                 const int n = n0 + tx + 16 * q;
                 if (n < N) {
-                    if (kWithS) S[(size_t)p * N + n] = accS[i][q];
+                    S[(size_t)p * N + n] = accS[i][q];
                     Gc[(size_t)p * N + n] = accG[i][q];
                 }
             }
@@ -1108,7 +1106,7 @@ cudaError_t launch_bwd_tc(const BwdArgs &a, cudaStream_t s)
     const size_t s1 = chunk_states_smem<4, tcb::kQ>();
     if (H % 2 == 0 && (H / G) % 2 == 0) {
         // S_c and the chunk decays are exactly the forward's chunk-state product: on
-        // tcgen05 (its head pairs lie inside one group); G_c on the fp32 kernel
+        // tcgen05 (its head pairs lie inside one group); G_c too, with other weights
         Problem fp;
         memset(&fp, 0, sizeof fp);
         fp.x = a.x;
@@ -1130,18 +1128,17 @@ cudaError_t launch_bwd_tc(const BwdArgs &a, cudaStream_t s)
         fws.states = a.hs;
         fws.decay = a.decay;
         if ((e = launch_chunk_state_tc(fp, fws, s)) != cudaSuccess) return e;
-        if ((e = ensure_smem_limit((const void *)bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ, false>, s1)) !=
-            cudaSuccess)
-            return e;
-        profile_kernel_begin(s);
-        bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ, false><<<grid, kThreads, s1, s>>>(a);
-        profile_kernel_end(s);
+        // G_c = sum_i e^{cs_i} dy_i C_i^T: the same product with dy, C and the weights e^{cs_i}
+        fp.x = a.dy;
+        fp.B = a.C;
+        fp.adjoint_states = 1;
+        fws.states = a.gs;
+        if ((e = launch_chunk_state_tc(fp, fws, s)) != cudaSuccess) return e;
     } else {  // both state sums on the fp32 kernel
-        if ((e = ensure_smem_limit((const void *)bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ, true>, s1)) !=
-            cudaSuccess)
+        if ((e = ensure_smem_limit((const void *)bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ>, s1)) != cudaSuccess)
             return e;
         profile_kernel_begin(s);
-        bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ, true><<<grid, kThreads, s1, s>>>(a);
+        bwd_chunk_states<__nv_bfloat16, 4, tcb::kQ><<<grid, kThreads, s1, s>>>(a);
         profile_kernel_end(s);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1202,8 +1199,8 @@ const char *bwd_kernel_names(const BwdProblem &p)
 {
     if (fwd_states(p))
         return p.nheads != p.ngroups
-                   ? "chunk_state_tc,bwd_chunk_states,bwd_state_pass,bwd_chunk_tc,bwd_reduce_groups,bwd_reduce_heads"
-                   : "chunk_state_tc,bwd_chunk_states,bwd_state_pass,bwd_chunk_tc,bwd_reduce_heads";
+                   ? "chunk_state_tc,chunk_state_tc,bwd_state_pass,bwd_chunk_tc,bwd_reduce_groups,bwd_reduce_heads"
+                   : "chunk_state_tc,chunk_state_tc,bwd_state_pass,bwd_chunk_tc,bwd_reduce_heads";
     if (use_tc(p))
         return p.nheads != p.ngroups
                    ? "bwd_chunk_states,bwd_state_pass,bwd_chunk_tc,bwd_reduce_groups,bwd_reduce_heads"

@@ -73,6 +73,9 @@ struct Problem {
     // workspace) whose look-back publications are withheld (-1: none).
     unsigned long long wait_ns;
     long long withhold;
+    // chunk_state_tc only: 1 computes the backward's adjoint chunk states
+    // G_c = sum_j exp(cs_j) x_j B_j^T (x, B given as dy, C) and leaves the decays alone.
+    int adjoint_states;
 };
 
 // Workspace carved out of one device buffer.

@@ -180,9 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     for (int e = tid; e < HB * 256; e += kThreads) {
         const int j = e & 255;
-        wts[e] = j < len ? expf((e < 256 ? cl0 : cl1) - cs[e]) * dtv[e] : 0.f;
+        wts[e] = j >= len ? 0.f : pr.adjoint_states ? expf(cs[e]) : expf((e < 256 ? cl0 : cl1) - cs[e]) * dtv[e];
     }
-    if (tid < HB) ws.decay[state_slot(pr, ref, h0 + tid)] = expf(tid == 0 ? cl0 : cl1);
+    if (tid < HB && !pr.adjoint_states) ws.decay[state_slot(pr, ref, h0 + tid)] = expf(tid == 0 ? cl0 : cl1);
     __syncthreads();
 
     bool ok = true;

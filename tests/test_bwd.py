@@ -130,7 +130,7 @@ def test_per_kernel_timing_hook_outside_capture():
 def test_tensor_core_kernel_is_the_one_that_runs():
     assert "bwd_chunk_tc" in ssd.ssd_bwd_kernels(2, 300, 8, 64, 2, 64, torch.bfloat16)
     assert ssd.ssd_bwd_kernels(2, 2048, 80, 64, 1, 64, torch.bfloat16) == [
-        "chunk_state_tc", "bwd_chunk_states", "bwd_state_pass", "bwd_chunk_tc", "bwd_reduce_groups", "bwd_reduce_heads"]
+        "chunk_state_tc", "chunk_state_tc", "bwd_state_pass", "bwd_chunk_tc", "bwd_reduce_groups", "bwd_reduce_heads"]
     # one head per group: the head pairs of the forward's chunk-state kernel straddle groups
     assert ssd.ssd_bwd_kernels(1, 128, 4, 64, 4, 64, torch.bfloat16) == [
         "bwd_chunk_states", "bwd_state_pass", "bwd_chunk_tc", "bwd_reduce_heads"]
