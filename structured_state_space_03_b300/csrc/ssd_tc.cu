@@ -98,6 +98,22 @@ __device__ __forceinline__ void segsum(const Problem &pr, int b, int h0, int nh,
     __syncthreads();
 }
 
+// segsum over a 256-thread block: thread t holds token t.  warp_tot: 8 floats.
+__device__ __forceinline__ void segsum256(const Problem &pr, int b, int h0, int nh, int t0, int len, float scale,
+                                          float *cs, float *dtv, float *warp_tot)
+{
+    const int t = threadIdx.x;
+    for (int hh = 0; hh < nh; ++hh) {
+        const int h = h0 + hh;
+        const float a = __ldg(pr.A + h) * scale;
+        const float d = t < len ? __ldg(pr.dt + ((size_t)b * pr.seqlen + t0 + t) * pr.nheads + h) : 0.f;
+        cs[hh * 256 + t] = block_inclusive_scan_256(d * a, warp_tot);
+        dtv[hh * 256 + t] = pr.dtin ? (t < len ? __ldg(pr.dtin + ((size_t)b * pr.seqlen + t0 + t) * pr.nheads + h) : 0.f)
+                                    : d;
+    }
+    __syncthreads();
+}
+
 // Pack 8 floats into 8 bf16 (one 16-byte chunk).
 __device__ __forceinline__ uint4 pack8(const float *f)
 {
@@ -263,15 +279,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // tile spans 128 columns, 80 KiB when it spans 256.
 __host__ __device__ constexpr int region1_bytes(int jmax) { return jmax > 128 ? 80 * 1024 : 64 * 1024; }
 
+constexpr int kOutThreads = 256;  // chunk_out_tc: warps w and w + 4 share TMEM lanes 32 (w & 3) ..
+
 template <int NS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kOutThreads, 1)
     chunk_out_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
                  const __grid_constant__ CUtensorMap cmap, Problem pr, Workspace ws)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_tma, bar_x, bar_mma;
     __shared__ uint32_t tmem_slot;
-    __shared__ float warp_tot[4];
+    __shared__ float warp_tot[8];
     __shared__ float cs[2 * 256], dtv[2 * 256];
     __shared__ int s_fail;
 
@@ -291,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t col_yd = wide ? 256 : 0;       // narrow tiles reuse G's columns once S is built
     const uint32_t col_yo = wide ? 384 : 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;  // TMEM lanes 32 quarter ..; half of the columns
 
     uint8_t *base = align1024(smem_raw);
     const int jmax = pr.chunk <= kBoxRows ? kBoxRows : 2 * kBoxRows;
@@ -324,10 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(xs + k * jn * 128 + r * kBoxBytes, &xmap, &bar_x, hb * 128 + 64 * k, t0 + r * kBoxRows,
                             b);
     }
-    segsum(pr, b, h0, HB, t0, len, kLog2e, cs, dtv, warp_tot);  // log2 domain: decays via exp2f
+    segsum256(pr, b, h0, HB, t0, len, kLog2e, cs, dtv, warp_tot);  // log2 domain: decays via exp2f
 
     // ---- phase 1: G = C_i B^T and Yoff = C_i h_c^T, over 64-wide slabs of the state dimension
-    const int m = tid;  // h-slab row (h, p) written by this thread
+    const int m = tid & 127;  // h-slab row (h, p) written by this thread (chunks 4 half .. 4 half + 3)
     const float *hsrc = ws.states + state_slot(pr, ref, h0 + m / P) * (size_t)P * NS + (size_t)(m % P) * NS;
     bool ok = true;
     for (int s = 0; s < NS / 64 && ok; ++s) {
@@ -341,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             const float4 *src = reinterpret_cast<const float4 *>(hsrc + 64 * s);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
+            for (int q = 4 * half; q < 4 * half + 4; ++q) {
                 const float4 a = __ldg(src + 2 * q), bq = __ldg(src + 2 * q + 1);
                 const float f[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
                 const uint4 hi = pack8(f);
@@ -388,15 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
 
     // ---- phase 2: S_h = G o decay o dt (causal) -> bf16; Ydiag_h = S_h x_h
-    const int i = warp * 32 + lane;       // accumulator row of this thread
+    const int i = quarter * 32 + lane;    // accumulator row of this thread
     const int ia = i0 + i;                // row within the chunk
     const bool row_ok = ia < len;
     const int heads_per_pass = wide ? 1 : HB;
     for (int hp0 = 0; hp0 < HB && ok; hp0 += heads_per_pass) {
-        for (int jb = 0; jb < jn / 32; ++jb) {
+        const int njb = jn / 32;  // 32-column blocks, the first half of them for warps 0-3
+        for (int jb = half * (njb / 2); jb < (half + 1) * (njb / 2); ++jb) {
             uint8_t *dst_base = r1;
             const int j0 = jb * 32;
-            if (j0 > i0 + warp * 32 + 31) {  // whole warp above the diagonal: zeros
+            if (j0 > i0 + quarter * 32 + 31) {  // whole warp above the diagonal: zeros
                 const uint4 z = make_uint4(0, 0, 0, 0);
                 for (int hh = hp0; hh < hp0 + heads_per_pass; ++hh) {
                     uint8_t *st = dst_base + (hh - hp0) * (jn * 256) + (j0 / 64) * kBoxBytes;
@@ -406,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             float gv[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + col_g + j0, gv);
+            tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col_g + j0, gv);
             for (int hh = hp0; hh < hp0 + heads_per_pass; ++hh) {
                 const float *csh = cs + hh * 256, *dth = dtv + hh * 256;
                 const float ci = csh[ia < 256 ? ia : 255];
@@ -455,13 +475,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- phase 3: y = Ydiag + exp(cs_i) Yoff + D x
     if (ok && !mbar_wait(&bar_x, 0)) ok = false;  // x tile (already complete) visible to every thread
     if (ok) {
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         for (int hh = 0; hh < HB; ++hh) {
             const int h = h0 + hh;
             const float e = exp2f(cs[hh * 256 + (ia < 256 ? ia : 255)]);
             const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
             __nv_bfloat16 *yrow = static_cast<__nv_bfloat16 *>(pr.y) + (((size_t)b * L + t0 + ia) * H + h) * P;
-            for (int p0 = 0; p0 < P; p0 += 32) {
+            for (int p0 = half * (P / 2); p0 < (half + 1) * (P / 2); p0 += 32) {
                 float yd[32], yo[32];
                 tmem_ld32(tmem + lane_base + col_yd + hh * P + p0, yd);
                 tmem_ld32(tmem + lane_base + col_yo + hh * P + p0, yo);
@@ -555,7 +575,7 @@ cudaError_t launch_tc(const Problem &pr, const Workspace &ws, cudaStream_t s, in
         const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
         const dim3 grid(ncx * ntile, pr.nheads / HB, mb);
         profile_kernel_begin(s);
-        chunk_out_tc<NS><<<grid, kThreads, smem, s>>>(xmap, bmap, cmap, pr, ws);
+        chunk_out_tc<NS><<<grid, kOutThreads, smem, s>>>(xmap, bmap, cmap, pr, ws);
         profile_kernel_end(s);
     }
     return cudaGetLastError();
