@@ -20,6 +20,8 @@
 namespace ssd {
 namespace {
 
+constexpr int kStepV = 2;  // float4s of state per thread at large batch
+
 template <typename T>
 __device__ __forceinline__ float to_f(T v);
 template <>
@@ -83,7 +85,12 @@ __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16 *p, flo
     v[0] = a.x, v[1] = a.y, v[2] = b.x, v[3] = b.y;
 }
 
-template <typename T>
+// V float4s of one row per thread (4 V states), interleaved: thread q of the row
+// owns float4s q, q + t, ..., t = 2^lg threads per row, dstate = 4 V t, so every
+// load and store instruction of a warp is contiguous.  All V state loads are
+// issued before any is used: each thread keeps 16 V bytes of the state stream
+// in flight.
+template <typename T, int V>
 __global__ void __launch_bounds__(256) ssd_step_vec_kernel(const T *__restrict__ x, const float *__restrict__ dt,
                                                            const float *__restrict__ A, const T *__restrict__ B,
                                                            const T *__restrict__ C, const float *__restrict__ D,
@@ -91,32 +98,50 @@ __global__ void __launch_bounds__(256) ssd_step_vec_kernel(const T *__restrict__
                                                            int H, int P, int G, int lg)
 {
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const int q = (int)(gid & ((1 << lg) - 1));  // which 4 states of the row
+    const int q = (int)(gid & ((1 << lg) - 1));  // which 4 V states of the row
     const long long row = gid >> lg;             // (b, h, p)
     const long long rows = (long long)batch * H * P;
     const bool live = row < rows;
     const long long r = live ? row : rows - 1;   // dead threads still join the shuffles
-    const int N = 4 << lg;
+    const int N = (4 * V) << lg;
     const int h = (int)((r / P) % H);
     const int b = (int)(r / ((long long)P * H));
     const int g = h / (H / G);
+    const int tpr = 1 << lg;  // threads per row
+    float4 *sp = reinterpret_cast<float4 *>(state + (size_t)r * N) + q;
+    float4 sv[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) sv[k] = __ldcs(sp + k * tpr);
     const float d = __ldg(dt + (size_t)b * H + h);
     const float a = expf(d * __ldg(A + h));
     const float xv = to_f(x[r]);
     const float dx = d * xv;
-    float bv[4], cv[4];
-    load4<T>(B + ((size_t)b * G + g) * N + 4 * q, bv);
-    load4<T>(C + ((size_t)b * G + g) * N + 4 * q, cv);
-    float4 *sp = reinterpret_cast<float4 *>(state + (size_t)r * N) + q;
-    float4 sv = __ldcs(sp);
-    sv.x = fmaf(a, sv.x, dx * bv[0]);
-    sv.y = fmaf(a, sv.y, dx * bv[1]);
-    sv.z = fmaf(a, sv.z, dx * bv[2]);
-    sv.w = fmaf(a, sv.w, dx * bv[3]);
-    if (live) __stcs(sp, sv);
-    float acc = fmaf(cv[0], sv.x, fmaf(cv[1], sv.y, fmaf(cv[2], sv.z, cv[3] * sv.w)));
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+        float bv[4], cv[4];
+        load4<T>(B + ((size_t)b * G + g) * N + 4 * (q + k * tpr), bv);
+        load4<T>(C + ((size_t)b * G + g) * N + 4 * (q + k * tpr), cv);
+        sv[k].x = fmaf(a, sv[k].x, dx * bv[0]);
+        sv[k].y = fmaf(a, sv[k].y, dx * bv[1]);
+        sv[k].z = fmaf(a, sv[k].z, dx * bv[2]);
+        sv[k].w = fmaf(a, sv[k].w, dx * bv[3]);
+        if (live) __stcs(sp + k * tpr, sv[k]);
+        acc = fmaf(cv[0], sv[k].x, fmaf(cv[1], sv[k].y, fmaf(cv[2], sv[k].z, fmaf(cv[3], sv[k].w, acc))));
+    }
     for (int o = 1; o < (1 << lg); o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (live && q == 0) y[r] = from_f<T>(acc + (D ? __ldg(D + h) * xv : 0.f));
+}
+
+template <typename T, int V>
+void launch_vec(const void *x, const float *dt, const float *A, const void *B, const void *C, const float *D,
+                float *state, void *y, int batch, int nheads, int headdim, int ngroups, int lg, cudaStream_t s)
+{
+    const long long threads = ((long long)batch * nheads * headdim) << lg;
+    const unsigned grid = (unsigned)((threads + 255) / 256);
+    ssd_step_vec_kernel<T, V><<<grid, 256, 0, s>>>(static_cast<const T *>(x), dt, A, static_cast<const T *>(B),
+                                                   static_cast<const T *>(C), D, state, static_cast<T *>(y), batch,
+                                                   nheads, headdim, ngroups, lg);
 }
 
 }  // namespace
@@ -126,27 +151,28 @@ cudaError_t launch_step(const void *x, const float *dt, const float *A, const vo
                         int dstate, ssd_dtype_t dtype, cudaStream_t s)
 {
     const long long rows = (long long)batch * nheads * headdim;
+    // V float4s of state per thread: more bytes in flight per thread when there are
+    // enough rows to fill the GPU anyway (one float4 per thread for small batches)
+    const int V = (rows * dstate / 4 >= (1ll << 20) && dstate >= 4 * kStepV) ? kStepV : 1;
     int lg = -1;
     for (int k = 0; k <= 5; ++k)
-        if (dstate == (4 << k)) lg = k;
-    if (lg >= 0 && (reinterpret_cast<uintptr_t>(state) & 15) == 0 &&
-        (reinterpret_cast<uintptr_t>(B) & 7) == 0 && (reinterpret_cast<uintptr_t>(C) & 7) == 0) {
-        const long long threads = rows << lg;
-        const unsigned grid = (unsigned)((threads + 255) / 256);
-        if (dtype == SSD_DTYPE_BF16)
-            ssd_step_vec_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-                static_cast<const __nv_bfloat16 *>(x), dt, A, static_cast<const __nv_bfloat16 *>(B),
-                static_cast<const __nv_bfloat16 *>(C), D, state, static_cast<__nv_bfloat16 *>(y), batch, nheads,
-                headdim, ngroups, lg);
-        else if ((reinterpret_cast<uintptr_t>(B) & 15) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0)
-            ssd_step_vec_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(x), dt, A,
-                                                            static_cast<const float *>(B),
-                                                            static_cast<const float *>(C), D, state,
-                                                            static_cast<float *>(y), batch, nheads, headdim, ngroups,
-                                                            lg);
+        if (dstate == ((4 * V) << k)) lg = k;
+    const bool al = (reinterpret_cast<uintptr_t>(state) & 15) == 0 && (reinterpret_cast<uintptr_t>(B) & 7) == 0 &&
+                    (reinterpret_cast<uintptr_t>(C) & 7) == 0;
+    if (lg >= 0 && al && dtype == SSD_DTYPE_BF16) {
+        if (V == 1)
+            launch_vec<__nv_bfloat16, 1>(x, dt, A, B, C, D, state, y, batch, nheads, headdim, ngroups, lg, s);
         else
-            lg = -1;
-        if (lg >= 0) return cudaGetLastError();
+            launch_vec<__nv_bfloat16, kStepV>(x, dt, A, B, C, D, state, y, batch, nheads, headdim, ngroups, lg, s);
+        return cudaGetLastError();
+    }
+    if (lg >= 0 && al && dtype == SSD_DTYPE_F32 && (reinterpret_cast<uintptr_t>(B) & 15) == 0 &&
+        (reinterpret_cast<uintptr_t>(C) & 15) == 0) {
+        if (V == 1)
+            launch_vec<float, 1>(x, dt, A, B, C, D, state, y, batch, nheads, headdim, ngroups, lg, s);
+        else
+            launch_vec<float, kStepV>(x, dt, A, B, C, D, state, y, batch, nheads, headdim, ngroups, lg, s);
+        return cudaGetLastError();
     }
     const unsigned grid = (unsigned)((rows + 7) / 8);  // 8 rows (warps) per block
     if (dtype == SSD_DTYPE_BF16)
