@@ -29,12 +29,17 @@
 //   ddt_u   = x_u . inner_u + A sum_{t >= u} dcs_t,   dA = sum_t dcs_t sum_{u <= t} dt_u,
 //   dD      = sum dy . x
 //
-// Kernels (all fp32 FMA; one CTA of 256 threads per (chunk, head, batch)):
-//   1. bwd_chunk_states  S_c, G_c and the chunk decays
+// Kernels (one CTA per (chunk, head, batch) unless noted):
+//   1. chunk states      bf16 / headdim 64 / dstate 64 (128-token chunks): S_c and
+//                        the decays by the forward's tcgen05 chunk-state kernel,
+//                        then G_c by the same kernel with dy, C and weights e^{cs_j}
+//                        (when its head pairs lie inside one group); otherwise
+//                        bwd_chunk_states, fp32 FMA (64-token chunks)
 //   2. bwd_state_pass    h_c forward and g_c backward over the chunks, dinit
-//   3. bwd_chunk         the in-chunk terms above, dx, ddt, per-head dB / dC,
+//   3. bwd_chunk_tc      the in-chunk terms on tcgen05 (bf16 / headdim 64 /
+//      or bwd_chunk      dstate 64), else on fp32 FMA: dx, ddt, per-head dB / dC,
 //                        per-chunk dA / dD parts
-//   4. bwd_reduce        dB / dC over the heads of a group (when a group has
+//   4. bwd_reduce_*      dB / dC over the heads of a group (when a group has
 //                        more than one head), dA / dD over batch and chunks
 // Every reduction runs in a fixed order, so results are bitwise reproducible.
 #include <algorithm>
