@@ -465,6 +465,58 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_before();
     __syncthreads();
 
+    if constexpr (NS == 128) {
+        // ---- wx = v dt x for all 128 tokens at once: hi in place over x, lo over the
+        // h operand region (unused until the look-back); then every chunk-state and
+        // diagonal-block MMA in one batch.  x itself comes back by TMA for the D x term.
+        uint8_t *wlo = hh_s;
+        if (ok) {
+#pragma unroll 2
+            for (int r = 0; r < (2 * kRows * 8) / kThreads; ++r) {
+                const int idx = tid + kThreads * r;  // 16-byte chunk: (64-column block, token, 8 columns)
+                const int mb = idx >> 10, j = (idx >> 3) & 127, qq = idx & 7;
+                const float w = vw[(P == 64 ? mb : 0) * kRows + j];
+                uint4 *ptr = reinterpret_cast<uint4 *>(xs + mb * kSlab + sw128(j, qq));
+                const uint4 xv = *ptr;
+                const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                float f[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 t = __bfloat1622float2(x2[u]);
+                    f[2 * u] = t.x * w;
+                    f[2 * u + 1] = t.y * w;
+                }
+                uint4 hi, lo;
+                split8(f, hi, lo);
+                *ptr = hi;
+                *reinterpret_cast<uint4 *>(wlo + mb * kSlab + sw128(j, qq)) = lo;
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
+        if (ok && tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_s = idesc_bf16(128, NS, 1, 1);
+            constexpr uint32_t id_d = idesc_bf16(128, 128, 0, 1);
+            for (int k = 0; k < kRows / 16; ++k) {
+                const uint64_t whi = sdesc_sw128(smem_u32(xs) + k * 2048, kSlab, 1024);
+                const uint64_t wlw = sdesc_sw128(smem_u32(wlo) + k * 2048, kSlab, 1024);
+                const uint64_t bd = sdesc_sw128(smem_u32(bs) + k * 2048, kSlab, 1024);
+                mma_bf16(tmem + col_st, whi, bd, id_s, k > 0);
+                mma_bf16(tmem + col_st, wlw, bd, id_s, 1);
+                if (fast) {
+                    const uint32_t goff = (k >> 2) * kSlab + (k & 3) * 32;
+                    const uint64_t ad = sdesc_sw128(smem_u32(cm) + goff, 16, 1024);
+                    const uint64_t adl = sdesc_sw128(smem_u32(gl) + goff, 16, 1024);
+                    mma_bf16(tmem + col_y, ad, whi, id_d, k > 0);
+                    mma_bf16(tmem + col_y, ad, wlw, id_d, 1);
+                    mma_bf16(tmem + col_y, adl, whi, id_d, 1);
+                }
+            }
+            mma_commit(&bar_empty[0]);
+        }
+        if (ok && !mbar_wait(&bar_empty[0], 0, lim)) s_fail = 1;
+    } else {
     // ---- eight 16-token steps through a 3-buffer ring: every thread builds its
     // 16-byte chunk of wx (hi, lo) for step k, each warp then arrives once on
     // full[k % 3]; after its own chunk thread 0 issues step k-1 (S_c += wx^T B ;
@@ -526,12 +578,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (good && !mbar_wait(&bar_empty[1], 0, lim)) good = false;
         if (!good) s_fail = 1;
     }
+    }
     __syncthreads();
     ok = !s_fail;
     tc_fence_after();
-    if (ok && fast && tid == 0) {  // B is consumed: bring C back for the off-diagonal product
-        mbar_expect_tx(&bar_c, (uint32_t)(NSL * kSlab));
+    // x for the D x term: over wx hi for dstate 128, so it comes back (into the dead
+    // tril(G) lo region) with C, which the off-diagonal product needs where B was
+    uint8_t *xe = NS == 128 ? gl : xs;
+    if (ok && fast && tid == 0) {
+        mbar_expect_tx(&bar_c, (uint32_t)((NSL + (NS == 128 ? 2 : 0)) * kSlab));
         for (int s = 0; s < NSL; ++s) tma_load_3d(bs + s * kSlab, &cmap, &bar_c, g * NS + 64 * s, tt, tb);
+        if (NS == 128)
+            for (int k = 0; k < 2; ++k) tma_load_3d(xe + k * kSlab, &xmap, &bar_c, hb * 128 + 64 * k, tt, tb);
     }
 
     // ---- state passing by decoupled look-back; this thread: row m = (head, headdim),
@@ -735,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint4 outv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const uint4 xv = *reinterpret_cast<const uint4 *>(xs + half * kSlab + sw128(i, pc / 8 + u));
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xe + half * kSlab + sw128(i, pc / 8 + u));
                 const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
                 float o[8];
 #pragma unroll
