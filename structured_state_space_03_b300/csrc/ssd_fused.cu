@@ -130,20 +130,6 @@ __device__ __forceinline__ void split8(const float *f, uint4 &hi, uint4 &lo)
     lo = pack8(r);
 }
 
-// acc += s * src[0..32) (src read through L2)
-__device__ __forceinline__ void fma_row32(float (&acc)[32], float s, const float *src, int qstride = 1)
-{
-    const float4 *s4 = reinterpret_cast<const float4 *>(src);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float4 v = __ldcg(s4 + q * qstride);
-        acc[4 * q] = fmaf(s, v.x, acc[4 * q]);
-        acc[4 * q + 1] = fmaf(s, v.y, acc[4 * q + 1]);
-        acc[4 * q + 2] = fmaf(s, v.z, acc[4 * q + 2]);
-        acc[4 * q + 3] = fmaf(s, v.w, acc[4 * q + 3]);
-    }
-}
-
 // A unit's aggregate (inclusive) state is published once its aggcnt (inclcnt)
 // reaches the CTA's thread count: every thread adds 1 with release semantics
 // after writing its own part, so an acquiring reader that sees the full count
@@ -258,8 +244,10 @@ __device__ void direct_unit_tmem(const Problem &pr, size_t tok0, int len, int h0
     }
 }
 
+// One CTA per SM: its shared memory (137 KiB at dstate 64, 217 KiB at 128) leaves
+// no room for a second, so the registers are not capped for one.
 template <int NS, bool kPacked>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
                  const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap, Problem pr,
                  FusedArgs fa)
@@ -671,12 +659,27 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float a_own = s_alpha[hh_m], ysc = s_yscale[hh_m];
         const int hg = h0 + hh_m;
         const float *init = pr.init_state ? pr.init_state + (((size_t)b * H + hg) * P + p_m) * NS + n0 : nullptr;
+        // the entry state (the stop chunk's inclusive state, or the init state) for all of
+        // this thread's columns, every load issued before any is used: one round trip
+        float4 ent[NS / 8];
+        {
+            const float4 *src = stop >= 0 ? reinterpret_cast<const float4 *>(fa.incl + (unit - (c - stop)) * ustride + row_off)
+                                          : reinterpret_cast<const float4 *>(init);
+            const int qs = stop >= 0 ? kRows : 1;
+#pragma unroll
+            for (int q = 0; q < NS / 8; ++q) ent[q] = src ? __ldcg(src + q * qs) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
         for (int cc = 0; cc < NS / 2; cc += 32) {
             float acc[32];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-            if (stop >= 0) fma_row32(acc, 1.f, fa.incl + (unit - (c - stop)) * ustride + row_off + cc * kRows, kRows);
-            else if (init) fma_row32(acc, 1.f, init + cc);
+            for (int q = 0; q < 8; ++q) {
+                const float4 v = ent[cc / 4 + q];
+                acc[4 * q] = v.x;
+                acc[4 * q + 1] = v.y;
+                acc[4 * q + 2] = v.z;
+                acc[4 * q + 3] = v.w;
+            }
             int k = stop + 1;
             for (; k + 1 < c; k += 2) {  // two aggregates per round trip
                 const size_t u = unit - (c - k);
