@@ -245,12 +245,14 @@ __device__ void direct_unit_tmem(const Problem &pr, size_t tok0, int len, int h0
 }
 
 // One CTA per SM: its shared memory (137 KiB at dstate 64, 217 KiB at 128) leaves
-// no room for a second, so the registers are not capped for one.
+// no room for a second, so the registers are not capped for one.  Persistent: the
+// CTA takes tickets one after another until `units` are handed out, its TMEM
+// allocated once, its barriers initialised afresh for every unit.
 template <int NS, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_fused_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
                  const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap, Problem pr,
-                 FusedArgs fa)
+                 FusedArgs fa, int units)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_ld, bar_c, bar_g, bar_full[3], bar_empty[3];
@@ -270,12 +272,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
     const int nhb = H / HB, nc = pr.nchunks;
 
-    // TMEM first, ticket second: a CTA never holds a ticket (that others may wait
-    // on) while it is itself still waiting for resources
+    // TMEM first, tickets second: a CTA never holds a ticket (that others may wait
+    // on) while it is itself still waiting for resources.  A CTA takes its next
+    // ticket only after finishing its unit, so every smaller ticket is finished or
+    // held by a running unit: the look-back always ends.
     if (warp == 0) tmem_alloc(&tmem_slot, 256);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t col_y = 0, col_st = 128;   // Y (G first), chunk state
+    for (;;) {
     if (tid == 0) {
         s_ticket = atomicAdd(fa.counters + kCtrTicket, 1u);
         mbar_init(&bar_ld, 1);
@@ -289,8 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_fail = 0;
     }
     __syncthreads();
-    const uint32_t tmem = tmem_slot;
-    const uint32_t col_y = 0, col_st = 128;   // Y (G first), chunk state
+    if (s_ticket >= (uint32_t)units) break;  // the same value for every thread
 
     // chunk-major unit order: every predecessor chunk has a smaller ticket.  (tt, tb):
     // TMA coordinates of the first token, whose global index is tb * seqlen + tt
@@ -840,6 +846,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncthreads();
     }
+    // the unit is done: its shared memory, barriers and TMEM columns are free again;
+    // a wait that gave up ends this CTA's work
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+    }
+    tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
@@ -1618,10 +1631,13 @@ cudaError_t launch(const Problem &pr, const FusedArgs &fa, cudaStream_t s)
         const size_t smem = fused_smem(NS);
         auto kern = pr.chunks ? ssd_fused_tc<NS, true> : ssd_fused_tc<NS, false>;
         if ((e = ensure_smem_limit(reinterpret_cast<const void *>(kern), smem)) != cudaSuccess) return e;
+        int nsm = 0;
+        if ((e = sm_count(&nsm)) != cudaSuccess) return e;
+        const unsigned grid = (unsigned)std::min<size_t>(units, (size_t)nsm);  // one persistent CTA per SM
         if ((e = cudaMemsetAsync(fa.aggcnt, 0, (2 * units + kCtrCount) * sizeof(uint32_t), s)) != cudaSuccess)
             return e;
         profile_kernel_begin(s);
-        kern<<<(unsigned)units, kThreads, smem, s>>>(xmap, bmap, cmap, ymap, pr, fa);
+        kern<<<grid, kThreads, smem, s>>>(xmap, bmap, cmap, ymap, pr, fa, (int)units);
         profile_kernel_end(s);
     }
     return cudaGetLastError();
