@@ -39,10 +39,15 @@
 //   5. Y += C (e^ref h_c)^T (h as hi + lo), then y = r_i Y + D x, staged in
 //      shared memory and written by TMA.
 //
-// A chunk whose span exceeds 120 (an extreme decay inside one chunk) keeps
-// steps 1-4 with the decay referenced to the chunk end and replaces 5 by a
-// direct evaluation with per-element decays (slow; never taken by the
-// workloads here, exercised by the tests).
+// A chunk whose span exceeds 120 (an extreme decay inside one chunk: the
+// factors would leave range) keeps steps 1-4 with the decay referenced to the
+// chunk end (v_j = exp(cs_last - cs_j) <= 1) and replaces the rank-one diagonal
+// block by the quadratic form itself: per head, the masked decayed matrix
+//   M_ij = G_ij exp(cs_i - cs_j) dt_j  (j <= i),
+// every factor at most 1 apart from G, formed from G in TMEM and multiplied
+// with x as loaded (exact in bf16) on the tensor cores, and the off-diagonal
+// part C h_c^T in a second accumulator scaled by exp(cs_i) <= 1:
+//   y_i = (M x)_i + exp(cs_i) C_i . h_c + D x_i.
 //
 // Forward progress: CTAs take their unit from an atomic ticket in chunk-major
 // order (after allocating tensor memory), so every unit a CTA waits on belongs
@@ -149,101 +154,6 @@ __device__ __forceinline__ void named_sync(int id, int n)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Direct fp32 evaluation of a wide unit's outputs (decay range beyond the
-// factored form).  Token m of the chunk is handled by kThr threads (`part` =
-// 0 .. kThr-1), each taking 64 / kThr columns of every 64-column block.  G = C B^T
-// (fp32 sums of the bf16 products) is still in the unit's TMEM accumulator,
-// row m at g_taddr: such a unit skips the diagonal and off-diagonal products.
-// Per head and block, y_m = exp(cs_m) C_m . h_c + sum_{j<=m} G_mj
-// exp(cs_m - cs_j) dt_j x_j + D x_m, each weight formed once per (m, j, head,
-// block, part).  The sums live in `accs` ([64 columns][128 tokens] fp32, 32 KiB
-// of shared memory, so a warp's accesses fall in distinct banks), which keeps
-// this rarely taken path light on registers.  `hcs` is h_c, [128 rows (head,
-// headdim)][NS] fp32 in shared memory; cs and dtv are the unit's per-token cs
-// and input scale, [2][128].
-template <int NS, int kThr>
-__device__ void direct_unit_tmem(const Problem &pr, size_t tok0, int len, int h0, uint32_t g_taddr,
-                                 const float *hcs, float *accs, const float *cs, const float *dtv, int m, int part)
-{
-    constexpr int kW = 64 / kThr;  // columns of a block per thread
-    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, G = pr.ngroups, g = h0 / (H / G);
-    const bool row = m < len;
-    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(pr.x);
-    const uint4 *crow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(pr.C) +
-                                                        ((tok0 + (row ? m : 0)) * G + g) * NS);
-    for (int hh = 0; hh < HB; ++hh) {
-        const int h = h0 + hh;
-        const float *csh = cs + hh * kRows, *dth = dtv + hh * kRows;
-        const float csm = csh[m], ecs = expf(csm);
-        const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
-        for (int pb = 0; pb < P; pb += 64) {
-            const int pc = pb + part * kW;  // this thread's first column
-            float *acp = accs + part * kW * kRows;
-            // exp(cs_m) C_m . h_c
-            for (int p = 0; p < kW; ++p) {
-                const float *hr = hcs + (size_t)(hh * P + pc + p) * NS;
-                float off = 0.f;
-                if (row) {
-#pragma unroll
-                    for (int q = 0; q < NS / 8; ++q) {
-                        const uint4 cv = __ldg(crow + q);
-                        const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&cv);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 t = __bfloat1622float2(c2[e]);
-                            off = fmaf(t.x, hr[8 * q + 2 * e], off);
-                            off = fmaf(t.y, hr[8 * q + 2 * e + 1], off);
-                        }
-                    }
-                }
-                acp[p * kRows + m] = ecs * off;
-            }
-            // + sum_{j <= m} G_mj exp(cs_m - cs_j) dt_j x_j
-            for (int jb = 0; jb < 8; ++jb) {
-                float gv[16];
-                tmem_ld16(g_taddr + jb * 16, gv);  // warp-collective: every lane, every row
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int j = jb * 16 + k;
-                    if (!row || j > m) continue;
-                    const float w = gv[k] * expf(csm - csh[j]) * dth[j];
-                    const uint4 *xr = reinterpret_cast<const uint4 *>(x + ((tok0 + j) * H + h) * P + pc);
-#pragma unroll 1
-                    for (int q = 0; q < kW / 8; ++q) {
-                        const uint4 xv = __ldg(xr + q);
-                        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 t = __bfloat1622float2(x2[e]);
-                            float *a0 = acp + (8 * q + 2 * e) * kRows + m;
-                            a0[0] = fmaf(w, t.x, a0[0]);
-                            a0[kRows] = fmaf(w, t.y, a0[kRows]);
-                        }
-                    }
-                }
-            }
-            if (row) {  // + D x_m, rounded to bf16 and stored
-                const size_t base = ((tok0 + m) * H + h) * P + pc;
-                const uint4 *xm = reinterpret_cast<const uint4 *>(x + base);
-                uint4 *ym = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) + base);
-#pragma unroll 1
-                for (int q = 0; q < kW / 8; ++q) {
-                    const uint4 xv = __ldg(xm + q);
-                    const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-                    float o[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 t = __bfloat1622float2(x2[e]);
-                        o[2 * e] = fmaf(Dh, t.x, acp[(8 * q + 2 * e) * kRows + m]);
-                        o[2 * e + 1] = fmaf(Dh, t.y, acp[(8 * q + 2 * e + 1) * kRows + m]);
-                    }
-                    ym[q] = pack8(o);
-                }
-            }
-        }
-    }
-}
-
 // One CTA per SM: its shared memory (137 KiB at dstate 64, 217 KiB at 128) leaves
 // no room for a second, so the registers are not capped for one.  Persistent: the
 // CTA takes tickets one after another until `units` are handed out, its TMEM
@@ -255,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  FusedArgs fa, int units)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_ld, bar_c, bar_g, bar_full[3], bar_empty[3];
+    __shared__ __align__(8) uint64_t bar_ld, bar_c, bar_g, bar_w, bar_full[3], bar_empty[3];
     __shared__ uint32_t tmem_slot, s_ticket;
     __shared__ float warp_tot[8], warp_mn[8], warp_mx[8];
     __shared__ float cs[2 * kRows], dtv[2 * kRows];
@@ -288,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_ld, 1);
         mbar_init(&bar_c, 1);
         mbar_init(&bar_g, 1);
+        mbar_init(&bar_w, 1);
         for (int k = 0; k < 3; ++k) {
             mbar_init(&bar_full[k], kThreads / 32);  // one arrival per warp
             mbar_init(&bar_empty[k], 1);
@@ -579,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // x for the D x term: over wx hi for dstate 128, so it comes back (into the dead
     // tril(G) lo region) with C, which the off-diagonal product needs where B was
     uint8_t *xe = NS == 128 ? gl : xs;
-    if (ok && fast && tid == 0) {
+    if (ok && tid == 0) {
         mbar_expect_tx(&bar_c, (uint32_t)((NSL + (NS == 128 ? 2 : 0)) * kSlab));
         for (int s = 0; s < NSL; ++s) tma_load_3d(bs + s * kSlab, &cmap, &bar_c, g * NS + 64 * s, tt, tb);
         if (NS == 128)
@@ -719,12 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc[4 * q + 3] = fmaf(a, acc[4 * q + 3], v.w);
                 }
             }
-            if (!fast) {  // the direct path reads h_c from shared memory (the unused h hi/lo region)
-                float *hcs = reinterpret_cast<float *>(hh_s) + (size_t)m * NS + n0 + cc;
-#pragma unroll
-                for (int k = 0; k < 32; ++k) hcs[k] = acc[k];
-            }
-            if (fast) {  // e^ref h_c -> bf16 hi / lo operand slabs (row m)
+            {  // e^ref h_c -> bf16 hi / lo operand slabs (row m); ref = 0 in a wide unit
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float f[8];
@@ -757,22 +663,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (ok && tid == 0) {
-        if (fast) {
-            // Y += C (e^ref h_c)^T
-            if (!mbar_wait(&bar_c, 0, lim)) {
-                s_fail = 1;
-            } else {
-                tc_fence_after();
-                constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 0);
-                for (int ks = 0; ks < NS / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * kSlab + (ks % 4) * 32;
-                    const uint64_t ad = sdesc_sw128(smem_u32(bs) + off, 16, 1024);
-                    mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(hh_s) + off, 16, 1024), id_o, 1);
-                    mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(hh_s) + NSL * kSlab + off, 16, 1024), id_o, 1);
+    if constexpr (NS == 128) {
+        if (!fast) {
+            // A wide unit has no rank-one decay.  Its diagonal block takes, per head, the
+            // masked decayed matrix M[i][j] = G_ij e^(cs_i - cs_j) dt_j (j <= i; every factor
+            // <= 1 apart from G) as bf16 hi (over the dead wx hi) and lo (over C, whose G is
+            // done) K-major operands, formed from G in TMEM, and Y_diag[:, hh P ..] = M_hh x_hh
+            // accumulates in S_c's columns (consumed above), so G stays whole for the next
+            // head; x is exact in bf16.  This thread: row m, columns [64 half, 64 half + 64).
+            for (int hh = 0; hh < HB; ++hh) {
+                if (ok) {
+                    const float csm = cs[hh * kRows + m];
+#pragma unroll 1
+                    for (int jb = 0; jb < 4; ++jb) {
+                        const int j0 = 64 * half + 16 * jb;
+                        uint8_t *dh = xs + half * kSlab, *dl = cm + half * kSlab;
+                        uint4 hi[2], lo[2];
+                        if (j0 <= 32 * quarter + 31) {  // warp-uniform: some row of this warp reaches j0
+                            float gv[16];
+                            tmem_ld16(tmem + lane_base + col_y + j0, gv);
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                const int j = j0 + k;
+                                const float w = __expf(csm - cs[hh * kRows + j]) * dtv[hh * kRows + j];
+                                gv[k] = j <= m ? gv[k] * w : 0.f;
+                            }
+                            split8(gv, hi[0], lo[0]);
+                            split8(gv + 8, hi[1], lo[1]);
+                        } else {
+                            hi[0] = hi[1] = lo[0] = lo[1] = make_uint4(0, 0, 0, 0);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            *reinterpret_cast<uint4 *>(dh + sw128(m, 2 * jb + u)) = hi[u];
+                            *reinterpret_cast<uint4 *>(dl + sw128(m, 2 * jb + u)) = lo[u];
+                        }
+                    }
                 }
-                mma_commit(&bar_g);
+                fence_async_smem();
+                tc_fence_before();
+                __syncthreads();
+                if (ok && tid == 0) {
+                    if (hh == 0 && !mbar_wait(&bar_c, 0, lim)) {
+                        s_fail = 1;
+                    } else {
+                        tc_fence_after();
+                        const uint32_t id_w = idesc_bf16(128, P, 0, 1);
+                        for (int k = 0; k < kRows / 16; ++k) {
+                            const uint32_t goff = (k >> 2) * kSlab + (k & 3) * 32;
+                            const uint64_t xd = sdesc_sw128(smem_u32(xe) + hh * kSlab + k * 2048, kSlab, 1024);
+                            mma_bf16(tmem + col_st + hh * P, sdesc_sw128(smem_u32(xs) + goff, 16, 1024), xd, id_w, k > 0);
+                            mma_bf16(tmem + col_st + hh * P, sdesc_sw128(smem_u32(cm) + goff, 16, 1024), xd, id_w, 1);
+                        }
+                        mma_commit(&bar_w);
+                    }
+                }
+                __syncthreads();
+                ok = ok && !s_fail;
+                // the next head's M goes where this one was: wait for its MMAs
+                if (ok && !mbar_wait(&bar_w, hh & 1, lim)) s_fail = 1;
+                __syncthreads();
+                ok = ok && !s_fail;
+                tc_fence_after();
             }
+        }
+    }
+    if (ok && tid == 0) {
+        // Y += C (e^ref h_c)^T; a wide unit's off-diagonal part starts its own accumulator over G
+        if (!mbar_wait(&bar_c, 0, lim)) {
+            s_fail = 1;
+        } else {
+            tc_fence_after();
+            constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 0);
+            for (int ks = 0; ks < NS / 16; ++ks) {
+                const uint32_t off = (ks / 4) * kSlab + (ks % 4) * 32;
+                const uint64_t ad = sdesc_sw128(smem_u32(bs) + off, 16, 1024);
+                mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(hh_s) + off, 16, 1024), id_o, fast || ks > 0);
+                mma_bf16(tmem + col_y, ad, sdesc_sw128(smem_u32(hh_s) + NSL * kSlab + off, 16, 1024), id_o, 1);
+            }
+            mma_commit(&bar_g);
         }
     }
     // publish h_{c+1} (written above) now that the off-diagonal MMA is running:
@@ -780,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && (long long)unit != pr.withhold) red_release_add(fa.inclcnt + unit, 1u);
     __syncthreads();
     ok = ok && !s_fail;
-    if (ok && fast && !mbar_wait(&bar_g, 1, lim)) s_fail = 1;
+    if (ok && !mbar_wait(&bar_g, 1, lim)) s_fail = 1;
     __syncthreads();
     ok = ok && !s_fail;
     tc_fence_after();
@@ -790,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk is stored row by row: the rows after it belong to the next sequence)
     const bool tma_out = pr.chunk == kRows && (!kPacked || len == kRows);
     uint8_t *ystage = cm;
-    if (ok && fast) {
+    if (ok) {
         const int i = m, col0 = half * 64;
         const int hh = col0 / P, h = h0 + hh;
         const float r = rs[hh * kRows + i];
@@ -799,6 +768,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col = col0 + pc;
             float yv[32];
             tmem_ld32(tmem + lane_base + col_y + col, yv);
+            if (!fast) {  // a wide unit: y = Y_diag + r Y_off + D x, r = e^cs
+                float yd[32];
+                tmem_ld32(tmem + lane_base + col_st + col, yd);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) yv[k] = fmaf(r, yv[k], yd[k]);
+            }
+            const float rr = fast ? r : 1.f;
             uint4 outv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -808,8 +784,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const float2 xf = __bfloat1622float2(x2[v]);
-                    o[2 * v] = fmaf(Dh, xf.x, r * yv[8 * u + 2 * v]);
-                    o[2 * v + 1] = fmaf(Dh, xf.y, r * yv[8 * u + 2 * v + 1]);
+                    o[2 * v] = fmaf(Dh, xf.x, rr * yv[8 * u + 2 * v]);
+                    o[2 * v + 1] = fmaf(Dh, xf.y, rr * yv[8 * u + 2 * v + 1]);
                 }
                 outv[u] = pack8(o);
             }
@@ -828,24 +804,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tma_out) {
         fence_async_smem();
         __syncthreads();
-        if (ok && fast && tid == 0) {
+        if (ok && tid == 0) {
             for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, hb * 128 + 64 * k, tt, tb);
             bulk_commit();
             bulk_wait_read_all();
         }
     }
     if (!ok && tid == 0) atomicOr(pr.err_word, kDevErrTimeout);
-    tc_fence_before();
-    // decay range too wide for the factored form: direct outputs from G in TMEM,
-    // two threads per token (the warp halves), sums over the dead x tile
-    if (__syncthreads_and(ok && !fast)) {
-        tc_fence_after();
-        direct_unit_tmem<NS, 2>(pr, (size_t)tb * L + tt, len, hb * HB, tmem + lane_base + col_y,
-                                reinterpret_cast<const float *>(hh_s), reinterpret_cast<float *>(xs), cs, dtv, m,
-                                half);
-        tc_fence_before();
-        __syncthreads();
-    }
     // the unit is done: its shared memory, barriers and TMEM columns are free again;
     // a wait that gave up ends this CTA's work
     tc_fence_before();
@@ -859,24 +824,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // dstate 64, persistent.  One CTA per SM takes units (chunk-major tickets, as
 // above) one after another and keeps two of them in flight: two shared-memory
-// stages of 96 KiB and two 256-column TMEM slots, unit it using stage and slot
-// it & 1.  Warp roles:
+// stages of 96 KiB and two TMEM slots, unit it using stage and slot it & 1.
+// Warp roles:
 //   warp 0      tickets; TMA loads of dt, x, B and C into a free stage;
-//   warp 1      G = C B^T, then the chunk-state and diagonal-block MMAs;
-//   warps 2-5   segment sums and factors, wx (hi, lo), tril(G) into TMEM;
+//   warp 1      G = C B^T; the chunk-state MMAs slice by slice, committed on
+//               their own (the chain waits for S_c only); then the diagonal
+//               block Y = tril(G) wx once tril(G) is in (hi and lo: 3 MMAs);
+//   warps 2-5   segment sums and factors, wx (hi, lo) in 16-token slices, then
+//               tril(G) as hi and lo bf16 into TMEM (after wx, so S_c does not
+//               wait for it);
 //   warps 6-9   team 0 (the units of stage 0), warps 10-13 team 1 (stage 1):
 //               look-back for h_c (publishing S_c as the aggregate if the walk
-//               is still waiting when S_c is ready), h_{c+1} published, the h
-//               operand and the off-diagonal MMA Y += C (e^ref h_c)^T, then
-//               y = r Y + D x with x brought into the staging region by TMA,
-//               and the TMA store of y.
+//               is still waiting when S_c is ready), h_{c+1} published, then
+//               (once the diagonal block is done with wx) x brought into the
+//               staging region by TMA, the h operand and the off-diagonal MMA
+//               Y += C (e^ref h_c)^T, y = r Y + D x, and the TMA store of y; a
+//               wide unit's outputs instead (see the team's code).
 // Each role walks its units in ticket order, so the forward-progress argument
 // of the one-unit kernel holds: the smallest unfinished ticket only waits on
 // finished units.  Stage s, 96 KiB: [0, 32K) x -> wx hi -> h hi | lo;
 // [32K, 64K) wx lo -> x -> y (staging); [64K, 80K) B; [80K, 96K) C; after the
-// two stages, 2 KiB of dt per stage.  TMEM slot s at column 256 s: Y [0,128),
-// S_c [128,192), tril(G) [192,256).  The stage's x, B and C are reloaded as soon
-// as the off-diagonal MMA completes; the wx-lo region waits for the y store.
+// two stages, 2 KiB of dt per stage.  TMEM: slot s at column 256 s holds Y
+// [0,128) and S_c [128,192); tril(G) hi [192,256) and lo [448,512) serve the
+// unit the front and the MMA warp are on (a unit's G commit follows the
+// previous unit's diagonal MMAs from the same thread, so the front may then
+// overwrite them).  The stage's x, B and C are reloaded as soon as the
+// off-diagonal MMA completes; the wx-lo region waits for the y store.
 // Per-unit scalars and the info and seg barriers have four sets (it & 3): a
 // team may still read them after its stage has been handed to the next unit.
 // ---------------------------------------------------------------------------
@@ -965,7 +938,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     // seg and the unit's scalars, which the epilogue may still read after the stage is free
     __shared__ __align__(8) uint64_t bar_info[4], bar_seg[4], bar_full[2], bar_dt[2], bar_free[2], bar_slot[2],
         bar_lo[2], bar_g[2], bar_mask[2], bar_slice[2][kSlices], bar_mma[2], bar_yo[2], bar_xe[2], bar_pincl[2],
-        bar_pdone[2];
+        bar_pdone[2], bar_wd[2], bar_dg[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int s_tk[4], s_fast[4];
     __shared__ float cs[4][2 * kRows], dtv[4][2 * kRows], vw[4][2 * kRows], rs[4][2 * kRows];
@@ -980,7 +953,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads;
     const int nhb = H / HB;
-    const uint32_t col_y = 0, col_st = 128, col_m = 192;
+    // per slot: Y, S_c; tril(G) hi | lo in the columns after each slot's S_c, shared by the units
+    const uint32_t col_y = 0, col_st = 128, col_mhi = 192, col_mlo = 448;
 
     if (warp == kWarpMma) tmem_alloc(&tmem_slot, 512);
     if (tid == 0) {
@@ -1002,6 +976,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             mbar_init(&bar_xe[k], 1);
             mbar_init(&bar_pincl[k], 4);
             mbar_init(&bar_pdone[k], 1);
+            mbar_init(&bar_wd[k], 1);
+            mbar_init(&bar_dg[k], 1);
         }
         mbar_fence_init();
         s_fail = 0;
@@ -1078,13 +1054,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     mma_bf16(slot + col_y, sdesc_sw128(st + 5 * kSlab + ks * 32, 16, 1024),
                              sdesc_sw128(st + 4 * kSlab + ks * 32, 16, 1024), id_g, ks > 0);
                 mma_commit(&bar_g[s]);
-                // tril(G) in TMEM first, then each 16-token slice of wx as the front
-                // warps finish it, so the build and the MMAs overlap
-                if (!mbar_wait(&bar_mask[s], ph, lim)) {
-                    s_fail = 1;
-                    break;
-                }
-                const bool fast = s_fast[ss] != 0;
+                // the chunk state slice by slice as the front warps finish wx, committed on its
+                // own (the chain waits for it); then the diagonal block once tril(G) is in
                 bool okm = true;
                 for (int ks = 0; ks < kRows / 16; ++ks) {
                     if (!mbar_wait(&bar_slice[s][ks], ph, lim)) {
@@ -1093,20 +1064,29 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                     }
                     tc_fence_after();
                     const uint64_t bd = sdesc_sw128(st + 4 * kSlab + ks * 2048, kSlab, 1024);
-                    const uint64_t whi = sdesc_sw128(st + ks * 2048, kSlab, 1024);
-                    const uint64_t wlo = sdesc_sw128(st + 2 * kSlab + ks * 2048, kSlab, 1024);
-                    mma_bf16(slot + col_st, whi, bd, id_s, ks > 0);
-                    mma_bf16(slot + col_st, wlo, bd, id_s, 1);
-                    if (fast) {
-                        mma_bf16_tA(slot + col_y, slot + col_m + ks * 8, whi, id_d, ks > 0);
-                        mma_bf16_tA(slot + col_y, slot + col_m + ks * 8, wlo, id_d, 1);
-                    }
+                    mma_bf16(slot + col_st, sdesc_sw128(st + ks * 2048, kSlab, 1024), bd, id_s, ks > 0);
+                    mma_bf16(slot + col_st, sdesc_sw128(st + 2 * kSlab + ks * 2048, kSlab, 1024), bd, id_s, 1);
                 }
                 if (!okm) {
                     s_fail = 1;
                     break;
                 }
                 mma_commit(&bar_mma[s]);
+                if (!mbar_wait(&bar_mask[s], ph, lim)) {
+                    s_fail = 1;
+                    break;
+                }
+                if (s_fast[ss] != 0) {  // written by the front before its bar_mask arrival
+                    tc_fence_after();
+                    for (int ks = 0; ks < kRows / 16; ++ks) {
+                        const uint64_t whi = sdesc_sw128(st + ks * 2048, kSlab, 1024);
+                        const uint64_t wlo = sdesc_sw128(st + 2 * kSlab + ks * 2048, kSlab, 1024);
+                        mma_bf16_tA(slot + col_y, tmem + col_mhi + ks * 8, whi, id_d, ks > 0);
+                        mma_bf16_tA(slot + col_y, tmem + col_mhi + ks * 8, wlo, id_d, 1);
+                        mma_bf16_tA(slot + col_y, tmem + col_mlo + ks * 8, whi, id_d, 1);
+                    }
+                }
+                mma_commit(&bar_dg[s]);
             }
         }
     } else if (warp < kWarpState) {
@@ -1186,38 +1166,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             if (ft == 0) s_fast[ss] = fast ? 1 : 0;
             mbar_arrive(&bar_seg[ss]);
             named_sync(kBarFront, 128);  // every v_j dt_j is in shared memory
-            ok = mbar_wait(&bar_full[s], ph, lim) && mbar_wait(&bar_g[s], ph, lim);
-            ok = __all_sync(0xffffffffu, ok);  // the TMEM accesses below are warp-collective
-            tc_fence_after();
-            if (ok && fast) {  // tril(G) -> bf16 pairs in TMEM (row m, columns jb*32 .. jb*32+31)
-                const uint32_t slot = tmem + s * 256 + lane_base;
-                for (int jb = 0; jb < 4; ++jb) {
-                    uint32_t pk[16];
-                    if (jb > quarter) {
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) pk[k] = 0u;
-                    } else {
-                        float gv[32];
-                        tmem_ld32(slot + col_y + jb * 32, gv);
-                        if (jb == quarter) {
-#pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                if (jb * 32 + k > m) gv[k] = 0.f;
-                        }
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            __nv_bfloat162 t2 = __floats2bfloat162_rn(gv[2 * k], gv[2 * k + 1]);
-                            pk[k] = *reinterpret_cast<uint32_t *>(&t2);
-                        }
-                    }
-                    tmem_st16(slot + col_m + jb * 16, pk);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&bar_mask[s]);
-            // the lo region is the staging region of the unit two back: wait for its y store
-            // only now, so the tril(G) build above overlaps that store
-            ok = ok && (it < 2 || mbar_wait(&bar_lo[s], ph ^ 1, lim));
+            // x in place; the lo region is the staging region of the unit two back: its y is stored
+            ok = ok && mbar_wait(&bar_full[s], ph, lim) && (it < 2 || mbar_wait(&bar_lo[s], ph ^ 1, lim));
             // wx = v dt x, hi in place over x, lo at +32K, in 16-token slices: slice
             // ks is rows 16 ks .. 16 ks + 15 of both 64-column slabs (256 chunks)
 #pragma unroll 1
@@ -1248,6 +1198,45 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                 fence_async_smem();
                 mbar_arrive(&bar_slice[s][ks]);
             }
+            // tril(G) after wx: the chunk state (the chain's next step) does not wait for it
+            ok = ok && mbar_wait(&bar_g[s], ph, lim);
+            ok = __all_sync(0xffffffffu, ok);  // the TMEM accesses below are warp-collective
+            tc_fence_after();
+            if (ok && fast) {
+                // tril(G) -> hi and lo bf16 pairs (row m, 16 tokens per step) in the shared
+                // tril columns.  The previous unit's diagonal MMAs, which read them, are
+                // complete: this unit's G commit follows them from the same issuing thread.
+                const uint32_t gsrc = tmem + s * 256 + lane_base + col_y;
+#pragma unroll 1
+                for (int jb = 0; jb < 4; ++jb) {
+                    uint32_t ph16[16], pl16[16];
+                    if (jb > quarter) {  // every row of this warp is above these columns
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) ph16[k] = pl16[k] = 0u;
+                    } else {
+                        float gv[32];
+                        tmem_ld32(gsrc + jb * 32, gv);
+                        if (jb == quarter) {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                if (jb * 32 + k > m) gv[k] = 0.f;
+                        }
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(gv[2 * k], gv[2 * k + 1]);
+                            const float2 hf = __bfloat1622float2(h2);
+                            __nv_bfloat162 l2 = __floats2bfloat162_rn(gv[2 * k] - hf.x, gv[2 * k + 1] - hf.y);
+                            ph16[k] = *reinterpret_cast<uint32_t *>(&h2);
+                            pl16[k] = *reinterpret_cast<uint32_t *>(&l2);
+                        }
+                    }
+                    tmem_st16_async(tmem + lane_base + col_mhi + jb * 16, ph16);
+                    tmem_st16_async(tmem + lane_base + col_mlo + jb * 16, pl16);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            mbar_arrive(&bar_mask[s]);
             if (named_sync_or(kBarFront, 128, !ok)) {
                 s_fail = 1;
                 break;
@@ -1293,6 +1282,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         const int s = team;
         uint8_t *st = base + s * kStageBytes;
         const uint32_t slot = tmem + s * 256 + lane_base;
+        int nwide = 0;  // commits to bar_wd so far (its phase): the MMA steps of wide units
         for (int it = team;; it += 2) {
             const int ss = it & 3;
             const uint32_t ph = (it >> 1) & 1, pq = (it >> 2) & 1;
@@ -1418,15 +1408,6 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
             tc_fence_after();
             const bool fast = s_fast[ss] != 0;
-            if (tt == 0) {  // x of the unit for the D x term, into the staging region (wx lo is dead)
-                if (ok && fast) {
-                    mbar_expect_tx(&bar_xe[s], (uint32_t)(2 * kSlab));
-                    for (int k = 0; k < 2; ++k)
-                        tma_load_3d(st + 2 * kSlab + k * kSlab, &xmap, &bar_xe[s], u.hb * 128 + 64 * k, u.tt, u.tb);
-                } else {
-                    mbar_arrive(&bar_xe[s]);
-                }
-            }
             // h_{c+1} = a_c h_c + S_c (S_c referenced to the chunk end), 32 columns at a
             // time, stored as it is formed: it is what the successors wait for, so it
             // goes out before the h_c operand of this unit's own off-diagonal product
@@ -1452,54 +1433,248 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_pincl[s]);  // the team's publisher releases h_{c+1}
-            if (ok) {
-                if (fast) {  // e^ref h_c -> bf16 hi / lo K-major slabs over the dead wx hi
-                    const float ysc = s_ysc[ss][hh_m];
+            // wx (hi and lo) is dead once the diagonal block's MMAs are done
+            ok = ok && mbar_wait(&bar_dg[s], ph, lim);
+            if (tt == 0) {  // x of the unit into the staging region (over wx lo): the D x term, and for
+                            // a wide unit also the operand of its diagonal block
+                if (ok) {
+                    mbar_expect_tx(&bar_xe[s], (uint32_t)(2 * kSlab));
+                    for (int k = 0; k < 2; ++k)
+                        tma_load_3d(st + 2 * kSlab + k * kSlab, &xmap, &bar_xe[s], u.hb * 128 + 64 * k, u.tt, u.tb);
+                } else {
+                    mbar_arrive(&bar_xe[s]);
+                }
+            }
+            if (ok) {  // e^ref h_c -> bf16 hi / lo K-major slabs over the dead wx hi (ref = 0 in a wide unit)
+                const float ysc = s_ysc[ss][hh_m];
 #pragma unroll
-                    for (int q = 0; q < NS / 8; ++q) {
-                        float f[8];
+                for (int q = 0; q < NS / 8; ++q) {
+                    float f[8];
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) f[k] = ysc * acc[8 * q + k];
-                        uint4 hi, lo;
-                        split8(f, hi, lo);
-                        *reinterpret_cast<uint4 *>(st + sw128(m, q)) = hi;
-                        *reinterpret_cast<uint4 *>(st + kSlab + sw128(m, q)) = lo;
-                    }
-                } else {  // the direct path reads h_c in fp32
-                    float *hcs = reinterpret_cast<float *>(st) + (size_t)m * NS;
-#pragma unroll
-                    for (int k = 0; k < NS; ++k) hcs[k] = acc[k];
+                    for (int k = 0; k < 8; ++k) f[k] = ysc * acc[8 * q + k];
+                    uint4 hi, lo;
+                    split8(f, hi, lo);
+                    *reinterpret_cast<uint4 *>(st + sw128(m, q)) = hi;
+                    *reinterpret_cast<uint4 *>(st + kSlab + sw128(m, q)) = lo;
                 }
             }
             fence_async_smem();
             tc_fence_before();
             bool any_fail = named_sync_or(bar_team, 128, !ok);
-            if (tt == 0) {
-                if (!any_fail && fast) {  // Y += C (e^ref h_c)^T; the stage's x, B, C are free once it completes
+            const uint32_t sbase = tmem + s * 256;
+            const uint32_t sa = smem_u32(st);
+            const bool row_in = m < u.len;
+            uint8_t *ystage = st + 2 * kSlab;
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
+                                                   (((size_t)u.tb * pr.seqlen + u.tt + m) * H + u.h0) * P);
+            bool okd = !any_fail;
+            if (!fast) {
+                // A wide unit has no rank-one decay.  Per head, the masked decayed matrix
+                // M[m][j] = G_mj e^(cs_m - cs_j) dt_j (j <= m; every factor <= 1 apart from G) is
+                // formed in place over G in Y's columns (the diagonal product was skipped) as
+                // hi | lo bf16 pairs, 16 columns per 16 tokens, and multiplied with x as loaded
+                // (exact in bf16) into S_c's columns (consumed); 64 output columns at a time,
+                // each finished in shared memory before the next:
+                //   two heads:  Y_off = C h_hh^T in Y's first 64 columns once M_hh is consumed,
+                //               y = Y_diag + e^cs Y_off + D x; the next head's M needs G again
+                //               (C B^T once more: the stage's B and C are still in place);
+                //   one head:   C' = e^cs C (hi, lo over the dead B and over C) joins the same
+                //               accumulator, y = (M x + C' h^T) + D x.
+                // Each step waits for the MMAs that read what the next one overwrites.
+                auto team_sync = [&]() {  // every thread learns whether the leader's steps held
+                    tc_fence_before();
+                    okd = !named_sync_or(bar_team, 128, !okd);
+                    tc_fence_after();
+                };
+                auto lead_commit_wait = [&]() {
+                    mma_commit(&bar_wd[s]);
+                    okd = mbar_wait(&bar_wd[s], nwide & 1, lim);
+                    ++nwide;
+                };
+                auto build_m = [&](int hh) {  // M_hh over G, row m = this thread's TMEM lane
+                    const float csm = cs[ss][hh * kRows + m];
+                    const float *csb = cs[ss] + hh * kRows, *dtb = dtv[ss] + hh * kRows;
+#pragma unroll 1
+                    for (int jb = 0; jb < 8; ++jb) {
+                        uint32_t pk[16];  // 8 hi pairs, then 8 lo pairs
+                        if (jb <= 2 * quarter + 1) {  // warp-uniform: some row of this warp reaches 16 jb
+                            float gv[16];
+                            tmem_ld16(slot + col_y + jb * 16, gv);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                float f2[2];
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const int j = jb * 16 + 2 * k + e;
+                                    const float w = __expf(csm - csb[j]) * dtb[j];
+                                    f2[e] = j <= m ? gv[2 * k + e] * w : 0.f;
+                                }
+                                __nv_bfloat162 h2 = __floats2bfloat162_rn(f2[0], f2[1]);
+                                const float2 hf = __bfloat1622float2(h2);
+                                __nv_bfloat162 l2 = __floats2bfloat162_rn(f2[0] - hf.x, f2[1] - hf.y);
+                                pk[k] = *reinterpret_cast<uint32_t *>(&h2);
+                                pk[8 + k] = *reinterpret_cast<uint32_t *>(&l2);
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) pk[k] = 0u;
+                        }
+                        tmem_st16(slot + col_y + jb * 16, pk);
+                    }
+                };
+                // y for the 64 columns `pb` of the unit (x slab pb / 64) from the accumulators
+                auto finish64 = [&](int pb, float r, bool with_off, bool last) {
+                    const int h = u.h0 + pb / P;
+                    const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {
+                        float yd[32], yo[32];
+                        tmem_ld32(slot + col_st + 32 * half, yd);
+                        if (with_off) tmem_ld32(slot + col_y + 32 * half, yo);
+                        if (last && half == 1) {  // this warp's last read of the slot
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&bar_slot[s]);
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uint4 *sp = reinterpret_cast<uint4 *>(ystage + (pb / 64) * kSlab + sw128(m, 4 * half + k));
+                            const uint4 xv = *sp;
+                            const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                            float o[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float2 xf = __bfloat1622float2(x2[e / 2]);
+                                const float yoff = with_off ? r * yo[8 * k + e] : 0.f;
+                                o[e] = fmaf(Dh, (e & 1) ? xf.y : xf.x, yd[8 * k + e] + yoff);
+                            }
+                            const uint4 ov = pack8(o);
+                            if (tma_out)
+                                *sp = ov;
+                            else if (row_in)
+                                dst[pb / 8 + 4 * half + k] = ov;
+                        }
+                    }
+                };
+                const uint32_t id64 = idesc_bf16(128, 64, 0, 1), id64k = idesc_bf16(128, 64, 0, 0);
+                // x (staging region) and C are read by every thread below: acquire their loads
+                okd = okd && mbar_wait(&bar_xe[s], ph, lim) && mbar_wait(&bar_full[s], ph, lim);
+                team_sync();
+                if (HB == 2) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (hh > 0 && tt == 0 && okd) {  // G again, over the consumed M and Y_off
+                            constexpr uint32_t id_g = idesc_bf16(128, 128, 0, 0);
+                            for (int ks = 0; ks < NS / 16; ++ks)
+                                mma_bf16(sbase + col_y, sdesc_sw128(sa + 5 * kSlab + ks * 32, 16, 1024),
+                                         sdesc_sw128(sa + 4 * kSlab + ks * 32, 16, 1024), id_g, ks > 0);
+                            lead_commit_wait();
+                        }
+                        team_sync();
+                        if (okd) build_m(hh);
+                        team_sync();
+                        if (tt == 0 && okd) {
+                            {
+                                tc_fence_after();
+                                for (int ks = 0; ks < kRows / 16; ++ks) {
+                                    const uint64_t xd = sdesc_sw128(sa + 2 * kSlab + hh * kSlab + ks * 2048, kSlab, 1024);
+                                    mma_bf16_tA(sbase + col_st, sbase + col_y + 16 * ks, xd, id64, ks > 0);
+                                    mma_bf16_tA(sbase + col_st, sbase + col_y + 16 * ks + 8, xd, id64, 1);
+                                }
+                                lead_commit_wait();
+                            }
+                            if (okd) {  // Y_off = C h_hh^T (rows 64 hh of the h operand), over M
+                                tc_fence_after();
+                                for (int ks = 0; ks < NS / 16; ++ks) {
+                                    const uint64_t ad = sdesc_sw128(sa + 5 * kSlab + ks * 32, 16, 1024);
+                                    mma_bf16(sbase + col_y, ad, sdesc_sw128(sa + hh * 8192 + ks * 32, 16, 1024), id64k,
+                                             ks > 0);
+                                    mma_bf16(sbase + col_y, ad, sdesc_sw128(sa + kSlab + hh * 8192 + ks * 32, 16, 1024),
+                                             id64k, 1);
+                                }
+                                lead_commit_wait();
+                            }
+                        }
+                        team_sync();
+                        if (okd) finish64(64 * hh, rs[ss][hh * kRows + m], true, hh == 1);
+                        team_sync();  // the outputs are read before the next head overwrites them
+                    }
+                } else {
+                    if (okd) {
+                        build_m(0);
+                        // C' = e^cs C for row m: hi over the dead B, lo over C
+                        const float ec = rs[ss][m];
+#pragma unroll
+                        for (int q = 0; q < NS / 8; ++q) {
+                            const uint4 cv = *reinterpret_cast<const uint4 *>(st + 5 * kSlab + sw128(m, q));
+                            const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&cv);
+                            float f[8];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 cf = __bfloat1622float2(c2[e]);
+                                f[2 * e] = ec * cf.x;
+                                f[2 * e + 1] = ec * cf.y;
+                            }
+                            uint4 hi, lo;
+                            split8(f, hi, lo);
+                            *reinterpret_cast<uint4 *>(st + 4 * kSlab + sw128(m, q)) = hi;
+                            *reinterpret_cast<uint4 *>(st + 5 * kSlab + sw128(m, q)) = lo;
+                        }
+                    }
+                    fence_async_smem();
+                    team_sync();
+                    for (int pb = 0; pb < 128; pb += 64) {
+                        if (tt == 0 && okd) {
+                            {
+                                tc_fence_after();
+                                for (int ks = 0; ks < kRows / 16; ++ks) {
+                                    const uint64_t xd = sdesc_sw128(sa + 2 * kSlab + (pb / 64) * kSlab + ks * 2048, kSlab, 1024);
+                                    mma_bf16_tA(sbase + col_st, sbase + col_y + 16 * ks, xd, id64, ks > 0);
+                                    mma_bf16_tA(sbase + col_st, sbase + col_y + 16 * ks + 8, xd, id64, 1);
+                                }
+                                for (int ks = 0; ks < NS / 16; ++ks) {
+                                    const uint64_t chi = sdesc_sw128(sa + 4 * kSlab + ks * 32, 16, 1024);
+                                    const uint64_t clo = sdesc_sw128(sa + 5 * kSlab + ks * 32, 16, 1024);
+                                    const uint64_t hhi = sdesc_sw128(sa + (pb / 64) * 8192 + ks * 32, 16, 1024);
+                                    const uint64_t hlo = sdesc_sw128(sa + kSlab + (pb / 64) * 8192 + ks * 32, 16, 1024);
+                                    mma_bf16(sbase + col_st, chi, hhi, id64k, 1);
+                                    mma_bf16(sbase + col_st, chi, hlo, id64k, 1);
+                                    mma_bf16(sbase + col_st, clo, hhi, id64k, 1);
+                                }
+                                lead_commit_wait();
+                            }
+                        }
+                        team_sync();
+                        if (okd) finish64(pb, 0.f, false, pb == 64);
+                        team_sync();  // S_c's columns are read before the next block overwrites them
+                    }
+                }
+                if (tt == 0) {
+                    if (okd) mbar_arrive(&bar_free[s]);  // every MMA of the unit is complete
+                    mbar_arrive(&bar_yo[s]);
+                }
+            } else if (tt == 0) {
+                // Y += C (e^ref h_c)^T, after the diagonal block's MMAs (issued by another thread,
+                // waited for above); the stage's x, B, C are free once it completes
+                if (okd) {
                     tc_fence_after();
                     constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 0);
-                    const uint32_t sa = smem_u32(st);
                     for (int ks = 0; ks < NS / 16; ++ks) {
                         const uint64_t ad = sdesc_sw128(sa + 5 * kSlab + ks * 32, 16, 1024);
-                        mma_bf16(tmem + s * 256 + col_y, ad, sdesc_sw128(sa + ks * 32, 16, 1024), id_o, 1);
-                        mma_bf16(tmem + s * 256 + col_y, ad, sdesc_sw128(sa + kSlab + ks * 32, 16, 1024), id_o, 1);
+                        mma_bf16(sbase + col_y, ad, sdesc_sw128(sa + ks * 32, 16, 1024), id_o, 1);
+                        mma_bf16(sbase + col_y, ad, sdesc_sw128(sa + kSlab + ks * 32, 16, 1024), id_o, 1);
                     }
                     mma_commit(&bar_yo[s]);
                     mma_commit(&bar_free[s]);
                 } else {
-                    mbar_arrive(&bar_yo[s]);  // the direct path frees the stage itself
+                    mbar_arrive(&bar_yo[s]);
                 }
             }
-            // ---- epilogue: y = r Y + D x, x read from the staging region and y
-            // written over it (the same swizzled position), then stored by TMA
-            const bool row_in = m < u.len;
+            // ---- epilogue of a factored unit: y = r Y + D x, x read from the staging region and
+            // y written over it (the same swizzled position), then stored by TMA
             ok = !any_fail && mbar_wait(&bar_yo[s], ph, lim) && mbar_wait(&bar_xe[s], ph, lim);
-            ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
+            ok = __all_sync(0xffffffffu, ok && (fast || okd));  // the TMEM loads below are warp-collective
             tc_fence_after();
-            uint8_t *ystage = st + 2 * kSlab;
             if (ok && fast) {
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
-                                                       (((size_t)u.tb * pr.seqlen + u.tt + m) * H + u.h0) * P);
 #pragma unroll
                 for (int col = 0; col < 128; col += 64) {
                     const int hh = col / P, h = u.h0 + hh;
@@ -1537,29 +1712,15 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
             fence_async_smem();
             tc_fence_before();
             const bool all_ok = !named_sync_or(bar_team, 128, !ok);
-            // every warp frees the slot once per unit: above after its last read of Y, here
-            // when it read nothing (a failed unit); a wide unit reads G below and frees it after
-            if (!(ok && fast) && !(all_ok && !fast) && lane == 0) mbar_arrive(&bar_slot[s]);
+            // every warp frees the slot once per unit: above after its last read, here when it read nothing
+            if (!ok && lane == 0) mbar_arrive(&bar_slot[s]);
             if (tt == 0) {
-                if (all_ok && fast && tma_out) {
+                if (all_ok && tma_out) {
                     for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, u.hb * 128 + 64 * k, u.tt, u.tb);
                     bulk_commit();
                     bulk_wait_read_all();
                 }
-                if (!(all_ok && !fast)) mbar_arrive(&bar_lo[s]);  // the staging region is free again
-            }
-            if (all_ok && !fast) {
-                tc_fence_after();
-                direct_unit_tmem<NS, 1>(pr, (size_t)u.tb * pr.seqlen + u.tt, u.len, u.h0, slot + col_y,
-                                        reinterpret_cast<const float *>(st), reinterpret_cast<float *>(st + 2 * kSlab),
-                                        cs[ss], dtv[ss], m, 0);
-                tc_fence_before();
-                named_sync(bar_team, 128);  // every thread is done with the stage and the TMEM slot
-                if (lane == 0) mbar_arrive(&bar_slot[s]);
-                if (tt == 0) {
-                    mbar_arrive(&bar_lo[s]);
-                    mbar_arrive(&bar_free[s]);
-                }
+                mbar_arrive(&bar_lo[s]);  // the staging region is free again
             }
             if (!all_ok) {
                 s_fail = 1;

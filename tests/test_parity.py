@@ -316,3 +316,39 @@ def test_mixed_fast_and_queued_chunks():
     inp = make_inputs(1, 512, 8, 64, 64, 1, "bf16", seed=78, with_init=True)
     inp["dt"][:, :, 4:] *= 20.0  # head blocks 2 and 3: spans beyond the factored path in every chunk
     check_full(inp, 128)
+
+
+# Wide in-chunk decay on each fused kernel: (b, L, H, P, N, G, Q, kernel).  Every
+# chunk's cs range is far beyond the factored form's, so every unit takes the
+# masked decayed matrix on the tensor cores.
+WIDE = [
+    (1, 700, 80, 64, 64, 1, 128, "ssd_fused_pipe_tc"),    # 40 sequences: the look-back kernel, ragged tail
+    (2, 600, 36, 128, 64, 2, 128, "ssd_fused_pipe_tc"),   # one head per unit
+    (1, 700, 66, 64, 64, 3, 96, "ssd_fused_pipe_tc"),     # chunk 96 (rows stored one by one), dt without TMA
+    (2, 513, 8, 128, 128, 2, 128, "ssd_fused_tc"),        # dstate 128, one head per unit
+    (1, 300, 4, 64, 128, 1, 128, "ssd_fused_tc"),         # dstate 128, two heads per unit
+    (3, 700, 4, 128, 128, 2, 100, "ssd_fused_tc"),        # chunk 100
+]
+
+
+@pytest.mark.parametrize("case", WIDE, ids=[f"{c[7]}_b{c[0]}L{c[1]}H{c[2]}P{c[3]}N{c[4]}Q{c[6]}" for c in WIDE])
+def test_wide_decay_on_each_fused_kernel(case):
+    b, L, H, P, N, G, Q, kern = case
+    assert ssd.ssd_fwd_kernels(b, L, H, P, G, N, Q, ssd.SSD_DTYPE_BF16) == [kern]
+    inp = make_inputs(b, L, H, P, N, G, "bf16", seed=79 + L, dt_range=(0.5, 2.0), with_init=True)
+    ey, ef = check_full(inp, Q)
+    print(f"{kern} wide: y error {ey:.2e} x RMS, final state {ef:.2e} x RMS")
+
+
+@pytest.mark.parametrize("kern,dims", [("ssd_fused_pipe_tc", (2, 512, 40, 64, 64, 1)),
+                                       ("ssd_fused_tc", (2, 512, 8, 64, 128, 2))])
+def test_wide_and_factored_units_interleaved(kern, dims):
+    """Half the heads with steps ~20x larger: wide and factored units share the
+    CTAs, the look-back chain and (in the persistent kernels) the two TMEM slots."""
+    b, L, H, P, N, G = dims
+    assert ssd.ssd_fwd_kernels(b, L, H, P, G, N, 128, ssd.SSD_DTYPE_BF16) == [kern]
+    inp = make_inputs(b, L, H, P, N, G, "bf16", seed=80 + H, with_init=True)
+    inp["dt"][:, :, H // 2:] *= 20.0
+    inp["dt"][:, 300:, :4] *= 20.0  # and the first head block turns wide after token 300
+    ey, ef = check_full(inp, 128)
+    print(f"{kern} mixed: y error {ey:.2e} x RMS, final state {ef:.2e} x RMS")

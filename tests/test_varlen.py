@@ -101,6 +101,14 @@ def test_packed_multi_kernel_in_place_state_carry():
     assert_close(st.cpu().numpy(), fr, TOL[torch.bfloat16], "final_state (packed, in place)")
 
 
+@pytest.mark.parametrize("N", [64, 128])
+def test_packed_wide_decay(N):
+    # steps of 0.5 .. 2 with |A| up to 16: every chunk is beyond the factored form's range
+    lengths = [700, 1, 128, 0, 255, 129, 64, 3]
+    d = make_varlen_inputs(lengths, 8, 64, N, 2, "bf16", seed=51 + N, dt_range=(0.5, 2.0), with_init=True)
+    _check(d, 128)
+
+
 def test_many_short_sequences():
     g = torch.Generator().manual_seed(11)
     lengths = [int(v) for v in torch.randint(0, 41, (300,), generator=g)]
