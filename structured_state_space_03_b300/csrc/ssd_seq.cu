@@ -345,7 +345,9 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads, nhb = H / HB, nc = pr.nchunks;
     const Plan pl = make_plan(sa, nc);
-    constexpr uint32_t col_y = 0, col_st = 128, col_m = 192;
+    // per slot: Y, S_c; tril(G) hi | lo after each slot's S_c, shared by the jobs (phase 1
+    // accumulates S_seg in slot 1's S_c columns)
+    constexpr uint32_t col_y = 0, col_st = 128, col_mhi = 192, col_mlo = 448;
     volatile int *vfail = &s_fail;
 
     if (warp == kWMma) tmem_alloc(&tmem_slot, 512);
@@ -542,8 +544,9 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
                         mma_bf16(slot + col_st, whi, bd, id_s, k2 > 0);
                         mma_bf16(slot + col_st, wlo, bd, id_s, 1);
                         if (!wide) {
-                            mma_bf16_tA(slot + col_y, slot + col_m + k2 * 8, whi, id_d, 1);
-                            mma_bf16_tA(slot + col_y, slot + col_m + k2 * 8, wlo, id_d, 1);
+                            mma_bf16_tA(slot + col_y, tmem + col_mhi + k2 * 8, whi, id_d, 1);
+                            mma_bf16_tA(slot + col_y, tmem + col_mhi + k2 * 8, wlo, id_d, 1);
+                            mma_bf16_tA(slot + col_y, tmem + col_mlo + k2 * 8, whi, id_d, 1);
                         }
                     }
                 }
@@ -662,12 +665,15 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
                 tc_fence_after();
                 if (ok && fast) {
                     const uint32_t slot = tmem + t * 256 + lane_base;
-                    // tril(G) -> bf16 pairs in TMEM (row m, columns jb*32 .. jb*32+31)
+                    // tril(G) -> hi and lo bf16 pairs (row m) in the shared tril columns; the
+                    // previous job's diagonal MMAs, which read them, are complete: this job's G
+                    // commit follows them from the same issuing thread
+#pragma unroll 1
                     for (int jb = 0; jb < 4; ++jb) {
-                        uint32_t pk[16];
+                        uint32_t ph16[16], pl16[16];
                         if (jb > quarter) {
 #pragma unroll
-                            for (int k = 0; k < 16; ++k) pk[k] = 0u;
+                            for (int k = 0; k < 16; ++k) ph16[k] = pl16[k] = 0u;
                         } else {
                             float gv[32];
                             tmem_ld32(slot + col_y + jb * 32, gv);
@@ -678,12 +684,17 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
                             }
 #pragma unroll
                             for (int k = 0; k < 16; ++k) {
-                                __nv_bfloat162 t2 = __floats2bfloat162_rn(gv[2 * k], gv[2 * k + 1]);
-                                pk[k] = *reinterpret_cast<uint32_t *>(&t2);
+                                __nv_bfloat162 h2 = __floats2bfloat162_rn(gv[2 * k], gv[2 * k + 1]);
+                                const float2 hf = __bfloat1622float2(h2);
+                                __nv_bfloat162 l2 = __floats2bfloat162_rn(gv[2 * k] - hf.x, gv[2 * k + 1] - hf.y);
+                                ph16[k] = *reinterpret_cast<uint32_t *>(&h2);
+                                pl16[k] = *reinterpret_cast<uint32_t *>(&l2);
                             }
                         }
-                        tmem_st16(slot + col_m + jb * 16, pk);
+                        tmem_st16_async(tmem + lane_base + col_mhi + jb * 16, ph16);
+                        tmem_st16_async(tmem + lane_base + col_mlo + jb * 16, pl16);
                     }
+                    tmem_wait_st();
                     // the Y accumulator starts from D x / r (fp32, token m, every column),
                     // read while x is still in place: y = r Y + D x once the products add up
 #pragma unroll 1

@@ -328,6 +328,8 @@ WIDE = [
     (2, 513, 8, 128, 128, 2, 128, "ssd_fused_tc"),        # dstate 128, one head per unit
     (1, 300, 4, 64, 128, 1, 128, "ssd_fused_tc"),         # dstate 128, two heads per unit
     (3, 700, 4, 128, 128, 2, 100, "ssd_fused_tc"),        # chunk 100
+    (1, 3000, 16, 64, 64, 1, 128, "ssd_seq_pipe_tc"),     # 8 sequences: the sequence-pipelined kernel
+    (2, 1500, 8, 128, 64, 2, 128, "ssd_seq_pipe_tc"),
 ]
 
 
@@ -341,7 +343,8 @@ def test_wide_decay_on_each_fused_kernel(case):
 
 
 @pytest.mark.parametrize("kern,dims", [("ssd_fused_pipe_tc", (2, 512, 40, 64, 64, 1)),
-                                       ("ssd_fused_tc", (2, 512, 8, 64, 128, 2))])
+                                       ("ssd_fused_tc", (2, 512, 8, 64, 128, 2)),
+                                       ("ssd_seq_pipe_tc", (1, 3000, 16, 64, 64, 1))])
 def test_wide_and_factored_units_interleaved(kern, dims):
     """Half the heads with steps ~20x larger: wide and factored units share the
     CTAs, the look-back chain and (in the persistent kernels) the two TMEM slots."""
