@@ -37,28 +37,32 @@
 // chunk's cs range, r_i = exp(cs_i - ref), v_j = exp(ref - cs_j), so
 //     y_i = r_i [ sum_{j<=i} (C_i . B_j) wx_j + C_i . (e^ref h_c) ] + D x_i,
 //     S_c = e^(cs_last - ref) wx^T B,   wx_j = v_j dt_j x_j,
-// with one masked bf16 tril(C B^T) shared by the heads of the block, and wx and
+// with one masked tril(C B^T) shared by the heads of the block, and tril, wx and
 // e^ref h_c fed to the tensor cores as hi + lo bf16 terms.  A chunk whose cs
 // range exceeds 120 (the factors would leave range) keeps the state path with
-// the decay referenced to the chunk end and evaluates its outputs directly in
-// fp32 from G = C B^T in TMEM and h_c in shared memory.
+// the decay referenced to the chunk end and has its outputs formed by the
+// epilogue warps from the quadratic form itself: per head the masked decayed
+// matrix G_ij exp(cs_i - cs_j) dt_j (every factor <= 1 apart from G) times x on
+// the tensor cores, plus exp(cs_i) C_i . h_c.
 //
 // Warp roles (448 threads, one CTA per SM, all 512 TMEM columns):
 //   warp 0       TMA loads of dt, x, B (and C in phase 2) into a free stage
 //   warp 1       tcgen05.mma: phase 1 S_seg; phase 2 G = C B^T, S_c and the
 //                diagonal block by 16-token slices, the off-diagonal product
-//   warps 2-5    front: segment sums, decay factors, tril(G) into TMEM, wx
-//                (hi, lo) by slices
+//   warps 2-5    front: segment sums, decay factors, tril(G) (hi, lo) into
+//                TMEM, D x / r into Y, wx (hi, lo) by slices
 //   warps 6-9    state team: the published states of phase 1, the segment
 //                entry states, and the chain h_c -> h_{c+1} with the bf16 h
 //                operand of each chunk's off-diagonal product
-//   warps 10-13  epilogue: y = r Y + D x staged in shared memory and stored by
-//                TMA (or the direct evaluation of a wide chunk)
-// Stage s (job j uses s = j & 1), 96 KiB: [0, 32K) x -> wx hi -> h hi | lo
-// (h fp32 for a wide chunk); [32K, 64K) wx lo -> x for the D x term -> y;
-// [64K, 80K) B; [80K, 96K) C; then 2 KiB of dt per stage.  TMEM slot t (phase-2
-// job i uses t = i & 1) at column 256 t: Y [0,128), S_c [128,192), tril(G)
-// [192,256); phase 1 accumulates S_seg in slot 1's S_c columns.
+//   warps 10-13  epilogue: y = r Y staged in shared memory and stored by TMA
+//                (a wide chunk: x back by TMA, its MMAs issued by the leader)
+// Stage s (job j uses s = j & 1), 96 KiB: [0, 32K) x -> wx hi -> h hi | lo;
+// [32K, 64K) wx lo -> (x for a wide chunk) -> y; [64K, 80K) B; [80K, 96K) C;
+// then 2 KiB of dt per stage.  TMEM slot t (phase-2 job i uses t = i & 1) at
+// column 256 t: Y [0,128), S_c [128,192); tril(G) hi [192,256) and lo
+// [448,512) serve the job the front and the MMA warp are on (a job's G commit
+// follows the previous job's diagonal MMAs from the same thread); phase 1
+// accumulates S_seg in slot 1's S_c columns.
 #include <cuda.h>
 
 #include <algorithm>
@@ -151,89 +155,6 @@ __device__ __forceinline__ Unit unit_of(const Problem &pr, int nhb, int unit)
     u.tt = u.c * pr.chunk;
     u.len = min(pr.chunk, pr.seqlen - u.tt);
     return u;
-}
-
-// Direct fp32 outputs of a wide chunk (decay range beyond the factored form):
-// token m of the chunk, all 64-column blocks of every head of the block.  G =
-// C B^T (fp32 sums of the bf16 products) is still in the slot's Y columns, row
-// m at g_taddr.  y_m = exp(cs_m) C_m . h_c + sum_{j<=m} G_mj exp(cs_m - cs_j)
-// dt_j x_j + D x_m, the sums in `accs` ([64 columns][128 tokens] fp32 in the
-// dead staging region).  `hcs` is h_c, [128 rows (head, headdim)][NS] fp32.
-__device__ void direct_unit(const Problem &pr, size_t tok0, int len, int h0, uint32_t g_taddr, const float *hcs,
-                            float *accs, const float *cs, const float *dtv, int m)
-{
-    const int P = pr.headdim, HB = 128 / P, H = pr.nheads, G = pr.ngroups, g = h0 / (H / G);
-    const bool row = m < len;
-    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(pr.x);
-    const uint4 *crow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(pr.C) +
-                                                        ((tok0 + (row ? m : 0)) * G + g) * NS);
-    for (int hh = 0; hh < HB; ++hh) {
-        const int h = h0 + hh;
-        const float *csh = cs + hh * kRows, *dth = dtv + hh * kRows;
-        const float csm = csh[m], ecs = expf(csm);
-        const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
-        for (int pc = 0; pc < P; pc += 64) {
-            for (int p = 0; p < 64; ++p) {  // exp(cs_m) C_m . h_c
-                const float *hr = hcs + (size_t)(hh * P + pc + p) * NS;
-                float off = 0.f;
-                if (row) {
-#pragma unroll
-                    for (int q = 0; q < NS / 8; ++q) {
-                        const uint4 cv = __ldg(crow + q);
-                        const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&cv);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 t = __bfloat1622float2(c2[e]);
-                            off = fmaf(t.x, hr[8 * q + 2 * e], off);
-                            off = fmaf(t.y, hr[8 * q + 2 * e + 1], off);
-                        }
-                    }
-                }
-                accs[p * kRows + m] = ecs * off;
-            }
-            for (int jb = 0; jb < 8; ++jb) {  // + sum_{j <= m} G_mj exp(cs_m - cs_j) dt_j x_j
-                float gv[16];
-                tmem_ld16(g_taddr + jb * 16, gv);  // warp-collective: every lane, every row
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int j = jb * 16 + k;
-                    if (!row || j > m) continue;
-                    const float w = gv[k] * expf(csm - csh[j]) * dth[j];
-                    const uint4 *xr = reinterpret_cast<const uint4 *>(x + ((tok0 + j) * H + h) * P + pc);
-#pragma unroll 1
-                    for (int q = 0; q < 8; ++q) {
-                        const uint4 xv = __ldg(xr + q);
-                        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 t = __bfloat1622float2(x2[e]);
-                            float *a0 = accs + (8 * q + 2 * e) * kRows + m;
-                            a0[0] = fmaf(w, t.x, a0[0]);
-                            a0[kRows] = fmaf(w, t.y, a0[kRows]);
-                        }
-                    }
-                }
-            }
-            if (row) {  // + D x_m, rounded to bf16 and stored
-                const size_t base = ((tok0 + m) * H + h) * P + pc;
-                const uint4 *xm = reinterpret_cast<const uint4 *>(x + base);
-                uint4 *ym = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) + base);
-#pragma unroll 1
-                for (int q = 0; q < 8; ++q) {
-                    const uint4 xv = __ldg(xm + q);
-                    const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-                    float o[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 t = __bfloat1622float2(x2[e]);
-                        o[2 * e] = fmaf(Dh, t.x, accs[(8 * q + 2 * e) * kRows + m]);
-                        o[2 * e + 1] = fmaf(Dh, t.y, accs[(8 * q + 2 * e + 1) * kRows + m]);
-                    }
-                    ym[q] = pack8(o);
-                }
-            }
-        }
-    }
 }
 
 // The entry state of a segment whose predecessor segment ends in slot k (state
@@ -331,6 +252,9 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
     __shared__ __align__(8) uint64_t bar_full[2], bar_dt[2], bar_free[2], bar_lo[2], bar_slice[2][kSlices];
     __shared__ __align__(8) uint64_t bar_g[2], bar_mask[2], bar_mma[2], bar_hop[2], bar_yo[2], bar_slot[2];
     __shared__ __align__(8) uint64_t bar_seg[4], bar_epi[4], bar_agg, bar_aggs, bar_aggread, bar_drain;
+    // wide jobs: S_c read by the state team (per slot), x back in the staging region, the
+    // epilogue leader's MMA steps
+    __shared__ __align__(8) uint64_t bar_scr[2], bar_xe, bar_wd;
     __shared__ uint32_t tmem_slot;
     __shared__ float cs[4][2 * kRows], dtv[4][2 * kRows], rs[4][2 * kRows], vwf[2 * kRows];
     __shared__ float s_alpha[4][2], s_sfac[4][2], s_ysc[4][2], s_aseg[2];
@@ -373,6 +297,10 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
         mbar_init(&bar_aggs, 128);
         mbar_init(&bar_aggread, 1);
         mbar_init(&bar_drain, 1);
+        mbar_init(&bar_scr[0], 1);
+        mbar_init(&bar_scr[1], 1);
+        mbar_init(&bar_xe, 1);
+        mbar_init(&bar_wd, 1);
         mbar_fence_init();
         s_fail = 0;
     }
@@ -845,25 +773,18 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
             }
             ok = mbar_wait(&bar_mma[t], (i >> 1) & 1, lim) && mbar_wait(&bar_seg[q], (i >> 2) & 1, lim);
             tc_fence_after();
-            const bool wide = s_wide[q] != 0;
             uint8_t *st = base + s * kStageBytes;
-            if (ok) {
-                if (!wide) {  // e^ref h_c -> bf16 hi / lo K-major slabs over the dead wx hi
-                    const float ysc = s_ysc[q][hh_m];
+            if (ok) {  // e^ref h_c -> bf16 hi / lo K-major slabs over the dead wx hi (ref = 0 if wide)
+                const float ysc = s_ysc[q][hh_m];
 #pragma unroll
-                    for (int q8 = 0; q8 < NS / 8; ++q8) {
-                        float f[8];
+                for (int q8 = 0; q8 < NS / 8; ++q8) {
+                    float f[8];
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) f[k] = ysc * h[8 * q8 + k];
-                        uint4 hi, lo;
-                        split8(f, hi, lo);
-                        *reinterpret_cast<uint4 *>(st + sw128(m, q8)) = hi;
-                        *reinterpret_cast<uint4 *>(st + kSlab + sw128(m, q8)) = lo;
-                    }
-                } else {  // the direct evaluation reads h_c in fp32
-                    float4 *hs = reinterpret_cast<float4 *>(st) + (size_t)m * (NS / 4);
-#pragma unroll
-                    for (int q4 = 0; q4 < NS / 4; ++q4) hs[q4] = make_float4(h[4 * q4], h[4 * q4 + 1], h[4 * q4 + 2], h[4 * q4 + 3]);
+                    for (int k = 0; k < 8; ++k) f[k] = ysc * h[8 * q8 + k];
+                    uint4 hi, lo;
+                    split8(f, hi, lo);
+                    *reinterpret_cast<uint4 *>(st + sw128(m, q8)) = hi;
+                    *reinterpret_cast<uint4 *>(st + kSlab + sw128(m, q8)) = lo;
                 }
             }
             fence_async_smem();
@@ -884,7 +805,10 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
             }
             tc_fence_before();
             named_sync(kBarState, 128);
-            if (tt == 0) mbar_arrive(&bar_slot[t]);  // S_c read (the epilogue gives the other arrival)
+            if (tt == 0) {
+                mbar_arrive(&bar_slot[t]);  // S_c read (the epilogue gives the other arrival)
+                mbar_arrive(&bar_scr[t]);   // a wide job's epilogue reuses S_c's columns
+            }
             if (u.c == nc - 1 && pr.final_state) {
                 float4 *fo = reinterpret_cast<float4 *>(pr.final_state +
                                                         (((size_t)u.b * H + u.h0 + hh_m) * P + p_m) * NS);
@@ -900,6 +824,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
         // full 128-row tiles go out by TMA (rows past the sequence end are clipped);
         // shorter chunks row by row, since the tile's later rows belong to the next chunk
         const bool tma_out = pr.chunk == kRows;
+        int nxe = 0, nwd = 0;  // completed phases of bar_xe and bar_wd (wide jobs only)
         for (int i = 0; i < pl.n2; ++i) {
             if (named_sync_or(kBarEpi, 128, *vfail != 0)) break;
             const int j = i + pl.n1, s = j & 1, t = i & 1, q = i & 3;
@@ -909,13 +834,14 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
             bool ok = mbar_wait(&bar_seg[q], (i >> 2) & 1, lim);
             const bool wide = s_wide[q] != 0;
             ok = ok && mbar_wait(&bar_yo[t], (i >> 1) & 1, lim);
+            if (wide) ok = ok && mbar_wait(&bar_scr[t], (i >> 1) & 1, lim);
             ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
             tc_fence_after();
             const uint32_t slot = tmem + t * 256 + lane_base;
+            const bool row_in = m < u.len;
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
+                                                   (((size_t)u.b * pr.seqlen + u.tt + (row_in ? m : 0)) * H + u.h0) * P);
             if (ok && !wide) {
-                const bool row_in = m < u.len;
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(pr.y) +
-                                                       (((size_t)u.b * pr.seqlen + u.tt + (row_in ? m : 0)) * H + u.h0) * P);
 #pragma unroll 1
                 for (int col = 0; col < 128; col += 64) {
                     const float r = rs[q][(col / P) * kRows + m];
@@ -934,33 +860,205 @@ __global__ void __launch_bounds__(kSeqThreads, 1)
                     }
                 }
             }
+            if (wide) {
+                // A wide job has no rank-one decay (its outputs are not in Y: the diagonal
+                // product was skipped and G = C B^T is still in Y's columns).  Per head, the
+                // masked decayed matrix M[m][j] = G_mj e^(cs_m - cs_j) dt_j (j <= m; every factor
+                // <= 1 apart from G) is formed in place over G as hi | lo bf16 pairs (16 columns
+                // per 16 tokens) and multiplied with x, brought back into the staging region by
+                // TMA (exact in bf16), into S_c's columns (read by the state team); 64 output
+                // columns at a time, each finished in shared memory before the next:
+                //   two heads:  Y_off = C h_hh^T in Y's first 64 columns once M_hh is consumed,
+                //               y = Y_diag + e^cs Y_off + D x; the next head's M needs G again
+                //               (C B^T once more: the stage's B and C are still in place);
+                //   one head:   C' = e^cs C (hi, lo over the dead B and over C) joins the same
+                //               accumulator, y = (M x + C' h^T) + D x.
+                // The h operand (e^0 h_c, hi and lo) is the state team's.  The leader (et == 0)
+                // issues the MMAs and waits for each step before the next overwrites its inputs.
+                const uint32_t sbase = tmem + t * 256;
+                const uint32_t sa = smem_u32(st);
+                bool okd = ok;
+                auto team_sync = [&]() {
+                    tc_fence_before();
+                    okd = !named_sync_or(kBarEpi, 128, !okd);
+                    tc_fence_after();
+                };
+                auto lead_commit_wait = [&]() {
+                    mma_commit(&bar_wd);
+                    okd = mbar_wait(&bar_wd, nwd & 1, lim);
+                    ++nwd;
+                };
+                team_sync();
+                if (et == 0) {  // x into the staging region (wx lo is dead: the chunk state is complete)
+                    if (okd) {
+                        mbar_expect_tx(&bar_xe, (uint32_t)(2 * kSlab));
+                        for (int k = 0; k < 2; ++k)
+                            tma_load_3d(ystage + k * kSlab, &xmap, &bar_xe, u.hb * 128 + 64 * k, u.tt, u.b);
+                    } else {
+                        mbar_arrive(&bar_xe);
+                    }
+                }
+                // x and C are read by every thread below: acquire their loads
+                okd = mbar_wait(&bar_xe, nxe & 1, lim) && okd && mbar_wait(&bar_full[s], (j >> 1) & 1, lim);
+                ++nxe;
+                team_sync();
+                auto build_m = [&](int hh) {  // M_hh over G, row m = this thread's TMEM lane
+                    const float csm = cs[q][hh * kRows + m];
+                    const float *csb = cs[q] + hh * kRows, *dtb = dtv[q] + hh * kRows;
+#pragma unroll 1
+                    for (int jb = 0; jb < 8; ++jb) {
+                        uint32_t pk[16];  // 8 hi pairs, then 8 lo pairs
+                        if (jb <= 2 * quarter + 1) {  // warp-uniform: some row of this warp reaches 16 jb
+                            float gv[16];
+                            tmem_ld16(slot + col_y + jb * 16, gv);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                float f2[2];
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const int jj = jb * 16 + 2 * k + e;
+                                    const float w = __expf(csm - csb[jj]) * dtb[jj];
+                                    f2[e] = jj <= m ? gv[2 * k + e] * w : 0.f;
+                                }
+                                __nv_bfloat162 h2 = __floats2bfloat162_rn(f2[0], f2[1]);
+                                const float2 hf = __bfloat1622float2(h2);
+                                __nv_bfloat162 l2 = __floats2bfloat162_rn(f2[0] - hf.x, f2[1] - hf.y);
+                                pk[k] = *reinterpret_cast<uint32_t *>(&h2);
+                                pk[8 + k] = *reinterpret_cast<uint32_t *>(&l2);
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) pk[k] = 0u;
+                        }
+                        tmem_st16(slot + col_y + jb * 16, pk);
+                    }
+                };
+                // y for the 64 columns `pb` of the job (x slab pb / 64) from the accumulators
+                auto finish64 = [&](int pb, float r, bool with_off) {
+                    const int h = u.h0 + pb / P;
+                    const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
+#pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        float yd[32], yo[32];
+                        tmem_ld32(slot + col_st + 32 * hf, yd);
+                        if (with_off) tmem_ld32(slot + col_y + 32 * hf, yo);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uint4 *sp = reinterpret_cast<uint4 *>(ystage + (pb / 64) * kSlab + sw128(m, 4 * hf + k));
+                            const uint4 xv = *sp;
+                            const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                            float o[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float2 xf = __bfloat1622float2(x2[e / 2]);
+                                const float yoff = with_off ? r * yo[8 * k + e] : 0.f;
+                                o[e] = fmaf(Dh, (e & 1) ? xf.y : xf.x, yd[8 * k + e] + yoff);
+                            }
+                            const uint4 ov = pack8(o);
+                            if (tma_out)
+                                *sp = ov;
+                            else if (row_in)
+                                dst[pb / 8 + 4 * hf + k] = ov;
+                        }
+                    }
+                };
+                const uint32_t id64 = idesc_bf16(128, 64, 0, 1), id64k = idesc_bf16(128, 64, 0, 0);
+                if (HB == 2) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (hh > 0 && et == 0 && okd) {  // G again, over the consumed M and Y_off
+                            for (int ks = 0; ks < NS / 16; ++ks)
+                                mma_bf16(sbase + col_y, sdesc_sw128(sa + 5 * kSlab + ks * 32, 16, 1024),
+                                         sdesc_sw128(sa + 4 * kSlab + ks * 32, 16, 1024), idesc_bf16(128, 128, 0, 0), ks > 0);
+                            lead_commit_wait();
+                        }
+                        team_sync();
+                        if (okd) build_m(hh);
+                        team_sync();
+                        if (et == 0 && okd) {
+                            for (int ks = 0; ks < kRows / 16; ++ks) {
+                                const uint64_t xd = sdesc_sw128(sa + 2 * kSlab + hh * kSlab + ks * 2048, kSlab, 1024);
+                                mma_bf16_tA(sbase + col_st, sbase + col_y + 16 * ks, xd, id64, ks > 0);
+                                mma_bf16_tA(sbase + col_st, sbase + col_y + 16 * ks + 8, xd, id64, 1);
+                            }
+                            lead_commit_wait();
+                            if (okd) {  // Y_off = C h_hh^T (rows 64 hh of the h operand), over M
+                                tc_fence_after();
+                                for (int ks = 0; ks < NS / 16; ++ks) {
+                                    const uint64_t ad = sdesc_sw128(sa + 5 * kSlab + ks * 32, 16, 1024);
+                                    mma_bf16(sbase + col_y, ad, sdesc_sw128(sa + hh * 8192 + ks * 32, 16, 1024), id64k,
+                                             ks > 0);
+                                    mma_bf16(sbase + col_y, ad, sdesc_sw128(sa + kSlab + hh * 8192 + ks * 32, 16, 1024),
+                                             id64k, 1);
+                                }
+                                lead_commit_wait();
+                            }
+                        }
+                        team_sync();
+                        if (okd) finish64(64 * hh, rs[q][hh * kRows + m], true);
+                        team_sync();  // the outputs are read before the next head overwrites them
+                    }
+                } else {
+                    if (okd) {
+                        build_m(0);
+                        // C' = e^cs C for row m: hi over the dead B, lo over C
+                        const float ec = rs[q][m];
+#pragma unroll
+                        for (int q8 = 0; q8 < NS / 8; ++q8) {
+                            const uint4 cv = *reinterpret_cast<const uint4 *>(st + 5 * kSlab + sw128(m, q8));
+                            const __nv_bfloat162 *c2 = reinterpret_cast<const __nv_bfloat162 *>(&cv);
+                            float f[8];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 cf = __bfloat1622float2(c2[e]);
+                                f[2 * e] = ec * cf.x;
+                                f[2 * e + 1] = ec * cf.y;
+                            }
+                            uint4 hi, lo;
+                            split8(f, hi, lo);
+                            *reinterpret_cast<uint4 *>(st + 4 * kSlab + sw128(m, q8)) = hi;
+                            *reinterpret_cast<uint4 *>(st + 5 * kSlab + sw128(m, q8)) = lo;
+                        }
+                    }
+                    fence_async_smem();
+                    team_sync();
+                    for (int pb = 0; pb < 128; pb += 64) {
+                        if (et == 0 && okd) {
+                            for (int ks = 0; ks < kRows / 16; ++ks) {
+                                const uint64_t xd = sdesc_sw128(sa + 2 * kSlab + (pb / 64) * kSlab + ks * 2048, kSlab, 1024);
+                                mma_bf16_tA(sbase + col_st, sbase + col_y + 16 * ks, xd, id64, ks > 0);
+                                mma_bf16_tA(sbase + col_st, sbase + col_y + 16 * ks + 8, xd, id64, 1);
+                            }
+                            for (int ks = 0; ks < NS / 16; ++ks) {
+                                const uint64_t chi = sdesc_sw128(sa + 4 * kSlab + ks * 32, 16, 1024);
+                                const uint64_t clo = sdesc_sw128(sa + 5 * kSlab + ks * 32, 16, 1024);
+                                const uint64_t hhi = sdesc_sw128(sa + (pb / 64) * 8192 + ks * 32, 16, 1024);
+                                const uint64_t hlo = sdesc_sw128(sa + kSlab + (pb / 64) * 8192 + ks * 32, 16, 1024);
+                                mma_bf16(sbase + col_st, chi, hhi, id64k, 1);
+                                mma_bf16(sbase + col_st, chi, hlo, id64k, 1);
+                                mma_bf16(sbase + col_st, clo, hhi, id64k, 1);
+                            }
+                            lead_commit_wait();
+                        }
+                        team_sync();
+                        if (okd) finish64(pb, 0.f, false);
+                        team_sync();  // S_c's columns are read before the next block overwrites them
+                    }
+                }
+                if (et == 0 && okd) mbar_arrive(&bar_free[s]);  // every MMA of the job is complete
+                ok = okd;
+            }
             fence_async_smem();
             tc_fence_before();
             const bool all_ok = !named_sync_or(kBarEpi, 128, !ok);
-            if (!(all_ok && wide)) {
-                if (et == 0) {
-                    mbar_arrive(&bar_slot[t]);  // Y read
-                    mbar_arrive(&bar_epi[q]);   // the job's scalars read
-                    if (all_ok && tma_out) {
-                        for (int k = 0; k < 2; ++k)
-                            tma_store_3d(&ymap, ystage + k * kSlab, u.hb * 128 + 64 * k, u.tt, u.b);
-                        bulk_commit();
-                        bulk_wait_read_all();
-                    }
-                    mbar_arrive(&bar_lo[s]);  // the staging region is free again
+            if (et == 0) {
+                mbar_arrive(&bar_slot[t]);  // Y (and, for a wide job, every column of the slot) read
+                mbar_arrive(&bar_epi[q]);   // the job's scalars read
+                if (all_ok && tma_out) {
+                    for (int k = 0; k < 2; ++k) tma_store_3d(&ymap, ystage + k * kSlab, u.hb * 128 + 64 * k, u.tt, u.b);
+                    bulk_commit();
+                    bulk_wait_read_all();
                 }
-            } else {
-                tc_fence_after();
-                direct_unit(pr, (size_t)u.b * pr.seqlen + u.tt, u.len, u.h0, slot + col_y,
-                            reinterpret_cast<const float *>(st), reinterpret_cast<float *>(ystage), cs[q], dtv[q], m);
-                tc_fence_before();
-                named_sync(kBarEpi, 128);  // every thread is done with the stage and the slot
-                if (et == 0) {
-                    mbar_arrive(&bar_slot[t]);
-                    mbar_arrive(&bar_epi[q]);
-                    mbar_arrive(&bar_lo[s]);
-                    mbar_arrive(&bar_free[s]);
-                }
+                mbar_arrive(&bar_lo[s]);  // the staging region is free again
             }
             if (!all_ok) {
                 *vfail = 1;
