@@ -544,6 +544,7 @@ def workload_record(w, dev, stream, peaks, steps=20):
     t_hbm = unavoidable_bytes(w) / (peaks["hbm_gbs"] * 1e9)
     t_tc = causal_flops(w) / (peaks["bf16_tflops"] * 1e12)
     rec = {"ms_per_step": ms, "tokens_per_s": w.tokens / (ms * 1e-3), "path": ssd.ssd_fwd_path(*dims, dtype),
+           "block": ssd.ssd_fwd_block(*dims, dtype),  # the chunk length evaluated (exact for any length)
            "unavoidable_bytes": unavoidable_bytes(w), "causal_flops": causal_flops(w),
            "roofline_ms": max(t_hbm, t_tc) * 1e3, "bound": "hbm" if t_hbm >= t_tc else "tensor",
            "frac": max(t_hbm, t_tc) * 1e3 / ms, "steps": steps,
@@ -814,7 +815,7 @@ def main():
         "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": workload_config(w),
-        "run": {"path": path, "kernels": kernels,
+        "run": {"path": path, "block": ssd.ssd_fwd_block(*dims, dtype), "kernels": kernels,
                 "timing": f"CUDA events around graph replays of the {steps} steps ({len(graphs)} graph(s))",
                 "l2": f"inputs rotate over {nsets} device copies ({nsets * per_set / 2**20:.0f} MiB > 126 MB L2)"},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": dom_gbs, "peak": peaks["hbm_gbs"],

@@ -71,7 +71,8 @@ typedef enum {
     SSD_PATH_TCGEN05 = 1,        /* bf16 chunked kernels on tcgen05 tensor cores, TMEM accumulators:
                                     chunk states, state passing, outputs */
     SSD_PATH_TCGEN05_FUSED = 2   /* one bf16 tcgen05 kernel; chunk-to-chunk states resolved by a
-                                    decoupled look-back (headdim 64/128, dstate 64/128, chunk <= 128) */
+                                    decoupled look-back (headdim 64/128, dstate 64/128, blocks of at
+                                    most 128 tokens) */
 } ssd_path_t;
 
 /*
@@ -89,7 +90,9 @@ typedef enum {
  *                                                           NULL skips it
  *   chunk       block length Q of the decomposition, 1..256 (the result does
  *               not depend on it beyond rounding); seqlen need not be a
- *               multiple of it.
+ *               multiple of it.  Where a fused kernel covers the sizes, a
+ *               chunk longer than 128 is evaluated as equal blocks of at most
+ *               128 tokens (ssd_fwd_block tells the length used).
  *
  * A device workspace of ssd_fwd_workspace_size() bytes is taken from the
  * stream-ordered allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
@@ -162,7 +165,7 @@ SSD_API ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A
  * workspace it uses a fixed 32 MiB scratch array compiled into the library,
  * which every device that loads the library holds until the process exits; it
  * calls no allocator at all.  It runs the fused bf16 kernel only (bf16,
- * headdim 64 or 128, dstate 64 or 128, chunk <= 128) and returns
+ * headdim 64 or 128, dstate 64 or 128) and returns
  * SSD_ERR_UNSUPPORTED, with the needed and available sizes in
  * ssd_last_error_detail(), for anything else or for a problem whose scratch
  * (ssd_fwd_workspace_size) exceeds 32 MiB.  At dstate 64 the scratch is one
@@ -352,6 +355,20 @@ SSD_API int ssd_bwd_kernels(int batch, int seqlen, int nheads, int headdim, int 
  */
 SSD_API ssd_path_t ssd_fwd_path(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate,
                         int chunk, ssd_dtype_t dtype);
+
+/*
+ * ssd_fwd_block -- the chunk length ssd_fwd evaluates for these sizes, or -1
+ * when they are rejected.  Pure host function: no CUDA call.  The block
+ * decomposition ("Mamba 模型" §4.1) is exact for any chunk length: a requested
+ * chunk longer than 128 tokens is evaluated as equal blocks of at most 128
+ * (256 -> 128, 200 -> 100) whenever the sizes take a fused kernel (bf16,
+ * headdim 64/128, dstate 64/128); the outputs then differ from the requested
+ * length only in rounding.  Otherwise the requested chunk itself.  ssd_fwd,
+ * ssd_fwd_varlen, ssd_fwd_host, ssd_fwd_pre and the workspace and kernel queries
+ * all use this length.
+ */
+SSD_API int ssd_fwd_block(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk,
+                          ssd_dtype_t dtype);
 
 /*
  * ssd_fwd_kernels -- how many kernels one ssd_fwd launches for these sizes,

@@ -6,7 +6,7 @@ step of the computation runs in the library's CUDA kernels.  PyTorch is used
 for device memory and streams only.  The functions carry the C names:
 
     ssd_fwd, ssd_fwd_ws, ssd_fwd_host, ssd_fwd_pre, ssd_fwd_varlen, ssd_fwd_noalloc, ssd_fwd_workspace_size,
-    ssd_fwd_path, ssd_step, ssd_fwd_kernels, ssd_bwd, ssd_bwd_workspace_size, ssd_bwd_kernels,
+    ssd_fwd_path, ssd_fwd_block, ssd_step, ssd_fwd_kernels, ssd_bwd, ssd_bwd_workspace_size, ssd_bwd_kernels,
     ssd_profile_events, ssd_test_set_fault,
     ssd_check_device_status, ssd_status_string, ssd_last_error_detail, ssd_version
 
@@ -54,6 +54,7 @@ SIGNATURES = {
     "ssd_bwd_kernels": (_I, [_I] * 7 + [ctypes.c_char_p, _S]),
     "ssd_fwd_workspace_size": (_I, _DIMS + [ctypes.POINTER(ctypes.c_size_t)]),
     "ssd_fwd_path": (_I, _DIMS),
+    "ssd_fwd_block": (_I, _DIMS),
     "ssd_fwd_kernels": (_I, _DIMS + [ctypes.c_char_p, _S]),
     "ssd_profile_events": (_I, [ctypes.POINTER(_P), _I]),
     "ssd_check_device_status": (_I, [_P]),
@@ -367,6 +368,12 @@ def ssd_fwd_host(x, dt, A, B, C, D=None, init_state=None, *, chunk: int, y=None,
 def ssd_fwd_path(batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype) -> str:
     code = _dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype)
     return PATH_NAMES[lib().ssd_fwd_path(batch, seqlen, nheads, headdim, ngroups, dstate, chunk, code)]
+
+
+def ssd_fwd_block(batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype) -> int:
+    """The chunk length ssd_fwd evaluates for these sizes (-1 when they are rejected)."""
+    code = _dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(lib().ssd_fwd_block(batch, seqlen, nheads, headdim, ngroups, dstate, chunk, code))
 
 
 def ssd_fwd_kernels(batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype) -> list:

@@ -111,6 +111,20 @@ static ssd_status_t check_dims(Problem &pr, int batch, int seqlen, int nheads, i
     pr.chunk = chunk;
     pr.nchunks = (seqlen + chunk - 1) / chunk;
     pr.dtype = dtype;
+    // The block decomposition is exact for any chunk length, so a chunk longer than the
+    // fused kernels' 128-token tile is evaluated as equal blocks of at most 128 tokens
+    // whenever a fused kernel covers the sizes (one kernel instead of three, no chunk
+    // states in HBM).  The results differ from the requested length only in rounding.
+    if (chunk > kFusedTile) {
+        Problem q = pr;
+        const int nb = (chunk + kFusedTile - 1) / kFusedTile;
+        q.chunk = (chunk + nb - 1) / nb;
+        q.nchunks = (seqlen + q.chunk - 1) / q.chunk;
+        if (fused_supported(q)) {
+            pr.chunk = q.chunk;
+            pr.nchunks = q.nchunks;
+        }
+    }
     return SSD_OK;
 }
 
@@ -217,6 +231,15 @@ ssd_path_t ssd_fwd_path(int batch, int seqlen, int nheads, int headdim, int ngro
     return choose_path(pr);
 }
 
+int ssd_fwd_block(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk,
+                  ssd_dtype_t dtype)
+{
+    Problem pr;
+    memset(&pr, 0, sizeof pr);
+    if (check_dims(pr, batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype) != SSD_OK) return -1;
+    return pr.chunk;
+}
+
 int ssd_fwd_kernels(int batch, int seqlen, int nheads, int headdim, int ngroups, int dstate, int chunk,
                     ssd_dtype_t dtype, char *names, size_t names_len)
 {
@@ -315,7 +338,9 @@ ssd_status_t ssd_fwd_varlen(const void *x, const float *dt, const float *A, cons
     ssd_status_t st = make_problem(pr, x, dt, A, B, C, D, init_state, y, final_state, nseq, total, nheads, headdim,
                                    ngroups, dstate, chunk, dtype);
     if (st != SSD_OK) return st;
-    // chunk table in chunk-major order (a counting sort over the chunk index)
+    // chunk table in chunk-major order (a counting sort over the chunk index), in chunks of
+    // the evaluated block length
+    chunk = pr.chunk;
     std::vector<int> nchunk(nseq);
     int max_nc = 0;
     size_t total_chunks = 0;
@@ -476,7 +501,7 @@ ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float *A, con
     if (choose_path(pr) != SSD_PATH_TCGEN05_FUSED)
         return fail(SSD_ERR_UNSUPPORTED,
                     "ssd_fwd_noalloc runs the fused bf16 kernel only (bf16, headdim 64 or 128, dstate 64 or "
-                    "128, chunk <= 128)");
+                    "128)");
     const size_t need = workspace_bytes(pr);
     if (need > kNoAllocScratchBytes)
         return fail(SSD_ERR_UNSUPPORTED,
@@ -545,6 +570,7 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
     memset(&pr, 0, sizeof pr);
     ssd_status_t st = check_dims(pr, batch, seqlen, nheads, headdim, ngroups, dstate, chunk, dtype);
     if (st != SSD_OK) return st;
+    chunk = pr.chunk;  // the evaluated block length: the parts are cut at its multiples
     if (!x || !dt || !A || !B || !C || !y)
         return fail(SSD_ERR_INVALID_ARG, "x, dt, A, B, C and y must be non-NULL");
     HostCopyRes *res = nullptr;

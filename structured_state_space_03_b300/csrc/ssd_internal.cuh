@@ -194,6 +194,7 @@ void profile_kernel_begin(cudaStream_t s);  // right before a kernel launch, aft
 void profile_kernel_end(cudaStream_t s);    // right after it
 
 constexpr int kMaxChunk = 256;
+constexpr int kFusedTile = 128;  // tokens per tile (TMEM lanes) of the fused kernels
 constexpr int kMaxHeaddim = 256;
 constexpr int kMaxDstate = 256;
 

@@ -123,11 +123,11 @@ def test_path_selection_is_a_pure_host_query(lib):
     assert ssd.ssd_fwd_path(1, 256, 4, 16, 1, 16, 64, ssd.SSD_DTYPE_F32) == "simt"
     assert ssd.ssd_fwd_path(1, 256, 4, 16, 1, 16, 999, ssd.SSD_DTYPE_F32) == "none"
     assert ssd.ssd_fwd_path(1, 256, 4, 16, 3, 16, 64, ssd.SSD_DTYPE_F32) == "none"
-    # bf16 with headdim 64/128, dstate 64/128 and chunk <= 128: one fused tcgen05 kernel;
-    # dstate 256 or chunk up to 256: the three-kernel tcgen05 path
+    # bf16 with headdim 64/128 and dstate 64/128: one fused tcgen05 kernel (a chunk longer
+    # than 128 evaluated as equal blocks of at most 128); dstate 256: the three-kernel path
     assert ssd.ssd_fwd_path(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == "tcgen05_fused"
     assert ssd.ssd_fwd_path(16, 4096, 32, 128, 8, 128, 128, ssd.SSD_DTYPE_BF16) == "tcgen05_fused"
-    assert ssd.ssd_fwd_path(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == "tcgen05"
+    assert ssd.ssd_fwd_path(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == "tcgen05_fused"
     assert ssd.ssd_fwd_path(1, 131072, 24, 64, 1, 256, 256, ssd.SSD_DTYPE_BF16) == "tcgen05"
     assert ssd.ssd_fwd_path(1, 1000, 4, 64, 1, 256, 128, ssd.SSD_DTYPE_BF16) == "tcgen05"
     assert ssd.ssd_fwd_path(2, 333, 6, 32, 3, 48, 100, ssd.SSD_DTYPE_BF16) == "simt"
@@ -135,8 +135,27 @@ def test_path_selection_is_a_pure_host_query(lib):
     assert ssd.ssd_fwd_kernels(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == ["ssd_fused_pipe_tc"]
     assert ssd.ssd_fwd_kernels(1, 65536, 8, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == ["ssd_seq_pipe_tc"]
     assert ssd.ssd_fwd_kernels(16, 4096, 32, 128, 8, 128, 128, ssd.SSD_DTYPE_BF16) == ["ssd_fused_tc"]
-    assert ssd.ssd_fwd_kernels(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == [
+    assert ssd.ssd_fwd_kernels(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == ["ssd_fused_tc"]
+    assert ssd.ssd_fwd_kernels(1, 131072, 24, 64, 1, 256, 256, ssd.SSD_DTYPE_BF16) == [
         "chunk_state_tc", "state_pass", "chunk_out_tc"]
+
+
+def test_block_length_of_long_chunks(lib):
+    # the evaluated chunk length: at most 128 on the fused paths, the requested one elsewhere
+    B = ssd.SSD_DTYPE_BF16
+    assert ssd.ssd_fwd_block(1, 8192, 80, 64, 1, 128, 256, B) == 128
+    assert ssd.ssd_fwd_block(2, 2048, 80, 64, 1, 64, 200, B) == 100
+    assert ssd.ssd_fwd_block(2, 2048, 80, 64, 1, 64, 129, B) == 65
+    assert ssd.ssd_fwd_block(2, 2048, 80, 64, 1, 64, 96, B) == 96
+    assert ssd.ssd_fwd_block(1, 131072, 24, 64, 1, 256, 256, B) == 256   # dstate 256: three-kernel path
+    assert ssd.ssd_fwd_block(1, 1000, 4, 32, 1, 64, 256, B) == 256       # headdim 32: SIMT path
+    assert ssd.ssd_fwd_block(1, 1000, 4, 64, 1, 64, 256, ssd.SSD_DTYPE_F32) == 256
+    assert ssd.ssd_fwd_block(1, 1000, 4, 64, 1, 64, 999, B) == -1
+    # the workspace follows the evaluated length
+    n256, n128 = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.ssd_fwd_workspace_size(1, 8192, 80, 64, 1, 128, 256, B, ctypes.byref(n256)) == ssd.SSD_OK
+    assert lib.ssd_fwd_workspace_size(1, 8192, 80, 64, 1, 128, 128, B, ctypes.byref(n128)) == ssd.SSD_OK
+    assert n256.value == n128.value
 
 
 def _step(lib, x=1, dt=1, A=1, B=1, C=1, state=1, y=1, **over):
