@@ -82,6 +82,18 @@ def test_backward_matches_oracle(case):
     _compare(_gpu(inp, dy, dfinal), _ref(inp, dy, dfinal), str(case))
 
 
+@pytest.mark.parametrize("case", [(2, 300, 8, 64, 64, 2, "bf16"), (1, 260, 4, 128, 64, 2, "bf16"), (1, 200, 4, 32, 48, 2, "f32")],
+                         ids=["tensor_core", "simt_bf16", "simt_f32"])
+def test_backward_with_large_steps(case):
+    # steps of 0.5 .. 2 with |A| up to 16: the decay inside a chunk spans hundreds of e-folds;
+    # every factor the kernels form is exp of a difference of segment sums in the decaying
+    # direction, so none can overflow
+    b, L, H, P, N, G, dt = case
+    inp = make_inputs(b, L, H, P, N, G, dt, seed=600 + L, dt_range=(0.5, 2.0), with_init=True)
+    dy, dfinal = make_cotangents(b, L, H, P, N, dt, seed=600 + L)
+    _compare(_gpu(inp, dy, dfinal), _ref(inp, dy, dfinal), f"large steps {case}")
+
+
 def test_optional_outputs_and_determinism():
     b, L, H, P, N, G = 2, 150, 4, 64, 64, 2
     inp = make_inputs(b, L, H, P, N, G, "bf16", seed=77, with_init=True)
