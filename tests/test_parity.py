@@ -224,6 +224,22 @@ def test_host_buffer_entry_matches_device_entry(dtype):
     assert_close(fh.numpy(), fr, TOL[yd.dtype], "final state, host entry vs oracle")
 
 
+# The largest sizes the library accepts: headdim, dstate and chunk at 256 together
+# (fp32 kernels for headdim 256, the three-kernel tensor-core path at headdim 128),
+# and many heads and batch elements (grid dimensions).
+MAX_CASES = [(1, 600, 2, 256, 256, 1, 256, "bf16", "simt"), (1, 520, 2, 256, 256, 2, 256, "f32", "simt"),
+             (1, 700, 4, 128, 256, 2, 256, "bf16", "tcgen05"), (2, 130, 1024, 16, 16, 8, 64, "f32", "simt"),
+             (300, 40, 2, 64, 64, 1, 32, "bf16", "tcgen05_fused")]
+
+
+@pytest.mark.parametrize("case", MAX_CASES, ids=[f"b{c[0]}L{c[1]}H{c[2]}P{c[3]}N{c[4]}Q{c[6]}{c[7]}" for c in MAX_CASES])
+def test_maximum_sizes(case):
+    b, L, H, P, N, G, Q, dtype, path = case
+    assert ssd.ssd_fwd_path(b, L, H, P, G, N, Q, torch.float32 if dtype == "f32" else torch.bfloat16) == path
+    inp = make_inputs(b, L, H, P, N, G, dtype, seed=17 + P + H, with_init=True)
+    check_full(inp, Q)
+
+
 # The host entry overlaps copies and compute over parts: batch groups (batch >= 4)
 # or whole-chunk token ranges with the state carried between them (batch < 4);
 # shapes whose token rows are not 16-byte multiples run as one part.
