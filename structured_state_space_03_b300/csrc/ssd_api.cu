@@ -603,11 +603,27 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
         }
     } else {
         const int per = std::max(1, std::min(nc, kHostParts / batch));  // token ranges per batch element
-        for (int b = 0; b < batch; ++b)
-            for (int k = 0; k < per; ++k) {
-                const int c0 = nc * k / per, c1 = nc * (k + 1) / per;
-                parts[np++] = {b, 1, c0 * chunk, std::min(seqlen, c1 * chunk) - c0 * chunk};
+        // The problem's first upload and last download overlap nothing, so its first and
+        // last ranges are short (1/16 of a batch element's chunks); the others share the rest.
+        const int small = std::max(1, nc / 16);
+        for (int b = 0; b < batch; ++b) {
+            const bool lo_small = b == 0 && per >= 2, hi_small = b == batch - 1 && per >= (lo_small ? 3 : 2);
+            const int nsmall = (lo_small ? 1 : 0) + (hi_small ? 1 : 0);
+            const int c_lo = lo_small ? small : 0, c_hi = hi_small ? nc - small : nc;
+            const bool shaped = nsmall > 0 && c_hi - c_lo >= per - nsmall;
+            int cut[kHostParts + 1];
+            cut[0] = 0;
+            cut[per] = nc;
+            if (shaped) {
+                const int k0 = lo_small ? 1 : 0, m = per - nsmall;  // m equal ranges over [c_lo, c_hi)
+                if (lo_small) cut[1] = c_lo;
+                for (int k = 0; k < m; ++k) cut[k0 + k + 1] = c_lo + (c_hi - c_lo) * (k + 1) / m;
+            } else {
+                for (int k = 1; k < per; ++k) cut[k] = nc * k / per;
             }
+            for (int k = 0; k < per; ++k)
+                parts[np++] = {b, 1, cut[k] * chunk, std::min(seqlen, cut[k + 1] * chunk) - cut[k] * chunk};
+        }
     }
     const bool chained = np > 1 && parts[0].nb == 1 && np > batch;  // token ranges carry the state
     size_t ws_need = 0;
