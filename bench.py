@@ -94,29 +94,30 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_digest():
+def source_digest(kernel=None):
     """Digest of the device sources: the headers and every translation unit that
-    defines a kernel (host-only files such as the C-ABI entry points are left out,
-    so a change there does not retire the recorded counters)."""
+    defines a kernel (host-only files such as the C-ABI entry points are left out).
+    With `kernel`, only the headers and the file that defines that kernel, so a
+    change to another kernel's file does not retire its recorded counters."""
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "structured_state_space_03_b300", "csrc", "*"))):
         with open(f, "rb") as fh:
             data = fh.read()
-        if f.endswith(".cuh") or b"__global__" in data:
+        if f.endswith(".cuh") or (b"__global__" in data and (kernel is None or kernel.encode() in data)):
             h.update(os.path.basename(f).encode() + data)
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current sources of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as fh:
         rec = json.load(fh)
     ent = rec.get(kernel)
-    if not ent or ent.get("source_digest") != source_digest():
+    if not ent or ent.get("source_digest") != source_digest(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 

@@ -215,21 +215,53 @@ __global__ void __launch_bounds__(kThreads) bwd_state_pass(BwdArgs a)
     const float *dec = a.decay + bh * nc;
     float *hs = a.hs + bh * nc * PN + e;
     float *gs = a.gs + bh * nc * PN + e;
+    // Both sweeps take the chunk states in double-buffered batches of kAhead: the next
+    // batch's loads go out before the current batch is applied, so each thread keeps
+    // kAhead loads in flight (as the forward's state pass does).
+    constexpr int kAhead = 8;
     float s = a.init_state ? a.init_state[bh * PN + e] : 0.f;
-    float nxt = hs[0];
-    for (int c = 0; c < nc; ++c) {
-        const float cur = nxt;
-        if (c + 1 < nc) nxt = hs[(size_t)(c + 1) * PN];
-        hs[(size_t)c * PN] = s;
-        s = fmaf(dec[c], s, cur);
+    {
+        float sc[kAhead], sn[kAhead];
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k)
+            if (k < nc) sc[k] = hs[(size_t)k * PN];
+        for (int c0 = 0; c0 < nc; c0 += kAhead) {
+#pragma unroll
+            for (int k = 0; k < kAhead; ++k)
+                if (c0 + kAhead + k < nc) sn[k] = hs[(size_t)(c0 + kAhead + k) * PN];
+#pragma unroll
+            for (int k = 0; k < kAhead; ++k) {
+                const int c = c0 + k;
+                if (c < nc) {
+                    hs[(size_t)c * PN] = s;
+                    s = fmaf(dec[c], s, sc[k]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kAhead; ++k) sc[k] = sn[k];
+        }
     }
     float gv = a.dfinal ? a.dfinal[bh * PN + e] : 0.f;
-    nxt = gs[(size_t)(nc - 1) * PN];
-    for (int c = nc - 1; c >= 0; --c) {
-        const float cur = nxt;
-        if (c > 0) nxt = gs[(size_t)(c - 1) * PN];
-        gs[(size_t)c * PN] = gv;
-        gv = fmaf(dec[c], gv, cur);
+    {
+        float sc[kAhead], sn[kAhead];  // k-th entry: chunk nc - 1 - (c0 + k)
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k)
+            if (k < nc) sc[k] = gs[(size_t)(nc - 1 - k) * PN];
+        for (int c0 = 0; c0 < nc; c0 += kAhead) {
+#pragma unroll
+            for (int k = 0; k < kAhead; ++k)
+                if (c0 + kAhead + k < nc) sn[k] = gs[(size_t)(nc - 1 - (c0 + kAhead + k)) * PN];
+#pragma unroll
+            for (int k = 0; k < kAhead; ++k) {
+                const int c = nc - 1 - (c0 + k);
+                if (c0 + k < nc) {
+                    gs[(size_t)c * PN] = gv;
+                    gv = fmaf(dec[c], gv, sc[k]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kAhead; ++k) sc[k] = sn[k];
+        }
     }
     if (a.dinit) a.dinit[bh * PN + e] = gv;
 }

@@ -230,17 +230,27 @@ __global__ void __launch_bounds__(kThreads) state_pass(Problem pr, Workspace ws)
     const size_t first = pr.chunks ? (size_t)h * pr.total_chunks + pr.seq_first[b] : bh * pr.nchunks;
     float *s = ws.states + first * (size_t)PN + e;
     const float *dec = ws.decay + first;
-    // kAhead chunk states are loaded before any is overwritten, so each thread
-    // keeps kAhead independent loads in flight instead of one per chunk
-    constexpr int kAhead = 16;
+    // Chunk states go in batches of kAhead, double-buffered: the next batch's loads
+    // are issued before the current batch is applied and overwritten, so each thread
+    // keeps kAhead independent loads in flight at all times (batches of 8 measured
+    // best: 0.49 -> 0.29 ms on 512 chunks x 24 heads x 64 x 256)
+    constexpr int kAhead = 8;
     const int nc = pr.chunks ? pr.seq_first[b + 1] - pr.seq_first[b] : pr.nchunks;
+    float sc[kAhead], dk[kAhead];
+#pragma unroll
+    for (int k = 0; k < kAhead; ++k) {
+        if (k < nc) {
+            sc[k] = s[(size_t)k * PN];
+            dk[k] = __ldg(dec + k);
+        }
+    }
     for (int c0 = 0; c0 < nc; c0 += kAhead) {
-        float sc[kAhead], dk[kAhead];
+        float sn[kAhead], dn[kAhead];
 #pragma unroll
         for (int k = 0; k < kAhead; ++k) {
-            if (c0 + k < nc) {
-                sc[k] = s[(size_t)(c0 + k) * PN];
-                dk[k] = __ldg(dec + c0 + k);
+            if (c0 + kAhead + k < nc) {
+                sn[k] = s[(size_t)(c0 + kAhead + k) * PN];
+                dn[k] = __ldg(dec + c0 + kAhead + k);
             }
         }
 #pragma unroll
@@ -249,6 +259,11 @@ __global__ void __launch_bounds__(kThreads) state_pass(Problem pr, Workspace ws)
                 s[(size_t)(c0 + k) * PN] = st;
                 st = fmaf(dk[k], st, sc[k]);
             }
+        }
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k) {
+            sc[k] = sn[k];
+            dk[k] = dn[k];
         }
     }
     if (pr.final_state) pr.final_state[bh * PN + e] = st;
