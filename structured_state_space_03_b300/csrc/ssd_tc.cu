@@ -37,6 +37,10 @@ using namespace ptx;
 constexpr int kThreads = 128;
 constexpr int kBoxRows = 128;           // tokens per TMA box
 constexpr int kBoxBytes = 64 * 2 * kBoxRows;  // 64 bf16 columns x 128 rows = 16 KiB
+// chunk_state_tc goes through the chunk in 64-token slabs: its shared memory (65 KiB at
+// dstate 256) then leaves room for two CTAs per SM, which hide each other's latencies
+constexpr int kStRows = 64;
+constexpr int kStBytes = 64 * 2 * kStRows;    // 64 bf16 columns x 64 rows = 8 KiB
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
@@ -154,15 +158,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads;
     const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
     const int b = ref.tb, t0 = ref.t0, len = ref.len;  // b: batch row of the token tensors
-    const int nbox = pr.chunk <= kBoxRows ? 1 : 2;  // 128-token slabs along K
+    const int nbox = (pr.chunk + kStRows - 1) / kStRows;  // 64-token slabs along K
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // one 128-token slab at a time: w*x as hi and lo bf16 terms (2 MN blocks of
+    // one 64-token slab at a time: w*x as hi and lo bf16 terms (2 MN blocks of
     // 64 (h,p) columns each), and B (NS/64 MN blocks of 64 n columns)
     uint8_t *base = align1024(smem_raw);
-    uint8_t *xs = base;                  // x, then hi(w*x) in place: 2 x 16 KiB
-    uint8_t *xl = base + 2 * kBoxBytes;  // lo(w*x): 2 x 16 KiB
-    uint8_t *bs = base + 4 * kBoxBytes;  // NS/64 x 16 KiB
+    uint8_t *xs = base;                 // x, then hi(w*x) in place: 2 x 8 KiB
+    uint8_t *xl = base + 2 * kStBytes;  // lo(w*x): 2 x 8 KiB
+    uint8_t *bs = base + 4 * kStBytes;  // NS/64 x 8 KiB
 
     if (tid == 0) {
         mbar_init(&bar_tma, 1);
@@ -177,11 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_slot;
 
     auto issue_loads = [&](int kh) {
-        mbar_expect_tx(&bar_tma, (uint32_t)((2 + NS / 64) * kBoxBytes));
+        mbar_expect_tx(&bar_tma, (uint32_t)((2 + NS / 64) * kStBytes));
         for (int k = 0; k < 2; ++k)
-            tma_load_3d(xs + k * kBoxBytes, &xmap, &bar_tma, hb * 128 + 64 * k, t0 + kh * kBoxRows, b);
+            tma_load_3d(xs + k * kStBytes, &xmap, &bar_tma, hb * 128 + 64 * k, t0 + kh * kStRows, b);
         for (int s = 0; s < NS / 64; ++s)
-            tma_load_3d(bs + s * kBoxBytes, &bmap, &bar_tma, g * NS + 64 * s, t0 + kh * kBoxRows, b);
+            tma_load_3d(bs + s * kStBytes, &bmap, &bar_tma, g * NS + 64 * s, t0 + kh * kStRows, b);
     };
     if (tid == 0) {
         tma_prefetch_desc(&xmap);
@@ -208,9 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = !s_fail;
         if (!ok) break;
         // w*x -> hi (in place) + lo; one 16-B chunk = 8 columns of one token row
-        for (int q = tid; q < 2 * kBoxRows * 8; q += kThreads) {
-            const int k = q / (kBoxRows * 8), row = (q / 8) % kBoxRows;
-            const float w = wts[(P == 64 ? k : 0) * 256 + kh * kBoxRows + row];
+        for (int q = tid; q < 2 * kStRows * 8; q += kThreads) {
+            const int k = q / (kStRows * 8), row = (q / 8) % kStRows;
+            const float w = wts[(P == 64 ? k : 0) * 256 + kh * kStRows + row];
             uint4 *ptr = reinterpret_cast<uint4 *>(xs) + q;
             uint4 v = *ptr;
             const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
@@ -237,10 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t idesc = idesc_bf16(128, NS, 1, 1);
-            for (int ks = 0; ks < kBoxRows / 16; ++ks) {
-                const uint64_t bd = sdesc_sw128(smem_u32(bs) + ks * 2048, kBoxBytes, 1024);
-                mma_bf16(tmem, sdesc_sw128(smem_u32(xs) + ks * 2048, kBoxBytes, 1024), bd, idesc, (kh | ks) != 0);
-                mma_bf16(tmem, sdesc_sw128(smem_u32(xl) + ks * 2048, kBoxBytes, 1024), bd, idesc, 1);
+            for (int ks = 0; ks < kStRows / 16; ++ks) {
+                const uint64_t bd = sdesc_sw128(smem_u32(bs) + ks * 2048, kStBytes, 1024);
+                mma_bf16(tmem, sdesc_sw128(smem_u32(xs) + ks * 2048, kStBytes, 1024), bd, idesc, (kh | ks) != 0);
+                mma_bf16(tmem, sdesc_sw128(smem_u32(xl) + ks * 2048, kStBytes, 1024), bd, idesc, 1);
             }
             mma_commit(&bar_mma);
         }
@@ -540,7 +544,7 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int width, int seqlen, i
     return cached_tensor_map(map, ptr, true, width, seqlen, batch, 64, kBoxRows, true);
 }
 
-size_t state_smem(const Problem &pr) { return 1024 + (size_t)(4 + pr.dstate / 64) * kBoxBytes; }
+size_t state_smem(const Problem &pr) { return 1024 + (size_t)(4 + pr.dstate / 64) * kStBytes; }
 
 size_t out_smem(const Problem &pr)
 {
@@ -558,8 +562,12 @@ cudaError_t launch_tc(const Problem &pr, const Workspace &ws, cudaStream_t s, in
     const int mb = pr.chunks ? 1 : pr.batch;
     const int ncx = pr.chunks ? pr.total_chunks : pr.nchunks;
     if (phase == 0) {
-        if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
-        if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
+        if ((e = cached_tensor_map(&xmap, pr.x, true, pr.nheads * pr.headdim, pr.seqlen, mb, 64, kStRows, true)) !=
+            cudaSuccess)
+            return e;
+        if ((e = cached_tensor_map(&bmap, pr.B, true, pr.ngroups * pr.dstate, pr.seqlen, mb, 64, kStRows, true)) !=
+            cudaSuccess)
+            return e;
         const size_t smem = state_smem(pr);
         if ((e = ensure_smem_limit(reinterpret_cast<const void *>(chunk_state_tc<NS>), smem)) != cudaSuccess) return e;
         const dim3 grid(ncx, pr.nheads / HB, mb);
