@@ -288,7 +288,8 @@ constexpr int kOutThreads = 256;  // chunk_out_tc: warps w and w + 4 share TMEM 
 template <int NS>
 __global__ void __launch_bounds__(kOutThreads, 1)
     chunk_out_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
-                 const __grid_constant__ CUtensorMap cmap, Problem pr, Workspace ws)
+                 const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap, Problem pr,
+                 Workspace ws)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_tma, bar_x, bar_mma;
@@ -476,7 +477,11 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         tc_fence_after();
     }
 
-    // ---- phase 3: y = Ydiag + exp(cs_i) Yoff + D x
+    // ---- phase 3: y = Ydiag + exp(cs_i) Yoff + D x, staged over this tile's x rows and
+    // stored by TMA when the tile's 128 rows all belong to the chunk (the batch layout
+    // with chunks of 128 or 256 tokens; rows past the sequence end are clipped by the
+    // tensor map), else stored row by row
+    const bool tma_out = !pr.chunks && (pr.chunk == kBoxRows || pr.chunk == 2 * kBoxRows);
     if (ok && !mbar_wait(&bar_x, 0)) ok = false;  // x tile (already complete) visible to every thread
     if (ok) {
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -489,30 +494,48 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 float yd[32], yo[32];
                 tmem_ld32(tmem + lane_base + col_yd + hh * P + p0, yd);
                 tmem_ld32(tmem + lane_base + col_yo + hh * P + p0, yo);
-                if (row_ok) {
+                if (row_ok || tma_out) {
                     const int col = hh * P + p0;            // column within the 128-wide x tile
-                    const uint8_t *xrow = xs + (col / 64) * jn * 128;
-                    float out[32];
+                    uint8_t *xrow = xs + (col / 64) * jn * 128;
+                    uint4 ov[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const uint4 xv = *reinterpret_cast<const uint4 *>(xrow + sw128(ia, (col % 64) / 8 + u));
                         const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                        float out[8];
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             const float2 xf = __bfloat1622float2(x2[v]);
                             const int k = 8 * u + 2 * v;
-                            out[k] = yd[k] + e * yo[k] + Dh * xf.x;
-                            out[k + 1] = yd[k + 1] + e * yo[k + 1] + Dh * xf.y;
+                            out[2 * v] = yd[k] + e * yo[k] + Dh * xf.x;
+                            out[2 * v + 1] = yd[k + 1] + e * yo[k + 1] + Dh * xf.y;
                         }
+                        ov[u] = pack8(out);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(yrow + p0);
+                    if (tma_out) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) dst[u] = pack8(out + 8 * u);
+                        for (int u = 0; u < 4; ++u)
+                            *reinterpret_cast<uint4 *>(xrow + sw128(ia, (col % 64) / 8 + u)) = ov[u];
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + p0);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) dst[u] = ov[u];
+                    }
                 }
             }
         }
     } else if (tid == 0) {
         set_error(pr, kDevErrTimeout);
+    }
+    if (tma_out) {
+        fence_async_smem();
+        __syncthreads();
+        if (ok && tid == 0) {  // the tile's rows i0 .. i0 + 127 of both 64-column blocks
+            for (int k = 0; k < 2; ++k)
+                tma_store_3d(&ymap, xs + k * jn * 128 + i0 * 128, hb * 128 + 64 * k, t0 + i0, b);
+            bulk_commit();
+            bulk_wait_read_all();
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -578,12 +601,14 @@ cudaError_t launch_tc(const Problem &pr, const Workspace &ws, cudaStream_t s, in
         if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
         if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
         if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
+        CUtensorMap ymap;
+        if ((e = make_map(&ymap, pr.y, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
         const size_t smem = out_smem(pr);
         if ((e = ensure_smem_limit(reinterpret_cast<const void *>(chunk_out_tc<NS>), smem)) != cudaSuccess) return e;
         const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
         const dim3 grid(ncx * ntile, pr.nheads / HB, mb);
         profile_kernel_begin(s);
-        chunk_out_tc<NS><<<grid, kOutThreads, smem, s>>>(xmap, bmap, cmap, pr, ws);
+        chunk_out_tc<NS><<<grid, kOutThreads, smem, s>>>(xmap, bmap, cmap, ymap, pr, ws);
         profile_kernel_end(s);
     }
     return cudaGetLastError();
