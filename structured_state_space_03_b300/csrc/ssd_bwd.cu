@@ -731,14 +731,24 @@ __device__ __forceinline__ void load_row(const uint8_t *tilep, int t, float (&f)
 }
 
 // e_ij = exp(cs_i - cs_j) on the causal triangle of the chunk (0 elsewhere), for
-// the 32 columns j = 32 jb ...; cs in shared memory.
+// the 32 columns j = 32 jb ...; cs in shared memory, 16-byte aligned, read as float4s.
+// __expf (the hardware exponential): its error is of the order of the fp32 segment
+// sums' own (|cs| 2^-24 in the exponent); an accurate expf with scalar loads ran
+// without instruction-level parallelism.  Masked entries are discarded whatever
+// the exponential gives there.
 __device__ __forceinline__ void decay_row(const float *cs, int i, int jb, bool row_in, float (&e)[32])
 {
     const float ci = cs[i];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        const int j = 32 * jb + k;
-        e[k] = (row_in && j <= i) ? expf(ci - cs[j]) : 0.f;
+    for (int q = 0; q < 8; ++q) {
+        const float4 c4 = reinterpret_cast<const float4 *>(cs + 32 * jb)[q];
+        const float cj[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int j = 32 * jb + 4 * q + v;
+            const float ev = __expf(ci - cj[v]);
+            e[4 * q + v] = (row_in && j <= i) ? ev : 0.f;
+        }
     }
 }
 
@@ -763,7 +773,9 @@ __global__ void __launch_bounds__(kTc, 1)
     __shared__ __align__(8) uint64_t bar_ld, bar_mma;
     __shared__ uint32_t tmem_slot;
     __shared__ float warp_tot[8];
-    __shared__ float cs_s[kQ], dt_s[kQ], cum_s[kQ], z_s[kQ], zv_s[kQ], ddt_s[kQ];
+    __shared__ __align__(16) float cs_s[kQ];  // read as float4s (decay_row)
+    __shared__ __align__(16) float dt_s[kQ];  // read as float4s below
+    __shared__ float cum_s[kQ], z_s[kQ], zv_s[kQ], ddt_s[kQ];
     __shared__ float row_s[2][kQ], diag_s[2][kQ];
     __shared__ float colp[4][kQ];
     __shared__ int s_fail;
@@ -911,13 +923,18 @@ __global__ void __launch_bounds__(kTc, 1)
                 tmem_ld32(lrow + 128 + 32 * jb, cb);
                 decay_row(cs_s, i, jb, row_in, e);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int j = 32 * jb + k;
-                    if (j == i) diag = dx[k];
-                    const float kv = e[k] * dx[k];
-                    w[k] = j < i ? kv * cb[k] * dt_s[j] : 0.f;
-                    rs += w[k];
-                    dx[k] = kv;
+                for (int q = 0; q < 8; ++q) {
+                    const float4 d4 = reinterpret_cast<const float4 *>(dt_s + 32 * jb)[q];
+                    const float dj[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int k = 4 * q + v, j = 32 * jb + k;
+                        if (j == i) diag = dx[k];
+                        const float kv = e[k] * dx[k];
+                        w[k] = j < i ? kv * cb[k] * dj[v] : 0.f;
+                        rs += w[k];
+                        dx[k] = kv;
+                    }
                 }
                 store_split32(base + oKh, base + oKl, i, jb, dx);
                 colp[quarter][32 * jb + lane] = reduce_scatter32(w, lane);
