@@ -343,6 +343,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         tma_prefetch_desc(&xmap);
         tma_prefetch_desc(&bmap);
         tma_prefetch_desc(&cmap);
+        // the chunk's entry states (one P x NS fp32 block per head, from DRAM) into L2, so
+        // that phase 1's per-slab loads of them find them there
+        for (int hh = 0; hh < HB; ++hh)
+            bulk_prefetch_l2(ws.states + state_slot(pr, ref, h0 + hh) * (size_t)P * NS, (uint32_t)(P * NS * sizeof(float)));
         mbar_expect_tx(&bar_x, (uint32_t)(2 * nbj * kBoxBytes));
         for (int k = 0; k < 2; ++k)
             for (int r = 0; r < nbj; ++r)
