@@ -702,6 +702,61 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
 }
 
 // Sum over the 256 threads in a fixed order (warp_tot: 8 floats); every thread gets it.
+// Three block sums at once (256 threads), each in sum256's order; red holds 3 x 8 floats.
+__device__ __forceinline__ float3 sum3_256(float a, float b, float c, float (*red)[8])
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+        c += __shfl_xor_sync(0xffffffffu, c, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        red[0][threadIdx.x >> 5] = a;
+        red[1][threadIdx.x >> 5] = b;
+        red[2][threadIdx.x >> 5] = c;
+    }
+    __syncthreads();
+    float r[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+        r[k] = ((red[k][0] + red[k][1]) + (red[k][2] + red[k][3])) + ((red[k][4] + red[k][5]) + (red[k][6] + red[k][7]));
+    __syncthreads();
+    return make_float3(r[0], r[1], r[2]);
+}
+
+// Inclusive block scan of v (256 threads) together with the block sums of v and of w, in one
+// exchange: returns (prefix, total of v, total of w); red holds 3 x 8 floats.
+__device__ __forceinline__ float3 scan_sum2_256(float v, float w, float (*red)[8])
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+    if (lane == 31) red[0][warp] = v;
+    if (lane == 0) red[2][warp] = w;
+    __syncthreads();
+    if (warp == 0) {
+        float x = lane < 8 ? red[0][lane] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += t;
+        }
+        if (lane < 8) red[1][lane] = x;  // inclusive prefix of the warp totals
+    }
+    __syncthreads();
+    const float pre = warp > 0 ? v + red[1][warp - 1] : v;
+    const float tot = red[1][7];
+    const float ws = ((red[2][0] + red[2][1]) + (red[2][2] + red[2][3])) + ((red[2][4] + red[2][5]) + (red[2][6] + red[2][7]));
+    __syncthreads();
+    return make_float3(pre, tot, ws);
+}
+
 __device__ __forceinline__ float sum256(float v, float *warp_tot)
 {
 #pragma unroll
@@ -778,6 +833,7 @@ __global__ void __launch_bounds__(kTc, 1)
     __shared__ float cum_s[kQ], z_s[kQ], zv_s[kQ], ddt_s[kQ];
     __shared__ float row_s[2][kQ], diag_s[2][kQ];
     __shared__ float colp[4][kQ];
+    __shared__ float red_s[3][8];
     __shared__ int s_fail;
 
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -1068,19 +1124,19 @@ __global__ void __launch_bounds__(kTc, 1)
     // dA / dD parts; sums over all 256 threads in a fixed order (the second half adds zeros)
     const bool tok = tid < kQ && tid < len;
     const float zv = tok ? zv_s[tid] : 0.f;
-    const float ssum = sum256(zv, warp_tot);  // sum_j e^{cs_end - cs_j} V_j
-    const float usum = sum256(u, warp_tot);
-    const float dsum = sum256(tid < kQ ? diag_s[0][tid] + diag_s[1][tid] : 0.f, warp_tot);
+    // sum_j e^{cs_end - cs_j} V_j, the u sum and the diagonal sum in one exchange
+    const float3 s3 = sum3_256(zv, u, tid < kQ ? diag_s[0][tid] + diag_s[1][tid] : 0.f, red_s);
+    const float ssum = s3.x, usum = s3.y, dsum = s3.z;
     float d = 0.f;
     if (tok) {
         const float colsum = (colp[0][tid] + colp[1][tid]) + (colp[2][tid] + colp[3][tid]);
         d = (row_s[0][tid] + row_s[1][tid]) - colsum + expf(cs_s[tid]) * z_s[tid] - zv;
         if (tid == len - 1) d += ssum + expf(cs_end) * usum;
     }
-    const float pre = block_inclusive_scan_256(d, warp_tot);
-    const float tot = sum256(d, warp_tot);
+    // the prefix of d, its total and the dA part sum_t d_t cum_t in one exchange
+    const float3 pt = scan_sum2_256(d, tid < kQ ? d * cum_s[tid] : 0.f, red_s);
+    const float pre = pt.x, tot = pt.y, da = pt.z;
     if (tok && ok) a.ddt[((size_t)b * L + t0 + tid) * H + h] = fmaf(Ah, tot - pre + d, ddt_s[tid]);
-    const float da = sum256(tid < kQ ? d * cum_s[tid] : 0.f, warp_tot);
     if (tid == 0 && ok) {
         const size_t o = ((size_t)b * a.nchunks + c) * H + h;
         a.dAp[o] = da;
