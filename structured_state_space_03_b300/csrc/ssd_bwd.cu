@@ -822,7 +822,9 @@ __device__ __forceinline__ void store_split32(uint8_t *hi_base, uint8_t *lo_base
 
 __global__ void __launch_bounds__(kTc, 1)
     bwd_chunk_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap dymap,
-                 const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap cmap, BwdArgs a)
+                 const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap cmap,
+                 const __grid_constant__ CUtensorMap dbmap, const __grid_constant__ CUtensorMap dcmap,
+                 const __grid_constant__ CUtensorMap dxmap, BwdArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_ld, bar_mma;
@@ -1072,29 +1074,32 @@ __global__ void __launch_bounds__(kTc, 1)
     // head), dx and x . inner (second half)
     const float cs_end = cs_s[len - 1], cs_i = cs_s[i];
     const float eS = row_in ? expf(cs_end - cs_i) : 0.f, eC = row_in ? expf(cs_i) : 0.f;
+    // Each row goes into an fp32 staging tile (dB over B and C, dC over dt B, dx over K: all
+    // dead now) of two [128][32] boxes with the 128-byte swizzle, so that a warp's row stores
+    // spread over the banks; the boxes then go out by TMA (rows past the sequence end are
+    // clipped by the tensor maps; the tensor-core backward has no packed layout).
+    uint8_t *stB = base + oB, *stC = base + oBh, *stX = base + oKh;
+    auto put_row = [&](uint8_t *tile, const float (&v)[64]) {
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4 *>(tile + hb * kTile + sw128(i, q)) =
+                    make_float4(v[32 * hb + 4 * q], v[32 * hb + 4 * q + 1], v[32 * hb + 4 * q + 2],
+                                v[32 * hb + 4 * q + 3]);
+    };
     if (ok && half == 0) {
-        const bool direct = a.dBp == nullptr;
-        const size_t orow = (((size_t)b * L + t0 + i) * (direct ? G : H) + (direct ? g : h)) * kD;
         float acc[64], add[64];
         tmem_ld64(lrow + 0, acc);
         tmem_ld64(lrow + 448, add);
-        if (row_in) {
-            float4 *o = reinterpret_cast<float4 *>((direct ? a.dB : a.dBp) + orow);
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-                o[q] = make_float4(dti * fmaf(eS, add[4 * q], acc[4 * q]), dti * fmaf(eS, add[4 * q + 1], acc[4 * q + 1]),
-                                   dti * fmaf(eS, add[4 * q + 2], acc[4 * q + 2]),
-                                   dti * fmaf(eS, add[4 * q + 3], acc[4 * q + 3]));
-        }
+        for (int k = 0; k < 64; ++k) acc[k] = dti * fmaf(eS, add[k], acc[k]);
+        put_row(stB, acc);
         tmem_ld64(lrow + 64, acc);
         tmem_ld64(lrow + 384, add);
-        if (row_in) {
-            float4 *o = reinterpret_cast<float4 *>((direct ? a.dC : a.dCp) + orow);
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-                o[q] = make_float4(fmaf(eC, add[4 * q], acc[4 * q]), fmaf(eC, add[4 * q + 1], acc[4 * q + 1]),
-                                   fmaf(eC, add[4 * q + 2], acc[4 * q + 2]), fmaf(eC, add[4 * q + 3], acc[4 * q + 3]));
-        }
+        for (int k = 0; k < 64; ++k) acc[k] = fmaf(eC, add[k], acc[k]);
+        put_row(stC, acc);
     } else if (ok) {
         float acc[64], add[64], f[64];
         tmem_ld64(lrow + 128, acc);
@@ -1108,17 +1113,23 @@ __global__ void __launch_bounds__(kTc, 1)
         for (int k = 0; k < 64; ++k) xin = fmaf(f[k], acc[k], xin);
         ddt_s[i] = xin;
         load_row(base + oDY, i, f);
-        if (row_in) {
-            float4 *o = reinterpret_cast<float4 *>(a.dx + (((size_t)b * L + t0 + i) * H + h) * kD);
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-                o[q] = make_float4(fmaf(Dh, f[4 * q], dti * acc[4 * q]), fmaf(Dh, f[4 * q + 1], dti * acc[4 * q + 1]),
-                                   fmaf(Dh, f[4 * q + 2], dti * acc[4 * q + 2]),
-                                   fmaf(Dh, f[4 * q + 3], dti * acc[4 * q + 3]));
-        }
+        for (int k = 0; k < 64; ++k) acc[k] = fmaf(Dh, f[k], dti * acc[k]);
+        put_row(stX, acc);
     }
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && ok) {
+        const bool direct = a.dBp == nullptr;  // one head per group: dB and dC themselves
+        for (int hb = 0; hb < 2; ++hb) {
+            tma_store_3d(&dbmap, stB + hb * kTile, (direct ? g : h) * kD + 32 * hb, t0, b);
+            tma_store_3d(&dcmap, stC + hb * kTile, (direct ? g : h) * kD + 32 * hb, t0, b);
+            tma_store_3d(&dxmap, stX + hb * kTile, h * kD + 32 * hb, t0, b);
+        }
+        bulk_commit();
+        bulk_wait_read_all();
+    }
 
     // dL/dcs_t (threads 0..127 = tokens t), then ddt = x . inner + A sum_{t' >= t} dcs_t' and the
     // dA / dD parts; sums over all 256 threads in a fixed order (the second half adds zeros)
@@ -1212,6 +1223,17 @@ cudaError_t launch_bwd_tc(const BwdArgs &a, cudaStream_t s)
     if ((e = cached_tensor_map(&dym, a.dy, true, H * 64, a.seqlen, a.batch, 64, 128, true)) != cudaSuccess) return e;
     if ((e = cached_tensor_map(&bm, a.B, true, G * 64, a.seqlen, a.batch, 64, 128, true)) != cudaSuccess) return e;
     if ((e = cached_tensor_map(&cm, a.C, true, G * 64, a.seqlen, a.batch, 64, 128, true)) != cudaSuccess) return e;
+    // fp32 outputs of the in-chunk kernel, stored by TMA from [128][32] swizzled boxes: dB and
+    // dC per head (their parts) or per group (one head per group), dx
+    CUtensorMap dbm, dcm, dxm;
+    const bool parts = a.dBp != nullptr;
+    if ((e = cached_tensor_map(&dbm, parts ? a.dBp : a.dB, false, (parts ? H : G) * 64, a.seqlen, a.batch, 32, 128,
+                               true)) != cudaSuccess)
+        return e;
+    if ((e = cached_tensor_map(&dcm, parts ? a.dCp : a.dC, false, (parts ? H : G) * 64, a.seqlen, a.batch, 32, 128,
+                               true)) != cudaSuccess)
+        return e;
+    if ((e = cached_tensor_map(&dxm, a.dx, false, H * 64, a.seqlen, a.batch, 32, 128, true)) != cudaSuccess) return e;
     const dim3 grid(a.nchunks, H, a.batch);
     const size_t s1 = chunk_states_smem<4, tcb::kQ>();
     if (H % 2 == 0 && (H / G) % 2 == 0) {
@@ -1259,7 +1281,7 @@ cudaError_t launch_bwd_tc(const BwdArgs &a, cudaStream_t s)
     profile_kernel_end(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     profile_kernel_begin(s);
-    tcb::bwd_chunk_tc<<<grid, tcb::kTc, tcb::kSmemTc, s>>>(xm, dym, bm, cm, a);
+    tcb::bwd_chunk_tc<<<grid, tcb::kTc, tcb::kSmemTc, s>>>(xm, dym, bm, cm, dbm, dcm, dxm, a);
     profile_kernel_end(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return launch_reductions(a, s);
