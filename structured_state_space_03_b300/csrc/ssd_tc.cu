@@ -143,8 +143,8 @@ __device__ __forceinline__ uint32_t sw128(int r, int q) { return (uint32_t)r * 1
 
 template <int NS>
 __global__ void __launch_bounds__(kThreads, 1)
-    chunk_state_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap, Problem pr,
-                   Workspace ws)
+    chunk_state_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
+                   const __grid_constant__ CUtensorMap smap, Problem pr, Workspace ws)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_tma, bar_mma;
@@ -255,18 +255,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_after();
 
+    // S_c out: 32 state columns at a time into a [128 rows][32] fp32 box with the 128-byte
+    // swizzle (double-buffered over the dead w*x hi / lo slabs), each head's P rows stored by
+    // TMA as one box of the [state rows][NS] view of the workspace
     if (ok) {
         const int m = warp * 32 + lane;
-        const int hh = m / P, p = m % P;
-        float *out = ws.states + state_slot(pr, ref, h0 + hh) * (size_t)P * NS + (size_t)p * NS;
 #pragma unroll 1
         for (int c0 = 0; c0 < NS; c0 += 32) {
+            uint8_t *buf = (c0 / 32) & 1 ? xl : xs;
+            if (c0 >= 64) {  // the store of two slabs ago must be done reading this buffer
+                if (tid == 0) bulk_wait_read_1();
+                __syncthreads();
+            }
             float v[32];
             tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
-            float4 *o4 = reinterpret_cast<float4 *>(out + c0);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) o4[u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4 *>(buf + sw128(m, q)) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                for (int hh = 0; hh < HB; ++hh)
+                    tma_store_3d(&smap, buf + hh * P * 128, c0, (int)(state_slot(pr, ref, h0 + hh) * P), 0);
+                bulk_commit();
+            }
         }
+        if (tid == 0) bulk_wait_read_all();
     } else if (tid == 0) {
         set_error(pr, kDevErrTimeout);
     }
@@ -608,11 +622,18 @@ cudaError_t launch_tc(const Problem &pr, const Workspace &ws, cudaStream_t s, in
         if ((e = cached_tensor_map(&bmap, pr.B, true, pr.ngroups * pr.dstate, pr.seqlen, mb, 64, kStRows, true)) !=
             cudaSuccess)
             return e;
+        // the chunk states as [state rows = slots x headdim][NS] fp32, boxes of headdim rows x 32
+        CUtensorMap smap;
+        const size_t slots = pr.chunks ? (size_t)pr.nheads * pr.total_chunks : (size_t)pr.batch * pr.nheads * pr.nchunks;
+        if (slots * pr.headdim > (size_t)INT32_MAX) return cudaErrorInvalidValue;  // box row coordinates are 32-bit
+        if ((e = cached_tensor_map(&smap, ws.states, false, NS, (int)(slots * pr.headdim), 1, 32, pr.headdim, true)) !=
+            cudaSuccess)
+            return e;
         const size_t smem = state_smem(pr);
         if ((e = ensure_smem_limit(reinterpret_cast<const void *>(chunk_state_tc<NS>), smem)) != cudaSuccess) return e;
         const dim3 grid(ncx, pr.nheads / HB, mb);
         profile_kernel_begin(s);
-        chunk_state_tc<NS><<<grid, kThreads, smem, s>>>(xmap, bmap, pr, ws);
+        chunk_state_tc<NS><<<grid, kThreads, smem, s>>>(xmap, bmap, smap, pr, ws);
         profile_kernel_end(s);
     } else {
         if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
