@@ -302,11 +302,11 @@ constexpr int kOutThreads = 256;  // chunk_out_tc: warps w and w + 4 share TMEM 
 template <int NS>
 __global__ void __launch_bounds__(kOutThreads, 1)
     chunk_out_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
-                 const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap, Problem pr,
-                 Workspace ws)
+                 const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap ymap,
+                 const __grid_constant__ CUtensorMap smap, Problem pr, Workspace ws)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_tma, bar_x, bar_mma;
+    __shared__ __align__(8) uint64_t bar_tma, bar_x, bar_mma, bar_h[2];
     __shared__ uint32_t tmem_slot;
     __shared__ float warp_tot[8];
     __shared__ __align__(16) float cs[2 * 256];
@@ -339,11 +339,14 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     uint8_t *h_sl = b_sl + jn * 128;              // 128 x 128 B, hi part of the state
     uint8_t *l_sl = h_sl + kBoxBytes;             // 128 x 128 B, lo part of the state
     uint8_t *xs = r1 + region1_bytes(jmax);       // 2 MN blocks, each jn x 128 B
+    uint8_t *hst = xs + 2 * jmax * 128;           // 2 x 32 KiB: an entry-state slab in fp32, by TMA
 
     if (tid == 0) {
         mbar_init(&bar_tma, 1);
         mbar_init(&bar_x, 1);
         mbar_init(&bar_mma, 1);
+        mbar_init(&bar_h[0], 1);
+        mbar_init(&bar_h[1], 1);
         mbar_fence_init();
         s_fail = 0;
     }
@@ -369,40 +372,65 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     }
     segsum256(pr, b, h0, HB, t0, len, kLog2e, cs, dtv, warp_tot);  // log2 domain: decays via exp2f
 
-    // ---- phase 1: G = C_i B^T and Yoff = C_i h_c^T, over 64-wide slabs of the state dimension
+    // ---- phase 1: G = C_i B^T and Yoff = C_i h_c^T, over 64-wide slabs of the state dimension.
+    // The entry state comes by TMA as fp32 slabs (two [rows][32] boxes with the 128-byte
+    // swizzle per head, double-buffered, two slabs ahead) and is split into hi and lo bf16
+    // operand rows here.
     const int m = tid & 127;  // h-slab row (h, p) written by this thread (chunks 4 half .. 4 half + 3)
-    const float *hsrc = ws.states + state_slot(pr, ref, h0 + m / P) * (size_t)P * NS + (size_t)(m % P) * NS;
+    constexpr int nsl = NS / 64;
+    auto issue_h = [&](int sl) {  // thread 0
+        uint8_t *dst = hst + (sl & 1) * 32768;
+        mbar_expect_tx(&bar_h[sl & 1], 32768u);
+        for (int hh = 0; hh < HB; ++hh)
+            for (int ch = 0; ch < 2; ++ch)
+                tma_load_3d(dst + ch * 16384 + hh * P * 128, &smap, &bar_h[sl & 1], 64 * sl + 32 * ch,
+                            (int)(state_slot(pr, ref, h0 + hh) * P), 0);
+    };
+    if (tid == 0) {
+        issue_h(0);
+        if (nsl > 1) issue_h(1);
+    }
     bool ok = true;
-    for (int s = 0; s < NS / 64 && ok; ++s) {
+    for (int s = 0; s < nsl && ok; ++s) {
         if (tid == 0) {
             mbar_expect_tx(&bar_tma, (uint32_t)((1 + nbj) * kBoxBytes));
             tma_load_3d(c_sl, &cmap, &bar_tma, g * NS + 64 * s, t0 + i0, b);
             for (int r = 0; r < nbj; ++r)
                 tma_load_3d(b_sl + r * kBoxBytes, &bmap, &bar_tma, g * NS + 64 * s, t0 + r * kBoxRows, b);
         }
-        // entry state slab -> hi and lo bf16 terms, 128-B swizzled K-major rows
+        // entry state slab -> hi and lo bf16 terms, 128-B swizzled K-major rows: this thread's
+        // row m, columns 32 half .. 32 half + 31 of the slab
+        if (!mbar_wait(&bar_h[s & 1], (s >> 1) & 1)) s_fail = 1;
         {
-            const float4 *src = reinterpret_cast<const float4 *>(hsrc + 64 * s);
+            const uint8_t *src = hst + (s & 1) * 32768 + half * 16384;
+            float f[32];
 #pragma unroll
-            for (int q = 4 * half; q < 4 * half + 4; ++q) {
-                const float4 a = __ldg(src + 2 * q), bq = __ldg(src + 2 * q + 1);
-                const float f[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
-                const uint4 hi = pack8(f);
+            for (int q = 0; q < 8; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(src + sw128(m, q));
+                f[4 * q] = v.x;
+                f[4 * q + 1] = v.y;
+                f[4 * q + 2] = v.z;
+                f[4 * q + 3] = v.w;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint4 hi = pack8(f + 8 * u);
                 const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
                 float r[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 t = __bfloat1622float2(h2[u]);
-                    r[2 * u] = f[2 * u] - t.x;
-                    r[2 * u + 1] = f[2 * u + 1] - t.y;
+                for (int e = 0; e < 4; ++e) {
+                    const float2 t = __bfloat1622float2(h2[e]);
+                    r[2 * e] = f[8 * u + 2 * e] - t.x;
+                    r[2 * e + 1] = f[8 * u + 2 * e + 1] - t.y;
                 }
-                *reinterpret_cast<uint4 *>(h_sl + sw128(m, q)) = hi;
-                *reinterpret_cast<uint4 *>(l_sl + sw128(m, q)) = pack8(r);
+                *reinterpret_cast<uint4 *>(h_sl + sw128(m, 4 * half + u)) = hi;
+                *reinterpret_cast<uint4 *>(l_sl + sw128(m, 4 * half + u)) = pack8(r);
             }
         }
         fence_async_smem();
         __syncthreads();
         if (tid == 0) {
+            if (s + 2 < nsl) issue_h(s + 2);  // every thread has read this slab's fp32 buffer
             if (mbar_wait(&bar_tma, s & 1)) {
                 tc_fence_after();
                 const uint32_t id_g = idesc_bf16(128, jn, 0, 0);
@@ -603,7 +631,7 @@ size_t state_smem(const Problem &pr) { return 1024 + (size_t)(4 + pr.dstate / 64
 size_t out_smem(const Problem &pr)
 {
     const int jmax = pr.chunk <= kBoxRows ? kBoxRows : 2 * kBoxRows;
-    return 1024 + region1_bytes(jmax) + (size_t)2 * jmax * 128;
+    return 1024 + region1_bytes(jmax) + (size_t)2 * jmax * 128 + 2 * 32768;  // ..., x tile, entry-state slabs
 }
 
 template <int NS>
@@ -639,14 +667,20 @@ cudaError_t launch_tc(const Problem &pr, const Workspace &ws, cudaStream_t s, in
         if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
         if ((e = make_map(&bmap, pr.B, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
         if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
-        CUtensorMap ymap;
+        CUtensorMap ymap, smap;
         if ((e = make_map(&ymap, pr.y, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
+        // the entry states h_c as [state rows = slots x headdim][NS] fp32, boxes of headdim rows x 32
+        const size_t slots = pr.chunks ? (size_t)pr.nheads * pr.total_chunks : (size_t)pr.batch * pr.nheads * pr.nchunks;
+        if (slots * pr.headdim > (size_t)INT32_MAX) return cudaErrorInvalidValue;  // box row coordinates are 32-bit
+        if ((e = cached_tensor_map(&smap, ws.states, false, NS, (int)(slots * pr.headdim), 1, 32, pr.headdim, true)) !=
+            cudaSuccess)
+            return e;
         const size_t smem = out_smem(pr);
         if ((e = ensure_smem_limit(reinterpret_cast<const void *>(chunk_out_tc<NS>), smem)) != cudaSuccess) return e;
         const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
         const dim3 grid(ncx * ntile, pr.nheads / HB, mb);
         profile_kernel_begin(s);
-        chunk_out_tc<NS><<<grid, kOutThreads, smem, s>>>(xmap, bmap, cmap, ymap, pr, ws);
+        chunk_out_tc<NS><<<grid, kOutThreads, smem, s>>>(xmap, bmap, cmap, ymap, smap, pr, ws);
         profile_kernel_end(s);
     }
     return cudaGetLastError();
