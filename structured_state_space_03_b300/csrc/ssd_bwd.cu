@@ -866,6 +866,10 @@ __global__ void __launch_bounds__(kTc, 1)
     const uint32_t lrow = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lanes
 
     if (tid == 0) {
+        // this chunk's h_c and g_c (16 KiB each, fresh from the state pass) into L2 while the
+        // chunk scalars are formed
+        bulk_prefetch_l2(hc, (uint32_t)(kD * kD * sizeof(float)));
+        bulk_prefetch_l2(gc, (uint32_t)(kD * kD * sizeof(float)));
         tma_prefetch_desc(&xmap);
         tma_prefetch_desc(&dymap);
         tma_prefetch_desc(&bmap);
