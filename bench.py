@@ -23,6 +23,7 @@ the other large workloads.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import glob
 import hashlib
 import json
@@ -60,6 +61,9 @@ def parse_args():
     ap.add_argument("--no-backward", action="store_true", help="skip the backward sub-record (headline run only)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip every sub-record (decode, pre-step, packed, backward, other workloads)")
+    ap.add_argument("--seqlen", type=int, default=0,
+                    help="run the named workload at this sequence length instead (a scaled-down case for "
+                         "profilers; the record's workload name gains the new length)")
     ap.add_argument("--ref-seconds", type=float, default=0.0,
                     help="oracle seconds per step of --impl reference (0: spread ~150 s over the steps)")
     return ap.parse_args()
@@ -108,15 +112,15 @@ def source_digest(kernel=None):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current sources of that kernel (else None)."""
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summaries, if they were taken on the current sources of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as fh:
         rec = json.load(fh)
-    ent = rec.get(kernel)
+    ent = rec.get(f"{kernel}@{workload}")
     if not ent or ent.get("source_digest") != source_digest(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
@@ -668,13 +672,13 @@ def backward_measurement(w, dev, stream, peaks, steps=20):
         nbytes = bwd_chunk_bytes(w, 128)
         ach = nbytes / (pk[dom] * 1e-3) / 1e9
         rec["roofline"] = {"bound": "hbm", "kernel": names[dom], "achieved": ach, "peak": peaks["hbm_gbs"],
-                           "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": recorded_traffic(names[dom]),
+                           "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": recorded_traffic(names[dom], w.name),
                            "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": kflops[names[dom]],
                            "launch_ms": pk[dom], "peak_source": "measured (copy bandwidth)"}
     elif names[dom] in kflops:
         ach = kflops[names[dom]] / (pk[dom] * 1e-3) / 1e12
         rec["roofline"] = {"bound": "alu", "kernel": names[dom], "achieved": ach, "peak": alu_peak,
-                           "unit": "TFLOP/s", "frac": ach / alu_peak, "traffic": recorded_traffic(names[dom]),
+                           "unit": "TFLOP/s", "frac": ach / alu_peak, "traffic": recorded_traffic(names[dom], w.name),
                            "algorithmic_flops_per_launch": kflops[names[dom]], "launch_ms": pk[dom],
                            "peak_source": "148 SMs x 128 fp32 lanes x 2 flops x max SM clock"}
     del sets, g
@@ -686,6 +690,8 @@ def main():
     args = parse_args()
     world, rank, local = dist_env()
     w = wl.by_name(args.workload)
+    if args.seqlen > 0 and args.seqlen != w.seqlen:
+        w = dataclasses.replace(w, seqlen=args.seqlen, name=f"{w.name}_at_L{args.seqlen}")
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
@@ -785,7 +791,7 @@ def main():
     peaks, peak_src = load_peaks()
     dom_bytes = kernel_algorithmic_bytes(w, dom_name)
     dom_gbs = dom_bytes / (per_kernel[dom] * 1e-3) / 1e9
-    traffic = recorded_traffic(dom_name)
+    traffic = recorded_traffic(dom_name, w.name)
 
     ms_per_step = elapsed_ms / steps
     tokens = w.tokens
