@@ -153,7 +153,7 @@ static const char *kernel_names(const Problem &pr)
 {
     switch (choose_path(pr)) {
     case SSD_PATH_SIMT: return "chunk_state_simt,state_pass,chunk_out_simt";
-    case SSD_PATH_TCGEN05: return "chunk_state_tc,state_pass,chunk_out_tc";
+    case SSD_PATH_TCGEN05: return "chunk_state_tc,state_pass_hilo,chunk_out_tc";
     case SSD_PATH_TCGEN05_FUSED:
         return seq_supported(pr) ? "ssd_seq_pipe_tc" : (pr.dstate == 64 ? "ssd_fused_pipe_tc" : "ssd_fused_tc");
     default: return "";
@@ -177,7 +177,7 @@ static ssd_status_t run(const Problem &pr_in, void *workspace, cudaStream_t s)
     const Workspace ws = carve_workspace(pr, workspace);
     const bool tc = path == SSD_PATH_TCGEN05;
     cudaError_t e = tc ? launch_chunk_state_tc(pr, ws, s) : launch_chunk_state_simt(pr, ws, s);
-    if (e == cudaSuccess) e = launch_state_pass(pr, ws, s);
+    if (e == cudaSuccess) e = launch_state_pass(pr, ws, s, tc);
     if (e == cudaSuccess) e = tc ? launch_chunk_out_tc(pr, ws, s) : launch_chunk_out_simt(pr, ws, s);
     if (e != cudaSuccess) return fail(SSD_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return ok();

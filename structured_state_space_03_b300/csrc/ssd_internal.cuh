@@ -80,7 +80,8 @@ struct Problem {
 
 // Workspace carved out of one device buffer.
 struct Workspace {
-    float *states;  // [batch][nheads][nchunks][headdim][dstate]: S_c, then h_c in place
+    float *states;  // [batch][nheads][nchunks][headdim][dstate]: S_c, then h_c in place (fp32, or
+                    // bf16 hi / lo per 64-wide slice on the tcgen05 path: launch_state_pass)
     float *decay;   // [batch][nheads][nchunks]: exp(cs_last) of each chunk
 };
 // (The packed layout uses [1][nheads][total_chunks] in the sequence-major chunk
@@ -151,7 +152,9 @@ bool seq_supported(const Problem &pr);
 size_t seq_workspace_bytes(const Problem &pr);
 cudaError_t launch_seq_tc(const Problem &pr, void *workspace, cudaStream_t s);
 // Sequential inter-chunk state passing, shared by the multi-kernel paths.
-cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream_t s);
+// hilo: write each entry state h_c in place as bf16 hi and lo terms per 64-wide slice
+// of the state dimension (the layout chunk_out_tc loads); else as fp32
+cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream_t s, bool hilo);
 
 // Backward (ssd_bwd.cu): gradients of a scalar loss given dL/dy and dL/d(final
 // state); fp32 FMA kernels, headdim <= kBwdMaxHeaddim, dstate <= kMaxDstate.

@@ -269,6 +269,82 @@ __global__ void __launch_bounds__(kThreads) state_pass(Problem pr, Workspace ws)
     if (pr.final_state) pr.final_state[bh * PN + e] = st;
 }
 
+// The same pass for the tcgen05 chunk-output kernel, which takes h_c as two bf16
+// terms (hi = bf16(h), lo = bf16(h - hi); a single rounding of a carried state can
+// cost ~2% of RMS(y)).  They are written in place of the fp32 values, per 64-wide
+// slice of the state dimension: row p of a slot, viewed as 2 NS bf16, holds for
+// slice s the 64 hi values at [128 s, 128 s + 64) and the 64 lo values at
+// [128 s + 64, 128 s + 128) -- the 256 bytes the slice's fp32 values occupied, so the
+// chunk-output kernel loads both operands by TMA as they are.  A warp owns one
+// (row, slice) block: lane l reads fp32 words l and l + 32 of it and carries elements
+// 2l and 2l + 1 (their chunk states come from the lanes that read them, by shuffles),
+// so every lane overwrites exactly the two words it read itself.
+__global__ void __launch_bounds__(kThreads) state_pass_hilo(Problem pr, Workspace ws)
+{
+    const int PN = pr.headdim * pr.dstate;
+    const int lane = threadIdx.x & 31;
+    const int blk = (int)((blockIdx.x * kThreads + threadIdx.x) >> 5);  // 64-element block of the slot
+    const int h = blockIdx.y, b = blockIdx.z;
+    if (blk * 64 >= PN) return;  // warp-uniform
+    const size_t bh = (size_t)b * pr.nheads + h;
+    const int ea = blk * 64 + 2 * lane;  // the two elements this lane carries
+    float st0 = pr.init_state ? pr.init_state[bh * PN + ea] : 0.f;
+    float st1 = pr.init_state ? pr.init_state[bh * PN + ea + 1] : 0.f;
+    const size_t first = pr.chunks ? (size_t)h * pr.total_chunks + pr.seq_first[b] : bh * pr.nchunks;
+    float *s = ws.states + first * (size_t)PN + blk * 64;
+    const float *dec = ws.decay + first;
+    const int nc = pr.chunks ? pr.seq_first[b + 1] - pr.seq_first[b] : pr.nchunks;
+    const int src0 = (2 * lane) & 31, src1 = (2 * lane + 1) & 31;
+    const bool upper = lane >= 16;  // elements 2 lane, 2 lane + 1 lie in the block's second half
+    // batches of kAhead chunks, double-buffered as in state_pass
+    constexpr int kAhead = 8;
+    float w0[kAhead], w1[kAhead], dk[kAhead];
+#pragma unroll
+    for (int k = 0; k < kAhead; ++k) {
+        if (k < nc) {
+            w0[k] = s[(size_t)k * PN + lane];
+            w1[k] = s[(size_t)k * PN + 32 + lane];
+            dk[k] = __ldg(dec + k);
+        }
+    }
+    for (int c0 = 0; c0 < nc; c0 += kAhead) {
+        float n0[kAhead], n1[kAhead], dn[kAhead];
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k) {
+            if (c0 + kAhead + k < nc) {
+                n0[k] = s[(size_t)(c0 + kAhead + k) * PN + lane];
+                n1[k] = s[(size_t)(c0 + kAhead + k) * PN + 32 + lane];
+                dn[k] = __ldg(dec + c0 + kAhead + k);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k) {
+            if (c0 + k < nc) {  // warp-uniform
+                const float a0 = __shfl_sync(0xffffffffu, w0[k], src0), a1 = __shfl_sync(0xffffffffu, w1[k], src0);
+                const float b0 = __shfl_sync(0xffffffffu, w0[k], src1), b1 = __shfl_sync(0xffffffffu, w1[k], src1);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(st0, st1);
+                const float2 hf = __bfloat1622float2(hi);
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(st0 - hf.x, st1 - hf.y);
+                uint32_t *slot = reinterpret_cast<uint32_t *>(s + (size_t)(c0 + k) * PN);
+                slot[lane] = *reinterpret_cast<const uint32_t *>(&hi);
+                slot[32 + lane] = *reinterpret_cast<const uint32_t *>(&lo);
+                st0 = fmaf(dk[k], st0, upper ? a1 : a0);
+                st1 = fmaf(dk[k], st1, upper ? b1 : b0);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k) {
+            w0[k] = n0[k];
+            w1[k] = n1[k];
+            dk[k] = dn[k];
+        }
+    }
+    if (pr.final_state) {
+        pr.final_state[bh * PN + ea] = st0;
+        pr.final_state[bh * PN + ea + 1] = st1;
+    }
+}
+
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes)
 {
@@ -317,12 +393,17 @@ cudaError_t launch_chunk_out_simt(const Problem &pr, const Workspace &ws, cudaSt
     return cudaGetLastError();
 }
 
-cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream_t s)
+cudaError_t launch_state_pass(const Problem &pr, const Workspace &ws, cudaStream_t s, bool hilo)
 {
     const int PN = pr.headdim * pr.dstate;
-    const dim3 grid((PN + kThreads - 1) / kThreads, pr.nheads, pr.batch);
     profile_kernel_begin(s);
-    state_pass<<<grid, kThreads, 0, s>>>(pr, ws);
+    if (hilo) {  // one warp per 64-element block (PN is a multiple of 64 on the tcgen05 path)
+        const dim3 grid((PN / 2 + kThreads - 1) / kThreads, pr.nheads, pr.batch);
+        state_pass_hilo<<<grid, kThreads, 0, s>>>(pr, ws);
+    } else {
+        const dim3 grid((PN + kThreads - 1) / kThreads, pr.nheads, pr.batch);
+        state_pass<<<grid, kThreads, 0, s>>>(pr, ws);
+    }
     profile_kernel_end(s);
     return cudaGetLastError();
 }

@@ -81,13 +81,21 @@ __device__ __forceinline__ void segsum(const Problem &pr, int b, int h0, int nh,
                                        float *cs, float *dtv, float *warp_tot)
 {
     const int t = threadIdx.x;
-    for (int hh = 0; hh < nh; ++hh) {
+    const int j0 = 2 * t, j1 = 2 * t + 1;
+    // every head's loads first (nh <= 2), so that their latencies overlap
+    float d0[2], d1[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const size_t o = ((size_t)b * pr.seqlen + t0) * pr.nheads + h0 + hh;
+        d0[hh] = hh < nh && j0 < len ? __ldg(pr.dt + o + (size_t)j0 * pr.nheads) : 0.f;
+        d1[hh] = hh < nh && j1 < len ? __ldg(pr.dt + o + (size_t)j1 * pr.nheads) : 0.f;
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        if (hh >= nh) break;  // block-uniform
         const int h = h0 + hh;
         const float a = __ldg(pr.A + h) * scale;
-        const int j0 = 2 * t, j1 = 2 * t + 1;
-        const float d0 = j0 < len ? __ldg(pr.dt + ((size_t)b * pr.seqlen + t0 + j0) * pr.nheads + h) : 0.f;
-        const float d1 = j1 < len ? __ldg(pr.dt + ((size_t)b * pr.seqlen + t0 + j1) * pr.nheads + h) : 0.f;
-        float v0 = d0 * a, v1 = d1 * a;
+        float v0 = d0[hh] * a, v1 = d1[hh] * a;
         scan_128x2(v0, v1, warp_tot);
         cs[hh * 256 + j0] = v0;
         cs[hh * 256 + j1] = v1;
@@ -95,25 +103,46 @@ __device__ __forceinline__ void segsum(const Problem &pr, int b, int h0, int nh,
             dtv[hh * 256 + j0] = j0 < len ? __ldg(pr.dtin + ((size_t)b * pr.seqlen + t0 + j0) * pr.nheads + h) : 0.f;
             dtv[hh * 256 + j1] = j1 < len ? __ldg(pr.dtin + ((size_t)b * pr.seqlen + t0 + j1) * pr.nheads + h) : 0.f;
         } else {
-            dtv[hh * 256 + j0] = d0;
-            dtv[hh * 256 + j1] = d1;
+            dtv[hh * 256 + j0] = d0[hh];
+            dtv[hh * 256 + j1] = d1[hh];
         }
     }
     __syncthreads();
 }
 
-// segsum over a 256-thread block: thread t holds token t.  warp_tot: 8 floats.
-__device__ __forceinline__ void segsum256(const Problem &pr, int b, int h0, int nh, int t0, int len, float scale,
-                                          float *cs, float *dtv, float *warp_tot)
+// The chunk's cumulative decays in two steps, so that the loads of dt can be issued
+// long before the scan needs them: seg_load reads thread t's token of each head
+// (nh <= 2); seg_scan writes the scaled inclusive prefix sums of dt * A into cs and
+// the per-token dt (dt_in when the caller passed one) into dtv.
+struct SegRegs {
+    float d[2], din[2];
+};
+
+__device__ __forceinline__ SegRegs seg_load(const Problem &pr, int b, int h0, int nh, int t0, int len)
+{
+    SegRegs r;
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const bool on = hh < nh && t < len;
+        const size_t o = ((size_t)b * pr.seqlen + t0 + t) * pr.nheads + h0 + hh;
+        r.d[hh] = on ? __ldg(pr.dt + o) : 0.f;
+        r.din[hh] = on && pr.dtin ? __ldg(pr.dtin + o) : 0.f;  // no use of a loaded value here
+    }
+    return r;
+}
+
+__device__ __forceinline__ void seg_scan(const Problem &pr, const SegRegs &r, int h0, int nh, float scale, float *cs,
+                                         float *dtv, float *warp_tot)
 {
     const int t = threadIdx.x;
-    for (int hh = 0; hh < nh; ++hh) {
-        const int h = h0 + hh;
-        const float a = __ldg(pr.A + h) * scale;
-        const float d = t < len ? __ldg(pr.dt + ((size_t)b * pr.seqlen + t0 + t) * pr.nheads + h) : 0.f;
-        cs[hh * 256 + t] = block_inclusive_scan_256(d * a, warp_tot);
-        dtv[hh * 256 + t] = pr.dtin ? (t < len ? __ldg(pr.dtin + ((size_t)b * pr.seqlen + t0 + t) * pr.nheads + h) : 0.f)
-                                    : d;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        if (hh < nh) {  // block-uniform
+            const float a = __ldg(pr.A + h0 + hh) * scale;
+            cs[hh * 256 + t] = block_inclusive_scan_256(r.d[hh] * a, warp_tot);
+            dtv[hh * 256 + t] = pr.dtin ? r.din[hh] : r.d[hh];
+        }
     }
     __syncthreads();
 }
@@ -293,9 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // chunk output
 // ---------------------------------------------------------------------------
 
-// Phase-1 slabs (C | B | h_hi | h_lo), then the masked S tiles: 64 KiB when the
-// tile spans 128 columns, 80 KiB when it spans 256.
-__host__ __device__ constexpr int region1_bytes(int jmax) { return jmax > 128 ? 80 * 1024 : 64 * 1024; }
+// One phase-1 stage (the C | B | h_hi | h_lo slabs of one 64-wide slice of the state
+// dimension): 64 KiB when the tile spans 128 columns, 80 KiB when it spans 256.  Two
+// stages alternate, then a 32 KiB fp32 entry-state slice.  Once the slices are done,
+// the x tile takes the first 64 KiB and the masked S tiles of both heads the rest.
+__host__ __device__ constexpr int stage_bytes(int jmax) { return jmax > 128 ? 80 * 1024 : 64 * 1024; }
 
 constexpr int kOutThreads = 256;  // chunk_out_tc: warps w and w + 4 share TMEM lanes 32 (w & 3) ..
 
@@ -306,7 +337,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                  const __grid_constant__ CUtensorMap smap, Problem pr, Workspace ws)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_tma, bar_x, bar_mma, bar_h[2];
+    __shared__ __align__(8) uint64_t bar_tma[2], bar_mma[2], bar_x, bar_mm2;
     __shared__ uint32_t tmem_slot;
     __shared__ float warp_tot[8];
     __shared__ __align__(16) float cs[2 * 256];
@@ -323,7 +354,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     if (i0 >= len) return;  // tile beyond the end of a partial last chunk (block-uniform)
     const int jn = i0 + kBoxRows;                 // columns j in [0, jn)
     const int nbj = jn / kBoxRows;                // 128-row boxes along j
-    const bool wide = jn > kBoxRows;              // 256 columns: one head per S pass, 512 TMEM columns
+    const bool wide = jn > kBoxRows;              // 256 columns: 512 TMEM columns
     const uint32_t tcols = wide ? 512 : 256;
     const uint32_t col_g = 0;
     const uint32_t col_yd = wide ? 256 : 0;       // narrow tiles reuse G's columns once S is built
@@ -333,20 +364,22 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 
     uint8_t *base = align1024(smem_raw);
     const int jmax = pr.chunk <= kBoxRows ? kBoxRows : 2 * kBoxRows;
-    uint8_t *r1 = base;                           // phase 1: C | B | h_hi | h_lo slabs; phase 2: S tiles
-    uint8_t *c_sl = r1;                           // 128 x 128 B
-    uint8_t *b_sl = r1 + kBoxBytes;               // jn x 128 B
-    uint8_t *h_sl = b_sl + jn * 128;              // 128 x 128 B, hi part of the state
-    uint8_t *l_sl = h_sl + kBoxBytes;             // 128 x 128 B, lo part of the state
-    uint8_t *xs = r1 + region1_bytes(jmax);       // 2 MN blocks, each jn x 128 B
-    uint8_t *hst = xs + 2 * jmax * 128;           // 2 x 32 KiB: an entry-state slab in fp32, by TMA
+    constexpr int nsl = NS / 64;                  // 64-wide slices of the state dimension
+    // stage k: C (128 x 128 B) | B (jn x 128 B) | h_hi | h_lo (128 x 128 B each); slice s
+    // uses stage (s + nsl) & 1, so that the last slice is in stage 1 and stage 0 is free
+    // for the x tile once slice nsl - 2 (if any) is multiplied
+    auto stage = [&](int sl) { return base + ((sl + nsl) & 1) * stage_bytes(jmax); };
+    auto bar_of = [&](uint64_t *bars, int sl) { return &bars[(sl + nsl) & 1]; };
+    uint8_t *xs = base;                           // x: 2 MN blocks, each jn x 128 B (<= 64 KiB)
+    uint8_t *r1 = base + 65536;                   // S tiles of every head, jn x 256 B each
 
     if (tid == 0) {
-        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_tma[0], 1);
+        mbar_init(&bar_tma[1], 1);
+        mbar_init(&bar_mma[0], 1);
+        mbar_init(&bar_mma[1], 1);
         mbar_init(&bar_x, 1);
-        mbar_init(&bar_mma, 1);
-        mbar_init(&bar_h[0], 1);
-        mbar_init(&bar_h[1], 1);
+        mbar_init(&bar_mm2, 1);
         mbar_fence_init();
         s_fail = 0;
     }
@@ -356,82 +389,61 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
-    if (tid == 0) {
-        tma_prefetch_desc(&xmap);
-        tma_prefetch_desc(&bmap);
-        tma_prefetch_desc(&cmap);
-        // the chunk's entry states (one P x NS fp32 block per head, from DRAM) into L2, so
-        // that phase 1's per-slab loads of them find them there
-        for (int hh = 0; hh < HB; ++hh)
-            bulk_prefetch_l2(ws.states + state_slot(pr, ref, h0 + hh) * (size_t)P * NS, (uint32_t)(P * NS * sizeof(float)));
+    // TMA issue: lane 0 of warp 1, so that lane 0 of warp 0 only waits for operands and
+    // issues MMAs.  A stage takes slice sl of C_i and B_j and of each head's entry state
+    // h_c, whose hi and lo bf16 terms the state pass laid out per slice (a [P][64] box of
+    // each at columns 128 sl and 128 sl + 64 of the slot's [P][2 NS] bf16 rows).
+    auto issue_stage = [&](int sl) {
+        uint8_t *st = stage(sl);
+        uint64_t *bar = bar_of(bar_tma, sl);
+        mbar_expect_tx(bar, (uint32_t)((1 + nbj) * kBoxBytes + 2 * kBoxBytes));
+        tma_load_3d(st, &cmap, bar, g * NS + 64 * sl, t0 + i0, b);
+        for (int r = 0; r < nbj; ++r)
+            tma_load_3d(st + kBoxBytes + r * kBoxBytes, &bmap, bar, g * NS + 64 * sl, t0 + r * kBoxRows, b);
+        uint8_t *h_sl = st + kBoxBytes + jn * 128, *l_sl = h_sl + kBoxBytes;
+        for (int hh = 0; hh < HB; ++hh) {
+            const int row = (int)(state_slot(pr, ref, h0 + hh) * P);
+            tma_load_3d(h_sl + hh * P * 128, &smap, bar, 128 * sl, row, 0);
+            tma_load_3d(l_sl + hh * P * 128, &smap, bar, 128 * sl + 64, row, 0);
+        }
+    };
+    auto issue_x = [&]() {  // the x rows of the whole tile span, both 64-column blocks
         mbar_expect_tx(&bar_x, (uint32_t)(2 * nbj * kBoxBytes));
         for (int k = 0; k < 2; ++k)
             for (int r = 0; r < nbj; ++r)
                 tma_load_3d(xs + k * jn * 128 + r * kBoxBytes, &xmap, &bar_x, hb * 128 + 64 * k, t0 + r * kBoxRows,
                             b);
-    }
-    segsum256(pr, b, h0, HB, t0, len, kLog2e, cs, dtv, warp_tot);  // log2 domain: decays via exp2f
-
-    // ---- phase 1: G = C_i B^T and Yoff = C_i h_c^T, over 64-wide slabs of the state dimension.
-    // The entry state comes by TMA as fp32 slabs (two [rows][32] boxes with the 128-byte
-    // swizzle per head, double-buffered, two slabs ahead) and is split into hi and lo bf16
-    // operand rows here.
-    const int m = tid & 127;  // h-slab row (h, p) written by this thread (chunks 4 half .. 4 half + 3)
-    constexpr int nsl = NS / 64;
-    auto issue_h = [&](int sl) {  // thread 0
-        uint8_t *dst = hst + (sl & 1) * 32768;
-        mbar_expect_tx(&bar_h[sl & 1], 32768u);
-        for (int hh = 0; hh < HB; ++hh)
-            for (int ch = 0; ch < 2; ++ch)
-                tma_load_3d(dst + ch * 16384 + hh * P * 128, &smap, &bar_h[sl & 1], 64 * sl + 32 * ch,
-                            (int)(state_slot(pr, ref, h0 + hh) * P), 0);
     };
-    if (tid == 0) {
-        issue_h(0);
-        if (nsl > 1) issue_h(1);
+    if (warp == 1 && lane == 0) {
+        tma_prefetch_desc(&smap);
+        tma_prefetch_desc(&cmap);
+        tma_prefetch_desc(&bmap);
+        issue_stage(0);
+        if (nsl > 1)
+            issue_stage(1);
+        else
+            issue_x();  // stage 0 is not used by the one slice
+        // the rest of the chunk's entry states (one P x NS block of hi / lo pairs per head,
+        // from DRAM) into L2, so that the later slice loads find them there
+        for (int hh = 0; hh < HB; ++hh)
+            bulk_prefetch_l2(ws.states + state_slot(pr, ref, h0 + hh) * (size_t)P * NS, (uint32_t)(P * NS * sizeof(float)));
+        tma_prefetch_desc(&xmap);
     }
-    bool ok = true;
-    for (int s = 0; s < nsl && ok; ++s) {
-        if (tid == 0) {
-            mbar_expect_tx(&bar_tma, (uint32_t)((1 + nbj) * kBoxBytes));
-            tma_load_3d(c_sl, &cmap, &bar_tma, g * NS + 64 * s, t0 + i0, b);
-            for (int r = 0; r < nbj; ++r)
-                tma_load_3d(b_sl + r * kBoxBytes, &bmap, &bar_tma, g * NS + 64 * s, t0 + r * kBoxRows, b);
-        }
-        // entry state slab -> hi and lo bf16 terms, 128-B swizzled K-major rows: this thread's
-        // row m, columns 32 half .. 32 half + 31 of the slab
-        if (!mbar_wait(&bar_h[s & 1], (s >> 1) & 1)) s_fail = 1;
-        {
-            const uint8_t *src = hst + (s & 1) * 32768 + half * 16384;
-            float f[32];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 v = *reinterpret_cast<const float4 *>(src + sw128(m, q));
-                f[4 * q] = v.x;
-                f[4 * q + 1] = v.y;
-                f[4 * q + 2] = v.z;
-                f[4 * q + 3] = v.w;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint4 hi = pack8(f + 8 * u);
-                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
-                float r[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 t = __bfloat1622float2(h2[e]);
-                    r[2 * e] = f[8 * u + 2 * e] - t.x;
-                    r[2 * e + 1] = f[8 * u + 2 * e + 1] - t.y;
+    // dt of this thread's token, read now and scanned after the slices
+    const SegRegs seg = seg_load(pr, b, h0, HB, t0, len);
+
+    // ---- phase 1: G = C_i B^T and Yoff = C_i (h_hi + h_lo)^T over the 64-wide slices of
+    // the state dimension, two stages in flight: slice s + 1 lands while slice s is
+    // multiplied.  The other warps wait for the last slice's MMAs below.
+    if (warp == 0) {
+        if (lane == 0) {
+            bool good = true;
+            for (int s = 0; s < nsl && good; ++s) {
+                uint8_t *c_sl = stage(s), *b_sl = c_sl + kBoxBytes, *h_sl = b_sl + jn * 128, *l_sl = h_sl + kBoxBytes;
+                if (!mbar_wait(bar_of(bar_tma, s), (s >> 1) & 1)) {
+                    good = false;
+                    break;
                 }
-                *reinterpret_cast<uint4 *>(h_sl + sw128(m, 4 * half + u)) = hi;
-                *reinterpret_cast<uint4 *>(l_sl + sw128(m, 4 * half + u)) = pack8(r);
-            }
-        }
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            if (s + 2 < nsl) issue_h(s + 2);  // every thread has read this slab's fp32 buffer
-            if (mbar_wait(&bar_tma, s & 1)) {
                 tc_fence_after();
                 const uint32_t id_g = idesc_bf16(128, jn, 0, 0);
                 constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 0);
@@ -444,34 +456,49 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                              (s | kk) != 0);
                     mma_bf16(tmem + col_yo, ad, sdesc_sw128(smem_u32(l_sl) + kk * 32, 16, 1024), id_o, 1);
                 }
-                mma_commit(&bar_mma);
-            } else {
-                s_fail = 1;
+                mma_commit(bar_of(bar_mma, s));
             }
+            if (!good) s_fail = 1;
         }
-        __syncthreads();
-        ok = !s_fail;
-        if (ok && !mbar_wait(&bar_mma, s & 1)) s_fail = 1;  // slabs are reused by the next iteration
-        __syncthreads();
-        ok = !s_fail;
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // the other stage is free once slice s - 1's MMAs are done: slice s + 1 goes
+            // there, or, after the last slice, the x tile (stage 0)
+            bool good = true;
+            for (int s = 1; s < nsl && good; ++s) {
+                if (!mbar_wait(bar_of(bar_mma, s - 1), ((s - 1) >> 1) & 1)) {
+                    good = false;
+                    break;
+                }
+                if (s + 1 < nsl)
+                    issue_stage(s + 1);
+                else
+                    issue_x();
+            }
+            if (!good) s_fail = 1;
+        }
+        __syncwarp();
     }
-    uint32_t mma_phase = (NS / 64) & 1;
+    // every slice's MMAs done (the last commit covers all earlier MMAs of this thread)
+    if (!mbar_wait(bar_of(bar_mma, nsl - 1), ((nsl - 1) >> 1) & 1)) s_fail = 1;
     tc_fence_after();
+    seg_scan(pr, seg, h0, HB, kLog2e, cs, dtv, warp_tot);  // log2 domain: decays via ex2; ends in a barrier
+    bool ok = !s_fail;
 
-    // ---- phase 2: S_h = G o decay o dt (causal) -> bf16; Ydiag_h = S_h x_h
+    // ---- phase 2: S_h = G o decay o dt (causal) -> bf16 for every head; Ydiag_h = S_h x_h
     const int i = quarter * 32 + lane;    // accumulator row of this thread
     const int ia = i0 + i;                // row within the chunk
     const bool row_ok = ia < len;
-    const int heads_per_pass = wide ? 1 : HB;
-    for (int hp0 = 0; hp0 < HB && ok; hp0 += heads_per_pass) {
+    if (ok) {
         const int njb = jn / 32;  // 32-column blocks, the first half of them for warps 0-3
         for (int jb = half * (njb / 2); jb < (half + 1) * (njb / 2); ++jb) {
             uint8_t *dst_base = r1;
             const int j0 = jb * 32;
             if (j0 > i0 + quarter * 32 + 31) {  // whole warp above the diagonal: zeros
                 const uint4 z = make_uint4(0, 0, 0, 0);
-                for (int hh = hp0; hh < hp0 + heads_per_pass; ++hh) {
-                    uint8_t *st = dst_base + (hh - hp0) * (jn * 256) + (j0 / 64) * kBoxBytes;
+                for (int hh = 0; hh < HB; ++hh) {
+                    uint8_t *st = dst_base + hh * (jn * 256) + (j0 / 64) * kBoxBytes;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4 *>(st + sw128(i, (j0 % 64) / 8 + u)) = z;
                 }
@@ -479,7 +506,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             }
             float gv[32];
             tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col_g + j0, gv);
-            for (int hh = hp0; hh < hp0 + heads_per_pass; ++hh) {
+            for (int hh = 0; hh < HB; ++hh) {
                 const float *csh = cs + hh * 256, *dth = dtv + hh * 256;
                 const float ci = csh[ia < 256 ? ia : 255];
                 // cs and dt of the block's 32 columns as float4s, the decays by the
@@ -500,7 +527,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                         sv[k] = (row_ok && j <= ia) ? gv[k] * e * dj[v] : 0.f;
                     }
                 }
-                uint8_t *st = dst_base + (hh - hp0) * (jn * 256) + (j0 / 64) * kBoxBytes;
+                uint8_t *st = dst_base + hh * (jn * 256) + (j0 / 64) * kBoxBytes;
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     *reinterpret_cast<uint4 *>(st + sw128(i, (j0 % 64) / 8 + u)) = pack8(sv + 8 * u);
@@ -513,8 +540,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             if (mbar_wait(&bar_x, 0)) {
                 tc_fence_after();
                 const uint32_t id_d = idesc_bf16(128, P, 0, 1);  // one head's headdim columns
-                for (int hh = hp0; hh < hp0 + heads_per_pass; ++hh) {
-                    const uint32_t s_addr = smem_u32(r1) + (hh - hp0) * (jn * 256);
+                for (int hh = 0; hh < HB; ++hh) {
+                    const uint32_t s_addr = smem_u32(r1) + hh * (jn * 256);
                     const uint32_t x_addr = smem_u32(xs) + (P == 64 ? hh : 0) * jn * 128;
                     for (int ks = 0; ks < jn / 16; ++ks) {
                         const uint64_t ad = sdesc_sw128(s_addr + (ks / 4) * kBoxBytes + (ks % 4) * 32, 16, 1024);
@@ -522,15 +549,14 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                         mma_bf16(tmem + col_yd + hh * P, ad, bd, id_d, ks > 0);
                     }
                 }
-                mma_commit(&bar_mma);
+                mma_commit(&bar_mm2);
             } else {
                 s_fail = 1;
             }
         }
         __syncthreads();
         ok = !s_fail;
-        if (ok && !mbar_wait(&bar_mma, mma_phase)) s_fail = 1;
-        mma_phase ^= 1;
+        if (ok && !mbar_wait(&bar_mm2, 0)) s_fail = 1;
         __syncthreads();
         ok = !s_fail;
         tc_fence_after();
@@ -631,7 +657,8 @@ size_t state_smem(const Problem &pr) { return 1024 + (size_t)(4 + pr.dstate / 64
 size_t out_smem(const Problem &pr)
 {
     const int jmax = pr.chunk <= kBoxRows ? kBoxRows : 2 * kBoxRows;
-    return 1024 + region1_bytes(jmax) + (size_t)2 * jmax * 128 + 2 * 32768;  // ..., x tile, entry-state slabs
+    // two stages, then room for the S tiles of both heads of a 256-column tile after x
+    return 1024 + 2 * (size_t)stage_bytes(jmax) + 32768;
 }
 
 template <int NS>
@@ -669,11 +696,12 @@ cudaError_t launch_tc(const Problem &pr, const Workspace &ws, cudaStream_t s, in
         if ((e = make_map(&cmap, pr.C, pr.ngroups * pr.dstate, pr.seqlen, mb)) != cudaSuccess) return e;
         CUtensorMap ymap, smap;
         if ((e = make_map(&ymap, pr.y, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
-        // the entry states h_c as [state rows = slots x headdim][NS] fp32, boxes of headdim rows x 32
+        // the entry states h_c as [state rows = slots x headdim][2 NS] bf16 (hi and lo terms per
+        // 64-wide slice, as the state pass writes them), boxes of headdim rows x 64
         const size_t slots = pr.chunks ? (size_t)pr.nheads * pr.total_chunks : (size_t)pr.batch * pr.nheads * pr.nchunks;
         if (slots * pr.headdim > (size_t)INT32_MAX) return cudaErrorInvalidValue;  // box row coordinates are 32-bit
-        if ((e = cached_tensor_map(&smap, ws.states, false, NS, (int)(slots * pr.headdim), 1, 32, pr.headdim, true)) !=
-            cudaSuccess)
+        if ((e = cached_tensor_map(&smap, ws.states, true, 2 * NS, (int)(slots * pr.headdim), 1, 64, pr.headdim,
+                                   true)) != cudaSuccess)
             return e;
         const size_t smem = out_smem(pr);
         if ((e = ensure_smem_limit(reinterpret_cast<const void *>(chunk_out_tc<NS>), smem)) != cudaSuccess) return e;

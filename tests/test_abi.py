@@ -137,7 +137,7 @@ def test_path_selection_is_a_pure_host_query(lib):
     assert ssd.ssd_fwd_kernels(16, 4096, 32, 128, 8, 128, 128, ssd.SSD_DTYPE_BF16) == ["ssd_fused_tc"]
     assert ssd.ssd_fwd_kernels(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == ["ssd_fused_tc"]
     assert ssd.ssd_fwd_kernels(1, 131072, 24, 64, 1, 256, 256, ssd.SSD_DTYPE_BF16) == [
-        "chunk_state_tc", "state_pass", "chunk_out_tc"]
+        "chunk_state_tc", "state_pass_hilo", "chunk_out_tc"]
 
 
 def test_block_length_of_long_chunks(lib):
