@@ -24,6 +24,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "ssd_internal.cuh"
@@ -324,8 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // One phase-1 stage (the C | B | h_hi | h_lo slabs of one 64-wide slice of the state
 // dimension): 64 KiB when the tile spans 128 columns, 80 KiB when it spans 256.  Two
-// stages alternate, then a 32 KiB fp32 entry-state slice.  Once the slices are done,
-// the x tile takes the first 64 KiB and the masked S tiles of both heads the rest.
+// stages alternate.  Once the slices are done, the x tile takes the first 64 KiB and
+// the masked S tiles (hi and lo terms) the next 128 KiB.
 __host__ __device__ constexpr int stage_bytes(int jmax) { return jmax > 128 ? 80 * 1024 : 64 * 1024; }
 
 constexpr int kOutThreads = 256;  // chunk_out_tc: warps w and w + 4 share TMEM lanes 32 (w & 3) ..
@@ -337,11 +338,12 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                  const __grid_constant__ CUtensorMap smap, Problem pr, Workspace ws)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_tma[2], bar_mma[2], bar_x, bar_mm2;
+    __shared__ __align__(8) uint64_t bar_tma[2], bar_mma[2], bar_x, bar_mm2[2];
     __shared__ uint32_t tmem_slot;
     __shared__ float warp_tot[8];
     __shared__ __align__(16) float cs[2 * 256];
     __shared__ __align__(16) float dtv[2 * 256];  // read as float4 in phase 2
+    __shared__ float s_mn[2][8], s_mx[2][8];
     __shared__ int s_fail;
 
     const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
@@ -354,11 +356,9 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     if (i0 >= len) return;  // tile beyond the end of a partial last chunk (block-uniform)
     const int jn = i0 + kBoxRows;                 // columns j in [0, jn)
     const int nbj = jn / kBoxRows;                // 128-row boxes along j
-    const bool wide = jn > kBoxRows;              // 256 columns: 512 TMEM columns
-    const uint32_t tcols = wide ? 512 : 256;
-    const uint32_t col_g = 0;
-    const uint32_t col_yd = wide ? 256 : 0;       // narrow tiles reuse G's columns once S is built
-    const uint32_t col_yo = wide ? 384 : 128;
+    // TMEM: G (jn columns), Ydiag and Yoff (128 each); one CTA per SM (its shared memory)
+    const uint32_t tcols = 512;
+    const uint32_t col_g = 0, col_yd = 256, col_yo = 384;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, half = warp >> 2;  // TMEM lanes 32 quarter ..; half of the columns
 
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     auto stage = [&](int sl) { return base + ((sl + nsl) & 1) * stage_bytes(jmax); };
     auto bar_of = [&](uint64_t *bars, int sl) { return &bars[(sl + nsl) & 1]; };
     uint8_t *xs = base;                           // x: 2 MN blocks, each jn x 128 B (<= 64 KiB)
-    uint8_t *r1 = base + 65536;                   // S tiles of every head, jn x 256 B each
+    uint8_t *r1 = base + 65536;                   // S tiles (hi, lo) of a pass's heads: 128 KiB
 
     if (tid == 0) {
         mbar_init(&bar_tma[0], 1);
@@ -379,7 +379,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         mbar_init(&bar_mma[0], 1);
         mbar_init(&bar_mma[1], 1);
         mbar_init(&bar_x, 1);
-        mbar_init(&bar_mm2, 1);
+        mbar_init(&bar_mm2[0], 1);
+        mbar_init(&bar_mm2[1], 1);
         mbar_fence_init();
         s_fail = 0;
     }
@@ -486,34 +487,108 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     seg_scan(pr, seg, h0, HB, kLog2e, cs, dtv, warp_tot);  // log2 domain: decays via ex2; ends in a barrier
     bool ok = !s_fail;
 
-    // ---- phase 2: S_h = G o decay o dt (causal) -> bf16 for every head; Ydiag_h = S_h x_h
+    // The decays exp2(cs_i - cs_j) in rank-one form, exp2(cs_i - ref) exp2(ref - cs_j) with
+    // ref the midpoint of each head's cs range over the chunk, whenever that range is at most
+    // kFactorSpan (every factor then within 2^(+-kFactorSpan / 2) of 1): one exp per row and
+    // per column instead of one per element of S.  The column factors, times dt_j, replace
+    // dtv.  A wider range keeps the exp per element.
+    constexpr float kFactorSpan = 160.f;  // log2 units
+    float rowf[2] = {1.f, 1.f};
+    bool factored;
+    {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const bool on = hh < HB && tid < len;
+            float mn = on ? cs[hh * 256 + tid] : 3.0e38f, mx = on ? cs[hh * 256 + tid] : -3.0e38f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
+            if (lane == 0) {
+                s_mn[hh][warp] = mn;
+                s_mx[hh][warp] = mx;
+            }
+        }
+        __syncthreads();
+        float ref[2];
+        factored = true;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float mn = s_mn[hh][0], mx = s_mx[hh][0];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) {
+                mn = fminf(mn, s_mn[hh][w]);
+                mx = fmaxf(mx, s_mx[hh][w]);
+            }
+            ref[hh] = 0.5f * (mn + mx);
+            if (hh < HB && !(mx - mn <= kFactorSpan)) factored = false;  // block-uniform
+        }
+        if (factored) {
+            const int ir = i0 + (warp & 3) * 32 + lane;  // this thread's accumulator row in phase 2
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                if (hh < HB) {
+                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(rowf[hh]) : "f"(cs[hh * 256 + (ir < 256 ? ir : 255)] - ref[hh]));
+                    float c;
+                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(c) : "f"(ref[hh] - cs[hh * 256 + tid]));
+                    dtv[hh * 256 + tid] = tid < len ? c * dtv[hh * 256 + tid] : 0.f;
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- phase 2: S_h = G o decay o dt (causal) as hi + lo bf16 terms (a single rounding of
+    // S costs up to 2^-9 |y_i| where one term dominates a row, i.e. under strong decay, when
+    // |y| reaches ~10x its RMS); Ydiag_h = S_hi x_h + S_lo x_h.  S goes in K-chunks of 128
+    // columns (head-major), double-buffered in 64 KiB (hi, then lo): chunk k + 1 is built
+    // while chunk k is multiplied.
     const int i = quarter * 32 + lane;    // accumulator row of this thread
     const int ia = i0 + i;                // row within the chunk
     const bool row_ok = ia < len;
-    if (ok) {
-        const int njb = jn / 32;  // 32-column blocks, the first half of them for warps 0-3
-        for (int jb = half * (njb / 2); jb < (half + 1) * (njb / 2); ++jb) {
-            uint8_t *dst_base = r1;
-            const int j0 = jb * 32;
+    const int nhalf = jn / 128;           // K-chunks per head
+    const int nkc = ok ? HB * nhalf : 0;  // block-uniform; no early exit below, so every
+    bool t0good = true;                   // thread meets every barrier of the loop
+    for (int kc = 0; kc < nkc; ++kc) {
+        const int hh = kc / nhalf, jh = kc % nhalf;
+        uint8_t *buf = r1 + (kc & 1) * 65536;
+        // the buffer was last read by the MMAs of chunk kc - 2
+        if (kc >= 2 && !mbar_wait(&bar_mm2[kc & 1], ((kc - 2) >> 1) & 1)) s_fail = 1;
+        const float *csh = cs + hh * 256, *dth = dtv + hh * 256;
+        const float ci = csh[ia < 256 ? ia : 255];
+        const float rf = hh == 0 ? rowf[0] : rowf[1];
+        for (int lb = half; lb < 4; lb += 2) {  // 32-column blocks lb of the chunk: warps 0-3 even, 4-7 odd
+            const int j0 = 128 * jh + 32 * lb;
+            uint8_t *st = buf + (lb / 2) * kBoxBytes;
+            const int cq = (lb & 1) * 4;          // first 16-byte column of the block in its 64-column box
             if (j0 > i0 + quarter * 32 + 31) {  // whole warp above the diagonal: zeros
                 const uint4 z = make_uint4(0, 0, 0, 0);
-                for (int hh = 0; hh < HB; ++hh) {
-                    uint8_t *st = dst_base + hh * (jn * 256) + (j0 / 64) * kBoxBytes;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4 *>(st + sw128(i, (j0 % 64) / 8 + u)) = z;
+                for (int u = 0; u < 4; ++u) {
+                    *reinterpret_cast<uint4 *>(st + sw128(i, cq + u)) = z;
+                    *reinterpret_cast<uint4 *>(st + 32768 + sw128(i, cq + u)) = z;
                 }
                 continue;
             }
             float gv[32];
             tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col_g + j0, gv);
-            for (int hh = 0; hh < HB; ++hh) {
-                const float *csh = cs + hh * 256, *dth = dtv + hh * 256;
-                const float ci = csh[ia < 256 ? ia : 255];
-                // cs and dt of the block's 32 columns as float4s, the decays by the
-                // hardware base-2 exponential (ex2.approx, relative error ~2^-22; the tile
-                // is rounded to bf16): a per-element exp2f with scalar loads ran without
-                // instruction-level parallelism and took ~70% of the phase
-                float sv[32];
+            // cs and dt (or the column factors) of the block's 32 columns as float4s
+            float sv[32];
+            if (factored) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 f4 = reinterpret_cast<const float4 *>(dth + j0)[q];
+                    const float fj[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int k = 4 * q + v, j = j0 + k;
+                        // masked entries (j > row) are discarded, whatever the product is
+                        sv[k] = (row_ok && j <= ia) ? gv[k] * (fj[v] * rf) : 0.f;
+                    }
+                }
+            } else {
+                // the decays by the hardware base-2 exponential (ex2.approx, relative error ~2^-22)
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const float4 c4 = reinterpret_cast<const float4 *>(csh + j0)[q];
@@ -527,40 +602,50 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                         sv[k] = (row_ok && j <= ia) ? gv[k] * e * dj[v] : 0.f;
                     }
                 }
-                uint8_t *st = dst_base + hh * (jn * 256) + (j0 / 64) * kBoxBytes;
+            }
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    *reinterpret_cast<uint4 *>(st + sw128(i, (j0 % 64) / 8 + u)) = pack8(sv + 8 * u);
+            for (int u = 0; u < 4; ++u) {
+                const uint4 hi = pack8(sv + 8 * u);
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
+                float r[8];
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const float2 t = __bfloat1622float2(h2[e2]);
+                    r[2 * e2] = sv[8 * u + 2 * e2] - t.x;
+                    r[2 * e2 + 1] = sv[8 * u + 2 * e2 + 1] - t.y;
+                }
+                *reinterpret_cast<uint4 *>(st + sw128(i, cq + u)) = hi;
+                *reinterpret_cast<uint4 *>(st + 32768 + sw128(i, cq + u)) = pack8(r);
             }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
-            if (mbar_wait(&bar_x, 0)) {
+        if (tid == 0 && t0good) {
+            if (kc == 0 && !mbar_wait(&bar_x, 0)) {
+                t0good = false;
+                s_fail = 1;
+            } else {
                 tc_fence_after();
                 const uint32_t id_d = idesc_bf16(128, P, 0, 1);  // one head's headdim columns
-                for (int hh = 0; hh < HB; ++hh) {
-                    const uint32_t s_addr = smem_u32(r1) + hh * (jn * 256);
-                    const uint32_t x_addr = smem_u32(xs) + (P == 64 ? hh : 0) * jn * 128;
-                    for (int ks = 0; ks < jn / 16; ++ks) {
-                        const uint64_t ad = sdesc_sw128(s_addr + (ks / 4) * kBoxBytes + (ks % 4) * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(x_addr + ks * 2048, jn * 128, 1024);
-                        mma_bf16(tmem + col_yd + hh * P, ad, bd, id_d, ks > 0);
-                    }
+                const uint32_t s_addr = smem_u32(buf);
+                const uint32_t x_addr = smem_u32(xs) + (P == 64 ? hh : 0) * jn * 128;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t so = (ks / 4) * kBoxBytes + (ks % 4) * 32;
+                    const uint64_t bd = sdesc_sw128(x_addr + (8 * jh + ks) * 2048, jn * 128, 1024);
+                    mma_bf16(tmem + col_yd + hh * P, sdesc_sw128(s_addr + so, 16, 1024), bd, id_d, (jh | ks) != 0);
+                    mma_bf16(tmem + col_yd + hh * P, sdesc_sw128(s_addr + 32768 + so, 16, 1024), bd, id_d, 1);
                 }
-                mma_commit(&bar_mm2);
-            } else {
-                s_fail = 1;
+                mma_commit(&bar_mm2[kc & 1]);
             }
         }
-        __syncthreads();
-        ok = !s_fail;
-        if (ok && !mbar_wait(&bar_mm2, 0)) s_fail = 1;
-        __syncthreads();
-        ok = !s_fail;
-        tc_fence_after();
     }
+    // every chunk's MMAs done (the last commit covers the earlier ones)
+    if (nkc > 0 && !mbar_wait(&bar_mm2[(nkc - 1) & 1], ((nkc - 1) >> 1) & 1)) s_fail = 1;
+    __syncthreads();
+    ok = !s_fail;
+    tc_fence_after();
 
     // ---- phase 3: y = Ydiag + exp(cs_i) Yoff + D x, staged over this tile's x rows and
     // stored by TMA when the tile's 128 rows all belong to the chunk (the batch layout
@@ -657,8 +742,8 @@ size_t state_smem(const Problem &pr) { return 1024 + (size_t)(4 + pr.dstate / 64
 size_t out_smem(const Problem &pr)
 {
     const int jmax = pr.chunk <= kBoxRows ? kBoxRows : 2 * kBoxRows;
-    // two stages, then room for the S tiles of both heads of a 256-column tile after x
-    return 1024 + 2 * (size_t)stage_bytes(jmax) + 32768;
+    // two stages of the slices; after them x (64 KiB at most) and 128 KiB of S tiles
+    return 1024 + std::max<size_t>(2 * (size_t)stage_bytes(jmax), 65536 + 131072);
 }
 
 template <int NS>

@@ -358,6 +358,25 @@ def test_wide_decay_on_each_fused_kernel(case):
     print(f"{kern} wide: y error {ey:.2e} x RMS, final state {ef:.2e} x RMS")
 
 
+@pytest.mark.parametrize("dims,Q", [((1, 700, 4, 64, 256, 1), 256), ((2, 600, 4, 128, 256, 2), 256),
+                                    ((1, 520, 6, 64, 256, 3), 128)],
+                         ids=["P64Q256", "P128Q256", "P64Q128"])
+@pytest.mark.parametrize("mix", ["wide", "mixed"])
+def test_wide_decay_on_the_three_kernel_path(dims, Q, mix):
+    """dstate 256 (the three-kernel tcgen05 path): chunks whose in-chunk decay range
+    is beyond the rank-one form of chunk_out_tc take the exp per element; with
+    "mixed", only half the heads (and so some head blocks) do."""
+    b, L, H, P, N, G = dims
+    assert ssd.ssd_fwd_path(b, L, H, P, G, N, Q, ssd.SSD_DTYPE_BF16) == "tcgen05"
+    if mix == "wide":
+        inp = make_inputs(b, L, H, P, N, G, "bf16", seed=81 + L, dt_range=(0.5, 2.0), with_init=True)
+    else:
+        inp = make_inputs(b, L, H, P, N, G, "bf16", seed=82 + L, with_init=True)
+        inp["dt"][:, :, H // 2:] *= 40.0
+    ey, ef = check_full(inp, Q)
+    print(f"three-kernel {mix}: y error {ey:.2e} x RMS, final state {ef:.2e} x RMS")
+
+
 @pytest.mark.parametrize("kern,dims", [("ssd_fused_pipe_tc", (2, 512, 40, 64, 64, 1)),
                                        ("ssd_fused_tc", (2, 512, 8, 64, 128, 2)),
                                        ("ssd_seq_pipe_tc", (1, 3000, 16, 64, 64, 1))])
