@@ -141,8 +141,11 @@ __device__ __forceinline__ void seg_scan(const Problem &pr, const SegRegs &r, in
     for (int hh = 0; hh < 2; ++hh) {
         if (hh < nh) {  // block-uniform
             const float a = __ldg(pr.A + h0 + hh) * scale;
-            cs[hh * 256 + t] = block_inclusive_scan_256(r.d[hh] * a, warp_tot);
-            dtv[hh * 256 + t] = pr.dtin ? r.din[hh] : r.d[hh];
+            const float v = block_inclusive_scan_256(r.d[hh] * a, warp_tot);
+            if (t < 256) {  // a 288-thread block: its ninth warp holds no token
+                cs[hh * 256 + t] = v;
+                dtv[hh * 256 + t] = pr.dtin ? r.din[hh] : r.d[hh];
+            }
         }
     }
     __syncthreads();
@@ -329,7 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the masked S tiles (hi and lo terms) the next 128 KiB.
 __host__ __device__ constexpr int stage_bytes(int jmax) { return jmax > 128 ? 80 * 1024 : 64 * 1024; }
 
-constexpr int kOutThreads = 256;  // chunk_out_tc: warps w and w + 4 share TMEM lanes 32 (w & 3) ..
+// chunk_out_tc: warps w and w + 4 (w < 4) share TMEM lanes 32 w .. 32 w + 31 and build S
+// and the epilogue; warp 8 issues the MMAs of the S products, so that no building warp
+// waits for an MMA issue
+constexpr int kOutThreads = 288;
 
 template <int NS>
 __global__ void __launch_bounds__(kOutThreads, 1)
@@ -338,12 +344,12 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                  const __grid_constant__ CUtensorMap smap, Problem pr, Workspace ws)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_tma[2], bar_mma[2], bar_x, bar_mm2[2];
+    __shared__ __align__(8) uint64_t bar_tma[2], bar_mma[2], bar_x, bar_mm2[2], bar_built[2];
     __shared__ uint32_t tmem_slot;
-    __shared__ float warp_tot[8];
+    __shared__ float warp_tot[9];
     __shared__ __align__(16) float cs[2 * 256];
     __shared__ __align__(16) float dtv[2 * 256];  // read as float4 in phase 2
-    __shared__ float s_mn[2][8], s_mx[2][8];
+    __shared__ float s_mn[2][9], s_mx[2][9];
     __shared__ int s_fail;
 
     const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
@@ -381,6 +387,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         mbar_init(&bar_x, 1);
         mbar_init(&bar_mm2[0], 1);
         mbar_init(&bar_mm2[1], 1);
+        mbar_init(&bar_built[0], 256);  // every building thread, once per S chunk
+        mbar_init(&bar_built[1], 256);
         mbar_fence_init();
         s_fail = 0;
     }
@@ -491,7 +499,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     // ref the midpoint of each head's cs range over the chunk, whenever that range is at most
     // kFactorSpan (every factor then within 2^(+-kFactorSpan / 2) of 1): one exp per row and
     // per column instead of one per element of S.  The column factors, times dt_j, replace
-    // dtv.  A wider range keeps the exp per element.
+    // dtv and go into S; the row factor multiplies row i of S x in the epilogue.  A wider
+    // range keeps the exp per element (and a row factor of 1).
     constexpr float kFactorSpan = 160.f;  // log2 units
     float rowf[2] = {1.f, 1.f};
     bool factored;
@@ -499,7 +508,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const bool on = hh < HB && tid < len;
-            float mn = on ? cs[hh * 256 + tid] : 3.0e38f, mx = on ? cs[hh * 256 + tid] : -3.0e38f;
+            const float cv = cs[hh * 256 + (tid & 255)];
+            float mn = on ? cv : 3.0e38f, mx = on ? cv : -3.0e38f;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
@@ -530,9 +540,11 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             for (int hh = 0; hh < 2; ++hh) {
                 if (hh < HB) {
                     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(rowf[hh]) : "f"(cs[hh * 256 + (ir < 256 ? ir : 255)] - ref[hh]));
-                    float c;
-                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(c) : "f"(ref[hh] - cs[hh * 256 + tid]));
-                    dtv[hh * 256 + tid] = tid < len ? c * dtv[hh * 256 + tid] : 0.f;
+                    if (tid < 256) {  // the ninth warp holds no column
+                        float c;
+                        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(c) : "f"(ref[hh] - cs[hh * 256 + tid]));
+                        dtv[hh * 256 + tid] = tid < len ? c * dtv[hh * 256 + tid] : 0.f;
+                    }
                 }
             }
         }
@@ -548,99 +560,113 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     const int ia = i0 + i;                // row within the chunk
     const bool row_ok = ia < len;
     const int nhalf = jn / 128;           // K-chunks per head
-    const int nkc = ok ? HB * nhalf : 0;  // block-uniform; no early exit below, so every
-    bool t0good = true;                   // thread meets every barrier of the loop
-    for (int kc = 0; kc < nkc; ++kc) {
-        const int hh = kc / nhalf, jh = kc % nhalf;
-        uint8_t *buf = r1 + (kc & 1) * 65536;
-        // the buffer was last read by the MMAs of chunk kc - 2
-        if (kc >= 2 && !mbar_wait(&bar_mm2[kc & 1], ((kc - 2) >> 1) & 1)) s_fail = 1;
-        const float *csh = cs + hh * 256, *dth = dtv + hh * 256;
-        const float ci = csh[ia < 256 ? ia : 255];
-        const float rf = hh == 0 ? rowf[0] : rowf[1];
-        for (int lb = half; lb < 4; lb += 2) {  // 32-column blocks lb of the chunk: warps 0-3 even, 4-7 odd
-            const int j0 = 128 * jh + 32 * lb;
-            uint8_t *st = buf + (lb / 2) * kBoxBytes;
-            const int cq = (lb & 1) * 4;          // first 16-byte column of the block in its 64-column box
-            if (j0 > i0 + quarter * 32 + 31) {  // whole warp above the diagonal: zeros
-                const uint4 z = make_uint4(0, 0, 0, 0);
+    const int nkc = ok ? HB * nhalf : 0;  // block-uniform
+    if (warp < 8) {
+        for (int kc = 0; kc < nkc; ++kc) {
+            const int hh = kc / nhalf, jh = kc % nhalf;
+            uint8_t *buf = r1 + (kc & 1) * 65536;
+            // the buffer was last read by the MMAs of chunk kc - 2
+            if (kc >= 2 && !mbar_wait(&bar_mm2[kc & 1], ((kc - 2) >> 1) & 1)) s_fail = 1;
+            const float *csh = cs + hh * 256, *dth = dtv + hh * 256;
+            const float ci = csh[ia < 256 ? ia : 255];
+            for (int lb = half; lb < 4; lb += 2) {  // 32-column blocks lb of the chunk: warps 0-3 even, 4-7 odd
+                const int j0 = 128 * jh + 32 * lb;
+                uint8_t *st = buf + (lb / 2) * kBoxBytes;
+                const int cq = (lb & 1) * 4;          // first 16-byte column of the block in its 64-column box
+                if (j0 > i0 + quarter * 32 + 31) {  // whole warp above the diagonal: zeros
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        *reinterpret_cast<uint4 *>(st + sw128(i, cq + u)) = z;
+                        *reinterpret_cast<uint4 *>(st + 32768 + sw128(i, cq + u)) = z;
+                    }
+                    continue;
+                }
+                float gv[32];
+                tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col_g + j0, gv);
+                // cs and dt (or the column factors) of the block's 32 columns as float4s
+                float sv[32];
+                // every row of the warp in the chunk and past the block's last column: no mask
+                const bool full = j0 + 31 <= i0 + quarter * 32 && i0 + quarter * 32 + 31 < len;
+                if (factored && full) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 f4 = reinterpret_cast<const float4 *>(dth + j0)[q];
+                        sv[4 * q] = gv[4 * q] * f4.x;
+                        sv[4 * q + 1] = gv[4 * q + 1] * f4.y;
+                        sv[4 * q + 2] = gv[4 * q + 2] * f4.z;
+                        sv[4 * q + 3] = gv[4 * q + 3] * f4.w;
+                    }
+                } else if (factored) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 f4 = reinterpret_cast<const float4 *>(dth + j0)[q];
+                        const float fj[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int k = 4 * q + v, j = j0 + k;
+                            // masked entries (j > row) are discarded, whatever the product is
+                            sv[k] = (row_ok && j <= ia) ? gv[k] * fj[v] : 0.f;
+                        }
+                    }
+                } else {
+                    // the decays by the hardware base-2 exponential (ex2.approx, relative error ~2^-22)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 c4 = reinterpret_cast<const float4 *>(csh + j0)[q];
+                        const float4 d4 = reinterpret_cast<const float4 *>(dth + j0)[q];
+                        const float cj[4] = {c4.x, c4.y, c4.z, c4.w}, dj[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int k = 4 * q + v, j = j0 + k;
+                            float e;  // masked entries (j > row) are discarded below, whatever e is
+                            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(ci - cj[v]));
+                            sv[k] = (row_ok && j <= ia) ? gv[k] * e * dj[v] : 0.f;
+                        }
+                    }
+                }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    *reinterpret_cast<uint4 *>(st + sw128(i, cq + u)) = z;
-                    *reinterpret_cast<uint4 *>(st + 32768 + sw128(i, cq + u)) = z;
-                }
-                continue;
-            }
-            float gv[32];
-            tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col_g + j0, gv);
-            // cs and dt (or the column factors) of the block's 32 columns as float4s
-            float sv[32];
-            if (factored) {
+                    const uint4 hi = pack8(sv + 8 * u);
+                    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
+                    float r[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 f4 = reinterpret_cast<const float4 *>(dth + j0)[q];
-                    const float fj[4] = {f4.x, f4.y, f4.z, f4.w};
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const int k = 4 * q + v, j = j0 + k;
-                        // masked entries (j > row) are discarded, whatever the product is
-                        sv[k] = (row_ok && j <= ia) ? gv[k] * (fj[v] * rf) : 0.f;
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const float2 t = __bfloat1622float2(h2[e2]);
+                        r[2 * e2] = sv[8 * u + 2 * e2] - t.x;
+                        r[2 * e2 + 1] = sv[8 * u + 2 * e2 + 1] - t.y;
                     }
-                }
-            } else {
-                // the decays by the hardware base-2 exponential (ex2.approx, relative error ~2^-22)
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 c4 = reinterpret_cast<const float4 *>(csh + j0)[q];
-                    const float4 d4 = reinterpret_cast<const float4 *>(dth + j0)[q];
-                    const float cj[4] = {c4.x, c4.y, c4.z, c4.w}, dj[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const int k = 4 * q + v, j = j0 + k;
-                        float e;  // masked entries (j > row) are discarded below, whatever e is
-                        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(ci - cj[v]));
-                        sv[k] = (row_ok && j <= ia) ? gv[k] * e * dj[v] : 0.f;
-                    }
+                    *reinterpret_cast<uint4 *>(st + sw128(i, cq + u)) = hi;
+                    *reinterpret_cast<uint4 *>(st + 32768 + sw128(i, cq + u)) = pack8(r);
                 }
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint4 hi = pack8(sv + 8 * u);
-                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
-                float r[8];
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    const float2 t = __bfloat1622float2(h2[e2]);
-                    r[2 * e2] = sv[8 * u + 2 * e2] - t.x;
-                    r[2 * e2 + 1] = sv[8 * u + 2 * e2 + 1] - t.y;
-                }
-                *reinterpret_cast<uint4 *>(st + sw128(i, cq + u)) = hi;
-                *reinterpret_cast<uint4 *>(st + 32768 + sw128(i, cq + u)) = pack8(r);
-            }
+            fence_async_smem();  // the S chunk, written here, is read by the tensor cores
+            mbar_arrive(&bar_built[kc & 1]);
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0 && t0good) {
-            if (kc == 0 && !mbar_wait(&bar_x, 0)) {
-                t0good = false;
-                s_fail = 1;
-            } else {
-                tc_fence_after();
-                const uint32_t id_d = idesc_bf16(128, P, 0, 1);  // one head's headdim columns
-                const uint32_t s_addr = smem_u32(buf);
-                const uint32_t x_addr = smem_u32(xs) + (P == 64 ? hh : 0) * jn * 128;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t so = (ks / 4) * kBoxBytes + (ks % 4) * 32;
-                    const uint64_t bd = sdesc_sw128(x_addr + (8 * jh + ks) * 2048, jn * 128, 1024);
-                    mma_bf16(tmem + col_yd + hh * P, sdesc_sw128(s_addr + so, 16, 1024), bd, id_d, (jh | ks) != 0);
-                    mma_bf16(tmem + col_yd + hh * P, sdesc_sw128(s_addr + 32768 + so, 16, 1024), bd, id_d, 1);
-                }
-                mma_commit(&bar_mm2[kc & 1]);
+    } else if (lane == 0) {  // warp 8: the MMAs of each S chunk once every building thread has arrived
+        bool good = true;
+        for (int kc = 0; kc < nkc && good; ++kc) {
+            const int hh = kc / nhalf, jh = kc % nhalf;
+            if (!mbar_wait(&bar_built[kc & 1], (kc >> 1) & 1) || (kc == 0 && !mbar_wait(&bar_x, 0))) {
+                good = false;
+                break;
             }
+            tc_fence_after();
+            const uint32_t id_d = idesc_bf16(128, P, 0, 1);  // one head's headdim columns
+            const uint32_t s_addr = smem_u32(r1 + (kc & 1) * 65536);
+            const uint32_t x_addr = smem_u32(xs) + (P == 64 ? hh : 0) * jn * 128;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t so = (ks / 4) * kBoxBytes + (ks % 4) * 32;
+                const uint64_t bd = sdesc_sw128(x_addr + (8 * jh + ks) * 2048, jn * 128, 1024);
+                mma_bf16(tmem + col_yd + hh * P, sdesc_sw128(s_addr + so, 16, 1024), bd, id_d, (jh | ks) != 0);
+                mma_bf16(tmem + col_yd + hh * P, sdesc_sw128(s_addr + 32768 + so, 16, 1024), bd, id_d, 1);
+            }
+            mma_commit(&bar_mm2[kc & 1]);
         }
+        if (!good) s_fail = 1;
     }
+    __syncwarp();
     // every chunk's MMAs done (the last commit covers the earlier ones)
     if (nkc > 0 && !mbar_wait(&bar_mm2[(nkc - 1) & 1], ((nkc - 1) >> 1) & 1)) s_fail = 1;
     __syncthreads();
@@ -653,11 +679,12 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     // tensor map), else stored row by row
     const bool tma_out = !pr.chunks && (pr.chunk == kBoxRows || pr.chunk == 2 * kBoxRows);
     if (ok && !mbar_wait(&bar_x, 0)) ok = false;  // x tile (already complete) visible to every thread
-    if (ok) {
+    if (ok && warp < 8) {
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         for (int hh = 0; hh < HB; ++hh) {
             const int h = h0 + hh;
             const float e = exp2f(cs[hh * 256 + (ia < 256 ? ia : 255)]);
+            const float rf = hh == 0 ? rowf[0] : rowf[1];  // 1 unless the decays are factored
             const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
             __nv_bfloat16 *yrow = static_cast<__nv_bfloat16 *>(pr.y) + (((size_t)b * L + t0 + ia) * H + h) * P;
             for (int p0 = half * (P / 2); p0 < (half + 1) * (P / 2); p0 += 32) {
@@ -677,8 +704,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                         for (int v = 0; v < 4; ++v) {
                             const float2 xf = __bfloat1622float2(x2[v]);
                             const int k = 8 * u + 2 * v;
-                            out[2 * v] = yd[k] + e * yo[k] + Dh * xf.x;
-                            out[2 * v + 1] = yd[k + 1] + e * yo[k + 1] + Dh * xf.y;
+                            out[2 * v] = fmaf(rf, yd[k], fmaf(e, yo[k], Dh * xf.x));
+                            out[2 * v + 1] = fmaf(rf, yd[k + 1], fmaf(e, yo[k + 1], Dh * xf.y));
                         }
                         ov[u] = pack8(out);
                     }
@@ -694,7 +721,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 }
             }
         }
-    } else if (tid == 0) {
+    } else if (!ok && tid == 0) {
         set_error(pr, kDevErrTimeout);
     }
     if (tma_out) {
