@@ -133,6 +133,27 @@ __device__ __forceinline__ SegRegs seg_load(const Problem &pr, int b, int h0, in
     return r;
 }
 
+// Barrier of the 256 threads (warps 0-7) of a larger block, while its other warps work on.
+__device__ __forceinline__ void sync256() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Inclusive scan of one value per thread over threads 0-255 (named barrier 1).
+__device__ __forceinline__ float scan256_named(float v, float *warp_tot)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    sync256();
+    float off = 0.f;
+    for (int w = 0; w < warp; ++w) off += warp_tot[w];
+    sync256();  // warp_tot is reused by the next call
+    return v + off;
+}
+
+// Called by threads 0-255 only.
 __device__ __forceinline__ void seg_scan(const Problem &pr, const SegRegs &r, int h0, int nh, float scale, float *cs,
                                          float *dtv, float *warp_tot)
 {
@@ -141,14 +162,11 @@ __device__ __forceinline__ void seg_scan(const Problem &pr, const SegRegs &r, in
     for (int hh = 0; hh < 2; ++hh) {
         if (hh < nh) {  // block-uniform
             const float a = __ldg(pr.A + h0 + hh) * scale;
-            const float v = block_inclusive_scan_256(r.d[hh] * a, warp_tot);
-            if (t < 256) {  // a 288-thread block: its ninth warp holds no token
-                cs[hh * 256 + t] = v;
-                dtv[hh * 256 + t] = pr.dtin ? r.din[hh] : r.d[hh];
-            }
+            cs[hh * 256 + t] = scan256_named(r.d[hh] * a, warp_tot);
+            dtv[hh * 256 + t] = pr.dtin ? r.din[hh] : r.d[hh];
         }
     }
-    __syncthreads();
+    sync256();
 }
 
 // Pack 8 floats into 8 bf16 (one 16-byte chunk).
@@ -332,10 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the masked S tiles (hi and lo terms) the next 128 KiB.
 __host__ __device__ constexpr int stage_bytes(int jmax) { return jmax > 128 ? 80 * 1024 : 64 * 1024; }
 
-// chunk_out_tc: warps w and w + 4 (w < 4) share TMEM lanes 32 w .. 32 w + 31 and build S
-// and the epilogue; warp 8 issues the MMAs of the S products, so that no building warp
-// waits for an MMA issue
-constexpr int kOutThreads = 288;
+// chunk_out_tc: warps w and w + 4 (w < 4) share TMEM lanes 32 w .. 32 w + 31, scan the
+// decays while the slices are multiplied, then build S and run the epilogue; warp 8 issues
+// every MMA and warp 9 every load of the slices, so that no building warp waits on either
+constexpr int kOutThreads = 320;
 
 template <int NS>
 __global__ void __launch_bounds__(kOutThreads, 1)
@@ -346,10 +364,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_tma[2], bar_mma[2], bar_x, bar_mm2[2], bar_built[2];
     __shared__ uint32_t tmem_slot;
-    __shared__ float warp_tot[9];
+    __shared__ float warp_tot[8];
     __shared__ __align__(16) float cs[2 * 256];
     __shared__ __align__(16) float dtv[2 * 256];  // read as float4 in phase 2
-    __shared__ float s_mn[2][9], s_mx[2][9];
+    __shared__ float s_mn[2][8], s_mx[2][8];
     __shared__ int s_fail;
 
     const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
@@ -423,7 +441,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 tma_load_3d(xs + k * jn * 128 + r * kBoxBytes, &xmap, &bar_x, hb * 128 + 64 * k, t0 + r * kBoxRows,
                             b);
     };
-    if (warp == 1 && lane == 0) {
+    if (warp == 9 && lane == 0) {
         tma_prefetch_desc(&smap);
         tma_prefetch_desc(&cmap);
         tma_prefetch_desc(&bmap);
@@ -438,13 +456,64 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             bulk_prefetch_l2(ws.states + state_slot(pr, ref, h0 + hh) * (size_t)P * NS, (uint32_t)(P * NS * sizeof(float)));
         tma_prefetch_desc(&xmap);
     }
-    // dt of this thread's token, read now and scanned after the slices
-    const SegRegs seg = seg_load(pr, b, h0, HB, t0, len);
-
     // ---- phase 1: G = C_i B^T and Yoff = C_i (h_hi + h_lo)^T over the 64-wide slices of
     // the state dimension, two stages in flight: slice s + 1 lands while slice s is
-    // multiplied.  The other warps wait for the last slice's MMAs below.
-    if (warp == 0) {
+    // multiplied.  Meanwhile warps 0-7 scan the decays.
+    constexpr float kFactorSpan = 160.f;  // log2 units (see below)
+    float rowf[2] = {1.f, 1.f};
+    bool factored = false;
+    if (warp < 8) {
+        const SegRegs seg = seg_load(pr, b, h0, HB, t0, len);
+        seg_scan(pr, seg, h0, HB, kLog2e, cs, dtv, warp_tot);  // log2 domain: decays via ex2
+
+        // The decays exp2(cs_i - cs_j) in rank-one form, exp2(cs_i - ref) exp2(ref - cs_j)
+        // with ref the midpoint of each head's cs range over the chunk, whenever that range is
+        // at most kFactorSpan (every factor then within 2^(+-kFactorSpan / 2) of 1): one exp
+        // per row and per column instead of one per element of S.  The column factors, times
+        // dt_j, replace dtv and go into S; the row factor multiplies row i of S x in the
+        // epilogue.  A wider range keeps the exp per element (and a row factor of 1).
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const bool on = hh < HB && tid < len;
+            const float cv = cs[hh * 256 + tid];
+            float mn = on ? cv : 3.0e38f, mx = on ? cv : -3.0e38f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
+            if (lane == 0) {
+                s_mn[hh][warp] = mn;
+                s_mx[hh][warp] = mx;
+            }
+        }
+        sync256();
+        float ref[2];
+        factored = true;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float mn = s_mn[hh][0], mx = s_mx[hh][0];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) {
+                mn = fminf(mn, s_mn[hh][w]);
+                mx = fmaxf(mx, s_mx[hh][w]);
+            }
+            ref[hh] = 0.5f * (mn + mx);
+            if (hh < HB && !(mx - mn <= kFactorSpan)) factored = false;  // uniform over warps 0-7
+        }
+        if (factored) {
+            const int ir = i0 + (warp & 3) * 32 + lane;  // this thread's accumulator row in phase 2
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                if (hh < HB) {
+                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(rowf[hh]) : "f"(cs[hh * 256 + (ir < 256 ? ir : 255)] - ref[hh]));
+                    float c;
+                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(c) : "f"(ref[hh] - cs[hh * 256 + tid]));
+                    dtv[hh * 256 + tid] = tid < len ? c * dtv[hh * 256 + tid] : 0.f;
+                }
+            }
+        }
+    } else if (warp == 8) {
         if (lane == 0) {
             bool good = true;
             for (int s = 0; s < nsl && good; ++s) {
@@ -470,7 +539,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             if (!good) s_fail = 1;
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else {  // warp 9
         if (lane == 0) {
             // the other stage is free once slice s - 1's MMAs are done: slice s + 1 goes
             // there, or, after the last slice, the x tile (stage 0)
@@ -492,64 +561,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     // every slice's MMAs done (the last commit covers all earlier MMAs of this thread)
     if (!mbar_wait(bar_of(bar_mma, nsl - 1), ((nsl - 1) >> 1) & 1)) s_fail = 1;
     tc_fence_after();
-    seg_scan(pr, seg, h0, HB, kLog2e, cs, dtv, warp_tot);  // log2 domain: decays via ex2; ends in a barrier
+    __syncthreads();  // also publishes cs and the column factors
     bool ok = !s_fail;
-
-    // The decays exp2(cs_i - cs_j) in rank-one form, exp2(cs_i - ref) exp2(ref - cs_j) with
-    // ref the midpoint of each head's cs range over the chunk, whenever that range is at most
-    // kFactorSpan (every factor then within 2^(+-kFactorSpan / 2) of 1): one exp per row and
-    // per column instead of one per element of S.  The column factors, times dt_j, replace
-    // dtv and go into S; the row factor multiplies row i of S x in the epilogue.  A wider
-    // range keeps the exp per element (and a row factor of 1).
-    constexpr float kFactorSpan = 160.f;  // log2 units
-    float rowf[2] = {1.f, 1.f};
-    bool factored;
-    {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const bool on = hh < HB && tid < len;
-            const float cv = cs[hh * 256 + (tid & 255)];
-            float mn = on ? cv : 3.0e38f, mx = on ? cv : -3.0e38f;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            }
-            if (lane == 0) {
-                s_mn[hh][warp] = mn;
-                s_mx[hh][warp] = mx;
-            }
-        }
-        __syncthreads();
-        float ref[2];
-        factored = true;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float mn = s_mn[hh][0], mx = s_mx[hh][0];
-#pragma unroll
-            for (int w = 1; w < 8; ++w) {
-                mn = fminf(mn, s_mn[hh][w]);
-                mx = fmaxf(mx, s_mx[hh][w]);
-            }
-            ref[hh] = 0.5f * (mn + mx);
-            if (hh < HB && !(mx - mn <= kFactorSpan)) factored = false;  // block-uniform
-        }
-        if (factored) {
-            const int ir = i0 + (warp & 3) * 32 + lane;  // this thread's accumulator row in phase 2
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                if (hh < HB) {
-                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(rowf[hh]) : "f"(cs[hh * 256 + (ir < 256 ? ir : 255)] - ref[hh]));
-                    if (tid < 256) {  // the ninth warp holds no column
-                        float c;
-                        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(c) : "f"(ref[hh] - cs[hh * 256 + tid]));
-                        dtv[hh * 256 + tid] = tid < len ? c * dtv[hh * 256 + tid] : 0.f;
-                    }
-                }
-            }
-        }
-        __syncthreads();
-    }
 
     // ---- phase 2: S_h = G o decay o dt (causal) as hi + lo bf16 terms (a single rounding of
     // S costs up to 2^-9 |y_i| where one term dominates a row, i.e. under strong decay, when
@@ -643,7 +656,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
             fence_async_smem();  // the S chunk, written here, is read by the tensor cores
             mbar_arrive(&bar_built[kc & 1]);
         }
-    } else if (lane == 0) {  // warp 8: the MMAs of each S chunk once every building thread has arrived
+    } else if (warp == 8 && lane == 0) {  // the MMAs of each S chunk once every building thread has arrived
         bool good = true;
         for (int kc = 0; kc < nkc && good; ++kc) {
             const int hh = kc / nhalf, jh = kc % nhalf;
