@@ -70,7 +70,7 @@ size_t workspace_bytes(const Problem &pr)
     if (choose_path(pr) == SSD_PATH_TCGEN05_FUSED) return fused_workspace_bytes(pr);
     const size_t units = state_units(pr);
     return align_up(units * pr.headdim * pr.dstate * sizeof(float), 256) +
-           align_up(units * sizeof(float), 256);
+           align_up(units * sizeof(float), 256) + 256;  // ..., the tile ticket
 }
 
 Workspace carve_workspace(const Problem &pr, void *base)
@@ -80,6 +80,7 @@ Workspace carve_workspace(const Problem &pr, void *base)
     ws.states = static_cast<float *>(base);
     ws.decay = reinterpret_cast<float *>(static_cast<char *>(base) +
                                          align_up(units * pr.headdim * pr.dstate * sizeof(float), 256));
+    ws.ticket = reinterpret_cast<uint32_t *>(reinterpret_cast<char *>(ws.decay) + align_up(units * sizeof(float), 256));
     return ws;
 }
 

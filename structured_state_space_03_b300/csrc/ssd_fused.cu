@@ -258,6 +258,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(bs + s * kSlab, &bmap, &bar_ld, g * NS + 64 * s, tt, tb);
             tma_load_3d(cm + s * kSlab, &cmap, &bar_ld, g * NS + 64 * s, tt, tb);
         }
+        // the predecessor's inclusive state (or the init state) into L2 ahead of the look-back:
+        // with many units per chain position, the predecessor finished long ago and its
+        // state (written back from L2 since) would otherwise come from DRAM
+        if (c > 0)
+            bulk_prefetch_l2(fa.incl + (unit - 1) * (size_t)kRows * NS, (uint32_t)(kRows * NS * sizeof(float)));
+        else if (pr.init_state)
+            bulk_prefetch_l2(pr.init_state + ((size_t)b * H + h0) * P * NS, (uint32_t)(kRows * NS * sizeof(float)));
     }
 
     // ---- segment sums, span, reference, factors: warps 0-3 head 0, warps 4-7 head 1

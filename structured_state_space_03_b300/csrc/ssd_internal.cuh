@@ -83,6 +83,7 @@ struct Workspace {
     float *states;  // [batch][nheads][nchunks][headdim][dstate]: S_c, then h_c in place (fp32, or
                     // bf16 hi / lo per 64-wide slice on the tcgen05 path: launch_state_pass)
     float *decay;   // [batch][nheads][nchunks]: exp(cs_last) of each chunk
+    uint32_t *ticket = nullptr;  // tile ticket of the persistent chunk_out_tc (zeroed per launch)
 };
 // (The packed layout uses [1][nheads][total_chunks] in the sequence-major chunk
 // numbering instead of [batch][nheads][nchunks].)

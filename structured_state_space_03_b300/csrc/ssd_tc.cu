@@ -368,18 +368,13 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     __shared__ __align__(16) float cs[2 * 256];
     __shared__ __align__(16) float dtv[2 * 256];  // read as float4 in phase 2
     __shared__ float s_mn[2][8], s_mx[2][8];
-    __shared__ int s_fail;
+    __shared__ int s_fail, s_tile;
 
     const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
-    const int it = blockIdx.x % ntile, hb = blockIdx.y;
-    const ChunkRef ref = chunk_ref(pr, blockIdx.x / ntile, blockIdx.z);
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
-    const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
-    const int b = ref.tb, t0 = ref.t0, len = ref.len;  // b: batch row of the token tensors
-    const int i0 = it * kBoxRows;
-    if (i0 >= len) return;  // tile beyond the end of a partial last chunk (block-uniform)
-    const int jn = i0 + kBoxRows;                 // columns j in [0, jn)
-    const int nbj = jn / kBoxRows;                // 128-row boxes along j
+    const int nhb = H / HB;
+    const int ncx = pr.chunks ? pr.total_chunks : pr.nchunks;
+    const int ntiles = nhb * ntile * ncx * (pr.chunks ? 1 : pr.batch);
     // TMEM: G (jn columns), Ydiag and Yoff (128 each); one CTA per SM (its shared memory)
     const uint32_t tcols = 512;
     const uint32_t col_g = 0, col_yd = 256, col_yo = 384;
@@ -416,337 +411,380 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
-    // TMA issue: lane 0 of warp 1, so that lane 0 of warp 0 only waits for operands and
-    // issues MMAs.  A stage takes slice sl of C_i and B_j and of each head's entry state
-    // h_c, whose hi and lo bf16 terms the state pass laid out per slice (a [P][64] box of
-    // each at columns 128 sl and 128 sl + 64 of the slot's [P][2 NS] bf16 rows).
-    auto issue_stage = [&](int sl) {
-        uint8_t *st = stage(sl);
-        uint64_t *bar = bar_of(bar_tma, sl);
-        mbar_expect_tx(bar, (uint32_t)((1 + nbj) * kBoxBytes + 2 * kBoxBytes));
-        tma_load_3d(st, &cmap, bar, g * NS + 64 * sl, t0 + i0, b);
-        for (int r = 0; r < nbj; ++r)
-            tma_load_3d(st + kBoxBytes + r * kBoxBytes, &bmap, bar, g * NS + 64 * sl, t0 + r * kBoxRows, b);
-        uint8_t *h_sl = st + kBoxBytes + jn * 128, *l_sl = h_sl + kBoxBytes;
-        for (int hh = 0; hh < HB; ++hh) {
-            const int row = (int)(state_slot(pr, ref, h0 + hh) * P);
-            tma_load_3d(h_sl + hh * P * 128, &smap, bar, 128 * sl, row, 0);
-            tma_load_3d(l_sl + hh * P * 128, &smap, bar, 128 * sl + 64, row, 0);
-        }
-    };
-    auto issue_x = [&]() {  // the x rows of the whole tile span, both 64-column blocks
-        mbar_expect_tx(&bar_x, (uint32_t)(2 * nbj * kBoxBytes));
-        for (int k = 0; k < 2; ++k)
-            for (int r = 0; r < nbj; ++r)
-                tma_load_3d(xs + k * jn * 128 + r * kBoxBytes, &xmap, &bar_x, hb * 128 + 64 * k, t0 + r * kBoxRows,
-                            b);
-    };
+    // Persistent: one CTA per SM takes tiles by ticket, head block fastest, so that the
+    // head blocks of one chunk tile follow each other and share C and B in L2.  Every
+    // mbarrier completes a known number of times per tile; the counts so far give the
+    // parity each wait needs.
     if (warp == 9 && lane == 0) {
         tma_prefetch_desc(&smap);
         tma_prefetch_desc(&cmap);
         tma_prefetch_desc(&bmap);
-        issue_stage(0);
-        if (nsl > 1)
-            issue_stage(1);
-        else
-            issue_x();  // stage 0 is not used by the one slice
-        // the rest of the chunk's entry states (one P x NS block of hi / lo pairs per head,
-        // from DRAM) into L2, so that the later slice loads find them there
-        for (int hh = 0; hh < HB; ++hh)
-            bulk_prefetch_l2(ws.states + state_slot(pr, ref, h0 + hh) * (size_t)P * NS, (uint32_t)(P * NS * sizeof(float)));
         tma_prefetch_desc(&xmap);
+        tma_prefetch_desc(&ymap);
     }
-    // ---- phase 1: G = C_i B^T and Yoff = C_i (h_hi + h_lo)^T over the 64-wide slices of
-    // the state dimension, two stages in flight: slice s + 1 lands while slice s is
-    // multiplied.  Meanwhile warps 0-7 scan the decays.
-    constexpr float kFactorSpan = 160.f;  // log2 units (see below)
-    float rowf[2] = {1.f, 1.f};
-    bool factored = false;
-    if (warp < 8) {
-        const SegRegs seg = seg_load(pr, b, h0, HB, t0, len);
-        seg_scan(pr, seg, h0, HB, kLog2e, cs, dtv, warp_tot);  // log2 domain: decays via ex2
+    uint32_t n_st0 = 0, n_st1 = 0, n_x = 0, n_s0 = 0, n_s1 = 0;
+    for (;;) {
+        tc_fence_before();
+        __syncthreads();  // the previous tile is done with TMEM and shared memory
+        if (tid == 0) s_tile = (int)atomicAdd(ws.ticket, 1u);
+        __syncthreads();
+        tc_fence_after();
+        const int tk = s_tile;
+        if (tk >= ntiles || s_fail) break;  // block-uniform
+        const int hb = tk % nhb, it = (tk / nhb) % ntile, cxz = tk / (nhb * ntile);
+        const ChunkRef ref = chunk_ref(pr, cxz % ncx, cxz / ncx);
+        const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
+        const int b = ref.tb, t0 = ref.t0, len = ref.len;  // b: batch row of the token tensors
+        const int i0 = it * kBoxRows;
+        if (i0 >= len) continue;  // tile beyond the end of a partial last chunk (block-uniform)
+        const int jn = i0 + kBoxRows;                 // columns j in [0, jn)
+        const int nbj = jn / kBoxRows;                // 128-row boxes along j
+        // parity of the wait for slice s on its stage's barriers, for S chunk kc on its buffer's
+        auto par_s = [&](int sl) { return (((sl + nsl) & 1 ? n_st1 : n_st0) + (uint32_t)(sl >> 1)) & 1u; };
+        auto par_k = [&](int kc) { return ((kc & 1 ? n_s1 : n_s0) + (uint32_t)(kc >> 1)) & 1u; };
 
-        // The decays exp2(cs_i - cs_j) in rank-one form, exp2(cs_i - ref) exp2(ref - cs_j)
-        // with ref the midpoint of each head's cs range over the chunk, whenever that range is
-        // at most kFactorSpan (every factor then within 2^(+-kFactorSpan / 2) of 1): one exp
-        // per row and per column instead of one per element of S.  The column factors, times
-        // dt_j, replace dtv and go into S; the row factor multiplies row i of S x in the
-        // epilogue.  A wider range keeps the exp per element (and a row factor of 1).
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const bool on = hh < HB && tid < len;
-            const float cv = cs[hh * 256 + tid];
-            float mn = on ? cv : 3.0e38f, mx = on ? cv : -3.0e38f;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        // TMA issue: lane 0 of warp 1, so that lane 0 of warp 0 only waits for operands and
+        // issues MMAs.  A stage takes slice sl of C_i and B_j and of each head's entry state
+        // h_c, whose hi and lo bf16 terms the state pass laid out per slice (a [P][64] box of
+        // each at columns 128 sl and 128 sl + 64 of the slot's [P][2 NS] bf16 rows).
+        auto issue_stage = [&](int sl) {
+            uint8_t *st = stage(sl);
+            uint64_t *bar = bar_of(bar_tma, sl);
+            mbar_expect_tx(bar, (uint32_t)((1 + nbj) * kBoxBytes + 2 * kBoxBytes));
+            tma_load_3d(st, &cmap, bar, g * NS + 64 * sl, t0 + i0, b);
+            for (int r = 0; r < nbj; ++r)
+                tma_load_3d(st + kBoxBytes + r * kBoxBytes, &bmap, bar, g * NS + 64 * sl, t0 + r * kBoxRows, b);
+            uint8_t *h_sl = st + kBoxBytes + jn * 128, *l_sl = h_sl + kBoxBytes;
+            for (int hh = 0; hh < HB; ++hh) {
+                const int row = (int)(state_slot(pr, ref, h0 + hh) * P);
+                tma_load_3d(h_sl + hh * P * 128, &smap, bar, 128 * sl, row, 0);
+                tma_load_3d(l_sl + hh * P * 128, &smap, bar, 128 * sl + 64, row, 0);
             }
-            if (lane == 0) {
-                s_mn[hh][warp] = mn;
-                s_mx[hh][warp] = mx;
-            }
+        };
+        auto issue_x = [&]() {  // the x rows of the whole tile span, both 64-column blocks
+            mbar_expect_tx(&bar_x, (uint32_t)(2 * nbj * kBoxBytes));
+            for (int k = 0; k < 2; ++k)
+                for (int r = 0; r < nbj; ++r)
+                    tma_load_3d(xs + k * jn * 128 + r * kBoxBytes, &xmap, &bar_x, hb * 128 + 64 * k, t0 + r * kBoxRows,
+                                b);
+        };
+        if (warp == 9 && lane == 0) {
+            issue_stage(0);
+            if (nsl > 1)
+                issue_stage(1);
+            else
+                issue_x();  // stage 0 is not used by the one slice
+            // the rest of the chunk's entry states (one P x NS block of hi / lo pairs per head,
+            // from DRAM) into L2, so that the later slice loads find them there
+            for (int hh = 0; hh < HB; ++hh)
+                bulk_prefetch_l2(ws.states + state_slot(pr, ref, h0 + hh) * (size_t)P * NS, (uint32_t)(P * NS * sizeof(float)));
         }
-        sync256();
-        float ref[2];
-        factored = true;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float mn = s_mn[hh][0], mx = s_mx[hh][0];
-#pragma unroll
-            for (int w = 1; w < 8; ++w) {
-                mn = fminf(mn, s_mn[hh][w]);
-                mx = fmaxf(mx, s_mx[hh][w]);
-            }
-            ref[hh] = 0.5f * (mn + mx);
-            if (hh < HB && !(mx - mn <= kFactorSpan)) factored = false;  // uniform over warps 0-7
-        }
-        if (factored) {
-            const int ir = i0 + (warp & 3) * 32 + lane;  // this thread's accumulator row in phase 2
+        // ---- phase 1: G = C_i B^T and Yoff = C_i (h_hi + h_lo)^T over the 64-wide slices of
+        // the state dimension, two stages in flight: slice s + 1 lands while slice s is
+        // multiplied.  Meanwhile warps 0-7 scan the decays.
+        constexpr float kFactorSpan = 160.f;  // log2 units (see below)
+        float rowf[2] = {1.f, 1.f};
+        bool factored = false;
+        if (warp < 8) {
+            const SegRegs seg = seg_load(pr, b, h0, HB, t0, len);
+            seg_scan(pr, seg, h0, HB, kLog2e, cs, dtv, warp_tot);  // log2 domain: decays via ex2
+
+            // The decays exp2(cs_i - cs_j) in rank-one form, exp2(cs_i - ref) exp2(ref - cs_j)
+            // with ref the midpoint of each head's cs range over the chunk, whenever that range is
+            // at most kFactorSpan (every factor then within 2^(+-kFactorSpan / 2) of 1): one exp
+            // per row and per column instead of one per element of S.  The column factors, times
+            // dt_j, replace dtv and go into S; the row factor multiplies row i of S x in the
+            // epilogue.  A wider range keeps the exp per element (and a row factor of 1).
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                if (hh < HB) {
-                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(rowf[hh]) : "f"(cs[hh * 256 + (ir < 256 ? ir : 255)] - ref[hh]));
-                    float c;
-                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(c) : "f"(ref[hh] - cs[hh * 256 + tid]));
-                    dtv[hh * 256 + tid] = tid < len ? c * dtv[hh * 256 + tid] : 0.f;
+                const bool on = hh < HB && tid < len;
+                const float cv = cs[hh * 256 + tid];
+                float mn = on ? cv : 3.0e38f, mx = on ? cv : -3.0e38f;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                }
+                if (lane == 0) {
+                    s_mn[hh][warp] = mn;
+                    s_mx[hh][warp] = mx;
                 }
             }
+            sync256();
+            float ref[2];
+            factored = true;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float mn = s_mn[hh][0], mx = s_mx[hh][0];
+#pragma unroll
+                for (int w = 1; w < 8; ++w) {
+                    mn = fminf(mn, s_mn[hh][w]);
+                    mx = fmaxf(mx, s_mx[hh][w]);
+                }
+                ref[hh] = 0.5f * (mn + mx);
+                if (hh < HB && !(mx - mn <= kFactorSpan)) factored = false;  // uniform over warps 0-7
+            }
+            if (factored) {
+                const int ir = i0 + (warp & 3) * 32 + lane;  // this thread's accumulator row in phase 2
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (hh < HB) {
+                        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(rowf[hh]) : "f"(cs[hh * 256 + (ir < 256 ? ir : 255)] - ref[hh]));
+                        float c;
+                        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(c) : "f"(ref[hh] - cs[hh * 256 + tid]));
+                        dtv[hh * 256 + tid] = tid < len ? c * dtv[hh * 256 + tid] : 0.f;
+                    }
+                }
+            }
+        } else if (warp == 8) {
+            if (lane == 0) {
+                bool good = true;
+                for (int s = 0; s < nsl && good; ++s) {
+                    uint8_t *c_sl = stage(s), *b_sl = c_sl + kBoxBytes, *h_sl = b_sl + jn * 128, *l_sl = h_sl + kBoxBytes;
+                    if (!mbar_wait(bar_of(bar_tma, s), par_s(s))) {
+                        good = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t id_g = idesc_bf16(128, jn, 0, 0);
+                    constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = sdesc_sw128(smem_u32(c_sl) + kk * 32, 16, 1024);
+                        mma_bf16(tmem + col_g, ad, sdesc_sw128(smem_u32(b_sl) + kk * 32, 16, 1024), id_g,
+                                 (s | kk) != 0);
+                        mma_bf16(tmem + col_yo, ad, sdesc_sw128(smem_u32(h_sl) + kk * 32, 16, 1024), id_o,
+                                 (s | kk) != 0);
+                        mma_bf16(tmem + col_yo, ad, sdesc_sw128(smem_u32(l_sl) + kk * 32, 16, 1024), id_o, 1);
+                    }
+                    mma_commit(bar_of(bar_mma, s));
+                }
+                if (!good) s_fail = 1;
+            }
+            __syncwarp();
+        } else {  // warp 9
+            if (lane == 0) {
+                // the other stage is free once slice s - 1's MMAs are done: slice s + 1 goes
+                // there, or, after the last slice, the x tile (stage 0)
+                bool good = true;
+                for (int s = 1; s < nsl && good; ++s) {
+                    if (!mbar_wait(bar_of(bar_mma, s - 1), par_s(s - 1))) {
+                        good = false;
+                        break;
+                    }
+                    if (s + 1 < nsl)
+                        issue_stage(s + 1);
+                    else
+                        issue_x();
+                }
+                if (!good) s_fail = 1;
+            }
+            __syncwarp();
         }
-    } else if (warp == 8) {
-        if (lane == 0) {
+        // every slice's MMAs done (the last commit covers all earlier MMAs of warp 8).  Warp 8
+        // alone waits: it has seen slice nsl - 3's MMAs complete, so the parity wait cannot
+        // mistake the barrier's previous phase for this one; the others learn it at the barrier.
+        if (warp == 8 && !mbar_wait(bar_of(bar_mma, nsl - 1), par_s(nsl - 1))) s_fail = 1;
+        __syncthreads();  // also publishes cs and the column factors
+        tc_fence_after();
+        bool ok = !s_fail;
+
+        // ---- phase 2: S_h = G o decay o dt (causal) as hi + lo bf16 terms (a single rounding of
+        // S costs up to 2^-9 |y_i| where one term dominates a row, i.e. under strong decay, when
+        // |y| reaches ~10x its RMS); Ydiag_h = S_hi x_h + S_lo x_h.  S goes in K-chunks of 128
+        // columns (head-major), double-buffered in 64 KiB (hi, then lo): chunk k + 1 is built
+        // while chunk k is multiplied.
+        const int i = quarter * 32 + lane;    // accumulator row of this thread
+        const int ia = i0 + i;                // row within the chunk
+        const bool row_ok = ia < len;
+        const int nhalf = jn / 128;           // K-chunks per head
+        const int nkc = ok ? HB * nhalf : 0;  // block-uniform
+        if (warp < 8) {
+            for (int kc = 0; kc < nkc; ++kc) {
+                const int hh = kc / nhalf, jh = kc % nhalf;
+                uint8_t *buf = r1 + (kc & 1) * 65536;
+                // the buffer was last read by the MMAs of chunk kc - 2
+                if (kc >= 2 && !mbar_wait(&bar_mm2[kc & 1], par_k(kc - 2))) s_fail = 1;
+                const float *csh = cs + hh * 256, *dth = dtv + hh * 256;
+                const float ci = csh[ia < 256 ? ia : 255];
+                for (int lb = half; lb < 4; lb += 2) {  // 32-column blocks lb of the chunk: warps 0-3 even, 4-7 odd
+                    const int j0 = 128 * jh + 32 * lb;
+                    uint8_t *st = buf + (lb / 2) * kBoxBytes;
+                    const int cq = (lb & 1) * 4;          // first 16-byte column of the block in its 64-column box
+                    if (j0 > i0 + quarter * 32 + 31) {  // whole warp above the diagonal: zeros
+                        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            *reinterpret_cast<uint4 *>(st + sw128(i, cq + u)) = z;
+                            *reinterpret_cast<uint4 *>(st + 32768 + sw128(i, cq + u)) = z;
+                        }
+                        continue;
+                    }
+                    float gv[32];
+                    tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col_g + j0, gv);
+                    // cs and dt (or the column factors) of the block's 32 columns as float4s
+                    float sv[32];
+                    // every row of the warp in the chunk and past the block's last column: no mask
+                    const bool full = j0 + 31 <= i0 + quarter * 32 && i0 + quarter * 32 + 31 < len;
+                    if (factored && full) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 f4 = reinterpret_cast<const float4 *>(dth + j0)[q];
+                            sv[4 * q] = gv[4 * q] * f4.x;
+                            sv[4 * q + 1] = gv[4 * q + 1] * f4.y;
+                            sv[4 * q + 2] = gv[4 * q + 2] * f4.z;
+                            sv[4 * q + 3] = gv[4 * q + 3] * f4.w;
+                        }
+                    } else if (factored) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 f4 = reinterpret_cast<const float4 *>(dth + j0)[q];
+                            const float fj[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                const int k = 4 * q + v, j = j0 + k;
+                                // masked entries (j > row) are discarded, whatever the product is
+                                sv[k] = (row_ok && j <= ia) ? gv[k] * fj[v] : 0.f;
+                            }
+                        }
+                    } else {
+                        // the decays by the hardware base-2 exponential (ex2.approx, relative error ~2^-22)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 c4 = reinterpret_cast<const float4 *>(csh + j0)[q];
+                            const float4 d4 = reinterpret_cast<const float4 *>(dth + j0)[q];
+                            const float cj[4] = {c4.x, c4.y, c4.z, c4.w}, dj[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                const int k = 4 * q + v, j = j0 + k;
+                                float e;  // masked entries (j > row) are discarded below, whatever e is
+                                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(ci - cj[v]));
+                                sv[k] = (row_ok && j <= ia) ? gv[k] * e * dj[v] : 0.f;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint4 hi = pack8(sv + 8 * u);
+                        const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
+                        float r[8];
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            const float2 t = __bfloat1622float2(h2[e2]);
+                            r[2 * e2] = sv[8 * u + 2 * e2] - t.x;
+                            r[2 * e2 + 1] = sv[8 * u + 2 * e2 + 1] - t.y;
+                        }
+                        *reinterpret_cast<uint4 *>(st + sw128(i, cq + u)) = hi;
+                        *reinterpret_cast<uint4 *>(st + 32768 + sw128(i, cq + u)) = pack8(r);
+                    }
+                }
+                fence_async_smem();  // the S chunk, written here, is read by the tensor cores
+                mbar_arrive(&bar_built[kc & 1]);
+            }
+        } else if (warp == 8 && lane == 0) {  // the MMAs of each S chunk once every building thread has arrived
             bool good = true;
-            for (int s = 0; s < nsl && good; ++s) {
-                uint8_t *c_sl = stage(s), *b_sl = c_sl + kBoxBytes, *h_sl = b_sl + jn * 128, *l_sl = h_sl + kBoxBytes;
-                if (!mbar_wait(bar_of(bar_tma, s), (s >> 1) & 1)) {
+            for (int kc = 0; kc < nkc && good; ++kc) {
+                const int hh = kc / nhalf, jh = kc % nhalf;
+                if (!mbar_wait(&bar_built[kc & 1], par_k(kc)) || (kc == 0 && !mbar_wait(&bar_x, n_x & 1u))) {
                     good = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t id_g = idesc_bf16(128, jn, 0, 0);
-                constexpr uint32_t id_o = idesc_bf16(128, 128, 0, 0);
+                const uint32_t id_d = idesc_bf16(128, P, 0, 1);  // one head's headdim columns
+                const uint32_t s_addr = smem_u32(r1 + (kc & 1) * 65536);
+                const uint32_t x_addr = smem_u32(xs) + (P == 64 ? hh : 0) * jn * 128;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = sdesc_sw128(smem_u32(c_sl) + kk * 32, 16, 1024);
-                    mma_bf16(tmem + col_g, ad, sdesc_sw128(smem_u32(b_sl) + kk * 32, 16, 1024), id_g,
-                             (s | kk) != 0);
-                    mma_bf16(tmem + col_yo, ad, sdesc_sw128(smem_u32(h_sl) + kk * 32, 16, 1024), id_o,
-                             (s | kk) != 0);
-                    mma_bf16(tmem + col_yo, ad, sdesc_sw128(smem_u32(l_sl) + kk * 32, 16, 1024), id_o, 1);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t so = (ks / 4) * kBoxBytes + (ks % 4) * 32;
+                    const uint64_t bd = sdesc_sw128(x_addr + (8 * jh + ks) * 2048, jn * 128, 1024);
+                    mma_bf16(tmem + col_yd + hh * P, sdesc_sw128(s_addr + so, 16, 1024), bd, id_d, (jh | ks) != 0);
+                    mma_bf16(tmem + col_yd + hh * P, sdesc_sw128(s_addr + 32768 + so, 16, 1024), bd, id_d, 1);
                 }
-                mma_commit(bar_of(bar_mma, s));
+                mma_commit(&bar_mm2[kc & 1]);
             }
             if (!good) s_fail = 1;
         }
         __syncwarp();
-    } else {  // warp 9
-        if (lane == 0) {
-            // the other stage is free once slice s - 1's MMAs are done: slice s + 1 goes
-            // there, or, after the last slice, the x tile (stage 0)
-            bool good = true;
-            for (int s = 1; s < nsl && good; ++s) {
-                if (!mbar_wait(bar_of(bar_mma, s - 1), ((s - 1) >> 1) & 1)) {
-                    good = false;
-                    break;
-                }
-                if (s + 1 < nsl)
-                    issue_stage(s + 1);
-                else
-                    issue_x();
-            }
-            if (!good) s_fail = 1;
-        }
-        __syncwarp();
-    }
-    // every slice's MMAs done (the last commit covers all earlier MMAs of this thread)
-    if (!mbar_wait(bar_of(bar_mma, nsl - 1), ((nsl - 1) >> 1) & 1)) s_fail = 1;
-    tc_fence_after();
-    __syncthreads();  // also publishes cs and the column factors
-    bool ok = !s_fail;
-
-    // ---- phase 2: S_h = G o decay o dt (causal) as hi + lo bf16 terms (a single rounding of
-    // S costs up to 2^-9 |y_i| where one term dominates a row, i.e. under strong decay, when
-    // |y| reaches ~10x its RMS); Ydiag_h = S_hi x_h + S_lo x_h.  S goes in K-chunks of 128
-    // columns (head-major), double-buffered in 64 KiB (hi, then lo): chunk k + 1 is built
-    // while chunk k is multiplied.
-    const int i = quarter * 32 + lane;    // accumulator row of this thread
-    const int ia = i0 + i;                // row within the chunk
-    const bool row_ok = ia < len;
-    const int nhalf = jn / 128;           // K-chunks per head
-    const int nkc = ok ? HB * nhalf : 0;  // block-uniform
-    if (warp < 8) {
-        for (int kc = 0; kc < nkc; ++kc) {
-            const int hh = kc / nhalf, jh = kc % nhalf;
-            uint8_t *buf = r1 + (kc & 1) * 65536;
-            // the buffer was last read by the MMAs of chunk kc - 2
-            if (kc >= 2 && !mbar_wait(&bar_mm2[kc & 1], ((kc - 2) >> 1) & 1)) s_fail = 1;
-            const float *csh = cs + hh * 256, *dth = dtv + hh * 256;
-            const float ci = csh[ia < 256 ? ia : 255];
-            for (int lb = half; lb < 4; lb += 2) {  // 32-column blocks lb of the chunk: warps 0-3 even, 4-7 odd
-                const int j0 = 128 * jh + 32 * lb;
-                uint8_t *st = buf + (lb / 2) * kBoxBytes;
-                const int cq = (lb & 1) * 4;          // first 16-byte column of the block in its 64-column box
-                if (j0 > i0 + quarter * 32 + 31) {  // whole warp above the diagonal: zeros
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        *reinterpret_cast<uint4 *>(st + sw128(i, cq + u)) = z;
-                        *reinterpret_cast<uint4 *>(st + 32768 + sw128(i, cq + u)) = z;
-                    }
-                    continue;
-                }
-                float gv[32];
-                tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col_g + j0, gv);
-                // cs and dt (or the column factors) of the block's 32 columns as float4s
-                float sv[32];
-                // every row of the warp in the chunk and past the block's last column: no mask
-                const bool full = j0 + 31 <= i0 + quarter * 32 && i0 + quarter * 32 + 31 < len;
-                if (factored && full) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 f4 = reinterpret_cast<const float4 *>(dth + j0)[q];
-                        sv[4 * q] = gv[4 * q] * f4.x;
-                        sv[4 * q + 1] = gv[4 * q + 1] * f4.y;
-                        sv[4 * q + 2] = gv[4 * q + 2] * f4.z;
-                        sv[4 * q + 3] = gv[4 * q + 3] * f4.w;
-                    }
-                } else if (factored) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 f4 = reinterpret_cast<const float4 *>(dth + j0)[q];
-                        const float fj[4] = {f4.x, f4.y, f4.z, f4.w};
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int k = 4 * q + v, j = j0 + k;
-                            // masked entries (j > row) are discarded, whatever the product is
-                            sv[k] = (row_ok && j <= ia) ? gv[k] * fj[v] : 0.f;
-                        }
-                    }
-                } else {
-                    // the decays by the hardware base-2 exponential (ex2.approx, relative error ~2^-22)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 c4 = reinterpret_cast<const float4 *>(csh + j0)[q];
-                        const float4 d4 = reinterpret_cast<const float4 *>(dth + j0)[q];
-                        const float cj[4] = {c4.x, c4.y, c4.z, c4.w}, dj[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int k = 4 * q + v, j = j0 + k;
-                            float e;  // masked entries (j > row) are discarded below, whatever e is
-                            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(ci - cj[v]));
-                            sv[k] = (row_ok && j <= ia) ? gv[k] * e * dj[v] : 0.f;
-                        }
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint4 hi = pack8(sv + 8 * u);
-                    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
-                    float r[8];
-#pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2) {
-                        const float2 t = __bfloat1622float2(h2[e2]);
-                        r[2 * e2] = sv[8 * u + 2 * e2] - t.x;
-                        r[2 * e2 + 1] = sv[8 * u + 2 * e2 + 1] - t.y;
-                    }
-                    *reinterpret_cast<uint4 *>(st + sw128(i, cq + u)) = hi;
-                    *reinterpret_cast<uint4 *>(st + 32768 + sw128(i, cq + u)) = pack8(r);
-                }
-            }
-            fence_async_smem();  // the S chunk, written here, is read by the tensor cores
-            mbar_arrive(&bar_built[kc & 1]);
-        }
-    } else if (warp == 8 && lane == 0) {  // the MMAs of each S chunk once every building thread has arrived
-        bool good = true;
-        for (int kc = 0; kc < nkc && good; ++kc) {
-            const int hh = kc / nhalf, jh = kc % nhalf;
-            if (!mbar_wait(&bar_built[kc & 1], (kc >> 1) & 1) || (kc == 0 && !mbar_wait(&bar_x, 0))) {
-                good = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t id_d = idesc_bf16(128, P, 0, 1);  // one head's headdim columns
-            const uint32_t s_addr = smem_u32(r1 + (kc & 1) * 65536);
-            const uint32_t x_addr = smem_u32(xs) + (P == 64 ? hh : 0) * jn * 128;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t so = (ks / 4) * kBoxBytes + (ks % 4) * 32;
-                const uint64_t bd = sdesc_sw128(x_addr + (8 * jh + ks) * 2048, jn * 128, 1024);
-                mma_bf16(tmem + col_yd + hh * P, sdesc_sw128(s_addr + so, 16, 1024), bd, id_d, (jh | ks) != 0);
-                mma_bf16(tmem + col_yd + hh * P, sdesc_sw128(s_addr + 32768 + so, 16, 1024), bd, id_d, 1);
-            }
-            mma_commit(&bar_mm2[kc & 1]);
-        }
-        if (!good) s_fail = 1;
-    }
-    __syncwarp();
-    // every chunk's MMAs done (the last commit covers the earlier ones)
-    if (nkc > 0 && !mbar_wait(&bar_mm2[(nkc - 1) & 1], ((nkc - 1) >> 1) & 1)) s_fail = 1;
-    __syncthreads();
-    ok = !s_fail;
-    tc_fence_after();
-
-    // ---- phase 3: y = Ydiag + exp(cs_i) Yoff + D x, staged over this tile's x rows and
-    // stored by TMA when the tile's 128 rows all belong to the chunk (the batch layout
-    // with chunks of 128 or 256 tokens; rows past the sequence end are clipped by the
-    // tensor map), else stored row by row
-    const bool tma_out = !pr.chunks && (pr.chunk == kBoxRows || pr.chunk == 2 * kBoxRows);
-    if (ok && !mbar_wait(&bar_x, 0)) ok = false;  // x tile (already complete) visible to every thread
-    if (ok && warp < 8) {
-        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        for (int hh = 0; hh < HB; ++hh) {
-            const int h = h0 + hh;
-            const float e = exp2f(cs[hh * 256 + (ia < 256 ? ia : 255)]);
-            const float rf = hh == 0 ? rowf[0] : rowf[1];  // 1 unless the decays are factored
-            const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
-            __nv_bfloat16 *yrow = static_cast<__nv_bfloat16 *>(pr.y) + (((size_t)b * L + t0 + ia) * H + h) * P;
-            for (int p0 = half * (P / 2); p0 < (half + 1) * (P / 2); p0 += 32) {
-                float yd[32], yo[32];
-                tmem_ld32(tmem + lane_base + col_yd + hh * P + p0, yd);
-                tmem_ld32(tmem + lane_base + col_yo + hh * P + p0, yo);
-                if (row_ok || tma_out) {
-                    const int col = hh * P + p0;            // column within the 128-wide x tile
-                    uint8_t *xrow = xs + (col / 64) * jn * 128;
-                    uint4 ov[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(xrow + sw128(ia, (col % 64) / 8 + u));
-                        const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-                        float out[8];
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const float2 xf = __bfloat1622float2(x2[v]);
-                            const int k = 8 * u + 2 * v;
-                            out[2 * v] = fmaf(rf, yd[k], fmaf(e, yo[k], Dh * xf.x));
-                            out[2 * v + 1] = fmaf(rf, yd[k + 1], fmaf(e, yo[k + 1], Dh * xf.y));
-                        }
-                        ov[u] = pack8(out);
-                    }
-                    if (tma_out) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            *reinterpret_cast<uint4 *>(xrow + sw128(ia, (col % 64) / 8 + u)) = ov[u];
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + p0);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) dst[u] = ov[u];
-                    }
-                }
-            }
-        }
-    } else if (!ok && tid == 0) {
-        set_error(pr, kDevErrTimeout);
-    }
-    if (tma_out) {
-        fence_async_smem();
+        // every chunk's MMAs done (the last commit covers the earlier ones); warps 0-8 have seen
+        // chunk nkc - 3's complete, warp 9 takes it from the barrier
+        if (nkc > 0 && warp < 9 && !mbar_wait(&bar_mm2[(nkc - 1) & 1], par_k(nkc - 1))) s_fail = 1;
         __syncthreads();
-        if (ok && tid == 0) {  // the tile's rows i0 .. i0 + 127 of both 64-column blocks
-            for (int k = 0; k < 2; ++k)
-                tma_store_3d(&ymap, xs + k * jn * 128 + i0 * 128, hb * 128 + 64 * k, t0 + i0, b);
-            bulk_commit();
-            bulk_wait_read_all();
+        ok = !s_fail;
+        tc_fence_after();
+
+        // ---- phase 3: y = Ydiag + exp(cs_i) Yoff + D x, staged over this tile's x rows and
+        // stored by TMA when the tile's 128 rows all belong to the chunk (the batch layout
+        // with chunks of 128 or 256 tokens; rows past the sequence end are clipped by the
+        // tensor map), else stored row by row
+        const bool tma_out = !pr.chunks && (pr.chunk == kBoxRows || pr.chunk == 2 * kBoxRows);
+        if (ok && !mbar_wait(&bar_x, n_x & 1u)) ok = false;  // x tile (already complete) visible to every thread
+        if (ok && warp < 8) {
+            const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+            for (int hh = 0; hh < HB; ++hh) {
+                const int h = h0 + hh;
+                const float e = exp2f(cs[hh * 256 + (ia < 256 ? ia : 255)]);
+                const float rf = hh == 0 ? rowf[0] : rowf[1];  // 1 unless the decays are factored
+                const float Dh = pr.D ? __ldg(pr.D + h) : 0.f;
+                __nv_bfloat16 *yrow = static_cast<__nv_bfloat16 *>(pr.y) + (((size_t)b * L + t0 + ia) * H + h) * P;
+                for (int p0 = half * (P / 2); p0 < (half + 1) * (P / 2); p0 += 32) {
+                    float yd[32], yo[32];
+                    tmem_ld32(tmem + lane_base + col_yd + hh * P + p0, yd);
+                    tmem_ld32(tmem + lane_base + col_yo + hh * P + p0, yo);
+                    if (row_ok || tma_out) {
+                        const int col = hh * P + p0;            // column within the 128-wide x tile
+                        uint8_t *xrow = xs + (col / 64) * jn * 128;
+                        uint4 ov[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint4 xv = *reinterpret_cast<const uint4 *>(xrow + sw128(ia, (col % 64) / 8 + u));
+                            const __nv_bfloat162 *x2 = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                            float out[8];
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                const float2 xf = __bfloat1622float2(x2[v]);
+                                const int k = 8 * u + 2 * v;
+                                out[2 * v] = fmaf(rf, yd[k], fmaf(e, yo[k], Dh * xf.x));
+                                out[2 * v + 1] = fmaf(rf, yd[k + 1], fmaf(e, yo[k + 1], Dh * xf.y));
+                            }
+                            ov[u] = pack8(out);
+                        }
+                        if (tma_out) {
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                *reinterpret_cast<uint4 *>(xrow + sw128(ia, (col % 64) / 8 + u)) = ov[u];
+                        } else {
+                            uint4 *dst = reinterpret_cast<uint4 *>(yrow + p0);
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) dst[u] = ov[u];
+                        }
+                    }
+                }
+            }
+        } else if (!ok && tid == 0) {
+            set_error(pr, kDevErrTimeout);
         }
-    }
+        if (tma_out) {
+            fence_async_smem();
+            __syncthreads();
+            if (ok && tid == 0) {  // the tile's rows i0 .. i0 + 127 of both 64-column blocks
+                for (int k = 0; k < 2; ++k)
+                    tma_store_3d(&ymap, xs + k * jn * 128 + i0 * 128, hb * 128 + 64 * k, t0 + i0, b);
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+        }
+        // completions of this tile on each barrier
+#pragma unroll
+        for (int sl = 0; sl < nsl; ++sl) {
+            if ((sl + nsl) & 1)
+                ++n_st1;
+            else
+                ++n_st0;
+        }
+        ++n_x;
+        n_s0 += (uint32_t)(nkc + 1) / 2;
+        n_s1 += (uint32_t)nkc / 2;
+    }  // tiles
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, tcols);
@@ -830,8 +868,14 @@ cudaError_t launch_tc(const Problem &pr, const Workspace &ws, cudaStream_t s, in
             return e;
         const size_t smem = out_smem(pr);
         if ((e = ensure_smem_limit(reinterpret_cast<const void *>(chunk_out_tc<NS>), smem)) != cudaSuccess) return e;
+        // persistent: one CTA per SM, tiles by ticket (the counter is zeroed per launch)
         const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
-        const dim3 grid(ncx * ntile, pr.nheads / HB, mb);
+        const long long tiles = (long long)ncx * ntile * (pr.nheads / HB) * mb;
+        if (tiles > INT32_MAX) return cudaErrorInvalidValue;
+        int sms = 148;
+        if ((e = sm_count(&sms)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(ws.ticket, 0, sizeof(uint32_t), s)) != cudaSuccess) return e;
+        const unsigned grid = (unsigned)std::min<long long>(tiles, sms);
         profile_kernel_begin(s);
         chunk_out_tc<NS><<<grid, kOutThreads, smem, s>>>(xmap, bmap, cmap, ymap, smap, pr, ws);
         profile_kernel_end(s);
