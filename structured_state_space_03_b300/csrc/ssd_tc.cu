@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     __shared__ __align__(16) float cs[2 * 256];
     __shared__ __align__(16) float dtv[2 * 256];  // read as float4 in phase 2
     __shared__ float s_mn[2][8], s_mx[2][8];
-    __shared__ int s_fail, s_tile;
+    __shared__ int s_fail, s_next;
 
     const int ntile = pr.chunk <= kBoxRows ? 1 : 2;
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads, L = pr.seqlen;
@@ -421,22 +421,25 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         tma_prefetch_desc(&bmap);
         tma_prefetch_desc(&xmap);
         tma_prefetch_desc(&ymap);
+        s_next = (int)atomicAdd(ws.ticket, 1u);  // the first tile; warp 9 takes each next one early
     }
     uint32_t n_st0 = 0, n_st1 = 0, n_x = 0, n_s0 = 0, n_s1 = 0;
     for (;;) {
         tc_fence_before();
         __syncthreads();  // the previous tile is done with TMEM and shared memory
-        if (tid == 0) s_tile = (int)atomicAdd(ws.ticket, 1u);
-        __syncthreads();
         tc_fence_after();
-        const int tk = s_tile;
+        const int tk = s_next;
         if (tk >= ntiles || s_fail) break;  // block-uniform
         const int hb = tk % nhb, it = (tk / nhb) % ntile, cxz = tk / (nhb * ntile);
         const ChunkRef ref = chunk_ref(pr, cxz % ncx, cxz / ncx);
         const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
         const int b = ref.tb, t0 = ref.t0, len = ref.len;  // b: batch row of the token tensors
         const int i0 = it * kBoxRows;
-        if (i0 >= len) continue;  // tile beyond the end of a partial last chunk (block-uniform)
+        if (i0 >= len) {  // tile beyond the end of a partial last chunk (block-uniform)
+            __syncthreads();  // every thread has read s_next
+            if (warp == 9 && lane == 0) s_next = (int)atomicAdd(ws.ticket, 1u);
+            continue;
+        }
         const int jn = i0 + kBoxRows;                 // columns j in [0, jn)
         const int nbj = jn / kBoxRows;                // 128-row boxes along j
         // parity of the wait for slice s on its stage's barriers, for S chunk kc on its buffer's
@@ -703,6 +706,23 @@ __global__ void __launch_bounds__(kOutThreads, 1)
                 mma_commit(&bar_mm2[kc & 1]);
             }
             if (!good) s_fail = 1;
+        } else if (warp == 9 && lane == 0) {
+            // idle here: take the next tile's ticket and bring its entry states and x rows
+            // into L2, so that its first slices do not wait on DRAM
+            const int tn = (int)atomicAdd(ws.ticket, 1u);
+            s_next = tn;
+            if (tn < ntiles) {
+                const int hbn = tn % nhb, itn = (tn / nhb) % ntile, czn = tn / (nhb * ntile);
+                const ChunkRef rn = chunk_ref(pr, czn % ncx, czn / ncx);
+                if (itn * kBoxRows < rn.len) {
+                    for (int hh = 0; hh < HB; ++hh)
+                        bulk_prefetch_l2(ws.states + state_slot(pr, rn, hbn * HB + hh) * (size_t)P * NS,
+                                         (uint32_t)(P * NS * sizeof(float)));
+                    for (int k = 0; k < 2; ++k)
+                        for (int r = 0; r <= itn; ++r)
+                            tma_prefetch_l2_3d(&xmap, hbn * 128 + 64 * k, rn.t0 + r * kBoxRows, rn.tb);
+                }
+            }
         }
         __syncwarp();
         // every chunk's MMAs done (the last commit covers the earlier ones); warps 0-8 have seen
