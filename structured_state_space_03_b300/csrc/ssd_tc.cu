@@ -38,10 +38,11 @@ using namespace ptx;
 constexpr int kThreads = 128;
 constexpr int kBoxRows = 128;           // tokens per TMA box
 constexpr int kBoxBytes = 64 * 2 * kBoxRows;  // 64 bf16 columns x 128 rows = 16 KiB
-// chunk_state_tc goes through the chunk in 64-token slabs: its shared memory (65 KiB at
-// dstate 256) then leaves room for two CTAs per SM, which hide each other's latencies
-constexpr int kStRows = 64;
-constexpr int kStBytes = 64 * 2 * kStRows;    // 64 bf16 columns x 64 rows = 8 KiB
+// chunk_state_tc goes through the chunk in 32-token slabs, a ring of three in flight: its
+// shared memory (97 KiB at dstate 256) leaves room for two CTAs per SM
+constexpr int kStRows = 32;
+constexpr int kStBytes = 64 * 2 * kStRows;    // 64 bf16 columns x 32 rows = 4 KiB
+constexpr int kStStages = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap smap, Problem pr, Workspace ws)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_tma, bar_mma;
+    __shared__ __align__(8) uint64_t bar_tma[kStStages], bar_mma[kStStages];
     __shared__ uint32_t tmem_slot;
     __shared__ float warp_tot[4];
     __shared__ float cs[2 * 256], dtv[2 * 256];
@@ -209,19 +210,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int P = pr.headdim, HB = 128 / P, H = pr.nheads;
     const int h0 = hb * HB, g = h0 / (H / pr.ngroups);
     const int b = ref.tb, t0 = ref.t0, len = ref.len;  // b: batch row of the token tensors
-    const int nbox = (pr.chunk + kStRows - 1) / kStRows;  // 64-token slabs along K
+    const int nbox = (pr.chunk + kStRows - 1) / kStRows;  // 32-token slabs along K
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // one 64-token slab at a time: w*x as hi and lo bf16 terms (2 MN blocks of
-    // 64 (h,p) columns each), and B (NS/64 MN blocks of 64 n columns)
+    // slab kh in stage kh % 3: w*x as hi and lo bf16 terms (2 MN blocks of 64 (h,p)
+    // columns each) and B (NS/64 MN blocks of 64 n columns)
     uint8_t *base = align1024(smem_raw);
-    uint8_t *xs = base;                 // x, then hi(w*x) in place: 2 x 8 KiB
-    uint8_t *xl = base + 2 * kStBytes;  // lo(w*x): 2 x 8 KiB
-    uint8_t *bs = base + 4 * kStBytes;  // NS/64 x 8 KiB
+    constexpr int kStage = (4 + NS / 64) * kStBytes;
+    auto xs_of = [&](int st) { return base + st * kStage; };                 // x, then hi(w*x) in place
+    auto xl_of = [&](int st) { return base + st * kStage + 2 * kStBytes; };  // lo(w*x)
+    auto bs_of = [&](int st) { return base + st * kStage + 4 * kStBytes; };  // B
 
     if (tid == 0) {
-        mbar_init(&bar_tma, 1);
-        mbar_init(&bar_mma, 1);
+        for (int k = 0; k < kStStages; ++k) {
+            mbar_init(&bar_tma[k], 1);
+            mbar_init(&bar_mma[k], 1);
+        }
         mbar_fence_init();
         s_fail = 0;
     }
@@ -232,16 +236,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_slot;
 
     auto issue_loads = [&](int kh) {
-        mbar_expect_tx(&bar_tma, (uint32_t)((2 + NS / 64) * kStBytes));
+        const int st = kh % kStStages;
+        uint64_t *bar = &bar_tma[st];
+        mbar_expect_tx(bar, (uint32_t)((2 + NS / 64) * kStBytes));
         for (int k = 0; k < 2; ++k)
-            tma_load_3d(xs + k * kStBytes, &xmap, &bar_tma, hb * 128 + 64 * k, t0 + kh * kStRows, b);
+            tma_load_3d(xs_of(st) + k * kStBytes, &xmap, bar, hb * 128 + 64 * k, t0 + kh * kStRows, b);
         for (int s = 0; s < NS / 64; ++s)
-            tma_load_3d(bs + s * kStBytes, &bmap, &bar_tma, g * NS + 64 * s, t0 + kh * kStRows, b);
+            tma_load_3d(bs_of(st) + s * kStBytes, &bmap, bar, g * NS + 64 * s, t0 + kh * kStRows, b);
     };
     if (tid == 0) {
         tma_prefetch_desc(&xmap);
         tma_prefetch_desc(&bmap);
-        issue_loads(0);
+        for (int kh = 0; kh < kStStages && kh < nbox; ++kh) issue_loads(kh);
     }
 
     // segment sums and decay-to-chunk-end weights (natural-log domain, accurate exp)
@@ -256,14 +262,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < HB && !pr.adjoint_states) ws.decay[state_slot(pr, ref, h0 + tid)] = expf(tid == 0 ? cl0 : cl1);
     __syncthreads();
 
-    bool ok = true;
-    for (int kh = 0; kh < nbox && ok; ++kh) {
-        if (!mbar_wait(&bar_tma, kh & 1)) s_fail = 1;
-        __syncthreads();
-        ok = !s_fail;
-        if (!ok) break;
+    // slab kh: every thread waits for its loads and builds w*x; thread 0 issues its MMAs,
+    // then, once slab kh - 1's MMAs are done, the loads of slab kh + 2 into that stage
+    bool t0good = true;
+    for (int kh = 0; kh < nbox; ++kh) {
+        const int st = kh % kStStages;
+        uint8_t *xs = xs_of(st), *xl = xl_of(st), *bs = bs_of(st);
+        const bool landed = mbar_wait(&bar_tma[st], (uint32_t)(kh / kStStages) & 1u);
+        if (!landed) s_fail = 1;
         // w*x -> hi (in place) + lo; one 16-B chunk = 8 columns of one token row
-        for (int q = tid; q < 2 * kStRows * 8; q += kThreads) {
+        for (int q = tid; q < 2 * kStRows * 8 && landed; q += kThreads) {
             const int k = q / (kStRows * 8), row = (q / 8) % kStRows;
             const float w = wts[(P == 64 ? k : 0) * 256 + kh * kStRows + row];
             uint4 *ptr = reinterpret_cast<uint4 *>(xs) + q;
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_async_smem();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0 && t0good) {
             tc_fence_after();
             constexpr uint32_t idesc = idesc_bf16(128, NS, 1, 1);
             for (int ks = 0; ks < kStRows / 16; ++ks) {
@@ -297,23 +305,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_bf16(tmem, sdesc_sw128(smem_u32(xs) + ks * 2048, kStBytes, 1024), bd, idesc, (kh | ks) != 0);
                 mma_bf16(tmem, sdesc_sw128(smem_u32(xl) + ks * 2048, kStBytes, 1024), bd, idesc, 1);
             }
-            mma_commit(&bar_mma);
+            mma_commit(&bar_mma[st]);
+            // slab kh + 2 goes into the stage of slab kh - 1 once that slab's MMAs are done
+            if (kh >= 1 && kh + 2 < nbox) {
+                const int sp = (kh - 1) % kStStages;
+                if (mbar_wait(&bar_mma[sp], (uint32_t)((kh - 1) / kStStages) & 1u))
+                    issue_loads(kh + 2);
+                else
+                    t0good = false;
+            }
+            if (!t0good) s_fail = 1;
         }
-        if (!mbar_wait(&bar_mma, kh & 1)) s_fail = 1;  // slab buffers are reused by the next half
-        __syncthreads();
-        ok = !s_fail;
-        if (ok && tid == 0 && kh + 1 < nbox) issue_loads(kh + 1);
     }
+    // every slab's MMAs done: thread 0 waits (it has seen slab nbox - 4's complete, so the
+    // parity wait cannot mistake the barrier's previous phase), the others at the barrier
+    if (tid == 0 && !mbar_wait(&bar_mma[(nbox - 1) % kStStages], (uint32_t)((nbox - 1) / kStStages) & 1u))
+        s_fail = 1;
+    __syncthreads();
     tc_fence_after();
-
+    const bool ok = !s_fail;
     // S_c out: 32 state columns at a time into a [128 rows][32] fp32 box with the 128-byte
-    // swizzle (double-buffered over the dead w*x hi / lo slabs), each head's P rows stored by
+    // swizzle (double-buffered over the dead stages), each head's P rows stored by
     // TMA as one box of the [state rows][NS] view of the workspace
     if (ok) {
         const int m = warp * 32 + lane;
 #pragma unroll 1
         for (int c0 = 0; c0 < NS; c0 += 32) {
-            uint8_t *buf = (c0 / 32) & 1 ? xl : xs;
+            uint8_t *buf = base + ((c0 / 32) & 1) * 16384;  // [128 rows][32] fp32, over the dead stages
             if (c0 >= 64) {  // the store of two slabs ago must be done reading this buffer
                 if (tid == 0) bulk_wait_read_1();
                 __syncthreads();
@@ -835,7 +853,10 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int width, int seqlen, i
     return cached_tensor_map(map, ptr, true, width, seqlen, batch, 64, kBoxRows, true);
 }
 
-size_t state_smem(const Problem &pr) { return 1024 + (size_t)(4 + pr.dstate / 64) * kStBytes; }
+size_t state_smem(const Problem &pr)
+{
+    return 1024 + std::max<size_t>((size_t)kStStages * (4 + pr.dstate / 64) * kStBytes, 2 * 16384);
+}
 
 size_t out_smem(const Problem &pr)
 {
