@@ -604,8 +604,47 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk(BwdArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// 4a. dB / dC: sum of the per-head parts over the heads of each group.
+// 4a. dB / dC: sum of the per-head parts over the heads of each group.  With dstate a
+//     multiple of 4, four consecutive state columns per thread as float4s, and four heads'
+//     loads in flight at a time (the sum runs over the heads in order either way).
 __global__ void __launch_bounds__(kThreads) bwd_reduce_groups(BwdArgs a)
+{
+    const int H = a.nheads, G = a.ngroups, N = a.dstate, hpg = H / G, N4 = N / 4;
+    const size_t total = (size_t)a.batch * a.seqlen * G * N4;
+    const float4 *dBp = reinterpret_cast<const float4 *>(a.dBp), *dCp = reinterpret_cast<const float4 *>(a.dCp);
+    for (size_t e = (size_t)blockIdx.x * kThreads + threadIdx.x; e < total; e += (size_t)gridDim.x * kThreads) {
+        const int n4 = (int)(e % N4);
+        const size_t bt_g = e / N4;
+        const int g = (int)(bt_g % G);
+        const size_t bt = bt_g / G;
+        const size_t base = (bt * H + (size_t)g * hpg) * N4 + n4;
+        float4 sb = make_float4(0.f, 0.f, 0.f, 0.f), sc = sb;
+        int k = 0;
+        for (; k + 4 <= hpg; k += 4) {
+            float4 vb[4], vc[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                vb[u] = __ldcs(dBp + base + (size_t)(k + u) * N4);
+                vc[u] = __ldcs(dCp + base + (size_t)(k + u) * N4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                sb.x += vb[u].x; sb.y += vb[u].y; sb.z += vb[u].z; sb.w += vb[u].w;
+                sc.x += vc[u].x; sc.y += vc[u].y; sc.z += vc[u].z; sc.w += vc[u].w;
+            }
+        }
+        for (; k < hpg; ++k) {
+            const float4 vb = __ldcs(dBp + base + (size_t)k * N4), vc = __ldcs(dCp + base + (size_t)k * N4);
+            sb.x += vb.x; sb.y += vb.y; sb.z += vb.z; sb.w += vb.w;
+            sc.x += vc.x; sc.y += vc.y; sc.z += vc.z; sc.w += vc.w;
+        }
+        reinterpret_cast<float4 *>(a.dB)[e] = sb;
+        reinterpret_cast<float4 *>(a.dC)[e] = sc;
+    }
+}
+
+// The same one column at a time (dstate not a multiple of 4, or dB / dC not 16-byte aligned).
+__global__ void __launch_bounds__(kThreads) bwd_reduce_groups_n1(BwdArgs a)
 {
     const int H = a.nheads, G = a.ngroups, N = a.dstate, hpg = H / G;
     const size_t total = (size_t)a.batch * a.seqlen * G * N;
@@ -755,18 +794,6 @@ __device__ __forceinline__ float3 scan_sum2_256(float v, float w, float (*red)[8
     const float ws = ((red[2][0] + red[2][1]) + (red[2][2] + red[2][3])) + ((red[2][4] + red[2][5]) + (red[2][6] + red[2][7]));
     __syncthreads();
     return make_float3(pre, tot, ws);
-}
-
-__device__ __forceinline__ float sum256(float v, float *warp_tot)
-{
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) == 0) warp_tot[threadIdx.x >> 5] = v;
-    __syncthreads();
-    const float s = ((warp_tot[0] + warp_tot[1]) + (warp_tot[2] + warp_tot[3])) +
-                    ((warp_tot[4] + warp_tot[5]) + (warp_tot[6] + warp_tot[7]));
-    __syncthreads();
-    return s;
 }
 
 // Row t (64 bf16) of a [128][64] swizzled tile, as floats.
@@ -1178,11 +1205,16 @@ cudaError_t launch_reductions(const BwdArgs &a, cudaStream_t s)
     if (a.dBp) {
         int sms = 148;
         if ((e = sm_count(&sms)) != cudaSuccess) return e;
-        const size_t total = (size_t)a.batch * a.seqlen * a.ngroups * a.dstate;
+        const bool v4 = a.dstate % 4 == 0 && reinterpret_cast<uintptr_t>(a.dB) % 16 == 0 &&
+                        reinterpret_cast<uintptr_t>(a.dC) % 16 == 0;
+        const size_t total = (size_t)a.batch * a.seqlen * a.ngroups * a.dstate / (v4 ? 4 : 1);
         const size_t want = (total + kThreads - 1) / kThreads;
         const unsigned blocks = (unsigned)std::min<size_t>(want, (size_t)sms * 8);
         profile_kernel_begin(s);
-        bwd_reduce_groups<<<blocks, kThreads, 0, s>>>(a);
+        if (v4)
+            bwd_reduce_groups<<<blocks, kThreads, 0, s>>>(a);
+        else
+            bwd_reduce_groups_n1<<<blocks, kThreads, 0, s>>>(a);
         profile_kernel_end(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
