@@ -114,9 +114,13 @@ static ssd_status_t check_dims(Problem &pr, int batch, int seqlen, int nheads, i
     pr.dtype = dtype;
     // The block decomposition is exact for any chunk length, so a chunk longer than the
     // fused kernels' 128-token tile is evaluated as equal blocks of at most 128 tokens
-    // whenever a fused kernel covers the sizes (one kernel instead of three, no chunk
-    // states in HBM).  The results differ from the requested length only in rounding.
-    if (chunk > kFusedTile) {
+    // where a fused kernel covers the sizes and is the faster choice: at dstate 64 (the
+    // pipelined fused kernels), and wherever the three-kernel tcgen05 path cannot take the
+    // requested length.  At dstate 128 the three-kernel path at the requested length
+    // measured faster than the one-unit-at-a-time fused kernel at 128-token blocks (0.27
+    // against 0.32 ms on 1 x 8192 tokens, 80 heads x 64, chunk 256).  The results differ
+    // from the requested length only in rounding.
+    if (chunk > kFusedTile && (dstate == 64 || !tc_supported(pr))) {
         Problem q = pr;
         const int nb = (chunk + kFusedTile - 1) / kFusedTile;
         q.chunk = (chunk + nb - 1) / nb;

@@ -127,7 +127,8 @@ def test_path_selection_is_a_pure_host_query(lib):
     # than 128 evaluated as equal blocks of at most 128); dstate 256: the three-kernel path
     assert ssd.ssd_fwd_path(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == "tcgen05_fused"
     assert ssd.ssd_fwd_path(16, 4096, 32, 128, 8, 128, 128, ssd.SSD_DTYPE_BF16) == "tcgen05_fused"
-    assert ssd.ssd_fwd_path(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == "tcgen05_fused"
+    assert ssd.ssd_fwd_path(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == "tcgen05"
+    assert ssd.ssd_fwd_path(1, 8192, 80, 64, 1, 128, 128, ssd.SSD_DTYPE_BF16) == "tcgen05_fused"
     assert ssd.ssd_fwd_path(1, 131072, 24, 64, 1, 256, 256, ssd.SSD_DTYPE_BF16) == "tcgen05"
     assert ssd.ssd_fwd_path(1, 1000, 4, 64, 1, 256, 128, ssd.SSD_DTYPE_BF16) == "tcgen05"
     assert ssd.ssd_fwd_path(2, 333, 6, 32, 3, 48, 100, ssd.SSD_DTYPE_BF16) == "simt"
@@ -135,15 +136,17 @@ def test_path_selection_is_a_pure_host_query(lib):
     assert ssd.ssd_fwd_kernels(2, 2048, 80, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == ["ssd_fused_pipe_tc"]
     assert ssd.ssd_fwd_kernels(1, 65536, 8, 64, 1, 64, 128, ssd.SSD_DTYPE_BF16) == ["ssd_seq_pipe_tc"]
     assert ssd.ssd_fwd_kernels(16, 4096, 32, 128, 8, 128, 128, ssd.SSD_DTYPE_BF16) == ["ssd_fused_tc"]
-    assert ssd.ssd_fwd_kernels(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == ["ssd_fused_tc"]
+    assert ssd.ssd_fwd_kernels(1, 8192, 80, 64, 1, 128, 256, ssd.SSD_DTYPE_BF16) == [
+        "chunk_state_tc", "state_pass_hilo", "chunk_out_tc"]
     assert ssd.ssd_fwd_kernels(1, 131072, 24, 64, 1, 256, 256, ssd.SSD_DTYPE_BF16) == [
         "chunk_state_tc", "state_pass_hilo", "chunk_out_tc"]
 
 
 def test_block_length_of_long_chunks(lib):
-    # the evaluated chunk length: at most 128 on the fused paths, the requested one elsewhere
+    # the evaluated chunk length: at most 128 on the fused paths, the requested one elsewhere;
+    # blocks of a longer chunk at dstate 64 (dstate 128 keeps it on the three-kernel path)
     B = ssd.SSD_DTYPE_BF16
-    assert ssd.ssd_fwd_block(1, 8192, 80, 64, 1, 128, 256, B) == 128
+    assert ssd.ssd_fwd_block(1, 8192, 80, 64, 1, 128, 256, B) == 256    # dstate 128: three-kernel path
     assert ssd.ssd_fwd_block(2, 2048, 80, 64, 1, 64, 200, B) == 100
     assert ssd.ssd_fwd_block(2, 2048, 80, 64, 1, 64, 129, B) == 65
     assert ssd.ssd_fwd_block(2, 2048, 80, 64, 1, 64, 96, B) == 96
@@ -153,8 +156,8 @@ def test_block_length_of_long_chunks(lib):
     assert ssd.ssd_fwd_block(1, 1000, 4, 64, 1, 64, 999, B) == -1
     # the workspace follows the evaluated length
     n256, n128 = ctypes.c_size_t(0), ctypes.c_size_t(0)
-    assert lib.ssd_fwd_workspace_size(1, 8192, 80, 64, 1, 128, 256, B, ctypes.byref(n256)) == ssd.SSD_OK
-    assert lib.ssd_fwd_workspace_size(1, 8192, 80, 64, 1, 128, 128, B, ctypes.byref(n128)) == ssd.SSD_OK
+    assert lib.ssd_fwd_workspace_size(2, 2048, 80, 64, 1, 64, 256, B, ctypes.byref(n256)) == ssd.SSD_OK
+    assert lib.ssd_fwd_workspace_size(2, 2048, 80, 64, 1, 64, 128, B, ctypes.byref(n128)) == ssd.SSD_OK
     assert n256.value == n128.value
 
 

@@ -24,7 +24,8 @@ CASES = [
     (2, 600, 8, 64, 64, 2, 128, "bf16", "tcgen05_fused"),   # persistent fused kernel
     (1, 400, 2, 128, 128, 1, 128, "bf16", "tcgen05_fused"),  # one-unit fused kernel
     (1, 500, 4, 64, 256, 1, 256, "bf16", "tcgen05"),         # three-kernel tensor-core path (dstate 256)
-    (1, 500, 4, 64, 128, 1, 256, "bf16", "tcgen05_fused"),   # chunk 256 as two 128-token blocks
+    (1, 500, 4, 64, 128, 1, 256, "bf16", "tcgen05"),         # dstate 128 at chunk 256: three kernels
+    (1, 500, 4, 64, 64, 1, 256, "bf16", "tcgen05_fused"),    # dstate 64: chunk 256 as two 128-token blocks
     (2, 300, 6, 32, 48, 3, 100, "f32", "simt"),             # fp32 path
 ]
 MODES = [dict(softplus=True, bias=True), dict(zoh=True), dict(softplus=True, bias=True, zoh=True)]

@@ -69,7 +69,7 @@ def test_packed_sequences_match_oracle(case, with_init):
 MULTI = [
     ([700, 1, 256, 0, 255, 257, 64, 3], 4, 64, 256, 1, 128, "bf16", "tcgen05"),   # dstate 256
     ([600, 0, 1, 256, 255, 300], 4, 64, 256, 1, 256, "bf16", "tcgen05"),          # chunk 256: two tiles per chunk
-    ([600, 0, 1, 256, 255, 300], 4, 64, 128, 2, 256, "bf16", "tcgen05_fused"),    # chunk 256 as two 128-token blocks
+    ([600, 0, 1, 256, 255, 300], 4, 64, 128, 2, 256, "bf16", "tcgen05"),          # dstate 128 at chunk 256: three kernels
     ([300, 77, 0, 128, 1, 200], 4, 128, 64, 2, 256, "bf16", "tcgen05_fused"),     # headdim 128, chunk 256 as 2 x 128
     ([333, 17, 0, 64, 65, 1, 190], 6, 32, 48, 3, 100, "f32", "simt"),
     ([250, 3, 128, 0, 77], 4, 32, 64, 2, 64, "bf16", "simt"),                     # headdim 32: fp32 FMA path
