@@ -3,23 +3,26 @@
 // Work unit: one chunk of Q tokens of one "head block" -- the 128 / headdim
 // heads (2 for headdim 64, 1 for headdim 128) whose headdim rows fill the
 // 128 lanes of a tensor-memory accumulator.  All heads of a block share one
-// B/C group.  Operands arrive by TMA in 128-byte-swizzled 64-column slabs
-// (box = 64 elements x 128 tokens); accumulators live in TMEM; one thread
-// issues the MMAs; the four warps of the CTA run the epilogues (thread i owns
-// accumulator row i).  The chunk algebra is written out in ssd_internal.cuh.
+// B/C group.  Operands arrive by TMA in 128-byte-swizzled 64-column slabs;
+// accumulators live in TMEM; one thread issues the MMAs.  The chunk algebra is
+// written out in ssd_internal.cuh.
 //
 // chunk_state_tc:  S_c[(h,p), n] = sum_j w_{h,j} x_j[h,p] B_j[n],
 //                  w_{h,j} = exp(cs_last - cs_j) dt_j           (M=128, N=dstate, K=chunk)
 //                  w*x is fed as two bf16 terms (hi + lo): a single rounding of it
-//                  costs up to ~2.4% of RMS(final_state) on short sequences
-// chunk_out_tc:    per 128-row tile of the chunk (rows i0 .. i0+127, columns j < i0+128)
+//                  costs up to ~2.4% of RMS(final_state) on short sequences.  32-token
+//                  slabs, three in flight; S_c leaves by TMA through swizzled fp32 boxes.
+// (state_pass_hilo, in ssd_simt.cu, turns S_c into the entry states h_c, in place, as
+//  bf16 hi + lo terms per 64-wide slice of the state dimension.)
+// chunk_out_tc:    persistent; per tile = (128 rows i0 .. i0+127 of a chunk, head block),
+//                  columns j < i0 + 128:
 //                  G    = C_i B_j^T                              (M=128, N=i0+128, K=dstate)
 //                  Yoff = C_i (h_hi + h_lo)^T  (both heads)       (M=128, N=128,    K=dstate)
-//                         h_c is split into two bf16 terms (hi = bf16(h), lo = bf16(h - hi)):
 //                         the carried state can be ~10x larger than y (an init state), and a
 //                         single bf16 rounding of it alone costs ~2% of RMS(y)
-//                  S_h  = G o exp(cs_i - cs_j) dt_j [j <= i]  -> bf16 in shared memory
-//                  Ydiag_h = S_h x_h                             (M=128, N=headdim, K=i0+128)
+//                  S_h  = G o exp(cs_i - cs_j) dt_j [j <= i]  as hi + lo bf16 in shared memory
+//                         (rank-one decays when the chunk's decay range allows)
+//                  Ydiag_h = S_hi x_h + S_lo x_h                  (M=128, N=headdim, K=i0+128)
 //                  y = Ydiag + exp(cs_i) Yoff + D x
 #include <cuda.h>
 #include <cudaTypedefs.h>
