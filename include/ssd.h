@@ -165,7 +165,8 @@ SSD_API ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A
  * workspace it uses a fixed 32 MiB scratch array compiled into the library,
  * which every device that loads the library holds until the process exits; it
  * calls no allocator at all.  It runs the fused bf16 kernel only (bf16,
- * headdim 64 or 128, dstate 64 or 128) and returns
+ * headdim 64 or 128, dstate 64 or 128; a chunk longer than 128 as equal blocks
+ * of at most 128 tokens, which changes the results only in rounding) and returns
  * SSD_ERR_UNSUPPORTED, with the needed and available sizes in
  * ssd_last_error_detail(), for anything else or for a problem whose scratch
  * (ssd_fwd_workspace_size) exceeds 32 MiB.  At dstate 64 the scratch is one

@@ -84,6 +84,21 @@ Workspace carve_workspace(const Problem &pr, void *base)
     return ws;
 }
 
+// Evaluates a chunk longer than the fused kernels' 128-token tile as equal blocks of
+// at most 128 tokens when a fused kernel then covers the sizes; false if none does.
+static bool to_fused_blocks(Problem &pr)
+{
+    if (pr.chunk <= kFusedTile) return false;
+    Problem q = pr;
+    const int nb = (pr.chunk + kFusedTile - 1) / kFusedTile;
+    q.chunk = (pr.chunk + nb - 1) / nb;
+    q.nchunks = (pr.seqlen + q.chunk - 1) / q.chunk;
+    if (!fused_supported(q)) return false;
+    pr.chunk = q.chunk;
+    pr.nchunks = q.nchunks;
+    return true;
+}
+
 // Checks that need no pointer; fills the dimension fields of `pr`.
 static ssd_status_t check_dims(Problem &pr, int batch, int seqlen, int nheads, int headdim, int ngroups,
                                int dstate, int chunk, ssd_dtype_t dtype)
@@ -120,16 +135,7 @@ static ssd_status_t check_dims(Problem &pr, int batch, int seqlen, int nheads, i
     // measured faster than the one-unit-at-a-time fused kernel at 128-token blocks (0.27
     // against 0.32 ms on 1 x 8192 tokens, 80 heads x 64, chunk 256).  The results differ
     // from the requested length only in rounding.
-    if (chunk > kFusedTile && (dstate == 64 || !tc_supported(pr))) {
-        Problem q = pr;
-        const int nb = (chunk + kFusedTile - 1) / kFusedTile;
-        q.chunk = (chunk + nb - 1) / nb;
-        q.nchunks = (seqlen + q.chunk - 1) / q.chunk;
-        if (fused_supported(q)) {
-            pr.chunk = q.chunk;
-            pr.nchunks = q.nchunks;
-        }
-    }
+    if (dstate == 64 || !tc_supported(pr)) to_fused_blocks(pr);
     return SSD_OK;
 }
 
@@ -503,6 +509,8 @@ ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float *A, con
     ssd_status_t st = make_problem(pr, x, dt, A, B, C, D, init_state, y, final_state, batch, seqlen, nheads,
                                    headdim, ngroups, dstate, chunk, dtype);
     if (st != SSD_OK) return st;
+    // only the fused kernels run here: a longer chunk at dstate 128 as 128-token blocks too
+    if (choose_path(pr) != SSD_PATH_TCGEN05_FUSED) to_fused_blocks(pr);
     if (choose_path(pr) != SSD_PATH_TCGEN05_FUSED)
         return fail(SSD_ERR_UNSUPPORTED,
                     "ssd_fwd_noalloc runs the fused bf16 kernel only (bf16, headdim 64 or 128, dstate 64 or "

@@ -73,6 +73,19 @@ def test_noalloc_matches_regular_entry_twice_in_a_row():
     assert_close(f.cpu().numpy(), fr, TOL[torch.bfloat16], "final state, no-alloc vs oracle")
 
 
+def test_noalloc_long_chunk_at_dstate_128():
+    # ssd_fwd takes a 256-token chunk at dstate 128 on the three-kernel path; the
+    # no-allocation entry runs the fused kernel only and evaluates it as two 128-token
+    # blocks: the same result up to rounding, so it agrees with the oracle
+    inp = make_inputs(1, 600, 4, 64, 128, 1, "bf16", seed=35, with_init=True)
+    c = to_cuda(inp)
+    assert ssd.ssd_fwd_path(1, 600, 4, 64, 1, 128, 256, torch.bfloat16) == "tcgen05"
+    y, f = _noalloc(c, 256)
+    yr, fr = oracle.recurrence(**inp)
+    assert_close(y.float().cpu().numpy(), yr, TOL[torch.bfloat16], "y, no-alloc chunk 256", STORAGE_U[torch.bfloat16])
+    assert_close(f.cpu().numpy(), fr, TOL[torch.bfloat16], "final state, no-alloc chunk 256")
+
+
 def test_noalloc_rejects_what_it_cannot_hold():
     # larger than the fixed scratch: a clear error, nothing enqueued.  (At dstate
     # 64 the scratch is one state slot per CTA, at most 16 MiB, so every size
