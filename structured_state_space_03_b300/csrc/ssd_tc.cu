@@ -38,7 +38,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 128;      // chunk_state_tc: the working threads (warps 0-3) ...
+constexpr int kStThreads = 160;    // ... and warp 4, which issues its loads, MMAs and stores
 constexpr int kBoxRows = 128;           // tokens per TMA box
 constexpr int kBoxBytes = 64 * 2 * kBoxRows;  // 64 bf16 columns x 128 rows = 16 KiB
 // chunk_state_tc goes through the chunk in 32-token slabs, a ring of three in flight: its
@@ -58,8 +59,11 @@ __device__ __forceinline__ void set_error(const Problem &pr, unsigned int flag)
     if (pr.err_word) atomicOr(pr.err_word, flag);
 }
 
+// Barrier of threads 0-127 of a larger block, while its other warps work on.
+__device__ __forceinline__ void sync128() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
 // Inclusive prefix sum of 256 values held two per thread (thread t holds
-// values 2t and 2t+1) across a 128-thread block.  warp_tot: 4 floats.
+// values 2t and 2t+1) across threads 0-127.  warp_tot: 4 floats.
 __device__ __forceinline__ void scan_128x2(float &v0, float &v1, float *warp_tot)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -71,10 +75,10 @@ __device__ __forceinline__ void scan_128x2(float &v0, float &v1, float *warp_tot
         if (lane >= o) s += t;
     }
     if (lane == 31) warp_tot[warp] = s;
-    __syncthreads();
+    sync128();
     float off = 0.f;
     for (int w = 0; w < warp; ++w) off += warp_tot[w];
-    __syncthreads();
+    sync128();
     v0 = off + (s - own) + v0;
     v1 = v0 + v1;
 }
@@ -112,7 +116,7 @@ __device__ __forceinline__ void segsum(const Problem &pr, int b, int h0, int nh,
             dtv[hh * 256 + j1] = d1[hh];
         }
     }
-    __syncthreads();
+    sync128();
 }
 
 // The chunk's cumulative decays in two steps, so that the loads of dt can be issued
@@ -197,12 +201,12 @@ __device__ __forceinline__ uint32_t sw128(int r, int q) { return (uint32_t)r * 1
 // ---------------------------------------------------------------------------
 
 template <int NS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kStThreads, 1)
     chunk_state_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap bmap,
                    const __grid_constant__ CUtensorMap smap, Problem pr, Workspace ws)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_tma[kStStages], bar_mma[kStStages];
+    __shared__ __align__(8) uint64_t bar_tma[kStStages], bar_mma[kStStages], bar_built[kStStages];
     __shared__ uint32_t tmem_slot;
     __shared__ float warp_tot[4];
     __shared__ float cs[2 * 256], dtv[2 * 256];
@@ -228,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < kStStages; ++k) {
             mbar_init(&bar_tma[k], 1);
             mbar_init(&bar_mma[k], 1);
+            mbar_init(&bar_built[k], kThreads);  // the working threads, once per slab
         }
         mbar_fence_init();
         s_fail = 0;
@@ -247,112 +252,129 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < NS / 64; ++s)
             tma_load_3d(bs_of(st) + s * kStBytes, &bmap, bar, g * NS + 64 * s, t0 + kh * kStRows, b);
     };
-    if (tid == 0) {
-        tma_prefetch_desc(&xmap);
-        tma_prefetch_desc(&bmap);
-        for (int kh = 0; kh < kStStages && kh < nbox; ++kh) issue_loads(kh);
-    }
-
-    // segment sums and decay-to-chunk-end weights (natural-log domain, accurate exp)
-    segsum(pr, b, h0, HB, t0, len, 1.f, cs, dtv, warp_tot);
-    float *wts = cs;  // overwrite cs with w after reading cs_last
-    const float cl0 = cs[len - 1], cl1 = HB > 1 ? cs[256 + len - 1] : 0.f;
-    __syncthreads();
-    for (int e = tid; e < HB * 256; e += kThreads) {
-        const int j = e & 255;
-        wts[e] = j >= len ? 0.f : pr.adjoint_states ? expf(cs[e]) : expf((e < 256 ? cl0 : cl1) - cs[e]) * dtv[e];
-    }
-    if (tid < HB && !pr.adjoint_states) ws.decay[state_slot(pr, ref, h0 + tid)] = expf(tid == 0 ? cl0 : cl1);
-    __syncthreads();
-
-    // slab kh: every thread waits for its loads and builds w*x; thread 0 issues its MMAs,
-    // then, once slab kh - 1's MMAs are done, the loads of slab kh + 2 into that stage
-    bool t0good = true;
-    for (int kh = 0; kh < nbox; ++kh) {
-        const int st = kh % kStStages;
-        uint8_t *xs = xs_of(st), *xl = xl_of(st), *bs = bs_of(st);
-        const bool landed = mbar_wait(&bar_tma[st], (uint32_t)(kh / kStStages) & 1u);
-        if (!landed) s_fail = 1;
-        // w*x -> hi (in place) + lo; one 16-B chunk = 8 columns of one token row
-        for (int q = tid; q < 2 * kStRows * 8 && landed; q += kThreads) {
-            const int k = q / (kStRows * 8), row = (q / 8) % kStRows;
-            const float w = wts[(P == 64 ? k : 0) * 256 + kh * kStRows + row];
-            uint4 *ptr = reinterpret_cast<uint4 *>(xs) + q;
-            uint4 v = *ptr;
-            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
-            float f[8];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 t = __bfloat1622float2(h2[u]);
-                f[2 * u] = t.x * w;
-                f[2 * u + 1] = t.y * w;
-            }
-            const uint4 hi = pack8(f);
-            const __nv_bfloat162 *hh2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 t = __bfloat1622float2(hh2[u]);
-                f[2 * u] -= t.x;
-                f[2 * u + 1] -= t.y;
-            }
-            *ptr = hi;
-            reinterpret_cast<uint4 *>(xl)[q] = pack8(f);
-        }
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0 && t0good) {
-            tc_fence_after();
-            constexpr uint32_t idesc = idesc_bf16(128, NS, 1, 1);
-            for (int ks = 0; ks < kStRows / 16; ++ks) {
-                const uint64_t bd = sdesc_sw128(smem_u32(bs) + ks * 2048, kStBytes, 1024);
-                mma_bf16(tmem, sdesc_sw128(smem_u32(xs) + ks * 2048, kStBytes, 1024), bd, idesc, (kh | ks) != 0);
-                mma_bf16(tmem, sdesc_sw128(smem_u32(xl) + ks * 2048, kStBytes, 1024), bd, idesc, 1);
-            }
-            mma_commit(&bar_mma[st]);
-            // slab kh + 2 goes into the stage of slab kh - 1 once that slab's MMAs are done
-            if (kh >= 1 && kh + 2 < nbox) {
-                const int sp = (kh - 1) % kStStages;
-                if (mbar_wait(&bar_mma[sp], (uint32_t)((kh - 1) / kStStages) & 1u))
+    bool ok;
+    if (warp == 4) {
+        // warp 4: the loads of the first three slabs, then per slab the MMAs once every
+        // working thread has built it, and the loads of slab kh + 2 into the stage of slab
+        // kh - 1 once that slab's MMAs are done
+        if (lane == 0) {
+            tma_prefetch_desc(&xmap);
+            tma_prefetch_desc(&bmap);
+            tma_prefetch_desc(&smap);
+            for (int kh = 0; kh < kStStages && kh < nbox; ++kh) issue_loads(kh);
+            bool good = true;
+            for (int kh = 0; kh < nbox && good; ++kh) {
+                const int st = kh % kStStages;
+                if (!mbar_wait(&bar_built[st], (uint32_t)(kh / kStStages) & 1u)) {
+                    good = false;
+                    break;
+                }
+                tc_fence_after();
+                constexpr uint32_t idesc = idesc_bf16(128, NS, 1, 1);
+                const uint32_t xa = smem_u32(xs_of(st)), xla = smem_u32(xl_of(st)), ba = smem_u32(bs_of(st));
+                for (int ks = 0; ks < kStRows / 16; ++ks) {
+                    const uint64_t bd = sdesc_sw128(ba + ks * 2048, kStBytes, 1024);
+                    mma_bf16(tmem, sdesc_sw128(xa + ks * 2048, kStBytes, 1024), bd, idesc, (kh | ks) != 0);
+                    mma_bf16(tmem, sdesc_sw128(xla + ks * 2048, kStBytes, 1024), bd, idesc, 1);
+                }
+                mma_commit(&bar_mma[st]);
+                if (kh >= 1 && kh + 2 < nbox) {
+                    if (!mbar_wait(&bar_mma[(kh - 1) % kStStages], (uint32_t)((kh - 1) / kStStages) & 1u)) {
+                        good = false;
+                        break;
+                    }
                     issue_loads(kh + 2);
-                else
-                    t0good = false;
+                }
             }
-            if (!t0good) s_fail = 1;
+            // every slab's MMAs done (this thread has seen slab nbox - 4's complete, so the
+            // parity wait cannot mistake the barrier's previous phase)
+            if (good && !mbar_wait(&bar_mma[(nbox - 1) % kStStages], (uint32_t)((nbox - 1) / kStStages) & 1u))
+                good = false;
+            if (!good) s_fail = 1;
+        }
+        __syncwarp();
+    } else {
+        // segment sums and decay-to-chunk-end weights (natural-log domain, accurate exp)
+        segsum(pr, b, h0, HB, t0, len, 1.f, cs, dtv, warp_tot);
+        float *wts = cs;  // overwrite cs with w after reading cs_last
+        const float cl0 = cs[len - 1], cl1 = HB > 1 ? cs[256 + len - 1] : 0.f;
+        sync128();
+        for (int e = tid; e < HB * 256; e += kThreads) {
+            const int j = e & 255;
+            wts[e] = j >= len ? 0.f : pr.adjoint_states ? expf(cs[e]) : expf((e < 256 ? cl0 : cl1) - cs[e]) * dtv[e];
+        }
+        if (tid < HB && !pr.adjoint_states) ws.decay[state_slot(pr, ref, h0 + tid)] = expf(tid == 0 ? cl0 : cl1);
+        sync128();
+
+        // slab kh: wait for its loads, build w*x, arrive; the stage is rewritten only by the
+        // loads of slab kh + 3, which warp 4 issues after slab kh's MMAs are done
+        for (int kh = 0; kh < nbox; ++kh) {
+            const int st = kh % kStStages;
+            uint8_t *xs = xs_of(st), *xl = xl_of(st);
+            const bool landed = mbar_wait(&bar_tma[st], (uint32_t)(kh / kStStages) & 1u);
+            if (!landed) s_fail = 1;
+            // w*x -> hi (in place) + lo; one 16-B chunk = 8 columns of one token row
+            for (int q = tid; q < 2 * kStRows * 8 && landed; q += kThreads) {
+                const int k = q / (kStRows * 8), row = (q / 8) % kStRows;
+                const float w = wts[(P == 64 ? k : 0) * 256 + kh * kStRows + row];
+                uint4 *ptr = reinterpret_cast<uint4 *>(xs) + q;
+                uint4 v = *ptr;
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
+                float f[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 t = __bfloat1622float2(h2[u]);
+                    f[2 * u] = t.x * w;
+                    f[2 * u + 1] = t.y * w;
+                }
+                const uint4 hi = pack8(f);
+                const __nv_bfloat162 *hh2 = reinterpret_cast<const __nv_bfloat162 *>(&hi);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 t = __bfloat1622float2(hh2[u]);
+                    f[2 * u] -= t.x;
+                    f[2 * u + 1] -= t.y;
+                }
+                *ptr = hi;
+                reinterpret_cast<uint4 *>(xl)[q] = pack8(f);
+            }
+            fence_async_smem();  // the slab, written here, is read by the tensor cores
+            mbar_arrive(&bar_built[st]);
         }
     }
-    // every slab's MMAs done: thread 0 waits (it has seen slab nbox - 4's complete, so the
-    // parity wait cannot mistake the barrier's previous phase), the others at the barrier
-    if (tid == 0 && !mbar_wait(&bar_mma[(nbox - 1) % kStStages], (uint32_t)((nbox - 1) / kStStages) & 1u))
-        s_fail = 1;
-    __syncthreads();
+    __syncthreads();  // warp 4 has seen the last MMAs complete
     tc_fence_after();
-    const bool ok = !s_fail;
+    ok = !s_fail;
     // S_c out: 32 state columns at a time into a [128 rows][32] fp32 box with the 128-byte
     // swizzle (double-buffered over the dead stages), each head's P rows stored by
     // TMA as one box of the [state rows][NS] view of the workspace
-    if (ok) {
+    if (ok) {  // warps 0-3 stage the rows (their TMEM lanes), lane 0 of warp 4 stores them
         const int m = warp * 32 + lane;
+        const bool issuer = warp == 4 && lane == 0;
 #pragma unroll 1
         for (int c0 = 0; c0 < NS; c0 += 32) {
             uint8_t *buf = base + ((c0 / 32) & 1) * 16384;  // [128 rows][32] fp32, over the dead stages
             if (c0 >= 64) {  // the store of two slabs ago must be done reading this buffer
-                if (tid == 0) bulk_wait_read_1();
+                if (issuer) bulk_wait_read_1();
                 __syncthreads();
             }
-            float v[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+            if (warp < 4) {
+                float v[32];
+                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<float4 *>(buf + sw128(m, q)) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            fence_async_smem();
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<float4 *>(buf + sw128(m, q)) =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                fence_async_smem();
+            }
             __syncthreads();
-            if (tid == 0) {
+            if (issuer) {
                 for (int hh = 0; hh < HB; ++hh)
                     tma_store_3d(&smap, buf + hh * P * 128, c0, (int)(state_slot(pr, ref, h0 + hh) * P), 0);
                 bulk_commit();
             }
         }
-        if (tid == 0) bulk_wait_read_all();
+        if (issuer) bulk_wait_read_all();
     } else if (tid == 0) {
         set_error(pr, kDevErrTimeout);
     }
@@ -895,7 +917,7 @@ cudaError_t launch_tc(const Problem &pr, const Workspace &ws, cudaStream_t s, in
         if ((e = ensure_smem_limit(reinterpret_cast<const void *>(chunk_state_tc<NS>), smem)) != cudaSuccess) return e;
         const dim3 grid(ncx, pr.nheads / HB, mb);
         profile_kernel_begin(s);
-        chunk_state_tc<NS><<<grid, kThreads, smem, s>>>(xmap, bmap, smap, pr, ws);
+        chunk_state_tc<NS><<<grid, kStThreads, smem, s>>>(xmap, bmap, smap, pr, ws);
         profile_kernel_end(s);
     } else {
         if ((e = make_map(&xmap, pr.x, pr.nheads * pr.headdim, pr.seqlen, mb)) != cudaSuccess) return e;
