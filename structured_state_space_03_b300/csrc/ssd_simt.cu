@@ -4,6 +4,9 @@
 // neither TF32 nor bf16 tensor cores give) and the general path for sizes the
 // tensor-core kernels are not built for.  One CTA of 256 threads per
 // (chunk, head, batch); the chunk algebra is written out in ssd_internal.cuh.
+// The chunk-to-chunk state pass is here for both multi-kernel paths: state_pass
+// writes fp32 entry states (this path), state_pass_hilo the bf16 hi + lo terms
+// per 64-wide slice that the tcgen05 chunk-output kernel loads by TMA.
 #include "ssd_internal.cuh"
 
 namespace ssd {

@@ -489,8 +489,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         auto par_s = [&](int sl) { return (((sl + nsl) & 1 ? n_st1 : n_st0) + (uint32_t)(sl >> 1)) & 1u; };
         auto par_k = [&](int kc) { return ((kc & 1 ? n_s1 : n_s0) + (uint32_t)(kc >> 1)) & 1u; };
 
-        // TMA issue: lane 0 of warp 1, so that lane 0 of warp 0 only waits for operands and
-        // issues MMAs.  A stage takes slice sl of C_i and B_j and of each head's entry state
+        // TMA issue (lane 0 of warp 9; lane 0 of warp 8 issues the MMAs).  A stage takes
+        // slice sl of C_i and B_j and of each head's entry state
         // h_c, whose hi and lo bf16 terms the state pass laid out per slice (a [P][64] box of
         // each at columns 128 sl and 128 sl + 64 of the slot's [P][2 NS] bf16 rows).
         auto issue_stage = [&](int sl) {
