@@ -865,19 +865,13 @@ __global__ void __launch_bounds__(kTc, 1)
     __shared__ float red_s[3][8];
     __shared__ int s_fail;
 
-    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int L = a.seqlen, H = a.nheads, G = a.ngroups, g = h / (H / G);
-    const int t0 = c * kQ, len = min(kQ, L - t0);
+    const int L = a.seqlen, H = a.nheads, G = a.ngroups;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // warps w and w + 4 share TMEM lanes 32 (w & 3) .. (token rows i) and split the columns
     const int quarter = warp & 3, half = warp >> 2;
     const int i = quarter * 32 + lane;
     uint8_t *base = tile::align1024(smem_raw);
     const uint32_t sb = smem_u32(base);
-    const size_t bh = (size_t)b * H + h;
-    const float *hc = a.hs + (bh * a.nchunks + c) * (size_t)(kD * kD);
-    const float *gc = a.gs + (bh * a.nchunks + c) * (size_t)(kD * kD);
-    const float Ah = __ldg(a.A + h);
 
     if (tid == 0) {
         mbar_init(&bar_ld, 1);
@@ -892,301 +886,318 @@ __global__ void __launch_bounds__(kTc, 1)
     const uint32_t tmem = tmem_slot;
     const uint32_t lrow = tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lanes
 
-    if (tid == 0) {
-        // this chunk's h_c and g_c (16 KiB each, fresh from the state pass) into L2 while the
-        // chunk scalars are formed
-        bulk_prefetch_l2(hc, (uint32_t)(kD * kD * sizeof(float)));
-        bulk_prefetch_l2(gc, (uint32_t)(kD * kD * sizeof(float)));
-        tma_prefetch_desc(&xmap);
-        tma_prefetch_desc(&dymap);
-        tma_prefetch_desc(&bmap);
-        tma_prefetch_desc(&cmap);
-        mbar_expect_tx(&bar_ld, (uint32_t)(4 * kTile));
-        tma_load_3d(base + oX, &xmap, &bar_ld, h * kD, t0, b);
-        tma_load_3d(base + oDY, &dymap, &bar_ld, h * kD, t0, b);
-        tma_load_3d(base + oB, &bmap, &bar_ld, g * kD, t0, b);
-        tma_load_3d(base + oC, &cmap, &bar_ld, g * kD, t0, b);
-    }
+    // Persistent: the CTAs take the (chunk, head, batch) tiles in turn, chunk fastest.  Per
+    // tile bar_ld completes once and bar_mma three times; the tile count gives the parities.
+    const int ntiles = a.nchunks * H * a.batch;
+    for (int tile_i = blockIdx.x, k = 0; tile_i < ntiles; tile_i += gridDim.x, ++k) {
+        const uint32_t pl = (uint32_t)k & 1u, pm = (uint32_t)(3 * k) & 1u;  // first completion parities
+        const int c = tile_i % a.nchunks, h = (tile_i / a.nchunks) % H, b = tile_i / (a.nchunks * H);
+        const int g = h / (H / G);
+        const int t0 = c * kQ, len = min(kQ, L - t0);
+        const size_t bh = (size_t)b * H + h;
+        const float *hc = a.hs + (bh * a.nchunks + c) * (size_t)(kD * kD);
+        const float *gc = a.gs + (bh * a.nchunks + c) * (size_t)(kD * kD);
+        const float Ah = __ldg(a.A + h);
 
-    // scalars of the chunk (threads 0..127 = tokens): cs (prefix of dt A), dt, cum (prefix of dt)
-    {
-        const float d = tid < len ? __ldg(a.dt + ((size_t)b * L + t0 + tid) * H + h) : 0.f;
-        const float cs_t = block_inclusive_scan_256(d * Ah, warp_tot);
-        const float cum_t = block_inclusive_scan_256(d, warp_tot);
-        if (tid < kQ) {
-            cs_s[tid] = cs_t;
-            dt_s[tid] = d;
-            cum_s[tid] = cum_t;
+        if (tid == 0) {
+            // this chunk's h_c and g_c (16 KiB each, fresh from the state pass) into L2 while the
+            // chunk scalars are formed
+            bulk_prefetch_l2(hc, (uint32_t)(kD * kD * sizeof(float)));
+            bulk_prefetch_l2(gc, (uint32_t)(kD * kD * sizeof(float)));
+            tma_prefetch_desc(&xmap);
+            tma_prefetch_desc(&dymap);
+            tma_prefetch_desc(&bmap);
+            tma_prefetch_desc(&cmap);
+            mbar_expect_tx(&bar_ld, (uint32_t)(4 * kTile));
+            tma_load_3d(base + oX, &xmap, &bar_ld, h * kD, t0, b);
+            tma_load_3d(base + oDY, &dymap, &bar_ld, h * kD, t0, b);
+            tma_load_3d(base + oB, &bmap, &bar_ld, g * kD, t0, b);
+            tma_load_3d(base + oC, &cmap, &bar_ld, g * kD, t0, b);
         }
-    }
 
-    // h_c, g_c -> [64 p][64 n] hi / lo tiles (row p = tid / 4, two 8-column chunks); <g_c, h_c>
-    float u = 0.f;
-    {
-        const int p = tid >> 2, q0 = (tid & 3) * 2;
-#pragma unroll
-        for (int q = q0; q < q0 + 2; ++q) {
-            float hv[8], gv[8];
-            const float4 *hp = reinterpret_cast<const float4 *>(hc + p * kD + 8 * q);
-            const float4 *gp = reinterpret_cast<const float4 *>(gc + p * kD + 8 * q);
-            const float4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1), g0 = __ldcg(gp), g1 = __ldcg(gp + 1);
-            hv[0] = h0.x; hv[1] = h0.y; hv[2] = h0.z; hv[3] = h0.w; hv[4] = h1.x; hv[5] = h1.y; hv[6] = h1.z; hv[7] = h1.w;
-            gv[0] = g0.x; gv[1] = g0.y; gv[2] = g0.z; gv[3] = g0.w; gv[4] = g1.x; gv[5] = g1.y; gv[6] = g1.z; gv[7] = g1.w;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) u = fmaf(hv[k], gv[k], u);
-            uint4 hi, lo;
-            split8(hv, hi, lo);
-            *reinterpret_cast<uint4 *>(base + oHh + sw128(p, q)) = hi;
-            *reinterpret_cast<uint4 *>(base + oHl + sw128(p, q)) = lo;
-            split8(gv, hi, lo);
-            *reinterpret_cast<uint4 *>(base + oGh + sw128(p, q)) = hi;
-            *reinterpret_cast<uint4 *>(base + oGl + sw128(p, q)) = lo;
-        }
-    }
-    __syncthreads();  // the scalars are in shared memory
-    const float dti = dt_s[i];
-    bool ok = mbar_wait(&bar_ld, 0);
-    // dt_j B_j -> hi / lo (row i, the four 8-column chunks of this half)
-    if (ok) {
-#pragma unroll
-        for (int q = 4 * half; q < 4 * half + 4; ++q) {
-            const uint4 raw = *reinterpret_cast<const uint4 *>(base + oB + sw128(i, q));
-            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(b2[e]);
-                v[2 * e] = dti * f.x;
-                v[2 * e + 1] = dti * f.y;
+        // scalars of the chunk (threads 0..127 = tokens): cs (prefix of dt A), dt, cum (prefix of dt)
+        {
+            const float d = tid < len ? __ldg(a.dt + ((size_t)b * L + t0 + tid) * H + h) : 0.f;
+            const float cs_t = block_inclusive_scan_256(d * Ah, warp_tot);
+            const float cum_t = block_inclusive_scan_256(d, warp_tot);
+            if (tid < kQ) {
+                cs_s[tid] = cs_t;
+                dt_s[tid] = d;
+                cum_s[tid] = cum_t;
             }
-            uint4 hi, lo;
-            split8(v, hi, lo);
-            *reinterpret_cast<uint4 *>(base + oBh + sw128(i, q)) = hi;
-            *reinterpret_cast<uint4 *>(base + oBl + sw128(i, q)) = lo;
         }
-    } else {
-        s_fail = 1;
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    ok = !s_fail;
 
-    // dy x^T, C B^T, C h^T, B g^T, dy h, x g
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        constexpr uint32_t id_sq = idesc_bf16(128, 128, 0, 0);
-        constexpr uint32_t id_kk = idesc_bf16(128, 64, 0, 0);
-        constexpr uint32_t id_km = idesc_bf16(128, 64, 0, 1);
+        // h_c, g_c -> [64 p][64 n] hi / lo tiles (row p = tid / 4, two 8-column chunks); <g_c, h_c>
+        float u = 0.f;
+        {
+            const int p = tid >> 2, q0 = (tid & 3) * 2;
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-            const uint32_t kk = ks * 32, km = ks * 2048;  // K step: 16 elements of a row / 16 rows
-            mma_bf16(tmem + 0, kdesc(sb + oDY + kk), kdesc(sb + oX + kk), id_sq, ks > 0);
-            mma_bf16(tmem + 128, kdesc(sb + oC + kk), kdesc(sb + oB + kk), id_sq, ks > 0);
-            mma_bf16(tmem + 256, kdesc(sb + oC + kk), kdesc(sb + oHh + kk), id_kk, ks > 0);
-            mma_bf16(tmem + 256, kdesc(sb + oC + kk), kdesc(sb + oHl + kk), id_kk, 1);
-            mma_bf16(tmem + 320, kdesc(sb + oB + kk), kdesc(sb + oGh + kk), id_kk, ks > 0);
-            mma_bf16(tmem + 320, kdesc(sb + oB + kk), kdesc(sb + oGl + kk), id_kk, 1);
-            mma_bf16(tmem + 384, kdesc(sb + oDY + kk), mdesc(sb + oHh + km), id_km, ks > 0);
-            mma_bf16(tmem + 384, kdesc(sb + oDY + kk), mdesc(sb + oHl + km), id_km, 1);
-            mma_bf16(tmem + 448, kdesc(sb + oX + kk), mdesc(sb + oGh + km), id_km, ks > 0);
-            mma_bf16(tmem + 448, kdesc(sb + oX + kk), mdesc(sb + oGl + km), id_km, 1);
+            for (int q = q0; q < q0 + 2; ++q) {
+                float hv[8], gv[8];
+                const float4 *hp = reinterpret_cast<const float4 *>(hc + p * kD + 8 * q);
+                const float4 *gp = reinterpret_cast<const float4 *>(gc + p * kD + 8 * q);
+                const float4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1), g0 = __ldcg(gp), g1 = __ldcg(gp + 1);
+                hv[0] = h0.x; hv[1] = h0.y; hv[2] = h0.z; hv[3] = h0.w; hv[4] = h1.x; hv[5] = h1.y; hv[6] = h1.z; hv[7] = h1.w;
+                gv[0] = g0.x; gv[1] = g0.y; gv[2] = g0.z; gv[3] = g0.w; gv[4] = g1.x; gv[5] = g1.y; gv[6] = g1.z; gv[7] = g1.w;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) u = fmaf(hv[k], gv[k], u);
+                uint4 hi, lo;
+                split8(hv, hi, lo);
+                *reinterpret_cast<uint4 *>(base + oHh + sw128(p, q)) = hi;
+                *reinterpret_cast<uint4 *>(base + oHl + sw128(p, q)) = lo;
+                split8(gv, hi, lo);
+                *reinterpret_cast<uint4 *>(base + oGh + sw128(p, q)) = hi;
+                *reinterpret_cast<uint4 *>(base + oGl + sw128(p, q)) = lo;
+            }
         }
-        mma_commit(&bar_mma);
-    }
-    ok = ok && mbar_wait(&bar_mma, 0);
-    ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
-    tc_fence_after();
+        __syncthreads();  // the scalars are in shared memory
+        const float dti = dt_s[i];
+        bool ok = mbar_wait(&bar_ld, pl);
+        // dt_j B_j -> hi / lo (row i, the four 8-column chunks of this half)
+        if (ok) {
+#pragma unroll
+            for (int q = 4 * half; q < 4 * half + 4; ++q) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(base + oB + sw128(i, q));
+                const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(b2[e]);
+                    v[2 * e] = dti * f.x;
+                    v[2 * e + 1] = dti * f.y;
+                }
+                uint4 hi, lo;
+                split8(v, hi, lo);
+                *reinterpret_cast<uint4 *>(base + oBh + sw128(i, q)) = hi;
+                *reinterpret_cast<uint4 *>(base + oBl + sw128(i, q)) = lo;
+            }
+        } else {
+            s_fail = 1;
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        ok = !s_fail;
 
-    // K = e o (dy x^T) -> hi / lo operand; W = e o (C B^T) o (dy x^T) dt_j below the diagonal:
-    // row sums here, column sums by a per-warp exchange; the diagonal of dy x^T gives dD's part.
-    // This half: column blocks 2 half, 2 half + 1.
-    const bool row_in = i < len;
-    {
-        float rs = 0.f, diag = 0.f;
+        // dy x^T, C B^T, C h^T, B g^T, dy h, x g
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            constexpr uint32_t id_sq = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t id_kk = idesc_bf16(128, 64, 0, 0);
+            constexpr uint32_t id_km = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const uint32_t kk = ks * 32, km = ks * 2048;  // K step: 16 elements of a row / 16 rows
+                mma_bf16(tmem + 0, kdesc(sb + oDY + kk), kdesc(sb + oX + kk), id_sq, ks > 0);
+                mma_bf16(tmem + 128, kdesc(sb + oC + kk), kdesc(sb + oB + kk), id_sq, ks > 0);
+                mma_bf16(tmem + 256, kdesc(sb + oC + kk), kdesc(sb + oHh + kk), id_kk, ks > 0);
+                mma_bf16(tmem + 256, kdesc(sb + oC + kk), kdesc(sb + oHl + kk), id_kk, 1);
+                mma_bf16(tmem + 320, kdesc(sb + oB + kk), kdesc(sb + oGh + kk), id_kk, ks > 0);
+                mma_bf16(tmem + 320, kdesc(sb + oB + kk), kdesc(sb + oGl + kk), id_kk, 1);
+                mma_bf16(tmem + 384, kdesc(sb + oDY + kk), mdesc(sb + oHh + km), id_km, ks > 0);
+                mma_bf16(tmem + 384, kdesc(sb + oDY + kk), mdesc(sb + oHl + km), id_km, 1);
+                mma_bf16(tmem + 448, kdesc(sb + oX + kk), mdesc(sb + oGh + km), id_km, ks > 0);
+                mma_bf16(tmem + 448, kdesc(sb + oX + kk), mdesc(sb + oGl + km), id_km, 1);
+            }
+            mma_commit(&bar_mma);
+        }
+        ok = ok && mbar_wait(&bar_mma, pm);
+        ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
+        tc_fence_after();
+
+        // K = e o (dy x^T) -> hi / lo operand; W = e o (C B^T) o (dy x^T) dt_j below the diagonal:
+        // row sums here, column sums by a per-warp exchange; the diagonal of dy x^T gives dD's part.
+        // This half: column blocks 2 half, 2 half + 1.
+        const bool row_in = i < len;
+        {
+            float rs = 0.f, diag = 0.f;
+            if (ok) {
+#pragma unroll 1
+                for (int jb = 2 * half; jb < 2 * half + 2; ++jb) {
+                    float dx[32], cb[32], e[32], w[32];
+                    tmem_ld32(lrow + 32 * jb, dx);
+                    tmem_ld32(lrow + 128 + 32 * jb, cb);
+                    decay_row(cs_s, i, jb, row_in, e);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 d4 = reinterpret_cast<const float4 *>(dt_s + 32 * jb)[q];
+                        const float dj[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int k = 4 * q + v, j = 32 * jb + k;
+                            if (j == i) diag = dx[k];
+                            const float kv = e[k] * dx[k];
+                            w[k] = j < i ? kv * cb[k] * dj[v] : 0.f;
+                            rs += w[k];
+                            dx[k] = kv;
+                        }
+                    }
+                    store_split32(base + oKh, base + oKl, i, jb, dx);
+                    colp[quarter][32 * jb + lane] = reduce_scatter32(w, lane);
+                }
+            }
+            row_s[half][i] = rs;
+            diag_s[half][i] = diag;
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // K^T C and K (dt B)
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            constexpr uint32_t id_mm = idesc_bf16(128, 64, 1, 1);
+            constexpr uint32_t id_km = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+            for (int ks = 0; ks < kQ / 16; ++ks) {
+                const uint32_t km = ks * 2048;                                    // 16 rows of a [128][..] operand
+                const uint32_t kk = (ks >> 2) * kTile + (ks & 3) * 32;            // 16 columns of the K operand
+                mma_bf16(tmem + 0, mdesc(sb + oKh + km), mdesc(sb + oC + km), id_mm, ks > 0);
+                mma_bf16(tmem + 0, mdesc(sb + oKl + km), mdesc(sb + oC + km), id_mm, 1);
+                mma_bf16(tmem + 64, kdesc(sb + oKh + kk), mdesc(sb + oBh + km), id_km, ks > 0);
+                mma_bf16(tmem + 64, kdesc(sb + oKh + kk), mdesc(sb + oBl + km), id_km, 1);
+                mma_bf16(tmem + 64, kdesc(sb + oKl + kk), mdesc(sb + oBh + km), id_km, 1);
+            }
+            mma_commit(&bar_mma);
+        }
+        // meanwhile, from columns the MMAs above do not touch: Z_i = dy_i . (C_i h^T) (first half),
+        // V_i = dt_i x_i . (B_i g^T) (second half)
+        if (ok) {
+            float r[64], f[64];
+            tmem_ld64(lrow + (half == 0 ? 256 : 320), r);
+            load_row(base + (half == 0 ? oDY : oX), i, f);
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < 64; ++k) acc = fmaf(f[k], r[k], acc);
+            if (half == 0)
+                z_s[i] = acc;
+            else
+                zv_s[i] = row_in ? expf(cs_s[len - 1] - cs_s[i]) * dti * acc : 0.f;  // e^{cs_end - cs_i} V_i
+        }
+        ok = ok && mbar_wait(&bar_mma, pm ^ 1u);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+
+        // M = e o (C B^T) -> hi / lo over the K operand, then M^T dy
         if (ok) {
 #pragma unroll 1
             for (int jb = 2 * half; jb < 2 * half + 2; ++jb) {
-                float dx[32], cb[32], e[32], w[32];
-                tmem_ld32(lrow + 32 * jb, dx);
+                float cb[32], e[32];
                 tmem_ld32(lrow + 128 + 32 * jb, cb);
                 decay_row(cs_s, i, jb, row_in, e);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 d4 = reinterpret_cast<const float4 *>(dt_s + 32 * jb)[q];
-                    const float dj[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const int k = 4 * q + v, j = 32 * jb + k;
-                        if (j == i) diag = dx[k];
-                        const float kv = e[k] * dx[k];
-                        w[k] = j < i ? kv * cb[k] * dj[v] : 0.f;
-                        rs += w[k];
-                        dx[k] = kv;
-                    }
-                }
-                store_split32(base + oKh, base + oKl, i, jb, dx);
-                colp[quarter][32 * jb + lane] = reduce_scatter32(w, lane);
+                for (int k = 0; k < 32; ++k) cb[k] *= e[k];
+                store_split32(base + oKh, base + oKl, i, jb, cb);
             }
         }
-        row_s[half][i] = rs;
-        diag_s[half][i] = diag;
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // K^T C and K (dt B)
-    if (tid == 0 && ok) {
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            constexpr uint32_t id_mm = idesc_bf16(128, 64, 1, 1);
+#pragma unroll
+            for (int ks = 0; ks < kQ / 16; ++ks) {
+                const uint32_t km = ks * 2048;
+                mma_bf16(tmem + 128, mdesc(sb + oKh + km), mdesc(sb + oDY + km), id_mm, ks > 0);
+                mma_bf16(tmem + 128, mdesc(sb + oKl + km), mdesc(sb + oDY + km), id_mm, 1);
+            }
+            mma_commit(&bar_mma);
+        }
+        ok = ok && mbar_wait(&bar_mma, pm);
+        ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
-        constexpr uint32_t id_mm = idesc_bf16(128, 64, 1, 1);
-        constexpr uint32_t id_km = idesc_bf16(128, 64, 0, 1);
-#pragma unroll
-        for (int ks = 0; ks < kQ / 16; ++ks) {
-            const uint32_t km = ks * 2048;                                    // 16 rows of a [128][..] operand
-            const uint32_t kk = (ks >> 2) * kTile + (ks & 3) * 32;            // 16 columns of the K operand
-            mma_bf16(tmem + 0, mdesc(sb + oKh + km), mdesc(sb + oC + km), id_mm, ks > 0);
-            mma_bf16(tmem + 0, mdesc(sb + oKl + km), mdesc(sb + oC + km), id_mm, 1);
-            mma_bf16(tmem + 64, kdesc(sb + oKh + kk), mdesc(sb + oBh + km), id_km, ks > 0);
-            mma_bf16(tmem + 64, kdesc(sb + oKh + kk), mdesc(sb + oBl + km), id_km, 1);
-            mma_bf16(tmem + 64, kdesc(sb + oKl + kk), mdesc(sb + oBh + km), id_km, 1);
-        }
-        mma_commit(&bar_mma);
-    }
-    // meanwhile, from columns the MMAs above do not touch: Z_i = dy_i . (C_i h^T) (first half),
-    // V_i = dt_i x_i . (B_i g^T) (second half)
-    if (ok) {
-        float r[64], f[64];
-        tmem_ld64(lrow + (half == 0 ? 256 : 320), r);
-        load_row(base + (half == 0 ? oDY : oX), i, f);
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 64; ++k) acc = fmaf(f[k], r[k], acc);
-        if (half == 0)
-            z_s[i] = acc;
-        else
-            zv_s[i] = row_in ? expf(cs_s[len - 1] - cs_s[i]) * dti * acc : 0.f;  // e^{cs_end - cs_i} V_i
-    }
-    ok = ok && mbar_wait(&bar_mma, 1);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
 
-    // M = e o (C B^T) -> hi / lo over the K operand, then M^T dy
-    if (ok) {
-#pragma unroll 1
-        for (int jb = 2 * half; jb < 2 * half + 2; ++jb) {
-            float cb[32], e[32];
-            tmem_ld32(lrow + 128 + 32 * jb, cb);
-            decay_row(cs_s, i, jb, row_in, e);
+        // outputs of row i: dB and dC (first half; per head, or the group's when it has one
+        // head), dx and x . inner (second half)
+        const float cs_end = cs_s[len - 1], cs_i = cs_s[i];
+        const float eS = row_in ? expf(cs_end - cs_i) : 0.f, eC = row_in ? expf(cs_i) : 0.f;
+        // Each row goes into an fp32 staging tile (dB over B and C, dC over dt B, dx over K: all
+        // dead now) of two [128][32] boxes with the 128-byte swizzle, so that a warp's row stores
+        // spread over the banks; the boxes then go out by TMA (rows past the sequence end are
+        // clipped by the tensor maps; the tensor-core backward has no packed layout).
+        uint8_t *stB = base + oB, *stC = base + oBh, *stX = base + oKh;
+        auto put_row = [&](uint8_t *tile, const float (&v)[64]) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) cb[k] *= e[k];
-            store_split32(base + oKh, base + oKl, i, jb, cb);
+            for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<float4 *>(tile + hb * kTile + sw128(i, q)) =
+                        make_float4(v[32 * hb + 4 * q], v[32 * hb + 4 * q + 1], v[32 * hb + 4 * q + 2],
+                                    v[32 * hb + 4 * q + 3]);
+        };
+        if (ok && half == 0) {
+            float acc[64], add[64];
+            tmem_ld64(lrow + 0, acc);
+            tmem_ld64(lrow + 448, add);
+#pragma unroll
+            for (int k = 0; k < 64; ++k) acc[k] = dti * fmaf(eS, add[k], acc[k]);
+            put_row(stB, acc);
+            tmem_ld64(lrow + 64, acc);
+            tmem_ld64(lrow + 384, add);
+#pragma unroll
+            for (int k = 0; k < 64; ++k) acc[k] = fmaf(eC, add[k], acc[k]);
+            put_row(stC, acc);
+        } else if (ok) {
+            float acc[64], add[64], f[64];
+            tmem_ld64(lrow + 128, acc);
+            tmem_ld64(lrow + 320, add);
+            const float Dh = a.D ? __ldg(a.D + h) : 0.f;
+#pragma unroll
+            for (int k = 0; k < 64; ++k) acc[k] = fmaf(eS, add[k], acc[k]);  // inner_i
+            load_row(base + oX, i, f);
+            float xin = 0.f;
+#pragma unroll
+            for (int k = 0; k < 64; ++k) xin = fmaf(f[k], acc[k], xin);
+            ddt_s[i] = xin;
+            load_row(base + oDY, i, f);
+#pragma unroll
+            for (int k = 0; k < 64; ++k) acc[k] = fmaf(Dh, f[k], dti * acc[k]);
+            put_row(stX, acc);
         }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && ok) {
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && ok) {
+            const bool direct = a.dBp == nullptr;  // one head per group: dB and dC themselves
+            for (int hb = 0; hb < 2; ++hb) {
+                tma_store_3d(&dbmap, stB + hb * kTile, (direct ? g : h) * kD + 32 * hb, t0, b);
+                tma_store_3d(&dcmap, stC + hb * kTile, (direct ? g : h) * kD + 32 * hb, t0, b);
+                tma_store_3d(&dxmap, stX + hb * kTile, h * kD + 32 * hb, t0, b);
+            }
+            bulk_commit();
+            bulk_wait_read_all();
+        }
+
+        // dL/dcs_t (threads 0..127 = tokens t), then ddt = x . inner + A sum_{t' >= t} dcs_t' and the
+        // dA / dD parts; sums over all 256 threads in a fixed order (the second half adds zeros)
+        const bool tok = tid < kQ && tid < len;
+        const float zv = tok ? zv_s[tid] : 0.f;
+        // sum_j e^{cs_end - cs_j} V_j, the u sum and the diagonal sum in one exchange
+        const float3 s3 = sum3_256(zv, u, tid < kQ ? diag_s[0][tid] + diag_s[1][tid] : 0.f, red_s);
+        const float ssum = s3.x, usum = s3.y, dsum = s3.z;
+        float d = 0.f;
+        if (tok) {
+            const float colsum = (colp[0][tid] + colp[1][tid]) + (colp[2][tid] + colp[3][tid]);
+            d = (row_s[0][tid] + row_s[1][tid]) - colsum + expf(cs_s[tid]) * z_s[tid] - zv;
+            if (tid == len - 1) d += ssum + expf(cs_end) * usum;
+        }
+        // the prefix of d, its total and the dA part sum_t d_t cum_t in one exchange
+        const float3 pt = scan_sum2_256(d, tid < kQ ? d * cum_s[tid] : 0.f, red_s);
+        const float pre = pt.x, tot = pt.y, da = pt.z;
+        if (tok && ok) a.ddt[((size_t)b * L + t0 + tid) * H + h] = fmaf(Ah, tot - pre + d, ddt_s[tid]);
+        if (tid == 0 && ok) {
+            const size_t o = ((size_t)b * a.nchunks + c) * H + h;
+            a.dAp[o] = da;
+            a.dDp[o] = dsum;
+        }
+        if (tid == 0 && !ok && a.err_word) atomicOr(a.err_word, kDevErrTimeout);
+        if (!ok) s_fail = 1;
+        tc_fence_before();
+        __syncthreads();  // the tile is done with TMEM and shared memory
         tc_fence_after();
-        constexpr uint32_t id_mm = idesc_bf16(128, 64, 1, 1);
-#pragma unroll
-        for (int ks = 0; ks < kQ / 16; ++ks) {
-            const uint32_t km = ks * 2048;
-            mma_bf16(tmem + 128, mdesc(sb + oKh + km), mdesc(sb + oDY + km), id_mm, ks > 0);
-            mma_bf16(tmem + 128, mdesc(sb + oKl + km), mdesc(sb + oDY + km), id_mm, 1);
-        }
-        mma_commit(&bar_mma);
-    }
-    ok = ok && mbar_wait(&bar_mma, 0);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
-
-    // outputs of row i: dB and dC (first half; per head, or the group's when it has one
-    // head), dx and x . inner (second half)
-    const float cs_end = cs_s[len - 1], cs_i = cs_s[i];
-    const float eS = row_in ? expf(cs_end - cs_i) : 0.f, eC = row_in ? expf(cs_i) : 0.f;
-    // Each row goes into an fp32 staging tile (dB over B and C, dC over dt B, dx over K: all
-    // dead now) of two [128][32] boxes with the 128-byte swizzle, so that a warp's row stores
-    // spread over the banks; the boxes then go out by TMA (rows past the sequence end are
-    // clipped by the tensor maps; the tensor-core backward has no packed layout).
-    uint8_t *stB = base + oB, *stC = base + oBh, *stX = base + oKh;
-    auto put_row = [&](uint8_t *tile, const float (&v)[64]) {
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<float4 *>(tile + hb * kTile + sw128(i, q)) =
-                    make_float4(v[32 * hb + 4 * q], v[32 * hb + 4 * q + 1], v[32 * hb + 4 * q + 2],
-                                v[32 * hb + 4 * q + 3]);
-    };
-    if (ok && half == 0) {
-        float acc[64], add[64];
-        tmem_ld64(lrow + 0, acc);
-        tmem_ld64(lrow + 448, add);
-#pragma unroll
-        for (int k = 0; k < 64; ++k) acc[k] = dti * fmaf(eS, add[k], acc[k]);
-        put_row(stB, acc);
-        tmem_ld64(lrow + 64, acc);
-        tmem_ld64(lrow + 384, add);
-#pragma unroll
-        for (int k = 0; k < 64; ++k) acc[k] = fmaf(eC, add[k], acc[k]);
-        put_row(stC, acc);
-    } else if (ok) {
-        float acc[64], add[64], f[64];
-        tmem_ld64(lrow + 128, acc);
-        tmem_ld64(lrow + 320, add);
-        const float Dh = a.D ? __ldg(a.D + h) : 0.f;
-#pragma unroll
-        for (int k = 0; k < 64; ++k) acc[k] = fmaf(eS, add[k], acc[k]);  // inner_i
-        load_row(base + oX, i, f);
-        float xin = 0.f;
-#pragma unroll
-        for (int k = 0; k < 64; ++k) xin = fmaf(f[k], acc[k], xin);
-        ddt_s[i] = xin;
-        load_row(base + oDY, i, f);
-#pragma unroll
-        for (int k = 0; k < 64; ++k) acc[k] = fmaf(Dh, f[k], dti * acc[k]);
-        put_row(stX, acc);
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && ok) {
-        const bool direct = a.dBp == nullptr;  // one head per group: dB and dC themselves
-        for (int hb = 0; hb < 2; ++hb) {
-            tma_store_3d(&dbmap, stB + hb * kTile, (direct ? g : h) * kD + 32 * hb, t0, b);
-            tma_store_3d(&dcmap, stC + hb * kTile, (direct ? g : h) * kD + 32 * hb, t0, b);
-            tma_store_3d(&dxmap, stX + hb * kTile, h * kD + 32 * hb, t0, b);
-        }
-        bulk_commit();
-        bulk_wait_read_all();
-    }
-
-    // dL/dcs_t (threads 0..127 = tokens t), then ddt = x . inner + A sum_{t' >= t} dcs_t' and the
-    // dA / dD parts; sums over all 256 threads in a fixed order (the second half adds zeros)
-    const bool tok = tid < kQ && tid < len;
-    const float zv = tok ? zv_s[tid] : 0.f;
-    // sum_j e^{cs_end - cs_j} V_j, the u sum and the diagonal sum in one exchange
-    const float3 s3 = sum3_256(zv, u, tid < kQ ? diag_s[0][tid] + diag_s[1][tid] : 0.f, red_s);
-    const float ssum = s3.x, usum = s3.y, dsum = s3.z;
-    float d = 0.f;
-    if (tok) {
-        const float colsum = (colp[0][tid] + colp[1][tid]) + (colp[2][tid] + colp[3][tid]);
-        d = (row_s[0][tid] + row_s[1][tid]) - colsum + expf(cs_s[tid]) * z_s[tid] - zv;
-        if (tid == len - 1) d += ssum + expf(cs_end) * usum;
-    }
-    // the prefix of d, its total and the dA part sum_t d_t cum_t in one exchange
-    const float3 pt = scan_sum2_256(d, tid < kQ ? d * cum_s[tid] : 0.f, red_s);
-    const float pre = pt.x, tot = pt.y, da = pt.z;
-    if (tok && ok) a.ddt[((size_t)b * L + t0 + tid) * H + h] = fmaf(Ah, tot - pre + d, ddt_s[tid]);
-    if (tid == 0 && ok) {
-        const size_t o = ((size_t)b * a.nchunks + c) * H + h;
-        a.dAp[o] = da;
-        a.dDp[o] = dsum;
-    }
-    if (tid == 0 && !ok && a.err_word) atomicOr(a.err_word, kDevErrTimeout);
-    tc_fence_after();
-    __syncthreads();
+        if (s_fail) break;  // block-uniform: read after the barrier
+    }  // tiles
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
@@ -1316,8 +1327,12 @@ cudaError_t launch_bwd_tc(const BwdArgs &a, cudaStream_t s)
     bwd_state_pass<<<dim3((unsigned)((PN + kThreads - 1) / kThreads), H, a.batch), kThreads, 0, s>>>(a);
     profile_kernel_end(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    int sms = 148;
+    if ((e = sm_count(&sms)) != cudaSuccess) return e;
+    const long long btiles = (long long)a.nchunks * H * a.batch;  // persistent: one CTA per SM
     profile_kernel_begin(s);
-    tcb::bwd_chunk_tc<<<grid, tcb::kTc, tcb::kSmemTc, s>>>(xm, dym, bm, cm, dbm, dcm, dxm, a);
+    tcb::bwd_chunk_tc<<<(unsigned)std::min<long long>(btiles, sms), tcb::kTc, tcb::kSmemTc, s>>>(xm, dym, bm, cm, dbm,
+                                                                                             dcm, dxm, a);
     profile_kernel_end(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return launch_reductions(a, s);
