@@ -97,15 +97,14 @@ __global__ void __launch_bounds__(256) ssd_step_vec_kernel(const T *__restrict__
                                                            float *__restrict__ state, T *__restrict__ y, int batch,
                                                            int H, int P, int G, int lg)
 {
-    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const int q = (int)(gid & ((1 << lg) - 1));  // which 4 V states of the row
-    const long long row = gid >> lg;             // (b, h, p)
-    const long long rows = (long long)batch * H * P;
-    const bool live = row < rows;
-    const long long r = live ? row : rows - 1;   // dead threads still join the shuffles
+    // grid: (rows of one (b, h) x threads per row) / 256, H, batch -- no per-thread division
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int lt = blockIdx.x * blockDim.x + threadIdx.x;  // thread within the (b, h) block of rows
+    const int q = lt & ((1 << lg) - 1);                    // which 4 V states of the row
+    const int p = lt >> lg;
+    const bool live = p < P;
+    const long long r = ((long long)b * H + h) * P + (live ? p : P - 1);  // dead threads still join the shuffles
     const int N = (4 * V) << lg;
-    const int h = (int)((r / P) % H);
-    const int b = (int)(r / ((long long)P * H));
     const int g = h / (H / G);
     const int tpr = 1 << lg;  // threads per row
     float4 *sp = reinterpret_cast<float4 *>(state + (size_t)r * N) + q;
@@ -137,9 +136,11 @@ template <typename T, int V>
 void launch_vec(const void *x, const float *dt, const float *A, const void *B, const void *C, const float *D,
                 float *state, void *y, int batch, int nheads, int headdim, int ngroups, int lg, cudaStream_t s)
 {
-    const long long threads = ((long long)batch * nheads * headdim) << lg;
-    const unsigned grid = (unsigned)((threads + 255) / 256);
-    ssd_step_vec_kernel<T, V><<<grid, 256, 0, s>>>(static_cast<const T *>(x), dt, A, static_cast<const T *>(B),
+    // the threads of one (b, h) -- headdim rows of 2^lg -- in blocks of at most 256, whole warps
+    const int per = headdim << lg;
+    const int block = per >= 256 ? 256 : (per + 31) / 32 * 32;
+    const dim3 grid((unsigned)((per + block - 1) / block), (unsigned)nheads, (unsigned)batch);
+    ssd_step_vec_kernel<T, V><<<grid, block, 0, s>>>(static_cast<const T *>(x), dt, A, static_cast<const T *>(B),
                                                    static_cast<const T *>(C), D, state, static_cast<T *>(y), batch,
                                                    nheads, headdim, ngroups, lg);
 }
@@ -158,7 +159,9 @@ cudaError_t launch_step(const void *x, const float *dt, const float *A, const vo
     for (int k = 0; k <= 5; ++k)
         if (dstate == ((4 * V) << k)) lg = k;
     const bool al = (reinterpret_cast<uintptr_t>(state) & 15) == 0 && (reinterpret_cast<uintptr_t>(B) & 7) == 0 &&
-                    (reinterpret_cast<uintptr_t>(C) & 7) == 0;
+                    (reinterpret_cast<uintptr_t>(C) & 7) == 0 &&
+                    nheads <= 65535 && batch <= 65535 &&  // the vector kernel's grid is (.., nheads, batch)
+                    ((long long)headdim << 5) < (1ll << 31);
     if (lg >= 0 && al && dtype == SSD_DTYPE_BF16) {
         if (V == 1)
             launch_vec<__nv_bfloat16, 1>(x, dt, A, B, C, D, state, y, batch, nheads, headdim, ngroups, lg, s);

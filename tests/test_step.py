@@ -32,7 +32,8 @@ def _token(inp, t):
 
 
 # (batch, nheads, headdim, dstate, ngroups)
-SHAPES = [(2, 80, 64, 64, 1), (3, 8, 16, 48, 2), (1, 4, 128, 256, 4), (2, 6, 33, 20, 3)]
+SHAPES = [(2, 80, 64, 64, 1), (3, 8, 16, 48, 2), (1, 4, 128, 256, 4), (2, 6, 33, 20, 3),
+          (5, 3, 8, 64, 1), (2, 3, 1, 16, 1)]  # the last two: few rows per head (partly idle blocks)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
