@@ -29,7 +29,7 @@
 //   ddt_u   = x_u . inner_u + A sum_{t >= u} dcs_t,   dA = sum_t dcs_t sum_{u <= t} dt_u,
 //   dD      = sum dy . x
 //
-// Kernels (one CTA per (chunk, head, batch) unless noted):
+// Kernels (one CTA per (chunk, head, batch) unless noted; bwd_chunk_tc is persistent):
 //   1. chunk states      bf16 / headdim 64 / dstate 64 (128-token chunks): S_c and
 //                        the decays by the forward's tcgen05 chunk-state kernel,
 //                        then G_c by the same kernel with dy, C and weights e^{cs_j}
@@ -693,8 +693,9 @@ __global__ void __launch_bounds__(kThreads) bwd_reduce_heads(BwdArgs a)
 
 // ---------------------------------------------------------------------------
 // 3'. The in-chunk terms on tcgen05 tensor cores (bf16 inputs, headdim 64,
-//     dstate 64, 128-token chunks): one CTA of 256 threads per (chunk, head,
-//     batch); warps w and w + 4 own token rows 32 (w & 3) .. 32 (w & 3) + 31 of
+//     dstate 64, 128-token chunks): persistent, one CTA of 256 threads per SM
+//     taking the (chunk, head, batch) tiles in turn; warps w and w + 4 own token
+//     rows 32 (w & 3) .. 32 (w & 3) + 31 of
 //     every accumulator (their TMEM lanes) and split its columns.
 //     x, dy, B, C arrive by TMA as 128-byte-swizzled [128 tokens][64] bf16
 //     tiles.  Exact bf16 products (dy x^T, C B^T) take the inputs as they are;
