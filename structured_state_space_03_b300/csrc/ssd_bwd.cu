@@ -605,41 +605,58 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk(BwdArgs a)
 
 // ---------------------------------------------------------------------------
 // 4a. dB / dC: sum of the per-head parts over the heads of each group.  With dstate a
-//     multiple of 4, four consecutive state columns per thread as float4s, and four heads'
-//     loads in flight at a time (the sum runs over the heads in order either way).
+//     multiple of 4 (and dB, dC 16-byte aligned): four consecutive state columns as
+//     float4s, the heads split over four threads (see below).
 __global__ void __launch_bounds__(kThreads) bwd_reduce_groups(BwdArgs a)
 {
+    // kSub threads per four columns, each summing every kSub-th head of the group; the
+    // partial sums are then added in shared memory, in a fixed order (results stay bitwise
+    // reproducible), so four times as many loads are in flight
+    constexpr int kSub = 4, kOut = kThreads / kSub;
+    __shared__ float4 pb[kSub][kOut], pc[kSub][kOut];
     const int H = a.nheads, G = a.ngroups, N = a.dstate, hpg = H / G, N4 = N / 4;
     const size_t total = (size_t)a.batch * a.seqlen * G * N4;
     const float4 *dBp = reinterpret_cast<const float4 *>(a.dBp), *dCp = reinterpret_cast<const float4 *>(a.dCp);
-    for (size_t e = (size_t)blockIdx.x * kThreads + threadIdx.x; e < total; e += (size_t)gridDim.x * kThreads) {
-        const int n4 = (int)(e % N4);
-        const size_t bt_g = e / N4;
-        const int g = (int)(bt_g % G);
-        const size_t bt = bt_g / G;
-        const size_t base = (bt * H + (size_t)g * hpg) * N4 + n4;
+    const int sub = threadIdx.x / kOut, o = threadIdx.x % kOut;
+    for (size_t e0 = (size_t)blockIdx.x * kOut; e0 < total; e0 += (size_t)gridDim.x * kOut) {  // block-uniform
+        const size_t e = e0 + o;
         float4 sb = make_float4(0.f, 0.f, 0.f, 0.f), sc = sb;
-        int k = 0;
-        for (; k + 4 <= hpg; k += 4) {
-            float4 vb[4], vc[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                vb[u] = __ldcs(dBp + base + (size_t)(k + u) * N4);
-                vc[u] = __ldcs(dCp + base + (size_t)(k + u) * N4);
+        if (e < total) {
+            const int n4 = (int)(e % N4);
+            const size_t bt_g = e / N4;
+            const int g = (int)(bt_g % G);
+            const size_t bt = bt_g / G;
+            const size_t base = (bt * H + (size_t)g * hpg) * N4 + n4;
+            int k = sub;
+            for (; k + kSub < hpg; k += 2 * kSub) {  // two heads' loads in flight per thread
+                const float4 vb0 = __ldcs(dBp + base + (size_t)k * N4), vc0 = __ldcs(dCp + base + (size_t)k * N4);
+                const float4 vb1 = __ldcs(dBp + base + (size_t)(k + kSub) * N4);
+                const float4 vc1 = __ldcs(dCp + base + (size_t)(k + kSub) * N4);
+                sb.x += vb0.x; sb.y += vb0.y; sb.z += vb0.z; sb.w += vb0.w;
+                sc.x += vc0.x; sc.y += vc0.y; sc.z += vc0.z; sc.w += vc0.w;
+                sb.x += vb1.x; sb.y += vb1.y; sb.z += vb1.z; sb.w += vb1.w;
+                sc.x += vc1.x; sc.y += vc1.y; sc.z += vc1.z; sc.w += vc1.w;
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                sb.x += vb[u].x; sb.y += vb[u].y; sb.z += vb[u].z; sb.w += vb[u].w;
-                sc.x += vc[u].x; sc.y += vc[u].y; sc.z += vc[u].z; sc.w += vc[u].w;
+            for (; k < hpg; k += kSub) {
+                const float4 vb = __ldcs(dBp + base + (size_t)k * N4), vc = __ldcs(dCp + base + (size_t)k * N4);
+                sb.x += vb.x; sb.y += vb.y; sb.z += vb.z; sb.w += vb.w;
+                sc.x += vc.x; sc.y += vc.y; sc.z += vc.z; sc.w += vc.w;
             }
         }
-        for (; k < hpg; ++k) {
-            const float4 vb = __ldcs(dBp + base + (size_t)k * N4), vc = __ldcs(dCp + base + (size_t)k * N4);
-            sb.x += vb.x; sb.y += vb.y; sb.z += vb.z; sb.w += vb.w;
-            sc.x += vc.x; sc.y += vc.y; sc.z += vc.z; sc.w += vc.w;
+        pb[sub][o] = sb;
+        pc[sub][o] = sc;
+        __syncthreads();
+        if (sub == 0 && e < total) {
+            float4 tb = pb[0][o], tc = pc[0][o];
+#pragma unroll
+            for (int q = 1; q < kSub; ++q) {
+                tb.x += pb[q][o].x; tb.y += pb[q][o].y; tb.z += pb[q][o].z; tb.w += pb[q][o].w;
+                tc.x += pc[q][o].x; tc.y += pc[q][o].y; tc.z += pc[q][o].z; tc.w += pc[q][o].w;
+            }
+            reinterpret_cast<float4 *>(a.dB)[e] = tb;
+            reinterpret_cast<float4 *>(a.dC)[e] = tc;
         }
-        reinterpret_cast<float4 *>(a.dB)[e] = sb;
-        reinterpret_cast<float4 *>(a.dC)[e] = sc;
+        __syncthreads();
     }
 }
 
@@ -1220,7 +1237,8 @@ cudaError_t launch_reductions(const BwdArgs &a, cudaStream_t s)
         const bool v4 = a.dstate % 4 == 0 && reinterpret_cast<uintptr_t>(a.dB) % 16 == 0 &&
                         reinterpret_cast<uintptr_t>(a.dC) % 16 == 0;
         const size_t total = (size_t)a.batch * a.seqlen * a.ngroups * a.dstate / (v4 ? 4 : 1);
-        const size_t want = (total + kThreads - 1) / kThreads;
+        const size_t per_block = v4 ? kThreads / 4 : kThreads;  // outputs per block
+        const size_t want = (total + per_block - 1) / per_block;
         const unsigned blocks = (unsigned)std::min<size_t>(want, (size_t)sms * 8);
         profile_kernel_begin(s);
         if (v4)
